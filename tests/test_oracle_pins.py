@@ -1,0 +1,349 @@
+"""Pins of the float64 oracle against what the pages and the mathematics fix.
+
+Every test here runs on the CPU. Each compares the C recurrence with
+something independent of it: a printed worked example, a closed form, or a
+different association order proved equal on the pages.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import forms
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def one(variant, q, k, v, gate=None, beta=None, state=None, **kw):
+    """Run the oracle on a single sequence-head; arrays [T, d]."""
+    ex = lambda a: None if a is None else np.asarray(a, np.float64)[None, None]
+    st = None if state is None else np.asarray(state, np.float64).reshape(1, 1, -1)
+    r = oracle.run(variant, ex(q), ex(k), ex(v), ex(gate), ex(beta), st, **kw)
+    den = None if r.den is None else r.den[0, 0]
+    return r.o[0, 0], r.state[0, 0], den
+
+
+def rng(seed):
+    return np.random.default_rng(seed)
+
+
+def sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def unit(x):
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+# ---------------------------------------------------------------- (a) norm
+
+@pytest.mark.parametrize("T", [64, 512])
+def test_norm_recurrent_equals_masked_parallel(T):
+    # "Linear attention and Hyena" 11.2: the two forms agree to machine
+    # precision in float64 (5.6e-16 at T=64, 2e-16 at T=512 printed).
+    r = rng(T)
+    q, k, v = (r.standard_normal((T, 16)) for _ in range(3))
+    o, st, den = one("norm", q, k, v)
+    o_p, S_p, z_p, den_p = forms.norm_masked_parallel(q, k, v)
+    S, z = oracle.split_norm_state(st, 16, 16)
+    assert np.max(np.abs(o - o_p)) <= 1e-12
+    assert np.max(np.abs(den - den_p) / den_p) <= 1e-12
+    assert np.max(np.abs(S - S_p)) <= 1e-12 * max(1.0, np.max(np.abs(S_p)))
+    assert np.max(np.abs(z - z_p)) <= 1e-12 * np.max(z_p)
+
+
+def test_norm_feature_map_closed_form():
+    # phi = elu+1: phi(-ln 2) = 1/2 on the exp branch, phi(1) = 2 on the
+    # linear branch. With d_k = d_v = 1 the output is a phi-weighted mean:
+    # o_2 = (1/2 * 1 + 2 * 0) / (1/2 + 2) = 0.2 exactly; o_1 = v_1.
+    q = np.array([[0.3], [-0.7]])
+    k = np.array([[-math.log(2.0)], [1.0]])
+    v = np.array([[1.0], [0.0]])
+    o, st, den = one("norm", q, k, v)
+    assert o[0, 0] == pytest.approx(1.0, abs=1e-15)
+    assert o[1, 0] == pytest.approx(0.2, abs=1e-15)
+    # den_2 = phi(q_2) * (phi(k_1) + phi(k_2)) = e^{-0.7} * 2.5
+    assert den[1] == pytest.approx(math.exp(-0.7) * 2.5, rel=1e-15)
+    assert st[0] == pytest.approx(0.5, abs=1e-15) and st[1] == pytest.approx(2.5, abs=1e-15)
+
+
+def test_norm_first_token_and_prefix_mean():
+    r = rng(1)
+    T, d = 20, 8
+    q, v = r.standard_normal((T, d)), r.standard_normal((T, d))
+    k = np.tile(r.standard_normal((1, d)), (T, 1))          # identical keys
+    o, _, _ = one("norm", q, k, v)
+    assert np.allclose(o[0], v[0], atol=1e-15, rtol=0)       # token attends to itself
+    prefix_mean = np.cumsum(v, axis=0) / np.arange(1, T + 1)[:, None]
+    assert np.max(np.abs(o - prefix_mean)) <= 1e-13
+
+
+def test_norm_output_in_value_hull():
+    r = rng(2)
+    T, d = 100, 8
+    q, k, v = (r.standard_normal((T, d)) for _ in range(3))
+    o, _, _ = one("norm", q, k, v)
+    lo = np.minimum.accumulate(v, axis=0)
+    hi = np.maximum.accumulate(v, axis=0)
+    assert np.all(o >= lo - 1e-12) and np.all(o <= hi + 1e-12)
+
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+def test_causality(variant):
+    # Changing tokens after t leaves outputs up to t bit-identical.
+    r = rng(3)
+    T, d, t0 = 40, 8, 17
+    q, k, v = (r.standard_normal((T, d)) for _ in range(3))
+    gate = beta = None
+    if variant == "gla":
+        gate = sigmoid(r.standard_normal((T, d)) + 2)
+    if variant == "gdn":
+        k = unit(k)
+        gate, beta = sigmoid(r.standard_normal(T) + 3), sigmoid(r.standard_normal(T))
+    o1, _, _ = one(variant, q, k, v, gate, beta)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    q2[t0 + 1:] += 5.0
+    k2[t0 + 1:] = -k2[t0 + 1:]
+    v2[t0 + 1:] *= 3.0
+    g2 = None if gate is None else gate.copy()
+    if g2 is not None:
+        g2[t0 + 1:] = 0.5
+    o2, _, _ = one(variant, q2, k2, v2, g2, beta)
+    assert np.array_equal(o1[: t0 + 1], o2[: t0 + 1])
+    assert not np.array_equal(o1[t0 + 1:], o2[t0 + 1:])
+
+
+# ----------------------------------------------------------------- (b) gla
+
+@pytest.mark.parametrize("identity_phi", [False, True])
+def test_gla_recurrent_equals_masked(identity_phi):
+    # "Linear attention and Hyena" 11.3 / Exercise 11.5 (2.8e-14 printed for
+    # their data-dependent gate).
+    r = rng(4)
+    T, dk, dv = 64, 16, 8
+    q, k, v = r.standard_normal((T, dk)), r.standard_normal((T, dk)), r.standard_normal((T, dv))
+    gamma = sigmoid(r.standard_normal((T, dk)) + 1.5)
+    o, S, _ = one("gla", q, k, v, gamma, identity_phi=identity_phi)
+    y, S_T = forms.gla_masked(q, k, v, gamma, identity_phi=identity_phi)
+    scale = max(1.0, np.max(np.abs(y)))
+    assert np.max(np.abs(o - y)) <= 1e-12 * scale
+    assert np.max(np.abs(S.reshape(dk, dv) - S_T)) <= 1e-12 * max(1.0, np.max(np.abs(S_T)))
+
+
+def test_gla_constant_gate_is_toeplitz():
+    r = rng(5)
+    T, d = 48, 8
+    q, k, v = (r.standard_normal((T, d)) for _ in range(3))
+    gam = 0.9
+    o, _, _ = one("gla", q, k, v, np.full((T, d), gam))
+    ref = forms.retnet_toeplitz(q, k, v, gam)
+    assert np.max(np.abs(o - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_gla_unit_gate_is_norm_numerator():
+    # gamma = 1 reduces the gated state to the undecayed one, so the gla
+    # output equals the normalized output times its denominator.
+    r = rng(6)
+    T, d = 50, 8
+    q, k, v = (r.standard_normal((T, d)) for _ in range(3))
+    o_g, S_g, _ = one("gla", q, k, v, np.ones((T, d)))
+    o_n, st_n, den = one("norm", q, k, v)
+    assert np.max(np.abs(o_g - o_n * den[:, None])) <= 1e-12 * np.max(np.abs(o_g))
+    assert np.max(np.abs(S_g - st_n[: d * d])) <= 1e-12 * np.max(np.abs(S_g))
+
+
+def test_gla_factorized_rescaling_tiny():
+    r = rng(7)
+    T, d = 12, 6
+    q, k, v = (r.standard_normal((T, d)) for _ in range(3))
+    gamma = sigmoid(r.standard_normal((T, d)) + 1)
+    o, _, _ = one("gla", q, k, v, gamma)
+    ref = forms.gla_factorized(q, k, v, gamma)
+    assert np.max(np.abs(o - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_gla_gate_timing_closed_form():
+    # gamma_t decays the state BEFORE token t's write: o_2 = phi(q_2)(gamma_2
+    # phi(k_1) v_1 + phi(k_2) v_2); gamma_1 only touches the zero state.
+    q = np.array([[0.0], [0.5]])
+    k = np.array([[1.0], [-1.0]])
+    v = np.array([[2.0], [3.0]])
+    gamma = np.array([[0.25], [0.5]])
+    o, S, _ = one("gla", q, k, v, gamma)
+    phi_k1, phi_k2, phi_q2 = 2.0, math.exp(-1.0), 1.5
+    assert o[0, 0] == pytest.approx(1.0 * phi_k1 * 2.0, rel=1e-15)
+    expect = phi_q2 * (0.5 * phi_k1 * 2.0 + phi_k2 * 3.0)
+    assert o[1, 0] == pytest.approx(expect, rel=1e-15)
+
+
+def test_additive_memory_regrouped_sum():
+    # "Beyond attention" 18.1 and its browser lab: for 50 random keys and
+    # values, the regrouped sum equals the state recurrence S = sum v k^T.
+    r = rng(8)
+    T, d = 50, 32
+    q, k, v = (r.standard_normal((T, d)) for _ in range(3))
+    o, _, _ = one("gla", q, k, v, np.ones((T, d)), identity_phi=True)
+    ref = forms.additive_regrouped(q, k, v)
+    assert np.max(np.abs(o - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+# ----------------------------------------------------------------- (c) gdn
+
+def _writes(case):
+    ks = np.array([w[0] for w in case["writes"]], np.float64)
+    vs = np.array([[w[1]] for w in case["writes"]], np.float64)
+    T = len(ks)
+    return ks, vs, np.ones(T), np.ones(T)
+
+
+def test_gdn_two_key_example_golden():
+    with open(os.path.join(GOLDEN, "two_key_delta.json")) as f:
+        case = json.load(f)["cases"][0]
+    ks, vs, g, b = _writes(case)
+    q = np.array([[0.0, 1.0], [0.0, 1.0], [0.0, 1.0]])     # read the orthogonal key
+    o, S, _ = one("gdn", q, ks, vs, g, b)
+    assert S.tolist() == case["final_state"]               # exact: [5, 3]
+    assert o[2, 0] == 3.0                                   # orthogonal association kept
+
+
+def test_gdn_repeated_key_overwrites():
+    with open(os.path.join(GOLDEN, "two_key_delta.json")) as f:
+        case = json.load(f)["cases"][1]
+    ks, vs, g, b = _writes(case)
+    q = np.array([[1.0, 0.0]] * 3)
+    o, S, _ = one("gdn", q, ks, vs, g, b)
+    assert o[1, 0] == case["recall_after_second_write"]
+    assert S.tolist() == case["final_state"]
+
+
+def test_gdn_beta_one_unit_key_recalls_exactly():
+    # With beta_t = 1 and |k_t| = 1 the write leaves S_t k_t = v_t for any
+    # gate (the delta term removes what the decayed state returns for k_t).
+    r = rng(9)
+    T, dk, dv = 30, 16, 8
+    q = unit(r.standard_normal((T, dk)))
+    k = unit(r.standard_normal((T, dk)))
+    v = r.standard_normal((T, dv))
+    g = sigmoid(r.standard_normal(T) + 1)
+    o, _, _ = one("gdn", k, k, v, g, np.ones(T))              # read with q = k_t
+    assert np.max(np.abs(o - v)) <= 1e-13
+
+
+def test_gdn_equals_product_form():
+    # The concept-page form (error against the decayed state) equals
+    # g S (I - beta k k^T) + beta v k^T of "Beyond attention" 18.2.
+    r = rng(10)
+    T, dk, dv = 40, 12, 10
+    q, k, v = r.standard_normal((T, dk)), unit(r.standard_normal((T, dk))), r.standard_normal((T, dv))
+    g, b = sigmoid(r.standard_normal(T) + 2), sigmoid(r.standard_normal(T))
+    S0 = r.standard_normal((dv, dk)) * 0.3
+    o, S, _ = one("gdn", q, k, v, g, b, state=S0)
+    o_l, S_l = forms.gdn_literal(q, k, v, g, b, S0)
+    assert np.max(np.abs(o - o_l)) <= 1e-12 * np.max(np.abs(o_l))
+    assert np.max(np.abs(S.reshape(dv, dk) - S_l)) <= 1e-12 * np.max(np.abs(S_l))
+
+
+def test_gdn_gate_one_is_gradient_step():
+    # g = 1: S_t = S_{t-1} - beta (S_{t-1} k - v) k^T ("Beyond attention" 18.2).
+    r = rng(11)
+    dk, dv = 8, 5
+    S0 = r.standard_normal((dv, dk))
+    k = unit(r.standard_normal((1, dk)))
+    v, q = r.standard_normal((1, dv)), r.standard_normal((1, dk))
+    beta = 0.37
+    _, S, _ = one("gdn", q, k, v, np.ones(1), np.array([beta]), state=S0)
+    expect = S0 - beta * np.outer(S0 @ k[0] - v[0], k[0])
+    assert np.max(np.abs(S.reshape(dv, dk) - expect)) <= 1e-15 * 10
+
+
+def test_gdn_beta_zero_is_pure_decay():
+    r = rng(12)
+    T, dk, dv = 10, 6, 4
+    S0 = r.standard_normal((dv, dk))
+    q, k, v = r.standard_normal((T, dk)), unit(r.standard_normal((T, dk))), r.standard_normal((T, dv))
+    g = sigmoid(r.standard_normal(T) + 1)
+    o, S, _ = one("gdn", q, k, v, g, np.zeros(T), state=S0)
+    dec = np.cumprod(g)
+    assert np.max(np.abs(S.reshape(dv, dk) - dec[-1] * S0)) <= 1e-15 * 10
+    assert np.max(np.abs(o - dec[:, None] * (q @ S0.T))) <= 1e-14
+
+
+def test_gdn_orthonormal_keys_exact_recall():
+    # K <= d_k orthonormal keys, beta = 1, g = 1: every binding recalls exactly.
+    r = rng(13)
+    dk, dv, K = 16, 8, 16
+    Qm, _ = np.linalg.qr(r.standard_normal((dk, dk)))
+    keys = Qm.T[:K]
+    vals = r.standard_normal((K, dv))
+    _, S, _ = one("gdn", keys, keys, vals, np.ones(K), np.ones(K))
+    S = S.reshape(dv, dk)
+    assert np.max(np.abs(keys @ S.T - vals)) <= 1e-13
+
+
+def test_gdn_unrolled_transition_product():
+    r = rng(14)
+    T, dk, dv = 12, 6, 5
+    q, k, v = r.standard_normal((T, dk)), unit(r.standard_normal((T, dk))), r.standard_normal((T, dv))
+    g, b = sigmoid(r.standard_normal(T) + 2), sigmoid(r.standard_normal(T))
+    S0 = r.standard_normal((dv, dk)) * 0.5
+    o, S, _ = one("gdn", q, k, v, g, b, state=S0)
+    o_u, S_u = forms.gdn_unrolled(q, k, v, g, b, S0)
+    assert np.max(np.abs(o - o_u)) <= 1e-12 * np.max(np.abs(o_u))
+    assert np.max(np.abs(S.reshape(dv, dk) - S_u)) <= 1e-12 * np.max(np.abs(S_u))
+
+
+def test_figure_18_2_delta_vs_additive():
+    # "Beyond attention", Figure 18.2: 4x4 state; a and b perpendicular, c
+    # overlaps a; write a, b, c, then a new value under a. The delta rule
+    # recalls exactly the new value for a; plain addition returns old + new
+    # + (c . a) times c's value.
+    r = rng(15)
+    a, b = np.eye(4)[0], np.eye(4)[1]
+    c = unit(np.array([1.0, 0.0, 1.0, 0.0]))
+    keys = np.stack([a, b, c, a])
+    vals = r.standard_normal((4, 4))
+    _, S_d, _ = one("gdn", keys, keys, vals, np.ones(4), np.ones(4))
+    assert np.max(np.abs(S_d.reshape(4, 4) @ a - vals[3])) <= 1e-15 * 10
+    o_add, _, _ = one("gla", keys, keys, vals, np.ones((4, 4)), identity_phi=True)
+    expect = vals[0] + vals[3] + (c @ a) * vals[2]
+    assert np.max(np.abs(o_add[3] - expect)) <= 1e-14
+
+
+# ------------------------------------------------------ all: state passing
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+def test_split_continuation_equals_one_shot(variant):
+    r = rng(16)
+    T, dk, dv, T1 = 37, 8, 6, 15
+    q, k, v = r.standard_normal((T, dk)), r.standard_normal((T, dk)), r.standard_normal((T, dv))
+    gate = beta = None
+    if variant == "gla":
+        gate = sigmoid(r.standard_normal((T, dk)) + 2)
+    if variant == "gdn":
+        k = unit(k)
+        gate, beta = sigmoid(r.standard_normal(T) + 3), sigmoid(r.standard_normal(T))
+    o, st, _ = one(variant, q, k, v, gate, beta)
+    sl = lambda a, s: None if a is None else a[s]
+    a, b = slice(0, T1), slice(T1, T)
+    o1, st1, _ = one(variant, q[a], k[a], v[a], sl(gate, a), sl(beta, a))
+    o2, st2, _ = one(variant, q[b], k[b], v[b], sl(gate, b), sl(beta, b), state=st1)
+    assert np.max(np.abs(np.concatenate([o1, o2]) - o)) <= 1e-13 * max(1, np.max(np.abs(o)))
+    assert np.max(np.abs(st2 - st)) <= 1e-13 * max(1, np.max(np.abs(st)))
+
+
+def test_oracle_batches_are_independent():
+    # A batched call equals per-sequence calls (no cross-talk between (b,h)).
+    r = rng(17)
+    B, H, T, d = 2, 3, 9, 4
+    q, k, v = (r.standard_normal((B, H, T, d)) for _ in range(3))
+    g = sigmoid(r.standard_normal((B, H, T)) + 2)
+    be = sigmoid(r.standard_normal((B, H, T)))
+    res = oracle.run("gdn", q, unit(k), v, g, be)
+    for bb in range(B):
+        for hh in range(H):
+            o, S, _ = one("gdn", q[bb, hh], unit(k[bb, hh]), v[bb, hh], g[bb, hh], be[bb, hh])
+            assert np.array_equal(res.o[bb, hh], o)
+            assert np.array_equal(res.state[bb, hh], S)
