@@ -1,0 +1,45 @@
+// Internal interface between the C ABI (api.cu) and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+namespace la {
+
+enum Variant : int { kNorm = 0, kGla = 1, kGdn = 2 };
+enum Io : int { kBf16 = 0, kFp32 = 1 };
+
+// Everything a launch needs. Pointers are device pointers owned by the caller.
+struct FwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* gate;
+    const float* beta;
+    const float* state_in;
+    void* out;
+    float* state_out;
+    float* den_out;
+    int BH;          // batch * heads
+    int T;           // tokens per sequence (1 for decode)
+    int dk, dv;
+    int variant;     // Variant
+    int io;          // Io
+    unsigned flags;  // LA_FLAG_*
+    int* status;     // device status word
+    int sm_count;
+};
+
+// Token-by-token recurrence on CUDA cores; any supported head size, fp32 or
+// bf16 io. One CTA per sequence-head.
+cudaError_t launch_recurrent(const FwdArgs& a, cudaStream_t s);
+
+// One decode step for every sequence-head; streams the fp32 state.
+cudaError_t launch_decode(const FwdArgs& a, cudaStream_t s);
+
+// Chunkwise tensor-core prefill (tcgen05, TMA); bf16 io, d_k, d_v in {64,128}.
+// Returns cudaSuccess or the first CUDA error; `what` names the failing step.
+cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEncodeTiled_v12000 encode,
+                           const char** what);
+
+}  // namespace la

@@ -1,0 +1,65 @@
+// Host side of the chunkwise prefill: TMA tensor maps and dispatch.
+#include "prefill.h"
+#include "prefill_impl.cuh"
+
+namespace la {
+
+namespace {
+
+// 3-D map over a [BH, T, d] tensor with 64x64 boxes (one 128-byte swizzle
+// atom wide). Rows past T read as zeros.
+CUresult map_qkv(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, int d, int T, int BH) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * T};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(chunk::C), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+// 3-D map over the per-channel gates [BH, T, dk] fp32, full-width boxes.
+CUresult map_gate(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, int dk, int T, int BH) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(dk), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(dk) * 4, static_cast<cuuint64_t>(dk) * 4 * T};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(dk), static_cast<cuuint32_t>(chunk::C), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEncodeTiled_v12000 enc, const char** what) {
+    chunk::Maps m;
+    *what = "cuTensorMapEncodeTiled";
+    if (map_qkv(enc, &m.q, a.q, a.dk, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (map_qkv(enc, &m.k, a.k, a.dk, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (map_qkv(enc, &m.v, a.v, a.dv, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (a.variant == kGla) {
+        if (map_gate(enc, &m.g, a.gate, a.dk, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    } else {
+        m.g = m.q;
+    }
+    chunk::Params p;
+    p.gate = a.gate;
+    p.beta = a.beta;
+    p.state_in = a.state_in;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.state_out = a.state_out;
+    p.den_out = a.den_out;
+    p.T = a.T;
+    p.nchunks = (a.T + chunk::C - 1) / chunk::C;
+    p.flags = a.flags;
+    p.status = a.status;
+    *what = "chunked prefill launch";
+    switch (a.variant) {
+        case kNorm: return chunk::launch_norm(a.dk, a.dv, m, p, a.BH, s);
+        case kGla: return chunk::launch_gla(a.dk, a.dv, m, p, a.BH, s);
+        case kGdn: return chunk::launch_gdn(a.dk, a.dv, m, p, a.BH, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace la

@@ -1,0 +1,30 @@
+// Instantiations of the chunkwise prefill kernel for one variant.
+#include "prefill.h"
+#include "prefill_impl.cuh"
+
+namespace la {
+namespace chunk {
+namespace {
+
+template <int DK, int DV>
+cudaError_t run(const Maps& m, const Params& p, int BH, cudaStream_t s) {
+    using L = Layout<kGla, DK, DV>;
+    auto kern = chunk_kernel<kGla, DK, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    kern<<<BH, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gla(int dk, int dv, const Maps& m, const Params& p, int BH, cudaStream_t s) {
+    if (dk == 64 && dv == 64) return run<64, 64>(m, p, BH, s);
+    if (dk == 64 && dv == 128) return run<64, 128>(m, p, BH, s);
+    if (dk == 128 && dv == 64) return run<128, 64>(m, p, BH, s);
+    if (dk == 128 && dv == 128) return run<128, 128>(m, p, BH, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace chunk
+}  // namespace la

@@ -1,0 +1,157 @@
+/*
+ * la.h - C ABI of the causal linear-attention operator with a fixed matrix
+ * state, for NVIDIA GB300 (sm_103a).
+ *
+ * The operator runs a sequence of tokens through a recurrent matrix state,
+ * one independent recurrence per (batch, head). Three variants:
+ *
+ *   LA_NORM_ELU1  normalized kernel attention, phi(x) = elu(x) + 1:
+ *                   S_t = S_{t-1} + phi(k_t) v_t^T,   z_t = z_{t-1} + phi(k_t),
+ *                   o_t = phi(q_t)^T S_t / phi(q_t)^T z_t.
+ *                 ("Linear Attention" concept page, normalized kernel
+ *                 formulation; "Linear attention and recurrent memory", The
+ *                 big idea; "Linear attention and Hyena", section 11.2.)
+ *   LA_GLA        per-channel gated attention (GLA / RetNet family):
+ *                   S_t = diag(gamma_t) S_{t-1} + phi(k_t) v_t^T,  o_t = S_t^T phi(q_t),
+ *                 gamma_t in (0,1]^{d_k}. ("Linear attention and Hyena",
+ *                 section 11.3 and Exercise 11.5.)
+ *   LA_GDN        gated delta rule, S in R^{d_v x d_k}, unit-length keys:
+ *                   S_t = g_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *                   o_t = S_t q_t.
+ *                 ("Beyond attention", section 18.2; "Linear Attention"
+ *                 concept page, gated delta rule.)
+ *
+ * Every variant updates first and then reads, so token t attends to itself.
+ *
+ * LAYOUTS. Every tensor is contiguous and row-major. BH = B*H and (b,h) is
+ * the index b*H + h.
+ *   q, k       [B, H, T, d_k]   io dtype
+ *   v, out     [B, H, T, d_v]   io dtype
+ *   gate       LA_NORM_ELU1: unused (pass NULL)
+ *              LA_GLA: [B, H, T, d_k] fp32, gamma in (0, 1]
+ *              LA_GDN: [B, H, T] fp32, g in (0, 1]
+ *   beta       LA_GDN: [B, H, T] fp32 in [0, 1]; NULL otherwise
+ *   state      fp32, one block per (b,h):
+ *              LA_NORM_ELU1: S [d_k, d_v] immediately followed by z [d_k]
+ *              LA_GLA:       S [d_k, d_v]
+ *              LA_GDN:       S [d_v, d_k]
+ *   den_out    LA_NORM_ELU1 only, optional: [B, H, T] fp32 denominators
+ *              phi(q_t)^T z_t.
+ * For la_decode_step, drop the T axis: q,k [B,H,d_k], v,out [B,H,d_v],
+ * gate [B,H,d_k] (gla) or [B,H] (gdn), beta [B,H].
+ *
+ * Keys of LA_GDN are assumed to have unit L2 norm; the library does not
+ * normalize them. No scale is applied to q.
+ *
+ * OWNERSHIP. The caller owns every buffer. Pointers to q, k, v, gate, beta,
+ * state and out are CUDA device pointers (device memory, or managed memory
+ * resident on the device). The library never frees or retains them after a
+ * call returns. la_create allocates the handle and one device status word;
+ * la_destroy frees both.
+ *
+ * EXECUTION. Calls are asynchronous on the given CUDA stream (NULL = the
+ * legacy default stream) and never synchronize the device, except
+ * la_status. A handle serves one host thread at a time.
+ *
+ * ERRORS. Every entry point returns 0 (LA_OK) or a positive LA_ERR_* code,
+ * and validates all arguments before anything is launched, so a rejected
+ * call never touches the GPU. la_last_error(h) returns the text of the
+ * last failure on h. Nothing is printed and no exception crosses the ABI.
+ * Device-side failures (a bounded wait that expired) are recorded in the
+ * device status word and reported by la_status.
+ */
+#ifndef LA_H
+#define LA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct la_handle la_handle;
+
+typedef enum { LA_NORM_ELU1 = 0, LA_GLA = 1, LA_GDN = 2 } la_variant;
+
+/* dtype of q, k, v and out. State, gates and beta are always fp32. */
+typedef enum { LA_BF16 = 0, LA_FP32 = 1 } la_dtype;
+
+enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,  /* NULL handle or required pointer, bad enum, negative size */
+    LA_ERR_UNSUPPORTED = 2,  /* head size or chunk size outside the supported set, wrong GPU */
+    LA_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned */
+    LA_ERR_CUDA = 4,         /* a CUDA runtime call failed; see la_last_error */
+    LA_ERR_TIMEOUT = 5       /* a bounded wait inside a kernel expired (la_status) */
+};
+
+/* la_config.flags */
+#define LA_FLAG_IDENTITY_PHI 0x1u   /* LA_GLA without the feature map (phi = identity) */
+#define LA_FLAG_TEST_TIMEOUT 0x100u /* test hook: the chunked prefill kernel waits once on a
+                                       barrier nothing signals, with a 1 ms limit, then
+                                       records LA_ERR_TIMEOUT in the status word and exits */
+
+typedef struct {
+    int B;          /* batch, >= 1 */
+    int H;          /* heads, >= 1 */
+    int d_k;        /* key/query size: 16, 32, 64 or 128 */
+    int d_v;        /* value size: 16, 32, 64 or 128 */
+    la_dtype io;    /* dtype of q, k, v, out */
+    unsigned flags; /* LA_FLAG_* */
+    int device;     /* CUDA device ordinal the handle is bound to */
+} la_config;
+
+/* Create a handle bound to cfg->device. Checks that the device is an
+ * sm_103 GPU (LA_ERR_UNSUPPORTED otherwise). */
+int la_create(const la_config* cfg, la_handle** out);
+
+/*
+ * Prefill: run T tokens of every (b,h) sequence from state_in and write the
+ * outputs and the final state.
+ *   state_in  NULL means S_0 = 0 (and z_0 = 0).
+ *   state_out NULL means the final state is not written. It may alias
+ *             state_in.
+ *   T         tokens per sequence, >= 0. T = 0 writes no output and copies
+ *             state_in (or zeros) to state_out.
+ *   chunk     0 = default (64). 1 = token-by-token recurrent kernel. 64 =
+ *             chunkwise tensor-core kernel (bf16 io, d_k and d_v in {64, 128}).
+ *             fp32 io and head sizes 16/32 always use the recurrent kernel.
+ *             Other values: LA_ERR_UNSUPPORTED.
+ *   den_out   optional, LA_NORM_ELU1 only.
+ * The chunkwise kernel needs q, k, v (and the LA_GLA gate) 16-byte aligned.
+ */
+int la_forward(la_handle* h, const void* q, const void* k, const void* v,
+               const float* gate, const float* beta, const float* state_in,
+               void* out, float* state_out, float* den_out,
+               int variant, int T, int chunk, void* cuda_stream);
+
+/*
+ * One decode step: advance every (b,h) state by one token and write its
+ * output. state_out may equal state_in, which updates the state in place.
+ * state_in NULL means a zero state. state_out must not be NULL.
+ * den_out is optional ([B,H] fp32, LA_NORM_ELU1 only).
+ */
+int la_decode_step(la_handle* h, const void* q, const void* k, const void* v,
+                   const float* gate, const float* beta, const float* state_in,
+                   void* out, float* state_out, float* den_out,
+                   int variant, void* cuda_stream);
+
+/* Synchronize cuda_stream, then read and clear the device status word.
+ * Returns LA_OK, LA_ERR_TIMEOUT if a kernel recorded an expired wait since
+ * the last call, or LA_ERR_CUDA. */
+int la_status(la_handle* h, void* cuda_stream);
+
+/* Destroy a handle (NULL is allowed). */
+void la_destroy(la_handle* h);
+
+/* Text of the last failure on h ("" if none). Valid until the next call on h. */
+const char* la_last_error(const la_handle* h);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int la_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H */

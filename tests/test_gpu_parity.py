@@ -1,0 +1,318 @@
+"""GPU parity: the CUDA path against the float64 oracle on the same seeded
+inputs. Tolerances: max relative error per (b,h) slice <= 2e-2 for bf16 io
+(output and final state) and <= 1e-4 for fp32 io; the normalizer
+denominator is checked elementwise against the oracle's."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from _helpers import TOL, from_torch, oracle_inputs, run_gpu_prefill, slice_rel_err, to_torch
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import gated_delta_rule_causal_gb300 as la  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    la.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def base(variant, d):
+    w = {"norm": W.NORM_B4H8_T2048_D64, "gla": W.GLA_B4H16_T4096_D128, "gdn": W.GDN_B2H16_T8192_D128}[variant]
+    return W.small(w, B=1, H=2, dk=d, dv=d)
+
+
+def handle(w, flags=0):
+    return la.Handle(w.B, w.H, w.dk, w.dv, io=w.io, flags=flags)
+
+
+def oracle_run(w, inp, state_in=None):
+    q, k, v, g, b = oracle_inputs(inp)
+    sin = None if state_in is None else np.asarray(state_in, np.float64)
+    return oracle.run(w.variant, q, k, v, g, b, sin)
+
+
+def assert_parity(w, inp, chunk=0, state_in=None, tol=None):
+    h = handle(w)
+    o, st, den = run_gpu_prefill(h, w, inp, chunk, state_in, with_den=(w.variant == "norm"))
+    ref = oracle_run(w, inp, state_in)
+    tol = tol or TOL[w.io]
+    e_o, e_s = slice_rel_err(o, ref.o), slice_rel_err(st, ref.state)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(st))
+    assert e_o <= tol, f"output rel err {e_o:.3g} > {tol}"
+    assert e_s <= tol, f"state rel err {e_s:.3g} > {tol}"
+    if den is not None:
+        e_d = float(np.max(np.abs(den - ref.den) / ref.den))
+        assert e_d <= tol, f"denominator rel err {e_d:.3g} > {tol}"
+    h.close()
+    return e_o, e_s
+
+
+# ------------------------------------------------------------- prefill, chunked
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [1, 15, 64, 65, 200])
+def test_chunked_prefill_parity(variant, d, T):
+    w = base(variant, d).with_(T=T)
+    assert_parity(w, W.draw(w, seed=T), chunk=64)
+
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64)])
+def test_chunked_prefill_rectangular_heads(variant, dk, dv):
+    w = base(variant, 64).with_(dk=dk, dv=dv, T=130)
+    assert_parity(w, W.draw(w, seed=3), chunk=64)
+
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+def test_chunked_prefill_from_a_state(variant):
+    w = base(variant, 128).with_(T=150)
+    inp = W.draw(w, seed=11)
+    rng = np.random.default_rng(5)
+    ss = oracle.state_size(variant, w.dk, w.dv)
+    sin = (rng.standard_normal((w.B, w.H, ss)) * 0.1).astype(np.float32)
+    if variant == "norm":   # z must stay a positive sum of feature maps
+        sin[..., w.dk * w.dv:] = np.abs(sin[..., w.dk * w.dv:]) * 50 + 1.0
+    assert_parity(w, inp, chunk=64, state_in=sin)
+
+
+def test_gla_identity_feature_map():
+    w = base("gla", 128).with_(T=100)
+    inp = W.draw(w, seed=4)
+    h = handle(w, flags=la.LA_FLAG_IDENTITY_PHI)
+    o, st, _ = run_gpu_prefill(h, w, inp, 64)
+    q, k, v, g, b = oracle_inputs(inp)
+    ref = oracle.run("gla", q, k, v, g, None, identity_phi=True)
+    assert slice_rel_err(o, ref.o) <= 2e-2 and slice_rel_err(st, ref.state) <= 2e-2
+
+
+def test_gla_small_gates():
+    # gamma = 0.5 on every channel: the in-chunk rescaling spans 2^64.
+    w = base("gla", 64).with_(T=200)
+    inp = W.draw(w, seed=8)
+    inp.gate[...] = 0.5
+    assert_parity(w, inp, chunk=64)
+
+
+def test_gdn_small_gates_and_full_beta():
+    w = base("gdn", 128).with_(T=200)
+    inp = W.draw(w, seed=9)
+    inp.gate[...] = 0.3
+    inp.beta[..., ::3] = 1.0
+    assert_parity(w, inp, chunk=64)
+
+
+# ------------------------------------------------------------- recurrent path
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("io", ["fp32", "bf16"])
+def test_recurrent_prefill_parity(variant, d, io):
+    w = base(variant, d).with_(T=70, io=io)
+    assert_parity(w, W.draw(w, seed=d), chunk=1)
+
+
+def test_normalized_t64_d16_fp32():
+    # The float64 correctness workload, run with fp32 io on the GPU.
+    w = W.NORM_T64_D16
+    e_o, e_s = assert_parity(w, W.draw(w, seed=0), chunk=0, tol=1e-4)
+    assert e_o <= 1e-4 and e_s <= 1e-4
+
+
+# ------------------------------------------------------------- state passing
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+def test_split_continuation(variant):
+    w = base(variant, 128).with_(T=192)
+    inp = W.draw(w, seed=21)
+    T1 = 80    # not a chunk multiple
+    h = handle(w)
+    o_full, st_full, _ = run_gpu_prefill(h, w, inp, 64)
+
+    def part(a, sl):
+        return None if a is None else np.ascontiguousarray(a[:, :, sl])
+
+    first = W.Inputs(part(inp.q, slice(0, T1)), part(inp.k, slice(0, T1)), part(inp.v, slice(0, T1)),
+                     part(inp.gate, slice(0, T1)), part(inp.beta, slice(0, T1)), None)
+    second = W.Inputs(part(inp.q, slice(T1, None)), part(inp.k, slice(T1, None)), part(inp.v, slice(T1, None)),
+                      part(inp.gate, slice(T1, None)), part(inp.beta, slice(T1, None)), None)
+    o1, st1, _ = run_gpu_prefill(h, w.with_(T=T1), first, 64)
+    o2, st2, _ = run_gpu_prefill(h, w.with_(T=w.T - T1), second, 64, state_in=st1.astype(np.float32))
+    ref = oracle_run(w, inp)
+    assert slice_rel_err(np.concatenate([o1, o2], axis=2), ref.o) <= 2e-2
+    assert slice_rel_err(st2, ref.state) <= 2e-2
+    assert slice_rel_err(st2, st_full) <= 2e-2
+
+
+# ------------------------------------------------------------- decode
+
+def decode_inputs(w, step, seed):
+    return W.draw_decode_step(w, step, seed)
+
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("d", [16, 64, 128])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_decode_parity(variant, d, in_place):
+    w = base(variant, d).with_(B=3, H=5, T=1, state_std=0.05)
+    st0 = W.draw_decode_state(w, seed=2).reshape(w.B, w.H, -1)
+    if variant == "norm":
+        st0[..., w.dk * w.dv:] = np.abs(st0[..., w.dk * w.dv:]) * 20 + 1.0
+    h = handle(w)
+    s_dev = torch.from_numpy(st0).cuda()
+    ref_state = st0.astype(np.float64)
+    for step in range(3):
+        inp = decode_inputs(w, step, seed=2)
+        q, k, v = (to_torch(a, h.device) for a in (inp.q, inp.k, inp.v))
+        g, b = to_torch(inp.gate, h.device), to_torch(inp.beta, h.device)
+        den = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda") if variant == "norm" else None
+        s_out = s_dev if in_place else None
+        o, s_new, den = h.decode_step(q, k, v, g, b, s_dev, variant=variant, state_out=s_out, den_out=den)
+        torch.cuda.synchronize()
+        qo, ko, vo, go, bo = oracle_inputs(inp)
+        ex = lambda a: None if a is None else a[:, :, None]
+        ref = oracle.run(variant, ex(qo), ex(ko), ex(vo), ex(go), ex(bo), ref_state)
+        assert slice_rel_err(from_torch(o), ref.o[:, :, 0]) <= 2e-2
+        assert slice_rel_err(s_new.cpu().numpy(), ref.state) <= 1e-5
+        if den is not None:
+            assert np.max(np.abs(den.cpu().numpy() - ref.den[:, :, 0]) / ref.den[:, :, 0]) <= 1e-5
+        ref_state = ref.state
+        s_dev = s_new
+
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+def test_prefill_then_decode_equals_longer_prefill(variant):
+    w = base(variant, 128).with_(T=100)
+    inp = W.draw(w, seed=31)
+    T1 = 97
+    h = handle(w)
+    cut = lambda a, sl: None if a is None else np.ascontiguousarray(a[:, :, sl])
+    pre = W.Inputs(cut(inp.q, slice(0, T1)), cut(inp.k, slice(0, T1)), cut(inp.v, slice(0, T1)),
+                   cut(inp.gate, slice(0, T1)), cut(inp.beta, slice(0, T1)), None)
+    _, st, _ = run_gpu_prefill(h, w.with_(T=T1), pre, 64)
+    s_dev = torch.from_numpy(st.astype(np.float32)).cuda()
+    outs = []
+    for t in range(T1, w.T):
+        sel = lambda a: None if a is None else to_torch(np.ascontiguousarray(a[:, :, t]), h.device)
+        o, s_dev, _ = h.decode_step(sel(inp.q), sel(inp.k), sel(inp.v), sel(inp.gate), sel(inp.beta), s_dev,
+                                    variant=variant, state_out=s_dev)
+        outs.append(from_torch(o))
+    torch.cuda.synchronize()
+    ref = oracle_run(w, inp)
+    assert slice_rel_err(np.stack(outs, axis=2), ref.o[:, :, T1:]) <= 2e-2
+    assert slice_rel_err(s_dev.cpu().numpy(), ref.state) <= 2e-2
+
+
+# ------------------------------------------------------------- full sizes, sampled
+
+SAMPLE_HEADS = [(0, 0), (0, 5), (-1, -1)]
+
+
+@pytest.mark.parametrize("w", [W.NORM_B4H8_T2048_D64, W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128],
+                         ids=lambda w: w.name)
+def test_full_size_sampled_heads(w):
+    inp = W.draw(w, seed=0)
+    h = handle(w)
+    o, st, den = run_gpu_prefill(h, w, inp, 0, with_den=(w.variant == "norm"))
+    q, k, v, g, b = oracle_inputs(inp)
+    for bb, hh in SAMPLE_HEADS:
+        sel = lambda a: None if a is None else a[bb:bb + 1 if bb != -1 else None][:, hh:hh + 1 if hh != -1 else None]
+        ref = oracle.run(w.variant, sel(q), sel(k), sel(v), sel(g), sel(b))
+        assert slice_rel_err(sel(o), ref.o) <= 2e-2
+        assert slice_rel_err(sel(st), ref.state) <= 2e-2
+        if den is not None:
+            assert np.max(np.abs(sel(den) - ref.den) / ref.den) <= 2e-2
+
+
+def test_full_size_decode_sampled_heads():
+    w = W.GDN_DECODE_N256H16_D128
+    st0 = W.draw_decode_state(w, seed=0).reshape(w.B, w.H, -1)
+    h = handle(w)
+    s_dev = torch.from_numpy(st0).cuda()
+    steps = 4
+    inps = [W.draw_decode_step(w, s, seed=0) for s in range(steps)]
+    for inp in inps:
+        q, k, v = (to_torch(a, h.device) for a in (inp.q, inp.k, inp.v))
+        _, s_dev, _ = h.decode_step(q, k, v, to_torch(inp.gate, h.device), to_torch(inp.beta, h.device), s_dev,
+                                    variant="gdn", state_out=s_dev)
+    last_o, _, _ = h.decode_step(*(to_torch(a, h.device) for a in (inps[0].q, inps[0].k, inps[0].v,
+                                                                     inps[0].gate, inps[0].beta)),
+                                 s_dev.clone(), variant="gdn")
+    torch.cuda.synchronize()
+    got = s_dev.cpu().numpy()
+    for bb, hh in [(0, 0), (17, 3), (255, 15)]:
+        ref_s = st0[bb, hh].astype(np.float64)[None, None]
+        for inp in inps:
+            qo, ko, vo, go, bo = oracle_inputs(inp)
+            one = lambda a: a[bb:bb + 1, hh:hh + 1, None]
+            ref_s = oracle.run("gdn", one(qo), one(ko), one(vo), one(go), one(bo), ref_s).state
+        assert slice_rel_err(got[bb:bb + 1, hh:hh + 1], ref_s) <= 1e-5
+        qo, ko, vo, go, bo = oracle_inputs(inps[0])
+        one = lambda a: a[bb:bb + 1, hh:hh + 1, None]
+        ref_o = oracle.run("gdn", one(qo), one(ko), one(vo), one(go), one(bo), ref_s).o[:, :, 0]
+        assert slice_rel_err(from_torch(last_o)[bb:bb + 1, hh:hh + 1], ref_o) <= 2e-2
+
+
+# ------------------------------------------------------------- edges and errors
+
+def test_zero_tokens_copies_state():
+    w = base("gdn", 64).with_(T=0)
+    h = handle(w)
+    sin = torch.randn(w.B, w.H, w.dk * w.dv, device="cuda")
+    sout = torch.full_like(sin, 7.0)
+    e = torch.empty(0, device="cuda", dtype=torch.bfloat16)
+    rc = la.la_forward(h._h, e.data_ptr(), e.data_ptr(), e.data_ptr(), None, None, sin.data_ptr(), e.data_ptr(),
+                       sout.data_ptr(), None, la.LA_GDN, 0, 0, la._stream_ptr(None))
+    assert rc == la.LA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(sin, sout)
+    rc = la.la_forward(h._h, None, None, None, None, None, None, None, sout.data_ptr(), None, la.LA_GDN, 0, 0,
+                       la._stream_ptr(None))
+    torch.cuda.synchronize()
+    assert rc == la.LA_OK and torch.count_nonzero(sout).item() == 0
+
+
+def test_rejected_calls_do_not_launch():
+    w = base("gdn", 64).with_(T=64)
+    h = handle(w)
+    inp = W.draw(w, 0)
+    q, k, v = (to_torch(a, h.device) for a in (inp.q, inp.k, inp.v))
+    g, b = to_torch(inp.gate, h.device), to_torch(inp.beta, h.device)
+    out = torch.empty_like(v)
+    st = la._stream_ptr(None)
+    P = lambda t: None if t is None else t.data_ptr()
+    fwd = lambda **kw: la.la_forward(h._h, kw.get("q", P(q)), P(k), P(v), kw.get("g", P(g)), kw.get("b", P(b)),
+                                     None, P(out), None, kw.get("den", None), kw.get("var", la.LA_GDN),
+                                     kw.get("T", 64), kw.get("chunk", 0), st)
+    assert fwd(chunk=32) == la.LA_ERR_UNSUPPORTED
+    assert fwd(b=None) == la.LA_ERR_INVALID_ARG
+    assert fwd(var=9) == la.LA_ERR_INVALID_ARG
+    assert fwd(T=-1) == la.LA_ERR_INVALID_ARG
+    assert fwd(q=P(q) + 2) == la.LA_ERR_MISALIGNED
+    dummy = torch.empty(64, device="cuda")
+    assert fwd(den=dummy.data_ptr()) == la.LA_ERR_INVALID_ARG
+    assert "den_out" in la.la_last_error(h._h)
+    assert h.status() == la.LA_OK
+    hf = la.Handle(1, 2, 64, 64, io="fp32")
+    qf = torch.zeros(1, 2, 64, 64, device="cuda")
+    assert la.la_forward(hf._h, P(qf), P(qf), P(qf), P(g), P(b), None, P(qf), None, None, la.LA_GDN, 64, 64,
+                         st) == la.LA_ERR_UNSUPPORTED
+
+
+def test_bounded_wait_expires_cleanly():
+    # The test hook makes the chunked kernel wait on a barrier nothing signals;
+    # the wait gives up after 1 ms, the kernel records it and exits cleanly.
+    w = base("gdn", 128).with_(T=128)
+    inp = W.draw(w, 0)
+    h = handle(w, flags=la.LA_FLAG_TEST_TIMEOUT)
+    run_gpu_prefill(h, w, inp, 64)
+    assert h.status() == la.LA_ERR_TIMEOUT
+    assert "status bits 0x4" in la.la_last_error(h._h)
+    assert h.status() == la.LA_OK            # the word was cleared
+    h.close()
+    assert_parity(w, inp, chunk=64)          # the context is healthy
