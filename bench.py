@@ -425,6 +425,22 @@ def gpu_arm(args):
         dist.destroy_process_group()
 
 
+def kernel_only(args):
+    """Only the workload's launches (no suite, e2e, baseline or sampler)."""
+    import torch
+    import gated_delta_rule_causal_gb300 as la
+    la.build()
+    w = W.BY_NAME[args.workload] if args.workload else HEADLINE
+    if w.decode_steps:
+        r = DecodeRunner(w.with_(decode_steps=8), 0, torch, la)
+    else:
+        props = torch.cuda.get_device_properties(0)
+        r = PrefillRunner(w, 0, int(getattr(props, "L2_cache_size", 126 * 2 ** 20)), torch, la)
+    total_ms, per = time_steps(r, args.steps, args.warmup, torch)
+    print(json.dumps({"workload": w.name, "steps": args.steps, "ms_per_step": round(total_ms / args.steps, 5),
+                      "kernel_ms": [round(x, 5) for x in per]}), flush=True)
+
+
 def reference_arm(args):
     """The float64 CPU oracle, timed on the host cores (rank 0 only)."""
     ws, rank, _ = dist_env()
@@ -433,8 +449,6 @@ def reference_arm(args):
     import oracle
     oracle.build()
     w = W.BY_NAME[args.workload] if args.workload else HEADLINE
-    for _ in range(args.warmup):
-        pass
     x = W.draw(w, 0)
     q, k, v = W.as_f64(x.q), W.as_f64(x.k), W.as_f64(x.v)
     g = None if x.gate is None else x.gate.astype(np.float64)
@@ -472,11 +486,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None, choices=sorted(W.BY_NAME))
     ap.add_argument("--no-suite", action="store_true")
+    ap.add_argument("--only-kernel", action="store_true",
+                    help="run warmup + steps of the workload's kernel and nothing else (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         reference_arm(args)
+    elif args.only_kernel:
+        kernel_only(args)
     else:
         gpu_arm(args)
 

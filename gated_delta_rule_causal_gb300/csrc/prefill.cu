@@ -37,6 +37,7 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     if (map_qkv(enc, &m.q, a.q, a.dk, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (map_qkv(enc, &m.k, a.k, a.dk, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (map_qkv(enc, &m.v, a.v, a.dv, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (map_qkv(enc, &m.o, a.out, a.dv, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (a.variant == kGla) {
         if (map_gate(enc, &m.g, a.gate, a.dk, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     } else {
@@ -46,7 +47,6 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     p.gate = a.gate;
     p.beta = a.beta;
     p.state_in = a.state_in;
-    p.out = static_cast<__nv_bfloat16*>(a.out);
     p.state_out = a.state_out;
     p.den_out = a.den_out;
     p.T = a.T;

@@ -11,7 +11,7 @@ namespace la {
 namespace chunk {
 
 struct Maps {
-    CUtensorMap q, k, v, g;
+    CUtensorMap q, k, v, g, o;
 };
 
 struct Params;

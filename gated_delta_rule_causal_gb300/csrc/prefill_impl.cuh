@@ -3,15 +3,18 @@
 // One CTA per (b,h) sequence-head walks its sequence in chunks of C = 64
 // tokens. TMA stages the q/k/v tiles (and the per-channel gate tile of the
 // gated variant) of chunk c+1 while chunk c is computed. The dense products
-// run as tcgen05 bf16 MMAs with fp32 accumulators in tensor memory. The fp32
-// state is kept in registers (thread r owns state row r, r = value index)
-// and re-published each chunk as a bf16 MMA operand in shared memory.
+// run as tcgen05 bf16 MMAs with fp32 accumulators in tensor memory. The
+// fp32 state lives in registers and is re-published each chunk as a bf16 MMA
+// operand in shared memory. Outputs leave through a shared-memory tile and a
+// TMA store.
 //
 // Inside the kernel the state is always held as X [d_v rows][d_k cols]:
 // X = S^T for the normalized and gated variants (S is d_k x d_v there) and
 // X = S for the gated delta rule (S is d_v x d_k there). With that
 // orientation every state-side product has M = 128 (value rows, padded
-// when d_v = 64) and N = tokens or d_k.
+// when d_v = 64) and N = tokens or d_k. The 256 threads pair up on the 128
+// tensor-memory lanes: thread (r, h) owns row r and the h-th half of the
+// columns of whatever it reads (warp w serves lanes 32*(w%4).., h = w/4).
 //
 // Chunk algebra (G_t = sum of log-gates inside the chunk up to t, Gam_t =
 // exp(G_t), L = causal mask including the diagonal):
@@ -30,12 +33,18 @@
 //      U^T = Ut^T - X_0 W^T
 //      O^T = X_0 (diag(gam) Q)^T + U^T (M o Q K^T)^T,  M_tj = gam_t/gam_j (j <= t)
 //      X   = gam_C X_0 + U^T diag(gam_C/gam) K
-//    The triangular inverse T is formed in shared memory (fp32, blocked
-//    forward substitution).
+//    The triangular inverse T is formed in shared memory in fp32: the four
+//    16x16 diagonal blocks by forward substitution, then the off-diagonal
+//    blocks block row by block row.
 //
 // Tail chunks (T not a multiple of 64): TMA zero-fills rows past the end.
 // phi(0) = 1, so padded keys are zeroed explicitly; padded gates are 1 and
-// padded betas 0, which makes padded tokens leave the state untouched.
+// padded betas 0, which makes padded tokens leave the state untouched; the
+// TMA store clips rows past the end.
+//
+// Limit of the per-channel gated variant: the in-chunk rescaling divides by
+// Gam_j, so the product of 64 consecutive gates of one channel must stay
+// above ~1e-38 (fp32 range); per-token gates >= 0.25 always satisfy it.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -47,14 +56,13 @@ namespace la {
 namespace chunk {
 
 constexpr int C = 64;          // tokens per chunk
-constexpr int kThreads = 128;  // one thread per TMEM lane / state row
+constexpr int kThreads = 256;  // two threads per tensor-memory lane / state row
 constexpr int kAStride = 68;   // fp32 row stride of the 64x64 solve matrix
 
 struct Params {
     const float* gate;      // gdn: [BH, T] (gla gates travel by TMA)
     const float* beta;      // gdn: [BH, T]
     const float* state_in;  // may be NULL
-    __nv_bfloat16* out;
     float* state_out;       // may be NULL
     float* den_out;         // norm, may be NULL
     int T;
@@ -67,28 +75,30 @@ template <int VAR, int DK, int DV>
 struct Layout {
     static constexpr int KA = DK / 64;  // 64-column atoms along d_k
     static constexpr int VA = DV / 64;
+    static constexpr bool GDN = (VAR == kGdn);
     // q/k tile pair: per k-atom, rows 0-63 hold block 0 and rows 64-127 block 1.
-    static constexpr uint32_t QK_ATOM = 16384;
-    static constexpr uint32_t QK_BYTES = KA * QK_ATOM;
-    static constexpr uint32_t V_ATOM = 8192;
-    static constexpr uint32_t V_BYTES = VA * V_ATOM;
+    static constexpr uint32_t QK_BYTES = KA * 16384;
+    static constexpr uint32_t V_BYTES = VA * 8192;
     static constexpr uint32_t G_BYTES = (VAR == kGla) ? C * DK * 4 : 0;
     static constexpr uint32_t STAGE = QK_BYTES + V_BYTES + G_BYTES;
     static constexpr uint32_t TX_BYTES = 2 * KA * 8192 + V_BYTES + G_BYTES;
-    static constexpr uint32_t OFF_SS = 2 * STAGE;               // bf16 state, [128 rows][DK]
-    static constexpr uint32_t OFF_PS = OFF_SS + KA * 16384;     // bf16 [64 t][64 j]
-    static constexpr uint32_t OFF_KH = OFF_PS + 8192;           // gla: k^ [64 j][DK]
+    static constexpr uint32_t OFF_SS = 2 * STAGE;                 // bf16 state [128 rows][DK]
+    static constexpr uint32_t OFF_PS = OFF_SS + KA * 16384;       // bf16 [64 t][64 j]
+    static constexpr uint32_t OFF_KH = OFF_PS + 8192;             // gla: k^ [64 j][DK]
     static constexpr uint32_t KH_BYTES = (VAR == kGla) ? KA * 8192 : 0;
-    static constexpr bool GDN = (VAR == kGdn);
-    static constexpr uint32_t OFF_TB1 = OFF_KH + KH_BYTES;      // gdn: T diag(beta)      [t][j]
-    static constexpr uint32_t OFF_TB2 = OFF_TB1 + (GDN ? 8192 : 0);   // T diag(beta gam) [t][j]
-    static constexpr uint32_t OFF_WS = OFF_TB2 + (GDN ? 8192 : 0);    // W^T [dk rows][t]
-    static constexpr uint32_t OFF_US = OFF_WS + (GDN ? 16384 : 0);    // U^T [dv rows][j]
-    static constexpr uint32_t OFF_AS = OFF_US + (GDN ? 16384 : 0);    // fp32 [64][68]
-    static constexpr uint32_t OFF_RS = OFF_AS + (GDN ? C * kAStride * 4 : 0);  // fp32 [16][48]
+    // output tile [64 t][DV] (norm: own buffer; gla: the current stage's gate
+    // tile, free once the gates are consumed; gdn: the W^T buffer)
+    static constexpr uint32_t OFF_OT = OFF_KH + KH_BYTES;
+    static constexpr uint32_t OT_BYTES = (VAR == kNorm) ? VA * 8192 : 0;
+    static constexpr uint32_t OFF_TB1 = OFF_OT + OT_BYTES;                 // gdn: T diag(beta)     [t][j]
+    static constexpr uint32_t OFF_TB2 = OFF_TB1 + (GDN ? 8192 : 0);        // gdn: T diag(beta gam) [t][j]
+    static constexpr uint32_t OFF_WS = OFF_TB2 + (GDN ? 8192 : 0);         // gdn: W^T [dk rows][t]
+    static constexpr uint32_t OFF_US = OFF_WS + (GDN ? 16384 : 0);         // gdn: U^T [dv rows][j]
+    static constexpr uint32_t OFF_AS = OFF_US + (GDN ? 16384 : 0);         // gdn: fp32 [64][68]
+    static constexpr uint32_t OFF_RS = OFF_AS + (GDN ? C * kAStride * 4 : 0);  // gdn: fp32 [16][48]
     static constexpr uint32_t OFF_MISC = OFF_RS + (GDN ? 16 * 48 * 4 : 0);
-    // misc: 6 arrays of 64 floats + 2 arrays of 128 floats
-    static constexpr uint32_t OFF_BAR = OFF_MISC + 6 * 64 * 4 + 2 * 128 * 4;
+    static constexpr uint32_t MISC_BYTES = (7 * 64 + 3 * 128 + 256) * 4;
+    static constexpr uint32_t OFF_BAR = OFF_MISC + MISC_BYTES;
     static constexpr uint32_t BYTES = OFF_BAR + 64;
     static constexpr uint32_t SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = GDN ? 512 : 256;
@@ -105,7 +115,8 @@ struct Layout {
 __device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sdesc_sw128(addr, 16, 1024); }
 __device__ __forceinline__ uint64_t mnmaj(uint32_t addr, uint32_t lbo) { return sdesc_sw128(addr, lbo, 1024); }
 
-__device__ __forceinline__ float elu1(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+// elu(x) + 1 with alpha = 1; exp via ex2 (x <= 0 here, so no overflow).
+__device__ __forceinline__ float elu1(float x) { return x > 0.f ? x + 1.f : ex2(x * 1.4426950408889634f); }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
@@ -114,6 +125,16 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
     return v;
+}
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, float x) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(x);
+    const unsigned short u = *reinterpret_cast<const unsigned short*>(&b);
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(u) : "memory");
+}
+__device__ __forceinline__ float ld_shared_bf16(uint32_t addr) {
+    unsigned short h;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(addr) : "memory");
+    return __bfloat162float(__ushort_as_bfloat16(h));
 }
 
 // Store 32 fp32 values as 4 swizzled 16-byte chunks (chunks c0..c0+3) of row r.
@@ -126,31 +147,45 @@ __device__ __forceinline__ void store_row32_bf16(uint32_t tile, uint32_t r, uint
     }
 }
 
+// Scale one 16-byte bf16 chunk in place by f.
+__device__ __forceinline__ void scale_chunk(uint32_t addr, float f) {
+    uint4 u = ld_shared_v4(addr);
+    const float2 x0 = unpack_bf16(u.x), x1 = unpack_bf16(u.y), x2 = unpack_bf16(u.z), x3 = unpack_bf16(u.w);
+    st_shared_v4(addr, pack_bf16(x0.x * f, x0.y * f), pack_bf16(x1.x * f, x1.y * f), pack_bf16(x2.x * f, x2.y * f),
+                 pack_bf16(x3.x * f, x3.y * f));
+}
+
 template <int VAR, int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
-             const Params p) {
+             const __grid_constant__ CUtensorMap tmo, const Params p) {
     using L = Layout<VAR, DK, DV>;
     constexpr int KA = L::KA, VA = L::VA;
+    constexpr int DKH = DK / 2;   // state columns per thread
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (sbase - raw);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = 32 * (warp & 3) + lane;   // tensor-memory lane / state row
+    const int hh = warp >> 2;               // column half
     const int bh = blockIdx.x;
     const int T = p.T, nch = p.nchunks;
     const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
 
-    float* sG = reinterpret_cast<float*>(sm + L::OFF_MISC);  // gdn: cumulative log-gate
-    float* sB = sG + 64;       // gdn: beta (0 on padded tokens)
+    float* sG2 = reinterpret_cast<float*>(sm + L::OFF_MISC);  // gdn: cumulative log2-gate
+    float* sB = sG2 + 64;      // gdn: beta (0 on padded tokens)
     float* sGam = sB + 64;     // gdn: exp(G_t)
     float* sBG = sGam + 64;    // gdn: beta_t exp(G_t)
     float* sKf = sBG + 64;     // gdn: exp(G_C - G_j)
     float* sDen = sKf + 64;    // norm: denominators of the chunk
-    float* sGC = sDen + 64;    // gla: Gam_C per channel (128)
+    float* sRden = sDen + 64;  // norm: 1 / den
+    float* sGC = sRden + 64;   // gla: Gam_C per channel (128)
     float* sZ = sGC + 128;     // norm: z (128)
+    float* sDz = sZ + 128;     // norm: this chunk's sum of phi(k) (128)
+    float* sPart = sDz + 128;  // gla: partial gate products of the scan (256)
     uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint64_t* bar_mma = bar_full + 2;
     uint64_t* bar_test = bar_full + 3;
@@ -171,25 +206,31 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
+        tma_prefetch_desc(&tmo);
         if (VAR == kGla) tma_prefetch_desc(&tmg);
     }
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
 
-    // ---- initial state: thread r owns row r of X (r = value index) -------------
-    const int r = tid;
+    // ---- initial state: thread (r, hh) owns X[r][hh*DK/2 .. +DK/2) ----------------
     const bool own = r < DV;
     const size_t ssz = static_cast<size_t>(DK) * DV + (VAR == kNorm ? DK : 0);
     const float* sin = p.state_in ? p.state_in + bh * ssz : nullptr;
-    float st[DK];
+    float st[DKH];
 #pragma unroll
-    for (int c = 0; c < DK; ++c) {
+    for (int i = 0; i < DKH; ++i) {
+        const int c = hh * DKH + i;
         float x = 0.f;
         if (own && sin) x = (VAR == kGdn) ? sin[static_cast<size_t>(r) * DK + c] : sin[static_cast<size_t>(c) * DV + r];
-        st[c] = x;
+        st[i] = x;
     }
+    auto publish_state = [&]() {   // bf16 copy of this thread's state columns
 #pragma unroll
-    for (int b = 0; b < DK / 32; ++b)
-        store_row32_bf16(aSS + (b / 2) * 16384, r, (b % 2) * 4, st + 32 * b);
+        for (int b = 0; b < DKH / 32; ++b) {
+            const int cb = hh * DKH + 32 * b;
+            store_row32_bf16(aSS + (cb / 64) * 16384, r, (cb % 64) / 8, st + 32 * b);
+        }
+    };
+    publish_state();
     if (VAR == kNorm && tid < DK) sZ[tid] = sin ? sin[static_cast<size_t>(DK) * DV + tid] : 0.f;
 
     fence_proxy_async_smem();
@@ -197,7 +238,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's lanes
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);  // this warp's lanes
 
     int status_bits = 0;
     bool failed = false;
@@ -224,9 +265,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     if (!failed && tid == 0 && nch > 0) issue_tma(0, 0);
 
     uint32_t mph = 0;
-    // Commit the MMAs thread 0 issued, wait for them, and agree on the outcome.
-    auto mma_round = [&]() -> bool {
-        if (tid == 0) mma_commit(bar_mma);
+    // Wait for the MMAs thread 0 committed, and agree on the outcome.
+    auto mma_wait = [&]() -> bool {
         const bool ok = mbar_wait(bar_mma, mph, kWaitLimitNs);
         mph ^= 1u;
         tc_fence_after();
@@ -241,6 +281,31 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         __syncthreads();
         tc_fence_after();
     };
+    // Output epilogue: O^T columns t in [32 hh, 32 hh + 32) of row r into the
+    // [64 t][DV] tile at `ot` (scaled by 1/den for norm), then one TMA store.
+    auto store_output = [&](uint32_t ot, int t0) {
+        if (own) {
+            float x[32];
+            tmem_ld32(tlane + L::COL_O + 32 * hh, x);
+            tmem_ld_wait();
+            const uint32_t rb = ot + (r / 64) * 8192 + (r % 8) * 2;
+            const uint32_t rc = (r % 64) / 8;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int t = 32 * hh + i;
+                const float o = (VAR == kNorm) ? x[i] * sRden[t] : x[i];
+                st_shared_b16(rb + (t >> 3) * 1024 + (t & 7) * 128 + ((rc ^ (t & 7)) << 4), o);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int a = 0; a < VA; ++a) tma_store_3d(&tmo, sm + (ot - sbase) + a * 8192, a * 64, t0, bh);
+            bulk_commit();
+        }
+    };
 
     constexpr uint32_t ID_128x64_KK = idesc_bf16(128, 64, false, false);
     constexpr uint32_t ID_128x64_MK = idesc_bf16(128, 64, true, false);
@@ -248,6 +313,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     constexpr uint32_t ID_128xDK_KM = idesc_bf16(128, DK, false, true);
     constexpr uint32_t ID_128xDK_MM = idesc_bf16(128, DK, true, true);
     const uint32_t v_lbo = 8192;  // second 64-row atom of V^T (garbage rows when DV = 64)
+    constexpr float kLog2e = 1.4426950408889634f;
 
     int c = 0;
     for (; c < nch && !failed; ++c) {
@@ -258,103 +324,94 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         const uint32_t aV = aQK + L::QK_BYTES;
         uint8_t* stg = sm + s * L::STAGE;
         if (tid == 0 && c + 1 < nch) {
+            if (VAR == kGla) bulk_wait_read_all();  // the output store of chunk c-1 read stage s^1
             fence_proxy_async_smem();
             issue_tma(c + 1, s ^ 1);
         }
         {
             const bool ok = mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitLimitNs);
             if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; break; }
+            tc_fence_after();
         }
 
         if constexpr (VAR == kGdn) {
-            // ---- per-token gate prefix sums ------------------------------------
+            // ---- per-token gate prefix sums (log2 domain) -----------------------
             if (tid < 64) {
                 float g = 1.f, b = 0.f;
                 if (tid < nvalid) {
                     g = p.gate[static_cast<size_t>(bh) * T + t0 + tid];
                     b = p.beta[static_cast<size_t>(bh) * T + t0 + tid];
                 }
-                float lg = __logf(g);
+                float lg = lg2(g);
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, lg, o);
                     if (lane >= o) lg += y;
                 }
-                sG[tid] = lg;
+                sG2[tid] = lg;
                 sB[tid] = b;
             }
-            __syncthreads();
-            if (tid >= 32 && tid < 64) sG[tid] += sG[31];
-            __syncthreads();
-            if (tid < 64) {
-                const float G = sG[tid];
-                const float gam = __expf(G);
-                sGam[tid] = gam;
-                sBG[tid] = sB[tid] * gam;
-                sKf[tid] = __expf(sG[63] - G);
-            }
-            // ---- [K;Q] K^T ----------------------------------------------------
+            // ---- [K;Q] K^T (needs only the tiles) ------------------------------
             if (tid == 0) {
-                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint64_t d = kmaj(aQK + (kk / 4) * 16384 + (kk % 4) * 32);
                     mma_bf16_ss(tmem + L::COL_G, d, d, ID_128x64_KK, kk > 0);
                 }
+                mma_commit(bar_mma);
             }
-            if (!mma_round()) { failed = true; break; }
-            if (warp < 2) {
+            __syncthreads();
+            if (tid >= 32 && tid < 64) sG2[tid] += sG2[31];
+            __syncthreads();
+            if (tid < 64) {
+                const float G = sG2[tid];
+                const float gam = ex2(G);
+                sGam[tid] = gam;
+                sBG[tid] = sB[tid] * gam;
+                sKf[tid] = ex2(sG2[63] - G);
+            }
+            if (!mma_wait()) { failed = true; break; }
+            if ((warp & 3) < 2) {
                 // rows 0-63: A_tj = beta_t exp(G_t - G_j) k_t.k_j for j < t
-                const int t = tid;
-                const float Gt = sG[t], bt = sB[t];
+                const int t = r;
+                const float Gt = sG2[t], bt = sB[t];
+                float x[32];
+                tmem_ld32(tlane + L::COL_G + 32 * hh, x);
+                tmem_ld_wait();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_G + 32 * h, x);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        float4 o;
-                        const int j = 32 * h + 4 * m;
-                        o.x = (j + 0 < t) ? bt * __expf(Gt - sG[j + 0]) * x[4 * m + 0] : 0.f;
-                        o.y = (j + 1 < t) ? bt * __expf(Gt - sG[j + 1]) * x[4 * m + 1] : 0.f;
-                        o.z = (j + 2 < t) ? bt * __expf(Gt - sG[j + 2]) * x[4 * m + 2] : 0.f;
-                        o.w = (j + 3 < t) ? bt * __expf(Gt - sG[j + 3]) * x[4 * m + 3] : 0.f;
-                        *reinterpret_cast<float4*>(As + t * kAStride + j) = o;
-                    }
+                for (int m = 0; m < 8; ++m) {
+                    const int j = 32 * hh + 4 * m;
+                    float4 o;
+                    o.x = (j + 0 < t) ? bt * ex2(Gt - sG2[j + 0]) * x[4 * m + 0] : 0.f;
+                    o.y = (j + 1 < t) ? bt * ex2(Gt - sG2[j + 1]) * x[4 * m + 1] : 0.f;
+                    o.z = (j + 2 < t) ? bt * ex2(Gt - sG2[j + 2]) * x[4 * m + 2] : 0.f;
+                    o.w = (j + 3 < t) ? bt * ex2(Gt - sG2[j + 3]) * x[4 * m + 3] : 0.f;
+                    *reinterpret_cast<float4*>(As + t * kAStride + j) = o;
                 }
             } else {
                 // rows 64-127: P_tj = exp(G_t - G_j) q_t.k_j for j <= t
-                const int t = tid - 64;
-                const float Gt = sG[t];
+                const int t = r - 64;
+                const float Gt = sG2[t];
+                float x[32];
+                tmem_ld32(tlane + L::COL_G + 32 * hh, x);
+                tmem_ld_wait();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_G + 32 * h, x);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int j = 32 * h + i;
-                        x[i] = (j <= t) ? __expf(Gt - sG[j]) * x[i] : 0.f;
-                    }
-                    store_row32_bf16(aPS, t, 4 * h, x);
+                for (int i = 0; i < 32; ++i) {
+                    const int j = 32 * hh + i;
+                    x[i] = (j <= t) ? ex2(Gt - sG2[j]) * x[i] : 0.f;
                 }
+                store_row32_bf16(aPS, t, 4 * hh, x);
             }
-            // Q' = diag(gam) Q in place (block 1); Q is no longer read by the Gram MMA.
+            // Q' = diag(gam) Q in place (block 1); the Gram MMA is done with it.
 #pragma unroll
             for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
                 const int e = tid + kThreads * i;
                 const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-                const uint32_t addr = aQK + a * 16384 + 8192 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
-                uint4 u = ld_shared_v4(addr);
-                const float f = sGam[row];
-                float2 x0 = unpack_bf16(u.x), x1 = unpack_bf16(u.y), x2 = unpack_bf16(u.z), x3 = unpack_bf16(u.w);
-                st_shared_v4(addr, pack_bf16(x0.x * f, x0.y * f), pack_bf16(x1.x * f, x1.y * f),
-                             pack_bf16(x2.x * f, x2.y * f), pack_bf16(x3.x * f, x3.y * f));
+                scale_chunk(aQK + a * 16384 + 8192 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16, sGam[row]);
             }
             __syncthreads();
             // ---- T = (I + A)^{-1}: diagonal 16x16 blocks, one warp each ---------
-            if (lane < 16) {
+            if (warp < 4 && lane < 16) {
                 const int w0 = 16 * warp, l = lane;
                 float x[16];
 #pragma unroll
@@ -369,34 +426,47 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 for (int i = 0; i < 16; ++i) As[(w0 + i) * kAStride + w0 + l] = x[i];
             }
             __syncthreads();
-            // ---- off-diagonal blocks, block row by block row --------------------
-            {
-                const int i = tid & 15, jg = tid >> 4;
-                for (int bi = 1; bi < 4; ++bi) {
-                    const int ncol = 16 * bi;
+            // ---- off-diagonal blocks, block row by block row: T_ij = -T_ii sum_k A_ik T_kj
+#pragma unroll
+            for (int bi = 1; bi < 4; ++bi) {
+                const int ncol = 16 * bi;
+#pragma unroll
+                for (int m = 0; m < bi; ++m) {
+                    const int o = tid + kThreads * m;
+                    const int i = o / ncol, j = o % ncol;
                     const float* arow = As + (16 * bi + i) * kAStride;
-                    for (int m = 0; m < 2 * bi; ++m) {
-                        const int j = jg + 8 * m;
-                        float acc = 0.f;
-                        for (int k = j; k < ncol; ++k) acc += arow[k] * As[k * kAStride + j];
-                        Rs[i * 48 + j] = acc;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int k = 0; k < ncol; k += 4) {
+                        const float4 av = *reinterpret_cast<const float4*>(arow + k);
+                        acc += av.x * As[(k + 0) * kAStride + j] + av.y * As[(k + 1) * kAStride + j] +
+                               av.z * As[(k + 2) * kAStride + j] + av.w * As[(k + 3) * kAStride + j];
                     }
-                    __syncthreads();
-                    for (int m = 0; m < 2 * bi; ++m) {
-                        const int j = jg + 8 * m;
-                        float acc = 0.f;
-                        for (int l = 0; l <= i; ++l) acc += arow[16 * bi + l] * Rs[l * 48 + j];
-                        As[(16 * bi + i) * kAStride + j] = -acc;
-                    }
-                    __syncthreads();
+                    Rs[i * 48 + j] = acc;
                 }
+                __syncthreads();
+#pragma unroll
+                for (int m = 0; m < bi; ++m) {
+                    const int o = tid + kThreads * m;
+                    const int i = o / ncol, j = o % ncol;
+                    const float* trow = As + (16 * bi + i) * kAStride + 16 * bi;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int l = 0; l < 16; l += 4) {
+                        const float4 tv = *reinterpret_cast<const float4*>(trow + l);
+                        acc += tv.x * Rs[(l + 0) * 48 + j] + tv.y * Rs[(l + 1) * 48 + j] +
+                               tv.z * Rs[(l + 2) * 48 + j] + tv.w * Rs[(l + 3) * 48 + j];
+                    }
+                    As[(16 * bi + i) * kAStride + j] = -acc;
+                }
+                __syncthreads();
             }
             // ---- T diag(beta) and T diag(beta gam) as bf16 MMA operands ---------
             {
-                const int t = tid >> 1, half = tid & 1;
+                const int t = tid >> 2, q4 = tid & 3;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const int c8 = half * 4 + cc;
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c8 = 2 * q4 + cc;
                     float y1[8], y2[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
@@ -421,29 +491,23 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     mma_bf16_ss(tmem + L::COL_U, mnmaj(aV + kk * 2048, v_lbo), kmaj(aTB1 + kk * 32),
                                 ID_128x64_MK, kk > 0);
                 }
+                mma_commit(bar_mma);
+                bulk_wait_read_all();  // the previous output store read the W^T buffer
             }
-            if (!mma_round()) { failed = true; break; }
+            if (!mma_wait()) { failed = true; break; }
             // W^T rows (d_k index) to shared memory as the MN-major operand [dk][t]
             if (r < DK) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_W + 32 * h, x);
-                    tmem_ld_wait();
-                    store_row32_bf16(aWS, r, 4 * h, x);
-                }
+                float x[32];
+                tmem_ld32(tlane + L::COL_W + 32 * hh, x);
+                tmem_ld_wait();
+                store_row32_bf16(aWS, r, 4 * hh, x);
             }
             // K' = diag(gam_C / gam) K in place (block 0); its MMAs are done.
 #pragma unroll
             for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
                 const int e = tid + kThreads * i;
                 const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-                const uint32_t addr = aQK + a * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
-                uint4 u = ld_shared_v4(addr);
-                const float f = sKf[row];
-                float2 x0 = unpack_bf16(u.x), x1 = unpack_bf16(u.y), x2 = unpack_bf16(u.z), x3 = unpack_bf16(u.w);
-                st_shared_v4(addr, pack_bf16(x0.x * f, x0.y * f), pack_bf16(x1.x * f, x1.y * f),
-                             pack_bf16(x2.x * f, x2.y * f), pack_bf16(x3.x * f, x3.y * f));
+                scale_chunk(aQK + a * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16, sKf[row]);
             }
             publish();
             // ---- U^T = Ut^T - X0 W^T ;  O^T = X0 Q'^T ----------------------------
@@ -455,16 +519,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     mma_bf16_ss(tmem + L::COL_O, kmaj(sa), kmaj(aQK + 8192 + (kk / 4) * 16384 + (kk % 4) * 32),
                                 ID_128x64_KK, kk > 0);
                 }
+                mma_commit(bar_mma);
             }
-            if (!mma_round()) { failed = true; break; }
+            if (!mma_wait()) { failed = true; break; }
             {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_U + 32 * h, x);
-                    tmem_ld_wait();
-                    store_row32_bf16(aUS, r, 4 * h, x);
-                }
+                float x[32];
+                tmem_ld32(tlane + L::COL_U + 32 * hh, x);
+                tmem_ld_wait();
+                store_row32_bf16(aUS, r, 4 * hh, x);
             }
             publish();
             // ---- O^T += U^T P^T ;  dX = U^T K' ------------------------------------
@@ -475,53 +537,58 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     mma_bf16_ss(tmem + L::COL_S, kmaj(aUS + kk * 32), mnmaj(aQK + kk * 2048, 16384),
                                 ID_128xDK_KM, kk > 0);
                 }
+                mma_commit(bar_mma);
             }
-            if (!mma_round()) { failed = true; break; }
+            if (!mma_wait()) { failed = true; break; }
             if (own) {
                 const float gC = sGam[63];
 #pragma unroll
-                for (int b = 0; b < DK / 32; ++b) {
+                for (int b = 0; b < DKH / 32; ++b) {
                     float x[32];
-                    tmem_ld32(tlane + L::COL_S + 32 * b, x);
+                    tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) st[32 * b + i] = gC * st[32 * b + i] + x[i];
-                    store_row32_bf16(aSS + (b / 2) * 16384, r, (b % 2) * 4, st + 32 * b);
                 }
-                __nv_bfloat16* orow = p.out + (static_cast<size_t>(bh) * T + t0) * DV + r;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_O + 32 * h, x);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = 32 * h + i;
-                        if (t < nvalid) orow[static_cast<size_t>(t) * DV] = __float2bfloat16_rn(x[i]);
-                    }
-                }
+                publish_state();
             }
-            publish();
+            store_output(aWS, t0);
         } else {
             // ======================= normalized / gated =========================
             if constexpr (VAR == kGla) {
                 // Running products Gam_t = prod_{i<=t} gamma_i per channel, in place.
+                // 256/DK threads per channel each scan a contiguous part of the chunk.
+                constexpr int NP = kThreads / DK, TP = C / NP;
                 float* gt = reinterpret_cast<float*>(stg + L::QK_BYTES + L::V_BYTES);
-                if (tid < DK) {
-                    float G = 1.f;
-                    for (int t = 0; t < C; ++t) {
-                        const float g = (t < nvalid) ? gt[t * DK + tid] : 1.f;
-                        G *= g;
-                        gt[t * DK + tid] = G;
-                    }
-                    sGC[tid] = G;
+                const int ch = tid % DK, part = tid / DK;
+                float G = 1.f;
+#pragma unroll 4
+                for (int t = part * TP; t < (part + 1) * TP; ++t) {
+                    const float g = (t < nvalid) ? gt[t * DK + ch] : 1.f;
+                    G *= g;
+                    gt[t * DK + ch] = G;
                 }
+                sPart[part * DK + ch] = G;
+                __syncthreads();
+                float pre = 1.f, tot = 1.f;
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const float v = sPart[q * DK + ch];
+                    if (q < part) pre *= v;
+                    tot *= v;
+                }
+                if (part > 0) {
+#pragma unroll 4
+                    for (int t = part * TP; t < (part + 1) * TP; ++t) gt[t * DK + ch] *= pre;
+                }
+                if (part == 0) sGC[ch] = tot;
                 __syncthreads();
             }
+            if (VAR == kNorm && tid < DK) sDz[tid] = 0.f;
             // q~ (block 0), k~ (block 1), k^ (gla: its own tile) in place, 8 channels per chunk.
             {
                 const float* gt = reinterpret_cast<const float*>(stg + L::QK_BYTES + L::V_BYTES);
-#pragma unroll 2
+#pragma unroll
                 for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
                     const int e = tid + kThreads * i;
                     const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
@@ -532,23 +599,28 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     const uint4 uq = ld_shared_v4(qa), uk = ld_shared_v4(ka);
                     float q8[8], k8[8];
                     {
-                        float2 t0v = unpack_bf16(uq.x), t1v = unpack_bf16(uq.y), t2v = unpack_bf16(uq.z), t3v = unpack_bf16(uq.w);
-                        q8[0] = t0v.x; q8[1] = t0v.y; q8[2] = t1v.x; q8[3] = t1v.y;
-                        q8[4] = t2v.x; q8[5] = t2v.y; q8[6] = t3v.x; q8[7] = t3v.y;
-                        float2 u0 = unpack_bf16(uk.x), u1 = unpack_bf16(uk.y), u2 = unpack_bf16(uk.z), u3 = unpack_bf16(uk.w);
-                        k8[0] = u0.x; k8[1] = u0.y; k8[2] = u1.x; k8[3] = u1.y;
-                        k8[4] = u2.x; k8[5] = u2.y; k8[6] = u3.x; k8[7] = u3.y;
+                        const float2 a0 = unpack_bf16(uq.x), a1 = unpack_bf16(uq.y), a2 = unpack_bf16(uq.z), a3 = unpack_bf16(uq.w);
+                        q8[0] = a0.x; q8[1] = a0.y; q8[2] = a1.x; q8[3] = a1.y;
+                        q8[4] = a2.x; q8[5] = a2.y; q8[6] = a3.x; q8[7] = a3.y;
+                        const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z), b3 = unpack_bf16(uk.w);
+                        k8[0] = b0.x; k8[1] = b0.y; k8[2] = b1.x; k8[3] = b1.y;
+                        k8[4] = b2.x; k8[5] = b2.y; k8[6] = b3.x; k8[7] = b3.y;
                     }
                     const bool valid = row < nvalid;
                     float kh[8];
+                    float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+                    if constexpr (VAR == kGla) {
+                        g0 = *reinterpret_cast<const float4*>(gt + row * DK + c0);
+                        g1 = *reinterpret_cast<const float4*>(gt + row * DK + c0 + 4);
+                    }
+                    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
                         float qq = phi_on ? elu1(q8[m]) : q8[m];
                         float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
                         if constexpr (VAR == kGla) {
-                            const float G = gt[row * DK + c0 + m];
-                            const float inv = __frcp_rn(G);
-                            qq *= G;
+                            const float inv = __fdividef(1.f, gg[m]);
+                            qq *= gg[m];
                             kh[m] = kv * sGC[c0 + m] * inv;
                             kv *= inv;
                         }
@@ -565,23 +637,6 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 }
             }
             publish();
-            if constexpr (VAR == kNorm) {
-                // den_t starts as q~_t . z_0 (z_0 = normalizer before this chunk).
-                if (tid < 64) {
-                    float d = 0.f;
-#pragma unroll
-                    for (int a = 0; a < KA; ++a)
-#pragma unroll
-                        for (int pc = 0; pc < 8; ++pc) {
-                            const uint4 u = ld_shared_v4(aQK + a * 16384 + sw128_off(tid, pc));
-                            const int c0 = a * 64 + pc * 8;
-                            float2 x0 = unpack_bf16(u.x), x1 = unpack_bf16(u.y), x2 = unpack_bf16(u.z), x3 = unpack_bf16(u.w);
-                            d += x0.x * sZ[c0 + 0] + x0.y * sZ[c0 + 1] + x1.x * sZ[c0 + 2] + x1.y * sZ[c0 + 3] +
-                                 x2.x * sZ[c0 + 4] + x2.y * sZ[c0 + 5] + x3.x * sZ[c0 + 6] + x3.y * sZ[c0 + 7];
-                        }
-                    sDen[tid] = d;
-                }
-            }
             // ---- P = Q~ K~^T ;  O^T = X0 Q~^T ;  dX = V^T K^ ---------------------
             if (tid == 0) {
 #pragma unroll
@@ -597,79 +652,85 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                                                          : mnmaj(aQK + 8192 + kk * 2048, 16384);
                     mma_bf16_ss(tmem + L::COL_S, mnmaj(aV + kk * 2048, v_lbo), bdesc, ID_128xDK_MM, kk > 0);
                 }
+                mma_commit(bar_mma);
             }
-            if (!mma_round()) { failed = true; break; }
-            if (warp < 2) {
+            if constexpr (VAR == kNorm) {
+                // While the MMAs run: den_t = q~_t . z_0, and this chunk's sum of phi(k).
+                {
+                    const int t = tid >> 2, q4 = tid & 3;
+                    float d = 0.f;
+#pragma unroll
+                    for (int m = 0; m < KA * 2; ++m) {
+                        const int cq = q4 * (KA * 2) + m;       // 8-channel group
+                        const int a = cq / 8, lc = cq % 8;
+                        const uint4 u = ld_shared_v4(aQK + a * 16384 + sw128_off(t, lc));
+                        const float2 x0 = unpack_bf16(u.x), x1 = unpack_bf16(u.y), x2 = unpack_bf16(u.z), x3 = unpack_bf16(u.w);
+                        const float* z = sZ + 8 * cq;
+                        d += x0.x * z[0] + x0.y * z[1] + x1.x * z[2] + x1.y * z[3] + x2.x * z[4] + x2.y * z[5] +
+                             x3.x * z[6] + x3.y * z[7];
+                    }
+                    d += __shfl_xor_sync(0xffffffffu, d, 1);
+                    d += __shfl_xor_sync(0xffffffffu, d, 2);
+                    if (q4 == 0) sDen[t] = d;
+                }
+                {
+                    constexpr int NP = kThreads / DK, RP = C / NP;
+                    const int ch = tid % DK, part = tid / DK;
+                    const uint32_t base = aQK + (ch / 64) * 16384 + 8192 + (ch % 8) * 2;
+                    const int lc = (ch % 64) / 8;
+                    float zs = 0.f;
+#pragma unroll 8
+                    for (int j = part * RP; j < (part + 1) * RP; ++j) zs += ld_shared_bf16(base + sw128_off(j, lc));
+                    atomicAdd(&sDz[ch], zs);
+                }
+            }
+            if (!mma_wait()) { failed = true; break; }
+            if ((warp & 3) < 2) {
                 // masked scores of rows t = 0..63 -> bf16 P; norm adds the row sums to den.
-                const int t = tid;
+                const int t = r;
+                float x[32];
+                tmem_ld32(tlane + L::COL_G + 32 * hh, x);
+                tmem_ld_wait();
                 float rs = 0.f;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_G + 32 * h, x);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        x[i] = (32 * h + i <= t) ? x[i] : 0.f;
-                        rs += x[i];
-                    }
-                    store_row32_bf16(aPS, t, 4 * h, x);
+                for (int i = 0; i < 32; ++i) {
+                    x[i] = (32 * hh + i <= t) ? x[i] : 0.f;
+                    rs += x[i];
                 }
-                if (VAR == kNorm) sDen[t] += rs;
+                store_row32_bf16(aPS, t, 4 * hh, x);
+                if (VAR == kNorm) atomicAdd(&sDen[t], rs);
             }
             if (own) {
 #pragma unroll
-                for (int b = 0; b < DK / 32; ++b) {
+                for (int b = 0; b < DKH / 32; ++b) {
                     float x[32];
-                    tmem_ld32(tlane + L::COL_S + 32 * b, x);
+                    tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float dec = (VAR == kGla) ? sGC[32 * b + i] : 1.f;
+                        const float dec = (VAR == kGla) ? sGC[hh * DKH + 32 * b + i] : 1.f;
                         st[32 * b + i] = dec * st[32 * b + i] + x[i];
                     }
-                    store_row32_bf16(aSS + (b / 2) * 16384, r, (b % 2) * 4, st + 32 * b);
                 }
+                publish_state();
             }
-            if (VAR == kNorm && tid < DK) {
-                // z += sum_j phi(k_j) over this chunk's (valid) keys.
-                const int a = tid / 64, lc = (tid % 64) / 8, e = tid % 8;
-                float zs = 0.f;
-                for (int j = 0; j < C; ++j) {
-                    const uint32_t addr = aQK + a * 16384 + 8192 + sw128_off(j, lc) + 2 * e;
-                    unsigned short hbits;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hbits) : "r"(addr));
-                    zs += __bfloat162float(__ushort_as_bfloat16(hbits));
-                }
-                sZ[tid] += zs;
-            }
+            if (VAR == kNorm && tid < DK) sZ[tid] += sDz[tid];
             publish();
             // ---- O^T += V^T P^T ----------------------------------------------------
             if (tid == 0) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16_ss(tmem + L::COL_O, mnmaj(aV + kk * 2048, v_lbo), kmaj(aPS + kk * 32), ID_128x64_MK, 1);
+                mma_commit(bar_mma);
+                if (VAR == kNorm) bulk_wait_read_all();  // the previous output store read the tile
             }
-            if (!mma_round()) { failed = true; break; }
-            if (own) {
-                __nv_bfloat16* orow = p.out + (static_cast<size_t>(bh) * T + t0) * DV + r;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_O + 32 * h, x);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int t = 32 * h + i;
-                        float o = x[i];
-                        if (VAR == kNorm) o = o / sDen[t];
-                        if (t < nvalid) orow[static_cast<size_t>(t) * DV] = __float2bfloat16_rn(o);
-                    }
-                }
+            if (VAR == kNorm && tid < 64) {
+                sRden[tid] = __fdividef(1.f, sDen[tid]);
+                if (p.den_out && tid < nvalid) p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
             }
-            if (VAR == kNorm && p.den_out && tid < nvalid)
-                p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
-            publish();
+            if (!mma_wait()) { failed = true; break; }
+            const uint32_t ot = (VAR == kGla) ? sbase + s * L::STAGE + L::QK_BYTES + L::V_BYTES : sbase + L::OFF_OT;
+            store_output(ot, t0);
         }
     }
 
@@ -684,13 +745,15 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         float* so = p.state_out + bh * ssz;
         if (own) {
 #pragma unroll
-            for (int cc = 0; cc < DK; ++cc) {
-                if (VAR == kGdn) so[static_cast<size_t>(r) * DK + cc] = st[cc];
-                else so[static_cast<size_t>(cc) * DV + r] = st[cc];
+            for (int i = 0; i < DKH; ++i) {
+                const int cc = hh * DKH + i;
+                if (VAR == kGdn) so[static_cast<size_t>(r) * DK + cc] = st[i];
+                else so[static_cast<size_t>(cc) * DV + r] = st[i];
             }
         }
         if (VAR == kNorm && tid < DK) so[static_cast<size_t>(DK) * DV + tid] = sZ[tid];
     }
+    if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);

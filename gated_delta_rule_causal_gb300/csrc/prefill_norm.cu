@@ -12,7 +12,7 @@ cudaError_t run(const Maps& m, const Params& p, int BH, cudaStream_t s) {
     auto kern = chunk_kernel<kNorm, DK, DV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<BH, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, p);
+    kern<<<BH, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, m.o, p);
     return cudaGetLastError();
 }
 
