@@ -11,8 +11,9 @@
 // Inside the kernel the state is always held as X [d_v rows][d_k cols]:
 // X = S^T for the normalized and gated variants (S is d_k x d_v there) and
 // X = S for the gated delta rule (S is d_v x d_k there). With that
-// orientation every state-side product has M = 128 (value rows, padded
-// when d_v = 64) and N = tokens or d_k. The 256 threads pair up on the 128
+// orientation the state products have M = 128 (value rows, padded when
+// d_v = 64); the output products put the 64 tokens on M (rows 64-127 of
+// those accumulators are unused) so each thread writes whole output rows. The 256 threads pair up on the 128
 // tensor-memory lanes: thread (r, h) owns row r and the h-th half of the
 // columns of whatever it reads (warp w serves lanes 32*(w%4).., h = w/4).
 //
@@ -21,7 +22,7 @@
 //
 //  norm / gla ("Linear attention and Hyena" 11.2-11.3, secondary rescaling):
 //    q~_t = phi(q_t) * Gam_t,  k~_j = phi(k_j) / Gam_j,  k^_j = phi(k_j) * Gam_C / Gam_j
-//    O^T  = X_0 Q~^T + V^T (L o Q~ K~^T)^T
+//    O    = Q~ X_0^T + (L o Q~ K~^T) V
 //    X    = diag-cols(Gam_C) X_0 + V^T K^
 //    norm adds den_t = q~_t . z_0 + sum_{j<=t} q~_t . k~_j, o_t = num_t / den_t.
 //
@@ -31,11 +32,11 @@
 //    A_tj = beta_t (gam_t/gam_j) k_t . k_j for j < t. With T = (I + A)^{-1},
 //    Ut = T diag(beta) V and W = T diag(beta gam) K:
 //      U^T = Ut^T - X_0 W^T
-//      O^T = X_0 (diag(gam) Q)^T + U^T (M o Q K^T)^T,  M_tj = gam_t/gam_j (j <= t)
+//      O   = diag(gam) Q X_0^T + (M o Q K^T) U,  M_tj = gam_t/gam_j (j <= t)
 //      X   = gam_C X_0 + U^T diag(gam_C/gam) K
 //    The triangular inverse T is formed in shared memory in fp32: the four
-//    16x16 diagonal blocks by forward substitution, then the off-diagonal
-//    blocks block row by block row.
+//    16x16 diagonal blocks by forward substitution, then two merge levels
+//    ([[T1, 0], [-T2 A21 T1, T2]] for 16 -> 32 -> 64 rows).
 //
 // Tail chunks (T not a multiple of 64): TMA zero-fills rows past the end.
 // phi(0) = 1, so padded keys are zeroed explicitly; padded gates are 1 and
@@ -95,19 +96,19 @@ struct Layout {
     static constexpr uint32_t OFF_WS = OFF_TB2 + (GDN ? 8192 : 0);         // gdn: W^T [dk rows][t]
     static constexpr uint32_t OFF_US = OFF_WS + (GDN ? 16384 : 0);         // gdn: U^T [dv rows][j]
     static constexpr uint32_t OFF_AS = OFF_US + (GDN ? 16384 : 0);         // gdn: fp32 [64][68]
-    static constexpr uint32_t OFF_RS = OFF_AS + (GDN ? C * kAStride * 4 : 0);  // gdn: fp32 [16][48]
-    static constexpr uint32_t OFF_MISC = OFF_RS + (GDN ? 16 * 48 * 4 : 0);
+    static constexpr uint32_t OFF_RS = OFF_AS + (GDN ? C * kAStride * 4 : 0);  // gdn: fp32 [32][32]
+    static constexpr uint32_t OFF_MISC = OFF_RS + (GDN ? 32 * 32 * 4 : 0);
     static constexpr uint32_t MISC_BYTES = (7 * 64 + 3 * 128 + 256) * 4;
     static constexpr uint32_t OFF_BAR = OFF_MISC + MISC_BYTES;
     static constexpr uint32_t BYTES = OFF_BAR + 64;
     static constexpr uint32_t SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
-    static constexpr uint32_t TMEM_COLS = GDN ? 512 : 256;
     // TMEM column map
     static constexpr uint32_t COL_G = 0;                 // gdn: [K;Q] K^T   | norm/gla: P
     static constexpr uint32_t COL_W = 64;                // gdn: W^T
     static constexpr uint32_t COL_U = GDN ? 128 : 0;     // gdn: U^T
-    static constexpr uint32_t COL_O = GDN ? 192 : 64;    // O^T
-    static constexpr uint32_t COL_S = GDN ? 256 : 128;   // Delta X
+    static constexpr uint32_t COL_O = GDN ? 192 : 64;    // O [t rows][DV]
+    static constexpr uint32_t COL_S = COL_O + DV;        // Delta X [dv rows][DK]
+    static constexpr uint32_t TMEM_COLS = (COL_S + DK <= 256) ? 256 : 512;
     static_assert(STAGE % 1024 == 0, "stage alignment");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
@@ -181,8 +182,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     float* sBG = sGam + 64;    // gdn: beta_t exp(G_t)
     float* sKf = sBG + 64;     // gdn: exp(G_C - G_j)
     float* sDen = sKf + 64;    // norm: denominators of the chunk
-    float* sRden = sDen + 64;  // norm: 1 / den
-    float* sGC = sRden + 64;   // gla: Gam_C per channel (128)
+    float* sGC = sDen + 128;   // gla: Gam_C per channel (128)
     float* sZ = sGC + 128;     // norm: z (128)
     float* sDz = sZ + 128;     // norm: this chunk's sum of phi(k) (128)
     float* sPart = sDz + 128;  // gla: partial gate products of the scan (256)
@@ -281,20 +281,24 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         __syncthreads();
         tc_fence_after();
     };
-    // Output epilogue: O^T columns t in [32 hh, 32 hh + 32) of row r into the
-    // [64 t][DV] tile at `ot` (scaled by 1/den for norm), then one TMA store.
+    // Output epilogue: rows t < 64 of O (thread (t, hh) holds columns
+    // [hh*DV/2, (hh+1)*DV/2)), scaled by 1/den for norm, into the swizzled
+    // [64 t][DV] tile at `ot`, then one TMA store per 64-column atom.
     auto store_output = [&](uint32_t ot, int t0) {
-        if (own) {
-            float x[32];
-            tmem_ld32(tlane + L::COL_O + 32 * hh, x);
-            tmem_ld_wait();
-            const uint32_t rb = ot + (r / 64) * 8192 + (r % 8) * 2;
-            const uint32_t rc = (r % 64) / 8;
+        if ((warp & 3) < 2) {
+            const int t = r;
+            const float sc = (VAR == kNorm) ? __fdividef(1.f, sDen[t]) : 1.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int t = 32 * hh + i;
-                const float o = (VAR == kNorm) ? x[i] * sRden[t] : x[i];
-                st_shared_b16(rb + (t >> 3) * 1024 + (t & 7) * 128 + ((rc ^ (t & 7)) << 4), o);
+            for (int b = 0; b < DV / 64; ++b) {
+                const int cb = hh * (DV / 2) + 32 * b;
+                float x[32];
+                tmem_ld32(tlane + L::COL_O + cb, x);
+                tmem_ld_wait();
+                if (VAR == kNorm) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] *= sc;
+                }
+                store_row32_bf16(ot + (cb / 64) * 8192, t, (cb % 64) / 8, x);
             }
         }
         fence_proxy_async_smem();
@@ -312,8 +316,16 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     constexpr uint32_t ID_128x64_KM_NEG = idesc_bf16(128, 64, false, true, true);
     constexpr uint32_t ID_128xDK_KM = idesc_bf16(128, DK, false, true);
     constexpr uint32_t ID_128xDK_MM = idesc_bf16(128, DK, true, true);
+    constexpr uint32_t ID_128xDV_KK = idesc_bf16(128, DV, false, false);
+    constexpr uint32_t ID_128xDV_KM = idesc_bf16(128, DV, false, true);
     const uint32_t v_lbo = 8192;  // second 64-row atom of V^T (garbage rows when DV = 64)
-    constexpr float kLog2e = 1.4426950408889634f;
+
+    // gdn: gate and beta of the next chunk, loaded one chunk ahead (threads 0-63)
+    float g_nx = 1.f, b_nx = 0.f;
+    if (VAR == kGdn && tid < 64 && tid < T) {
+        g_nx = p.gate[static_cast<size_t>(bh) * T + tid];
+        b_nx = p.beta[static_cast<size_t>(bh) * T + tid];
+    }
 
     int c = 0;
     for (; c < nch && !failed; ++c) {
@@ -337,11 +349,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         if constexpr (VAR == kGdn) {
             // ---- per-token gate prefix sums (log2 domain) -----------------------
             if (tid < 64) {
-                float g = 1.f, b = 0.f;
-                if (tid < nvalid) {
-                    g = p.gate[static_cast<size_t>(bh) * T + t0 + tid];
-                    b = p.beta[static_cast<size_t>(bh) * T + t0 + tid];
-                }
+                const float g = g_nx, b = b_nx;
+                const int tn = t0 + C + tid;
+                g_nx = tn < T ? p.gate[static_cast<size_t>(bh) * T + tn] : 1.f;
+                b_nx = tn < T ? p.beta[static_cast<size_t>(bh) * T + tn] : 0.f;
                 float lg = lg2(g);
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
@@ -426,39 +437,81 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 for (int i = 0; i < 16; ++i) As[(w0 + i) * kAStride + w0 + l] = x[i];
             }
             __syncthreads();
-            // ---- off-diagonal blocks, block row by block row: T_ij = -T_ii sum_k A_ik T_kj
+            // ---- merge level 1: T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (16x16)
+            {
+                const int m = tid >> 7, tl = tid & 127;
+                const int rb = 16 + 32 * m, cb = 32 * m;
+                const int i = tl >> 3, j = 2 * (tl & 7);
+                float* X = Rs + m * 256;
+                const float* arow = As + (rb + i) * kAStride + cb;
+                float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-            for (int bi = 1; bi < 4; ++bi) {
-                const int ncol = 16 * bi;
-#pragma unroll
-                for (int m = 0; m < bi; ++m) {
-                    const int o = tid + kThreads * m;
-                    const int i = o / ncol, j = o % ncol;
-                    const float* arow = As + (16 * bi + i) * kAStride;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int k = 0; k < ncol; k += 4) {
-                        const float4 av = *reinterpret_cast<const float4*>(arow + k);
-                        acc += av.x * As[(k + 0) * kAStride + j] + av.y * As[(k + 1) * kAStride + j] +
-                               av.z * As[(k + 2) * kAStride + j] + av.w * As[(k + 3) * kAStride + j];
-                    }
-                    Rs[i * 48 + j] = acc;
+                for (int k = 0; k < 16; k += 4) {
+                    const float4 av = *reinterpret_cast<const float4*>(arow + k);
+                    const float2 u0 = *reinterpret_cast<const float2*>(As + (cb + k + 0) * kAStride + cb + j);
+                    const float2 u1 = *reinterpret_cast<const float2*>(As + (cb + k + 1) * kAStride + cb + j);
+                    const float2 u2 = *reinterpret_cast<const float2*>(As + (cb + k + 2) * kAStride + cb + j);
+                    const float2 u3 = *reinterpret_cast<const float2*>(As + (cb + k + 3) * kAStride + cb + j);
+                    x0 += av.x * u0.x + av.y * u1.x + av.z * u2.x + av.w * u3.x;
+                    x1 += av.x * u0.y + av.y * u1.y + av.z * u2.y + av.w * u3.y;
                 }
+                *reinterpret_cast<float2*>(X + i * 16 + j) = make_float2(x0, x1);
                 __syncthreads();
+                const float* trow = As + (rb + i) * kAStride + rb;
+                float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-                for (int m = 0; m < bi; ++m) {
-                    const int o = tid + kThreads * m;
-                    const int i = o / ncol, j = o % ncol;
-                    const float* trow = As + (16 * bi + i) * kAStride + 16 * bi;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int l = 0; l < 16; l += 4) {
-                        const float4 tv = *reinterpret_cast<const float4*>(trow + l);
-                        acc += tv.x * Rs[(l + 0) * 48 + j] + tv.y * Rs[(l + 1) * 48 + j] +
-                               tv.z * Rs[(l + 2) * 48 + j] + tv.w * Rs[(l + 3) * 48 + j];
-                    }
-                    As[(16 * bi + i) * kAStride + j] = -acc;
+                for (int l = 0; l < 16; l += 4) {
+                    const float4 tv = *reinterpret_cast<const float4*>(trow + l);
+                    const float2 u0 = *reinterpret_cast<const float2*>(X + (l + 0) * 16 + j);
+                    const float2 u1 = *reinterpret_cast<const float2*>(X + (l + 1) * 16 + j);
+                    const float2 u2 = *reinterpret_cast<const float2*>(X + (l + 2) * 16 + j);
+                    const float2 u3 = *reinterpret_cast<const float2*>(X + (l + 3) * 16 + j);
+                    y0 += tv.x * u0.x + tv.y * u1.x + tv.z * u2.x + tv.w * u3.x;
+                    y1 += tv.x * u0.y + tv.y * u1.y + tv.z * u2.y + tv.w * u3.y;
                 }
+                *reinterpret_cast<float2*>(As + (rb + i) * kAStride + cb + j) = make_float2(-y0, -y1);
+                __syncthreads();
+            }
+            // ---- merge level 2: T[32:64, 0:32] = -T_B (A[32:64, 0:32] T_A), 2x2 tiles
+            {
+                const int i = 2 * (tid >> 4), j = 2 * (tid & 15);
+                const float* a0 = As + (32 + i) * kAStride;
+                const float* a1 = a0 + kAStride;
+                float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+#pragma unroll
+                for (int k = 0; k < 32; k += 4) {
+                    const float4 p0 = *reinterpret_cast<const float4*>(a0 + k);
+                    const float4 p1 = *reinterpret_cast<const float4*>(a1 + k);
+                    const float2 u0 = *reinterpret_cast<const float2*>(As + (k + 0) * kAStride + j);
+                    const float2 u1 = *reinterpret_cast<const float2*>(As + (k + 1) * kAStride + j);
+                    const float2 u2 = *reinterpret_cast<const float2*>(As + (k + 2) * kAStride + j);
+                    const float2 u3 = *reinterpret_cast<const float2*>(As + (k + 3) * kAStride + j);
+                    x00 += p0.x * u0.x + p0.y * u1.x + p0.z * u2.x + p0.w * u3.x;
+                    x01 += p0.x * u0.y + p0.y * u1.y + p0.z * u2.y + p0.w * u3.y;
+                    x10 += p1.x * u0.x + p1.y * u1.x + p1.z * u2.x + p1.w * u3.x;
+                    x11 += p1.x * u0.y + p1.y * u1.y + p1.z * u2.y + p1.w * u3.y;
+                }
+                *reinterpret_cast<float2*>(Rs + i * 32 + j) = make_float2(x00, x01);
+                *reinterpret_cast<float2*>(Rs + (i + 1) * 32 + j) = make_float2(x10, x11);
+                __syncthreads();
+                const float* b0 = As + (32 + i) * kAStride + 32;
+                const float* b1 = b0 + kAStride;
+                float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+#pragma unroll
+                for (int l = 0; l < 32; l += 4) {
+                    const float4 q0 = *reinterpret_cast<const float4*>(b0 + l);
+                    const float4 q1 = *reinterpret_cast<const float4*>(b1 + l);
+                    const float2 u0 = *reinterpret_cast<const float2*>(Rs + (l + 0) * 32 + j);
+                    const float2 u1 = *reinterpret_cast<const float2*>(Rs + (l + 1) * 32 + j);
+                    const float2 u2 = *reinterpret_cast<const float2*>(Rs + (l + 2) * 32 + j);
+                    const float2 u3 = *reinterpret_cast<const float2*>(Rs + (l + 3) * 32 + j);
+                    y00 += q0.x * u0.x + q0.y * u1.x + q0.z * u2.x + q0.w * u3.x;
+                    y01 += q0.x * u0.y + q0.y * u1.y + q0.z * u2.y + q0.w * u3.y;
+                    y10 += q1.x * u0.x + q1.y * u1.x + q1.z * u2.x + q1.w * u3.x;
+                    y11 += q1.x * u0.y + q1.y * u1.y + q1.z * u2.y + q1.w * u3.y;
+                }
+                *reinterpret_cast<float2*>(As + (32 + i) * kAStride + j) = make_float2(-y00, -y01);
+                *reinterpret_cast<float2*>(As + (33 + i) * kAStride + j) = make_float2(-y10, -y11);
                 __syncthreads();
             }
             // ---- T diag(beta) and T diag(beta gam) as bf16 MMA operands ---------
@@ -510,14 +563,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 scale_chunk(aQK + a * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16, sKf[row]);
             }
             publish();
-            // ---- U^T = Ut^T - X0 W^T ;  O^T = X0 Q'^T ----------------------------
+            // ---- U^T = Ut^T - X0 W^T ;  O = Q' X0^T -------------------------------
             if (tid == 0) {
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t sa = aSS + (kk / 4) * 16384 + (kk % 4) * 32;
                     mma_bf16_ss(tmem + L::COL_U, kmaj(sa), mnmaj(aWS + kk * 2048, 8192), ID_128x64_KM_NEG, 1);
-                    mma_bf16_ss(tmem + L::COL_O, kmaj(sa), kmaj(aQK + 8192 + (kk / 4) * 16384 + (kk % 4) * 32),
-                                ID_128x64_KK, kk > 0);
+                    mma_bf16_ss(tmem + L::COL_O, kmaj(aQK + 8192 + (kk / 4) * 16384 + (kk % 4) * 32), kmaj(sa),
+                                ID_128xDV_KK, kk > 0);
                 }
                 mma_commit(bar_mma);
             }
@@ -529,11 +582,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 store_row32_bf16(aUS, r, 4 * hh, x);
             }
             publish();
-            // ---- O^T += U^T P^T ;  dX = U^T K' ------------------------------------
+            // ---- O += P U ;  dX = U^T K' -------------------------------------------
             if (tid == 0) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    mma_bf16_ss(tmem + L::COL_O, kmaj(aUS + kk * 32), kmaj(aPS + kk * 32), ID_128x64_KK, 1);
+                    mma_bf16_ss(tmem + L::COL_O, kmaj(aPS + kk * 32), kmaj(aUS + kk * 32), ID_128xDV_KK, 1);
                     mma_bf16_ss(tmem + L::COL_S, kmaj(aUS + kk * 32), mnmaj(aQK + kk * 2048, 16384),
                                 ID_128xDK_KM, kk > 0);
                 }
@@ -561,12 +614,17 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 constexpr int NP = kThreads / DK, TP = C / NP;
                 float* gt = reinterpret_cast<float*>(stg + L::QK_BYTES + L::V_BYTES);
                 const int ch = tid % DK, part = tid / DK;
+                float gv[TP];
+#pragma unroll
+                for (int i = 0; i < TP; ++i) {
+                    const int t = part * TP + i;
+                    gv[i] = (t < nvalid) ? gt[t * DK + ch] : 1.f;
+                }
                 float G = 1.f;
-#pragma unroll 4
-                for (int t = part * TP; t < (part + 1) * TP; ++t) {
-                    const float g = (t < nvalid) ? gt[t * DK + ch] : 1.f;
-                    G *= g;
-                    gt[t * DK + ch] = G;
+#pragma unroll
+                for (int i = 0; i < TP; ++i) {
+                    G *= gv[i];
+                    gv[i] = G;
                 }
                 sPart[part * DK + ch] = G;
                 __syncthreads();
@@ -577,10 +635,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     if (q < part) pre *= v;
                     tot *= v;
                 }
-                if (part > 0) {
-#pragma unroll 4
-                    for (int t = part * TP; t < (part + 1) * TP; ++t) gt[t * DK + ch] *= pre;
-                }
+#pragma unroll
+                for (int i = 0; i < TP; ++i) gt[(part * TP + i) * DK + ch] = gv[i] * pre;
                 if (part == 0) sGC[ch] = tot;
                 __syncthreads();
             }
@@ -637,14 +693,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 }
             }
             publish();
-            // ---- P = Q~ K~^T ;  O^T = X0 Q~^T ;  dX = V^T K^ ---------------------
+            // ---- P = Q~ K~^T ;  O = Q~ X0^T ;  dX = V^T K^ -----------------------
             if (tid == 0) {
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint32_t qa = aQK + (kk / 4) * 16384 + (kk % 4) * 32;
                     mma_bf16_ss(tmem + L::COL_G, kmaj(qa), kmaj(qa + 8192), ID_128x64_KK, kk > 0);
-                    mma_bf16_ss(tmem + L::COL_O, kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32), kmaj(qa),
-                                ID_128x64_KK, kk > 0);
+                    mma_bf16_ss(tmem + L::COL_O, kmaj(qa), kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
+                                ID_128xDV_KK, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -716,18 +772,16 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             }
             if (VAR == kNorm && tid < DK) sZ[tid] += sDz[tid];
             publish();
-            // ---- O^T += V^T P^T ----------------------------------------------------
+            // ---- O += P V ----------------------------------------------------------
             if (tid == 0) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + L::COL_O, mnmaj(aV + kk * 2048, v_lbo), kmaj(aPS + kk * 32), ID_128x64_MK, 1);
+                    mma_bf16_ss(tmem + L::COL_O, kmaj(aPS + kk * 32), mnmaj(aV + kk * 2048, v_lbo), ID_128xDV_KM, 1);
                 mma_commit(bar_mma);
                 if (VAR == kNorm) bulk_wait_read_all();  // the previous output store read the tile
             }
-            if (VAR == kNorm && tid < 64) {
-                sRden[tid] = __fdividef(1.f, sDen[tid]);
-                if (p.den_out && tid < nvalid) p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
-            }
+            if (VAR == kNorm && p.den_out && tid < nvalid)
+                p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
             if (!mma_wait()) { failed = true; break; }
             const uint32_t ot = (VAR == kGla) ? sbase + s * L::STAGE + L::QK_BYTES + L::V_BYTES : sbase + L::OFF_OT;
             store_output(ot, t0);
