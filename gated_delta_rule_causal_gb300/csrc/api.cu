@@ -16,6 +16,8 @@ struct la_handle {
     la_config cfg;
     int sm_count;
     int* d_status;  // device status word (bounded-wait failures)
+    float* d_ws;    // segment-summary workspace of the chunked prefill
+    size_t ws_bytes;
     PFN_cuTensorMapEncodeTiled_v12000 encode;
     std::string last_error;
 };
@@ -93,6 +95,8 @@ la::FwdArgs make_args(la_handle* h, const void* q, const void* k, const void* v,
     a.flags = h->cfg.flags;
     a.status = h->d_status;
     a.sm_count = h->sm_count;
+    a.workspace = h->d_ws;
+    a.ws_bytes = h->ws_bytes;
     return a;
 }
 
@@ -124,6 +128,8 @@ int la_create(const la_config* cfg, la_handle** out) {
     h->cfg = *cfg;
     h->sm_count = prop.multiProcessorCount;
     h->d_status = nullptr;
+    h->d_ws = nullptr;
+    h->ws_bytes = 0;
     h->encode = nullptr;
     DeviceGuard g(cfg->device);
     if (!g.ok) { delete h; return LA_ERR_CUDA; }
@@ -133,11 +139,22 @@ int la_create(const la_config* cfg, la_handle** out) {
         delete h;
         return LA_ERR_CUDA;
     }
+    // Fixed workspace: one state block (S plus a d_k vector) per SM, enough
+    // for every segment split the chunked prefill chooses (B*H*(segments-1)
+    // stays below the SM count).
+    h->ws_bytes = static_cast<size_t>(h->sm_count) * (static_cast<size_t>(cfg->d_k) * cfg->d_v + cfg->d_k) * sizeof(float);
+    if (cudaMalloc(&h->d_ws, h->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(h->d_status);
+        delete h;
+        return LA_ERR_CUDA;
+    }
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn) {
         cudaGetLastError();
+        cudaFree(h->d_ws);
         cudaFree(h->d_status);
         delete h;
         return LA_ERR_CUDA;
@@ -152,6 +169,7 @@ void la_destroy(la_handle* h) {
     {
         DeviceGuard g(h->cfg.device);
         if (h->d_status) cudaFree(h->d_status);
+        if (h->d_ws) cudaFree(h->d_ws);
     }
     delete h;
 }

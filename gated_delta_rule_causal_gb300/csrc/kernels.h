@@ -28,6 +28,8 @@ struct FwdArgs {
     unsigned flags;  // LA_FLAG_*
     int* status;     // device status word
     int sm_count;
+    float* workspace;  // scratch for segment summaries (may be NULL)
+    size_t ws_bytes;
 };
 
 // Token-by-token recurrence on CUDA cores; any supported head size, fp32 or

@@ -53,6 +53,21 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     p.nchunks = (a.T + chunk::C - 1) / chunk::C;
     p.flags = a.flags;
     p.status = a.status;
+    // Split each sequence into segments when there are too few sequence-heads
+    // to fill the GPU (norm / gla only; one CTA per segment, one CTA per SM).
+    p.nseg = 1;
+    p.seg_len = p.nchunks;
+    p.scratch = a.workspace;
+    if (a.variant != kGdn && a.workspace && a.BH < a.sm_count && p.nchunks >= 4) {
+        int nseg = a.sm_count / a.BH;
+        if (nseg > p.nchunks / 2) nseg = p.nchunks / 2;
+        const size_t blk = (static_cast<size_t>(a.dk) * a.dv + a.dk) * sizeof(float);
+        while (nseg > 1 && static_cast<size_t>(a.BH) * (nseg - 1) * blk > a.ws_bytes) --nseg;
+        if (nseg > 1) {
+            p.seg_len = (p.nchunks + nseg - 1) / nseg;
+            p.nseg = (p.nchunks + p.seg_len - 1) / p.seg_len;
+        }
+    }
     *what = "chunked prefill launch";
     switch (a.variant) {
         case kNorm: return chunk::launch_norm(a.dk, a.dv, m, p, a.BH, s);

@@ -9,10 +9,11 @@ namespace {
 template <int DK, int DV>
 cudaError_t run(const Maps& m, const Params& p, int BH, cudaStream_t s) {
     using L = Layout<kGdn, DK, DV>;
+    cudaError_t e = cudaSuccess;
     auto kern = chunk_kernel<kGdn, DK, DV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<BH, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, m.o, p);
+    kern<<<BH * p.nseg, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, m.o, p);
     return cudaGetLastError();
 }
 

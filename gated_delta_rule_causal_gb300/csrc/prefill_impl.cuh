@@ -70,6 +70,14 @@ struct Params {
     int nchunks;
     unsigned flags;
     int* status;
+    // Segments (norm / gla): the chunks of each sequence are split into nseg
+    // runs of seg_len chunks, each run on its own CTA. scratch holds, for
+    // every (b,h) and every segment but the last, the state that segment
+    // produces from a zero start: X [DV][DK] followed by DK floats (gla: the
+    // segment's per-channel decay; norm: its sum of phi(k)).
+    int nseg;
+    int seg_len;
+    float* scratch;
 };
 
 template <int VAR, int DK, int DV>
@@ -172,8 +180,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = 32 * (warp & 3) + lane;   // tensor-memory lane / state row
     const int hh = warp >> 2;               // column half
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x / p.nseg;
+    const int seg = blockIdx.x % p.nseg;
     const int T = p.T, nch = p.nchunks;
+    const int c_begin = seg * p.seg_len;
+    const int nloc = min(nch, c_begin + p.seg_len) - c_begin;
     const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
 
     float* sG2 = reinterpret_cast<float*>(sm + L::OFF_MISC);  // gdn: cumulative log2-gate
@@ -223,6 +234,25 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         if (own && sin) x = (VAR == kGdn) ? sin[static_cast<size_t>(r) * DK + c] : sin[static_cast<size_t>(c) * DV + r];
         st[i] = x;
     }
+    // Later segments start from the states of the earlier ones: X = D_s' X + X_s'.
+    const size_t sblk = static_cast<size_t>(DV) * DK + DK;
+    const float* sc0 = p.scratch + static_cast<size_t>(bh) * (p.nseg - 1) * sblk;
+    if (VAR != kGdn && own) {
+        for (int s2 = 0; s2 < seg; ++s2) {
+            const float* xs = sc0 + s2 * sblk + static_cast<size_t>(r) * DK + hh * DKH;
+            const float* ds = sc0 + s2 * sblk + static_cast<size_t>(DV) * DK + hh * DKH;
+#pragma unroll
+            for (int i = 0; i < DKH; i += 4) {
+                const float4 x4 = *reinterpret_cast<const float4*>(xs + i);
+                float4 d4 = make_float4(1.f, 1.f, 1.f, 1.f);
+                if (VAR == kGla) d4 = *reinterpret_cast<const float4*>(ds + i);
+                st[i + 0] = d4.x * st[i + 0] + x4.x;
+                st[i + 1] = d4.y * st[i + 1] + x4.y;
+                st[i + 2] = d4.z * st[i + 2] + x4.z;
+                st[i + 3] = d4.w * st[i + 3] + x4.w;
+            }
+        }
+    }
     auto publish_state = [&]() {   // bf16 copy of this thread's state columns
 #pragma unroll
         for (int b = 0; b < DKH / 32; ++b) {
@@ -231,7 +261,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         }
     };
     publish_state();
-    if (VAR == kNorm && tid < DK) sZ[tid] = sin ? sin[static_cast<size_t>(DK) * DV + tid] : 0.f;
+    if (VAR == kNorm && tid < DK) {
+        float z = sin ? sin[static_cast<size_t>(DK) * DV + tid] : 0.f;
+        for (int s2 = 0; s2 < seg; ++s2) z += sc0[s2 * sblk + static_cast<size_t>(DV) * DK + tid];
+        sZ[tid] = z;
+    }
 
     fence_proxy_async_smem();
     tc_fence_before();
@@ -262,7 +296,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         if (VAR == kGla) tma_load_3d(&tmg, bar, stg + L::QK_BYTES + L::V_BYTES, 0, y, bh);
     };
 
-    if (!failed && tid == 0 && nch > 0) issue_tma(0, 0);
+    if (!failed && tid == 0 && nloc > 0) issue_tma(c_begin, 0);
 
     uint32_t mph = 0;
     // Wait for the MMAs thread 0 committed, and agree on the outcome.
@@ -322,26 +356,27 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
 
     // gdn: gate and beta of the next chunk, loaded one chunk ahead (threads 0-63)
     float g_nx = 1.f, b_nx = 0.f;
-    if (VAR == kGdn && tid < 64 && tid < T) {
-        g_nx = p.gate[static_cast<size_t>(bh) * T + tid];
-        b_nx = p.beta[static_cast<size_t>(bh) * T + tid];
+    if (VAR == kGdn && tid < 64 && c_begin * C + tid < T) {
+        g_nx = p.gate[static_cast<size_t>(bh) * T + c_begin * C + tid];
+        b_nx = p.beta[static_cast<size_t>(bh) * T + c_begin * C + tid];
     }
 
-    int c = 0;
-    for (; c < nch && !failed; ++c) {
-        const int s = c & 1;
+    int it = 0;
+    for (; it < nloc && !failed; ++it) {
+        const int c = c_begin + it;
+        const int s = it & 1;
         const int t0 = c * C;
         const int nvalid = min(C, T - t0);
         const uint32_t aQK = sbase + s * L::STAGE;
         const uint32_t aV = aQK + L::QK_BYTES;
         uint8_t* stg = sm + s * L::STAGE;
-        if (tid == 0 && c + 1 < nch) {
+        if (tid == 0 && it + 1 < nloc) {
             if (VAR == kGla) bulk_wait_read_all();  // the output store of chunk c-1 read stage s^1
             fence_proxy_async_smem();
             issue_tma(c + 1, s ^ 1);
         }
         {
-            const bool ok = mbar_wait(&bar_full[s], (c >> 1) & 1, kWaitLimitNs);
+            const bool ok = mbar_wait(&bar_full[s], (it >> 1) & 1, kWaitLimitNs);
             if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; break; }
             tc_fence_after();
         }
@@ -789,13 +824,13 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     }
 
     // ---- on failure, let an in-flight prefetch land before the CTA exits -----
-    if (failed && c + 1 < nch) {
-        const int s2 = (c + 1) & 1;
-        mbar_wait(&bar_full[s2], ((c + 1) >> 1) & 1, 100000000ull);
+    if (failed && it + 1 < nloc) {
+        const int s2 = (it + 1) & 1;
+        mbar_wait(&bar_full[s2], ((it + 1) >> 1) & 1, 100000000ull);
     }
 
     // ---- final state ------------------------------------------------------------
-    if (!failed && p.state_out) {
+    if (!failed && p.state_out && seg == p.nseg - 1) {
         float* so = p.state_out + bh * ssz;
         if (own) {
 #pragma unroll
@@ -808,6 +843,215 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         if (VAR == kNorm && tid < DK) so[static_cast<size_t>(DK) * DV + tid] = sZ[tid];
     }
     if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+    if (status_bits && tid == 0) atomicOr(p.status, status_bits);
+}
+
+
+// ---------------------------------------------------------------------------
+// Segment summaries (normalized and per-channel gated variants).
+//
+// For segment s of sequence-head bh (every segment but the last), compute the
+// state the segment's chunks produce from a zero state,
+//   X_s = sum_c (prod_{c' > c} Gam_C(c')) o (V_c^T K^_c),
+// its per-channel decay D_s = prod_c Gam_C(c) (gla) and its sum of phi(k)
+// (norm), and store them in p.scratch. The chunks are walked last to first so
+// the decay to the segment end folds into K^ (column scaling commutes with
+// V^T K^), and every chunk accumulates into one TMEM accumulator.
+// ---------------------------------------------------------------------------
+template <int VAR, int DK, int DV>
+struct SLayout {
+    static constexpr int KA = DK / 64;
+    static constexpr int VA = DV / 64;
+    static constexpr uint32_t K_BYTES = KA * 8192;
+    static constexpr uint32_t V_BYTES = VA * 8192;
+    static constexpr uint32_t G_BYTES = (VAR == kGla) ? C * DK * 4 : 0;
+    static constexpr uint32_t STAGE = K_BYTES + V_BYTES + G_BYTES;
+    static constexpr uint32_t TX_BYTES = K_BYTES + V_BYTES + G_BYTES;
+    static constexpr uint32_t OFF_KH = 2 * STAGE;                  // k^ [64 j][DK]
+    static constexpr uint32_t OFF_MISC = OFF_KH + KA * 8192;
+    static constexpr uint32_t MISC_BYTES = (128 + 128 + 256 + 128) * 4;   // R, Gam_C, scan parts, z
+    static constexpr uint32_t OFF_BAR = OFF_MISC + MISC_BYTES;
+    static constexpr uint32_t SMEM_ALLOC = OFF_BAR + 64 + 1024;
+    static constexpr uint32_t TMEM_COLS = DK <= 64 ? 64 : 128;
+    static_assert(STAGE % 1024 == 0, "stage alignment");
+};
+
+template <int VAR, int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+               const __grid_constant__ CUtensorMap tmg, const Params p) {
+    using L = SLayout<VAR, DK, DV>;
+    constexpr int KA = L::KA, VA = L::VA, DKH = DK / 2;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (sbase - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = 32 * (warp & 3) + lane, hh = warp >> 2;
+    const int nsum = p.nseg - 1;
+    const int bh = blockIdx.x / nsum, seg = blockIdx.x % nsum;
+    const int T = p.T;
+    const int c_begin = seg * p.seg_len;
+    const int nloc = p.seg_len;   // segments before the last one are full
+    const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
+
+    float* sR = reinterpret_cast<float*>(sm + L::OFF_MISC);   // decay from the chunk end to the segment end
+    float* sGC = sR + 128;
+    float* sPart = sGC + 128;
+    float* sZ = sPart + 256;
+    uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+    uint64_t* bar_mma = bar_full + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_full + 3);
+    const uint32_t aKH = sbase + L::OFF_KH;
+
+    if (tid == 0) {
+        mbar_init(&bar_full[0], 1);
+        mbar_init(&bar_full[1], 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
+    if (tid < DK) {
+        sR[tid] = 1.f;
+        sZ[tid] = 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+
+    auto issue_tma = [&](int cc, int s) {
+        uint8_t* stg = sm + s * L::STAGE;
+        mbar_arrive_expect_tx(&bar_full[s], L::TX_BYTES);
+#pragma unroll
+        for (int a = 0; a < KA; ++a) tma_load_3d(&tmk, &bar_full[s], stg + a * 8192, a * 64, cc * C, bh);
+#pragma unroll
+        for (int a = 0; a < VA; ++a) tma_load_3d(&tmv, &bar_full[s], stg + L::K_BYTES + a * 8192, a * 64, cc * C, bh);
+        if (VAR == kGla) tma_load_3d(&tmg, &bar_full[s], stg + L::K_BYTES + L::V_BYTES, 0, cc * C, bh);
+    };
+    if (tid == 0) issue_tma(c_begin + nloc - 1, 0);
+
+    constexpr uint32_t ID_MM = idesc_bf16(128, DK, true, true);
+    int status_bits = 0;
+    bool failed = false;
+    uint32_t mph = 0;
+    int it = 0;
+    for (; it < nloc; ++it) {
+        const int c = c_begin + nloc - 1 - it;     // last chunk first
+        const int s = it & 1;
+        const int t0 = c * C;
+        const int nvalid = min(C, T - t0);
+        uint8_t* stg = sm + s * L::STAGE;
+        const uint32_t aK = sbase + s * L::STAGE, aV = aK + L::K_BYTES;
+        if (tid == 0 && it + 1 < nloc) {
+            fence_proxy_async_smem();
+            issue_tma(c - 1, s ^ 1);   // stage s^1's MMA finished in the previous iteration
+        }
+        {
+            const bool ok = mbar_wait(&bar_full[s], (it >> 1) & 1, kWaitLimitNs);
+            if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; break; }
+        }
+        float* gt = reinterpret_cast<float*>(stg + L::K_BYTES + L::V_BYTES);
+        if constexpr (VAR == kGla) {
+            constexpr int NP = kThreads / DK, TP = C / NP;
+            const int ch = tid % DK, part = tid / DK;
+            float gv[TP];
+#pragma unroll
+            for (int i = 0; i < TP; ++i) {
+                const int t = part * TP + i;
+                gv[i] = (t < nvalid) ? gt[t * DK + ch] : 1.f;
+            }
+            float G = 1.f;
+#pragma unroll
+            for (int i = 0; i < TP; ++i) {
+                G *= gv[i];
+                gv[i] = G;
+            }
+            sPart[part * DK + ch] = G;
+            __syncthreads();
+            float pre = 1.f, tot = 1.f;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float v = sPart[q * DK + ch];
+                if (q < part) pre *= v;
+                tot *= v;
+            }
+#pragma unroll
+            for (int i = 0; i < TP; ++i) gt[(part * TP + i) * DK + ch] = gv[i] * pre;
+            if (part == 0) sGC[ch] = tot;
+            __syncthreads();
+        }
+        // k^'_j = phi(k_j) * Gam_C / Gam_j * R (gla), phi(k_j) (norm); padded rows 0.
+#pragma unroll
+        for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
+            const int e = tid + kThreads * i;
+            const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
+            const int c0 = a * 64 + (pc ^ (row & 7)) * 8;
+            const uint32_t off = a * 8192 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
+            const uint4 uk = ld_shared_v4(aK + off);
+            const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z), b3 = unpack_bf16(uk.w);
+            float k8[8] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y, b3.x, b3.y};
+            const bool valid = row < nvalid;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
+                if constexpr (VAR == kGla) kv *= sGC[c0 + m] * sR[c0 + m] * __fdividef(1.f, gt[row * DK + c0 + m]);
+                k8[m] = kv;
+            }
+            st_shared_v4(aKH + off, pack_bf16(k8[0], k8[1]), pack_bf16(k8[2], k8[3]), pack_bf16(k8[4], k8[5]),
+                         pack_bf16(k8[6], k8[7]));
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem, mnmaj(aV + kk * 2048, 8192), mnmaj(aKH + kk * 2048, 8192), ID_MM, (it > 0 || kk > 0));
+            mma_commit(bar_mma);
+        }
+        if constexpr (VAR == kNorm) {
+            // sum of phi(k) over this chunk: each thread sums a strip of rows of one channel
+            constexpr int NP = kThreads / DK, RP = C / NP;
+            const int ch = tid % DK, part = tid / DK;
+            const uint32_t base = aKH + (ch / 64) * 8192 + (ch % 8) * 2;
+            const int lc = (ch % 64) / 8;
+            float zs = 0.f;
+#pragma unroll 8
+            for (int j = part * RP; j < (part + 1) * RP; ++j) zs += ld_shared_bf16(base + sw128_off(j, lc));
+            atomicAdd(&sZ[ch], zs);
+        }
+        {
+            const bool ok = mbar_wait(bar_mma, mph, kWaitLimitNs);
+            mph ^= 1u;
+            tc_fence_after();
+            if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        }
+        if (VAR == kGla && tid < DK) sR[tid] *= sGC[tid];
+        __syncthreads();
+    }
+    if (failed && it + 1 < nloc) mbar_wait(&bar_full[(it + 1) & 1], ((it + 1) >> 1) & 1, 100000000ull);
+    if (!failed) {
+        const size_t sblk = static_cast<size_t>(DV) * DK + DK;
+        float* out = p.scratch + (static_cast<size_t>(bh) * nsum + seg) * sblk;
+        if (r < DV) {
+#pragma unroll
+            for (int b = 0; b < DKH / 32; ++b) {
+                float x[32];
+                tmem_ld32(tlane + hh * DKH + 32 * b, x);
+                tmem_ld_wait();
+                float* o = out + static_cast<size_t>(r) * DK + hh * DKH + 32 * b;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+            }
+        }
+        if (tid < DK) out[static_cast<size_t>(DV) * DK + tid] = (VAR == kGla) ? sR[tid] : sZ[tid];
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);

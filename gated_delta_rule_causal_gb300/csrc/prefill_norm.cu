@@ -9,10 +9,20 @@ namespace {
 template <int DK, int DV>
 cudaError_t run(const Maps& m, const Params& p, int BH, cudaStream_t s) {
     using L = Layout<kNorm, DK, DV>;
+    cudaError_t e = cudaSuccess;
+    if (p.nseg > 1) {
+        using SL = SLayout<kNorm, DK, DV>;
+        auto sk = summary_kernel<kNorm, DK, DV>;
+        e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SL::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        sk<<<BH * (p.nseg - 1), kThreads, SL::SMEM_ALLOC, s>>>(m.k, m.v, m.g, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     auto kern = chunk_kernel<kNorm, DK, DV>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<BH, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, m.o, p);
+    kern<<<BH * p.nseg, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, m.o, p);
     return cudaGetLastError();
 }
 

@@ -46,8 +46,11 @@
  * OWNERSHIP. The caller owns every buffer. Pointers to q, k, v, gate, beta,
  * state and out are CUDA device pointers (device memory, or managed memory
  * resident on the device). The library never frees or retains them after a
- * call returns. la_create allocates the handle and one device status word;
- * la_destroy frees both.
+ * call returns. la_create allocates the handle, one device status word and a
+ * fixed workspace of (SM count) x (d_k*d_v + d_k) floats, which the chunked
+ * prefill uses for segment summaries when B*H is too small to fill the GPU;
+ * la_destroy frees all three. Calls that overlap on the GPU through the same
+ * handle (different streams) would share that workspace: serialize them.
  *
  * EXECUTION. Calls are asynchronous on the given CUDA stream (NULL = the
  * legacy default stream) and never synchronize the device, except

@@ -81,6 +81,21 @@ def test_chunked_prefill_from_a_state(variant):
     assert_parity(w, inp, chunk=64, state_in=sin)
 
 
+@pytest.mark.parametrize("variant", ["norm", "gla"])
+@pytest.mark.parametrize("T", [256, 1000, 1023])
+def test_segmented_prefill_parity(variant, T):
+    # B*H = 2 leaves most SMs idle, so the sequence is split into segments
+    # (up to T/128 of them); a non-zero initial state and a ragged tail too.
+    w = base(variant, 128).with_(T=T)
+    inp = W.draw(w, seed=T + 7)
+    rng = np.random.default_rng(T)
+    ss = oracle.state_size(variant, w.dk, w.dv)
+    sin = (rng.standard_normal((w.B, w.H, ss)) * 0.1).astype(np.float32)
+    if variant == "norm":
+        sin[..., w.dk * w.dv:] = np.abs(sin[..., w.dk * w.dv:]) * 50 + 1.0
+    assert_parity(w, inp, chunk=64, state_in=sin)
+
+
 def test_gla_identity_feature_map():
     w = base("gla", 128).with_(T=100)
     inp = W.draw(w, seed=4)
