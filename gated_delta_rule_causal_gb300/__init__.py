@@ -8,7 +8,8 @@ calls raise.
 
 Low level (same names as the C ABI): ``la_create``, ``la_forward``,
 ``la_decode_step``, ``la_status``, ``la_destroy``, ``la_last_error``,
-``la_version``. Convenience: ``Handle`` takes torch tensors.
+``la_version``, ``la_forward_noalloc``. Convenience: ``Handle`` takes torch
+tensors.
 """
 from __future__ import annotations
 
@@ -69,6 +70,8 @@ def lib() -> ctypes.CDLL:
             L.la_last_error.restype = ctypes.c_char_p
             L.la_version.argtypes = []
             L.la_version.restype = i
+            L.la_forward_noalloc.argtypes = [ctypes.POINTER(la_config), vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, vp]
+            L.la_forward_noalloc.restype = i
             _lib = L
     return _lib
 
@@ -92,6 +95,13 @@ def la_forward(h, q, k, v, gate, beta, state_in, out, state_out, den_out, varian
 
 def la_decode_step(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, stream) -> int:
     return lib().la_decode_step(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, stream)
+
+
+def la_forward_noalloc(cfg: la_config, q, k, v, gate, beta, state_in, out, state_out, den_out,
+                       variant, T, stream) -> int:
+    """Prefill without any device allocation by the library (see la.h)."""
+    return lib().la_forward_noalloc(ctypes.byref(cfg), q, k, v, gate, beta, state_in, out, state_out,
+                                    den_out, variant, T, stream)
 
 
 def la_status(h, stream) -> int:

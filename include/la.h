@@ -139,6 +139,37 @@ int la_decode_step(la_handle* h, const void* q, const void* k, const void* v,
                    void* out, float* state_out, float* den_out,
                    int variant, void* cuda_stream);
 
+/*
+ * Prefill without any device allocation by the library (no handle).
+ *
+ * The pages describe no counterpart of this call; it exists for callers that
+ * cannot let a library call cudaMalloc: code running under a host framework
+ * that owns all device memory (an inference server or plugin host with its
+ * own pool), or a latency-critical loop that forbids allocation after
+ * start-up. la_create allocates, so this entry point takes the configuration
+ * directly and computes exactly what la_forward computes with the chunkwise
+ * tensor-core kernel (chunk 64; bf16 io; d_k, d_v in {64, 128}; all three
+ * variants). Arguments, layouts and results are those of la_forward.
+ *
+ * Scratch: a file-scope device array of 16 MiB in the library's own image,
+ * held on every GPU that loads the library until the process exits. It holds
+ * the segment summaries of the normalized and per-channel gated variants and
+ * a status word for expired device waits (not reported by this call). A shape
+ * whose summaries would not fit returns LA_ERR_UNSUPPORTED; on a GB300 every
+ * supported shape fits. Every call shares the array: calls that overlap on
+ * the GPU (different streams, or other host threads) race on it and must be
+ * serialized by the caller.
+ *
+ * Set-up: the first call on a device, with cfg->device current, resolves the
+ * array's device address, clears the status word and loads the tensor-map
+ * encoder; make that first call before any stream capture. cfg->device must
+ * be the current device (LA_ERR_INVALID_ARG otherwise).
+ */
+int la_forward_noalloc(const la_config* cfg, const void* q, const void* k, const void* v,
+                       const float* gate, const float* beta, const float* state_in,
+                       void* out, float* state_out, float* den_out,
+                       int variant, int T, void* cuda_stream);
+
 /* Synchronize cuda_stream, then read and clear the device status word.
  * Returns LA_OK, LA_ERR_TIMEOUT if a kernel recorded an expired wait since
  * the last call, or LA_ERR_CUDA. */

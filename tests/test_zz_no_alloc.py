@@ -1,0 +1,83 @@
+"""la_forward_noalloc: the prefill for callers that cannot let a library
+allocate device memory (a host framework that owns the GPU's memory, or a
+loop that must not allocate after start-up). It must give what la_forward
+gives, call after call, while its scratch lives in a static device array.
+
+Collected last on purpose (file name), so a run that stops at the first
+failure has already run every other test."""
+import numpy as np
+import pytest
+
+import workloads as W
+from _helpers import TOL, from_torch, to_torch
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import gated_delta_rule_causal_gb300 as la  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    la.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _run_both(w, seed):
+    x = W.draw(w, seed)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v = (to_torch(a, dev) for a in (x.q, x.k, x.v))
+    g, b = to_torch(x.gate, dev), to_torch(x.beta, dev)
+    var = la.VARIANTS[w.variant]
+    ss = la.state_size(w.variant, w.dk, w.dv)
+    sin = torch.randn((w.B, w.H, ss), device=dev) * 0.1
+    if w.variant == "norm":
+        sin[..., w.dk * w.dv:] = sin[..., w.dk * w.dv:].abs() * 50 + 1.0
+
+    h = la.Handle(w.B, w.H, w.dk, w.dv)
+    den_ref = torch.empty((w.B, w.H, w.T), device=dev) if w.variant == "norm" else None
+    o_ref, s_ref, _ = h.forward(q, k, v, g, b, sin, variant=w.variant, chunk=64, den_out=den_ref)
+
+    o = torch.empty_like(o_ref)
+    s = torch.empty_like(s_ref)
+    den = torch.empty_like(den_ref) if den_ref is not None else None
+    cfg = la.la_config(w.B, w.H, w.dk, w.dv, la.LA_BF16, 0, dev.index)
+    P = lambda t: None if t is None else t.data_ptr()
+    rc = la.la_forward_noalloc(cfg, P(q), P(k), P(v), P(g), P(b), P(sin), P(o), P(s), P(den), var, w.T,
+                               la._stream_ptr(None))
+    assert rc == la.LA_OK
+    torch.cuda.synchronize()
+    h.close()
+    return (from_torch(o), s.cpu().numpy(), None if den is None else den.cpu().numpy(),
+            from_torch(o_ref), s_ref.cpu().numpy(), None if den_ref is None else den_ref.cpu().numpy())
+
+
+def _rel(x, r):
+    return float(np.max(np.abs(x - r)) / max(np.max(np.abs(r)), 1e-30))
+
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+def test_noalloc_matches_la_forward_twice(variant):
+    # B*H = 2 with 16 chunks: norm and gla split into segments, so their
+    # summaries go through the static scratch; two calls in a row with
+    # different data must both match la_forward.
+    base = {"norm": W.NORM_B4H8_T2048_D64, "gla": W.GLA_B4H16_T4096_D128, "gdn": W.GDN_B2H16_T8192_D128}[variant]
+    w = W.small(base, B=1, H=2, T=1000, dk=128, dv=128)
+    for seed in (1, 2):
+        o, s, den, o_ref, s_ref, den_ref = _run_both(w, seed)
+        assert _rel(o, o_ref) <= TOL["bf16"]
+        assert _rel(s, s_ref) <= TOL["bf16"]
+        if den is not None:
+            assert float(np.max(np.abs(den - den_ref) / den_ref)) <= TOL["bf16"]
+
+
+def test_noalloc_rejects_what_it_cannot_run():
+    dev = torch.cuda.current_device()
+    x = torch.zeros(16, device="cuda")
+    P = x.data_ptr()
+    st = la._stream_ptr(None)
+    fp32 = la.la_config(1, 1, 64, 64, la.LA_FP32, 0, dev)
+    assert la.la_forward_noalloc(fp32, P, P, P, None, None, None, P, None, None, la.LA_NORM_ELU1, 8, st) == la.LA_ERR_UNSUPPORTED
+    bf = la.la_config(1, 1, 64, 64, la.LA_BF16, 0, dev)
+    assert la.la_forward_noalloc(bf, P, P, P, None, None, None, P, None, None, la.LA_GDN, 8, st) == la.LA_ERR_INVALID_ARG
+    assert la.la_forward_noalloc(bf, P + 4, P, P, None, None, None, P, None, None, la.LA_NORM_ELU1, 8, st) == la.LA_ERR_MISALIGNED
