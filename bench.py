@@ -155,14 +155,29 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def traffic_from_profiles(kernel_key: str):
-    """DRAM bytes per launch recorded from an ncu capture of this kernel, if any."""
+def kernel_source_hash() -> str:
+    """sha1 (12 hex) of the CUDA sources and the C header."""
+    import glob
+    import hashlib
+    h = hashlib.sha1()
+    files = sorted(glob.glob(os.path.join(ROOT, "gated_delta_rule_causal_gb300", "csrc", "*")))
+    for f in files + [os.path.join(ROOT, "include", "la.h")]:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def traffic_from_profiles(key: str):
+    """DRAM bytes (read + write) per unit from the committed ncu capture, or
+    None when the kernels changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    return d.get(kernel_key)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get(key)
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -259,6 +274,8 @@ def measure_prefill(w, steps, warmup, torch, la, l2, dist=None):
 
 
 def roofline_prefill(w, kern_ms, pk, key):
+    """Roofline of one forward call (the chunk kernel, plus the segment-summary
+    kernel when the sequence is split), timed with CUDA events around it."""
     byts = prefill_bytes(w)
     gbs = byts / (kern_ms * 1e-3) / 1e9
     t_hbm = byts / (pk["hbm_gbs"] * 1e9)
@@ -267,7 +284,8 @@ def roofline_prefill(w, kern_ms, pk, key):
             "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
             "traffic": traffic_from_profiles(key), "algorithmic_bytes": byts,
             "tflops": round(prefill_flops(w) / (kern_ms * 1e-3) / 1e12, 2),
-            "kernel_ms": round(kern_ms, 4), "peak_source": pk["source"] + " (burst copy bandwidth)"}
+            "kernel_ms": round(kern_ms, 4), "unit_timed": "one la_forward (summary + chunk kernels)",
+            "peak_source": pk["source"] + " (burst copy bandwidth)"}
 
 
 def e2e_prefill(r: PrefillRunner, steps: int, torch):
@@ -377,7 +395,7 @@ def gpu_arm(args):
                    "d_v": w.dv, "chunk": 64, "parallelism": f"replicas x{n}",
                    "l2": f"{r.copies} rotating input copies, {r.copies * prefill_bytes(w) / 1e6:.0f} MB > 2x L2 "
                          f"({l2 / 1e6:.0f} MB)"},
-        "roofline": roofline_prefill(w, kern_ms, pk, f"chunk_kernel/{w.variant}"),
+        "roofline": roofline_prefill(w, kern_ms, pk, f"forward/{w.variant}"),
         "gpu_launches": args.steps * r.launches_per_step,
         "clocks": clocks,
     }
@@ -404,6 +422,7 @@ def gpu_arm(args):
                               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
                                            "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                                            "traffic": traffic_from_profiles("decode_gdn"),
+                                           "peak_source": pk["source"] + " (burst copy bandwidth)",
                                            "algorithmic_bytes": byts},
                               "gpu_launches": steps * dr.launches_per_step})
                 del dr
@@ -412,7 +431,7 @@ def gpu_arm(args):
                 suite.append({"workload": sw.name, "metric": "prefill tokens/s (B*T)",
                               "value": round(sw.tokens * args.steps / (tot * 1e-3), 1), "unit": "tokens/s",
                               "ms_per_step": round(tot / args.steps, 4),
-                              "roofline": roofline_prefill(sw, kms, pk, f"chunk_kernel/{sw.variant}"),
+                              "roofline": roofline_prefill(sw, kms, pk, f"forward/{sw.variant}"),
                               "gpu_launches": args.steps})
                 del pr
             torch.cuda.empty_cache()
