@@ -11,12 +11,13 @@
 
 #include "../../include/la.h"
 #include "kernels.h"
+#include "prefill.h"
 
 struct la_handle {
     la_config cfg;
     int sm_count;
     int* d_status;  // device status word (bounded-wait failures)
-    float* d_ws;    // segment-summary workspace of the chunked prefill
+    float* d_ws;    // workspace of the chunked prefill
     size_t ws_bytes;
     PFN_cuTensorMapEncodeTiled_v12000 encode;
     std::string last_error;
@@ -139,10 +140,17 @@ int la_create(const la_config* cfg, la_handle** out) {
         delete h;
         return LA_ERR_CUDA;
     }
-    // Fixed workspace: one state block (S plus a d_k vector) per SM, enough
-    // for every segment split the chunked prefill chooses (B*H*(segments-1)
-    // stays below the SM count).
+    // Fixed workspace. Normalized / gated: one state block (S plus a d_k
+    // vector) per SM, enough for every segment split the chunked prefill
+    // chooses (B*H*(segments-1) stays below the SM count). Gated delta rule on
+    // the tensor-core path: the states of one group of sequence-heads and two
+    // windows of per-chunk intermediates.
     h->ws_bytes = static_cast<size_t>(h->sm_count) * (static_cast<size_t>(cfg->d_k) * cfg->d_v + cfg->d_k) * sizeof(float);
+    const bool tc_shape = cfg->io == LA_BF16 && (cfg->d_k == 64 || cfg->d_k == 128) && (cfg->d_v == 64 || cfg->d_v == 128);
+    if (tc_shape) {
+        const size_t gdn = la::chunk::gdn_workspace_bytes(cfg->B * cfg->H, cfg->d_k, cfg->d_v, la::chunk::kGdnWindow);
+        if (gdn > h->ws_bytes) h->ws_bytes = gdn;
+    }
     if (cudaMalloc(&h->d_ws, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(h->d_status);

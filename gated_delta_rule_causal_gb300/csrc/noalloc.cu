@@ -11,8 +11,10 @@
 // The scratch is one file-scope array of kScratchBytes per GPU that loads the
 // library; it stays allocated until the process exits. Its first 256 bytes
 // hold the status word the kernels set when a bounded wait expires; the rest
-// holds segment summaries, which the summary kernel fully writes before the
-// chunk kernel reads them, so nothing else needs clearing between calls.
+// holds segment summaries (normalized / gated), which the summary kernel fully
+// writes before the chunk kernel reads them, or the gated delta rule's states
+// and per-chunk slots, each written by one launch before the next reads it,
+// so nothing else needs clearing between calls.
 #include <cstdint>
 #include <mutex>
 
@@ -21,6 +23,7 @@
 
 #include "../../include/la.h"
 #include "kernels.h"
+#include "prefill.h"
 
 namespace {
 
@@ -77,11 +80,13 @@ int setup(int dev, void** addr, int* sms) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Segment count the chunked prefill picks for this shape (mirrors the
-// launcher), and the scratch it then needs.
+// Scratch the chunked prefill needs for this shape: the segment summaries the
+// normalized / gated launcher picks (mirrors it), or the least the gated
+// delta rule's launcher accepts (it sizes its windows to the scratch).
 size_t scratch_needed(int variant, int BH, int T, int dk, int dv, int sms) {
     const int nch = (T + 63) / 64;
-    if (variant == LA_GDN || BH >= sms || nch < 4) return 0;
+    if (variant == LA_GDN) return la::chunk::gdn_workspace_bytes(BH, dk, dv, 1);
+    if (BH >= sms || nch < 4) return 0;
     int nseg = sms / BH;
     if (nseg > nch / 2) nseg = nch / 2;
     if (nseg <= 1) return 0;

@@ -43,9 +43,11 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     } else {
         m.g = m.q;
     }
+    if (a.variant == kGdn) {
+        *what = "chunked prefill launch";
+        return chunk::launch_gdn(a, m, s);
+    }
     chunk::Params p;
-    p.gate = a.gate;
-    p.beta = a.beta;
     p.state_in = a.state_in;
     p.state_out = a.state_out;
     p.den_out = a.den_out;
@@ -54,11 +56,11 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     p.flags = a.flags;
     p.status = a.status;
     // Split each sequence into segments when there are too few sequence-heads
-    // to fill the GPU (norm / gla only; one CTA per segment, one CTA per SM).
+    // to fill the GPU (one CTA per segment, one CTA per SM).
     p.nseg = 1;
     p.seg_len = p.nchunks;
     p.scratch = a.workspace;
-    if (a.variant != kGdn && a.workspace && a.BH < a.sm_count && p.nchunks >= 4) {
+    if (a.workspace && a.BH < a.sm_count && p.nchunks >= 4) {
         int nseg = a.sm_count / a.BH;
         if (nseg > p.nchunks / 2) nseg = p.nchunks / 2;
         const size_t blk = (static_cast<size_t>(a.dk) * a.dv + a.dk) * sizeof(float);
@@ -72,7 +74,6 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     switch (a.variant) {
         case kNorm: return chunk::launch_norm(a.dk, a.dv, m, p, a.BH, s);
         case kGla: return chunk::launch_gla(a.dk, a.dv, m, p, a.BH, s);
-        case kGdn: return chunk::launch_gdn(a.dk, a.dv, m, p, a.BH, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,29 +1,909 @@
-// Instantiations of the chunkwise prefill kernel for one variant.
+// Chunkwise prefill of the gated delta rule on the tcgen05 tensor cores.
+//
+// Recurrence ("Beyond attention" §18.2, with the decay applied to the state
+// before the error is taken): S_t = g_t S_{t-1} (I - beta_t k_t k_t^T) +
+// beta_t v_t k_t^T, o_t = S_t q_t. The state is held as X = S [d_v][d_k].
+//
+// Chunk algebra (C = 64 tokens; G_t = sum of log2 g inside the chunk up to t,
+// gam_t = 2^G_t, gam_C = gam_63). Writing S_t = gam_t S_0 +
+// sum_{j<=t} (gam_t/gam_j) u_j k_j^T gives (I + A) U = diag(beta) V -
+// diag(beta gam) K S_0^T with A_tj = beta_t (gam_t/gam_j) k_t.k_j (j < t).
+// With T = (I + A)^{-1}, Ut = T diag(beta) V and W = T diag(beta gam) K:
+//    U^T = Ut^T - X_0 W^T
+//    O^T = X_0 Q^T diag(gam) + U^T P^T,       P_tj = (gam_t/gam_j) q_t.k_j (j <= t)
+//    X   = gam_C X_0 + U^T diag(gam_C/gam) K
+// Everything but these three lines is independent of the state.
+//
+// Work split. Each launch runs two kinds of CTA:
+//  * prep CTAs, in parallel over (head, chunk) of a window of W chunks:
+//    gate prefix sums, [K;Q] K^T on the tensor cores, A and P, the
+//    triangular inverse T in fp32 (16x16 diagonal blocks by forward
+//    substitution, then two merge levels as warp-level tf32 MMAs), W^T and
+//    Ut^T on the tensor cores. Each chunk's results ("slot": W^T, Ut^T, P as
+//    bf16 MMA operands and the gate factors) go to a workspace ring of two
+//    windows with one bulk copy.
+//  * chain CTAs, one per sequence-head of the group, walking the previous
+//    window: per chunk the MMAs X_0 W^T and X_0 Q^T, then U^T K' and U^T P^T,
+//    and three short conversions (U, the state, the output). One control
+//    warp issues every copy and MMA; eight warps convert. They hand work to
+//    each other through mbarriers, so that no converting thread ever waits
+//    on an issue queue.
+// Window j is prepared in launch j and walked in launch j+1, so the launch
+// boundary orders producer and consumer and no CTA waits on another one. The
+// chain CTAs carry the fp32 state from one launch to the next through the
+// workspace.
+//
+// The output is formed transposed (value rows on the 128 tensor-memory
+// lanes, tokens on 64 columns) so that no product pads 64 tokens to M = 128;
+// the epilogue writes it straight to global memory, two adjacent values per
+// 32-bit store.
+//
+// Tail chunks: TMA zero-fills rows past T; padded tokens have g = 1 and
+// beta = 0, which makes their rows of A, W and Ut zero, so they leave the
+// state untouched; no output row past T is written.
 #include "prefill.h"
 #include "prefill_impl.cuh"
 
 namespace la {
-namespace chunk {
-namespace {
+namespace gdn {
+
+using chunk::C;
+using chunk::kAStride;
+using chunk::kmaj;
+using chunk::ld_shared_v4;
+using chunk::mnmaj;
+using chunk::st_shared_v4;
+using chunk::store_row32_bf16;
+
+constexpr int kConv = 256;              // converting threads (8 warps)
+constexpr int kThreads = kConv + 32;    // + one control warp
+constexpr uint32_t kBarConv = 1;        // named barrier of the converting warps
+
+__host__ __device__ constexpr uint32_t align1024(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+// One chunk's intermediates, byte-identical in the workspace and in shared
+// memory. Tiles are bf16 with the 128-byte swizzle (1024-aligned offsets).
+template <int DK, int DV>
+struct Slot {
+    static constexpr uint32_t W_OFF = 0;                  // W^T [dk][64 t]: MN-major B operand
+    static constexpr uint32_t U_OFF = DK * 128;           // Ut^T [dv][64 t]
+    static constexpr uint32_t P_OFF = U_OFF + DV * 128;   // P [64 t][64 j]: K-major B operand
+    static constexpr uint32_t V_OFF = P_OFF + 8192;       // gam_t [64], gam_C/gam_t [64] (fp32)
+    static constexpr uint32_t BYTES = V_OFF + 512;
+    static_assert(BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
+};
 
 template <int DK, int DV>
-cudaError_t run(const Maps& m, const Params& p, int BH, cudaStream_t s) {
-    using L = Layout<kGdn, DK, DV>;
-    cudaError_t e = cudaSuccess;
-    auto kern = chunk_kernel<kGdn, DK, DV>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    kern<<<BH * p.nseg, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, m.o, p);
-    return cudaGetLastError();
+struct ChainLayout {
+    static constexpr int KA = DK / 64;
+    using S = Slot<DK, DV>;
+    static constexpr uint32_t Q_OFF = 0;                   // q [64 t][DK], KA atoms of 8 KB
+    static constexpr uint32_t K_OFF = KA * 8192;           // k [64 j][DK]
+    static constexpr uint32_t SLOT_OFF = 2 * KA * 8192;
+    static constexpr uint32_t STAGE = align1024(SLOT_OFF + S::BYTES);
+    static constexpr uint32_t TX = 2 * KA * 8192 + S::BYTES;
+    static constexpr uint32_t OFF_SS = 2 * STAGE;               // X_0 bf16 [128 rows][DK]
+    static constexpr uint32_t OFF_US = OFF_SS + KA * 16384;     // U^T bf16 [128 rows][64 j]
+    static constexpr uint32_t OFF_US2 = OFF_US + 16384;         // U^T diag(gam_C/gam)
+    static constexpr uint32_t OFF_VEC = OFF_US2 + 16384;        // gam_t, gam_C/gam_t per stage
+    static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 512;
+    static constexpr uint32_t BYTES = OFF_BAR + 128;
+    // TMEM columns (lanes = value rows)
+    static constexpr uint32_t COL_U = 0;        // X_0 W^T           [dv][64]
+    static constexpr uint32_t COL_O = 64;       // two buffers of [O1 | O2], 128 columns each
+    static constexpr uint32_t COL_S = 320;      // U^T K'            [dv][DK]
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(COL_S + DK <= TMEM_COLS, "tensor memory budget");
+};
+
+template <int DK, int DV>
+struct PrepLayout {
+    static constexpr int KA = DK / 64;
+    static constexpr int VA = DV / 64;
+    using S = Slot<DK, DV>;
+    static constexpr uint32_t QK_BYTES = KA * 16384;    // per k-atom: rows 0-63 k, rows 64-127 q
+    static constexpr uint32_t V_BYTES = VA * 8192;
+    static constexpr uint32_t STAGE = QK_BYTES + V_BYTES;
+    static constexpr uint32_t TX = STAGE;
+    static constexpr uint32_t OFF_TB1 = 2 * STAGE;       // T diag(beta)     bf16 [t][j]
+    static constexpr uint32_t OFF_TB2 = OFF_TB1 + 8192;  // T diag(beta gam) bf16 [t][j]
+    static constexpr uint32_t OUT_STRIDE = align1024(S::BYTES);
+    static constexpr uint32_t OFF_OUT = OFF_TB2 + 8192;  // two slots being assembled / stored
+    static constexpr uint32_t OFF_AS = OFF_OUT + 2 * OUT_STRIDE;        // fp32 [64][kAStride]
+    static constexpr uint32_t OFF_RS = OFF_AS + C * kAStride * 4;       // fp32 [32][kRStride]
+    static constexpr uint32_t OFF_MISC = OFF_RS + 32 * 40 * 4;          // log2 prefix, beta, beta gam
+    static constexpr uint32_t OFF_BAR = OFF_MISC + 3 * 64 * 4;
+    static constexpr uint32_t BYTES = OFF_BAR + 128;
+    static constexpr uint32_t COL_G = 0;     // [K;Q] K^T  [128][64]
+    static constexpr uint32_t COL_W = 64;    // W^T        [dk][64]
+    static constexpr uint32_t COL_UT = 128;  // Ut^T       [dv][64]
+    static constexpr uint32_t TMEM_COLS = 256;
+};
+constexpr int kRStride = 40;   // fp32 row stride of the merge scratch (conflict-free fragment reads)
+
+template <int DK, int DV>
+constexpr uint32_t smem_alloc() {
+    return (ChainLayout<DK, DV>::BYTES > PrepLayout<DK, DV>::BYTES ? ChainLayout<DK, DV>::BYTES
+                                                                   : PrepLayout<DK, DV>::BYTES) + 1024;
 }
 
-}  // namespace
+struct Params {
+    const float* gate;      // [BH, T]
+    const float* beta;      // [BH, T]
+    const float* state_in;  // [BH, DV, DK] or NULL (zeros)
+    float* state_out;       // [BH, DV, DK] or NULL
+    __nv_bfloat16* out;     // [BH, T, DV]
+    float* ws_state;        // [G, DV, DK]: the state between launches
+    uint8_t* ws_slot;       // [2][G][W] slots
+    int T;
+    int h0;                 // first sequence-head of the group
+    int G;                  // sequence-heads in the group
+    int W;                  // chunks per window (slot ring stride)
+    int chain_c0, chain_n, chain_buf, chain_first, chain_last;
+    int prep_c0, prep_n, prep_buf;
+    int n_chain;            // CTAs [0, n_chain) walk the chain, the others prepare
+    unsigned flags;
+    int* status;
+};
 
-cudaError_t launch_gdn(int dk, int dv, const Maps& m, const Params& p, int BH, cudaStream_t s) {
-    if (dk == 64 && dv == 64) return run<64, 64>(m, p, BH, s);
-    if (dk == 64 && dv == 128) return run<64, 128>(m, p, BH, s);
-    if (dk == 128 && dv == 64) return run<128, 64>(m, p, BH, s);
-    if (dk == 128 && dv == 128) return run<128, 128>(m, p, BH, s);
+__device__ __forceinline__ void st_global_b32(void* p, uint32_t v) {
+    asm volatile("st.global.b32 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(v) : "memory");
+}
+
+// ============================================================================
+// chain CTA: the state-dependent part of every chunk of one window
+// ============================================================================
+template <int DK, int DV>
+__device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtensorMap* tmk, const Params& p,
+                                           uint8_t* sm, uint32_t sbase) {
+    using L = ChainLayout<DK, DV>;
+    using S = Slot<DK, DV>;
+    constexpr int KA = L::KA, DKH = DK / 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool control = warp == kConv / 32;
+    const int r = 32 * (warp & 3) + lane;   // tensor-memory lane = value row (converting warps)
+    const int hh = (warp >> 2) & 1;         // column half
+    const int g = blockIdx.x;
+    const int bh = p.h0 + g;
+    const int n = p.chain_n;
+    const int T = p.T;
+    const bool own = !control && r < DV;
+
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+    uint64_t* bar_full = bar;        // [2] stage loaded (control expects the bytes)
+    uint64_t* bar_u = bar + 2;       // MMA: X_0 W^T done
+    uint64_t* bar_c = bar + 3;       // MMA: U^T K' done
+    uint64_t* bar_o = bar + 4;       // MMA: U^T P^T done (and everything before it)
+    uint64_t* bar_us = bar + 5;      // converters: U^T written          (8 arrivals)
+    uint64_t* bar_x = bar + 6;       // converters: X_0 written          (8 arrivals)
+    uint64_t* bar_ep = bar + 7;      // converters: output columns read  (8 arrivals)
+    uint64_t* bar_test = bar + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 10);
+    const uint32_t aSS = sbase + L::OFF_SS, aUS = sbase + L::OFF_US, aUS2 = sbase + L::OFF_US2;
+    float* sVec = reinterpret_cast<float*>(sm + L::OFF_VEC);
+
+    if (tid == 0) {
+        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
+        for (int i = 5; i < 8; ++i) mbar_init(&bar[i], kConv / 32);
+        mbar_init(bar_test, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (control && lane == 0) {
+        tma_prefetch_desc(tmq);
+        tma_prefetch_desc(tmk);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+
+    int status_bits = 0;
+    bool failed = false;
+    if (p.flags & 0x100u) {  // test hook: a wait nothing will satisfy, 1 ms limit
+        const bool ok = mbar_wait(bar_test, 0, 1000000ull);
+        if (__syncthreads_or(!ok)) { status_bits |= kStatusTestHook; failed = true; }
+    }
+
+    const size_t ssz = static_cast<size_t>(DK) * DV;
+    constexpr uint32_t ID_U = idesc_bf16(128, 64, false, true);     // X_0 W^T
+    constexpr uint32_t ID_O = idesc_bf16(128, 64, false, false);    // X_0 Q^T, U^T P^T
+    constexpr uint32_t ID_S = idesc_bf16(128, DK, false, true);     // U^T K'
+
+    if (control) {
+        // ======================= control warp (lane 0) =========================
+        if (lane == 0 && !failed && n > 0) {
+            bool pending[2] = {false, false};
+            int load_idx[2] = {0, 0};   // window chunk of the load last issued on each stage
+            auto issue_load = [&](int i, int s) {
+                const int c = p.chain_c0 + i;
+                uint8_t* stg = sm + s * L::STAGE;
+                mbar_arrive_expect_tx(&bar_full[s], L::TX);
+#pragma unroll
+                for (int a = 0; a < KA; ++a) {
+                    tma_load_3d(tmq, &bar_full[s], stg + L::Q_OFF + a * 8192, a * 64, c * C, bh);
+                    tma_load_3d(tmk, &bar_full[s], stg + L::K_OFF + a * 8192, a * 64, c * C, bh);
+                }
+                const uint8_t* src = p.ws_slot + (static_cast<size_t>(p.chain_buf * p.G + g) * p.W + i) * S::BYTES;
+                bulk_load(stg + L::SLOT_OFF, src, S::BYTES, &bar_full[s]);
+                pending[s] = true;
+                load_idx[s] = i;
+            };
+            // Commits issued so far per MMA barrier: the k-th completes phase k.
+            int n_u = 0, n_c = 0, n_o = 0;
+            // X_0 W^T into COL_U (commit) and X_0 Q^T into the chunk's O1 buffer.
+            auto issue_state_mmas = [&](int i) {
+                const int s = i & 1;
+                const uint32_t stg = sbase + s * L::STAGE;
+                const uint32_t aW = stg + L::SLOT_OFF + S::W_OFF;
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint64_t sa = kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32);
+                    mma_bf16_ss(tmem + L::COL_U, sa, mnmaj(aW + kk * 2048, 8192), ID_U, kk > 0);
+                }
+                mma_commit(bar_u);
+                ++n_u;
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    const uint64_t sa = kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32);
+                    mma_bf16_ss(tmem + L::COL_O + 128 * s, sa,
+                                kmaj(stg + L::Q_OFF + (kk / 4) * 8192 + (kk % 4) * 32), ID_O, kk > 0);
+                }
+            };
+            bool fail = false;
+            auto wait = [&](uint64_t* b, uint32_t parity, int bit) {
+                if (fail) return;
+                if (!mbar_wait_or_abort(b, parity, abort_flag)) {
+                    fail = true;
+                    status_bits |= bit;
+                    *abort_flag = 1;
+                }
+            };
+            issue_load(0, 0);
+            if (n > 1) issue_load(1, 1);
+            wait(bar_x, 0, kStatusMmaWait);
+            wait(&bar_full[0], 0, kStatusTmaWait);
+            if (!fail) {
+                pending[0] = false;
+                tc_fence_after();
+                issue_state_mmas(0);
+            }
+            for (int it = 0; it < n && !fail; ++it) {
+                const int s = it & 1;
+                const uint32_t stg = sbase + s * L::STAGE;
+                wait(bar_us, it & 1, kStatusMmaWait);
+                if (it >= 1) wait(bar_ep, (it - 1) & 1, kStatusMmaWait);
+                if (fail) break;
+                tc_fence_after();
+                // dX = U^T K' (commit), O2 = U^T P^T (commit)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + L::COL_S, kmaj(aUS2 + kk * 32), mnmaj(stg + L::K_OFF + kk * 2048, 8192), ID_S,
+                                kk > 0);
+                mma_commit(bar_c);
+                ++n_c;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + L::COL_O + 128 * s + 64, kmaj(aUS + kk * 32),
+                                kmaj(stg + L::SLOT_OFF + S::P_OFF + kk * 32), ID_O, kk > 0);
+                mma_commit(bar_o);
+                ++n_o;
+                if (it + 1 < n) {
+                    wait(&bar_full[s ^ 1], ((it + 1) >> 1) & 1, kStatusTmaWait);
+                    wait(bar_x, (it + 1) & 1, kStatusMmaWait);
+                    if (fail) break;
+                    pending[s ^ 1] = false;
+                    tc_fence_after();
+                    issue_state_mmas(it + 1);
+                }
+                if (it + 2 < n) {
+                    wait(bar_o, it & 1, kStatusMmaWait);   // every reader of stage s is done
+                    if (fail) break;
+                    issue_load(it + 2, s);
+                }
+            }
+            if (fail) {
+                // Let copies and MMAs in flight finish before the CTA exits
+                // (bounded: 100 ms each). MMAs complete in issue order, so the
+                // newest commit of each barrier covers the ones before it.
+                for (int s2 = 0; s2 < 2; ++s2)
+                    if (pending[s2]) mbar_wait(&bar_full[s2], (load_idx[s2] >> 1) & 1, 100000000ull);
+                if (n_u > 0) mbar_wait(bar_u, (n_u - 1) & 1, 100000000ull);
+                if (n_c > 0) mbar_wait(bar_c, (n_c - 1) & 1, 100000000ull);
+                if (n_o > 0) mbar_wait(bar_o, (n_o - 1) & 1, 100000000ull);
+            }
+        }
+    } else {
+        // ======================= converting warps ==============================
+        // initial state: thread (r, hh) owns X[r][hh*DK/2 .. +DK/2)
+        const float* sin = p.chain_first ? (p.state_in ? p.state_in + bh * ssz : nullptr) : p.ws_state + g * ssz;
+        float st[DKH];
+#pragma unroll
+        for (int i = 0; i < DKH; i += 4) {
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (own && sin) x = *reinterpret_cast<const float4*>(sin + static_cast<size_t>(r) * DK + hh * DKH + i);
+            st[i] = x.x;
+            st[i + 1] = x.y;
+            st[i + 2] = x.z;
+            st[i + 3] = x.w;
+        }
+        auto publish_state = [&]() {
+#pragma unroll
+            for (int b = 0; b < DKH / 32; ++b) {
+                const int cb = hh * DKH + 32 * b;
+                store_row32_bf16(aSS + (cb / 64) * 16384, r, (cb % 64) / 8, st + 32 * b);
+            }
+        };
+        // Every row is written once (rows >= d_v as zeros) so that padded MMA
+        // rows never see stale bits.
+        publish_state();
+        {
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+            store_row32_bf16(aUS, r, 4 * hh, z);
+            store_row32_bf16(aUS2, r, 4 * hh, z);
+        }
+        auto signal = [&](uint64_t* b) {   // this warp's writes / TMEM reads are done
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b);
+        };
+        signal(bar_x);
+
+        uint32_t ph_u = 0, ph_c = 0, ph_o = 0;
+        bool bad = failed;
+        int it = 0;
+        for (; it < n; ++it) {
+            const int s = it & 1;
+            const int t0 = (p.chain_c0 + it) * C;
+            const float* vec = reinterpret_cast<const float*>(sm + s * L::STAGE + L::SLOT_OFF + S::V_OFF);
+            float* sv = sVec + 128 * s;
+            // ---- U^T = Ut^T - X_0 W^T; bf16 copies U^T and U^T diag(gam_C/gam) ----
+            bool ok = !bad && mbar_wait_or_abort(&bar_full[s], (it >> 1) & 1, abort_flag) &&
+                      mbar_wait_or_abort(bar_u, ph_u, abort_flag);
+            ph_u ^= 1u;
+            tc_fence_after();
+            if (ok) {
+                if (tid < 128) sv[tid] = vec[tid];
+                if (own) {
+                    const uint32_t aUt = sbase + s * L::STAGE + L::SLOT_OFF + S::U_OFF;
+                    float x[32];
+                    tmem_ld32(tlane + L::COL_U + 32 * hh, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint4 u = ld_shared_v4(aUt + sw128_off(r, 4 * hh + m));
+                        const float2 a0 = unpack_bf16(u.x), a1 = unpack_bf16(u.y), a2 = unpack_bf16(u.z),
+                                     a3 = unpack_bf16(u.w);
+                        float* y = x + 8 * m;
+                        y[0] = a0.x - y[0];
+                        y[1] = a0.y - y[1];
+                        y[2] = a1.x - y[2];
+                        y[3] = a1.y - y[3];
+                        y[4] = a2.x - y[4];
+                        y[5] = a2.y - y[5];
+                        y[6] = a3.x - y[6];
+                        y[7] = a3.y - y[7];
+                    }
+                    store_row32_bf16(aUS, r, 4 * hh, x);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] *= vec[64 + 32 * hh + i];
+                    store_row32_bf16(aUS2, r, 4 * hh, x);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            // agreement point of the converting warps (also publishes sVec)
+            if (named_sync_or(kBarConv, kConv, !ok)) {
+                bad = true;
+                break;
+            }
+            if (lane == 0) mbar_arrive(bar_us);
+            // ---- X = gam_C X_0 + dX, republished as the bf16 operand -------------
+            ok = mbar_wait_or_abort(bar_c, ph_c, abort_flag);
+            ph_c ^= 1u;
+            tc_fence_after();
+            if (ok && own) {
+                const float gC = sv[63];
+#pragma unroll
+                for (int b = 0; b < DKH / 32; ++b) {
+                    float x[32];
+                    tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) st[32 * b + i] = gC * st[32 * b + i] + x[i];
+                }
+                publish_state();
+            }
+            signal(bar_x);
+            bad |= !ok;
+            // ---- output: o_t = gam_t O1[t] + O2[t] -------------------------------
+            ok = mbar_wait_or_abort(bar_o, ph_o, abort_flag);
+            ph_o ^= 1u;
+            tc_fence_after();
+            if (ok && own) {
+                // Lane pairs (r even, r + 1) exchange values so that each
+                // stores two adjacent columns of one token row in one word.
+                const bool odd = lane & 1;
+                const int col = r & ~1;
+                __nv_bfloat16* ob = p.out + (static_cast<size_t>(bh) * T + t0) * DV + col;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int tb = 32 * hh + 16 * q;   // first token of these 16 columns
+                    float o1[16], o2[16];
+                    tmem_ld16(tlane + L::COL_O + 128 * s + tb, o1);
+                    tmem_ld16(tlane + L::COL_O + 128 * s + 64 + tb, o2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o1[i] = sv[tb + i] * o1[i] + o2[i];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const float send = odd ? o1[2 * m] : o1[2 * m + 1];
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+                        const int t = tb + 2 * m + (odd ? 1 : 0);
+                        const uint32_t w = odd ? pack_bf16(recv, o1[2 * m + 1]) : pack_bf16(o1[2 * m], recv);
+                        if (t0 + t < T) st_global_b32(ob + static_cast<size_t>(t) * DV, w);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ep);
+            bad |= !ok;
+        }
+        // ---- state for the next launch, or the final state ----------------------
+        bad = named_sync_or(kBarConv, kConv, bad);
+        if (!bad) {
+            float* dst = p.chain_last ? (p.state_out ? p.state_out + bh * ssz : nullptr) : p.ws_state + g * ssz;
+            if (dst && own) {
+#pragma unroll
+                for (int i = 0; i < DKH; i += 4)
+                    *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * DK + hh * DKH + i) =
+                        make_float4(st[i], st[i + 1], st[i + 2], st[i + 3]);
+            }
+        } else if (tid == 0 && !failed) {
+            status_bits |= kStatusMmaWait;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+    if (status_bits && (tid == 0 || (control && lane == 0))) atomicOr(p.status, status_bits);
+}
+
+// ============================================================================
+// prep CTA: the state-independent part of (head, chunk) units (8 warps)
+// ============================================================================
+__device__ __forceinline__ void sync_conv() { named_sync(kBarConv, kConv); }
+
+// 16x8 tile of A[r0.., k..] * B[k.., n0..] over K = 8*ksteps, A and B fp32
+// row-major in shared memory (strides lda, ldb), accumulated into d.
+template <int KSTEPS>
+__device__ __forceinline__ void tile_mma(float (&d)[4], const float* A, int lda, int r0, int ka0, const float* B,
+                                         int ldb, int kb0, int n0) {
+    const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int ka = ka0 + 8 * ks, kb = kb0 + 8 * ks;
+        uint32_t a[4], b[2];
+        a[0] = to_tf32(A[(r0 + gq) * lda + ka + cq]);
+        a[1] = to_tf32(A[(r0 + gq + 8) * lda + ka + cq]);
+        a[2] = to_tf32(A[(r0 + gq) * lda + ka + cq + 4]);
+        a[3] = to_tf32(A[(r0 + gq + 8) * lda + ka + cq + 4]);
+        b[0] = to_tf32(B[(kb + cq) * ldb + n0 + gq]);
+        b[1] = to_tf32(B[(kb + cq + 4) * ldb + n0 + gq]);
+        mma_tf32_m16n8k8(d, a, b);
+    }
+}
+// Store s * d (a 16x8 tile) to M[r0.., n0..] (fp32 row-major, stride ld).
+__device__ __forceinline__ void tile_store(float* M, int ld, int r0, int n0, const float (&d)[4], float s) {
+    const int lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
+    *reinterpret_cast<float2*>(M + (r0 + gq) * ld + n0 + 2 * cq) = make_float2(s * d[0], s * d[1]);
+    *reinterpret_cast<float2*>(M + (r0 + gq + 8) * ld + n0 + 2 * cq) = make_float2(s * d[2], s * d[3]);
+}
+
+template <int DK, int DV>
+__device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                          const Params& p, uint8_t* sm, uint32_t sbase) {
+    using L = PrepLayout<DK, DV>;
+    using S = Slot<DK, DV>;
+    constexpr int KA = L::KA, VA = L::VA;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = 32 * (warp & 3) + lane;
+    const int hh = warp >> 2;
+    const int pid = blockIdx.x - p.n_chain;
+    const int np = gridDim.x - p.n_chain;
+    const int nunits = p.G * p.prep_n;
+    const int T = p.T;
+
+    float* As = reinterpret_cast<float*>(sm + L::OFF_AS);
+    float* Rs = reinterpret_cast<float*>(sm + L::OFF_RS);
+    float* sG2 = reinterpret_cast<float*>(sm + L::OFF_MISC);   // cumulative log2-gate
+    float* sB = sG2 + 64;                                        // beta (0 on padded tokens)
+    float* sBG = sB + 64;                                        // beta_t gam_t
+    uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+    uint64_t* bar_m = bar_full + 2;
+    uint64_t* bar_test = bar_full + 3;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_full + 4);
+    const uint32_t aTB1 = sbase + L::OFF_TB1, aTB2 = sbase + L::OFF_TB2;
+
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bar_full[i], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(tmq);
+        tma_prefetch_desc(tmk);
+        tma_prefetch_desc(tmv);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tc_fence_before();
+    sync_conv();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+
+    auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
+        const bool ok = mbar_wait(b, parity, kWaitLimitNs);
+        tc_fence_after();
+        return !named_sync_or(kBarConv, kConv, !ok);
+    };
+    auto publish = [&]() {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        sync_conv();
+        tc_fence_after();
+    };
+
+    int status_bits = 0;
+    bool failed = false;
+    if (p.flags & 0x100u) {
+        const bool ok = mbar_wait(bar_test, 0, 1000000ull);
+        if (named_sync_or(kBarConv, kConv, !ok)) { status_bits |= kStatusTestHook; failed = true; }
+    }
+
+    // unit u -> (head g = u % G, chunk prep_c0 + u / G)
+    auto unit_g = [&](int u) { return u % p.G; };
+    auto unit_i = [&](int u) { return u / p.G; };
+    bool pending[2] = {false, false};
+    auto issue_load = [&](int u, int s) {
+        const int bh = p.h0 + unit_g(u);
+        const int y = (p.prep_c0 + unit_i(u)) * C;
+        uint8_t* stg = sm + s * L::STAGE;
+        mbar_arrive_expect_tx(&bar_full[s], L::TX);
+#pragma unroll
+        for (int a = 0; a < KA; ++a) {
+            tma_load_3d(tmk, &bar_full[s], stg + a * 16384, a * 64, y, bh);
+            tma_load_3d(tmq, &bar_full[s], stg + a * 16384 + 8192, a * 64, y, bh);
+        }
+#pragma unroll
+        for (int a = 0; a < VA; ++a) tma_load_3d(tmv, &bar_full[s], stg + L::QK_BYTES + a * 8192, a * 64, y, bh);
+        pending[s] = true;
+    };
+    // gate and beta of a unit, one token per thread (threads 0-63)
+    auto load_gb = [&](int u, float& gv, float& bv) {
+        gv = 1.f;
+        bv = 0.f;
+        if (u < nunits && tid < 64) {
+            const int bh = p.h0 + unit_g(u);
+            const int t = (p.prep_c0 + unit_i(u)) * C + tid;
+            if (t < T) {
+                gv = p.gate[static_cast<size_t>(bh) * T + t];
+                bv = p.beta[static_cast<size_t>(bh) * T + t];
+            }
+        }
+    };
+
+    constexpr uint32_t ID_G = idesc_bf16(128, 64, false, false);   // [K;Q] K^T
+    constexpr uint32_t ID_WU = idesc_bf16(128, 64, true, false);   // K^T TB2^T, V^T TB1^T
+
+    float g_nx, b_nx;
+    load_gb(pid, g_nx, b_nx);
+    if (!failed && tid == 0 && pid < nunits) issue_load(pid, 0);
+    uint32_t mph = 0;
+    int k = 0;
+    for (; !failed; ++k) {
+        const int u = pid + k * np;
+        if (u >= nunits) break;
+        const int s = k & 1;
+        const int un = u + np;
+        const uint32_t stg = sbase + s * L::STAGE;
+        const uint32_t aOut = sbase + L::OFF_OUT + s * L::OUT_STRIDE;
+        float* oGam = reinterpret_cast<float*>(sm + L::OFF_OUT + s * L::OUT_STRIDE + S::V_OFF);   // gam_t
+        float* oKf = oGam + 64;                                                                // gam_C / gam_t
+        if (tid == 0 && un < nunits) {
+            fence_proxy_async_smem();
+            issue_load(un, s ^ 1);   // stage s^1's MMAs finished with the previous unit
+        }
+        if (!wait_all(&bar_full[s], (k >> 1) & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
+        if (tid == 0) pending[s] = false;
+
+        // ---- gate prefix sums (log2 domain) and [K;Q] K^T --------------------------
+        if (tid < 64) {
+            const float gv = g_nx, bv = b_nx;
+            float lg = lg2(gv);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, lg, o);
+                if (lane >= o) lg += y;
+            }
+            sG2[tid] = lg;
+            sB[tid] = bv;
+        }
+        load_gb(un, g_nx, b_nx);
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                const uint64_t d = kmaj(stg + (kk / 4) * 16384 + (kk % 4) * 32);
+                mma_bf16_ss(tmem + L::COL_G, d, d, ID_G, kk > 0);
+            }
+            mma_commit(bar_m);
+            // the slot buffer written below was last stored two units ago
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        }
+        sync_conv();
+        if (tid >= 32 && tid < 64) sG2[tid] += sG2[31];
+        sync_conv();
+        if (tid < 64) {
+            const float G = sG2[tid];
+            const float gam = ex2(G);
+            sBG[tid] = sB[tid] * gam;
+            oGam[tid] = gam;
+            oKf[tid] = ex2(sG2[63] - G);
+        }
+        if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        mph ^= 1u;
+        if ((warp & 3) < 2) {
+            // rows 0-63: A_tj = beta_t 2^(G_t - G_j) k_t.k_j for j < t
+            const int t = r;
+            const float Gt = sG2[t], bt = sB[t];
+            float x[32];
+            tmem_ld32(tlane + L::COL_G + 32 * hh, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int j = 32 * hh + 4 * m;
+                float4 o;
+                o.x = (j + 0 < t) ? bt * ex2(Gt - sG2[j + 0]) * x[4 * m + 0] : 0.f;
+                o.y = (j + 1 < t) ? bt * ex2(Gt - sG2[j + 1]) * x[4 * m + 1] : 0.f;
+                o.z = (j + 2 < t) ? bt * ex2(Gt - sG2[j + 2]) * x[4 * m + 2] : 0.f;
+                o.w = (j + 3 < t) ? bt * ex2(Gt - sG2[j + 3]) * x[4 * m + 3] : 0.f;
+                *reinterpret_cast<float4*>(As + t * kAStride + j) = o;
+            }
+        } else {
+            // rows 64-127: P_tj = 2^(G_t - G_j) q_t.k_j for j <= t
+            const int t = r - 64;
+            const float Gt = sG2[t];
+            float x[32];
+            tmem_ld32(tlane + L::COL_G + 32 * hh, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int j = 32 * hh + i;
+                x[i] = (j <= t) ? ex2(Gt - sG2[j]) * x[i] : 0.f;
+            }
+            store_row32_bf16(aOut + S::P_OFF, t, 4 * hh, x);
+        }
+        sync_conv();
+        // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution ------
+        if (warp < 4 && lane < 16) {
+            const int w0 = 16 * warp, l = lane;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float* arow = As + (w0 + i) * kAStride + w0;
+                float a0 = (i == l) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+                for (int kq = 0; kq + 1 < i; kq += 2) {
+                    a0 -= arow[kq] * x[kq];
+                    a1 -= arow[kq + 1] * x[kq + 1];
+                }
+                if (i & 1) a0 -= arow[i - 1] * x[i - 1];
+                x[i] = a0 + a1;
+            }
+            __syncwarp(0x0000ffffu);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) As[(w0 + i) * kAStride + w0 + l] = x[i];
+        }
+        sync_conv();
+        // ---- merge level 1 (warps 0-3, one 16x8 tile each):
+        //      T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22)
+        {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const int m = warp >> 1, nt = warp & 1;
+            const int rb = 16 + 32 * m, cb = 32 * m;
+            float* X = Rs + warp * 16 * 8;   // 16x8, stride 8
+            if (warp < 4) {
+                tile_mma<2>(d, As, kAStride, rb, cb, As, kAStride, cb, cb + 8 * nt);
+                tile_store(X, 8, 0, 0, d, 1.f);
+            }
+            sync_conv();   // every read of A_10 / A_32 precedes the overwrite below
+            if (warp < 4) {
+                float e[4] = {0.f, 0.f, 0.f, 0.f};
+                tile_mma<2>(e, As, kAStride, rb, rb, X, 8, 0, 0);
+                tile_store(As, kAStride, rb, cb + 8 * nt, e, -1.f);
+            }
+            sync_conv();
+        }
+        // ---- merge level 2 (8 warps, one 16x8 tile each):
+        //      T[32:64, 0:32] = -T_B (A[32:64, 0:32] T_A)
+        {
+            const int mt = warp >> 2, nt = warp & 3;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma<4>(d, As, kAStride, 32 + 16 * mt, 0, As, kAStride, 0, 8 * nt);
+            tile_store(Rs, kRStride, 16 * mt, 8 * nt, d, 1.f);
+            sync_conv();
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma<4>(e, As, kAStride, 32 + 16 * mt, 32, Rs, kRStride, 0, 8 * nt);
+            tile_store(As, kAStride, 32 + 16 * mt, 8 * nt, e, -1.f);
+            sync_conv();
+        }
+        // ---- T diag(beta) and T diag(beta gam) as bf16 MMA operands --------------
+        {
+            const int t = tid >> 2, q4 = tid & 3;
+            const float* trow = As + t * kAStride + 16 * q4;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const float4 t0 = *reinterpret_cast<const float4*>(trow + 8 * cc);
+                const float4 t1 = *reinterpret_cast<const float4*>(trow + 8 * cc + 4);
+                const float4 b0 = *reinterpret_cast<const float4*>(sB + 16 * q4 + 8 * cc);
+                const float4 b1 = *reinterpret_cast<const float4*>(sB + 16 * q4 + 8 * cc + 4);
+                const float4 c0 = *reinterpret_cast<const float4*>(sBG + 16 * q4 + 8 * cc);
+                const float4 c1 = *reinterpret_cast<const float4*>(sBG + 16 * q4 + 8 * cc + 4);
+                const int c8 = 2 * q4 + cc;
+                st_shared_v4(aTB1 + sw128_off(t, c8), pack_bf16(t0.x * b0.x, t0.y * b0.y), pack_bf16(t0.z * b0.z, t0.w * b0.w),
+                             pack_bf16(t1.x * b1.x, t1.y * b1.y), pack_bf16(t1.z * b1.z, t1.w * b1.w));
+                st_shared_v4(aTB2 + sw128_off(t, c8), pack_bf16(t0.x * c0.x, t0.y * c0.y), pack_bf16(t0.z * c0.z, t0.w * c0.w),
+                             pack_bf16(t1.x * c1.x, t1.y * c1.y), pack_bf16(t1.z * c1.z, t1.w * c1.w));
+            }
+        }
+        publish();
+        // ---- W^T = K^T (T diag(beta gam))^T, Ut^T = V^T (T diag(beta))^T --------
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                mma_bf16_ss(tmem + L::COL_W, mnmaj(stg + kk * 2048, 16384), kmaj(aTB2 + kk * 32), ID_WU, kk > 0);
+                mma_bf16_ss(tmem + L::COL_UT, mnmaj(stg + L::QK_BYTES + kk * 2048, 8192), kmaj(aTB1 + kk * 32),
+                            ID_WU, kk > 0);
+            }
+            mma_commit(bar_m);
+        }
+        if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        mph ^= 1u;
+        if (r < DK) {
+            float x[32];
+            tmem_ld32(tlane + L::COL_W + 32 * hh, x);
+            tmem_ld_wait();
+            store_row32_bf16(aOut + S::W_OFF, r, 4 * hh, x);
+        }
+        if (r < DV) {
+            float x[32];
+            tmem_ld32(tlane + L::COL_UT + 32 * hh, x);
+            tmem_ld_wait();
+            store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, x);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        sync_conv();
+        if (tid == 0) {
+            uint8_t* dst = p.ws_slot + (static_cast<size_t>(p.prep_buf * p.G + unit_g(u)) * p.W + unit_i(u)) * S::BYTES;
+            bulk_store(dst, aOut, S::BYTES);
+            bulk_commit();
+        }
+    }
+
+    if (failed && tid == 0) {
+        for (int s2 = 0; s2 < 2; ++s2)
+            if (pending[s2]) mbar_wait(&bar_full[s2], ((s2 == (k & 1) ? k : k + 1) >> 1) & 1, 100000000ull);
+    }
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    sync_conv();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+    if (status_bits && tid == 0) atomicOr(p.status, status_bits);
+}
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads, 1)
+gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+           const __grid_constant__ CUtensorMap tmv, const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (sbase - raw);
+    if (static_cast<int>(blockIdx.x) < p.n_chain) {
+        chain_role<DK, DV>(&tmq, &tmk, p, sm, sbase);
+    } else {
+        if (threadIdx.x >= kConv) return;   // the prep role runs on eight warps
+        prep_role<DK, DV>(&tmq, &tmk, &tmv, p, sm, sbase);
+    }
+}
+
+template <int DK, int DV>
+cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int W, cudaStream_t s) {
+    constexpr uint32_t smem = smem_alloc<DK, DV>();
+    static_assert(smem <= 232448, "shared memory budget");
+    auto kern = gdn_kernel<DK, DV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int nch = (a.T + C - 1) / C;
+    const int NW = (nch + W - 1) / W;
+    const size_t state_bytes = static_cast<size_t>(G) * DK * DV * sizeof(float);
+    Params p;
+    p.gate = a.gate;
+    p.beta = a.beta;
+    p.state_in = a.state_in;
+    p.state_out = a.state_out;
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.ws_state = a.workspace;
+    p.ws_slot = reinterpret_cast<uint8_t*>(a.workspace) + state_bytes;
+    p.T = a.T;
+    p.W = W;
+    p.flags = a.flags;
+    p.status = a.status;
+    for (int h0 = 0; h0 < a.BH; h0 += G) {
+        p.h0 = h0;
+        p.G = a.BH - h0 < G ? a.BH - h0 : G;
+        for (int j = 0; j <= NW; ++j) {
+            p.chain_n = 0;
+            p.prep_n = 0;
+            if (j >= 1) {
+                p.chain_c0 = (j - 1) * W;
+                p.chain_n = nch - p.chain_c0 < W ? nch - p.chain_c0 : W;
+                p.chain_buf = (j - 1) & 1;
+                p.chain_first = (j == 1);
+                p.chain_last = (j == NW);
+            }
+            if (j < NW) {
+                p.prep_c0 = j * W;
+                p.prep_n = nch - p.prep_c0 < W ? nch - p.prep_c0 : W;
+                p.prep_buf = j & 1;
+            }
+            p.n_chain = p.chain_n > 0 ? p.G : 0;
+            int n_prep = 0;
+            if (p.prep_n > 0) {
+                const int units = p.G * p.prep_n;
+                n_prep = a.sm_count - p.n_chain > 0 ? a.sm_count - p.n_chain : a.sm_count;
+                if (n_prep > units) n_prep = units;
+            }
+            kern<<<p.n_chain + n_prep, kThreads, smem, s>>>(m.q, m.k, m.v, p);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
+}  // namespace gdn
+
+namespace chunk {
+
+size_t gdn_slot_bytes(int dk, int dv) { return static_cast<size_t>(dk + dv) * 128 + 8192 + 512; }
+
+int gdn_group(int BH) { return BH < kGdnMaxGroup ? BH : kGdnMaxGroup; }
+
+size_t gdn_workspace_bytes(int BH, int dk, int dv, int W) {
+    const int G = gdn_group(BH);
+    return static_cast<size_t>(G) * dk * dv * sizeof(float) + 2 * static_cast<size_t>(G) * W * gdn_slot_bytes(dk, dv);
+}
+
+cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s) {
+    const int G = gdn_group(a.BH);
+    const size_t state_bytes = static_cast<size_t>(G) * a.dk * a.dv * sizeof(float);
+    const size_t per_w = 2 * static_cast<size_t>(G) * gdn_slot_bytes(a.dk, a.dv);
+    if (!a.workspace || a.ws_bytes < state_bytes + per_w) return cudaErrorInvalidValue;
+    const int nch = (a.T + C - 1) / C;
+    size_t W = (a.ws_bytes - state_bytes) / per_w;
+    if (W > static_cast<size_t>(kGdnWindow)) W = kGdnWindow;
+    if (W > static_cast<size_t>(nch)) W = nch;
+    const int w = static_cast<int>(W);
+    if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64>(m, a, G, w, s);
+    if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128>(m, a, G, w, s);
+    if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64>(m, a, G, w, s);
+    if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128>(m, a, G, w, s);
     return cudaErrorInvalidValue;
 }
 

@@ -1,4 +1,6 @@
-// Chunkwise prefill on the tcgen05 tensor cores (sm_103a).
+// Chunkwise prefill on the tcgen05 tensor cores (sm_103a): normalized and
+// per-channel gated variants (the gated delta rule is in prefill_gdn.cu and
+// shares the helpers below).
 //
 // One CTA per (b,h) sequence-head walks its sequence in chunks of C = 64
 // tokens. TMA stages the q/k/v tiles (and the per-channel gate tile of the
@@ -8,10 +10,8 @@
 // operand in shared memory. Outputs leave through a shared-memory tile and a
 // TMA store.
 //
-// Inside the kernel the state is always held as X [d_v rows][d_k cols]:
-// X = S^T for the normalized and gated variants (S is d_k x d_v there) and
-// X = S for the gated delta rule (S is d_v x d_k there). With that
-// orientation the state products have M = 128 (value rows, padded when
+// Inside the kernel the state is held as X = S^T [d_v rows][d_k cols] (S is
+// d_k x d_v for these variants). With that orientation the state products have M = 128 (value rows, padded when
 // d_v = 64); the output products put the 64 tokens on M (rows 64-127 of
 // those accumulators are unused) so each thread writes whole output rows. The 256 threads pair up on the 128
 // tensor-memory lanes: thread (r, h) owns row r and the h-th half of the
@@ -26,22 +26,10 @@
 //    X    = diag-cols(Gam_C) X_0 + V^T K^
 //    norm adds den_t = q~_t . z_0 + sum_{j<=t} q~_t . k~_j, o_t = num_t / den_t.
 //
-//  gated delta rule (S_t = g_t S_{t-1}(I - beta_t k_t k_t^T) + beta_t v_t k_t^T):
-//    writing S_t = gam_t S_0 + sum_{j<=t} (gam_t/gam_j) u_j k_j^T gives
-//    (I + A) U = diag(beta) V - diag(beta gam) K S_0^T with
-//    A_tj = beta_t (gam_t/gam_j) k_t . k_j for j < t. With T = (I + A)^{-1},
-//    Ut = T diag(beta) V and W = T diag(beta gam) K:
-//      U^T = Ut^T - X_0 W^T
-//      O   = diag(gam) Q X_0^T + (M o Q K^T) U,  M_tj = gam_t/gam_j (j <= t)
-//      X   = gam_C X_0 + U^T diag(gam_C/gam) K
-//    The triangular inverse T is formed in shared memory in fp32: the four
-//    16x16 diagonal blocks by forward substitution, then two merge levels
-//    ([[T1, 0], [-T2 A21 T1, T2]] for 16 -> 32 -> 64 rows).
-//
 // Tail chunks (T not a multiple of 64): TMA zero-fills rows past the end.
-// phi(0) = 1, so padded keys are zeroed explicitly; padded gates are 1 and
-// padded betas 0, which makes padded tokens leave the state untouched; the
-// TMA store clips rows past the end.
+// phi(0) = 1, so padded keys are zeroed explicitly and padded gates read as 1,
+// which makes padded tokens leave the state untouched; the TMA store clips
+// rows past the end.
 //
 // Limit of the per-channel gated variant: the in-chunk rescaling divides by
 // Gam_j, so the product of 64 consecutive gates of one channel must stay
@@ -61,8 +49,6 @@ constexpr int kThreads = 256;  // two threads per tensor-memory lane / state row
 constexpr int kAStride = 68;   // fp32 row stride of the 64x64 solve matrix
 
 struct Params {
-    const float* gate;      // gdn: [BH, T] (gla gates travel by TMA)
-    const float* beta;      // gdn: [BH, T]
     const float* state_in;  // may be NULL
     float* state_out;       // may be NULL
     float* den_out;         // norm, may be NULL
@@ -84,7 +70,6 @@ template <int VAR, int DK, int DV>
 struct Layout {
     static constexpr int KA = DK / 64;  // 64-column atoms along d_k
     static constexpr int VA = DV / 64;
-    static constexpr bool GDN = (VAR == kGdn);
     // q/k tile pair: per k-atom, rows 0-63 hold block 0 and rows 64-127 block 1.
     static constexpr uint32_t QK_BYTES = KA * 16384;
     static constexpr uint32_t V_BYTES = VA * 8192;
@@ -96,25 +81,17 @@ struct Layout {
     static constexpr uint32_t OFF_KH = OFF_PS + 8192;             // gla: k^ [64 j][DK]
     static constexpr uint32_t KH_BYTES = (VAR == kGla) ? KA * 8192 : 0;
     // output tile [64 t][DV] (norm: own buffer; gla: the current stage's gate
-    // tile, free once the gates are consumed; gdn: the W^T buffer)
+    // tile, free once the gates are consumed)
     static constexpr uint32_t OFF_OT = OFF_KH + KH_BYTES;
     static constexpr uint32_t OT_BYTES = (VAR == kNorm) ? VA * 8192 : 0;
-    static constexpr uint32_t OFF_TB1 = OFF_OT + OT_BYTES;                 // gdn: T diag(beta)     [t][j]
-    static constexpr uint32_t OFF_TB2 = OFF_TB1 + (GDN ? 8192 : 0);        // gdn: T diag(beta gam) [t][j]
-    static constexpr uint32_t OFF_WS = OFF_TB2 + (GDN ? 8192 : 0);         // gdn: W^T [dk rows][t]
-    static constexpr uint32_t OFF_US = OFF_WS + (GDN ? 16384 : 0);         // gdn: U^T [dv rows][j]
-    static constexpr uint32_t OFF_AS = OFF_US + (GDN ? 16384 : 0);         // gdn: fp32 [64][68]
-    static constexpr uint32_t OFF_RS = OFF_AS + (GDN ? C * kAStride * 4 : 0);  // gdn: fp32 [32][32]
-    static constexpr uint32_t OFF_MISC = OFF_RS + (GDN ? 32 * 32 * 4 : 0);
-    static constexpr uint32_t MISC_BYTES = (7 * 64 + 3 * 128 + 256) * 4;
+    static constexpr uint32_t OFF_MISC = OFF_OT + OT_BYTES;
+    static constexpr uint32_t MISC_BYTES = (128 + 3 * 128 + 256) * 4;
     static constexpr uint32_t OFF_BAR = OFF_MISC + MISC_BYTES;
     static constexpr uint32_t BYTES = OFF_BAR + 64;
     static constexpr uint32_t SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
     // TMEM column map
-    static constexpr uint32_t COL_G = 0;                 // gdn: [K;Q] K^T   | norm/gla: P
-    static constexpr uint32_t COL_W = 64;                // gdn: W^T
-    static constexpr uint32_t COL_U = GDN ? 128 : 0;     // gdn: U^T
-    static constexpr uint32_t COL_O = GDN ? 192 : 64;    // O [t rows][DV]
+    static constexpr uint32_t COL_G = 0;                 // P = Q~ K~^T [t rows][64 j]
+    static constexpr uint32_t COL_O = 64;                // O [t rows][DV]
     static constexpr uint32_t COL_S = COL_O + DV;        // Delta X [dv rows][DK]
     static constexpr uint32_t TMEM_COLS = (COL_S + DK <= 256) ? 256 : 512;
     static_assert(STAGE % 1024 == 0, "stage alignment");
@@ -169,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
              const __grid_constant__ CUtensorMap tmo, const Params p) {
+    static_assert(VAR == kNorm || VAR == kGla, "the gated delta rule has its own kernel");
     using L = Layout<VAR, DK, DV>;
     constexpr int KA = L::KA, VA = L::VA;
     constexpr int DKH = DK / 2;   // state columns per thread
@@ -187,12 +165,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     const int nloc = min(nch, c_begin + p.seg_len) - c_begin;
     const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
 
-    float* sG2 = reinterpret_cast<float*>(sm + L::OFF_MISC);  // gdn: cumulative log2-gate
-    float* sB = sG2 + 64;      // gdn: beta (0 on padded tokens)
-    float* sGam = sB + 64;     // gdn: exp(G_t)
-    float* sBG = sGam + 64;    // gdn: beta_t exp(G_t)
-    float* sKf = sBG + 64;     // gdn: exp(G_C - G_j)
-    float* sDen = sKf + 64;    // norm: denominators of the chunk
+    float* sDen = reinterpret_cast<float*>(sm + L::OFF_MISC);   // norm: denominators of the chunk
     float* sGC = sDen + 128;   // gla: Gam_C per channel (128)
     float* sZ = sGC + 128;     // norm: z (128)
     float* sDz = sZ + 128;     // norm: this chunk's sum of phi(k) (128)
@@ -203,10 +176,6 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_full + 4);
 
     const uint32_t aSS = sbase + L::OFF_SS, aPS = sbase + L::OFF_PS, aKH = sbase + L::OFF_KH;
-    const uint32_t aTB1 = sbase + L::OFF_TB1, aTB2 = sbase + L::OFF_TB2;
-    const uint32_t aWS = sbase + L::OFF_WS, aUS = sbase + L::OFF_US;
-    float* As = reinterpret_cast<float*>(sm + L::OFF_AS);
-    float* Rs = reinterpret_cast<float*>(sm + L::OFF_RS);
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
@@ -231,13 +200,13 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     for (int i = 0; i < DKH; ++i) {
         const int c = hh * DKH + i;
         float x = 0.f;
-        if (own && sin) x = (VAR == kGdn) ? sin[static_cast<size_t>(r) * DK + c] : sin[static_cast<size_t>(c) * DV + r];
+        if (own && sin) x = sin[static_cast<size_t>(c) * DV + r];
         st[i] = x;
     }
     // Later segments start from the states of the earlier ones: X = D_s' X + X_s'.
     const size_t sblk = static_cast<size_t>(DV) * DK + DK;
     const float* sc0 = p.scratch + static_cast<size_t>(bh) * (p.nseg - 1) * sblk;
-    if (VAR != kGdn && own) {
+    if (own) {
         for (int s2 = 0; s2 < seg; ++s2) {
             const float* xs = sc0 + s2 * sblk + static_cast<size_t>(r) * DK + hh * DKH;
             const float* ds = sc0 + s2 * sblk + static_cast<size_t>(DV) * DK + hh * DKH;
@@ -288,8 +257,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         const int y = cc * C;
 #pragma unroll
         for (int a = 0; a < KA; ++a) {
-            tma_load_3d(&tmq, bar, stg + a * 16384 + (VAR == kGdn ? 8192 : 0), a * 64, y, bh);
-            tma_load_3d(&tmk, bar, stg + a * 16384 + (VAR == kGdn ? 0 : 8192), a * 64, y, bh);
+            tma_load_3d(&tmq, bar, stg + a * 16384, a * 64, y, bh);
+            tma_load_3d(&tmk, bar, stg + a * 16384 + 8192, a * 64, y, bh);
         }
 #pragma unroll
         for (int a = 0; a < VA; ++a) tma_load_3d(&tmv, bar, stg + L::QK_BYTES + a * 8192, a * 64, y, bh);
@@ -346,20 +315,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     };
 
     constexpr uint32_t ID_128x64_KK = idesc_bf16(128, 64, false, false);
-    constexpr uint32_t ID_128x64_MK = idesc_bf16(128, 64, true, false);
-    constexpr uint32_t ID_128x64_KM_NEG = idesc_bf16(128, 64, false, true, true);
-    constexpr uint32_t ID_128xDK_KM = idesc_bf16(128, DK, false, true);
     constexpr uint32_t ID_128xDK_MM = idesc_bf16(128, DK, true, true);
     constexpr uint32_t ID_128xDV_KK = idesc_bf16(128, DV, false, false);
     constexpr uint32_t ID_128xDV_KM = idesc_bf16(128, DV, false, true);
     const uint32_t v_lbo = 8192;  // second 64-row atom of V^T (garbage rows when DV = 64)
-
-    // gdn: gate and beta of the next chunk, loaded one chunk ahead (threads 0-63)
-    float g_nx = 1.f, b_nx = 0.f;
-    if (VAR == kGdn && tid < 64 && c_begin * C + tid < T) {
-        g_nx = p.gate[static_cast<size_t>(bh) * T + c_begin * C + tid];
-        b_nx = p.beta[static_cast<size_t>(bh) * T + c_begin * C + tid];
-    }
 
     int it = 0;
     for (; it < nloc && !failed; ++it) {
@@ -381,446 +340,183 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             tc_fence_after();
         }
 
-        if constexpr (VAR == kGdn) {
-            // ---- per-token gate prefix sums (log2 domain) -----------------------
-            if (tid < 64) {
-                const float g = g_nx, b = b_nx;
-                const int tn = t0 + C + tid;
-                g_nx = tn < T ? p.gate[static_cast<size_t>(bh) * T + tn] : 1.f;
-                b_nx = tn < T ? p.beta[static_cast<size_t>(bh) * T + tn] : 0.f;
-                float lg = lg2(g);
+        if constexpr (VAR == kGla) {
+            // Running products Gam_t = prod_{i<=t} gamma_i per channel, in place.
+            // 256/DK threads per channel each scan a contiguous part of the chunk.
+            constexpr int NP = kThreads / DK, TP = C / NP;
+            float* gt = reinterpret_cast<float*>(stg + L::QK_BYTES + L::V_BYTES);
+            const int ch = tid % DK, part = tid / DK;
+            float gv[TP];
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, lg, o);
-                    if (lane >= o) lg += y;
-                }
-                sG2[tid] = lg;
-                sB[tid] = b;
+            for (int i = 0; i < TP; ++i) {
+                const int t = part * TP + i;
+                gv[i] = (t < nvalid) ? gt[t * DK + ch] : 1.f;
             }
-            // ---- [K;Q] K^T (needs only the tiles) ------------------------------
-            if (tid == 0) {
+            float G = 1.f;
 #pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint64_t d = kmaj(aQK + (kk / 4) * 16384 + (kk % 4) * 32);
-                    mma_bf16_ss(tmem + L::COL_G, d, d, ID_128x64_KK, kk > 0);
+            for (int i = 0; i < TP; ++i) {
+                G *= gv[i];
+                gv[i] = G;
+            }
+            sPart[part * DK + ch] = G;
+            __syncthreads();
+            float pre = 1.f, tot = 1.f;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                const float v = sPart[q * DK + ch];
+                if (q < part) pre *= v;
+                tot *= v;
+            }
+#pragma unroll
+            for (int i = 0; i < TP; ++i) gt[(part * TP + i) * DK + ch] = gv[i] * pre;
+            if (part == 0) sGC[ch] = tot;
+            __syncthreads();
+        }
+        if (VAR == kNorm && tid < DK) sDz[tid] = 0.f;
+        // q~ (block 0), k~ (block 1), k^ (gla: its own tile) in place, 8 channels per chunk.
+        {
+            const float* gt = reinterpret_cast<const float*>(stg + L::QK_BYTES + L::V_BYTES);
+#pragma unroll
+            for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
+                const int e = tid + kThreads * i;
+                const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
+                const int lc = pc ^ (row & 7);
+                const int c0 = a * 64 + lc * 8;
+                const uint32_t off = (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
+                const uint32_t qa = aQK + a * 16384 + off, ka = qa + 8192;
+                const uint4 uq = ld_shared_v4(qa), uk = ld_shared_v4(ka);
+                float q8[8], k8[8];
+                {
+                    const float2 a0 = unpack_bf16(uq.x), a1 = unpack_bf16(uq.y), a2 = unpack_bf16(uq.z), a3 = unpack_bf16(uq.w);
+                    q8[0] = a0.x; q8[1] = a0.y; q8[2] = a1.x; q8[3] = a1.y;
+                    q8[4] = a2.x; q8[5] = a2.y; q8[6] = a3.x; q8[7] = a3.y;
+                    const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z), b3 = unpack_bf16(uk.w);
+                    k8[0] = b0.x; k8[1] = b0.y; k8[2] = b1.x; k8[3] = b1.y;
+                    k8[4] = b2.x; k8[5] = b2.y; k8[6] = b3.x; k8[7] = b3.y;
                 }
-                mma_commit(bar_mma);
-            }
-            __syncthreads();
-            if (tid >= 32 && tid < 64) sG2[tid] += sG2[31];
-            __syncthreads();
-            if (tid < 64) {
-                const float G = sG2[tid];
-                const float gam = ex2(G);
-                sGam[tid] = gam;
-                sBG[tid] = sB[tid] * gam;
-                sKf[tid] = ex2(sG2[63] - G);
-            }
-            if (!mma_wait()) { failed = true; break; }
-            if ((warp & 3) < 2) {
-                // rows 0-63: A_tj = beta_t exp(G_t - G_j) k_t.k_j for j < t
-                const int t = r;
-                const float Gt = sG2[t], bt = sB[t];
-                float x[32];
-                tmem_ld32(tlane + L::COL_G + 32 * hh, x);
-                tmem_ld_wait();
+                const bool valid = row < nvalid;
+                float kh[8];
+                float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+                if constexpr (VAR == kGla) {
+                    g0 = *reinterpret_cast<const float4*>(gt + row * DK + c0);
+                    g1 = *reinterpret_cast<const float4*>(gt + row * DK + c0 + 4);
+                }
+                const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
-                    const int j = 32 * hh + 4 * m;
-                    float4 o;
-                    o.x = (j + 0 < t) ? bt * ex2(Gt - sG2[j + 0]) * x[4 * m + 0] : 0.f;
-                    o.y = (j + 1 < t) ? bt * ex2(Gt - sG2[j + 1]) * x[4 * m + 1] : 0.f;
-                    o.z = (j + 2 < t) ? bt * ex2(Gt - sG2[j + 2]) * x[4 * m + 2] : 0.f;
-                    o.w = (j + 3 < t) ? bt * ex2(Gt - sG2[j + 3]) * x[4 * m + 3] : 0.f;
-                    *reinterpret_cast<float4*>(As + t * kAStride + j) = o;
+                    float qq = phi_on ? elu1(q8[m]) : q8[m];
+                    float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
+                    if constexpr (VAR == kGla) {
+                        const float inv = __fdividef(1.f, gg[m]);
+                        qq *= gg[m];
+                        kh[m] = kv * sGC[c0 + m] * inv;
+                        kv *= inv;
+                    }
+                    q8[m] = qq;
+                    k8[m] = kv;
                 }
-            } else {
-                // rows 64-127: P_tj = exp(G_t - G_j) q_t.k_j for j <= t
-                const int t = r - 64;
-                const float Gt = sG2[t];
-                float x[32];
-                tmem_ld32(tlane + L::COL_G + 32 * hh, x);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = 32 * hh + i;
-                    x[i] = (j <= t) ? ex2(Gt - sG2[j]) * x[i] : 0.f;
-                }
-                store_row32_bf16(aPS, t, 4 * hh, x);
+                st_shared_v4(qa, pack_bf16(q8[0], q8[1]), pack_bf16(q8[2], q8[3]), pack_bf16(q8[4], q8[5]),
+                             pack_bf16(q8[6], q8[7]));
+                st_shared_v4(ka, pack_bf16(k8[0], k8[1]), pack_bf16(k8[2], k8[3]), pack_bf16(k8[4], k8[5]),
+                             pack_bf16(k8[6], k8[7]));
+                if constexpr (VAR == kGla)
+                    st_shared_v4(aKH + a * 8192 + off, pack_bf16(kh[0], kh[1]), pack_bf16(kh[2], kh[3]),
+                                 pack_bf16(kh[4], kh[5]), pack_bf16(kh[6], kh[7]));
             }
-            // Q' = diag(gam) Q in place (block 1); the Gram MMA is done with it.
+        }
+        publish();
+        // ---- P = Q~ K~^T ;  O = Q~ X0^T ;  dX = V^T K^ -----------------------
+        if (tid == 0) {
 #pragma unroll
-            for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
-                const int e = tid + kThreads * i;
-                const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-                scale_chunk(aQK + a * 16384 + 8192 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16, sGam[row]);
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                const uint32_t qa = aQK + (kk / 4) * 16384 + (kk % 4) * 32;
+                mma_bf16_ss(tmem + L::COL_G, kmaj(qa), kmaj(qa + 8192), ID_128x64_KK, kk > 0);
+                mma_bf16_ss(tmem + L::COL_O, kmaj(qa), kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
+                            ID_128xDV_KK, kk > 0);
             }
-            __syncthreads();
-            // ---- T = (I + A)^{-1}: diagonal 16x16 blocks, one warp each ---------
-            if (warp < 4 && lane < 16) {
-                const int w0 = 16 * warp, l = lane;
-                float x[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float acc = (i == l) ? 1.f : 0.f;
-#pragma unroll
-                    for (int k = 0; k < i; ++k) acc -= As[(w0 + i) * kAStride + w0 + k] * x[k];
-                    x[i] = acc;
-                }
-                __syncwarp(0x0000ffffu);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) As[(w0 + i) * kAStride + w0 + l] = x[i];
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bdesc = (VAR == kGla) ? mnmaj(aKH + kk * 2048, 8192)
+                                                     : mnmaj(aQK + 8192 + kk * 2048, 16384);
+                mma_bf16_ss(tmem + L::COL_S, mnmaj(aV + kk * 2048, v_lbo), bdesc, ID_128xDK_MM, kk > 0);
             }
-            __syncthreads();
-            // ---- merge level 1: T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22 (16x16)
-            {
-                const int m = tid >> 7, tl = tid & 127;
-                const int rb = 16 + 32 * m, cb = 32 * m;
-                const int i = tl >> 3, j = 2 * (tl & 7);
-                float* X = Rs + m * 256;
-                const float* arow = As + (rb + i) * kAStride + cb;
-                float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; k += 4) {
-                    const float4 av = *reinterpret_cast<const float4*>(arow + k);
-                    const float2 u0 = *reinterpret_cast<const float2*>(As + (cb + k + 0) * kAStride + cb + j);
-                    const float2 u1 = *reinterpret_cast<const float2*>(As + (cb + k + 1) * kAStride + cb + j);
-                    const float2 u2 = *reinterpret_cast<const float2*>(As + (cb + k + 2) * kAStride + cb + j);
-                    const float2 u3 = *reinterpret_cast<const float2*>(As + (cb + k + 3) * kAStride + cb + j);
-                    x0 += av.x * u0.x + av.y * u1.x + av.z * u2.x + av.w * u3.x;
-                    x1 += av.x * u0.y + av.y * u1.y + av.z * u2.y + av.w * u3.y;
-                }
-                *reinterpret_cast<float2*>(X + i * 16 + j) = make_float2(x0, x1);
-                __syncthreads();
-                const float* trow = As + (rb + i) * kAStride + rb;
-                float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-                for (int l = 0; l < 16; l += 4) {
-                    const float4 tv = *reinterpret_cast<const float4*>(trow + l);
-                    const float2 u0 = *reinterpret_cast<const float2*>(X + (l + 0) * 16 + j);
-                    const float2 u1 = *reinterpret_cast<const float2*>(X + (l + 1) * 16 + j);
-                    const float2 u2 = *reinterpret_cast<const float2*>(X + (l + 2) * 16 + j);
-                    const float2 u3 = *reinterpret_cast<const float2*>(X + (l + 3) * 16 + j);
-                    y0 += tv.x * u0.x + tv.y * u1.x + tv.z * u2.x + tv.w * u3.x;
-                    y1 += tv.x * u0.y + tv.y * u1.y + tv.z * u2.y + tv.w * u3.y;
-                }
-                *reinterpret_cast<float2*>(As + (rb + i) * kAStride + cb + j) = make_float2(-y0, -y1);
-                __syncthreads();
-            }
-            // ---- merge level 2: T[32:64, 0:32] = -T_B (A[32:64, 0:32] T_A), 2x2 tiles
-            {
-                const int i = 2 * (tid >> 4), j = 2 * (tid & 15);
-                const float* a0 = As + (32 + i) * kAStride;
-                const float* a1 = a0 + kAStride;
-                float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-#pragma unroll
-                for (int k = 0; k < 32; k += 4) {
-                    const float4 p0 = *reinterpret_cast<const float4*>(a0 + k);
-                    const float4 p1 = *reinterpret_cast<const float4*>(a1 + k);
-                    const float2 u0 = *reinterpret_cast<const float2*>(As + (k + 0) * kAStride + j);
-                    const float2 u1 = *reinterpret_cast<const float2*>(As + (k + 1) * kAStride + j);
-                    const float2 u2 = *reinterpret_cast<const float2*>(As + (k + 2) * kAStride + j);
-                    const float2 u3 = *reinterpret_cast<const float2*>(As + (k + 3) * kAStride + j);
-                    x00 += p0.x * u0.x + p0.y * u1.x + p0.z * u2.x + p0.w * u3.x;
-                    x01 += p0.x * u0.y + p0.y * u1.y + p0.z * u2.y + p0.w * u3.y;
-                    x10 += p1.x * u0.x + p1.y * u1.x + p1.z * u2.x + p1.w * u3.x;
-                    x11 += p1.x * u0.y + p1.y * u1.y + p1.z * u2.y + p1.w * u3.y;
-                }
-                *reinterpret_cast<float2*>(Rs + i * 32 + j) = make_float2(x00, x01);
-                *reinterpret_cast<float2*>(Rs + (i + 1) * 32 + j) = make_float2(x10, x11);
-                __syncthreads();
-                const float* b0 = As + (32 + i) * kAStride + 32;
-                const float* b1 = b0 + kAStride;
-                float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
-#pragma unroll
-                for (int l = 0; l < 32; l += 4) {
-                    const float4 q0 = *reinterpret_cast<const float4*>(b0 + l);
-                    const float4 q1 = *reinterpret_cast<const float4*>(b1 + l);
-                    const float2 u0 = *reinterpret_cast<const float2*>(Rs + (l + 0) * 32 + j);
-                    const float2 u1 = *reinterpret_cast<const float2*>(Rs + (l + 1) * 32 + j);
-                    const float2 u2 = *reinterpret_cast<const float2*>(Rs + (l + 2) * 32 + j);
-                    const float2 u3 = *reinterpret_cast<const float2*>(Rs + (l + 3) * 32 + j);
-                    y00 += q0.x * u0.x + q0.y * u1.x + q0.z * u2.x + q0.w * u3.x;
-                    y01 += q0.x * u0.y + q0.y * u1.y + q0.z * u2.y + q0.w * u3.y;
-                    y10 += q1.x * u0.x + q1.y * u1.x + q1.z * u2.x + q1.w * u3.x;
-                    y11 += q1.x * u0.y + q1.y * u1.y + q1.z * u2.y + q1.w * u3.y;
-                }
-                *reinterpret_cast<float2*>(As + (32 + i) * kAStride + j) = make_float2(-y00, -y01);
-                *reinterpret_cast<float2*>(As + (33 + i) * kAStride + j) = make_float2(-y10, -y11);
-                __syncthreads();
-            }
-            // ---- T diag(beta) and T diag(beta gam) as bf16 MMA operands ---------
+            mma_commit(bar_mma);
+        }
+        if constexpr (VAR == kNorm) {
+            // While the MMAs run: den_t = q~_t . z_0, and this chunk's sum of phi(k).
             {
                 const int t = tid >> 2, q4 = tid & 3;
+                float d = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c8 = 2 * q4 + cc;
-                    float y1[8], y2[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 8 * c8 + e;
-                        const float tv = As[t * kAStride + j];
-                        y1[e] = tv * sB[j];
-                        y2[e] = tv * sBG[j];
-                    }
-                    st_shared_v4(aTB1 + sw128_off(t, c8), pack_bf16(y1[0], y1[1]), pack_bf16(y1[2], y1[3]),
-                                 pack_bf16(y1[4], y1[5]), pack_bf16(y1[6], y1[7]));
-                    st_shared_v4(aTB2 + sw128_off(t, c8), pack_bf16(y2[0], y2[1]), pack_bf16(y2[2], y2[3]),
-                                 pack_bf16(y2[4], y2[5]), pack_bf16(y2[6], y2[7]));
+                for (int m = 0; m < KA * 2; ++m) {
+                    const int cq = q4 * (KA * 2) + m;       // 8-channel group
+                    const int a = cq / 8, lc = cq % 8;
+                    const uint4 u = ld_shared_v4(aQK + a * 16384 + sw128_off(t, lc));
+                    const float2 x0 = unpack_bf16(u.x), x1 = unpack_bf16(u.y), x2 = unpack_bf16(u.z), x3 = unpack_bf16(u.w);
+                    const float* z = sZ + 8 * cq;
+                    d += x0.x * z[0] + x0.y * z[1] + x1.x * z[2] + x1.y * z[3] + x2.x * z[4] + x2.y * z[5] +
+                         x3.x * z[6] + x3.y * z[7];
                 }
+                d += __shfl_xor_sync(0xffffffffu, d, 1);
+                d += __shfl_xor_sync(0xffffffffu, d, 2);
+                if (q4 == 0) sDen[t] = d;
             }
-            publish();
-            // ---- W^T = K^T (T diag(beta gam))^T, Ut^T = V^T (T diag(beta))^T ------
-            if (tid == 0) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    mma_bf16_ss(tmem + L::COL_W, mnmaj(aQK + kk * 2048, 16384), kmaj(aTB2 + kk * 32),
-                                ID_128x64_MK, kk > 0);
-                    mma_bf16_ss(tmem + L::COL_U, mnmaj(aV + kk * 2048, v_lbo), kmaj(aTB1 + kk * 32),
-                                ID_128x64_MK, kk > 0);
-                }
-                mma_commit(bar_mma);
-                bulk_wait_read_all();  // the previous output store read the W^T buffer
-            }
-            if (!mma_wait()) { failed = true; break; }
-            // W^T rows (d_k index) to shared memory as the MN-major operand [dk][t]
-            if (r < DK) {
-                float x[32];
-                tmem_ld32(tlane + L::COL_W + 32 * hh, x);
-                tmem_ld_wait();
-                store_row32_bf16(aWS, r, 4 * hh, x);
-            }
-            // K' = diag(gam_C / gam) K in place (block 0); its MMAs are done.
-#pragma unroll
-            for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
-                const int e = tid + kThreads * i;
-                const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-                scale_chunk(aQK + a * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16, sKf[row]);
-            }
-            publish();
-            // ---- U^T = Ut^T - X0 W^T ;  O = Q' X0^T -------------------------------
-            if (tid == 0) {
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint32_t sa = aSS + (kk / 4) * 16384 + (kk % 4) * 32;
-                    mma_bf16_ss(tmem + L::COL_U, kmaj(sa), mnmaj(aWS + kk * 2048, 8192), ID_128x64_KM_NEG, 1);
-                    mma_bf16_ss(tmem + L::COL_O, kmaj(aQK + 8192 + (kk / 4) * 16384 + (kk % 4) * 32), kmaj(sa),
-                                ID_128xDV_KK, kk > 0);
-                }
-                mma_commit(bar_mma);
-            }
-            if (!mma_wait()) { failed = true; break; }
             {
-                float x[32];
-                tmem_ld32(tlane + L::COL_U + 32 * hh, x);
-                tmem_ld_wait();
-                store_row32_bf16(aUS, r, 4 * hh, x);
-            }
-            publish();
-            // ---- O += P U ;  dX = U^T K' -------------------------------------------
-            if (tid == 0) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    mma_bf16_ss(tmem + L::COL_O, kmaj(aPS + kk * 32), kmaj(aUS + kk * 32), ID_128xDV_KK, 1);
-                    mma_bf16_ss(tmem + L::COL_S, kmaj(aUS + kk * 32), mnmaj(aQK + kk * 2048, 16384),
-                                ID_128xDK_KM, kk > 0);
-                }
-                mma_commit(bar_mma);
-            }
-            if (!mma_wait()) { failed = true; break; }
-            if (own) {
-                const float gC = sGam[63];
-#pragma unroll
-                for (int b = 0; b < DKH / 32; ++b) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) st[32 * b + i] = gC * st[32 * b + i] + x[i];
-                }
-                publish_state();
-            }
-            store_output(aWS, t0);
-        } else {
-            // ======================= normalized / gated =========================
-            if constexpr (VAR == kGla) {
-                // Running products Gam_t = prod_{i<=t} gamma_i per channel, in place.
-                // 256/DK threads per channel each scan a contiguous part of the chunk.
-                constexpr int NP = kThreads / DK, TP = C / NP;
-                float* gt = reinterpret_cast<float*>(stg + L::QK_BYTES + L::V_BYTES);
+                constexpr int NP = kThreads / DK, RP = C / NP;
                 const int ch = tid % DK, part = tid / DK;
-                float gv[TP];
-#pragma unroll
-                for (int i = 0; i < TP; ++i) {
-                    const int t = part * TP + i;
-                    gv[i] = (t < nvalid) ? gt[t * DK + ch] : 1.f;
-                }
-                float G = 1.f;
-#pragma unroll
-                for (int i = 0; i < TP; ++i) {
-                    G *= gv[i];
-                    gv[i] = G;
-                }
-                sPart[part * DK + ch] = G;
-                __syncthreads();
-                float pre = 1.f, tot = 1.f;
-#pragma unroll
-                for (int q = 0; q < NP; ++q) {
-                    const float v = sPart[q * DK + ch];
-                    if (q < part) pre *= v;
-                    tot *= v;
-                }
-#pragma unroll
-                for (int i = 0; i < TP; ++i) gt[(part * TP + i) * DK + ch] = gv[i] * pre;
-                if (part == 0) sGC[ch] = tot;
-                __syncthreads();
-            }
-            if (VAR == kNorm && tid < DK) sDz[tid] = 0.f;
-            // q~ (block 0), k~ (block 1), k^ (gla: its own tile) in place, 8 channels per chunk.
-            {
-                const float* gt = reinterpret_cast<const float*>(stg + L::QK_BYTES + L::V_BYTES);
-#pragma unroll
-                for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
-                    const int e = tid + kThreads * i;
-                    const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-                    const int lc = pc ^ (row & 7);
-                    const int c0 = a * 64 + lc * 8;
-                    const uint32_t off = (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
-                    const uint32_t qa = aQK + a * 16384 + off, ka = qa + 8192;
-                    const uint4 uq = ld_shared_v4(qa), uk = ld_shared_v4(ka);
-                    float q8[8], k8[8];
-                    {
-                        const float2 a0 = unpack_bf16(uq.x), a1 = unpack_bf16(uq.y), a2 = unpack_bf16(uq.z), a3 = unpack_bf16(uq.w);
-                        q8[0] = a0.x; q8[1] = a0.y; q8[2] = a1.x; q8[3] = a1.y;
-                        q8[4] = a2.x; q8[5] = a2.y; q8[6] = a3.x; q8[7] = a3.y;
-                        const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z), b3 = unpack_bf16(uk.w);
-                        k8[0] = b0.x; k8[1] = b0.y; k8[2] = b1.x; k8[3] = b1.y;
-                        k8[4] = b2.x; k8[5] = b2.y; k8[6] = b3.x; k8[7] = b3.y;
-                    }
-                    const bool valid = row < nvalid;
-                    float kh[8];
-                    float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
-                    if constexpr (VAR == kGla) {
-                        g0 = *reinterpret_cast<const float4*>(gt + row * DK + c0);
-                        g1 = *reinterpret_cast<const float4*>(gt + row * DK + c0 + 4);
-                    }
-                    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        float qq = phi_on ? elu1(q8[m]) : q8[m];
-                        float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
-                        if constexpr (VAR == kGla) {
-                            const float inv = __fdividef(1.f, gg[m]);
-                            qq *= gg[m];
-                            kh[m] = kv * sGC[c0 + m] * inv;
-                            kv *= inv;
-                        }
-                        q8[m] = qq;
-                        k8[m] = kv;
-                    }
-                    st_shared_v4(qa, pack_bf16(q8[0], q8[1]), pack_bf16(q8[2], q8[3]), pack_bf16(q8[4], q8[5]),
-                                 pack_bf16(q8[6], q8[7]));
-                    st_shared_v4(ka, pack_bf16(k8[0], k8[1]), pack_bf16(k8[2], k8[3]), pack_bf16(k8[4], k8[5]),
-                                 pack_bf16(k8[6], k8[7]));
-                    if constexpr (VAR == kGla)
-                        st_shared_v4(aKH + a * 8192 + off, pack_bf16(kh[0], kh[1]), pack_bf16(kh[2], kh[3]),
-                                     pack_bf16(kh[4], kh[5]), pack_bf16(kh[6], kh[7]));
-                }
-            }
-            publish();
-            // ---- P = Q~ K~^T ;  O = Q~ X0^T ;  dX = V^T K^ -----------------------
-            if (tid == 0) {
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint32_t qa = aQK + (kk / 4) * 16384 + (kk % 4) * 32;
-                    mma_bf16_ss(tmem + L::COL_G, kmaj(qa), kmaj(qa + 8192), ID_128x64_KK, kk > 0);
-                    mma_bf16_ss(tmem + L::COL_O, kmaj(qa), kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
-                                ID_128xDV_KK, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bdesc = (VAR == kGla) ? mnmaj(aKH + kk * 2048, 8192)
-                                                         : mnmaj(aQK + 8192 + kk * 2048, 16384);
-                    mma_bf16_ss(tmem + L::COL_S, mnmaj(aV + kk * 2048, v_lbo), bdesc, ID_128xDK_MM, kk > 0);
-                }
-                mma_commit(bar_mma);
-            }
-            if constexpr (VAR == kNorm) {
-                // While the MMAs run: den_t = q~_t . z_0, and this chunk's sum of phi(k).
-                {
-                    const int t = tid >> 2, q4 = tid & 3;
-                    float d = 0.f;
-#pragma unroll
-                    for (int m = 0; m < KA * 2; ++m) {
-                        const int cq = q4 * (KA * 2) + m;       // 8-channel group
-                        const int a = cq / 8, lc = cq % 8;
-                        const uint4 u = ld_shared_v4(aQK + a * 16384 + sw128_off(t, lc));
-                        const float2 x0 = unpack_bf16(u.x), x1 = unpack_bf16(u.y), x2 = unpack_bf16(u.z), x3 = unpack_bf16(u.w);
-                        const float* z = sZ + 8 * cq;
-                        d += x0.x * z[0] + x0.y * z[1] + x1.x * z[2] + x1.y * z[3] + x2.x * z[4] + x2.y * z[5] +
-                             x3.x * z[6] + x3.y * z[7];
-                    }
-                    d += __shfl_xor_sync(0xffffffffu, d, 1);
-                    d += __shfl_xor_sync(0xffffffffu, d, 2);
-                    if (q4 == 0) sDen[t] = d;
-                }
-                {
-                    constexpr int NP = kThreads / DK, RP = C / NP;
-                    const int ch = tid % DK, part = tid / DK;
-                    const uint32_t base = aQK + (ch / 64) * 16384 + 8192 + (ch % 8) * 2;
-                    const int lc = (ch % 64) / 8;
-                    float zs = 0.f;
+                const uint32_t base = aQK + (ch / 64) * 16384 + 8192 + (ch % 8) * 2;
+                const int lc = (ch % 64) / 8;
+                float zs = 0.f;
 #pragma unroll 8
-                    for (int j = part * RP; j < (part + 1) * RP; ++j) zs += ld_shared_bf16(base + sw128_off(j, lc));
-                    atomicAdd(&sDz[ch], zs);
-                }
+                for (int j = part * RP; j < (part + 1) * RP; ++j) zs += ld_shared_bf16(base + sw128_off(j, lc));
+                atomicAdd(&sDz[ch], zs);
             }
-            if (!mma_wait()) { failed = true; break; }
-            if ((warp & 3) < 2) {
-                // masked scores of rows t = 0..63 -> bf16 P; norm adds the row sums to den.
-                const int t = r;
+        }
+        if (!mma_wait()) { failed = true; break; }
+        if ((warp & 3) < 2) {
+            // masked scores of rows t = 0..63 -> bf16 P; norm adds the row sums to den.
+            const int t = r;
+            float x[32];
+            tmem_ld32(tlane + L::COL_G + 32 * hh, x);
+            tmem_ld_wait();
+            float rs = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                x[i] = (32 * hh + i <= t) ? x[i] : 0.f;
+                rs += x[i];
+            }
+            store_row32_bf16(aPS, t, 4 * hh, x);
+            if (VAR == kNorm) atomicAdd(&sDen[t], rs);
+        }
+        if (own) {
+#pragma unroll
+            for (int b = 0; b < DKH / 32; ++b) {
                 float x[32];
-                tmem_ld32(tlane + L::COL_G + 32 * hh, x);
+                tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
                 tmem_ld_wait();
-                float rs = 0.f;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    x[i] = (32 * hh + i <= t) ? x[i] : 0.f;
-                    rs += x[i];
+                    const float dec = (VAR == kGla) ? sGC[hh * DKH + 32 * b + i] : 1.f;
+                    st[32 * b + i] = dec * st[32 * b + i] + x[i];
                 }
-                store_row32_bf16(aPS, t, 4 * hh, x);
-                if (VAR == kNorm) atomicAdd(&sDen[t], rs);
             }
-            if (own) {
-#pragma unroll
-                for (int b = 0; b < DKH / 32; ++b) {
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float dec = (VAR == kGla) ? sGC[hh * DKH + 32 * b + i] : 1.f;
-                        st[32 * b + i] = dec * st[32 * b + i] + x[i];
-                    }
-                }
-                publish_state();
-            }
-            if (VAR == kNorm && tid < DK) sZ[tid] += sDz[tid];
-            publish();
-            // ---- O += P V ----------------------------------------------------------
-            if (tid == 0) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + L::COL_O, kmaj(aPS + kk * 32), mnmaj(aV + kk * 2048, v_lbo), ID_128xDV_KM, 1);
-                mma_commit(bar_mma);
-                if (VAR == kNorm) bulk_wait_read_all();  // the previous output store read the tile
-            }
-            if (VAR == kNorm && p.den_out && tid < nvalid)
-                p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
-            if (!mma_wait()) { failed = true; break; }
-            const uint32_t ot = (VAR == kGla) ? sbase + s * L::STAGE + L::QK_BYTES + L::V_BYTES : sbase + L::OFF_OT;
-            store_output(ot, t0);
+            publish_state();
         }
+        if (VAR == kNorm && tid < DK) sZ[tid] += sDz[tid];
+        publish();
+        // ---- O += P V ----------------------------------------------------------
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + L::COL_O, kmaj(aPS + kk * 32), mnmaj(aV + kk * 2048, v_lbo), ID_128xDV_KM, 1);
+            mma_commit(bar_mma);
+            if (VAR == kNorm) bulk_wait_read_all();  // the previous output store read the tile
+        }
+        if (VAR == kNorm && p.den_out && tid < nvalid)
+            p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
+        if (!mma_wait()) { failed = true; break; }
+        const uint32_t ot = (VAR == kGla) ? sbase + s * L::STAGE + L::QK_BYTES + L::V_BYTES : sbase + L::OFF_OT;
+        store_output(ot, t0);
     }
 
     // ---- on failure, let an in-flight prefetch land before the CTA exits -----
@@ -836,8 +532,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
 #pragma unroll
             for (int i = 0; i < DKH; ++i) {
                 const int cc = hh * DKH + i;
-                if (VAR == kGdn) so[static_cast<size_t>(r) * DK + cc] = st[i];
-                else so[static_cast<size_t>(cc) * DV + r] = st[i];
+                so[static_cast<size_t>(cc) * DV + r] = st[i];
             }
         }
         if (VAR == kNorm && tid < DK) so[static_cast<size_t>(DK) * DV + tid] = sZ[tid];
