@@ -23,6 +23,7 @@ LA_NORM_ELU1, LA_GLA, LA_GDN = 0, 1, 2
 LA_BF16, LA_FP32 = 0, 1
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(6)
 LA_FLAG_IDENTITY_PHI = 0x1
+LA_FLAG_SEQUENTIAL_CHUNKS = 0x2
 LA_FLAG_TEST_TIMEOUT = 0x100
 
 VARIANTS = {"norm": LA_NORM_ELU1, "gla": LA_GLA, "gdn": LA_GDN}

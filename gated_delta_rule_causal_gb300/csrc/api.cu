@@ -150,6 +150,11 @@ int la_create(const la_config* cfg, la_handle** out) {
     if (tc_shape) {
         const size_t gdn = la::chunk::gdn_workspace_bytes(cfg->B * cfg->H, cfg->d_k, cfg->d_v, la::chunk::kGdnWindow);
         if (gdn > h->ws_bytes) h->ws_bytes = gdn;
+        // three-phase normalized / gated prefill: per-chunk states of up to
+        // 128 chunks (T = 8192) per sequence-head, capped at the L2 budget
+        size_t par = static_cast<size_t>(cfg->B) * cfg->H * 128 * la::chunk::par_chunk_bytes(cfg->d_k, cfg->d_v);
+        if (par > la::chunk::kParL2Bytes) par = la::chunk::kParL2Bytes;
+        if (par > h->ws_bytes) h->ws_bytes = par;
     }
     if (cudaMalloc(&h->d_ws, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();

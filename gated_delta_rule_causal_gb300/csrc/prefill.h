@@ -30,5 +30,13 @@ int gdn_group(int BH);
 size_t gdn_workspace_bytes(int BH, int dk, int dv, int W);
 cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s);
 
+// Normalized / per-channel gated: three fully parallel phases (chunk
+// summaries, a scan over the chunks, outputs) when the per-chunk states of
+// the whole problem fit in the workspace and comfortably in L2.
+constexpr size_t kParL2Bytes = size_t(48) << 20;
+size_t par_chunk_bytes(int dk, int dv);
+bool par_fits(int BH, int T, int dk, int dv, size_t ws_bytes);
+cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s);
+
 }  // namespace chunk
 }  // namespace la

@@ -96,6 +96,11 @@ enum {
 
 /* la_config.flags */
 #define LA_FLAG_IDENTITY_PHI 0x1u   /* LA_GLA without the feature map (phi = identity) */
+#define LA_FLAG_SEQUENTIAL_CHUNKS 0x2u /* LA_NORM_ELU1 / LA_GLA chunked prefill: always walk the
+                                          chunks of a sequence-head in order (split into segments
+                                          when B*H is small) instead of the three-phase parallel
+                                          form the library picks when the per-chunk states fit
+                                          its workspace; results agree within rounding */
 #define LA_FLAG_TEST_TIMEOUT 0x100u /* test hook: the chunked prefill kernel waits once on a
                                        barrier nothing signals, with a 1 ms limit, then
                                        records LA_ERR_TIMEOUT in the status word and exits */

@@ -36,8 +36,8 @@ def oracle_run(w, inp, state_in=None):
     return oracle.run(w.variant, q, k, v, g, b, sin)
 
 
-def assert_parity(w, inp, chunk=0, state_in=None, tol=None):
-    h = handle(w)
+def assert_parity(w, inp, chunk=0, state_in=None, tol=None, flags=0):
+    h = handle(w, flags=flags)
     o, st, den = run_gpu_prefill(h, w, inp, chunk, state_in, with_den=(w.variant == "norm"))
     ref = oracle_run(w, inp, state_in)
     tol = tol or TOL[w.io]
@@ -62,6 +62,16 @@ def test_chunked_prefill_parity(variant, d, T):
     assert_parity(w, W.draw(w, seed=T), chunk=64)
 
 
+@pytest.mark.parametrize("variant", ["norm", "gla"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [65, 200])
+def test_chunked_prefill_sequential_parity(variant, d, T):
+    # the chunk-by-chunk kernel the parallel three-phase form replaces when
+    # the per-chunk states fit the workspace
+    w = base(variant, d).with_(T=T)
+    assert_parity(w, W.draw(w, seed=T), chunk=64, flags=la.LA_FLAG_SEQUENTIAL_CHUNKS)
+
+
 @pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
 @pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64)])
 def test_chunked_prefill_rectangular_heads(variant, dk, dv):
@@ -83,9 +93,11 @@ def test_chunked_prefill_from_a_state(variant):
 
 @pytest.mark.parametrize("variant", ["norm", "gla"])
 @pytest.mark.parametrize("T", [256, 1000, 1023])
-def test_segmented_prefill_parity(variant, T):
-    # B*H = 2 leaves most SMs idle, so the sequence is split into segments
-    # (up to T/128 of them); a non-zero initial state and a ragged tail too.
+@pytest.mark.parametrize("flags", [0, la.LA_FLAG_SEQUENTIAL_CHUNKS], ids=["auto", "sequential"])
+def test_segmented_prefill_parity(variant, T, flags):
+    # B*H = 2 leaves most SMs idle: the parallel form, or with the flag the
+    # sequence split into segments (up to T/128 of them); a non-zero initial
+    # state and a ragged tail too.
     w = base(variant, 128).with_(T=T)
     inp = W.draw(w, seed=T + 7)
     rng = np.random.default_rng(T)
@@ -93,7 +105,7 @@ def test_segmented_prefill_parity(variant, T):
     sin = (rng.standard_normal((w.B, w.H, ss)) * 0.1).astype(np.float32)
     if variant == "norm":
         sin[..., w.dk * w.dv:] = np.abs(sin[..., w.dk * w.dv:]) * 50 + 1.0
-    assert_parity(w, inp, chunk=64, state_in=sin)
+    assert_parity(w, inp, chunk=64, state_in=sin, flags=flags)
 
 
 def test_gla_identity_feature_map():
