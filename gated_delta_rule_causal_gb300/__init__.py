@@ -8,7 +8,7 @@ calls raise.
 
 Low level (same names as the C ABI): ``la_create``, ``la_forward``,
 ``la_decode_step``, ``la_status``, ``la_destroy``, ``la_last_error``,
-``la_version``, ``la_forward_noalloc``. Convenience: ``Handle`` takes torch
+``la_last_launches``, ``la_version``, ``la_forward_noalloc``. Convenience: ``Handle`` takes torch
 tensors.
 """
 from __future__ import annotations
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.la_destroy.restype = None
             L.la_last_error.argtypes = [vp]
             L.la_last_error.restype = ctypes.c_char_p
+            L.la_last_launches.argtypes = [vp]
+            L.la_last_launches.restype = i
             L.la_version.argtypes = []
             L.la_version.restype = i
             L.la_forward_noalloc.argtypes = [ctypes.POINTER(la_config), vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, vp]
@@ -116,6 +118,10 @@ def la_destroy(h) -> None:
 def la_last_error(h) -> str:
     s = lib().la_last_error(h)
     return s.decode() if s else ""
+
+
+def la_last_launches(h) -> int:
+    return lib().la_last_launches(h)
 
 
 # ------------------------------------------------------------------ torch marshalling
@@ -219,6 +225,10 @@ class Handle:
                             _ptr(out), _ptr(state_out), _ptr(den_out), var, _stream_ptr(stream))
         self._check(rc)
         return out, state_out, den_out
+
+    def last_launches(self) -> int:
+        """Kernels the last forward / decode_step call enqueued."""
+        return la_last_launches(self._h)
 
     def status(self, stream=None) -> int:
         """Synchronize the stream and return (and clear) the device status."""

@@ -21,6 +21,7 @@ struct la_handle {
     size_t ws_bytes;
     PFN_cuTensorMapEncodeTiled_v12000 encode;
     std::string last_error;
+    int last_launches;  // kernels enqueued by the last successful call
 };
 
 namespace {
@@ -98,6 +99,7 @@ la::FwdArgs make_args(la_handle* h, const void* q, const void* k, const void* v,
     a.sm_count = h->sm_count;
     a.workspace = h->d_ws;
     a.ws_bytes = h->ws_bytes;
+    a.nlaunch = &h->last_launches;
     return a;
 }
 
@@ -132,6 +134,7 @@ int la_create(const la_config* cfg, la_handle** out) {
     h->d_ws = nullptr;
     h->ws_bytes = 0;
     h->encode = nullptr;
+    h->last_launches = 0;
     DeviceGuard g(cfg->device);
     if (!g.ok) { delete h; return LA_ERR_CUDA; }
     if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess || cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
@@ -194,6 +197,7 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v, const 
                void* cuda_stream) {
     if (!h) return LA_ERR_INVALID_ARG;
     h->last_error.clear();
+    h->last_launches = 0;
     if (T < 0) return fail(h, LA_ERR_INVALID_ARG, "T must be >= 0");
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const la_config& c = h->cfg;
@@ -228,6 +232,7 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v, const 
     } else {
         e = la::launch_recurrent(a, s);
         if (e != cudaSuccess) return cuda_fail(h, e, "recurrent kernel launch");
+        h->last_launches = 1;
     }
     return LA_OK;
 }
@@ -237,6 +242,7 @@ int la_decode_step(la_handle* h, const void* q, const void* k, const void* v, co
                    void* cuda_stream) {
     if (!h) return LA_ERR_INVALID_ARG;
     h->last_error.clear();
+    h->last_launches = 0;
     int rc = check_common(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant);
     if (rc != LA_OK) return rc;
     if (!state_out) return fail(h, LA_ERR_INVALID_ARG, "state_out is required for a decode step");
@@ -245,8 +251,11 @@ int la_decode_step(la_handle* h, const void* q, const void* k, const void* v, co
     la::FwdArgs a = make_args(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, 1);
     cudaError_t e = la::launch_decode(a, static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "decode kernel launch");
+    h->last_launches = 1;
     return LA_OK;
 }
+
+int la_last_launches(const la_handle* h) { return h ? h->last_launches : 0; }
 
 int la_status(la_handle* h, void* cuda_stream) {
     if (!h) return LA_ERR_INVALID_ARG;

@@ -30,6 +30,7 @@ struct FwdArgs {
     int sm_count;
     float* workspace;  // scratch for segment summaries (may be NULL)
     size_t ws_bytes;
+    int* nlaunch;      // if not NULL, incremented by the number of kernels enqueued
 };
 
 // Token-by-token recurrence on CUDA cores; any supported head size, fp32 or

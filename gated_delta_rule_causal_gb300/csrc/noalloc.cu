@@ -152,6 +152,7 @@ extern "C" int la_forward_noalloc(const la_config* cfg, const void* q, const voi
     a.sm_count = sms;
     a.workspace = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kStatusBytes);
     a.ws_bytes = kScratchBytes - kStatusBytes;
+    a.nlaunch = nullptr;
     const char* what = "";
     if (la::launch_chunked(a, static_cast<cudaStream_t>(cuda_stream), g_encode, &what) != cudaSuccess) {
         cudaGetLastError();

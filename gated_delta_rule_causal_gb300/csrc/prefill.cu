@@ -75,6 +75,7 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
         }
     }
     *what = "chunked prefill launch";
+    if (a.nlaunch) *a.nlaunch += (p.nseg > 1) ? 2 : 1;   // segment summaries + chunk kernel
     switch (a.variant) {
         case kNorm: return chunk::launch_norm(a.dk, a.dv, m, p, a.BH, s);
         case kGla: return chunk::launch_gla(a.dk, a.dv, m, p, a.BH, s);

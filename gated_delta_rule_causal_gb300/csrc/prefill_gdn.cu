@@ -872,6 +872,7 @@ cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int W, cudaStream
             kern<<<p.n_chain + n_prep, kThreads, smem, s>>>(m.q, m.k, m.v, p);
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
+            if (a.nlaunch) ++*a.nlaunch;
         }
     }
     return cudaSuccess;

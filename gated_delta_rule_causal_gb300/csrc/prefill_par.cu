@@ -733,6 +733,7 @@ cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     p.nch = static_cast<int>(nch);
     p.flags = a.flags;
     p.status = a.status;
+    if (a.nlaunch) *a.nlaunch += 3;   // summary, scan, output
     if (a.variant == kNorm) return par::dispatch<kNorm>(a.dk, a.dv, m, p, a.sm_count, s);
     if (a.variant == kGla) return par::dispatch<kGla>(a.dk, a.dv, m, p, a.sm_count, s);
     return cudaErrorInvalidValue;

@@ -192,6 +192,14 @@ void la_destroy(la_handle* h);
 /* Text of the last failure on h ("" if none). Valid until the next call on h. */
 const char* la_last_error(const la_handle* h);
 
+/* Number of CUDA kernels the last successful la_forward / la_decode_step on h
+ * enqueued (0 after a failed or a T = 0 call, or for a NULL handle). A
+ * diagnostic: which algorithm the library picked shows in this count (1: the
+ * recurrent kernel or a decode step; 1 or 2: the chunk kernel, with segment
+ * summaries when B*H is small; 3: the three-phase parallel form; for LA_GDN
+ * one per window of chunks plus one, for each group of 32 sequence-heads). */
+int la_last_launches(const la_handle* h);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int la_version(void);
 

@@ -44,6 +44,7 @@ def test_null_handle_is_rejected(lib):
     assert la.la_status(None, None) == la.LA_ERR_INVALID_ARG
     la.la_destroy(None)                     # allowed
     assert la.la_last_error(None) == "null handle"
+    assert la.la_last_launches(None) == 0
 
 
 @pytest.mark.parametrize("cfg,code", [

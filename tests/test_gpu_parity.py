@@ -331,6 +331,27 @@ def test_rejected_calls_do_not_launch():
                          st) == la.LA_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("variant,T,flags,chunk,expect", [
+    ("norm", 200, 0, 64, 3),                                 # three-phase parallel form
+    ("gla", 200, 0, 64, 3),
+    ("norm", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 2),      # segment summaries + chunk kernel
+    ("norm", 100, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),      # too short to split
+    ("gdn", 200, 0, 64, 2),                                  # one window of 4 chunks, + 1
+    ("gdn", 64 * 40, 0, 64, 4),                              # windows of 16: 3, + 1
+    ("gla", 200, 0, 1, 1),                                   # the recurrent kernel
+])
+def test_launch_counts(variant, T, flags, chunk, expect):
+    # la_last_launches reports the kernels one call enqueued, which names the
+    # algorithm the library picked for the shape.
+    w = base(variant, 64).with_(T=T)
+    inp = W.draw(w, seed=1)
+    h = handle(w, flags=flags)
+    run_gpu_prefill(h, w, inp, chunk)
+    assert h.last_launches() == expect
+    h.close()
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")   # the aborted call leaves `out` unwritten
 def test_bounded_wait_expires_cleanly():
     # The test hook makes the chunked kernel wait on a barrier nothing signals;
     # the wait gives up after 1 ms, the kernel records it and exits cleanly.
