@@ -11,7 +11,7 @@
 // so the work splits into
 //  1. summary (per (head, chunk)): dX_c, and D_c (gla) or the chunk's sum
 //     of phi(k) (norm);
-//  2. scan (one thread per 4 state elements): the state entering every
+//  2. scan (one thread per 2 state elements): the state entering every
 //     chunk, stored as the bf16 operand tile the output phase loads as is,
 //     the normalizer entering every chunk (norm) and the final state;
 //  3. output (per (head, chunk)): O = Q~ X_{c-1}^T + (L o Q~ K~^T) V
@@ -47,6 +47,7 @@ struct Params {
     float* dd;              // [BH][nch][DK]: gla Gam_C, norm sum of phi(k)
     uint8_t* xs;            // [BH][nch] state entering the chunk, bf16 MMA tile (DK*DV*2 bytes)
     float* zs;              // norm: [BH][nch][DK] normalizer entering the chunk
+    uint8_t* kh;            // norm: [BH][nch] phi(k) as the bf16 operand tile (DK*128 bytes)
     int BH, T, nch;
     unsigned flags;
     int* status;
@@ -72,10 +73,10 @@ struct SumLayout {
     static constexpr uint32_t TX = STAGE;
     static constexpr uint32_t TMEM_COLS = DK;
 };
-constexpr int kSumThreads = 128;
+constexpr int kSumThreads = 256;
 
 template <int VAR, int DK, int DV>
-__global__ void __launch_bounds__(kSumThreads, 4)
+__global__ void __launch_bounds__(kSumThreads, 3)
 summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                const __grid_constant__ CUtensorMap tmg, const Params p) {
     using L = SumLayout<VAR, DK, DV>;
@@ -140,6 +141,7 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             issue_load(u + gridDim.x, s ^ 1);   // the previous unit is done with stage s^1
             pending[s ^ 1] = true;
         }
+        if (VAR == kNorm && tid == 0) bulk_wait_read_all();   // the previous phi(k) tile has left
         {
             const bool ok = mbar_wait(&bar[s], (k >> 1) & 1, kWaitLimitNs);
             if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; break; }
@@ -207,6 +209,10 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 mma_bf16_ss(tmem, mnmaj(aV + kk * 2048, 8192), mnmaj(aKH + kk * 2048, 8192),
                             idesc_bf16(128, DK, true, true), kk > 0);
             mma_commit(&bar[2]);
+            if (VAR == kNorm) {   // phi(k) for the output phase, as the operand tile it reads
+                bulk_store(p.kh + static_cast<size_t>(u) * KA * 8192, aKH, KA * 8192);
+                bulk_commit();
+            }
         }
         if constexpr (VAR == kNorm) {
             // sum of phi(k) per channel, from the bf16 operand the MMA reads
@@ -231,13 +237,14 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             tc_fence_after();
             if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; break; }
         }
-        const int r = 32 * warp + lane;
+        // thread (r, hh) stores columns [hh*DK/2, (hh+1)*DK/2) of dX row r
+        const int r = 32 * (warp & 3) + lane, hh = warp >> 2;
         if (r < DV) {
-            float* dst = p.dx + (static_cast<size_t>(bh) * p.nch + c) * DV * DK + static_cast<size_t>(r) * DK;
+            float* dst = p.dx + (static_cast<size_t>(bh) * p.nch + c) * DV * DK + static_cast<size_t>(r) * DK + hh * (DK / 2);
 #pragma unroll
-            for (int b = 0; b < DK / 32; ++b) {
+            for (int b = 0; b < DK / 64; ++b) {
                 float x[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * b, x);
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + hh * (DK / 2) + 32 * b, x);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; i += 4)
@@ -252,6 +259,7 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         for (int s2 = 0; s2 < 2; ++s2)
             if (pending[s2]) mbar_wait(&bar[s2], ((s2 == (k & 1) ? k : k + 1) >> 1) & 1, 100000000ull);
     }
+    if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
@@ -261,17 +269,18 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 // ---------------------------------------------------------------------------
 // 2. scan over the chunks of every head
 // ---------------------------------------------------------------------------
-constexpr int kScanThreads = 128;
-constexpr int kScanBatch = 8;   // chunks whose loads are in flight together
+constexpr int kScanThreads = 256;
+constexpr int kScanBatch = 32;   // chunks whose loads are in flight together
 
-// One thread per 4 state columns of one value row (and, for norm, per 4
+// One thread per 2 state columns of one value row (and, for norm, per 2
 // channels of z): a running sum over the chunks, with the loads of
-// kScanBatch chunks issued before they are consumed.
+// kScanBatch chunks issued before they are consumed, so that a sequence of
+// up to 32 chunks costs one round trip to L2.
 template <int VAR, int DK, int DV>
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
-    constexpr int E4 = DV * DK / 4;                   // 4-column groups of X
-    constexpr int Z4 = (VAR == kNorm) ? DK / 4 : 0;   // 4-channel groups of z
-    constexpr int PER = E4 + Z4;
+    constexpr int E2 = DV * DK / 2;                   // column pairs of X
+    constexpr int Z2 = (VAR == kNorm) ? DK / 2 : 0;   // channel pairs of z
+    constexpr int PER = E2 + Z2;
     constexpr size_t SSZ = static_cast<size_t>(DK) * DV + (VAR == kNorm ? DK : 0);
     constexpr size_t XS_BYTES = static_cast<size_t>(DK) * DV * 2;
     griddep_launch_dependents();
@@ -280,38 +289,34 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
     const int bh = gi / PER, e = gi % PER;
     if (bh >= p.BH) return;
     const int nch = p.nch;
-    if (e < E4) {
-        const int r = e / (DK / 4), c4 = e % (DK / 4);   // value row r, columns 4*c4 .. +4
-        const int col = 4 * c4;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e < E2) {
+        const int r = e / (DK / 2), col = 2 * (e % (DK / 2));   // value row r, columns col, col+1
+        float2 x = make_float2(0.f, 0.f);
         if (p.state_in) {
             const float* si = p.state_in + bh * SSZ + r;
-            x = make_float4(si[static_cast<size_t>(col) * DV], si[static_cast<size_t>(col + 1) * DV],
-                            si[static_cast<size_t>(col + 2) * DV], si[static_cast<size_t>(col + 3) * DV]);
+            x = make_float2(si[static_cast<size_t>(col) * DV], si[static_cast<size_t>(col + 1) * DV]);
         }
         const float* dx = p.dx + (static_cast<size_t>(bh) * nch * DV + r) * DK + col;
         const float* dd = p.dd + static_cast<size_t>(bh) * nch * DK + col;
         uint8_t* xs = p.xs + static_cast<size_t>(bh) * nch * XS_BYTES + (col / 64) * (DV * 128) +
                       sw128_off(r, (col % 64) / 8) + (col % 8) * 2;
         for (int c = 0; c < nch; c += kScanBatch) {
-            float4 a[kScanBatch], d[kScanBatch];
+            float2 a[kScanBatch], d[kScanBatch];
 #pragma unroll
             for (int u = 0; u < kScanBatch; ++u) {
                 if (c + u < nch) {
-                    a[u] = *reinterpret_cast<const float4*>(dx + static_cast<size_t>(c + u) * DV * DK);
-                    if (VAR == kGla) d[u] = *reinterpret_cast<const float4*>(dd + static_cast<size_t>(c + u) * DK);
+                    a[u] = *reinterpret_cast<const float2*>(dx + static_cast<size_t>(c + u) * DV * DK);
+                    if (VAR == kGla) d[u] = *reinterpret_cast<const float2*>(dd + static_cast<size_t>(c + u) * DK);
                 }
             }
 #pragma unroll
             for (int u = 0; u < kScanBatch; ++u) {
                 if (c + u < nch) {
-                    *reinterpret_cast<uint2*>(xs + (c + u) * XS_BYTES) =
-                        make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+                    *reinterpret_cast<uint32_t*>(xs + (c + u) * XS_BYTES) = pack_bf16(x.x, x.y);
                     if constexpr (VAR == kGla) {
-                        x = make_float4(d[u].x * x.x + a[u].x, d[u].y * x.y + a[u].y, d[u].z * x.z + a[u].z,
-                                        d[u].w * x.w + a[u].w);
+                        x = make_float2(d[u].x * x.x + a[u].x, d[u].y * x.y + a[u].y);
                     } else {
-                        x = make_float4(x.x + a[u].x, x.y + a[u].y, x.z + a[u].z, x.w + a[u].w);
+                        x = make_float2(x.x + a[u].x, x.y + a[u].y);
                     }
                 }
             }
@@ -320,28 +325,26 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
             float* so = p.state_out + bh * SSZ + r;
             so[static_cast<size_t>(col) * DV] = x.x;
             so[static_cast<size_t>(col + 1) * DV] = x.y;
-            so[static_cast<size_t>(col + 2) * DV] = x.z;
-            so[static_cast<size_t>(col + 3) * DV] = x.w;
         }
     } else {
         // norm: the normalizer entering every chunk
-        const int ch = 4 * (e - E4);
-        float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.state_in) z = *reinterpret_cast<const float4*>(p.state_in + bh * SSZ + static_cast<size_t>(DK) * DV + ch);
+        const int ch = 2 * (e - E2);
+        float2 z = make_float2(0.f, 0.f);
+        if (p.state_in) z = *reinterpret_cast<const float2*>(p.state_in + bh * SSZ + static_cast<size_t>(DK) * DV + ch);
         for (int c = 0; c < nch; c += kScanBatch) {
-            float4 a[kScanBatch];
+            float2 a[kScanBatch];
 #pragma unroll
             for (int u = 0; u < kScanBatch; ++u)
-                if (c + u < nch) a[u] = *reinterpret_cast<const float4*>(p.dd + (static_cast<size_t>(bh) * nch + c + u) * DK + ch);
+                if (c + u < nch) a[u] = *reinterpret_cast<const float2*>(p.dd + (static_cast<size_t>(bh) * nch + c + u) * DK + ch);
 #pragma unroll
             for (int u = 0; u < kScanBatch; ++u) {
                 if (c + u < nch) {
-                    *reinterpret_cast<float4*>(p.zs + (static_cast<size_t>(bh) * nch + c + u) * DK + ch) = z;
-                    z = make_float4(z.x + a[u].x, z.y + a[u].y, z.z + a[u].z, z.w + a[u].w);
+                    *reinterpret_cast<float2*>(p.zs + (static_cast<size_t>(bh) * nch + c + u) * DK + ch) = z;
+                    z = make_float2(z.x + a[u].x, z.y + a[u].y);
                 }
             }
         }
-        if (p.state_out) *reinterpret_cast<float4*>(p.state_out + bh * SSZ + static_cast<size_t>(DK) * DV + ch) = z;
+        if (p.state_out) *reinterpret_cast<float2*>(p.state_out + bh * SSZ + static_cast<size_t>(DK) * DV + ch) = z;
     }
 }
 
@@ -430,7 +433,11 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
 #pragma unroll
         for (int a = 0; a < KA; ++a) {
             tma_load_3d(&tmq, &bar[s], stg + L::QK_OFF + a * 16384, a * 64, t0, bh);
-            tma_load_3d(&tmk, &bar[s], stg + L::QK_OFF + a * 16384 + 8192, a * 64, t0, bh);
+            if (VAR == kNorm)   // phi(k) as the summary phase stored it
+                bulk_load(stg + L::QK_OFF + a * 16384 + 8192, p.kh + (static_cast<size_t>(u) * KA + a) * 8192, 8192,
+                          &bar[s]);
+            else
+                tma_load_3d(&tmk, &bar[s], stg + L::QK_OFF + a * 16384 + 8192, a * 64, t0, bh);
         }
 #pragma unroll
         for (int a = 0; a < VA; ++a) tma_load_3d(&tmv, &bar[s], stg + L::V_OFF + a * 8192, a * 64, t0, bh);
@@ -485,9 +492,23 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
             for (int i = 0; i < TP; ++i) gt[(part * TP + i) * DK + ch] = gv[i] * pre;
             __syncthreads();
         }
-        // q~ (rows 0-63), k~ (rows 64-127) in place, 8 channels per 16 bytes.
+        // q~ (rows 0-63), k~ (rows 64-127) in place, 8 channels per 16 bytes
+        // (norm: k~ = phi(k) arrived ready from the summary phase).
+        if constexpr (VAR == kNorm) {
 #pragma unroll
-        for (int i = 0; i < (64 * 8 * KA) / kOutThreads; ++i) {
+            for (int i = 0; i < (64 * 8 * KA) / kOutThreads; ++i) {
+                const int e = tid + kOutThreads * i;
+                const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
+                const uint32_t qa = aQK + a * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
+                const uint4 uq = ld_shared_v4(qa);
+                const float2 a0 = unpack_bf16(uq.x), a1 = unpack_bf16(uq.y), a2 = unpack_bf16(uq.z),
+                             a3 = unpack_bf16(uq.w);
+                st_shared_v4(qa, pack_bf16(elu1(a0.x), elu1(a0.y)), pack_bf16(elu1(a1.x), elu1(a1.y)),
+                             pack_bf16(elu1(a2.x), elu1(a2.y)), pack_bf16(elu1(a3.x), elu1(a3.y)));
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < ((VAR == kNorm) ? 0 : (64 * 8 * KA) / kOutThreads); ++i) {
             const int e = tid + kOutThreads * i;
             const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
             const int c0 = a * 64 + (pc ^ (row & 7)) * 8;
@@ -676,13 +697,13 @@ cudaError_t run(const chunk::Maps& m, const Params& p, int sm_count, cudaStream_
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, S3::SMEM);
     if (e != cudaSuccess) return e;
     const int units = p.BH * p.nch;
-    int g1 = sm_count * per_sm(S1::SMEM, S1::TMEM_COLS, kSumThreads, 4);
+    int g1 = sm_count * per_sm(S1::SMEM, S1::TMEM_COLS, kSumThreads, 3);
     int g3 = sm_count * per_sm(S3::SMEM, S3::TMEM_COLS, kOutThreads, 2);
     if (g1 > units) g1 = units;
     if (g3 > units) g3 = units;
     e = launch_pdl(k1, g1, kSumThreads, S1::SMEM, s, m.k, m.v, m.g, p);
     if (e != cudaSuccess) return e;
-    constexpr int PER = DV * DK / 4 + (VAR == kNorm ? DK / 4 : 0);
+    constexpr int PER = DV * DK / 2 + (VAR == kNorm ? DK / 2 : 0);
     const long long threads = static_cast<long long>(p.BH) * PER;
     e = launch_pdl(k2, static_cast<unsigned>((threads + kScanThreads - 1) / kScanThreads), kScanThreads, 0, s, p);
     if (e != cudaSuccess) return e;
@@ -703,7 +724,8 @@ cudaError_t dispatch(int dk, int dv, const chunk::Maps& m, const Params& p, int 
 namespace chunk {
 
 size_t par_chunk_bytes(int dk, int dv) {
-    return static_cast<size_t>(dk) * dv * 6 + static_cast<size_t>(dk) * 8;   // dX fp32 + start state bf16 + dd + zs
+    // dX fp32 + start state bf16 + dd + zs + phi(k) tile (norm)
+    return static_cast<size_t>(dk) * dv * 6 + static_cast<size_t>(dk) * 8 + static_cast<size_t>(dk) * 128;
 }
 
 bool par_fits(int BH, int T, int dk, int dv, size_t ws_bytes) {
@@ -728,6 +750,8 @@ cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     p.xs = w;
     w += units * a.dk * a.dv * 2;
     p.zs = reinterpret_cast<float*>(w);
+    w += units * a.dk * sizeof(float);
+    p.kh = w;
     p.BH = a.BH;
     p.T = a.T;
     p.nch = static_cast<int>(nch);

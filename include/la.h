@@ -48,12 +48,15 @@
  * resident on the device). The library never frees or retains them after a
  * call returns. la_create allocates the handle, one device status word and a
  * fixed workspace; la_destroy frees all three. The chunked prefill uses the
- * workspace for segment summaries when B*H is too small to fill the GPU
- * (LA_NORM_ELU1, LA_GLA: (SM count) x (d_k*d_v + d_k) floats) and, for
+ * workspace for the per-chunk states of the three-phase form (LA_NORM_ELU1,
+ * LA_GLA: up to 128 chunks per sequence-head, at most 48 MB; a call whose
+ * states do not fit takes the sequential kernel instead), for segment
+ * summaries when B*H is too small to fill the GPU ((SM count) x
+ * (d_k*d_v + d_k) floats) and, for
  * LA_GDN, for the fp32 states of a group of G = min(B*H, 32) sequence-heads
  * plus two windows of 16 chunks of per-chunk intermediates
  * (G*d_k*d_v*4 + 2*G*16*((d_k+d_v)*128 + 8704) bytes; 44.5 MB at
- * G = 32, d_k = d_v = 128). The larger of the two is allocated when the
+ * G = 32, d_k = d_v = 128). The largest of these is allocated when the
  * configuration can take the tensor-core path (bf16, d_k, d_v in {64, 128}).
  * Calls that overlap on the GPU through the same handle (different streams)
  * would share that workspace: serialize them.
