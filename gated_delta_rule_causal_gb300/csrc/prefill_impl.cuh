@@ -21,9 +21,9 @@
 // exp(G_t), L = causal mask including the diagonal):
 //
 //  norm / gla ("Linear attention and Hyena" 11.2-11.3, secondary rescaling):
-//    q~_t = phi(q_t) * Gam_t,  k~_j = phi(k_j) / Gam_j,  k^_j = phi(k_j) * Gam_C / Gam_j
+//    q~_t = phi(q_t) * Gam_t,  k~_j = phi(k_j) / Gam_j
 //    O    = Q~ X_0^T + (L o Q~ K~^T) V
-//    X    = diag-cols(Gam_C) X_0 + V^T K^
+//    X    = diag-cols(Gam_C) (X_0 + V^T K~)
 //    norm adds den_t = q~_t . z_0 + sum_{j<=t} q~_t . k~_j, o_t = num_t / den_t.
 //
 // Tail chunks (T not a multiple of 64): TMA zero-fills rows past the end.
@@ -76,13 +76,14 @@ struct Layout {
     static constexpr uint32_t G_BYTES = (VAR == kGla) ? C * DK * 4 : 0;
     static constexpr uint32_t STAGE = QK_BYTES + V_BYTES + G_BYTES;
     static constexpr uint32_t TX_BYTES = 2 * KA * 8192 + V_BYTES + G_BYTES;
-    static constexpr uint32_t OFF_SS = 2 * STAGE;                 // bf16 state [128 rows][DK]
-    static constexpr uint32_t OFF_PS = OFF_SS + KA * 16384;       // bf16 [64 t][64 j]
-    static constexpr uint32_t OFF_KH = OFF_PS + 8192;             // gla: k^ [64 j][DK]
-    static constexpr uint32_t KH_BYTES = (VAR == kGla) ? KA * 8192 : 0;
+    // bf16 P [64 t][64 j]. The P V product reads it as a 128-row A operand,
+    // so the 8 KB after it (rows 64-127, whose results are unused) must be
+    // shared memory of this CTA: the state tile follows.
+    static constexpr uint32_t OFF_PS = 2 * STAGE;
+    static constexpr uint32_t OFF_SS = OFF_PS + 8192;             // bf16 state [128 rows][DK]
     // output tile [64 t][DV] (norm: own buffer; gla: the current stage's gate
     // tile, free once the gates are consumed)
-    static constexpr uint32_t OFF_OT = OFF_KH + KH_BYTES;
+    static constexpr uint32_t OFF_OT = OFF_SS + KA * 16384;
     static constexpr uint32_t OT_BYTES = (VAR == kNorm) ? VA * 8192 : 0;
     static constexpr uint32_t OFF_MISC = OFF_OT + OT_BYTES;
     static constexpr uint32_t MISC_BYTES = (128 + 3 * 128 + 256) * 4;
@@ -188,7 +189,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     uint64_t* bar_test = bar_full + 3;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_full + 4);
 
-    const uint32_t aSS = sbase + L::OFF_SS, aPS = sbase + L::OFF_PS, aKH = sbase + L::OFF_KH;
+    const uint32_t aSS = sbase + L::OFF_SS, aPS = sbase + L::OFF_PS;
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
@@ -386,7 +387,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             __syncthreads();
         }
         if (VAR == kNorm && tid < DK) sDz[tid] = 0.f;
-        // q~ (block 0), k~ (block 1), k^ (gla: its own tile) in place, 8 channels per chunk.
+        // q~ (block 0), k~ (block 1) in place, 8 channels per chunk.
         {
             const float* gt = reinterpret_cast<const float*>(stg + L::QK_BYTES + L::V_BYTES);
 #pragma unroll
@@ -408,7 +409,6 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     k8[4] = b2.x; k8[5] = b2.y; k8[6] = b3.x; k8[7] = b3.y;
                 }
                 const bool valid = row < nvalid;
-                float kh[8];
                 float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
                 if constexpr (VAR == kGla) {
                     g0 = *reinterpret_cast<const float4*>(gt + row * DK + c0);
@@ -420,10 +420,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     float qq = phi_on ? elu1(q8[m]) : q8[m];
                     float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
                     if constexpr (VAR == kGla) {
-                        const float inv = __fdividef(1.f, gg[m]);
                         qq *= gg[m];
-                        kh[m] = kv * sGC[c0 + m] * inv;
-                        kv *= inv;
+                        kv *= __fdividef(1.f, gg[m]);
                     }
                     q8[m] = qq;
                     k8[m] = kv;
@@ -432,13 +430,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                              pack_bf16(q8[6], q8[7]));
                 st_shared_v4(ka, pack_bf16(k8[0], k8[1]), pack_bf16(k8[2], k8[3]), pack_bf16(k8[4], k8[5]),
                              pack_bf16(k8[6], k8[7]));
-                if constexpr (VAR == kGla)
-                    st_shared_v4(aKH + a * 8192 + off, pack_bf16(kh[0], kh[1]), pack_bf16(kh[2], kh[3]),
-                                 pack_bf16(kh[4], kh[5]), pack_bf16(kh[6], kh[7]));
             }
         }
         publish();
-        // ---- P = Q~ K~^T ;  O = Q~ X0^T ;  dX = V^T K^ -----------------------
+        // ---- P = Q~ K~^T ;  O = Q~ X0^T ;  dX = V^T K~ -----------------------
         if (tid == 0) {
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
@@ -448,11 +443,9 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                             ID_128xDV_KK, kk > 0);
             }
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bdesc = (VAR == kGla) ? mnmaj(aKH + kk * 2048, 8192)
-                                                     : mnmaj(aQK + 8192 + kk * 2048, 16384);
-                mma_bf16_ss(tmem + L::COL_S, mnmaj(aV + kk * 2048, v_lbo), bdesc, ID_128xDK_MM, kk > 0);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + L::COL_S, mnmaj(aV + kk * 2048, v_lbo), mnmaj(aQK + 8192 + kk * 2048, 16384),
+                            ID_128xDK_MM, kk > 0);
             mma_commit(bar_mma);
         }
         if constexpr (VAR == kNorm) {
@@ -509,8 +502,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float dec = (VAR == kGla) ? sGC[hh * DKH + 32 * b + i] : 1.f;
-                    st[32 * b + i] = dec * st[32 * b + i] + x[i];
+                    if constexpr (VAR == kGla)
+                        st[32 * b + i] = sGC[hh * DKH + 32 * b + i] * (st[32 * b + i] + x[i]);
+                    else
+                        st[32 * b + i] += x[i];
                 }
             }
             publish_state();
