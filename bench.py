@@ -369,6 +369,9 @@ def gpu_arm(args):
     uuid = str(getattr(props, "uuid", "")) or None
     pk = peaks()
     w = W.BY_NAME[args.workload] if args.workload else HEADLINE
+    if w.decode_steps:
+        raise SystemExit(f"{w.name} is a decode workload: it is measured in the suite entries of the default run "
+                         "(or alone with --only-kernel)")
 
     sampler = ClockSampler(uuid)
     sampler.start()

@@ -8,7 +8,12 @@
 // ("Linear Attention" concept page, gated delta rule; "Beyond attention"
 // 18.2). Rows are independent, so warps take units of rows of any head.
 // Each lane holds 4 consecutive columns (one 16-byte vector) of a row, and
-// the two row dot products are reduced with warp shuffles.
+// the two row dot products are reduced with warp shuffles. Every load of a
+// unit (its state rows, and the head's q, k, v, g, beta) is issued before the
+// first one is used, so a unit costs one trip to memory; the grid is sized
+// to the CTAs that are resident at once, and consecutive steps chain with
+// programmatic dependent launch so that one step's dispatch overlaps the
+// previous step's tail.
 //
 // Normalized / gated variants (state S [d_k, d_v]): each row i of S is
 // scaled (gla: gamma_i; norm: 1), gets phi(k_i) v added, and contributes
@@ -18,6 +23,8 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "launch.cuh"
+#include "ptx.cuh"
 
 namespace la {
 namespace {
@@ -87,16 +94,15 @@ __global__ void __launch_bounds__(kGdnThreads) decode_gdn_kernel(FwdArgs a) {
     IO* out = static_cast<IO*>(a.out);
     const size_t ssz = static_cast<size_t>(DK) * dv;
 
+    griddep_launch_dependents();
+    griddep_wait();   // the previous step's state is complete
     for (long long u = warp0; u < units; u += nwarps) {
         const int h = static_cast<int>(u / uph);
         const int r0 = static_cast<int>(u % uph) * R;
-        const float4 k4 = ld4(k + static_cast<size_t>(h) * DK + 4 * cl);
-        const float4 q4 = ld4(q + static_cast<size_t>(h) * DK + 4 * cl);
-        const float g = __ldg(a.gate + h), b = __ldg(a.beta + h);
-        const float kq = group_sum<LPR>(dot4(k4, q4));
         const float* sin = a.state_in ? a.state_in + h * ssz : nullptr;
         float* sout = a.state_out + h * ssz;
         float4 S[kGdnPasses];
+        float vr[kGdnPasses];
 #pragma unroll
         for (int p = 0; p < kGdnPasses; ++p) {
             const int row = r0 + p * RPP + sub;
@@ -106,11 +112,19 @@ __global__ void __launch_bounds__(kGdnThreads) decode_gdn_kernel(FwdArgs a) {
 #pragma unroll
         for (int p = 0; p < kGdnPasses; ++p) {
             const int row = r0 + p * RPP + sub;
+            vr[p] = row < dv ? ld1(v + static_cast<size_t>(h) * dv + row) : 0.f;
+        }
+        const float4 k4 = ld4(k + static_cast<size_t>(h) * DK + 4 * cl);
+        const float4 q4 = ld4(q + static_cast<size_t>(h) * DK + 4 * cl);
+        const float g = __ldg(a.gate + h), b = __ldg(a.beta + h);
+        const float kq = group_sum<LPR>(dot4(k4, q4));
+#pragma unroll
+        for (int p = 0; p < kGdnPasses; ++p) {
+            const int row = r0 + p * RPP + sub;
             const float sk = group_sum<LPR>(dot4(S[p], k4));
             const float sq = group_sum<LPR>(dot4(S[p], q4));
             if (row < dv) {
-                const float vi = ld1(v + static_cast<size_t>(h) * dv + row);
-                const float ui = b * (vi - g * sk);
+                const float ui = b * (vr[p] - g * sk);
                 float4 n;
                 n.x = g * S[p].x + ui * k4.x;
                 n.y = g * S[p].y + ui * k4.y;
@@ -213,17 +227,29 @@ __global__ void __launch_bounds__(kColThreads) decode_cols_kernel(FwdArgs a) {
     }
 }
 
+template <int DK, typename IO>
+cudaError_t launch_gdn_dk(const FwdArgs& a, cudaStream_t s) {
+    // persistent: as many CTAs as are resident at once (cached per kernel)
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_gdn_kernel<DK, IO>, kGdnThreads, 0) != cudaSuccess ||
+            n < 1)
+            n = 1;
+        per_sm = n;
+    }
+    return launch_pdl(decode_gdn_kernel<DK, IO>, static_cast<unsigned>(a.sm_count * per_sm), kGdnThreads, 0, s, a);
+}
+
 template <typename IO>
 cudaError_t launch_gdn(const FwdArgs& a, cudaStream_t s) {
-    int blocks = a.sm_count * 8;
     switch (a.dk) {
-        case 16: decode_gdn_kernel<16, IO><<<blocks, kGdnThreads, 0, s>>>(a); break;
-        case 32: decode_gdn_kernel<32, IO><<<blocks, kGdnThreads, 0, s>>>(a); break;
-        case 64: decode_gdn_kernel<64, IO><<<blocks, kGdnThreads, 0, s>>>(a); break;
-        case 128: decode_gdn_kernel<128, IO><<<blocks, kGdnThreads, 0, s>>>(a); break;
+        case 16: return launch_gdn_dk<16, IO>(a, s);
+        case 32: return launch_gdn_dk<32, IO>(a, s);
+        case 64: return launch_gdn_dk<64, IO>(a, s);
+        case 128: return launch_gdn_dk<128, IO>(a, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 template <int VAR, int DK, typename IO>

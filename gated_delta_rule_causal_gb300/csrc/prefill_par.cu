@@ -26,6 +26,7 @@
 // (fp32 dX, bf16 states) stay in L2 between the phases.
 #include "prefill.h"
 #include "prefill_impl.cuh"
+#include "launch.cuh"
 
 namespace la {
 namespace par {
@@ -653,24 +654,6 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
     if (status_bits && tid == 0) atomicOr(p.status, status_bits);
-}
-
-// Launch with programmatic stream serialization: the kernel may be
-// dispatched while the previous one in the stream finishes; it waits in
-// griddep_wait() before touching shared data.
-template <typename Kern, typename... Args>
-cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 // CTAs of a persistent kernel that fit on one SM next to each other
