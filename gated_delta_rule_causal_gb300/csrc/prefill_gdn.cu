@@ -43,6 +43,7 @@
 // state untouched; no output row past T is written.
 #include "prefill.h"
 #include "prefill_impl.cuh"
+#include "launch.cuh"
 
 namespace la {
 namespace gdn {
@@ -142,6 +143,7 @@ struct Params {
     int chain_c0, chain_n, chain_buf, chain_first, chain_last;
     int prep_c0, prep_n, prep_buf;
     int n_chain;            // CTAs [0, n_chain) walk the chain, the others prepare
+    int early;              // prep CTAs may read the inputs before the previous launch completes
     unsigned flags;
     int* status;
 };
@@ -200,6 +202,10 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // The previous window launch has written this window's slots and the
+    // state; only then may the next launch be dispatched.
+    griddep_wait();
+    griddep_launch_dependents();
 
     int status_bits = 0;
     bool failed = false;
@@ -545,6 +551,18 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // Programmatic dependent launch. The first launch of a call waits for
+    // the kernels before it at once (they may have produced the inputs). A
+    // later launch may only be dispatched after every CTA of the previous one
+    // passed this point, so its inputs are complete; it computes its first
+    // unit while the previous launch finishes and waits only before its
+    // first write to the slot ring, whose buffer that launch's chain reads.
+    bool waited = false;
+    if (!p.early) {
+        griddep_wait();
+        griddep_launch_dependents();
+        waited = true;
+    }
 
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
         const bool ok = mbar_wait(b, parity, kWaitLimitNs);
@@ -788,6 +806,11 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         fence_proxy_async_smem();
         tc_fence_before();
         sync_conv();
+        if (!waited) {
+            griddep_wait();
+            griddep_launch_dependents();
+            waited = true;
+        }
         if (tid == 0) {
             uint8_t* dst = p.ws_slot + (static_cast<size_t>(p.prep_buf * p.G + unit_g(u)) * p.W + unit_i(u)) * S::BYTES;
             bulk_store(dst, aOut, S::BYTES);
@@ -830,7 +853,17 @@ cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int W, cudaStream
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nch = (a.T + C - 1) / C;
-    const int NW = (nch + W - 1) / W;
+    // Windows of 2, 4, 8 chunks, then W: the chain starts after a short
+    // prep-only first launch, and the prep of each window fits in the walk
+    // of the previous one.
+    int wstart[130];
+    int NW = 0;
+    for (int c0 = 0, w = 2; c0 < nch; c0 += w, w *= 2) {
+        if (w > W) w = W;
+        wstart[NW++] = c0;
+        if (NW == 129) return cudaErrorInvalidValue;
+    }
+    wstart[NW] = nch;
     const size_t state_bytes = static_cast<size_t>(G) * DK * DV * sizeof(float);
     Params p;
     p.gate = a.gate;
@@ -851,17 +884,18 @@ cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int W, cudaStream
             p.chain_n = 0;
             p.prep_n = 0;
             if (j >= 1) {
-                p.chain_c0 = (j - 1) * W;
-                p.chain_n = nch - p.chain_c0 < W ? nch - p.chain_c0 : W;
+                p.chain_c0 = wstart[j - 1];
+                p.chain_n = wstart[j] - wstart[j - 1];
                 p.chain_buf = (j - 1) & 1;
                 p.chain_first = (j == 1);
                 p.chain_last = (j == NW);
             }
             if (j < NW) {
-                p.prep_c0 = j * W;
-                p.prep_n = nch - p.prep_c0 < W ? nch - p.prep_c0 : W;
+                p.prep_c0 = wstart[j];
+                p.prep_n = wstart[j + 1] - wstart[j];
                 p.prep_buf = j & 1;
             }
+            p.early = (j >= 1);
             p.n_chain = p.chain_n > 0 ? p.G : 0;
             int n_prep = 0;
             if (p.prep_n > 0) {
@@ -869,8 +903,7 @@ cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int W, cudaStream
                 n_prep = a.sm_count - p.n_chain > 0 ? a.sm_count - p.n_chain : a.sm_count;
                 if (n_prep > units) n_prep = units;
             }
-            kern<<<p.n_chain + n_prep, kThreads, smem, s>>>(m.q, m.k, m.v, p);
-            e = cudaGetLastError();
+            e = launch_pdl(kern, static_cast<unsigned>(p.n_chain + n_prep), kThreads, smem, s, m.q, m.k, m.v, p);
             if (e != cudaSuccess) return e;
             if (a.nlaunch) ++*a.nlaunch;
         }

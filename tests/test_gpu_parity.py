@@ -336,8 +336,8 @@ def test_rejected_calls_do_not_launch():
     ("gla", 200, 0, 64, 3),
     ("norm", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 2),      # segment summaries + chunk kernel
     ("norm", 100, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),      # too short to split
-    ("gdn", 200, 0, 64, 2),                                  # one window of 4 chunks, + 1
-    ("gdn", 64 * 40, 0, 64, 4),                              # windows of 16: 3, + 1
+    ("gdn", 200, 0, 64, 3),                                  # windows of 2 and 2 chunks, + 1
+    ("gdn", 64 * 40, 0, 64, 6),                              # windows of 2, 4, 8, 16, 10, + 1
     ("gla", 200, 0, 1, 1),                                   # the recurrent kernel
 ])
 def test_launch_counts(variant, T, flags, chunk, expect):
