@@ -212,3 +212,76 @@ def draw_decode_step(w: Workload, step: int, seed: int = 0) -> Inputs:
 def small(w: Workload, **kw) -> Workload:
     """A reduced copy of a workload (same distributions), for fast parity."""
     return w.with_(name=w.name + "_small", **kw)
+
+
+# --------------------------------------------------------------------------
+# associative-recall probe
+# --------------------------------------------------------------------------
+
+@dataclass
+class Probe:
+    """A recall probe as one call's inputs: K writes (a second K writes of new
+    values under the same keys when `rewrite`), then K reads, one per key.
+    The output at read token `read0 + j` is the recall for key j; `target[j]`
+    is the value most recently written under it."""
+    inputs: Inputs
+    target: np.ndarray    # [K, dv] float64 (exact: one-hot values)
+    read0: int
+    K: int
+    variant: str
+    identity_phi: bool
+
+
+def recall_probe(variant: str, K: int, dk: int, dv: int, keys: str = "random", rewrite: bool = False,
+                 io: str = "fp32", seed: int = 0) -> Probe:
+    """Store K key-value bindings and read each back through one call.
+
+    * Keys: "random" unit vectors (N(0,1) rows normalized in float64) or
+      "orthonormal" ones (K <= dk; columns of a QR factor of a Gaussian).
+    * Values: one-hot, v_j = e_j (orthonormal; dv >= K); rewritten values
+      are e_{(j+1) mod K}.
+    * variant "gla": additive memory (S += k v^T), i.e. the per-channel gated
+      form with gate 1 and no feature map; reads carry v = 0, so they write
+      nothing. variant "gdn": the delta rule with beta = 1 and g = 1 on
+      writes, beta = 0 on reads.
+    * q is the key being read on read tokens and 0 elsewhere.
+    B = H = 1. Values and keys are rounded to `io` like any other input.
+    """
+    if variant not in ("gla", "gdn"):
+        raise ValueError("the probe runs the additive (gla) or delta (gdn) rule")
+    if dv < K:
+        raise ValueError("one-hot values need dv >= K")
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed)))
+    if keys == "random":
+        kk = _unit_rows(rng.standard_normal((K, dk)))
+    elif keys == "orthonormal":
+        if K > dk:
+            raise ValueError("at most dk orthonormal keys")
+        qm, _ = np.linalg.qr(rng.standard_normal((dk, dk)))
+        kk = qm[:, :K].T.copy()
+    else:
+        raise ValueError(f"unknown key kind {keys!r}")
+    eye = np.eye(dv)
+    old = eye[:K]
+    new = eye[[(j + 1) % K for j in range(K)]]
+    nw = 2 * K if rewrite else K
+    T = nw + K
+    q = np.zeros((T, dk))
+    k = np.zeros((T, dk))
+    v = np.zeros((T, dv))
+    k[:K], v[:K] = kk, old
+    if rewrite:
+        k[K:2 * K], v[K:2 * K] = kk, new
+    q[nw:], k[nw:] = kk, kk
+    lead = (1, 1)
+    gate = beta = None
+    if variant == "gla":
+        gate = np.ones(lead + (T, dk), np.float32)
+    else:
+        gate = np.ones(lead + (T,), np.float32)
+        beta = np.zeros(lead + (T,), np.float32)
+        beta[..., :nw] = 1.0
+    inp = Inputs(q=round_io(q.reshape(lead + (T, dk)), io), k=round_io(k.reshape(lead + (T, dk)), io),
+                 v=round_io(v.reshape(lead + (T, dv)), io), gate=gate, beta=beta, state=None)
+    return Probe(inputs=inp, target=new if rewrite else old, read0=nw, K=K, variant=variant,
+                 identity_phi=(variant == "gla"))
