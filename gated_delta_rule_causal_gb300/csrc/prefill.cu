@@ -63,6 +63,8 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     // to fill the GPU (one CTA per segment, one CTA per SM).
     p.nseg = 1;
     p.seg_len = p.nchunks;
+    p.nsub = 0;
+    p.sub_len = p.nchunks;
     p.scratch = a.workspace;
     if (a.workspace && a.BH < a.sm_count && p.nchunks >= 4) {
         int nseg = a.sm_count / a.BH;
@@ -72,6 +74,15 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
         if (nseg > 1) {
             p.seg_len = (p.nchunks + nseg - 1) / nseg;
             p.nseg = (p.nchunks + p.seg_len - 1) / p.seg_len;
+            // Summary runs: cut each segment before the last into m runs while
+            // the runs still fit one wave of CTAs and the workspace.
+            int m = 1;
+            const size_t nbefore = static_cast<size_t>(a.BH) * (p.nseg - 1);
+            while (p.seg_len % (2 * m) == 0 && p.seg_len / (2 * m) >= 2 &&
+                   nbefore * 2 * m <= static_cast<size_t>(a.sm_count) && nbefore * 2 * m * blk <= a.ws_bytes)
+                m *= 2;
+            p.sub_len = p.seg_len / m;
+            p.nsub = (p.nseg - 1) * m;
         }
     }
     *what = "chunked prefill launch";

@@ -15,7 +15,7 @@ cudaError_t run(const Maps& m, const Params& p, int BH, cudaStream_t s) {
         auto sk = summary_kernel<kGla, DK, DV>;
         e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SL::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        sk<<<BH * (p.nseg - 1), kThreads, SL::SMEM_ALLOC, s>>>(m.k, m.v, m.g, p);
+        sk<<<BH * p.nsub, kThreads, SL::SMEM_ALLOC, s>>>(m.k, m.v, m.g, p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -57,12 +57,16 @@ struct Params {
     unsigned flags;
     int* status;
     // Segments (norm / gla): the chunks of each sequence are split into nseg
-    // runs of seg_len chunks, each run on its own CTA. scratch holds, for
-    // every (b,h) and every segment but the last, the state that segment
-    // produces from a zero start: X [DV][DK] followed by DK floats (gla: the
-    // segment's per-channel decay; norm: its sum of phi(k)).
+    // runs of seg_len chunks, each run on its own CTA. The chunks before the
+    // last segment are also cut into nsub summary runs of sub_len chunks
+    // (sub_len divides seg_len). scratch holds, for every (b,h) and every
+    // summary run, the state that run produces from a zero start: X [DV][DK]
+    // followed by DK floats (gla: the run's per-channel decay; norm: its sum
+    // of phi(k)).
     int nseg;
     int seg_len;
+    int nsub;
+    int sub_len;
     float* scratch;
 };
 
@@ -217,11 +221,13 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         if (own && sin) x = sin[static_cast<size_t>(c) * DV + r];
         st[i] = x;
     }
-    // Later segments start from the states of the earlier ones: X = D_s' X + X_s'.
+    // Later segments start from the states of the summary runs before them,
+    // in order: X = D_u X + X_u.
     const size_t sblk = static_cast<size_t>(DV) * DK + DK;
-    const float* sc0 = p.scratch + static_cast<size_t>(bh) * (p.nseg - 1) * sblk;
+    const float* sc0 = p.scratch + static_cast<size_t>(bh) * p.nsub * sblk;
+    const int nprev = seg * (p.seg_len / p.sub_len);
     if (own) {
-        for (int s2 = 0; s2 < seg; ++s2) {
+        for (int s2 = 0; s2 < nprev; ++s2) {
             const float* xs = sc0 + s2 * sblk + static_cast<size_t>(r) * DK + hh * DKH;
             const float* ds = sc0 + s2 * sblk + static_cast<size_t>(DV) * DK + hh * DKH;
 #pragma unroll
@@ -246,7 +252,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     publish_state();
     if (VAR == kNorm && tid < DK) {
         float z = sin ? sin[static_cast<size_t>(DK) * DV + tid] : 0.f;
-        for (int s2 = 0; s2 < seg; ++s2) z += sc0[s2 * sblk + static_cast<size_t>(DV) * DK + tid];
+        for (int s2 = 0; s2 < nprev; ++s2) z += sc0[s2 * sblk + static_cast<size_t>(DV) * DK + tid];
         sZ[tid] = z;
     }
 
@@ -556,12 +562,12 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
 // ---------------------------------------------------------------------------
 // Segment summaries (normalized and per-channel gated variants).
 //
-// For segment s of sequence-head bh (every segment but the last), compute the
-// state the segment's chunks produce from a zero state,
+// For summary run u of sequence-head bh (the runs tile every segment but the
+// last), compute the state the run's chunks produce from a zero state,
 //   X_s = sum_c (prod_{c' > c} Gam_C(c')) o (V_c^T K^_c),
 // its per-channel decay D_s = prod_c Gam_C(c) (gla) and its sum of phi(k)
 // (norm), and store them in p.scratch. The chunks are walked last to first so
-// the decay to the segment end folds into K^ (column scaling commutes with
+// the decay to the run's end folds into K^ (column scaling commutes with
 // V^T K^), and every chunk accumulates into one TMEM accumulator.
 // ---------------------------------------------------------------------------
 template <int VAR, int DK, int DV>
@@ -594,14 +600,14 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     uint8_t* sm = smem_raw + (sbase - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = 32 * (warp & 3) + lane, hh = warp >> 2;
-    const int nsum = p.nseg - 1;
+    const int nsum = p.nsub;
     const int bh = blockIdx.x / nsum, seg = blockIdx.x % nsum;
     const int T = p.T;
-    const int c_begin = seg * p.seg_len;
-    const int nloc = p.seg_len;   // segments before the last one are full
+    const int c_begin = seg * p.sub_len;
+    const int nloc = p.sub_len;   // runs lie before the last segment, so they are full
     const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
 
-    float* sR = reinterpret_cast<float*>(sm + L::OFF_MISC);   // decay from the chunk end to the segment end
+    float* sR = reinterpret_cast<float*>(sm + L::OFF_MISC);   // decay from the chunk end to the run's end
     float* sGC = sR + 128;
     float* sPart = sGC + 128;
     float* sZ = sPart + 256;
