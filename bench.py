@@ -256,6 +256,11 @@ def time_steps(runner, steps: int, warmup: int, torch, dist=None):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    # Hold the stream for ~0.5 ms before the timed region so that the host
+    # has queued the first steps when it opens: the device clock then
+    # measures the device's work, not the host's head start (the host-side
+    # cost of a call is in the e2e figure).
+    torch.cuda._sleep(1_000_000)
     t0.record(stream)
     for a, b in evs:
         a.record(stream)
