@@ -10,8 +10,9 @@ pages state are equal to the recurrence (masked-parallel, literal, unrolled).
 The tests use them to pin the C recurrences.
 
 Arrays use the operator's layouts: q,k [B,H,T,dk]; v [B,H,T,dv]; gla gate
-[B,H,T,dk]; gdn gate/beta [B,H,T]; state per (b,h): norm S[dk,dv] then
-z[dk]; gla S[dk,dv]; gdn S[dv,dk].
+[B,H,T,dk]; gdn gate/beta [B,H,T]; norm_decay gate [B,H] (one decay per
+sequence-head); state per (b,h): norm and norm_decay S[dk,dv] then z[dk];
+gla S[dk,dv]; gdn S[dv,dk].
 """
 from __future__ import annotations
 
@@ -58,9 +59,10 @@ def _load():
             P = ctypes.POINTER(ctypes.c_double)
             i = ctypes.c_int
             lib.la_oracle_norm.argtypes = [i, i, i, i, P, P, P, P, P, P, P, i]
+            lib.la_oracle_norm_decay.argtypes = [i, i, i, i, P, P, P, P, P, P, P, P, i]
             lib.la_oracle_gla.argtypes = [i, i, i, i, P, P, P, P, P, P, P, i, i]
             lib.la_oracle_gdn.argtypes = [i, i, i, i, P, P, P, P, P, P, P, P, i]
-            for f in (lib.la_oracle_norm, lib.la_oracle_gla, lib.la_oracle_gdn):
+            for f in (lib.la_oracle_norm, lib.la_oracle_norm_decay, lib.la_oracle_gla, lib.la_oracle_gdn):
                 f.restype = ctypes.c_int
             lib.la_oracle_threads_available.restype = ctypes.c_int
             _lib = lib
@@ -87,11 +89,11 @@ def _f64(a):
 class Result:
     o: np.ndarray            # [B,H,T,dv]
     state: np.ndarray        # [B,H,*] flat per-(b,h) state (see module doc)
-    den: np.ndarray | None   # norm only: [B,H,T] denominators phi(q)^T z
+    den: np.ndarray | None   # norm, norm_decay: [B,H,T] denominators phi(q)^T z
 
 
 def state_size(variant: str, dk: int, dv: int) -> int:
-    return dk * dv + (dk if variant == "norm" else 0)
+    return dk * dv + (dk if variant in ("norm", "norm_decay") else 0)
 
 
 def run(variant: str, q, k, v, gate=None, beta=None, state_in=None,
@@ -111,6 +113,14 @@ def run(variant: str, q, k, v, gate=None, beta=None, state_in=None,
         den = np.empty((B, H, T), dtype=np.float64)
         rc = lib.la_oracle_norm(BH, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(sin),
                                 _ptr(o), _ptr(sout), _ptr(den), nthreads)
+        if rc == 2:
+            raise FloatingPointError("normalizer denominator not positive")
+    elif variant == "norm_decay":
+        gm = _f64(gate)
+        assert gm.shape == (B, H)
+        den = np.empty((B, H, T), dtype=np.float64)
+        rc = lib.la_oracle_norm_decay(BH, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(gm), _ptr(sin),
+                                      _ptr(o), _ptr(sout), _ptr(den), nthreads)
         if rc == 2:
             raise FloatingPointError("normalizer denominator not positive")
     elif variant == "gla":

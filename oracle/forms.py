@@ -37,6 +37,26 @@ def norm_masked_parallel(q, k, v):
     return num / den[:, None], Kp.T @ v, Kp.sum(axis=0), den
 
 
+def norm_decay_masked_parallel(q, k, v, gamma: float):
+    """Normalized elu+1 attention with one fixed decay, as one masked product.
+
+    "Linear attention and recurrent memory", Fixed decay versus an
+    input-dependent gate, and its Pitfalls (the parallel form weights the
+    pair (t, i) by gamma^(t-i), in the numerator and the normalizer alike):
+    A_ti = gamma^(t-i) phi(q_t) . phi(k_i) for i <= t, num = A V, den = A 1.
+    The final state is S_T = sum_i gamma^(T-1-i) phi(k_i) v_i^T and z_T the
+    same sum of phi(k_i). Returns (o, S_T, z_T, den).
+    """
+    Qp, Kp = elu1(q), elu1(k)
+    T = q.shape[0]
+    t = np.arange(T, dtype=np.float64)
+    W = np.where(t[:, None] >= t[None, :], float(gamma) ** np.maximum(t[:, None] - t[None, :], 0.0), 0.0)
+    A = W * (Qp @ Kp.T)
+    den = A.sum(axis=1)
+    w_end = float(gamma) ** (T - 1 - t)
+    return (A @ v) / den[:, None], (Kp * w_end[:, None]).T @ v, (Kp * w_end[:, None]).sum(axis=0), den
+
+
 def gla_masked(q, k, v, gamma, identity_phi: bool = False):
     """Per-channel gated attention as a masked sum.
 

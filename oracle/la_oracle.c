@@ -12,6 +12,7 @@
  * Layouts (contiguous, row-major), with BH = batch*heads:
  *   q, k   [BH, T, dk]      v, o [BH, T, dv]
  *   norm:  state = S [dk, dv] followed by z [dk], per sequence
+ *   norm with decay: gamma [BH]; state as norm
  *   gla:   gamma [BH, T, dk]; state = S [dk, dv] per sequence
  *   gdn:   g, beta [BH, T];   state = S [dv, dk] per sequence
  * A NULL state_in means a zero initial state; a NULL state_out skips the
@@ -85,6 +86,63 @@ int la_oracle_norm(int BH, int T, int dk, int dv,
             for (int i = 0; i < dk; ++i) {
                 for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += f[i] * vt[j];
                 z[i] += f[i];
+            }
+            for (int i = 0; i < dk; ++i) p[i] = phi(qt[i]);
+            double d = 0.0;
+            for (int i = 0; i < dk; ++i) d += p[i] * z[i];
+            for (int j = 0; j < dv; ++j) num[j] = 0.0;
+            for (int i = 0; i < dk; ++i)
+                for (int j = 0; j < dv; ++j) num[j] += p[i] * S[(size_t)i * dv + j];
+            if (!(d > 0.0)) bad = 1;
+            double* ot = o + ((size_t)bh * T + t) * dv;
+            for (int j = 0; j < dv; ++j) ot[j] = num[j] / d;
+            if (den_out) den_out[(size_t)bh * T + t] = d;
+        }
+        if (state_out) memcpy(state_out + bh * sz, S, sizeof(double) * sz);
+        free(S);
+    }
+    if (oom) return 1;
+    return bad ? 2 : 0;
+}
+
+/*
+ * (a') Normalized kernel linear attention with a fixed decay per sequence-head,
+ * update first:
+ *   S_t = gamma S_{t-1} + phi(k_t) v_t^T,  z_t = gamma z_{t-1} + phi(k_t),
+ *   o_t = phi(q_t)^T S_t / phi(q_t)^T z_t.
+ * "Linear attention and recurrent memory", Fixed decay versus an
+ * input-dependent gate (one scalar per head decays both the matrix state and
+ * the normalizer). gamma [BH]; gamma = 1 is variant (a).
+ */
+int la_oracle_norm_decay(int BH, int T, int dk, int dv,
+                         const double* q, const double* k, const double* v, const double* gamma,
+                         const double* state_in, double* o, double* state_out,
+                         double* den_out, int nthreads) {
+    int bad = 0, oom = 0;
+    int nt = set_threads(nthreads);
+    (void)nt;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt) reduction(|:bad, oom)
+#endif
+    for (int bh = 0; bh < BH; ++bh) {
+        double* S = (double*)malloc(sizeof(double) * ((size_t)dk * dv + dk + dk + dk + dv));
+        if (!S) { oom = 1; continue; }
+        double* z = S + (size_t)dk * dv;
+        double* f = z + dk;
+        double* p = f + dk;
+        double* num = p + dk;
+        const size_t sz = (size_t)dk * dv + dk;
+        const double g = gamma[bh];
+        if (state_in) memcpy(S, state_in + bh * sz, sizeof(double) * sz);
+        else memset(S, 0, sizeof(double) * sz);
+        for (int t = 0; t < T; ++t) {
+            const double* kt = k + ((size_t)bh * T + t) * dk;
+            const double* qt = q + ((size_t)bh * T + t) * dk;
+            const double* vt = v + ((size_t)bh * T + t) * dv;
+            for (int i = 0; i < dk; ++i) f[i] = phi(kt[i]);
+            for (int i = 0; i < dk; ++i) {
+                for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] = g * S[(size_t)i * dv + j] + f[i] * vt[j];
+                z[i] = g * z[i] + f[i];
             }
             for (int i = 0; i < dk; ++i) p[i] = phi(qt[i]);
             double d = 0.0;

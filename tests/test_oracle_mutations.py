@@ -24,6 +24,13 @@ MUTANTS = {
         "for (int i = 0; i < dk; ++i) p[i] = phi(qt[i]);"
         " for (int i = 0; i < dk; ++i) { for (int j = 0; j < dv; ++j)"
         " S[(size_t)i * dv + j] -= f[i] * vt[j]; z[i] -= f[i]; }"),
+    "decay_misses_normalizer": ("z[i] = g * z[i] + f[i];", "z[i] = z[i] + f[i];"),
+    "decay_misses_state": (
+        "S[(size_t)i * dv + j] = g * S[(size_t)i * dv + j] + f[i] * vt[j];",
+        "S[(size_t)i * dv + j] = S[(size_t)i * dv + j] + f[i] * vt[j];"),
+    "decay_after_write": (
+        "S[(size_t)i * dv + j] = g * S[(size_t)i * dv + j] + f[i] * vt[j];",
+        "S[(size_t)i * dv + j] = g * (S[(size_t)i * dv + j] + f[i] * vt[j]);"),
     "gla_gate_after_write": (
         "S[(size_t)i * dv + j] = gt[i] * S[(size_t)i * dv + j] + f[i] * vt[j];",
         "S[(size_t)i * dv + j] = gt[i] * (S[(size_t)i * dv + j] + f[i] * vt[j]);"),

@@ -91,13 +91,15 @@ def test_norm_output_in_value_hull():
     assert np.all(o >= lo - 1e-12) and np.all(o <= hi + 1e-12)
 
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "norm_decay", "gla", "gdn"])
 def test_causality(variant):
     # Changing tokens after t leaves outputs up to t bit-identical.
     r = rng(3)
     T, d, t0 = 40, 8, 17
     q, k, v = (r.standard_normal((T, d)) for _ in range(3))
     gate = beta = None
+    if variant == "norm_decay":
+        gate = 0.9
     if variant == "gla":
         gate = sigmoid(r.standard_normal((T, d)) + 2)
     if variant == "gdn":
@@ -108,12 +110,62 @@ def test_causality(variant):
     q2[t0 + 1:] += 5.0
     k2[t0 + 1:] = -k2[t0 + 1:]
     v2[t0 + 1:] *= 3.0
-    g2 = None if gate is None else gate.copy()
-    if g2 is not None:
+    g2 = None if gate is None else np.array(gate, np.float64)
+    if g2 is not None and g2.ndim > 0:
         g2[t0 + 1:] = 0.5
     o2, _, _ = one(variant, q2, k2, v2, g2, beta)
     assert np.array_equal(o1[: t0 + 1], o2[: t0 + 1])
     assert not np.array_equal(o1[t0 + 1:], o2[t0 + 1:])
+
+
+# ------------------------------------------------------- (a') norm with decay
+
+@pytest.mark.parametrize("gamma", [0.5, 0.9, 0.995])
+@pytest.mark.parametrize("T", [64, 200])
+def test_norm_decay_recurrent_equals_masked_parallel(gamma, T):
+    # "Linear attention and recurrent memory", Fixed decay and its Pitfalls:
+    # the recurrence and the parallel form weighted by gamma^(t-i) agree,
+    # numerator and normalizer alike.
+    r = rng(int(T + 1000 * gamma))
+    q, k, v = r.standard_normal((T, 16)), r.standard_normal((T, 16)), r.standard_normal((T, 12))
+    o, st, den = one("norm_decay", q, k, v, gamma)
+    o_p, S_p, z_p, den_p = forms.norm_decay_masked_parallel(q, k, v, gamma)
+    S, z = oracle.split_norm_state(st, 16, 12)
+    assert np.max(np.abs(o - o_p)) <= 1e-12 * max(1.0, np.max(np.abs(o_p)))
+    assert np.max(np.abs(den - den_p) / den_p) <= 1e-12
+    assert np.max(np.abs(S - S_p)) <= 1e-12 * max(1.0, np.max(np.abs(S_p)))
+    assert np.max(np.abs(z - z_p)) <= 1e-12 * np.max(z_p)
+
+
+def test_norm_decay_one_is_undecayed():
+    # gamma = 1 is the undecayed form (the module's own reference check).
+    r = rng(41)
+    T = 90
+    q, k, v = (r.standard_normal((T, 8)) for _ in range(3))
+    o1, st1, den1 = one("norm_decay", q, k, v, 1.0)
+    o0, st0, den0 = one("norm", q, k, v)
+    assert np.max(np.abs(o1 - o0)) <= 1e-13 * max(1.0, np.max(np.abs(o0)))
+    assert np.max(np.abs(st1 - st0)) <= 1e-13 * max(1.0, np.max(np.abs(st0)))
+    assert np.max(np.abs(den1 - den0) / den0) <= 1e-13
+
+
+def test_norm_decay_constant_key_closed_form():
+    # One key repeated: every score phi(q_t).phi(k) is the same c_t, so
+    # o_t = sum_i gamma^(t-i) v_i / sum_i gamma^(t-i), den_t = c_t (1 - gamma^(t+1)) / (1 - gamma),
+    # z_T = phi(k) (1 - gamma^T) / (1 - gamma).
+    r = rng(42)
+    T, d, gamma = 30, 6, 0.8
+    k = np.tile(r.standard_normal(d), (T, 1))
+    q, v = r.standard_normal((T, d)), r.standard_normal((T, 3))
+    o, st, den = one("norm_decay", q, k, v, gamma)
+    t = np.arange(T)
+    W = np.where(t[:, None] >= t[None, :], gamma ** np.maximum(t[:, None] - t[None, :], 0), 0.0)
+    expect = (W @ v) / W.sum(axis=1, keepdims=True)
+    assert np.max(np.abs(o - expect)) <= 1e-13
+    c = forms.elu1(q) @ forms.elu1(k[0])
+    assert np.max(np.abs(den - c * (1 - gamma ** (t + 1)) / (1 - gamma)) / den) <= 1e-13
+    _, z = oracle.split_norm_state(st, d, 3)
+    assert np.max(np.abs(z - forms.elu1(k[0]) * (1 - gamma ** T) / (1 - gamma))) <= 1e-13 * np.max(z)
 
 
 # ----------------------------------------------------------------- (b) gla
@@ -314,19 +366,21 @@ def test_figure_18_2_delta_vs_additive():
 
 # ------------------------------------------------------ all: state passing
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "norm_decay", "gla", "gdn"])
 def test_split_continuation_equals_one_shot(variant):
     r = rng(16)
     T, dk, dv, T1 = 37, 8, 6, 15
     q, k, v = r.standard_normal((T, dk)), r.standard_normal((T, dk)), r.standard_normal((T, dv))
     gate = beta = None
+    if variant == "norm_decay":
+        gate = 0.93
     if variant == "gla":
         gate = sigmoid(r.standard_normal((T, dk)) + 2)
     if variant == "gdn":
         k = unit(k)
         gate, beta = sigmoid(r.standard_normal(T) + 3), sigmoid(r.standard_normal(T))
     o, st, _ = one(variant, q, k, v, gate, beta)
-    sl = lambda a, s: None if a is None else a[s]
+    sl = lambda a, s: None if a is None else (a if np.ndim(a) == 0 else a[s])
     a, b = slice(0, T1), slice(T1, T)
     o1, st1, _ = one(variant, q[a], k[a], v[a], sl(gate, a), sl(beta, a))
     o2, st2, _ = one(variant, q[b], k[b], v[b], sl(gate, b), sl(beta, b), state=st1)
