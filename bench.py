@@ -34,7 +34,7 @@ import numpy as np  # noqa: E402
 import workloads as W  # noqa: E402
 
 HEADLINE = W.NORM_B4H8_T2048_D64
-SUITE = (W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128, W.GDN_DECODE_N256H16_D128)
+SUITE = (W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128, W.GDN_DECODE_N256H16_D128, W.NORM_DECAY_B4H8_T2048_D64)
 C_FLOPS = 64   # chunk size the algorithmic FLOP count is quoted at
 
 
@@ -45,7 +45,7 @@ def io_bytes(w: W.Workload) -> int:
 
 
 def state_elems(w: W.Workload) -> int:
-    return w.dk * w.dv + (w.dk if w.variant == "norm" else 0)
+    return w.dk * w.dv + (w.dk if w.variant in ("norm", "norm_decay") else 0)
 
 
 def prefill_bytes(w: W.Workload) -> int:
@@ -56,13 +56,15 @@ def prefill_bytes(w: W.Workload) -> int:
         b += n * w.dk * 4
     elif w.variant == "gdn":
         b += n * 2 * 4
+    elif w.variant == "norm_decay":
+        b += w.B * w.H * 4
     return b + w.B * w.H * state_elems(w) * 4
 
 
 def prefill_flops(w: W.Workload) -> float:
     """Dense chunk contractions per sequence-head-token at C = 64."""
     C, dk, dv = C_FLOPS, w.dk, w.dv
-    if w.variant == "norm":
+    if w.variant in ("norm", "norm_decay"):
         per = 2 * C * (dk + dv + 1) + 4 * dk * (dv + 1)
     elif w.variant == "gla":
         per = 2 * C * (dk + dv) + 4 * dk * dv

@@ -19,14 +19,14 @@ import threading
 
 from ._build import LIB as LIB_PATH, build  # noqa: F401  (build() compiles in-tree)
 
-LA_NORM_ELU1, LA_GLA, LA_GDN = 0, 1, 2
+LA_NORM_ELU1, LA_GLA, LA_GDN, LA_NORM_DECAY = 0, 1, 2, 3
 LA_BF16, LA_FP32 = 0, 1
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(6)
 LA_FLAG_IDENTITY_PHI = 0x1
 LA_FLAG_SEQUENTIAL_CHUNKS = 0x2
 LA_FLAG_TEST_TIMEOUT = 0x100
 
-VARIANTS = {"norm": LA_NORM_ELU1, "gla": LA_GLA, "gdn": LA_GDN}
+VARIANTS = {"norm": LA_NORM_ELU1, "gla": LA_GLA, "gdn": LA_GDN, "norm_decay": LA_NORM_DECAY}
 ERRORS = {1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_MISALIGNED",
           4: "LA_ERR_CUDA", 5: "LA_ERR_TIMEOUT"}
 
@@ -137,8 +137,8 @@ def _stream_ptr(stream):
 
 
 def state_size(variant: str, d_k: int, d_v: int) -> int:
-    """fp32 elements of one sequence-head's state (norm appends z)."""
-    return d_k * d_v + (d_k if variant == "norm" else 0)
+    """fp32 elements of one sequence-head's state (norm and norm_decay append z)."""
+    return d_k * d_v + (d_k if variant in ("norm", "norm_decay") else 0)
 
 
 class Handle:
@@ -193,6 +193,8 @@ class Handle:
         self._expect("v", v, (B, H, T, self.d_v), self.dtype)
         if var == LA_GLA:
             self._expect("gate", gate, (B, H, T, self.d_k), torch.float32)
+        elif var == LA_NORM_DECAY:
+            self._expect("gate", gate, (B, H), torch.float32)
         elif var == LA_GDN:
             self._expect("gate", gate, (B, H, T), torch.float32)
             self._expect("beta", beta, (B, H, T), torch.float32)

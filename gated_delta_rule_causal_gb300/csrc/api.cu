@@ -12,6 +12,7 @@
 #include "../../include/la.h"
 #include "kernels.h"
 #include "prefill.h"
+#include "prefill.h"
 
 struct la_handle {
     la_config cfg;
@@ -53,20 +54,23 @@ struct DeviceGuard {
     }
 };
 
+bool valid_variant(int v) { return v == LA_NORM_ELU1 || v == LA_GLA || v == LA_GDN || v == LA_NORM_DECAY; }
+
 size_t state_elems(const la_config& c, int variant) {
-    return static_cast<size_t>(c.d_k) * c.d_v + (variant == LA_NORM_ELU1 ? c.d_k : 0);
+    return static_cast<size_t>(c.d_k) * c.d_v + ((variant == LA_NORM_ELU1 || variant == LA_NORM_DECAY) ? c.d_k : 0);
 }
 
 int check_common(la_handle* h, const void* q, const void* k, const void* v, const float* gate,
                  const float* beta, const float* state_in, const void* out, const float* state_out,
                  const float* den_out, int variant) {
-    if (variant != LA_NORM_ELU1 && variant != LA_GLA && variant != LA_GDN)
-        return fail(h, LA_ERR_INVALID_ARG, "variant must be LA_NORM_ELU1, LA_GLA or LA_GDN");
+    if (!valid_variant(variant))
+        return fail(h, LA_ERR_INVALID_ARG, "variant must be LA_NORM_ELU1, LA_GLA, LA_GDN or LA_NORM_DECAY");
     if (!q || !k || !v || !out) return fail(h, LA_ERR_INVALID_ARG, "q, k, v and out are required");
-    if (variant != LA_NORM_ELU1 && !gate) return fail(h, LA_ERR_INVALID_ARG, "gate is required for LA_GLA and LA_GDN");
+    if (variant != LA_NORM_ELU1 && !gate)
+        return fail(h, LA_ERR_INVALID_ARG, "gate is required for LA_GLA, LA_GDN and LA_NORM_DECAY");
     if (variant == LA_GDN && !beta) return fail(h, LA_ERR_INVALID_ARG, "beta is required for LA_GDN");
-    if (variant != LA_NORM_ELU1 && den_out)
-        return fail(h, LA_ERR_INVALID_ARG, "den_out is only defined for LA_NORM_ELU1");
+    if (variant != LA_NORM_ELU1 && variant != LA_NORM_DECAY && den_out)
+        return fail(h, LA_ERR_INVALID_ARG, "den_out is only defined for LA_NORM_ELU1 and LA_NORM_DECAY");
     const void* ptrs[] = {q, k, v, gate, beta, state_in, out, state_out, den_out};
     const char* names[] = {"q", "k", "v", "gate", "beta", "state_in", "out", "state_out", "den_out"};
     for (int i = 0; i < 9; ++i)
@@ -92,7 +96,10 @@ la::FwdArgs make_args(la_handle* h, const void* q, const void* k, const void* v,
     a.T = T;
     a.dk = h->cfg.d_k;
     a.dv = h->cfg.d_v;
-    a.variant = variant;
+    // LA_NORM_DECAY runs as the normalized variant with a per-(b,h) decay in
+    // `gate`; plain LA_NORM_ELU1 carries no gate.
+    a.variant = (variant == LA_NORM_DECAY) ? la::kNorm : variant;
+    if (variant == LA_NORM_ELU1) a.gate = nullptr;
     a.io = h->cfg.io == LA_FP32 ? la::kFp32 : la::kBf16;
     a.flags = h->cfg.flags;
     a.status = h->d_status;
@@ -202,8 +209,8 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v, const 
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const la_config& c = h->cfg;
     if (T == 0) {
-        if (variant != LA_NORM_ELU1 && variant != LA_GLA && variant != LA_GDN)
-            return fail(h, LA_ERR_INVALID_ARG, "variant must be LA_NORM_ELU1, LA_GLA or LA_GDN");
+        if (!valid_variant(variant))
+            return fail(h, LA_ERR_INVALID_ARG, "variant must be LA_NORM_ELU1, LA_GLA, LA_GDN or LA_NORM_DECAY");
         if (state_out && !aligned16(state_out)) return fail(h, LA_ERR_MISALIGNED, "state_out is not 16-byte aligned");
         if (!state_out || state_out == state_in) return LA_OK;
         DeviceGuard g(c.device);
@@ -225,7 +232,12 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v, const 
     if (!g.ok) return fail(h, LA_ERR_CUDA, "cannot select the handle's device");
     la::FwdArgs a = make_args(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, T);
     cudaError_t e;
-    if (tc_ok && chunk != 1) {
+    // the decayed normalized variant runs chunkwise only in the three-phase form
+    const bool chunked = tc_ok && chunk != 1 &&
+                         (variant != LA_NORM_DECAY ||
+                          (!(c.flags & LA_FLAG_SEQUENTIAL_CHUNKS) &&
+                           la::chunk::par_fits(a.BH, T, c.d_k, c.d_v, h->ws_bytes)));
+    if (chunked) {
         const char* what = "";
         e = la::launch_chunked(a, s, h->encode, &what);
         if (e != cudaSuccess) return cuda_fail(h, e, what);

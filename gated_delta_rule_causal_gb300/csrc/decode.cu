@@ -16,7 +16,8 @@
 // previous step's tail.
 //
 // Normalized / gated variants (state S [d_k, d_v]): each row i of S is
-// scaled (gla: gamma_i; norm: 1), gets phi(k_i) v added, and contributes
+// scaled (gla: gamma_i; norm: the head's fixed decay, 1 without one), gets
+// phi(k_i) v added (z_i scaled the same way), and contributes
 // phi(q_i) S'_i to the output column sums ("Linear attention and recurrent
 // memory", recurrent step; "Linear attention and Hyena" 11.3). One CTA per
 // head; the column sums are reduced in shared memory.
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kColThreads) decode_cols_kernel(FwdArgs a) {
 
     for (int h = blockIdx.x; h < a.BH; h += gridDim.x) {
         const float4 v4 = ld4(v + static_cast<size_t>(h) * DV + 4 * cl);
+        const float gnorm = (VAR == kNorm && a.gate) ? __ldg(a.gate + h) : 1.f;   // norm: fixed decay
         const float* sin = a.state_in ? a.state_in + h * ssz : nullptr;
         float* sout = a.state_out + h * ssz;
         float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kColThreads) decode_cols_kernel(FwdArgs a) {
                     const float qr = ld1(q + static_cast<size_t>(h) * DK + row);
                     const float f = phi_on ? elu1(kr) : kr;
                     const float pr = phi_on ? elu1(qr) : qr;
-                    const float gm = (VAR == kGla) ? __ldg(a.gate + static_cast<size_t>(h) * DK + row) : 1.f;
+                    const float gm = (VAR == kGla) ? __ldg(a.gate + static_cast<size_t>(h) * DK + row) : gnorm;
                     float4 n;
                     n.x = gm * S[j].x + f * v4.x;
                     n.y = gm * S[j].y + f * v4.y;
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kColThreads) decode_cols_kernel(FwdArgs a) {
                     o4.z += pr * n.z;
                     o4.w += pr * n.w;
                     if (VAR == kNorm && cl == 0) {
-                        const float z = (sin ? sin[static_cast<size_t>(DK) * DV + row] : 0.f) + f;
+                        const float z = gnorm * (sin ? sin[static_cast<size_t>(DK) * DV + row] : 0.f) + f;
                         sout[static_cast<size_t>(DK) * DV + row] = z;
                         den += pr * z;
                     }

@@ -49,6 +49,7 @@ struct Params {
     uint8_t* xs;            // [BH][nch] state entering the chunk, bf16 MMA tile (DK*DV*2 bytes)
     float* zs;              // norm: [BH][nch][DK] normalizer entering the chunk
     uint8_t* kh;            // norm: [BH][nch] phi(k) as the bf16 operand tile (DK*128 bytes)
+    const float* gamma;     // norm: [BH] fixed decay per sequence-head, or NULL (none)
     int BH, T, nch;
     unsigned flags;
     int* status;
@@ -199,6 +200,23 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             st_shared_v4(aKH + off, pack_bf16(k8[0], k8[1]), pack_bf16(k8[2], k8[3]), pack_bf16(k8[4], k8[5]),
                          pack_bf16(k8[6], k8[7]));
         }
+        // norm with a fixed decay: token j of the chunk reaches the chunk's
+        // end decayed by gamma^(nvalid-1-j); the weight goes on v_j (the
+        // phi(k) tile stays as the output phase reads it)
+        const float lg2g = (VAR == kNorm && p.gamma) ? lg2(__ldg(p.gamma + bh)) : 0.f;
+        if (VAR == kNorm && p.gamma) {
+#pragma unroll
+            for (int i = 0; i < (64 * 8 * VA) / kSumThreads; ++i) {
+                const int e = tid + kSumThreads * i;
+                const int row = e / (8 * VA), a = (e / 8) % VA, pc = e % 8;
+                const uint32_t off = a * 8192 + row * 128 + pc * 16;
+                const float wv = (row < nvalid) ? ex2(static_cast<float>(nvalid - 1 - row) * lg2g) : 0.f;
+                const uint4 uv = ld_shared_v4(aV + off);
+                const float2 c0 = unpack_bf16(uv.x), c1 = unpack_bf16(uv.y), c2 = unpack_bf16(uv.z), c3 = unpack_bf16(uv.w);
+                st_shared_v4(aV + off, pack_bf16(c0.x * wv, c0.y * wv), pack_bf16(c1.x * wv, c1.y * wv),
+                             pack_bf16(c2.x * wv, c2.y * wv), pack_bf16(c3.x * wv, c3.y * wv));
+            }
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -222,8 +240,14 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             const uint32_t base = aKH + (ch / 64) * 8192 + (ch % 8) * 2;
             const int lc = (ch % 64) / 8;
             float zs = 0.f;
+            if (p.gamma) {
 #pragma unroll 8
-            for (int j = part * RP; j < (part + 1) * RP; ++j) zs += ld_shared_bf16(base + sw128_off(j, lc));
+                for (int j = part * RP; j < (part + 1) * RP; ++j)
+                    if (j < nvalid) zs += ex2(static_cast<float>(nvalid - 1 - j) * lg2g) * ld_shared_bf16(base + sw128_off(j, lc));
+            } else {
+#pragma unroll 8
+                for (int j = part * RP; j < (part + 1) * RP; ++j) zs += ld_shared_bf16(base + sw128_off(j, lc));
+            }
             sPart[part * DK + ch] = zs;
             __syncthreads();
             if (part == 0) {
@@ -290,6 +314,11 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
     const int bh = gi / PER, e = gi % PER;
     if (bh >= p.BH) return;
     const int nch = p.nch;
+    // norm with a fixed decay: each chunk decays what enters it by gamma^nvalid
+    const float lg2g = (VAR == kNorm && p.gamma) ? lg2(__ldg(p.gamma + bh)) : 0.f;
+    auto chunk_decay = [&](int c) -> float {
+        return (VAR == kNorm && p.gamma) ? ex2(static_cast<float>(min(C, p.T - c * C)) * lg2g) : 1.f;
+    };
     if (e < E2) {
         const int r = e / (DK / 2), col = 2 * (e % (DK / 2));   // value row r, columns col, col+1
         float2 x = make_float2(0.f, 0.f);
@@ -316,6 +345,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
                     *reinterpret_cast<uint32_t*>(xs + (c + u) * XS_BYTES) = pack_bf16(x.x, x.y);
                     if constexpr (VAR == kGla) {
                         x = make_float2(d[u].x * x.x + a[u].x, d[u].y * x.y + a[u].y);
+                    } else if (p.gamma) {
+                        const float dc = chunk_decay(c + u);
+                        x = make_float2(dc * x.x + a[u].x, dc * x.y + a[u].y);
                     } else {
                         x = make_float2(x.x + a[u].x, x.y + a[u].y);
                     }
@@ -341,7 +373,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
             for (int u = 0; u < kScanBatch; ++u) {
                 if (c + u < nch) {
                     *reinterpret_cast<float2*>(p.zs + (static_cast<size_t>(bh) * nch + c + u) * DK + ch) = z;
-                    z = make_float2(z.x + a[u].x, z.y + a[u].y);
+                    const float dc = chunk_decay(c + u);
+                    z = make_float2(dc * z.x + a[u].x, dc * z.y + a[u].y);
                 }
             }
         }
@@ -457,6 +490,7 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
         const int s = (NS == 2) ? (k & 1) : 0;
         const uint32_t par_full = (NS == 2) ? ((k >> 1) & 1) : (k & 1);
         const int bh = u / p.nch, c = u % p.nch;
+        const float lg2g = (VAR == kNorm && p.gamma) ? lg2(__ldg(p.gamma + bh)) : 0.f;   // norm: log2 of the decay
         const int t0 = c * C, nvalid = min(C, T - t0);
         const uint32_t aQK = sbase + s * L::STAGE + L::QK_OFF, aV = sbase + s * L::STAGE + L::V_OFF;
         const uint32_t aXS = sbase + s * L::STAGE + L::XS_OFF;
@@ -568,7 +602,7 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
             }
             d += __shfl_xor_sync(0xffffffffu, d, 1);
             d += __shfl_xor_sync(0xffffffffu, d, 2);
-            if (q4 == 0) sDen[t] = d;
+            if (q4 == 0) sDen[t] = p.gamma ? d * ex2(static_cast<float>(t + 1) * lg2g) : d;
         }
         {
             const bool ok = mbar_wait(&bar[2], mph, kWaitLimitNs);
@@ -583,10 +617,33 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
             tmem_ld32(tlane + L::COL_G + 32 * hh, x);
             tmem_ld_wait();
             float rs = 0.f;
+            if (VAR == kNorm && p.gamma) {
+                // norm with a fixed decay: score (t, j) weighs gamma^(t-j), and
+                // the product with the state entering the chunk gamma^(t+1)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                x[i] = (32 * hh + i <= t) ? x[i] : 0.f;
-                rs += x[i];
+                for (int i = 0; i < 32; ++i) {
+                    const int j = 32 * hh + i;
+                    x[i] = (j <= t) ? x[i] * ex2(static_cast<float>(t - j) * lg2g) : 0.f;
+                    rs += x[i];
+                }
+                const float gt1 = ex2(static_cast<float>(t + 1) * lg2g);
+#pragma unroll
+                for (int b = 0; b < DV / 64; ++b) {
+                    float y[32];
+                    uint32_t u32[32];
+                    tmem_ld32(tlane + L::COL_O + hh * (DV / 2) + 32 * b, y);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) u32[i] = __float_as_uint(y[i] * gt1);
+                    tmem_st32(tlane + L::COL_O + hh * (DV / 2) + 32 * b, u32);
+                }
+                tmem_st_wait();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    x[i] = (32 * hh + i <= t) ? x[i] : 0.f;
+                    rs += x[i];
+                }
             }
             store_row32_bf16(aPS, t, 4 * hh, x);
             if (VAR == kNorm) atomicAdd(&sDen[t], rs);
@@ -735,6 +792,7 @@ cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     p.zs = reinterpret_cast<float*>(w);
     w += units * a.dk * sizeof(float);
     p.kh = w;
+    p.gamma = (a.variant == kNorm) ? a.gate : nullptr;   // the normalized variant's decay, if any
     p.BH = a.BH;
     p.T = a.T;
     p.nch = static_cast<int>(nch);

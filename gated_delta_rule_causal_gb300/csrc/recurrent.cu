@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(FwdArgs a) {
     const int tid = threadIdx.x;
     const int T = a.T, dv = a.dv;
     const bool phi_on = !(VAR == kGla && (a.flags & 0x1u));
+    // norm: the fixed decay of this sequence-head (1 without one)
+    const float gam = (VAR == kNorm && a.gate) ? a.gate[bh] : 1.f;
 
     __shared__ float sq[kTB][DK];
     __shared__ float sk[kTB][DK];
@@ -86,11 +88,11 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(FwdArgs a) {
         }
         __syncthreads();
         if (VAR == kNorm) {
-            // z_t = z_{t-1} + phi(k_t); den_t = phi(q_t) . z_t (update first).
+            // z_t = gamma z_{t-1} + phi(k_t); den_t = phi(q_t) . z_t (update first).
             if (tid < DK) {
                 float z = zsh[tid];
                 for (int t = 0; t < nt; ++t) {
-                    z += sk[t][tid];
+                    z = gam * z + sk[t][tid];
                     pz[t][tid] = sq[t][tid] * z;
                 }
                 zsh[tid] = z;
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(FwdArgs a) {
                 if (VAR == kNorm) {
 #pragma unroll
                     for (int i = 0; i < DK; ++i) {
-                        s[i] += sk[t][i] * vj;
+                        s[i] = gam * s[i] + sk[t][i] * vj;
                         o += sq[t][i] * s[i];
                     }
                     o = o / sden[t];

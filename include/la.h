@@ -3,7 +3,7 @@
  * state, for NVIDIA GB300 (sm_103a).
  *
  * The operator runs a sequence of tokens through a recurrent matrix state,
- * one independent recurrence per (batch, head). Three variants:
+ * one independent recurrence per (batch, head). Four variants:
  *
  *   LA_NORM_ELU1  normalized kernel attention, phi(x) = elu(x) + 1:
  *                   S_t = S_{t-1} + phi(k_t) v_t^T,   z_t = z_{t-1} + phi(k_t),
@@ -11,6 +11,11 @@
  *                 ("Linear Attention" concept page, normalized kernel
  *                 formulation; "Linear attention and recurrent memory", The
  *                 big idea; "Linear attention and Hyena", section 11.2.)
+ *   LA_NORM_DECAY LA_NORM_ELU1 with a fixed decay per sequence-head,
+ *                 gamma in (0, 1], on the state and the normalizer alike:
+ *                   S_t = gamma S_{t-1} + phi(k_t) v_t^T,  z_t = gamma z_{t-1} + phi(k_t).
+ *                 ("Linear attention and recurrent memory", Fixed decay
+ *                 versus an input-dependent gate.)
  *   LA_GLA        per-channel gated attention (GLA / RetNet family):
  *                   S_t = diag(gamma_t) S_{t-1} + phi(k_t) v_t^T,  o_t = S_t^T phi(q_t),
  *                 gamma_t in (0,1]^{d_k}. ("Linear attention and Hyena",
@@ -28,17 +33,18 @@
  *   q, k       [B, H, T, d_k]   io dtype
  *   v, out     [B, H, T, d_v]   io dtype
  *   gate       LA_NORM_ELU1: unused (pass NULL)
+ *              LA_NORM_DECAY: [B, H] fp32, gamma in (0, 1], one per sequence-head
  *              LA_GLA: [B, H, T, d_k] fp32, gamma in (0, 1]
  *              LA_GDN: [B, H, T] fp32, g in (0, 1]
  *   beta       LA_GDN: [B, H, T] fp32 in [0, 1]; NULL otherwise
  *   state      fp32, one block per (b,h):
- *              LA_NORM_ELU1: S [d_k, d_v] immediately followed by z [d_k]
+ *              LA_NORM_ELU1, LA_NORM_DECAY: S [d_k, d_v] immediately followed by z [d_k]
  *              LA_GLA:       S [d_k, d_v]
  *              LA_GDN:       S [d_v, d_k]
- *   den_out    LA_NORM_ELU1 only, optional: [B, H, T] fp32 denominators
- *              phi(q_t)^T z_t.
+ *   den_out    LA_NORM_ELU1, LA_NORM_DECAY, optional: [B, H, T] fp32
+ *              denominators phi(q_t)^T z_t.
  * For la_decode_step, drop the T axis: q,k [B,H,d_k], v,out [B,H,d_v],
- * gate [B,H,d_k] (gla) or [B,H] (gdn), beta [B,H].
+ * gate [B,H,d_k] (gla) or [B,H] (gdn, norm with decay), beta [B,H].
  *
  * Keys of LA_GDN are assumed to have unit L2 norm; the library does not
  * normalize them. No scale is applied to q.
@@ -83,7 +89,7 @@ extern "C" {
 
 typedef struct la_handle la_handle;
 
-typedef enum { LA_NORM_ELU1 = 0, LA_GLA = 1, LA_GDN = 2 } la_variant;
+typedef enum { LA_NORM_ELU1 = 0, LA_GLA = 1, LA_GDN = 2, LA_NORM_DECAY = 3 } la_variant;
 
 /* dtype of q, k, v and out. State, gates and beta are always fp32. */
 typedef enum { LA_BF16 = 0, LA_FP32 = 1 } la_dtype;
@@ -134,8 +140,10 @@ int la_create(const la_config* cfg, la_handle** out);
  *             chunkwise tensor-core kernel (bf16 io, d_k and d_v in {64, 128}).
  *             fp32 io and head sizes 16/32 always use the recurrent kernel.
  *             Other values: LA_ERR_UNSUPPORTED.
- *   den_out   optional, LA_NORM_ELU1 only.
+ *   den_out   optional, LA_NORM_ELU1 and LA_NORM_DECAY only.
  * The chunkwise kernel needs q, k, v (and the LA_GLA gate) 16-byte aligned.
+ * LA_NORM_DECAY runs chunkwise only in the three-phase form; a call whose
+ * per-chunk states do not fit the workspace runs the recurrent kernel.
  */
 int la_forward(la_handle* h, const void* q, const void* k, const void* v,
                const float* gate, const float* beta, const float* state_in,
@@ -146,7 +154,7 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v,
  * One decode step: advance every (b,h) state by one token and write its
  * output. state_out may equal state_in, which updates the state in place.
  * state_in NULL means a zero state. state_out must not be NULL.
- * den_out is optional ([B,H] fp32, LA_NORM_ELU1 only).
+ * den_out is optional ([B,H] fp32, LA_NORM_ELU1 and LA_NORM_DECAY only).
  */
 int la_decode_step(la_handle* h, const void* q, const void* k, const void* v,
                    const float* gate, const float* beta, const float* state_in,

@@ -21,8 +21,17 @@ def built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
+NORMED = ("norm", "norm_decay")   # the variants with a normalizer z
+
+
+def per_token(a, variant):
+    """Whether a gate array has a T axis (the decayed norm's is one per (b,h))."""
+    return a is not None and variant != "norm_decay"
+
+
 def base(variant, d):
-    w = {"norm": W.NORM_B4H8_T2048_D64, "gla": W.GLA_B4H16_T4096_D128, "gdn": W.GDN_B2H16_T8192_D128}[variant]
+    w = {"norm": W.NORM_B4H8_T2048_D64, "gla": W.GLA_B4H16_T4096_D128, "gdn": W.GDN_B2H16_T8192_D128,
+         "norm_decay": W.NORM_DECAY_B4H8_T2048_D64}[variant]
     return W.small(w, B=1, H=2, dk=d, dv=d)
 
 
@@ -38,7 +47,7 @@ def oracle_run(w, inp, state_in=None):
 
 def assert_parity(w, inp, chunk=0, state_in=None, tol=None, flags=0):
     h = handle(w, flags=flags)
-    o, st, den = run_gpu_prefill(h, w, inp, chunk, state_in, with_den=(w.variant == "norm"))
+    o, st, den = run_gpu_prefill(h, w, inp, chunk, state_in, with_den=(w.variant in NORMED))
     ref = oracle_run(w, inp, state_in)
     tol = tol or TOL[w.io]
     e_o, e_s = slice_rel_err(o, ref.o), slice_rel_err(st, ref.state)
@@ -54,7 +63,7 @@ def assert_parity(w, inp, chunk=0, state_in=None, tol=None, flags=0):
 
 # ------------------------------------------------------------- prefill, chunked
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [1, 15, 64, 65, 200])
 def test_chunked_prefill_parity(variant, d, T):
@@ -72,21 +81,21 @@ def test_chunked_prefill_sequential_parity(variant, d, T):
     assert_parity(w, W.draw(w, seed=T), chunk=64, flags=la.LA_FLAG_SEQUENTIAL_CHUNKS)
 
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
 @pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64)])
 def test_chunked_prefill_rectangular_heads(variant, dk, dv):
     w = base(variant, 64).with_(dk=dk, dv=dv, T=130)
     assert_parity(w, W.draw(w, seed=3), chunk=64)
 
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
 def test_chunked_prefill_from_a_state(variant):
     w = base(variant, 128).with_(T=150)
     inp = W.draw(w, seed=11)
     rng = np.random.default_rng(5)
     ss = oracle.state_size(variant, w.dk, w.dv)
     sin = (rng.standard_normal((w.B, w.H, ss)) * 0.1).astype(np.float32)
-    if variant == "norm":   # z must stay a positive sum of feature maps
+    if variant in NORMED:   # z must stay a positive sum of feature maps
         sin[..., w.dk * w.dv:] = np.abs(sin[..., w.dk * w.dv:]) * 50 + 1.0
     assert_parity(w, inp, chunk=64, state_in=sin)
 
@@ -136,7 +145,7 @@ def test_gdn_small_gates_and_full_beta():
 
 # ------------------------------------------------------------- recurrent path
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("io", ["fp32", "bf16"])
 def test_recurrent_prefill_parity(variant, d, io):
@@ -151,9 +160,40 @@ def test_normalized_t64_d16_fp32():
     assert e_o <= 1e-4 and e_s <= 1e-4
 
 
+# ------------------------------------------------------------- fixed decay (norm_decay)
+
+@pytest.mark.parametrize("T", [256, 1000, 1023])
+def test_norm_decay_long_prefill_from_a_state(T):
+    # the three-phase form over many chunks, a ragged tail and a start state
+    w = base("norm_decay", 64).with_(T=T)
+    inp = W.draw(w, seed=T + 3)
+    rng = np.random.default_rng(T)
+    ss = oracle.state_size("norm_decay", w.dk, w.dv)
+    sin = (rng.standard_normal((w.B, w.H, ss)) * 0.1).astype(np.float32)
+    sin[..., w.dk * w.dv:] = np.abs(sin[..., w.dk * w.dv:]) * 50 + 1.0
+    assert_parity(w, inp, chunk=64, state_in=sin)
+
+
+@pytest.mark.parametrize("gamma", [1.0, 0.3])
+@pytest.mark.parametrize("chunk", [64, 1])
+def test_norm_decay_edge_gammas(gamma, chunk):
+    # gamma = 1 is the undecayed variant; gamma = 0.3 forgets within a few tokens
+    w = base("norm_decay", 64).with_(T=200)
+    inp = W.draw(w, seed=5)
+    inp.gate[...] = gamma
+    assert_parity(w, inp, chunk=chunk)
+    if gamma == 1.0:
+        h = handle(w)
+        o_d, st_d, _ = run_gpu_prefill(h, w, inp, chunk)
+        wn = base("norm", 64).with_(T=200)
+        o_n, st_n, _ = run_gpu_prefill(h, wn, W.Inputs(inp.q, inp.k, inp.v, None, None, None), chunk)
+        h.close()
+        assert slice_rel_err(o_d, o_n) <= 1e-2 and slice_rel_err(st_d, st_n) <= 1e-3
+
+
 # ------------------------------------------------------------- state passing
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
 def test_split_continuation(variant):
     w = base(variant, 128).with_(T=192)
     inp = W.draw(w, seed=21)
@@ -164,10 +204,12 @@ def test_split_continuation(variant):
     def part(a, sl):
         return None if a is None else np.ascontiguousarray(a[:, :, sl])
 
+    g1 = part(inp.gate, slice(0, T1)) if per_token(inp.gate, variant) else inp.gate
+    g2 = part(inp.gate, slice(T1, None)) if per_token(inp.gate, variant) else inp.gate
     first = W.Inputs(part(inp.q, slice(0, T1)), part(inp.k, slice(0, T1)), part(inp.v, slice(0, T1)),
-                     part(inp.gate, slice(0, T1)), part(inp.beta, slice(0, T1)), None)
+                     g1, part(inp.beta, slice(0, T1)), None)
     second = W.Inputs(part(inp.q, slice(T1, None)), part(inp.k, slice(T1, None)), part(inp.v, slice(T1, None)),
-                      part(inp.gate, slice(T1, None)), part(inp.beta, slice(T1, None)), None)
+                      g2, part(inp.beta, slice(T1, None)), None)
     o1, st1, _ = run_gpu_prefill(h, w.with_(T=T1), first, 64)
     o2, st2, _ = run_gpu_prefill(h, w.with_(T=w.T - T1), second, 64, state_in=st1.astype(np.float32))
     ref = oracle_run(w, inp)
@@ -182,13 +224,13 @@ def decode_inputs(w, step, seed):
     return W.draw_decode_step(w, step, seed)
 
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
 @pytest.mark.parametrize("d", [16, 64, 128])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_decode_parity(variant, d, in_place):
     w = base(variant, d).with_(B=3, H=5, T=1, state_std=0.05)
     st0 = W.draw_decode_state(w, seed=2).reshape(w.B, w.H, -1)
-    if variant == "norm":
+    if variant in NORMED:
         st0[..., w.dk * w.dv:] = np.abs(st0[..., w.dk * w.dv:]) * 20 + 1.0
     h = handle(w)
     s_dev = torch.from_numpy(st0).cuda()
@@ -197,13 +239,14 @@ def test_decode_parity(variant, d, in_place):
         inp = decode_inputs(w, step, seed=2)
         q, k, v = (to_torch(a, h.device) for a in (inp.q, inp.k, inp.v))
         g, b = to_torch(inp.gate, h.device), to_torch(inp.beta, h.device)
-        den = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda") if variant == "norm" else None
+        den = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda") if variant in NORMED else None
         s_out = s_dev if in_place else None
         o, s_new, den = h.decode_step(q, k, v, g, b, s_dev, variant=variant, state_out=s_out, den_out=den)
         torch.cuda.synchronize()
         qo, ko, vo, go, bo = oracle_inputs(inp)
         ex = lambda a: None if a is None else a[:, :, None]
-        ref = oracle.run(variant, ex(qo), ex(ko), ex(vo), ex(go), ex(bo), ref_state)
+        ref = oracle.run(variant, ex(qo), ex(ko), ex(vo), ex(go) if per_token(go, variant) else go, ex(bo),
+                         ref_state)
         assert slice_rel_err(from_torch(o), ref.o[:, :, 0]) <= 2e-2
         assert slice_rel_err(s_new.cpu().numpy(), ref.state) <= 1e-5
         if den is not None:
@@ -212,7 +255,7 @@ def test_decode_parity(variant, d, in_place):
         s_dev = s_new
 
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
 def test_prefill_then_decode_equals_longer_prefill(variant):
     w = base(variant, 128).with_(T=100)
     inp = W.draw(w, seed=31)
@@ -220,13 +263,15 @@ def test_prefill_then_decode_equals_longer_prefill(variant):
     h = handle(w)
     cut = lambda a, sl: None if a is None else np.ascontiguousarray(a[:, :, sl])
     pre = W.Inputs(cut(inp.q, slice(0, T1)), cut(inp.k, slice(0, T1)), cut(inp.v, slice(0, T1)),
-                   cut(inp.gate, slice(0, T1)), cut(inp.beta, slice(0, T1)), None)
+                   cut(inp.gate, slice(0, T1)) if per_token(inp.gate, variant) else inp.gate,
+                   cut(inp.beta, slice(0, T1)), None)
     _, st, _ = run_gpu_prefill(h, w.with_(T=T1), pre, 64)
     s_dev = torch.from_numpy(st.astype(np.float32)).cuda()
     outs = []
     for t in range(T1, w.T):
         sel = lambda a: None if a is None else to_torch(np.ascontiguousarray(a[:, :, t]), h.device)
-        o, s_dev, _ = h.decode_step(sel(inp.q), sel(inp.k), sel(inp.v), sel(inp.gate), sel(inp.beta), s_dev,
+        gt = sel(inp.gate) if per_token(inp.gate, variant) else to_torch(inp.gate, h.device)
+        o, s_dev, _ = h.decode_step(sel(inp.q), sel(inp.k), sel(inp.v), gt, sel(inp.beta), s_dev,
                                     variant=variant, state_out=s_dev)
         outs.append(from_torch(o))
     torch.cuda.synchronize()
@@ -240,12 +285,12 @@ def test_prefill_then_decode_equals_longer_prefill(variant):
 SAMPLE_HEADS = [(0, 0), (0, 5), (-1, -1)]
 
 
-@pytest.mark.parametrize("w", [W.NORM_B4H8_T2048_D64, W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128],
-                         ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.NORM_B4H8_T2048_D64, W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128,
+                               W.NORM_DECAY_B4H8_T2048_D64], ids=lambda w: w.name)
 def test_full_size_sampled_heads(w):
     inp = W.draw(w, seed=0)
     h = handle(w)
-    o, st, den = run_gpu_prefill(h, w, inp, 0, with_den=(w.variant == "norm"))
+    o, st, den = run_gpu_prefill(h, w, inp, 0, with_den=(w.variant in NORMED))
     q, k, v, g, b = oracle_inputs(inp)
     for bb, hh in SAMPLE_HEADS:
         sel = lambda a: None if a is None else a[bb:bb + 1 if bb != -1 else None][:, hh:hh + 1 if hh != -1 else None]
@@ -339,6 +384,8 @@ def test_rejected_calls_do_not_launch():
     ("gdn", 200, 0, 64, 3),                                  # windows of 2 and 2 chunks, + 1
     ("gdn", 64 * 40, 0, 64, 6),                              # windows of 2, 4, 8, 16, 10, + 1
     ("gla", 200, 0, 1, 1),                                   # the recurrent kernel
+    ("norm_decay", 200, 0, 64, 3),                           # decayed: the three-phase form
+    ("norm_decay", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),  # decayed, not three-phase: recurrent
 ])
 def test_launch_counts(variant, T, flags, chunk, expect):
     # la_last_launches reports the kernels one call enqueued, which names the

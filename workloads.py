@@ -85,7 +85,7 @@ def _unit_rows(x: np.ndarray) -> np.ndarray:
 class Workload:
     """One synthetic workload: shapes, dtypes and value distributions."""
     name: str
-    variant: str          # norm | gla | gdn
+    variant: str          # norm | gla | gdn | norm_decay
     B: int
     H: int
     T: int                # tokens per sequence (1 for one decode step)
@@ -122,6 +122,9 @@ GLA_B4H16_T4096_D128 = Workload(
     "gla_b4h16_t4096_d128_bf16", "gla", 4, 16, 4096, 128, 128, "bf16",
     qkv_scale=1.0 / math.sqrt(128.0), gate_mu=3.0,
     note="per-channel gate gamma=sigmoid(N(3,1)) fp32, bf16 q,k,v N(0,1)/sqrt(128)")
+NORM_DECAY_B4H8_T2048_D64 = Workload(
+    "norm_decay_b4h8_t2048_d64_bf16", "norm_decay", 4, 8, 2048, 64, 64, "bf16", qkv_scale=0.5, gate_mu=4.0,
+    note="normalized elu+1 with a fixed decay per head gamma=sigmoid(N(4,1)), bf16 q,k,v N(0,1)*0.5")
 GDN_B2H16_T8192_D128 = Workload(
     "gdn_b2h16_t8192_d128_bf16", "gdn", 2, 16, 8192, 128, 128, "bf16",
     unit_keys=True, gate_mu=4.0, beta_mu=0.0,
@@ -133,7 +136,10 @@ GDN_DECODE_N256H16_D128 = Workload(
 
 ALL = (NORM_T64_D16, NORM_B4H8_T2048_D64, GLA_B4H16_T4096_D128,
        GDN_B2H16_T8192_D128, GDN_DECODE_N256H16_D128)
-BY_NAME = {w.name: w for w in ALL}
+# Beyond the five: the normalized variant with a fixed decay per head, on
+# the shapes of the normalized headline workload.
+EXTRA = (NORM_DECAY_B4H8_T2048_D64,)
+BY_NAME = {w.name: w for w in ALL + EXTRA}
 
 
 # --------------------------------------------------------------------------
@@ -146,7 +152,7 @@ class Inputs:
     q: np.ndarray
     k: np.ndarray
     v: np.ndarray
-    gate: np.ndarray | None   # norm: None; gla: [B,H,T,dk]; gdn: [B,H,T]
+    gate: np.ndarray | None   # norm: None; gla: [B,H,T,dk]; gdn: [B,H,T]; norm_decay: [B,H]
     beta: np.ndarray | None   # gdn: [B,H,T]; else None
     state: np.ndarray | None  # fp32 initial state or None (zeros)
 
@@ -163,12 +169,14 @@ def _draw_qkvgb(rng: np.random.Generator, w: Workload, lead: tuple) -> tuple:
     elif w.variant == "gdn":
         gate = _sigmoid(rng.standard_normal(lead) + w.gate_mu)
         beta = _sigmoid(rng.standard_normal(lead) + w.beta_mu)
+    elif w.variant == "norm_decay":   # one fixed decay per sequence-head
+        gate = _sigmoid(rng.standard_normal(lead[:2]) + w.gate_mu)
     return q, k, v, gate, beta
 
 
 def state_shape(w: Workload) -> tuple:
-    """Flat fp32 state of one call: S (+ z for norm) per (b,h)."""
-    if w.variant == "norm":
+    """Flat fp32 state of one call: S (+ z for norm, norm_decay) per (b,h)."""
+    if w.variant in ("norm", "norm_decay"):
         return (w.B * w.H * (w.dk * w.dv + w.dk),)
     return (w.B * w.H * w.dk * w.dv,)
 
