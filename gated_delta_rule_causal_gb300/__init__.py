@@ -6,7 +6,7 @@ marshals arguments: torch supplies device memory and streams. There is no
 fallback. If the library has not been built, or no GB300 is present, the
 calls raise.
 
-Low level (same names as the C ABI): ``la_create``, ``la_forward``,
+Low level (same names as the C ABI): ``la_create``, ``la_forward``, ``la_forward_host``,
 ``la_decode_step``, ``la_status``, ``la_destroy``, ``la_last_error``,
 ``la_last_launches``, ``la_version``, ``la_forward_noalloc``. Convenience: ``Handle`` takes torch
 tensors.
@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             L.la_create.restype = i
             L.la_forward.argtypes = [vp, vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, vp]
             L.la_forward.restype = i
+            L.la_forward_host.argtypes = [vp, vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, vp]
+            L.la_forward_host.restype = i
             L.la_decode_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, vp, fp, fp, i, vp]
             L.la_decode_step.restype = i
             L.la_status.argtypes = [vp, vp]
@@ -94,6 +96,11 @@ def la_create(B, H, d_k, d_v, io=LA_BF16, flags=0, device=0) -> tuple[int, ctype
 
 def la_forward(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, T, chunk, stream) -> int:
     return lib().la_forward(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, T, chunk, stream)
+
+
+def la_forward_host(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, T, chunk, stream) -> int:
+    """la_forward with every tensor in (page-locked) host memory (see la.h)."""
+    return lib().la_forward_host(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, T, chunk, stream)
 
 
 def la_decode_step(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, stream) -> int:
@@ -206,6 +213,50 @@ class Handle:
             state_out = torch.empty((B, H, ss), dtype=torch.float32, device=self.device)
         rc = la_forward(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(beta), _ptr(state_in),
                         _ptr(out), _ptr(state_out), _ptr(den_out), var, T, chunk, _stream_ptr(stream))
+        self._check(rc)
+        return out, state_out, den_out
+
+    def forward_host(self, q, k, v, gate=None, beta=None, state_in=None, *, variant="gdn", chunk=0,
+                     out=None, state_out=None, den_out=None, return_state=True, stream=None):
+        """Prefill from pinned host tensors (CPU, ``pin_memory()``); the outputs
+        are pinned host tensors too. The copies overlap the kernels inside the
+        library. Returns (out, state_out, den_out), complete once ``stream``
+        (default: the current stream) reaches the end of the call."""
+        import torch
+        var = VARIANTS[variant]
+        B, H, T = q.shape[0], q.shape[1], q.shape[2]
+        if (B, H) != (self.B, self.H):
+            raise ValueError("q batch/heads differ from the handle's")
+        cpu = torch.device("cpu")
+
+        def chk(name, t, shape, dtype):
+            if t is None:
+                return
+            if not isinstance(t, torch.Tensor) or t.device != cpu or t.dtype != dtype:
+                raise ValueError(f"{name}: expected a {dtype} host tensor")
+            if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+                raise ValueError(f"{name}: expected contiguous shape {tuple(shape)}, got {tuple(t.shape)}")
+
+        chk("q", q, (B, H, T, self.d_k), self.dtype)
+        chk("k", k, (B, H, T, self.d_k), self.dtype)
+        chk("v", v, (B, H, T, self.d_v), self.dtype)
+        if var == LA_GLA:
+            chk("gate", gate, (B, H, T, self.d_k), torch.float32)
+        elif var == LA_NORM_DECAY:
+            chk("gate", gate, (B, H), torch.float32)
+        elif var == LA_GDN:
+            chk("gate", gate, (B, H, T), torch.float32)
+            chk("beta", beta, (B, H, T), torch.float32)
+        ss = state_size(variant, self.d_k, self.d_v)
+        chk("state_in", state_in, (B, H, ss), torch.float32)
+        if out is None:
+            out = torch.empty((B, H, T, self.d_v), dtype=self.dtype).pin_memory()
+        if state_out is None and return_state:
+            state_out = torch.empty((B, H, ss), dtype=torch.float32).pin_memory()
+        chk("out", out, (B, H, T, self.d_v), self.dtype)
+        chk("state_out", state_out, (B, H, ss), torch.float32)
+        rc = la_forward_host(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(beta), _ptr(state_in),
+                             _ptr(out), _ptr(state_out), _ptr(den_out), var, T, chunk, _stream_ptr(stream))
         self._check(rc)
         return out, state_out, den_out
 

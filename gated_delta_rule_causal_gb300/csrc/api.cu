@@ -12,7 +12,6 @@
 #include "../../include/la.h"
 #include "kernels.h"
 #include "prefill.h"
-#include "prefill.h"
 
 struct la_handle {
     la_config cfg;
@@ -23,9 +22,78 @@ struct la_handle {
     PFN_cuTensorMapEncodeTiled_v12000 encode;
     std::string last_error;
     int last_launches;  // kernels enqueued by the last successful call
+    // la_forward_host: device staging for two groups of sequence-heads, the
+    // copy-in / compute / copy-out streams and the events that chain them
+    // (all created on first use)
+    uint8_t* d_stage;
+    size_t stage_bytes;
+    cudaStream_t s_in, s_comp, s_out;
+    cudaEvent_t ev_start, ev_done, ev_in[2], ev_comp[2], ev_out[2];
+    bool host_ready;
 };
 
 namespace {
+
+constexpr int kHostGroups = 2;   // la_forward_host: groups of sequence-heads in flight (2 measured best of 1, 2, 4, 8)
+constexpr int kCopyCtas = 64;    // CTAs of one gather / scatter over the host link
+
+// Up to six contiguous byte ranges copied by one launch: the inputs of a
+// group of sequence-heads from mapped page-locked host memory into the
+// staging, or its results back. One launch instead of one copy per tensor
+// (each copy costs several microseconds of fixed time); the host link, not
+// the launch, bounds the rate. 16-byte accesses where both ends and the
+// length allow, else 4-byte, else bytes.
+struct CopySeg {
+    const uint8_t* src;
+    uint8_t* dst;
+    size_t bytes;
+};
+struct CopyJob {
+    CopySeg seg[6];
+    int n;
+};
+
+__global__ void __launch_bounds__(256) copy_segments_kernel(const CopyJob job) {
+    const size_t tid = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+    const size_t nthr = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (int s = 0; s < job.n; ++s) {
+        const CopySeg g = job.seg[s];
+        const uintptr_t al = reinterpret_cast<uintptr_t>(g.src) | reinterpret_cast<uintptr_t>(g.dst) | g.bytes;
+        if ((al & 15) == 0) {
+            const uint4* a = reinterpret_cast<const uint4*>(g.src);
+            uint4* b = reinterpret_cast<uint4*>(g.dst);
+            const size_t n = g.bytes / 16;
+            size_t i = tid;
+            for (; i + 3 * nthr < n; i += 4 * nthr) {   // four loads in flight per thread
+                const uint4 x0 = a[i], x1 = a[i + nthr], x2 = a[i + 2 * nthr], x3 = a[i + 3 * nthr];
+                b[i] = x0;
+                b[i + nthr] = x1;
+                b[i + 2 * nthr] = x2;
+                b[i + 3 * nthr] = x3;
+            }
+            for (; i < n; i += nthr) b[i] = a[i];
+        } else if ((al & 3) == 0) {
+            const uint32_t* a = reinterpret_cast<const uint32_t*>(g.src);
+            uint32_t* b = reinterpret_cast<uint32_t*>(g.dst);
+            for (size_t i = tid; i < g.bytes / 4; i += nthr) b[i] = a[i];
+        } else {
+            for (size_t i = tid; i < g.bytes; i += nthr) g.dst[i] = g.src[i];
+        }
+    }
+}
+
+// The device address of page-locked host memory (its own address under
+// unified addressing), or NULL when the GPU cannot address it directly.
+const uint8_t* mapped(const void* p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+    return static_cast<const uint8_t*>(at.devicePointer);
+}
 
 int fail(la_handle* h, int code, const std::string& msg) {
     if (h) h->last_error = msg;
@@ -110,6 +178,30 @@ la::FwdArgs make_args(la_handle* h, const void* q, const void* k, const void* v,
     return a;
 }
 
+// Enqueue the kernels of one prefill whose arguments were validated: the
+// chunkwise tensor-core form when the configuration allows it, else the
+// recurrent kernel. Adds the launches to h->last_launches.
+int enqueue_forward(la_handle* h, la::FwdArgs& a, int variant, int chunk, cudaStream_t s) {
+    const la_config& c = h->cfg;
+    const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
+    // the decayed normalized variant runs chunkwise only in the three-phase form
+    const bool chunked = tc_ok && chunk != 1 &&
+                         (variant != LA_NORM_DECAY ||
+                          (!(c.flags & LA_FLAG_SEQUENTIAL_CHUNKS) &&
+                           la::chunk::par_fits(a.BH, a.T, c.d_k, c.d_v, h->ws_bytes)));
+    cudaError_t e;
+    if (chunked) {
+        const char* what = "";
+        e = la::launch_chunked(a, s, h->encode, &what);
+        if (e != cudaSuccess) return cuda_fail(h, e, what);
+    } else {
+        e = la::launch_recurrent(a, s);
+        if (e != cudaSuccess) return cuda_fail(h, e, "recurrent kernel launch");
+        h->last_launches += 1;
+    }
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -142,6 +234,9 @@ int la_create(const la_config* cfg, la_handle** out) {
     h->ws_bytes = 0;
     h->encode = nullptr;
     h->last_launches = 0;
+    h->d_stage = nullptr;
+    h->stage_bytes = 0;
+    h->host_ready = false;
     DeviceGuard g(cfg->device);
     if (!g.ok) { delete h; return LA_ERR_CUDA; }
     if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess || cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
@@ -191,6 +286,18 @@ void la_destroy(la_handle* h) {
     if (!h) return;
     {
         DeviceGuard g(h->cfg.device);
+        if (h->host_ready) {
+            cudaStreamSynchronize(h->s_in);
+            cudaStreamSynchronize(h->s_comp);
+            cudaStreamSynchronize(h->s_out);
+            cudaStreamDestroy(h->s_in);
+            cudaStreamDestroy(h->s_comp);
+            cudaStreamDestroy(h->s_out);
+            for (cudaEvent_t e : {h->ev_start, h->ev_done, h->ev_in[0], h->ev_in[1], h->ev_comp[0], h->ev_comp[1],
+                                  h->ev_out[0], h->ev_out[1]})
+                cudaEventDestroy(e);
+        }
+        if (h->d_stage) cudaFree(h->d_stage);
         if (h->d_status) cudaFree(h->d_status);
         if (h->d_ws) cudaFree(h->d_ws);
     }
@@ -231,21 +338,153 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v, const 
     DeviceGuard g(c.device);
     if (!g.ok) return fail(h, LA_ERR_CUDA, "cannot select the handle's device");
     la::FwdArgs a = make_args(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, T);
+    return enqueue_forward(h, a, variant, chunk, s);
+}
+
+int la_forward_host(la_handle* h, const void* q, const void* k, const void* v, const float* gate, const float* beta,
+                    const float* state_in, void* out, float* state_out, float* den_out, int variant, int T, int chunk,
+                    void* cuda_stream) {
+    if (!h) return LA_ERR_INVALID_ARG;
+    h->last_error.clear();
+    h->last_launches = 0;
+    if (T < 1) return fail(h, LA_ERR_INVALID_ARG, "T must be >= 1");
+    int rc = check_common(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant);
+    if (rc != LA_OK) return rc;
+    if (chunk != 0 && chunk != 1 && chunk != 64)
+        return fail(h, LA_ERR_UNSUPPORTED, "chunk must be 0 (default), 1 (recurrent) or 64");
+    const la_config& c = h->cfg;
+    const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
+    if (chunk == 64 && !tc_ok)
+        return fail(h, LA_ERR_UNSUPPORTED, "chunk 64 needs bf16 io and d_k, d_v in {64, 128}");
+    if (static_cast<long long>(T) * (c.d_k > c.d_v ? c.d_k : c.d_v) > (1LL << 31) - 1)
+        return fail(h, LA_ERR_UNSUPPORTED, "T * d exceeds 2^31 - 1");
+    DeviceGuard g(c.device);
+    if (!g.ok) return fail(h, LA_ERR_CUDA, "cannot select the handle's device");
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t e;
-    // the decayed normalized variant runs chunkwise only in the three-phase form
-    const bool chunked = tc_ok && chunk != 1 &&
-                         (variant != LA_NORM_DECAY ||
-                          (!(c.flags & LA_FLAG_SEQUENTIAL_CHUNKS) &&
-                           la::chunk::par_fits(a.BH, T, c.d_k, c.d_v, h->ws_bytes)));
-    if (chunked) {
-        const char* what = "";
-        e = la::launch_chunked(a, s, h->encode, &what);
-        if (e != cudaSuccess) return cuda_fail(h, e, what);
-    } else {
-        e = la::launch_recurrent(a, s);
-        if (e != cudaSuccess) return cuda_fail(h, e, "recurrent kernel launch");
-        h->last_launches = 1;
+    if (!h->host_ready) {
+        e = cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s_comp, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking);
+        cudaEvent_t* evs[] = {&h->ev_start, &h->ev_done, &h->ev_in[0], &h->ev_in[1], &h->ev_comp[0], &h->ev_comp[1],
+                              &h->ev_out[0], &h->ev_out[1]};
+        for (cudaEvent_t* ev : evs)
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(h, e, "stream / event creation");
+        h->host_ready = true;
     }
+
+    // Sequence-heads in up to kHostGroups groups; per group the bytes of
+    // every staged tensor, each slice 256-byte aligned.
+    const int BH = c.B * c.H;
+    const int G0 = BH < kHostGroups ? BH : kHostGroups;
+    const int gbh = (BH + G0 - 1) / G0;
+    const int G = (BH + gbh - 1) / gbh;
+    const size_t io = (c.io == LA_BF16) ? 2 : 4;
+    const size_t ss = state_elems(c, variant);
+    const size_t tok = static_cast<size_t>(T);
+    const size_t gate_per_head = (variant == LA_GLA) ? tok * c.d_k : (variant == LA_GDN) ? tok
+                               : (variant == LA_NORM_DECAY) ? 1 : 0;
+    const size_t per_head[9] = {
+        tok * c.d_k * io, tok * c.d_k * io, tok * c.d_v * io,                    // q, k, v
+        gate ? gate_per_head * 4 : 0, beta ? tok * 4 : 0, state_in ? ss * 4 : 0,  // gate, beta, state_in
+        tok * c.d_v * io, state_out ? ss * 4 : 0, den_out ? tok * 4 : 0};         // out, state_out, den_out
+    size_t off[9], buf = 0;
+    for (int i = 0; i < 9; ++i) {
+        off[i] = buf;
+        buf += (per_head[i] * gbh + 255) & ~static_cast<size_t>(255);
+    }
+    if (2 * buf > h->stage_bytes) {
+        // grow the staging (frees the old one after the work that used it)
+        if (h->d_stage) {
+            cudaStreamSynchronize(h->s_in);
+            cudaStreamSynchronize(h->s_comp);
+            cudaStreamSynchronize(h->s_out);
+            cudaFree(h->d_stage);
+            h->d_stage = nullptr;
+            h->stage_bytes = 0;
+        }
+        e = cudaMalloc(&h->d_stage, 2 * buf);
+        if (e != cudaSuccess) return cuda_fail(h, e, "staging allocation");
+        h->stage_bytes = 2 * buf;
+    }
+    const void* src[6] = {q, k, v, gate, beta, state_in};
+    void* dst[3] = {out, state_out, den_out};
+    // copy kernels when the GPU can address every host buffer, else the copy engine
+    const uint8_t* msrc[6];
+    uint8_t* mdst[3];
+    bool by_kernel = true;
+    for (int i = 0; i < 6; ++i) {
+        msrc[i] = mapped(src[i]);
+        if (src[i] && !msrc[i]) by_kernel = false;
+    }
+    for (int i = 0; i < 3; ++i) {
+        mdst[i] = const_cast<uint8_t*>(mapped(dst[i]));
+        if (dst[i] && !mdst[i]) by_kernel = false;
+    }
+
+    // copy-in, compute and copy-out of group i overlap those of its
+    // neighbours; each staging half b is reused two groups later, after its
+    // kernels (copy-in waits) and its copy-out (compute waits) are done
+    e = cudaEventRecord(h->ev_start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_in, h->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_comp, h->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_out, h->ev_start, 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "stream ordering");
+    for (int gi = 0; gi < G; ++gi) {
+        const int b = gi & 1;
+        const int h0 = gi * gbh;
+        const int nh = (BH - h0 < gbh) ? BH - h0 : gbh;
+        uint8_t* st = h->d_stage + b * buf;
+        if (gi >= 2) e = cudaStreamWaitEvent(h->s_in, h->ev_comp[b], 0);
+        if (by_kernel && e == cudaSuccess) {
+            CopyJob job{};
+            for (int i = 0; i < 6; ++i)
+                if (src[i] && per_head[i]) job.seg[job.n++] = {msrc[i] + per_head[i] * h0, st + off[i], per_head[i] * nh};
+            copy_segments_kernel<<<kCopyCtas, 256, 0, h->s_in>>>(job);
+            e = cudaGetLastError();
+            ++h->last_launches;
+        } else {
+            for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+                if (src[i] && per_head[i])
+                    e = cudaMemcpyAsync(st + off[i], static_cast<const uint8_t*>(src[i]) + per_head[i] * h0,
+                                        per_head[i] * nh, cudaMemcpyHostToDevice, h->s_in);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(h->ev_in[b], h->s_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_comp, h->ev_in[b], 0);
+        if (e == cudaSuccess && gi >= 2) e = cudaStreamWaitEvent(h->s_comp, h->ev_out[b], 0);
+        if (e != cudaSuccess) return cuda_fail(h, e, "staging copy-in");
+        la::FwdArgs a = make_args(h, st + off[0], st + off[1], st + off[2],
+                                  gate ? reinterpret_cast<const float*>(st + off[3]) : nullptr,
+                                  beta ? reinterpret_cast<const float*>(st + off[4]) : nullptr,
+                                  state_in ? reinterpret_cast<const float*>(st + off[5]) : nullptr, st + off[6],
+                                  state_out ? reinterpret_cast<float*>(st + off[7]) : nullptr,
+                                  den_out ? reinterpret_cast<float*>(st + off[8]) : nullptr, variant, T);
+        a.BH = nh;
+        rc = enqueue_forward(h, a, variant, chunk, h->s_comp);
+        if (rc != LA_OK) return rc;
+        e = cudaEventRecord(h->ev_comp[b], h->s_comp);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_out, h->ev_comp[b], 0);
+        if (by_kernel && e == cudaSuccess) {
+            CopyJob job{};
+            for (int i = 0; i < 3; ++i)
+                if (dst[i] && per_head[6 + i])
+                    job.seg[job.n++] = {st + off[6 + i], mdst[i] + per_head[6 + i] * h0, per_head[6 + i] * nh};
+            copy_segments_kernel<<<kCopyCtas, 256, 0, h->s_out>>>(job);
+            e = cudaGetLastError();
+            ++h->last_launches;
+        } else {
+            for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+                if (dst[i] && per_head[6 + i])
+                    e = cudaMemcpyAsync(static_cast<uint8_t*>(dst[i]) + per_head[6 + i] * h0, st + off[6 + i],
+                                        per_head[6 + i] * nh, cudaMemcpyDeviceToHost, h->s_out);
+        }
+        if (e == cudaSuccess) e = cudaEventRecord(h->ev_out[b], h->s_out);
+        if (e != cudaSuccess) return cuda_fail(h, e, "staging copy-out");
+    }
+    e = cudaEventRecord(h->ev_done, h->s_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_done, 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "stream ordering");
     return LA_OK;
 }
 

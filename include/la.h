@@ -151,6 +151,29 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v,
                int variant, int T, int chunk, void* cuda_stream);
 
 /*
+ * Prefill from host memory: the same operation and arguments as la_forward,
+ * but q, k, v, gate, beta, state_in, out, state_out and den_out are host
+ * pointers (page-locked memory, cudaHostAlloc or cudaHostRegister, for the
+ * copies to run asynchronously). The library splits the B*H sequence-heads
+ * into up to 2 groups and, on three streams of its own, copies group i + 1
+ * in, runs the kernels of group i and copies group i - 1 out at the same
+ * time. When the GPU can address every buffer (page-locked memory under
+ * unified addressing) one copy kernel per group and direction moves the
+ * data over the host link; otherwise the copy engine does, one copy per
+ * tensor. la_last_launches counts the copy kernels too. Staging for two
+ * groups lives in device memory that the handle allocates on
+ * first use and grows when a call needs more (la_destroy frees it). The call
+ * is ordered after the work already enqueued on cuda_stream, and the work
+ * enqueued on cuda_stream after it waits for its last copy-out; the host
+ * buffers must stay valid until then. T >= 1. Calls through one handle must
+ * not overlap (they share the staging and the workspace).
+ */
+int la_forward_host(la_handle* h, const void* q, const void* k, const void* v,
+                    const float* gate, const float* beta, const float* state_in,
+                    void* out, float* state_out, float* den_out,
+                    int variant, int T, int chunk, void* cuda_stream);
+
+/*
  * One decode step: advance every (b,h) state by one token and write its
  * output. state_out may equal state_in, which updates the state in place.
  * state_in NULL means a zero state. state_out must not be NULL.
