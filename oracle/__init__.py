@@ -11,8 +11,9 @@ The tests use them to pin the C recurrences.
 
 Arrays use the operator's layouts: q,k [B,H,T,dk]; v [B,H,T,dv]; gla gate
 [B,H,T,dk]; gdn gate/beta [B,H,T]; norm_decay gate [B,H] (one decay per
-sequence-head); state per (b,h): norm and norm_decay S[dk,dv] then z[dk];
-gla S[dk,dv]; gdn S[dv,dk].
+sequence-head); kda gate [B,H,T,dk] (per-channel decay) and beta [B,H,T];
+state per (b,h): norm and norm_decay S[dk,dv] then z[dk]; gla S[dk,dv];
+gdn and kda S[dv,dk].
 """
 from __future__ import annotations
 
@@ -62,7 +63,9 @@ def _load():
             lib.la_oracle_norm_decay.argtypes = [i, i, i, i, P, P, P, P, P, P, P, P, i]
             lib.la_oracle_gla.argtypes = [i, i, i, i, P, P, P, P, P, P, P, i, i]
             lib.la_oracle_gdn.argtypes = [i, i, i, i, P, P, P, P, P, P, P, P, i]
-            for f in (lib.la_oracle_norm, lib.la_oracle_norm_decay, lib.la_oracle_gla, lib.la_oracle_gdn):
+            lib.la_oracle_kda.argtypes = [i, i, i, i, P, P, P, P, P, P, P, P, i]
+            for f in (lib.la_oracle_norm, lib.la_oracle_norm_decay, lib.la_oracle_gla, lib.la_oracle_gdn,
+                      lib.la_oracle_kda):
                 f.restype = ctypes.c_int
             lib.la_oracle_threads_available.restype = ctypes.c_int
             _lib = lib
@@ -132,6 +135,11 @@ def run(variant: str, q, k, v, gate=None, beta=None, state_in=None,
         g, b = _f64(gate), _f64(beta)
         assert g.shape == (B, H, T) and b.shape == (B, H, T)
         rc = lib.la_oracle_gdn(BH, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b),
+                               _ptr(sin), _ptr(o), _ptr(sout), nthreads)
+    elif variant == "kda":
+        a, b = _f64(gate), _f64(beta)
+        assert a.shape == (B, H, T, dk) and b.shape == (B, H, T)
+        rc = lib.la_oracle_kda(BH, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
                                _ptr(sin), _ptr(o), _ptr(sout), nthreads)
     else:
         raise ValueError(variant)

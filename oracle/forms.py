@@ -150,3 +150,50 @@ def gdn_unrolled(q, k, v, g, beta, S0=None):
             S = S + beta[j] * np.outer(v[j], k[j]) @ prod(j + 1, t)
         o[t] = S @ q[t]
     return o, S
+
+
+def kda_literal(q, k, v, alpha, beta, S0=None):
+    """Gated delta rule with a diagonal decay, in product form.
+
+    "Linear attention and recurrent memory", From fixed decay to KDA's gated
+    delta write, with the decay per key channel:
+    S_t = S_{t-1} Diag(alpha_t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+    o_t = S_t q_t, every matrix formed explicitly. alpha [T, dk].
+    """
+    T, dk = q.shape
+    dv = v.shape[1]
+    S = np.zeros((dv, dk)) if S0 is None else np.array(S0, dtype=np.float64)
+    I = np.eye(dk)
+    o = np.empty((T, dv))
+    for t in range(T):
+        kt = k[t][:, None]
+        S = S @ np.diag(alpha[t]) @ (I - beta[t] * (kt @ kt.T)) + beta[t] * np.outer(v[t], k[t])
+        o[t] = S @ q[t]
+    return o, S
+
+
+def kda_unrolled(q, k, v, alpha, beta, S0=None):
+    """Brute-force unrolled diagonal-decay delta rule (tiny T only).
+
+    With A_i = Diag(alpha_i) (I - beta_i k_i k_i^T): S_t = S_0 A_1...A_t +
+    sum_j beta_j v_j k_j^T A_{j+1}...A_t, every product rebuilt for every t.
+    """
+    T, dk = q.shape
+    dv = v.shape[1]
+    S0 = np.zeros((dv, dk)) if S0 is None else np.asarray(S0, dtype=np.float64)
+    A = [np.diag(alpha[i]) @ (np.eye(dk) - beta[i] * np.outer(k[i], k[i])) for i in range(T)]
+
+    def prod(lo, hi):
+        P = np.eye(dk)
+        for i in range(lo, hi + 1):
+            P = P @ A[i]
+        return P
+
+    o = np.empty((T, dv))
+    S = S0
+    for t in range(T):
+        S = S0 @ prod(0, t)
+        for j in range(t + 1):
+            S = S + beta[j] * np.outer(v[j], k[j]) @ prod(j + 1, t)
+        o[t] = S @ q[t]
+    return o, S

@@ -15,6 +15,7 @@
  *   norm with decay: gamma [BH]; state as norm
  *   gla:   gamma [BH, T, dk]; state = S [dk, dv] per sequence
  *   gdn:   g, beta [BH, T];   state = S [dv, dk] per sequence
+ *   kda:   alpha [BH, T, dk], beta [BH, T]; state as gdn
  * A NULL state_in means a zero initial state; a NULL state_out skips the
  * write. Return value: 0 on success, 2 if a normalizer denominator was not
  * strictly positive (norm only), 1 on allocation failure.
@@ -252,6 +253,63 @@ int la_oracle_gdn(int BH, int T, int dk, int dv,
             for (int i = 0; i < dv; ++i)                             /* S = S~ + u k^T */
                 for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] += u[i] * kt[c];
             double* ot = o + row * dv;                               /* o = S q */
+            for (int i = 0; i < dv; ++i) {
+                double acc = 0.0;
+                for (int c = 0; c < dk; ++c) acc += S[(size_t)i * dk + c] * qt[c];
+                ot[i] = acc;
+            }
+        }
+        if (state_out) memcpy(state_out + bh * sz, S, sizeof(double) * sz);
+        free(S);
+    }
+    return oom ? 1 : 0;
+}
+
+/*
+ * (c') Gated delta rule with a per-channel (diagonal) decay, S in R^{dv x dk},
+ * unit keys assumed (not enforced):
+ *   S~_t = S_{t-1} Diag(alpha_t),  S_t = S~_t + beta_t (v_t - S~_t k_t) k_t^T,
+ *   o_t = S_t q_t.
+ * "Linear attention and recurrent memory", From fixed decay to KDA's gated
+ * delta write: the decay gate of the corrective write acting per channel
+ * (KDA's finer-grained diagonal decay), taken here on the d_k (key) channels
+ * before the write, with the error against the decayed state as in (c).
+ * alpha [BH, T, dk]; alpha_t = g_t 1 is variant (c).
+ */
+int la_oracle_kda(int BH, int T, int dk, int dv,
+                  const double* q, const double* k, const double* v,
+                  const double* alpha, const double* beta, const double* state_in,
+                  double* o, double* state_out, int nthreads) {
+    int oom = 0;
+    int nt = set_threads(nthreads);
+    (void)nt;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt) reduction(|:oom)
+#endif
+    for (int bh = 0; bh < BH; ++bh) {
+        double* S = (double*)malloc(sizeof(double) * ((size_t)dk * dv + dv));
+        if (!S) { oom = 1; continue; }
+        double* u = S + (size_t)dk * dv;
+        const size_t sz = (size_t)dk * dv;
+        if (state_in) memcpy(S, state_in + bh * sz, sizeof(double) * sz);
+        else memset(S, 0, sizeof(double) * sz);
+        for (int t = 0; t < T; ++t) {
+            const size_t row = (size_t)bh * T + t;
+            const double* kt = k + row * dk;
+            const double* qt = q + row * dk;
+            const double* vt = v + row * dv;
+            const double* at = alpha + row * dk;
+            const double bt = beta[row];
+            for (int i = 0; i < dv; ++i)                             /* S~ = S Diag(alpha) */
+                for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] *= at[c];
+            for (int i = 0; i < dv; ++i) {                           /* u = beta (v - S~ k) */
+                double sk = 0.0;
+                for (int c = 0; c < dk; ++c) sk += S[(size_t)i * dk + c] * kt[c];
+                u[i] = bt * (vt[i] - sk);
+            }
+            for (int i = 0; i < dv; ++i)                             /* S = S~ + u k^T (after the decay) */
+                for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] += u[i] * kt[c];
+            double* ot = o + row * dv;                               /* o = S q, new state */
             for (int i = 0; i < dv; ++i) {
                 double acc = 0.0;
                 for (int c = 0; c < dk; ++c) acc += S[(size_t)i * dk + c] * qt[c];

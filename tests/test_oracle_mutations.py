@@ -31,6 +31,11 @@ MUTANTS = {
     "decay_after_write": (
         "S[(size_t)i * dv + j] = g * S[(size_t)i * dv + j] + f[i] * vt[j];",
         "S[(size_t)i * dv + j] = g * (S[(size_t)i * dv + j] + f[i] * vt[j]);"),
+    "kda_decay_on_value_axis": (
+        "for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] *= at[c];",
+        "for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] *= at[i % dk];"),
+    "kda_error_against_undecayed": (
+        "for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] *= at[c];", "/* decay moved below */"),
     "gla_gate_after_write": (
         "S[(size_t)i * dv + j] = gt[i] * S[(size_t)i * dv + j] + f[i] * vt[j];",
         "S[(size_t)i * dv + j] = gt[i] * (S[(size_t)i * dv + j] + f[i] * vt[j]);"),
@@ -45,8 +50,14 @@ MUTANTS = {
     "gdn_reads_with_key": ("acc += S[(size_t)i * dk + c] * qt[c];", "acc += S[(size_t)i * dk + c] * kt[c];"),
     "gdn_drops_beta": ("u[i] = bt * (vt[i] - sk);", "u[i] = (vt[i] - sk);"),
 }
-# the undecayed-error mutant keeps the decay, but applies it after the write
+# the undecayed-error mutants keep the decay, but apply it after the write
 MUTANTS_EXTRA = {
+    "kda_error_against_undecayed": (
+        "/* S = S~ + u k^T (after the decay) */\n"
+        "                for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] += u[i] * kt[c];\n",
+        "/* S = S~ + u k^T (after the decay) */\n"
+        "                for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] += u[i] * kt[c];\n"
+        "            for (int i = 0; i < dv; ++i) for (int c = 0; c < dk; ++c) S[(size_t)i * dk + c] *= at[c];\n"),
     "gdn_error_against_undecayed": (
         "double* ot = o + row * dv;                               /* o = S q */",
         "for (size_t e = 0; e < sz; ++e) S[e] *= gt; double* ot = o + row * dv;"),

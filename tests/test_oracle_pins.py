@@ -91,7 +91,7 @@ def test_norm_output_in_value_hull():
     assert np.all(o >= lo - 1e-12) and np.all(o <= hi + 1e-12)
 
 
-@pytest.mark.parametrize("variant", ["norm", "norm_decay", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "norm_decay", "gla", "gdn", "kda"])
 def test_causality(variant):
     # Changing tokens after t leaves outputs up to t bit-identical.
     r = rng(3)
@@ -105,6 +105,9 @@ def test_causality(variant):
     if variant == "gdn":
         k = unit(k)
         gate, beta = sigmoid(r.standard_normal(T) + 3), sigmoid(r.standard_normal(T))
+    if variant == "kda":
+        k = unit(k)
+        gate, beta = sigmoid(r.standard_normal((T, d)) + 3), sigmoid(r.standard_normal(T))
     o1, _, _ = one(variant, q, k, v, gate, beta)
     q2, k2, v2 = q.copy(), k.copy(), v.copy()
     q2[t0 + 1:] += 5.0
@@ -364,9 +367,74 @@ def test_figure_18_2_delta_vs_additive():
     assert np.max(np.abs(o_add[3] - expect)) <= 1e-14
 
 
+# ------------------------------------------- (c') delta rule, diagonal decay
+
+def kda_inputs(r, T, dk, dv):
+    q, k, v = r.standard_normal((T, dk)), unit(r.standard_normal((T, dk))), r.standard_normal((T, dv))
+    alpha = sigmoid(r.standard_normal((T, dk)) + 2.5)
+    beta = sigmoid(r.standard_normal(T))
+    return q, k, v, alpha, beta
+
+
+def test_kda_equals_product_form():
+    # "Linear attention and recurrent memory", the KDA bridge: the corrective
+    # write after a per-channel decay, S Diag(alpha)(I - beta k k^T) + beta v k^T.
+    r = rng(51)
+    q, k, v, alpha, beta = kda_inputs(r, 50, 12, 7)
+    S0 = r.standard_normal((7, 12)) * 0.3
+    o, st, _ = one("kda", q, k, v, alpha, beta, state=S0)
+    o_l, S_l = forms.kda_literal(q, k, v, alpha, beta, S0)
+    assert np.max(np.abs(o - o_l)) <= 1e-12 * max(1.0, np.max(np.abs(o_l)))
+    assert np.max(np.abs(st.reshape(7, 12) - S_l)) <= 1e-12 * max(1.0, np.max(np.abs(S_l)))
+
+
+def test_kda_unrolled_transition_product():
+    r = rng(52)
+    q, k, v, alpha, beta = kda_inputs(r, 6, 5, 3)
+    o, st, _ = one("kda", q, k, v, alpha, beta)
+    o_u, S_u = forms.kda_unrolled(q, k, v, alpha, beta)
+    assert np.max(np.abs(o - o_u)) <= 1e-13 and np.max(np.abs(st.reshape(3, 5) - S_u)) <= 1e-13
+
+
+def test_kda_uniform_decay_is_gdn():
+    # alpha_t = g_t on every channel is the scalar-gated delta rule (c).
+    r = rng(53)
+    T, dk, dv = 40, 8, 6
+    q, k, v, _, beta = kda_inputs(r, T, dk, dv)
+    g = sigmoid(r.standard_normal(T) + 3)
+    o1, st1, _ = one("kda", q, k, v, np.repeat(g[:, None], dk, axis=1), beta)
+    o0, st0, _ = one("gdn", q, k, v, g, beta)
+    assert np.max(np.abs(o1 - o0)) <= 1e-13 * max(1.0, np.max(np.abs(o0)))
+    assert np.max(np.abs(st1 - st0)) <= 1e-13 * max(1.0, np.max(np.abs(st0)))
+
+
+def test_kda_beta_zero_is_channel_decay():
+    # No write: each key channel of the state decays by its own running product.
+    r = rng(54)
+    T, dk, dv = 20, 6, 4
+    q, k, v, alpha, _ = kda_inputs(r, T, dk, dv)
+    S0 = r.standard_normal((dv, dk))
+    o, st, _ = one("kda", q, k, v, alpha, np.zeros(T), state=S0)
+    P = np.cumprod(alpha, axis=0)
+    for t in (0, 7, T - 1):
+        assert np.max(np.abs(o[t] - (S0 * P[t]) @ q[t])) <= 1e-13
+    assert np.max(np.abs(st.reshape(dv, dk) - S0 * P[-1])) <= 1e-13
+
+
+def test_kda_unit_key_full_write_recalls_exactly():
+    # beta = 1 and a unit key: reading that key right after the write returns
+    # the written value, whatever the decay and the state before.
+    r = rng(55)
+    T, dk, dv = 10, 8, 5
+    _, k, v, alpha, _ = kda_inputs(r, T, dk, dv)
+    S0 = r.standard_normal((dv, dk))
+    o, _, _ = one("kda", k, k, v, alpha, np.ones(T), state=S0)
+    assert np.max(np.abs(o - v)) <= 1e-12
+
+
 # ------------------------------------------------------ all: state passing
 
-@pytest.mark.parametrize("variant", ["norm", "norm_decay", "gla", "gdn"])
+@pytest.mark.parametrize("variant", ["norm", "norm_decay", "gla", "gdn", "kda"])
 def test_split_continuation_equals_one_shot(variant):
     r = rng(16)
     T, dk, dv, T1 = 37, 8, 6, 15
@@ -379,6 +447,9 @@ def test_split_continuation_equals_one_shot(variant):
     if variant == "gdn":
         k = unit(k)
         gate, beta = sigmoid(r.standard_normal(T) + 3), sigmoid(r.standard_normal(T))
+    if variant == "kda":
+        k = unit(k)
+        gate, beta = sigmoid(r.standard_normal((T, dk)) + 3), sigmoid(r.standard_normal(T))
     o, st, _ = one(variant, q, k, v, gate, beta)
     sl = lambda a, s: None if a is None else (a if np.ndim(a) == 0 else a[s])
     a, b = slice(0, T1), slice(T1, T)
