@@ -34,7 +34,8 @@ import numpy as np  # noqa: E402
 import workloads as W  # noqa: E402
 
 HEADLINE = W.NORM_B4H8_T2048_D64
-SUITE = (W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128, W.GDN_DECODE_N256H16_D128, W.NORM_DECAY_B4H8_T2048_D64)
+SUITE = (W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128, W.GDN_DECODE_N256H16_D128, W.NORM_DECAY_B4H8_T2048_D64,
+         W.KDA_DECODE_N256H16_D128)
 C_FLOPS = 64   # chunk size the algorithmic FLOP count is quoted at
 
 
@@ -77,6 +78,7 @@ def decode_step_bytes(w: W.Workload) -> int:
     n = w.B * w.H
     b = 2 * n * state_elems(w) * 4 + n * (2 * w.dk + 2 * w.dv) * io_bytes(w)
     b += n * 2 * 4 if w.variant == "gdn" else (n * w.dk * 4 if w.variant == "gla" else 0)
+    b += n * (w.dk + 1) * 4 if w.variant == "kda" else 0
     return b
 
 
@@ -220,7 +222,7 @@ class PrefillRunner:
 
 
 class DecodeRunner:
-    """The 1024-step gated-delta decode workload; inputs drawn on the device."""
+    """A gated-delta decode workload (scalar or per-channel decay); inputs drawn on the device."""
 
     def __init__(self, w: W.Workload, seed: int, torch, la):
         self.w, self.torch, self.la = w, torch, la
@@ -234,7 +236,8 @@ class DecodeRunner:
         k = torch.randn(n + (w.dk,), generator=g, device=dev)
         self.k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
         self.v = torch.randn(n + (w.dv,), generator=g, device=dev).to(torch.bfloat16)
-        self.gate = torch.sigmoid(torch.randn(n, generator=g, device=dev) + w.gate_mu)
+        gshape = n + (w.dk,) if w.variant == "kda" else n   # kda: one decay per key channel
+        self.gate = torch.sigmoid(torch.randn(gshape, generator=g, device=dev) + w.gate_mu)
         self.beta = torch.sigmoid(torch.randn(n, generator=g, device=dev) + w.beta_mu)
         self.state = torch.randn((w.B, w.H, state_elems(w)), generator=g, device=dev) * w.state_std
         self.out = torch.empty((w.B, w.H, w.dv), dtype=torch.bfloat16, device=dev)
@@ -243,7 +246,7 @@ class DecodeRunner:
     def step(self):
         for s in range(self.w.decode_steps):
             self.h.decode_step(self.q[s], self.k[s], self.v[s], self.gate[s], self.beta[s], self.state,
-                               variant="gdn", out=self.out, state_out=self.state)
+                               variant=self.w.variant, out=self.out, state_out=self.state)
 
 
 def time_steps(runner, steps: int, warmup: int, torch, dist=None):
@@ -429,7 +432,7 @@ def gpu_arm(args):
                               "us_per_decode_launch": round(launch_ms * 1e3, 3),
                               "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
                                            "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                                           "traffic": traffic_from_profiles("decode_gdn"),
+                                           "traffic": traffic_from_profiles(f"decode_{sw.variant}"),
                                            "peak_source": pk["source"] + " (burst copy bandwidth)",
                                            "algorithmic_bytes": byts},
                               "gpu_launches": steps * dr.launches_per_step})

@@ -19,14 +19,14 @@ import threading
 
 from ._build import LIB as LIB_PATH, build  # noqa: F401  (build() compiles in-tree)
 
-LA_NORM_ELU1, LA_GLA, LA_GDN, LA_NORM_DECAY = 0, 1, 2, 3
+LA_NORM_ELU1, LA_GLA, LA_GDN, LA_NORM_DECAY, LA_KDA = 0, 1, 2, 3, 4
 LA_BF16, LA_FP32 = 0, 1
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(6)
 LA_FLAG_IDENTITY_PHI = 0x1
 LA_FLAG_SEQUENTIAL_CHUNKS = 0x2
 LA_FLAG_TEST_TIMEOUT = 0x100
 
-VARIANTS = {"norm": LA_NORM_ELU1, "gla": LA_GLA, "gdn": LA_GDN, "norm_decay": LA_NORM_DECAY}
+VARIANTS = {"norm": LA_NORM_ELU1, "gla": LA_GLA, "gdn": LA_GDN, "norm_decay": LA_NORM_DECAY, "kda": LA_KDA}
 ERRORS = {1: "LA_ERR_INVALID_ARG", 2: "LA_ERR_UNSUPPORTED", 3: "LA_ERR_MISALIGNED",
           4: "LA_ERR_CUDA", 5: "LA_ERR_TIMEOUT"}
 
@@ -200,6 +200,9 @@ class Handle:
         self._expect("v", v, (B, H, T, self.d_v), self.dtype)
         if var == LA_GLA:
             self._expect("gate", gate, (B, H, T, self.d_k), torch.float32)
+        elif var == LA_KDA:
+            self._expect("gate", gate, (B, H, T, self.d_k), torch.float32)
+            self._expect("beta", beta, (B, H, T), torch.float32)
         elif var == LA_NORM_DECAY:
             self._expect("gate", gate, (B, H), torch.float32)
         elif var == LA_GDN:
@@ -242,6 +245,9 @@ class Handle:
         chk("v", v, (B, H, T, self.d_v), self.dtype)
         if var == LA_GLA:
             chk("gate", gate, (B, H, T, self.d_k), torch.float32)
+        elif var == LA_KDA:
+            chk("gate", gate, (B, H, T, self.d_k), torch.float32)
+            chk("beta", beta, (B, H, T), torch.float32)
         elif var == LA_NORM_DECAY:
             chk("gate", gate, (B, H), torch.float32)
         elif var == LA_GDN:

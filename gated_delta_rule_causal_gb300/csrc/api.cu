@@ -122,7 +122,9 @@ struct DeviceGuard {
     }
 };
 
-bool valid_variant(int v) { return v == LA_NORM_ELU1 || v == LA_GLA || v == LA_GDN || v == LA_NORM_DECAY; }
+bool valid_variant(int v) {
+    return v == LA_NORM_ELU1 || v == LA_GLA || v == LA_GDN || v == LA_NORM_DECAY || v == LA_KDA;
+}
 
 size_t state_elems(const la_config& c, int variant) {
     return static_cast<size_t>(c.d_k) * c.d_v + ((variant == LA_NORM_ELU1 || variant == LA_NORM_DECAY) ? c.d_k : 0);
@@ -132,11 +134,12 @@ int check_common(la_handle* h, const void* q, const void* k, const void* v, cons
                  const float* beta, const float* state_in, const void* out, const float* state_out,
                  const float* den_out, int variant) {
     if (!valid_variant(variant))
-        return fail(h, LA_ERR_INVALID_ARG, "variant must be LA_NORM_ELU1, LA_GLA, LA_GDN or LA_NORM_DECAY");
+        return fail(h, LA_ERR_INVALID_ARG, "variant must be LA_NORM_ELU1, LA_GLA, LA_GDN, LA_NORM_DECAY or LA_KDA");
     if (!q || !k || !v || !out) return fail(h, LA_ERR_INVALID_ARG, "q, k, v and out are required");
     if (variant != LA_NORM_ELU1 && !gate)
-        return fail(h, LA_ERR_INVALID_ARG, "gate is required for LA_GLA, LA_GDN and LA_NORM_DECAY");
-    if (variant == LA_GDN && !beta) return fail(h, LA_ERR_INVALID_ARG, "beta is required for LA_GDN");
+        return fail(h, LA_ERR_INVALID_ARG, "gate is required for LA_GLA, LA_GDN, LA_NORM_DECAY and LA_KDA");
+    if ((variant == LA_GDN || variant == LA_KDA) && !beta)
+        return fail(h, LA_ERR_INVALID_ARG, "beta is required for LA_GDN and LA_KDA");
     if (variant != LA_NORM_ELU1 && variant != LA_NORM_DECAY && den_out)
         return fail(h, LA_ERR_INVALID_ARG, "den_out is only defined for LA_NORM_ELU1 and LA_NORM_DECAY");
     const void* ptrs[] = {q, k, v, gate, beta, state_in, out, state_out, den_out};
@@ -166,7 +169,7 @@ la::FwdArgs make_args(la_handle* h, const void* q, const void* k, const void* v,
     a.dv = h->cfg.d_v;
     // LA_NORM_DECAY runs as the normalized variant with a per-(b,h) decay in
     // `gate`; plain LA_NORM_ELU1 carries no gate.
-    a.variant = (variant == LA_NORM_DECAY) ? la::kNorm : variant;
+    a.variant = (variant == LA_NORM_DECAY) ? la::kNorm : (variant == LA_KDA) ? la::kKda : variant;
     if (variant == LA_NORM_ELU1) a.gate = nullptr;
     a.io = h->cfg.io == LA_FP32 ? la::kFp32 : la::kBf16;
     a.flags = h->cfg.flags;
@@ -185,7 +188,8 @@ int enqueue_forward(la_handle* h, la::FwdArgs& a, int variant, int chunk, cudaSt
     const la_config& c = h->cfg;
     const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
     // the decayed normalized variant runs chunkwise only in the three-phase form
-    const bool chunked = tc_ok && chunk != 1 &&
+    // the per-channel-decay delta rule has no chunkwise form here
+    const bool chunked = tc_ok && chunk != 1 && variant != LA_KDA &&
                          (variant != LA_NORM_DECAY ||
                           (!(c.flags & LA_FLAG_SEQUENTIAL_CHUNKS) &&
                            la::chunk::par_fits(a.BH, a.T, c.d_k, c.d_v, h->ws_bytes)));
@@ -317,7 +321,7 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v, const 
     const la_config& c = h->cfg;
     if (T == 0) {
         if (!valid_variant(variant))
-            return fail(h, LA_ERR_INVALID_ARG, "variant must be LA_NORM_ELU1, LA_GLA, LA_GDN or LA_NORM_DECAY");
+            return fail(h, LA_ERR_INVALID_ARG, "variant must be LA_NORM_ELU1, LA_GLA, LA_GDN, LA_NORM_DECAY or LA_KDA");
         if (state_out && !aligned16(state_out)) return fail(h, LA_ERR_MISALIGNED, "state_out is not 16-byte aligned");
         if (!state_out || state_out == state_in) return LA_OK;
         DeviceGuard g(c.device);
@@ -333,6 +337,8 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v, const 
     const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
     if (chunk == 64 && !tc_ok)
         return fail(h, LA_ERR_UNSUPPORTED, "chunk 64 needs bf16 io and d_k, d_v in {64, 128}");
+    if (chunk == 64 && variant == LA_KDA)
+        return fail(h, LA_ERR_UNSUPPORTED, "LA_KDA has no chunkwise kernel: chunk must be 0 or 1");
     if (static_cast<long long>(T) * (c.d_k > c.d_v ? c.d_k : c.d_v) > (1LL << 31) - 1)
         return fail(h, LA_ERR_UNSUPPORTED, "T * d exceeds 2^31 - 1");
     DeviceGuard g(c.device);
@@ -356,6 +362,8 @@ int la_forward_host(la_handle* h, const void* q, const void* k, const void* v, c
     const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
     if (chunk == 64 && !tc_ok)
         return fail(h, LA_ERR_UNSUPPORTED, "chunk 64 needs bf16 io and d_k, d_v in {64, 128}");
+    if (chunk == 64 && variant == LA_KDA)
+        return fail(h, LA_ERR_UNSUPPORTED, "LA_KDA has no chunkwise kernel: chunk must be 0 or 1");
     if (static_cast<long long>(T) * (c.d_k > c.d_v ? c.d_k : c.d_v) > (1LL << 31) - 1)
         return fail(h, LA_ERR_UNSUPPORTED, "T * d exceeds 2^31 - 1");
     DeviceGuard g(c.device);
@@ -383,7 +391,7 @@ int la_forward_host(la_handle* h, const void* q, const void* k, const void* v, c
     const size_t io = (c.io == LA_BF16) ? 2 : 4;
     const size_t ss = state_elems(c, variant);
     const size_t tok = static_cast<size_t>(T);
-    const size_t gate_per_head = (variant == LA_GLA) ? tok * c.d_k : (variant == LA_GDN) ? tok
+    const size_t gate_per_head = (variant == LA_GLA || variant == LA_KDA) ? tok * c.d_k : (variant == LA_GDN) ? tok
                                : (variant == LA_NORM_DECAY) ? 1 : 0;
     const size_t per_head[9] = {
         tok * c.d_k * io, tok * c.d_k * io, tok * c.d_v * io,                    // q, k, v

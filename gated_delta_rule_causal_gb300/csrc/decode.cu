@@ -77,7 +77,9 @@ __device__ __forceinline__ float elu1(float x) { return x > 0.f ? x + 1.f : __ex
 constexpr int kGdnThreads = 256;
 constexpr int kGdnPasses = 8;   // row passes per warp unit (loads in flight per lane)
 
-template <int DK, typename IO>
+// PC: the per-channel decay of the kda variant (gate [BH][DK]): with
+// S~ = S Diag(alpha), S~ . k = S . (alpha o k) and S~ . q = S . (alpha o q).
+template <int DK, typename IO, bool PC>
 __global__ void __launch_bounds__(kGdnThreads) decode_gdn_kernel(FwdArgs a) {
     constexpr int LPR = DK / 4;          // lanes per row
     constexpr int RPP = 32 / LPR;        // rows per pass
@@ -117,20 +119,25 @@ __global__ void __launch_bounds__(kGdnThreads) decode_gdn_kernel(FwdArgs a) {
         }
         const float4 k4 = ld4(k + static_cast<size_t>(h) * DK + 4 * cl);
         const float4 q4 = ld4(q + static_cast<size_t>(h) * DK + 4 * cl);
-        const float g = __ldg(a.gate + h), b = __ldg(a.beta + h);
+        const float b = __ldg(a.beta + h);
+        const float g = PC ? 1.f : __ldg(a.gate + h);
+        const float4 al = PC ? __ldg(reinterpret_cast<const float4*>(a.gate + static_cast<size_t>(h) * DK) + cl)
+                             : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float4 ka = make_float4(al.x * k4.x, al.y * k4.y, al.z * k4.z, al.w * k4.w);
+        const float4 qa = make_float4(al.x * q4.x, al.y * q4.y, al.z * q4.z, al.w * q4.w);
         const float kq = group_sum<LPR>(dot4(k4, q4));
 #pragma unroll
         for (int p = 0; p < kGdnPasses; ++p) {
             const int row = r0 + p * RPP + sub;
-            const float sk = group_sum<LPR>(dot4(S[p], k4));
-            const float sq = group_sum<LPR>(dot4(S[p], q4));
+            const float sk = group_sum<LPR>(dot4(S[p], PC ? ka : k4));
+            const float sq = group_sum<LPR>(dot4(S[p], PC ? qa : q4));
             if (row < dv) {
                 const float ui = b * (vr[p] - g * sk);
                 float4 n;
-                n.x = g * S[p].x + ui * k4.x;
-                n.y = g * S[p].y + ui * k4.y;
-                n.z = g * S[p].z + ui * k4.z;
-                n.w = g * S[p].w + ui * k4.w;
+                n.x = g * al.x * S[p].x + ui * k4.x;
+                n.y = g * al.y * S[p].y + ui * k4.y;
+                n.z = g * al.z * S[p].z + ui * k4.z;
+                n.w = g * al.w * S[p].w + ui * k4.w;
                 st_stream(sout + static_cast<size_t>(row) * DK + 4 * cl, n);
                 if (cl == 0) st1(out + static_cast<size_t>(h) * dv + row, g * sq + ui * kq);
             }
@@ -229,27 +236,28 @@ __global__ void __launch_bounds__(kColThreads) decode_cols_kernel(FwdArgs a) {
     }
 }
 
-template <int DK, typename IO>
+template <int DK, typename IO, bool PC>
 cudaError_t launch_gdn_dk(const FwdArgs& a, cudaStream_t s) {
     // persistent: as many CTAs as are resident at once (cached per kernel)
     static int per_sm = 0;
     if (per_sm == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_gdn_kernel<DK, IO>, kGdnThreads, 0) != cudaSuccess ||
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_gdn_kernel<DK, IO, PC>, kGdnThreads, 0) !=
+                cudaSuccess ||
             n < 1)
             n = 1;
         per_sm = n;
     }
-    return launch_pdl(decode_gdn_kernel<DK, IO>, static_cast<unsigned>(a.sm_count * per_sm), kGdnThreads, 0, s, a);
+    return launch_pdl(decode_gdn_kernel<DK, IO, PC>, static_cast<unsigned>(a.sm_count * per_sm), kGdnThreads, 0, s, a);
 }
 
-template <typename IO>
+template <typename IO, bool PC>
 cudaError_t launch_gdn(const FwdArgs& a, cudaStream_t s) {
     switch (a.dk) {
-        case 16: return launch_gdn_dk<16, IO>(a, s);
-        case 32: return launch_gdn_dk<32, IO>(a, s);
-        case 64: return launch_gdn_dk<64, IO>(a, s);
-        case 128: return launch_gdn_dk<128, IO>(a, s);
+        case 16: return launch_gdn_dk<16, IO, PC>(a, s);
+        case 32: return launch_gdn_dk<32, IO, PC>(a, s);
+        case 64: return launch_gdn_dk<64, IO, PC>(a, s);
+        case 128: return launch_gdn_dk<128, IO, PC>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -283,7 +291,8 @@ cudaError_t launch_io(const FwdArgs& a, cudaStream_t s) {
     switch (a.variant) {
         case kNorm: return launch_cols<kNorm, IO>(a, s);
         case kGla: return launch_cols<kGla, IO>(a, s);
-        case kGdn: return launch_gdn<IO>(a, s);
+        case kGdn: return launch_gdn<IO, false>(a, s);
+        case kKda: return launch_gdn<IO, true>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -6,7 +6,7 @@
 
 namespace la {
 
-enum Variant : int { kNorm = 0, kGla = 1, kGdn = 2 };
+enum Variant : int { kNorm = 0, kGla = 1, kGdn = 2, kKda = 3 };   // kKda: gated delta rule, per-channel decay
 enum Io : int { kBf16 = 0, kFp32 = 1 };
 
 // Everything a launch needs. Pointers are device pointers owned by the caller.

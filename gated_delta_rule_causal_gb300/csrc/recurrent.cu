@@ -6,7 +6,8 @@
 //
 // One CTA per (b,h). Thread j < d_v owns one d_v index of the state in
 // registers: column j of S [d_k, d_v] for the norm/gla variants, row j of
-// S [d_v, d_k] for the gated delta rule. Tokens are staged in shared memory
+// S [d_v, d_k] for the gated delta rule (scalar or per-channel decay). Tokens
+// are staged in shared memory
 // kTB at a time.
 #include <cuda_bf16.h>
 
@@ -44,7 +45,8 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(FwdArgs a) {
     __shared__ float sq[kTB][DK];
     __shared__ float sk[kTB][DK];
     __shared__ float sv[kTB][128];
-    __shared__ float sg[kTB][VAR == kGla ? DK : 1];
+    __shared__ float sg[kTB][(VAR == kGla || VAR == kKda) ? DK : 1];
+    constexpr bool DELTA = (VAR == kGdn || VAR == kKda);   // S [d_v, d_k], delta-rule write
     __shared__ float sgs[kTB], sbs[kTB], sden[kTB];
     __shared__ float pz[kTB][DK];
     __shared__ float zsh[DK];
@@ -62,7 +64,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(FwdArgs a) {
 #pragma unroll
     for (int i = 0; i < DK; ++i) {
         float x = 0.f;
-        if (own && sin) x = (VAR == kGdn) ? sin[static_cast<size_t>(tid) * DK + i] : sin[static_cast<size_t>(i) * dv + tid];
+        if (own && sin) x = DELTA ? sin[static_cast<size_t>(tid) * DK + i] : sin[static_cast<size_t>(i) * dv + tid];
         s[i] = x;
     }
     if (VAR == kNorm && tid < DK) zsh[tid] = sin ? sin[static_cast<size_t>(DK) * dv + tid] : 0.f;
@@ -74,16 +76,16 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(FwdArgs a) {
             const int t = e / DK, c = e % DK;
             const size_t gi = static_cast<size_t>(t0 + t) * DK + c;
             const float qv = ld_io(q, gi), kv = ld_io(k, gi);
-            sq[t][c] = (VAR != kGdn && phi_on) ? elu1(qv) : qv;
-            sk[t][c] = (VAR != kGdn && phi_on) ? elu1(kv) : kv;
-            if (VAR == kGla) sg[t][c] = a.gate[(static_cast<size_t>(bh) * T + t0 + t) * DK + c];
+            sq[t][c] = (!DELTA && phi_on) ? elu1(qv) : qv;
+            sk[t][c] = (!DELTA && phi_on) ? elu1(kv) : kv;
+            if (VAR == kGla || VAR == kKda) sg[t][c] = a.gate[(static_cast<size_t>(bh) * T + t0 + t) * DK + c];
         }
         for (int e = tid; e < nt * dv; e += kThreads) {
             const int t = e / dv, c = e % dv;
             sv[t][c] = ld_io(v, static_cast<size_t>(t0 + t) * dv + c);
         }
-        if (VAR == kGdn && tid < nt) {
-            sgs[tid] = a.gate[static_cast<size_t>(bh) * T + t0 + tid];
+        if (DELTA && tid < nt) {
+            if (VAR == kGdn) sgs[tid] = a.gate[static_cast<size_t>(bh) * T + t0 + tid];
             sbs[tid] = a.beta[static_cast<size_t>(bh) * T + t0 + tid];
         }
         __syncthreads();
@@ -124,11 +126,11 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(FwdArgs a) {
                         o += sq[t][i] * s[i];
                     }
                 } else {
-                    const float g = sgs[t], b = sbs[t];
+                    const float b = sbs[t];
                     float sk_dot = 0.f;
 #pragma unroll
                     for (int c = 0; c < DK; ++c) {
-                        s[c] *= g;                      // S~ = g S
+                        s[c] *= (VAR == kKda) ? sg[t][c] : sgs[t];   // S~ = S Diag(alpha) (kda) or g S
                         sk_dot += s[c] * sk[t][c];
                     }
                     const float u = b * (vj - sk_dot);  // beta (v - S~ k)
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) recurrent_kernel(FwdArgs a) {
         if (own) {
 #pragma unroll
             for (int i = 0; i < DK; ++i) {
-                if (VAR == kGdn) so[static_cast<size_t>(tid) * DK + i] = s[i];
+                if (DELTA) so[static_cast<size_t>(tid) * DK + i] = s[i];
                 else so[static_cast<size_t>(i) * dv + tid] = s[i];
             }
         }
@@ -177,6 +179,7 @@ cudaError_t launch_var(const FwdArgs& a, cudaStream_t s) {
         case kNorm: return launch_dk<kNorm, IO>(a, s);
         case kGla: return launch_dk<kGla, IO>(a, s);
         case kGdn: return launch_dk<kGdn, IO>(a, s);
+        case kKda: return launch_dk<kKda, IO>(a, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -3,7 +3,7 @@
  * state, for NVIDIA GB300 (sm_103a).
  *
  * The operator runs a sequence of tokens through a recurrent matrix state,
- * one independent recurrence per (batch, head). Four variants:
+ * one independent recurrence per (batch, head). Five variants:
  *
  *   LA_NORM_ELU1  normalized kernel attention, phi(x) = elu(x) + 1:
  *                   S_t = S_{t-1} + phi(k_t) v_t^T,   z_t = z_{t-1} + phi(k_t),
@@ -25,6 +25,11 @@
  *                   o_t = S_t q_t.
  *                 ("Beyond attention", section 18.2; "Linear Attention"
  *                 concept page, gated delta rule.)
+ *   LA_KDA        LA_GDN with a per-channel (diagonal) decay on the key channels:
+ *                   S_t = S_{t-1} Diag(alpha_t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *                 alpha_t in (0,1]^{d_k}. ("Linear attention and recurrent
+ *                 memory", From fixed decay to KDA's gated delta write.)
+ *                 Runs on the recurrent kernel (chunk 0 or 1) and the decode step.
  *
  * Every variant updates first and then reads, so token t attends to itself.
  *
@@ -36,17 +41,18 @@
  *              LA_NORM_DECAY: [B, H] fp32, gamma in (0, 1], one per sequence-head
  *              LA_GLA: [B, H, T, d_k] fp32, gamma in (0, 1]
  *              LA_GDN: [B, H, T] fp32, g in (0, 1]
- *   beta       LA_GDN: [B, H, T] fp32 in [0, 1]; NULL otherwise
+ *              LA_KDA: [B, H, T, d_k] fp32, alpha in (0, 1]
+ *   beta       LA_GDN, LA_KDA: [B, H, T] fp32 in [0, 1]; NULL otherwise
  *   state      fp32, one block per (b,h):
  *              LA_NORM_ELU1, LA_NORM_DECAY: S [d_k, d_v] immediately followed by z [d_k]
  *              LA_GLA:       S [d_k, d_v]
- *              LA_GDN:       S [d_v, d_k]
+ *              LA_GDN, LA_KDA: S [d_v, d_k]
  *   den_out    LA_NORM_ELU1, LA_NORM_DECAY, optional: [B, H, T] fp32
  *              denominators phi(q_t)^T z_t.
  * For la_decode_step, drop the T axis: q,k [B,H,d_k], v,out [B,H,d_v],
- * gate [B,H,d_k] (gla) or [B,H] (gdn, norm with decay), beta [B,H].
+ * gate [B,H,d_k] (gla, kda) or [B,H] (gdn, norm with decay), beta [B,H].
  *
- * Keys of LA_GDN are assumed to have unit L2 norm; the library does not
+ * Keys of LA_GDN and LA_KDA are assumed to have unit L2 norm; the library does not
  * normalize them. No scale is applied to q.
  *
  * OWNERSHIP. The caller owns every buffer. Pointers to q, k, v, gate, beta,
@@ -89,7 +95,7 @@ extern "C" {
 
 typedef struct la_handle la_handle;
 
-typedef enum { LA_NORM_ELU1 = 0, LA_GLA = 1, LA_GDN = 2, LA_NORM_DECAY = 3 } la_variant;
+typedef enum { LA_NORM_ELU1 = 0, LA_GLA = 1, LA_GDN = 2, LA_NORM_DECAY = 3, LA_KDA = 4 } la_variant;
 
 /* dtype of q, k, v and out. State, gates and beta are always fp32. */
 typedef enum { LA_BF16 = 0, LA_FP32 = 1 } la_dtype;

@@ -31,7 +31,8 @@ def per_token(a, variant):
 
 def base(variant, d):
     w = {"norm": W.NORM_B4H8_T2048_D64, "gla": W.GLA_B4H16_T4096_D128, "gdn": W.GDN_B2H16_T8192_D128,
-         "norm_decay": W.NORM_DECAY_B4H8_T2048_D64}[variant]
+         "norm_decay": W.NORM_DECAY_B4H8_T2048_D64,
+         "kda": W.KDA_DECODE_N256H16_D128.with_(B=4, H=16, T=2048, decode_steps=0, state_std=0.0)}[variant]
     return W.small(w, B=1, H=2, dk=d, dv=d)
 
 
@@ -45,7 +46,7 @@ def oracle_run(w, inp, state_in=None):
     return oracle.run(w.variant, q, k, v, g, b, sin)
 
 
-def assert_parity(w, inp, chunk=0, state_in=None, tol=None, flags=0):
+def assert_parity(w, inp, chunk=0, state_in=None, tol=None, flags=0, launches=None):
     h = handle(w, flags=flags)
     o, st, den = run_gpu_prefill(h, w, inp, chunk, state_in, with_den=(w.variant in NORMED))
     ref = oracle_run(w, inp, state_in)
@@ -57,6 +58,8 @@ def assert_parity(w, inp, chunk=0, state_in=None, tol=None, flags=0):
     if den is not None:
         e_d = float(np.max(np.abs(den - ref.den) / ref.den))
         assert e_d <= tol, f"denominator rel err {e_d:.3g} > {tol}"
+    if launches is not None:
+        assert h.last_launches() == launches
     h.close()
     return e_o, e_s
 
@@ -145,7 +148,7 @@ def test_gdn_small_gates_and_full_beta():
 
 # ------------------------------------------------------------- recurrent path
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay", "kda"])
 @pytest.mark.parametrize("d", [16, 32, 64, 128])
 @pytest.mark.parametrize("io", ["fp32", "bf16"])
 def test_recurrent_prefill_parity(variant, d, io):
@@ -191,10 +194,43 @@ def test_norm_decay_edge_gammas(gamma, chunk):
         assert slice_rel_err(o_d, o_n) <= 1e-2 and slice_rel_err(st_d, st_n) <= 1e-3
 
 
+# ------------------------------------------------------------- per-channel delta rule (kda)
+
+@pytest.mark.parametrize("T", [1, 64, 333])
+def test_kda_default_prefill_parity(T):
+    # chunk 0 runs the recurrent kernel for this variant, bf16 io, d = 128
+    w = base("kda", 128).with_(T=T)
+    assert_parity(w, W.draw(w, seed=T), chunk=0, launches=1)
+
+
+def test_kda_uniform_decay_matches_gdn():
+    # alpha_t = g_t on every channel is the scalar-gated rule, through both paths
+    w = base("kda", 64).with_(T=150)
+    inp = W.draw(w, seed=9)
+    g = inp.gate[..., 0].copy()
+    inp.gate[...] = g[..., None]
+    h = handle(w)
+    o_k, st_k, _ = run_gpu_prefill(h, w, inp, 1)
+    wg = base("gdn", 64).with_(T=150)
+    o_g, st_g, _ = run_gpu_prefill(h, wg, W.Inputs(inp.q, inp.k, inp.v, g, inp.beta, None), 1)
+    h.close()
+    assert slice_rel_err(o_k, o_g) <= 1e-5 and slice_rel_err(st_k, st_g) <= 1e-5
+
+
+def test_kda_rejects_chunk_64():
+    w = base("kda", 64).with_(T=64)
+    inp = W.draw(w, seed=1)
+    h = handle(w)
+    with pytest.raises(la.LAError):
+        run_gpu_prefill(h, w, inp, 64)
+    assert "LA_KDA" in la.la_last_error(h._h)
+    h.close()
+
+
 # ------------------------------------------------------------- prefill from host memory
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
-@pytest.mark.parametrize("H,T,chunk", [(5, 200, 64), (8, 130, 64), (3, 70, 1)])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay", "kda"])
+@pytest.mark.parametrize("H,T,chunk", [(5, 200, 0), (8, 130, 0), (3, 70, 1)])
 def test_forward_host_parity(variant, H, T, chunk):
     # la_forward_host: groups of sequence-heads copied in, computed and copied
     # out on overlapping streams; 5 heads make groups of 3 and 2.
@@ -227,13 +263,14 @@ def test_forward_host_parity(variant, H, T, chunk):
 
 # ------------------------------------------------------------- state passing
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay", "kda"])
 def test_split_continuation(variant):
+    ck = 0 if variant == "kda" else 64   # kda has no chunkwise kernel
     w = base(variant, 128).with_(T=192)
     inp = W.draw(w, seed=21)
     T1 = 80    # not a chunk multiple
     h = handle(w)
-    o_full, st_full, _ = run_gpu_prefill(h, w, inp, 64)
+    o_full, st_full, _ = run_gpu_prefill(h, w, inp, ck)
 
     def part(a, sl):
         return None if a is None else np.ascontiguousarray(a[:, :, sl])
@@ -244,8 +281,8 @@ def test_split_continuation(variant):
                      g1, part(inp.beta, slice(0, T1)), None)
     second = W.Inputs(part(inp.q, slice(T1, None)), part(inp.k, slice(T1, None)), part(inp.v, slice(T1, None)),
                       g2, part(inp.beta, slice(T1, None)), None)
-    o1, st1, _ = run_gpu_prefill(h, w.with_(T=T1), first, 64)
-    o2, st2, _ = run_gpu_prefill(h, w.with_(T=w.T - T1), second, 64, state_in=st1.astype(np.float32))
+    o1, st1, _ = run_gpu_prefill(h, w.with_(T=T1), first, ck)
+    o2, st2, _ = run_gpu_prefill(h, w.with_(T=w.T - T1), second, ck, state_in=st1.astype(np.float32))
     ref = oracle_run(w, inp)
     assert slice_rel_err(np.concatenate([o1, o2], axis=2), ref.o) <= 2e-2
     assert slice_rel_err(st2, ref.state) <= 2e-2
@@ -258,7 +295,7 @@ def decode_inputs(w, step, seed):
     return W.draw_decode_step(w, step, seed)
 
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay", "kda"])
 @pytest.mark.parametrize("d", [16, 64, 128])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_decode_parity(variant, d, in_place):
@@ -289,8 +326,9 @@ def test_decode_parity(variant, d, in_place):
         s_dev = s_new
 
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay"])
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay", "kda"])
 def test_prefill_then_decode_equals_longer_prefill(variant):
+    ck = 0 if variant == "kda" else 64   # kda has no chunkwise kernel
     w = base(variant, 128).with_(T=100)
     inp = W.draw(w, seed=31)
     T1 = 97
@@ -299,7 +337,7 @@ def test_prefill_then_decode_equals_longer_prefill(variant):
     pre = W.Inputs(cut(inp.q, slice(0, T1)), cut(inp.k, slice(0, T1)), cut(inp.v, slice(0, T1)),
                    cut(inp.gate, slice(0, T1)) if per_token(inp.gate, variant) else inp.gate,
                    cut(inp.beta, slice(0, T1)), None)
-    _, st, _ = run_gpu_prefill(h, w.with_(T=T1), pre, 64)
+    _, st, _ = run_gpu_prefill(h, w.with_(T=T1), pre, ck)
     s_dev = torch.from_numpy(st.astype(np.float32)).cuda()
     outs = []
     for t in range(T1, w.T):
@@ -420,6 +458,7 @@ def test_rejected_calls_do_not_launch():
     ("gla", 200, 0, 1, 1),                                   # the recurrent kernel
     ("norm_decay", 200, 0, 64, 3),                           # decayed: the three-phase form
     ("norm_decay", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),  # decayed, not three-phase: recurrent
+    ("kda", 200, 0, 0, 1),                                   # per-channel delta rule: recurrent
 ])
 def test_launch_counts(variant, T, flags, chunk, expect):
     # la_last_launches reports the kernels one call enqueued, which names the

@@ -85,7 +85,7 @@ def _unit_rows(x: np.ndarray) -> np.ndarray:
 class Workload:
     """One synthetic workload: shapes, dtypes and value distributions."""
     name: str
-    variant: str          # norm | gla | gdn | norm_decay
+    variant: str          # norm | gla | gdn | norm_decay | kda
     B: int
     H: int
     T: int                # tokens per sequence (1 for one decode step)
@@ -125,6 +125,10 @@ GLA_B4H16_T4096_D128 = Workload(
 NORM_DECAY_B4H8_T2048_D64 = Workload(
     "norm_decay_b4h8_t2048_d64_bf16", "norm_decay", 4, 8, 2048, 64, 64, "bf16", qkv_scale=0.5, gate_mu=4.0,
     note="normalized elu+1 with a fixed decay per head gamma=sigmoid(N(4,1)), bf16 q,k,v N(0,1)*0.5")
+KDA_DECODE_N256H16_D128 = Workload(
+    "kda_decode_n256h16_d128_s256", "kda", 256, 16, 1, 128, 128, "bf16",
+    unit_keys=True, gate_mu=4.0, beta_mu=0.0, state_std=0.02, decode_steps=256,
+    note="delta rule with a per-channel decay, decode: alpha=sigmoid(N(4,1)) per channel, 256 steps")
 GDN_B2H16_T8192_D128 = Workload(
     "gdn_b2h16_t8192_d128_bf16", "gdn", 2, 16, 8192, 128, 128, "bf16",
     unit_keys=True, gate_mu=4.0, beta_mu=0.0,
@@ -138,7 +142,7 @@ ALL = (NORM_T64_D16, NORM_B4H8_T2048_D64, GLA_B4H16_T4096_D128,
        GDN_B2H16_T8192_D128, GDN_DECODE_N256H16_D128)
 # Beyond the five: the normalized variant with a fixed decay per head, on
 # the shapes of the normalized headline workload.
-EXTRA = (NORM_DECAY_B4H8_T2048_D64,)
+EXTRA = (NORM_DECAY_B4H8_T2048_D64, KDA_DECODE_N256H16_D128)
 BY_NAME = {w.name: w for w in ALL + EXTRA}
 
 
@@ -152,7 +156,7 @@ class Inputs:
     q: np.ndarray
     k: np.ndarray
     v: np.ndarray
-    gate: np.ndarray | None   # norm: None; gla: [B,H,T,dk]; gdn: [B,H,T]; norm_decay: [B,H]
+    gate: np.ndarray | None   # norm: None; gla, kda: [B,H,T,dk]; gdn: [B,H,T]; norm_decay: [B,H]
     beta: np.ndarray | None   # gdn: [B,H,T]; else None
     state: np.ndarray | None  # fp32 initial state or None (zeros)
 
@@ -171,6 +175,9 @@ def _draw_qkvgb(rng: np.random.Generator, w: Workload, lead: tuple) -> tuple:
         beta = _sigmoid(rng.standard_normal(lead) + w.beta_mu)
     elif w.variant == "norm_decay":   # one fixed decay per sequence-head
         gate = _sigmoid(rng.standard_normal(lead[:2]) + w.gate_mu)
+    elif w.variant == "kda":          # per-channel decay of the delta rule
+        gate = _sigmoid(rng.standard_normal(lead + (w.dk,)) + w.gate_mu)
+        beta = _sigmoid(rng.standard_normal(lead) + w.beta_mu)
     return q, k, v, gate, beta
 
 
