@@ -35,7 +35,7 @@ import workloads as W  # noqa: E402
 
 HEADLINE = W.NORM_B4H8_T2048_D64
 SUITE = (W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128, W.GDN_DECODE_N256H16_D128, W.NORM_DECAY_B4H8_T2048_D64,
-         W.KDA_DECODE_N256H16_D128)
+         W.KDA_B2H16_T8192_D128, W.KDA_DECODE_N256H16_D128)
 C_FLOPS = 64   # chunk size the algorithmic FLOP count is quoted at
 
 
@@ -57,6 +57,8 @@ def prefill_bytes(w: W.Workload) -> int:
         b += n * w.dk * 4
     elif w.variant == "gdn":
         b += n * 2 * 4
+    elif w.variant == "kda":
+        b += n * (w.dk + 1) * 4
     elif w.variant == "norm_decay":
         b += w.B * w.H * 4
     return b + w.B * w.H * state_elems(w) * 4

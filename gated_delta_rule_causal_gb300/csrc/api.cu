@@ -188,8 +188,7 @@ int enqueue_forward(la_handle* h, la::FwdArgs& a, int variant, int chunk, cudaSt
     const la_config& c = h->cfg;
     const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
     // the decayed normalized variant runs chunkwise only in the three-phase form
-    // the per-channel-decay delta rule has no chunkwise form here
-    const bool chunked = tc_ok && chunk != 1 && variant != LA_KDA &&
+    const bool chunked = tc_ok && chunk != 1 &&
                          (variant != LA_NORM_DECAY ||
                           (!(c.flags & LA_FLAG_SEQUENTIAL_CHUNKS) &&
                            la::chunk::par_fits(a.BH, a.T, c.d_k, c.d_v, h->ws_bytes)));
@@ -257,7 +256,9 @@ int la_create(const la_config* cfg, la_handle** out) {
     h->ws_bytes = static_cast<size_t>(h->sm_count) * (static_cast<size_t>(cfg->d_k) * cfg->d_v + cfg->d_k) * sizeof(float);
     const bool tc_shape = cfg->io == LA_BF16 && (cfg->d_k == 64 || cfg->d_k == 128) && (cfg->d_v == 64 || cfg->d_v == 128);
     if (tc_shape) {
-        const size_t gdn = la::chunk::gdn_workspace_bytes(cfg->B * cfg->H, cfg->d_k, cfg->d_v, la::chunk::kGdnWindow);
+        // (sized for the per-channel decay, whose slots are the larger)
+        const size_t gdn =
+            la::chunk::gdn_workspace_bytes(cfg->B * cfg->H, cfg->d_k, cfg->d_v, la::chunk::kGdnWindow, true);
         if (gdn > h->ws_bytes) h->ws_bytes = gdn;
         // three-phase normalized / gated prefill: per-chunk states of up to
         // 128 chunks (T = 8192) per sequence-head, capped at the L2 budget
@@ -337,8 +338,6 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v, const 
     const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
     if (chunk == 64 && !tc_ok)
         return fail(h, LA_ERR_UNSUPPORTED, "chunk 64 needs bf16 io and d_k, d_v in {64, 128}");
-    if (chunk == 64 && variant == LA_KDA)
-        return fail(h, LA_ERR_UNSUPPORTED, "LA_KDA has no chunkwise kernel: chunk must be 0 or 1");
     if (static_cast<long long>(T) * (c.d_k > c.d_v ? c.d_k : c.d_v) > (1LL << 31) - 1)
         return fail(h, LA_ERR_UNSUPPORTED, "T * d exceeds 2^31 - 1");
     DeviceGuard g(c.device);
@@ -362,8 +361,6 @@ int la_forward_host(la_handle* h, const void* q, const void* k, const void* v, c
     const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
     if (chunk == 64 && !tc_ok)
         return fail(h, LA_ERR_UNSUPPORTED, "chunk 64 needs bf16 io and d_k, d_v in {64, 128}");
-    if (chunk == 64 && variant == LA_KDA)
-        return fail(h, LA_ERR_UNSUPPORTED, "LA_KDA has no chunkwise kernel: chunk must be 0 or 1");
     if (static_cast<long long>(T) * (c.d_k > c.d_v ? c.d_k : c.d_v) > (1LL << 31) - 1)
         return fail(h, LA_ERR_UNSUPPORTED, "T * d exceeds 2^31 - 1");
     DeviceGuard g(c.device);

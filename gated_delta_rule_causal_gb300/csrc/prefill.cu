@@ -43,7 +43,7 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     } else {
         m.g = m.q;
     }
-    if (a.variant == kGdn) {
+    if (a.variant == kGdn || a.variant == kKda) {
         *what = "chunked prefill launch";
         return chunk::launch_gdn(a, m, s);
     }

@@ -41,6 +41,24 @@
 // Tail chunks: TMA zero-fills rows past T; padded tokens have g = 1 and
 // beta = 0, which makes their rows of A, W and Ut zero, so they leave the
 // state untouched; no output row past T is written.
+//
+// Per-channel decay (the KDA form of the rule, "Linear attention and
+// recurrent memory", from fixed decay to KDA: S_t = S_{t-1} Diag(alpha_t)
+// (I - beta_t k_t k_t^T) + beta_t v_t k_t^T). With Gam_t = the per-channel
+// product of alpha inside the chunk up to t (a d_k vector), the same
+// derivation gives
+//    A_tj = beta_t (k_t o Gam_t).(k_j / Gam_j),   W = T diag(beta) (K o Gam)
+//    O^T  = X_0 (Q o Gam)^T + U^T P^T,           P_tj = (q_t o Gam_t).(k_j / Gam_j)
+//    X    = X_0 Diag(Gam_C) + U^T (K o Gam_C / Gam)
+// A ratio Gam_t / Gam_j is never formed across a whole chunk: inside each
+// 16-token sub-chunk a the factors are taken relative to a reference token
+// (the 8th of the sub-chunk, cumulative log2 r_a), so the row operand
+// [K;Q] o 2^(G_t - r_a) and the column operand K o 2^(r_a - G_j) of the
+// pair products span at most eight tokens of decay each; columns of later
+// sub-chunks b > a(j) use 2^(r_b - G_j) <= 1. Every other factor (Gam_t,
+// Gam_C / Gam_t, Gam_C) is at most 1. Exact in fp32 while every alpha >=
+// 2^-15. The prep CTAs write Q o Gam and K o Gam_C / Gam into the slot, so
+// the chain CTAs load no q or k tiles of their own.
 #include "prefill.h"
 #include "prefill_impl.cuh"
 #include "launch.cuh"
@@ -64,29 +82,39 @@ __host__ __device__ constexpr uint32_t align1024(uint32_t x) { return (x + 1023u
 
 // One chunk's intermediates, byte-identical in the workspace and in shared
 // memory. Tiles are bf16 with the 128-byte swizzle (1024-aligned offsets).
-template <int DK, int DV>
+// With the per-channel decay (KDA) the slot also carries Q o Gam and
+// K o Gam_C / Gam ([64][DK] K-major tiles, KA atoms of 8 KB), and its vector
+// is Gam_C [DK].
+template <int DK, int DV, bool KDA>
 struct Slot {
+    static constexpr int KA = DK / 64;
     static constexpr uint32_t W_OFF = 0;                  // W^T [dk][64 t]: MN-major B operand
     static constexpr uint32_t U_OFF = DK * 128;           // Ut^T [dv][64 t]
     static constexpr uint32_t P_OFF = U_OFF + DV * 128;   // P [64 t][64 j]: K-major B operand
-    static constexpr uint32_t V_OFF = P_OFF + 8192;       // gam_t [64], gam_C/gam_t [64] (fp32)
+    static constexpr uint32_t QG_OFF = P_OFF + 8192;      // KDA: Q o Gam        [64 t][DK]
+    static constexpr uint32_t KP_OFF = QG_OFF + (KDA ? KA * 8192 : 0);   // KDA: K o Gam_C/Gam [64 j][DK]
+    static constexpr uint32_t V_OFF = KP_OFF + (KDA ? KA * 8192 : 0);
+    // gdn: gam_t [64], gam_C/gam_t [64]; KDA: Gam_C [DK] (fp32)
     static constexpr uint32_t BYTES = V_OFF + 512;
     static_assert(BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
 
-template <int DK, int DV>
+template <int DK, int DV, bool KDA>
 struct ChainLayout {
     static constexpr int KA = DK / 64;
-    using S = Slot<DK, DV>;
-    static constexpr uint32_t Q_OFF = 0;                   // q [64 t][DK], KA atoms of 8 KB
-    static constexpr uint32_t K_OFF = KA * 8192;           // k [64 j][DK]
-    static constexpr uint32_t SLOT_OFF = 2 * KA * 8192;
+    using S = Slot<DK, DV, KDA>;
+    // gdn: q and k come by TMA in front of the slot; KDA: the slot holds
+    // their rescaled forms.
+    static constexpr uint32_t QK_BYTES = KDA ? 0 : 2 * KA * 8192;
+    static constexpr uint32_t Q_OFF = KDA ? S::QG_OFF : 0;              // q [64 t][DK], KA atoms of 8 KB
+    static constexpr uint32_t K_OFF = KDA ? S::KP_OFF : KA * 8192;      // k [64 j][DK]
+    static constexpr uint32_t SLOT_OFF = QK_BYTES;
     static constexpr uint32_t STAGE = align1024(SLOT_OFF + S::BYTES);
-    static constexpr uint32_t TX = 2 * KA * 8192 + S::BYTES;
+    static constexpr uint32_t TX = QK_BYTES + S::BYTES;
     static constexpr uint32_t OFF_SS = 2 * STAGE;               // X_0 bf16 [128 rows][DK]
     static constexpr uint32_t OFF_US = OFF_SS + KA * 16384;     // U^T bf16 [128 rows][64 j]
-    static constexpr uint32_t OFF_US2 = OFF_US + 16384;         // U^T diag(gam_C/gam)
-    static constexpr uint32_t OFF_VEC = OFF_US2 + 16384;        // gam_t, gam_C/gam_t per stage
+    static constexpr uint32_t OFF_US2 = KDA ? OFF_US : OFF_US + 16384;   // U^T diag(gam_C/gam) (gdn)
+    static constexpr uint32_t OFF_VEC = OFF_US2 + 16384;        // the slot vector per stage
     static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 512;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
     // TMEM columns (lanes = value rows)
@@ -101,7 +129,7 @@ template <int DK, int DV>
 struct PrepLayout {
     static constexpr int KA = DK / 64;
     static constexpr int VA = DV / 64;
-    using S = Slot<DK, DV>;
+    using S = Slot<DK, DV, false>;
     static constexpr uint32_t QK_BYTES = KA * 16384;    // per k-atom: rows 0-63 k, rows 64-127 q
     static constexpr uint32_t V_BYTES = VA * 8192;
     static constexpr uint32_t STAGE = QK_BYTES + V_BYTES;
@@ -122,14 +150,50 @@ struct PrepLayout {
 };
 constexpr int kRStride = 40;   // fp32 row stride of the merge scratch (conflict-free fragment reads)
 
+// Prep CTA of the per-channel decay. [K;Q] is double-buffered and rescaled
+// in place into the row operand; V, the fp32 gate tile and the outgoing slot
+// are single-buffered (V and the gates of the next unit are loaded once the
+// MMAs that read their buffer are done; the slot store of the previous unit
+// has drained before the buffer is written again). The column operands of
+// the four sub-chunks (16, 32, 48, 64 rows) are written over the gate tile
+// and TB1, both of which are dead while they live.
 template <int DK, int DV>
+struct PrepLayoutKda {
+    static constexpr int KA = DK / 64;
+    static constexpr int VA = DV / 64;
+    using S = Slot<DK, DV, true>;
+    static constexpr uint32_t QK_BYTES = KA * 16384;     // per k-atom: rows 0-63 k, rows 64-127 q
+    static constexpr uint32_t OFF_V = 2 * QK_BYTES;      // V [64 t][DV]
+    static constexpr uint32_t OFF_GATE = OFF_V + VA * 8192;   // alpha fp32 [64 t][DK]
+    static constexpr uint32_t OFF_TB1 = OFF_GATE + DK * 256;  // T diag(beta) bf16 [t][j]
+    static constexpr uint32_t OFF_B = OFF_GATE;               // column operands, over gate + TB1
+    static constexpr uint32_t B_BYTES = 160 * 128 * KA;
+    static_assert(B_BYTES <= DK * 256 + 8192, "column operands fit over the gate tile and TB1");
+    static constexpr uint32_t OFF_OUT = align1024(OFF_TB1 + 8192);
+    static constexpr uint32_t OFF_AS = OFF_OUT + align1024(S::BYTES);   // fp32 [64][kAStride]
+    static constexpr uint32_t OFF_RS = OFF_AS + C * kAStride * 4;        // fp32 [32][kRStride]
+    static constexpr uint32_t OFF_BLK = OFF_RS + 32 * 40 * 4;            // log2-gate sums of 8-token blocks [8][DK]
+    static constexpr uint32_t OFF_PR = OFF_BLK + 8 * DK * 4;             // 2^r_a [4][DK]
+    static constexpr uint32_t OFF_MISC = OFF_PR + 4 * DK * 4;            // beta [64]
+    static constexpr uint32_t OFF_BAR = OFF_MISC + 64 * 4;
+    static constexpr uint32_t BYTES = OFF_BAR + 128;
+    // Column operand of sub-chunk a: rows j < 16(a+1), KA atoms of 2048(a+1) bytes.
+    static __host__ __device__ constexpr uint32_t b_off(int a) { return OFF_B + 1024u * KA * a * (a + 1); }
+    static constexpr uint32_t COL_G = 0;     // [K;Q] B_a^T, four blocks of 64 columns
+    static constexpr uint32_t COL_W = 0;     // W^T per sub-chunk (four blocks; the products above are read by then)
+    static constexpr uint32_t COL_UT = 256;  // Ut^T [dv][64]
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+
+template <int DK, int DV, bool KDA>
 constexpr uint32_t smem_alloc() {
-    return (ChainLayout<DK, DV>::BYTES > PrepLayout<DK, DV>::BYTES ? ChainLayout<DK, DV>::BYTES
-                                                                   : PrepLayout<DK, DV>::BYTES) + 1024;
+    constexpr uint32_t prep = KDA ? PrepLayoutKda<DK, DV>::BYTES : PrepLayout<DK, DV>::BYTES;
+    constexpr uint32_t chain = ChainLayout<DK, DV, KDA>::BYTES;
+    return (chain > prep ? chain : prep) + 1024;
 }
 
 struct Params {
-    const float* gate;      // [BH, T]
+    const float* gate;      // [BH, T]; per-channel decay: [BH, T, DK]
     const float* beta;      // [BH, T]
     const float* state_in;  // [BH, DV, DK] or NULL (zeros)
     float* state_out;       // [BH, DV, DK] or NULL
@@ -155,11 +219,11 @@ __device__ __forceinline__ void st_global_b32(void* p, uint32_t v) {
 // ============================================================================
 // chain CTA: the state-dependent part of every chunk of one window
 // ============================================================================
-template <int DK, int DV>
+template <int DK, int DV, bool KDA>
 __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtensorMap* tmk, const Params& p,
                                            uint8_t* sm, uint32_t sbase) {
-    using L = ChainLayout<DK, DV>;
-    using S = Slot<DK, DV>;
+    using L = ChainLayout<DK, DV, KDA>;
+    using S = Slot<DK, DV, KDA>;
     constexpr int KA = L::KA, DKH = DK / 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool control = warp == kConv / 32;
@@ -192,7 +256,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (control && lane == 0) {
+    if (!KDA && control && lane == 0) {
         tma_prefetch_desc(tmq);
         tma_prefetch_desc(tmk);
     }
@@ -228,10 +292,12 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                 const int c = p.chain_c0 + i;
                 uint8_t* stg = sm + s * L::STAGE;
                 mbar_arrive_expect_tx(&bar_full[s], L::TX);
+                if (!KDA) {
 #pragma unroll
-                for (int a = 0; a < KA; ++a) {
-                    tma_load_3d(tmq, &bar_full[s], stg + L::Q_OFF + a * 8192, a * 64, c * C, bh);
-                    tma_load_3d(tmk, &bar_full[s], stg + L::K_OFF + a * 8192, a * 64, c * C, bh);
+                    for (int a = 0; a < KA; ++a) {
+                        tma_load_3d(tmq, &bar_full[s], stg + L::Q_OFF + a * 8192, a * 64, c * C, bh);
+                        tma_load_3d(tmk, &bar_full[s], stg + L::K_OFF + a * 8192, a * 64, c * C, bh);
+                    }
                 }
                 const uint8_t* src = p.ws_slot + (static_cast<size_t>(p.chain_buf * p.G + g) * p.W + i) * S::BYTES;
                 bulk_load(stg + L::SLOT_OFF, src, S::BYTES, &bar_full[s]);
@@ -284,7 +350,8 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                 if (it >= 1) wait(bar_ep, (it - 1) & 1, kStatusMmaWait);
                 if (fail) break;
                 tc_fence_after();
-                // dX = U^T K' (commit), O2 = U^T P^T (commit)
+                // dX = U^T K' (commit), O2 = U^T P^T (commit); K' is the raw k
+                // tile (gdn, its token factors sit on U^T) or K o Gam_C / Gam (KDA)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16_ss(tmem + L::COL_S, kmaj(aUS2 + kk * 32), mnmaj(stg + L::K_OFF + kk * 2048, 8192), ID_S,
@@ -397,9 +464,11 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                         y[7] = a3.y - y[7];
                     }
                     store_row32_bf16(aUS, r, 4 * hh, x);
+                    if (!KDA) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] *= vec[64 + 32 * hh + i];
-                    store_row32_bf16(aUS2, r, 4 * hh, x);
+                        for (int i = 0; i < 32; ++i) x[i] *= vec[64 + 32 * hh + i];
+                        store_row32_bf16(aUS2, r, 4 * hh, x);
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -410,7 +479,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                 break;
             }
             if (lane == 0) mbar_arrive(bar_us);
-            // ---- X = gam_C X_0 + dX, republished as the bf16 operand -------------
+            // ---- X = gam_C X_0 + dX (KDA: X_0 Diag(Gam_C) + dX), republished -----
             ok = mbar_wait_or_abort(bar_c, ph_c, abort_flag);
             ph_c ^= 1u;
             tc_fence_after();
@@ -422,13 +491,14 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                     tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) st[32 * b + i] = gC * st[32 * b + i] + x[i];
+                    for (int i = 0; i < 32; ++i)
+                        st[32 * b + i] = (KDA ? sv[hh * DKH + 32 * b + i] : gC) * st[32 * b + i] + x[i];
                 }
                 publish_state();
             }
             signal(bar_x);
             bad |= !ok;
-            // ---- output: o_t = gam_t O1[t] + O2[t] -------------------------------
+            // ---- output: o_t = gam_t O1[t] + O2[t] (KDA: Gam_t is inside O1) -----
             ok = mbar_wait_or_abort(bar_o, ph_o, abort_flag);
             ph_o ^= 1u;
             tc_fence_after();
@@ -446,7 +516,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                     tmem_ld16(tlane + L::COL_O + 128 * s + 64 + tb, o2);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) o1[i] = sv[tb + i] * o1[i] + o2[i];
+                    for (int i = 0; i < 16; ++i) o1[i] = (KDA ? o1[i] : sv[tb + i] * o1[i]) + o2[i];
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
                         const float send = odd ? o1[2 * m] : o1[2 * m + 1];
@@ -513,11 +583,70 @@ __device__ __forceinline__ void tile_store(float* M, int ld, int r0, int n0, con
     *reinterpret_cast<float2*>(M + (r0 + gq + 8) * ld + n0 + 2 * cq) = make_float2(s * d[2], s * d[3]);
 }
 
+// T = (I + A)^{-1} in place, A strictly lower triangular in As (fp32
+// [64][kAStride]); Rs is scratch. Run by the eight converting warps; every
+// step ends at their named barrier.
+__device__ __forceinline__ void invert_unit_lower(float* As, float* Rs, int warp, int lane) {
+    // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution ------
+    if (warp < 4 && lane < 16) {
+        const int w0 = 16 * warp, l = lane;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float* arow = As + (w0 + i) * kAStride + w0;
+            float a0 = (i == l) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+            for (int kq = 0; kq + 1 < i; kq += 2) {
+                a0 -= arow[kq] * x[kq];
+                a1 -= arow[kq + 1] * x[kq + 1];
+            }
+            if (i & 1) a0 -= arow[i - 1] * x[i - 1];
+            x[i] = a0 + a1;
+        }
+        __syncwarp(0x0000ffffu);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) As[(w0 + i) * kAStride + w0 + l] = x[i];
+    }
+    sync_conv();
+    // ---- merge level 1 (warps 0-3, one 16x8 tile each):
+    //      T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22)
+    {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        const int m = warp >> 1, nt = warp & 1;
+        const int rb = 16 + 32 * m, cb = 32 * m;
+        float* X = Rs + warp * 16 * 8;   // 16x8, stride 8
+        if (warp < 4) {
+            tile_mma<2>(d, As, kAStride, rb, cb, As, kAStride, cb, cb + 8 * nt);
+            tile_store(X, 8, 0, 0, d, 1.f);
+        }
+        sync_conv();   // every read of A_10 / A_32 precedes the overwrite below
+        if (warp < 4) {
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma<2>(e, As, kAStride, rb, rb, X, 8, 0, 0);
+            tile_store(As, kAStride, rb, cb + 8 * nt, e, -1.f);
+        }
+        sync_conv();
+    }
+    // ---- merge level 2 (8 warps, one 16x8 tile each):
+    //      T[32:64, 0:32] = -T_B (A[32:64, 0:32] T_A)
+    {
+        const int mt = warp >> 2, nt = warp & 3;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma<4>(d, As, kAStride, 32 + 16 * mt, 0, As, kAStride, 0, 8 * nt);
+        tile_store(Rs, kRStride, 16 * mt, 8 * nt, d, 1.f);
+        sync_conv();
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma<4>(e, As, kAStride, 32 + 16 * mt, 32, Rs, kRStride, 0, 8 * nt);
+        tile_store(As, kAStride, 32 + 16 * mt, 8 * nt, e, -1.f);
+        sync_conv();
+    }
+}
+
 template <int DK, int DV>
 __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                           const Params& p, uint8_t* sm, uint32_t sbase) {
     using L = PrepLayout<DK, DV>;
-    using S = Slot<DK, DV>;
+    using S = Slot<DK, DV, false>;
     constexpr int KA = L::KA, VA = L::VA;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = 32 * (warp & 3) + lane;
@@ -706,59 +835,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
             store_row32_bf16(aOut + S::P_OFF, t, 4 * hh, x);
         }
         sync_conv();
-        // ---- T = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution ------
-        if (warp < 4 && lane < 16) {
-            const int w0 = 16 * warp, l = lane;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float* arow = As + (w0 + i) * kAStride + w0;
-                float a0 = (i == l) ? 1.f : 0.f, a1 = 0.f;
-#pragma unroll
-                for (int kq = 0; kq + 1 < i; kq += 2) {
-                    a0 -= arow[kq] * x[kq];
-                    a1 -= arow[kq + 1] * x[kq + 1];
-                }
-                if (i & 1) a0 -= arow[i - 1] * x[i - 1];
-                x[i] = a0 + a1;
-            }
-            __syncwarp(0x0000ffffu);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) As[(w0 + i) * kAStride + w0 + l] = x[i];
-        }
-        sync_conv();
-        // ---- merge level 1 (warps 0-3, one 16x8 tile each):
-        //      T_10 = -T_11 (A_10 T_00), T_32 = -T_33 (A_32 T_22)
-        {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            const int m = warp >> 1, nt = warp & 1;
-            const int rb = 16 + 32 * m, cb = 32 * m;
-            float* X = Rs + warp * 16 * 8;   // 16x8, stride 8
-            if (warp < 4) {
-                tile_mma<2>(d, As, kAStride, rb, cb, As, kAStride, cb, cb + 8 * nt);
-                tile_store(X, 8, 0, 0, d, 1.f);
-            }
-            sync_conv();   // every read of A_10 / A_32 precedes the overwrite below
-            if (warp < 4) {
-                float e[4] = {0.f, 0.f, 0.f, 0.f};
-                tile_mma<2>(e, As, kAStride, rb, rb, X, 8, 0, 0);
-                tile_store(As, kAStride, rb, cb + 8 * nt, e, -1.f);
-            }
-            sync_conv();
-        }
-        // ---- merge level 2 (8 warps, one 16x8 tile each):
-        //      T[32:64, 0:32] = -T_B (A[32:64, 0:32] T_A)
-        {
-            const int mt = warp >> 2, nt = warp & 3;
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma<4>(d, As, kAStride, 32 + 16 * mt, 0, As, kAStride, 0, 8 * nt);
-            tile_store(Rs, kRStride, 16 * mt, 8 * nt, d, 1.f);
-            sync_conv();
-            float e[4] = {0.f, 0.f, 0.f, 0.f};
-            tile_mma<4>(e, As, kAStride, 32 + 16 * mt, 32, Rs, kRStride, 0, 8 * nt);
-            tile_store(As, kAStride, 32 + 16 * mt, 8 * nt, e, -1.f);
-            sync_conv();
-        }
+        invert_unit_lower(As, Rs, warp, lane);
         // ---- T diag(beta) and T diag(beta gam) as bf16 MMA operands --------------
         {
             const int t = tid >> 2, q4 = tid & 3;
@@ -829,7 +906,402 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     if (status_bits && tid == 0) atomicOr(p.status, status_bits);
 }
 
+// ============================================================================
+// prep CTA of the per-channel decay (8 warps)
+// ============================================================================
+__device__ __forceinline__ uint32_t ld_shared_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Exponent kept inside the fp32 range, so that a factor stays finite even
+// for decays below the form's stated limit.
+__device__ __forceinline__ float ex2c(float x) { return ex2(fminf(fmaxf(x, -126.f), 126.f)); }
+
 template <int DK, int DV>
+__device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                              const Params& p, uint8_t* sm, uint32_t sbase) {
+    using L = PrepLayoutKda<DK, DV>;
+    using S = Slot<DK, DV, true>;
+    constexpr int KA = L::KA, VA = L::VA;
+    constexpr int NCP = DK / 2;          // channel pairs
+    constexpr int NSEG = kConv / NCP;    // token segments of the element pass
+    constexpr int SL = C / NSEG;         // 16 tokens (d_k 128) or 8 (d_k 64)
+    static_assert(SL == 8 || SL == 16, "a segment is one or two 8-token blocks of one sub-chunk");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = 32 * (warp & 3) + lane;
+    const int hh = warp >> 2;
+    const int pid = blockIdx.x - p.n_chain;
+    const int np = gridDim.x - p.n_chain;
+    const int nunits = p.G * p.prep_n;
+    const int T = p.T;
+    // element pass: thread (cp, seg) owns channels c0, c0 + 1 of tokens
+    // [seg*SL, seg*SL + SL), all inside sub-chunk sa
+    const int cp = tid % NCP, seg = tid / NCP;
+    const int c0 = 2 * cp;
+    const int ka = c0 / 64;
+    const uint32_t ch = (c0 % 64) / 8, bo = (c0 % 8) * 2;
+    const int sa = seg * SL / 16;
+    const int blk0 = seg * SL / 8;       // first 8-token block of the segment
+
+    float* As = reinterpret_cast<float*>(sm + L::OFF_AS);
+    float* Rs = reinterpret_cast<float*>(sm + L::OFF_RS);
+    float* sBlk = reinterpret_cast<float*>(sm + L::OFF_BLK);   // log2-gate sum of each 8-token block [8][DK]
+    float* sPr = reinterpret_cast<float*>(sm + L::OFF_PR);     // 2^r_a [4][DK]
+    float* sB = reinterpret_cast<float*>(sm + L::OFF_MISC);    // beta (0 on padded tokens)
+    const float* sGate = reinterpret_cast<const float*>(sm + L::OFF_GATE);
+    uint8_t* outp = sm + L::OFF_OUT;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+    uint64_t* bar_qk = bar;       // [2] k and q of a unit
+    uint64_t* bar_v = bar + 2;    // v of a unit
+    uint64_t* bar_g = bar + 3;    // gate tile of a unit
+    uint64_t* bar_m = bar + 4;    // MMAs
+    uint64_t* bar_test = bar + 5;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 6);
+    const uint32_t aTB1 = sbase + L::OFF_TB1, aOut = sbase + L::OFF_OUT, aV = sbase + L::OFF_V;
+
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(tmq);
+        tma_prefetch_desc(tmk);
+        tma_prefetch_desc(tmv);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tc_fence_before();
+    sync_conv();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    // Programmatic dependent launch as in the scalar-gate prep role: a later
+    // window launch computes its first unit before it waits.
+    bool waited = false;
+    if (!p.early) {
+        griddep_wait();
+        griddep_launch_dependents();
+        waited = true;
+    }
+
+    auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
+        const bool ok = mbar_wait(b, parity, kWaitLimitNs);
+        tc_fence_after();
+        return !named_sync_or(kBarConv, kConv, !ok);
+    };
+    auto publish = [&]() {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        sync_conv();
+        tc_fence_after();
+    };
+
+    int status_bits = 0;
+    bool failed = false;
+    if (p.flags & 0x100u) {
+        const bool ok = mbar_wait(bar_test, 0, 1000000ull);
+        if (named_sync_or(kBarConv, kConv, !ok)) { status_bits |= kStatusTestHook; failed = true; }
+    }
+
+    auto unit_g = [&](int u) { return u % p.G; };
+    auto unit_i = [&](int u) { return u / p.G; };
+    // Copies in flight (thread 0): the k/q stages, and the single V and gate
+    // buffers (one load at a time each, the n-th completing phase n).
+    bool pend_qk[2] = {false, false};
+    int v_issued = 0, v_done = 0, g_issued = 0, g_done = 0;
+    auto issue_qk = [&](int u, int s) {
+        const int bh = p.h0 + unit_g(u);
+        const int y = (p.prep_c0 + unit_i(u)) * C;
+        uint8_t* stg = sm + s * L::QK_BYTES;
+        mbar_arrive_expect_tx(&bar_qk[s], L::QK_BYTES);
+#pragma unroll
+        for (int a = 0; a < KA; ++a) {
+            tma_load_3d(tmk, &bar_qk[s], stg + a * 16384, a * 64, y, bh);
+            tma_load_3d(tmq, &bar_qk[s], stg + a * 16384 + 8192, a * 64, y, bh);
+        }
+        pend_qk[s] = true;
+    };
+    auto issue_v = [&](int u) {
+        const int bh = p.h0 + unit_g(u);
+        const int y = (p.prep_c0 + unit_i(u)) * C;
+        mbar_arrive_expect_tx(bar_v, VA * 8192);
+#pragma unroll
+        for (int a = 0; a < VA; ++a) tma_load_3d(tmv, bar_v, sm + L::OFF_V + a * 8192, a * 64, y, bh);
+        ++v_issued;
+    };
+    // the gate rows of a chunk are contiguous: one bulk copy of the valid rows
+    auto issue_g = [&](int u) {
+        const int bh = p.h0 + unit_g(u);
+        const int y = (p.prep_c0 + unit_i(u)) * C;
+        const int rows = T - y < C ? T - y : C;
+        const uint32_t bytes = static_cast<uint32_t>(rows) * DK * 4;
+        mbar_arrive_expect_tx(bar_g, bytes);
+        bulk_load(sm + L::OFF_GATE, p.gate + (static_cast<size_t>(bh) * T + y) * DK, bytes, bar_g);
+        ++g_issued;
+    };
+    auto load_b = [&](int u, float& bv) {
+        bv = 0.f;
+        if (u < nunits && tid < 64) {
+            const int bh = p.h0 + unit_g(u);
+            const int t = (p.prep_c0 + unit_i(u)) * C + tid;
+            if (t < T) bv = p.beta[static_cast<size_t>(bh) * T + t];
+        }
+    };
+
+    constexpr uint32_t ID_WU = idesc_bf16(128, 64, true, false);   // K^T TB1^T per sub-chunk, V^T TB1^T
+
+    float b_nx;
+    load_b(pid, b_nx);
+    if (!failed && tid == 0 && pid < nunits) {
+        issue_qk(pid, 0);
+        issue_v(pid);
+        issue_g(pid);
+    }
+    uint32_t mph = 0;
+    int k = 0;
+    for (; !failed; ++k) {
+        const int u = pid + k * np;
+        if (u >= nunits) break;
+        const int s = k & 1;
+        const int un = u + np;
+        const uint32_t stg = sbase + s * L::QK_BYTES;
+        const int nvalid = T - (p.prep_c0 + unit_i(u)) * C;   // tokens of the unit inside the sequence
+        if (tid == 0 && un < nunits) {
+            fence_proxy_async_smem();
+            issue_qk(un, s ^ 1);   // stage s^1's MMAs finished with the previous unit
+        }
+        // ---- log2 gates: prefix sums inside each segment, 8-token block sums -----
+        if (!wait_all(bar_g, k & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
+        if (tid == 0) ++g_done;
+        float lp0[SL], lp1[SL];
+        {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < SL; ++i) {
+                const int t = seg * SL + i;
+                float2 g = make_float2(1.f, 1.f);
+                if (t < nvalid) g = *reinterpret_cast<const float2*>(sGate + t * DK + c0);
+                a0 += lg2(g.x);
+                a1 += lg2(g.y);
+                lp0[i] = a0;
+                lp1[i] = a1;
+            }
+            *reinterpret_cast<float2*>(sBlk + blk0 * DK + c0) = make_float2(lp0[7], lp1[7]);
+            if (SL == 16)
+                *reinterpret_cast<float2*>(sBlk + (blk0 + 1) * DK + c0) =
+                    make_float2(lp0[SL - 1] - lp0[7], lp1[SL - 1] - lp1[7]);
+        }
+        if (tid < 64) sB[tid] = b_nx;
+        load_b(un, b_nx);
+        // the slot buffer is written below: the store of the previous unit has read it
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        sync_conv();
+        // ---- cumulative log2 at the block ends: segment offset, the sub-chunk
+        //      references r_a (end of block 2a), G_C ---------------------------------
+        float off0 = 0.f, off1 = 0.f, rr0[4], rr1[4], GC0, GC1;
+        {
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const float2 x = *reinterpret_cast<const float2*>(sBlk + b * DK + c0);
+                s0 += x.x;
+                s1 += x.y;
+                if (b + 1 == blk0) { off0 = s0; off1 = s1; }
+                if ((b & 1) == 0) { rr0[b / 2] = s0; rr1[b / 2] = s1; }
+            }
+            GC0 = s0;
+            GC1 = s1;
+        }
+        float ra0 = rr0[0], ra1 = rr1[0];
+#pragma unroll
+        for (int a = 1; a < 4; ++a)
+            if (a == sa) { ra0 = rr0[a]; ra1 = rr1[a]; }
+        if (seg == 0) {
+            *reinterpret_cast<float2*>(outp + S::V_OFF + c0 * 4) = make_float2(ex2(GC0), ex2(GC1));
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                *reinterpret_cast<float2*>(sPr + a * DK + c0) = make_float2(ex2(rr0[a]), ex2(rr1[a]));
+        }
+        if (!wait_all(&bar_qk[s], (k >> 1) & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
+        if (tid == 0) pend_qk[s] = false;
+        // ---- element pass over the thread's tokens and channel pair:
+        //      [K;Q] o 2^(G - r_a) in place (row operand), K o 2^(r_a - G) (own
+        //      column operand), K o 2^(r_b - G) (columns of later sub-chunks b),
+        //      Q o Gam and K o Gam_C/Gam into the slot ------------------------------
+        {
+            const uint32_t aKQ = stg + ka * 16384;
+#pragma unroll
+            for (int i = 0; i < SL; ++i) {
+                const int t = seg * SL + i;
+                const uint32_t ro = sw128_off(t, ch) + bo;   // in [64][DK] tiles of 8 KB atoms
+                const uint32_t ak = aKQ + ro;
+                const uint32_t aq = aKQ + sw128_off(64 + t, ch) + bo;
+                const float2 kv = unpack_bf16(ld_shared_b32(ak));
+                const float2 qv = unpack_bf16(ld_shared_b32(aq));
+                const float G0 = off0 + lp0[i], G1 = off1 + lp1[i];
+                const float e10 = ex2c(G0 - ra0), e11 = ex2c(G1 - ra1);
+                const float e20 = ex2c(ra0 - G0), e21 = ex2c(ra1 - G1);
+                st_shared_b32(ak, pack_bf16(kv.x * e10, kv.y * e11));
+                st_shared_b32(aq, pack_bf16(qv.x * e10, qv.y * e11));
+                st_shared_b32(aOut + S::QG_OFF + ka * 8192 + ro, pack_bf16(qv.x * ex2(G0), qv.y * ex2(G1)));
+                st_shared_b32(aOut + S::KP_OFF + ka * 8192 + ro,
+                              pack_bf16(kv.x * ex2(GC0 - G0), kv.y * ex2(GC1 - G1)));
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const uint32_t ab = sbase + L::b_off(b) + ka * 2048 * (b + 1) + ro;
+                    if (b == sa) st_shared_b32(ab, pack_bf16(kv.x * e20, kv.y * e21));
+                    if (b > sa) st_shared_b32(ab, pack_bf16(kv.x * ex2(rr0[b] - G0), kv.y * ex2(rr1[b] - G1)));
+                }
+            }
+        }
+        publish();
+        // ---- [K;Q] B_a^T on the tensor cores, one product per sub-chunk a ------------
+        if (tid == 0) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const uint32_t idg = idesc_bf16(128, 16 * (a + 1), false, false);
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk)
+                    mma_bf16_ss(tmem + L::COL_G + 64 * a, kmaj(stg + (kk / 4) * 16384 + (kk % 4) * 32),
+                                kmaj(sbase + L::b_off(a) + (kk / 4) * 2048 * (a + 1) + (kk % 4) * 32), idg, kk > 0);
+            }
+            mma_commit(bar_m);
+        }
+        if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        mph ^= 1u;
+        if (tid == 0 && un < nunits) {
+            fence_proxy_async_smem();
+            issue_g(un);   // the column operands over the gate tile are read
+        }
+        // ---- A (rows 0-63) and P (rows 64-127). A warp's lanes 0-15 and 16-31
+        //      lie in consecutive sub-chunks a0, a0 + 1: it reads both products and
+        //      each lane keeps its own. --------------------------------------------
+        {
+            const int a0 = 2 * (warp & 1);
+            float x[32];
+            {
+                float y[32];
+                tmem_ld32(tlane + L::COL_G + 64 * a0 + 32 * hh, x);
+                tmem_ld32(tlane + L::COL_G + 64 * (a0 + 1) + 32 * hh, y);
+                tmem_ld_wait();
+                const bool hi = lane >= 16;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = hi ? y[i] : x[i];
+            }
+            if ((warp & 3) < 2) {
+                // A_tj = beta_t (k_t o Gam_t).(k_j / Gam_j) for j < t
+                const int t = r;
+                const float bt = sB[t];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int j = 32 * hh + 4 * m;
+                    float4 o;
+                    o.x = (j + 0 < t) ? bt * x[4 * m + 0] : 0.f;
+                    o.y = (j + 1 < t) ? bt * x[4 * m + 1] : 0.f;
+                    o.z = (j + 2 < t) ? bt * x[4 * m + 2] : 0.f;
+                    o.w = (j + 3 < t) ? bt * x[4 * m + 3] : 0.f;
+                    *reinterpret_cast<float4*>(As + t * kAStride + j) = o;
+                }
+            } else {
+                // P_tj = (q_t o Gam_t).(k_j / Gam_j) for j <= t
+                const int t = r - 64;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = 32 * hh + i;
+                    x[i] = (j <= t) ? x[i] : 0.f;
+                }
+                store_row32_bf16(aOut + S::P_OFF, t, 4 * hh, x);
+            }
+        }
+        sync_conv();
+        invert_unit_lower(As, Rs, warp, lane);
+        // ---- T diag(beta) as a bf16 MMA operand -----------------------------------
+        {
+            const int t = tid >> 2, q4 = tid & 3;
+            const float* trow = As + t * kAStride + 16 * q4;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const float4 t0 = *reinterpret_cast<const float4*>(trow + 8 * cc);
+                const float4 t1 = *reinterpret_cast<const float4*>(trow + 8 * cc + 4);
+                const float4 b0 = *reinterpret_cast<const float4*>(sB + 16 * q4 + 8 * cc);
+                const float4 b1 = *reinterpret_cast<const float4*>(sB + 16 * q4 + 8 * cc + 4);
+                st_shared_v4(aTB1 + sw128_off(t, 2 * q4 + cc), pack_bf16(t0.x * b0.x, t0.y * b0.y),
+                             pack_bf16(t0.z * b0.z, t0.w * b0.w), pack_bf16(t1.x * b1.x, t1.y * b1.y),
+                             pack_bf16(t1.z * b1.z, t1.w * b1.w));
+            }
+        }
+        if (!wait_all(bar_v, k & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
+        if (tid == 0) ++v_done;
+        publish();
+        // ---- W^T = sum_a Diag(2^r_a) Kr_a^T (T diag(beta))_a^T, one product per
+        //      sub-chunk a (Kr = the row operand's k rows); Ut^T = V^T (T diag(beta))^T
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + L::COL_W + 64 * kk, mnmaj(stg + kk * 2048, 16384), kmaj(aTB1 + kk * 32), ID_WU,
+                            false);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + L::COL_UT, mnmaj(aV + kk * 2048, 8192), kmaj(aTB1 + kk * 32), ID_WU, kk > 0);
+            mma_commit(bar_m);
+        }
+        if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        mph ^= 1u;
+        if (tid == 0 && un < nunits) {
+            fence_proxy_async_smem();
+            issue_v(un);
+        }
+        if (r < DK) {
+            float w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = 0.f;
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                float x[32];
+                tmem_ld32(tlane + L::COL_W + 64 * a + 32 * hh, x);
+                tmem_ld_wait();
+                const float f = sPr[a * DK + r];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] += f * x[i];
+            }
+            store_row32_bf16(aOut + S::W_OFF, r, 4 * hh, w);
+        }
+        if (r < DV) {
+            float x[32];
+            tmem_ld32(tlane + L::COL_UT + 32 * hh, x);
+            tmem_ld_wait();
+            store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, x);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        sync_conv();
+        if (!waited) {
+            griddep_wait();
+            griddep_launch_dependents();
+            waited = true;
+        }
+        if (tid == 0) {
+            uint8_t* dst = p.ws_slot + (static_cast<size_t>(p.prep_buf * p.G + unit_g(u)) * p.W + unit_i(u)) * S::BYTES;
+            bulk_store(dst, aOut, S::BYTES);
+            bulk_commit();
+        }
+    }
+
+    if (failed && tid == 0) {
+        for (int s2 = 0; s2 < 2; ++s2)
+            if (pend_qk[s2]) mbar_wait(&bar_qk[s2], ((s2 == (k & 1) ? k : k + 1) >> 1) & 1, 100000000ull);
+        if (v_issued > v_done) mbar_wait(bar_v, (v_issued - 1) & 1, 100000000ull);
+        if (g_issued > g_done) mbar_wait(bar_g, (g_issued - 1) & 1, 100000000ull);
+    }
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    sync_conv();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+    if (status_bits && tid == 0) atomicOr(p.status, status_bits);
+}
+
+template <int DK, int DV, bool KDA>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
            const __grid_constant__ CUtensorMap tmv, const Params p) {
@@ -838,18 +1310,21 @@ gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (sbase - raw);
     if (static_cast<int>(blockIdx.x) < p.n_chain) {
-        chain_role<DK, DV>(&tmq, &tmk, p, sm, sbase);
+        chain_role<DK, DV, KDA>(&tmq, &tmk, p, sm, sbase);
     } else {
         if (threadIdx.x >= kConv) return;   // the prep role runs on eight warps
-        prep_role<DK, DV>(&tmq, &tmk, &tmv, p, sm, sbase);
+        if constexpr (KDA)
+            prep_role_kda<DK, DV>(&tmq, &tmk, &tmv, p, sm, sbase);
+        else
+            prep_role<DK, DV>(&tmq, &tmk, &tmv, p, sm, sbase);
     }
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool KDA>
 cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int W, cudaStream_t s) {
-    constexpr uint32_t smem = smem_alloc<DK, DV>();
+    constexpr uint32_t smem = smem_alloc<DK, DV, KDA>();
     static_assert(smem <= 232448, "shared memory budget");
-    auto kern = gdn_kernel<DK, DV>;
+    auto kern = gdn_kernel<DK, DV, KDA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nch = (a.T + C - 1) / C;
@@ -915,29 +1390,40 @@ cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int W, cudaStream
 
 namespace chunk {
 
-size_t gdn_slot_bytes(int dk, int dv) { return static_cast<size_t>(dk + dv) * 128 + 8192 + 512; }
+size_t gdn_slot_bytes(int dk, int dv, bool kda) {
+    return static_cast<size_t>(dk + dv) * 128 + 8192 + (kda ? static_cast<size_t>(dk) * 256 : 0) + 512;
+}
 
 int gdn_group(int BH) { return BH < kGdnMaxGroup ? BH : kGdnMaxGroup; }
 
-size_t gdn_workspace_bytes(int BH, int dk, int dv, int W) {
+size_t gdn_workspace_bytes(int BH, int dk, int dv, int W, bool kda) {
     const int G = gdn_group(BH);
-    return static_cast<size_t>(G) * dk * dv * sizeof(float) + 2 * static_cast<size_t>(G) * W * gdn_slot_bytes(dk, dv);
+    return static_cast<size_t>(G) * dk * dv * sizeof(float) +
+           2 * static_cast<size_t>(G) * W * gdn_slot_bytes(dk, dv, kda);
 }
 
 cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     const int G = gdn_group(a.BH);
     const size_t state_bytes = static_cast<size_t>(G) * a.dk * a.dv * sizeof(float);
-    const size_t per_w = 2 * static_cast<size_t>(G) * gdn_slot_bytes(a.dk, a.dv);
+    const bool kda = a.variant == kKda;
+    const size_t per_w = 2 * static_cast<size_t>(G) * gdn_slot_bytes(a.dk, a.dv, kda);
     if (!a.workspace || a.ws_bytes < state_bytes + per_w) return cudaErrorInvalidValue;
     const int nch = (a.T + C - 1) / C;
     size_t W = (a.ws_bytes - state_bytes) / per_w;
     if (W > static_cast<size_t>(kGdnWindow)) W = kGdnWindow;
     if (W > static_cast<size_t>(nch)) W = nch;
     const int w = static_cast<int>(W);
-    if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64>(m, a, G, w, s);
-    if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128>(m, a, G, w, s);
-    if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64>(m, a, G, w, s);
-    if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128>(m, a, G, w, s);
+    if (kda) {
+        if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, true>(m, a, G, w, s);
+        if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, true>(m, a, G, w, s);
+        if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, true>(m, a, G, w, s);
+        if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, true>(m, a, G, w, s);
+        return cudaErrorInvalidValue;
+    }
+    if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, false>(m, a, G, w, s);
+    if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, false>(m, a, G, w, s);
+    if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, false>(m, a, G, w, s);
+    if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, false>(m, a, G, w, s);
     return cudaErrorInvalidValue;
 }
 

@@ -29,7 +29,9 @@
  *                   S_t = S_{t-1} Diag(alpha_t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
  *                 alpha_t in (0,1]^{d_k}. ("Linear attention and recurrent
  *                 memory", From fixed decay to KDA's gated delta write.)
- *                 Runs on the recurrent kernel (chunk 0 or 1) and the decode step.
+ *                 The chunkwise kernel is exact in fp32 while every alpha >= 2^-15
+ *                 (smaller values stay finite but lose accuracy); the recurrent
+ *                 kernel (chunk 1) has no such limit.
  *
  * Every variant updates first and then reads, so token t attends to itself.
  *
@@ -65,10 +67,11 @@
  * states do not fit takes the sequential kernel instead), for segment
  * summaries when B*H is too small to fill the GPU ((SM count) x
  * (d_k*d_v + d_k) floats) and, for
- * LA_GDN, for the fp32 states of a group of G = min(B*H, 32) sequence-heads
- * plus two windows of 16 chunks of per-chunk intermediates
- * (G*d_k*d_v*4 + 2*G*16*((d_k+d_v)*128 + 8704) bytes; 44.5 MB at
- * G = 32, d_k = d_v = 128). The largest of these is allocated when the
+ * LA_GDN and LA_KDA, for the fp32 states of a group of G = min(B*H, 32)
+ * sequence-heads plus two windows of 16 chunks of per-chunk intermediates
+ * (G*d_k*d_v*4 + 2*G*16*((d_k+d_v)*128 + 8704 [+ 256*d_k for LA_KDA])
+ * bytes; 78 MB at G = 32, d_k = d_v = 128, sized for LA_KDA; a smaller
+ * workspace only shortens the windows). The largest of these is allocated when the
  * configuration can take the tensor-core path (bf16, d_k, d_v in {64, 128}).
  * Calls that overlap on the GPU through the same handle (different streams)
  * would share that workspace: serialize them.
@@ -147,7 +150,7 @@ int la_create(const la_config* cfg, la_handle** out);
  *             fp32 io and head sizes 16/32 always use the recurrent kernel.
  *             Other values: LA_ERR_UNSUPPORTED.
  *   den_out   optional, LA_NORM_ELU1 and LA_NORM_DECAY only.
- * The chunkwise kernel needs q, k, v (and the LA_GLA gate) 16-byte aligned.
+ * Every pointer must be 16-byte aligned (LA_ERR_MISALIGNED otherwise).
  * LA_NORM_DECAY runs chunkwise only in the three-phase form; a call whose
  * per-chunk states do not fit the workspace runs the recurrent kernel.
  */
@@ -237,7 +240,8 @@ const char* la_last_error(const la_handle* h);
  * diagnostic: which algorithm the library picked shows in this count (1: the
  * recurrent kernel or a decode step; 1 or 2: the chunk kernel, with segment
  * summaries when B*H is small; 3: the three-phase parallel form; for LA_GDN
- * one per window of chunks plus one, for each group of 32 sequence-heads). */
+ * and LA_KDA one per window of chunks plus one, for each group of 32
+ * sequence-heads). */
 int la_last_launches(const la_handle* h);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */

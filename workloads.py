@@ -133,6 +133,10 @@ GDN_B2H16_T8192_D128 = Workload(
     "gdn_b2h16_t8192_d128_bf16", "gdn", 2, 16, 8192, 128, 128, "bf16",
     unit_keys=True, gate_mu=4.0, beta_mu=0.0,
     note="gated delta rule, bf16 q,v N(0,1), unit k, beta=sigmoid(N(0,1)), g=sigmoid(N(4,1))")
+KDA_B2H16_T8192_D128 = Workload(
+    "kda_b2h16_t8192_d128_bf16", "kda", 2, 16, 8192, 128, 128, "bf16",
+    unit_keys=True, gate_mu=4.0, beta_mu=0.0,
+    note="delta rule with a per-channel decay, prefill: the gated delta shapes, alpha=sigmoid(N(4,1)) per channel")
 GDN_DECODE_N256H16_D128 = Workload(
     "gdn_decode_n256h16_d128_s1024", "gdn", 256, 16, 1, 128, 128, "bf16",
     unit_keys=True, gate_mu=4.0, beta_mu=0.0, state_std=0.02, decode_steps=1024,
@@ -141,8 +145,9 @@ GDN_DECODE_N256H16_D128 = Workload(
 ALL = (NORM_T64_D16, NORM_B4H8_T2048_D64, GLA_B4H16_T4096_D128,
        GDN_B2H16_T8192_D128, GDN_DECODE_N256H16_D128)
 # Beyond the five: the normalized variant with a fixed decay per head, on
-# the shapes of the normalized headline workload.
-EXTRA = (NORM_DECAY_B4H8_T2048_D64, KDA_DECODE_N256H16_D128)
+# the shapes of the normalized headline workload; the delta rule with a
+# per-channel decay, prefill on the gated delta shapes and decode.
+EXTRA = (NORM_DECAY_B4H8_T2048_D64, KDA_B2H16_T8192_D128, KDA_DECODE_N256H16_D128)
 BY_NAME = {w.name: w for w in ALL + EXTRA}
 
 
