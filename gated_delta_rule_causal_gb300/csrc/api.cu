@@ -526,7 +526,7 @@ int la_status(la_handle* h, void* cuda_stream) {
         e = cudaMemset(h->d_status, 0, sizeof(int));
         if (e != cudaSuccess) return cuda_fail(h, e, "status clear");
         char buf[160];
-        std::snprintf(buf, sizeof(buf), "a bounded device wait expired (status bits 0x%x: 1=TMA, 2=MMA, 4=test hook)", word);
+        std::snprintf(buf, sizeof(buf), "a bounded device wait expired (status bits 0x%x: 1=TMA, 2=MMA, 4=test hook, 8=hand-off flag)", word);
         return fail(h, LA_ERR_TIMEOUT, buf);
     }
     return LA_OK;

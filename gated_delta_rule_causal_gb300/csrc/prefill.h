@@ -19,15 +19,16 @@ struct Params;
 cudaError_t launch_norm(int dk, int dv, const Maps& m, const Params& p, int BH, cudaStream_t s);
 cudaError_t launch_gla(int dk, int dv, const Maps& m, const Params& p, int BH, cudaStream_t s);
 
-// Gated delta rule, scalar or per-channel (kda) decay: prep and chain CTAs
-// over windows of chunks, one group of at most kGdnMaxGroup sequence-heads at
-// a time; the workspace holds the group's states and two windows of
-// per-chunk slots.
+// Gated delta rule, scalar or per-channel (kda) decay: one cooperative
+// launch per group of at most kGdnMaxGroup sequence-heads, in which prep CTAs
+// feed a ring of per-chunk slots to one chain CTA per head; the workspace
+// holds the hand-off flags and the ring (2 kGdnWindow chunks per head at
+// most, as deep as the workspace allows).
 constexpr int kGdnMaxGroup = 32;   // chain CTAs per launch
-constexpr int kGdnWindow = 16;     // chunks per window, at most
+constexpr int kGdnWindow = 16;     // half the deepest ring, in chunks
 size_t gdn_slot_bytes(int dk, int dv, bool kda);
 int gdn_group(int BH);
-// Workspace for a window of W chunks (W >= 1 is the least the launcher accepts).
+// Workspace for a ring of 2W chunks (W >= 1 is the least the launcher accepts).
 size_t gdn_workspace_bytes(int BH, int dk, int dv, int W, bool kda);
 cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s);
 

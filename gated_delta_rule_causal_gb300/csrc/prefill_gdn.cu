@@ -14,24 +14,26 @@
 //    X   = gam_C X_0 + U^T diag(gam_C/gam) K
 // Everything but these three lines is independent of the state.
 //
-// Work split. Each launch runs two kinds of CTA:
-//  * prep CTAs, in parallel over (head, chunk) of a window of W chunks:
+// Work split. One cooperative launch per group of up to 32 sequence-heads
+// runs two kinds of CTA, all resident at once:
+//  * prep CTAs, in parallel over (head, chunk) units taken chunk by chunk:
 //    gate prefix sums, [K;Q] K^T on the tensor cores, A and P, the
 //    triangular inverse T in fp32 (16x16 diagonal blocks by forward
 //    substitution, then two merge levels as warp-level tf32 MMAs), W^T and
 //    Ut^T on the tensor cores. Each chunk's results ("slot": W^T, Ut^T, P as
-//    bf16 MMA operands and the gate factors) go to a workspace ring of two
-//    windows with one bulk copy.
-//  * chain CTAs, one per sequence-head of the group, walking the previous
-//    window: per chunk the MMAs X_0 W^T and X_0 Q^T, then U^T K' and U^T P^T,
-//    and three short conversions (U, the state, the output). One control
-//    warp issues every copy and MMA; eight warps convert. They hand work to
-//    each other through mbarriers, so that no converting thread ever waits
-//    on an issue queue.
-// Window j is prepared in launch j and walked in launch j+1, so the launch
-// boundary orders producer and consumer and no CTA waits on another one. The
-// chain CTAs carry the fp32 state from one launch to the next through the
-// workspace.
+//    bf16 MMA operands and the gate factors) go with one bulk copy to a ring
+//    of R chunks per head in the workspace.
+//  * chain CTAs, one per sequence-head, walking its whole sequence with the
+//    fp32 state in registers: per chunk the MMAs X_0 W^T and X_0 Q^T, then
+//    U^T K' and U^T P^T, and three short conversions (U, the state, the
+//    output). One control warp issues every copy and MMA; eight warps
+//    convert. They hand work to each other through mbarriers, so that no
+//    converting thread ever waits on an issue queue.
+// The two kinds hand the ring over through flags in global memory: a prep CTA
+// raises a chunk's ready flag once its slot store has completed, and stores
+// into a ring position only after the chain CTA has loaded the chunk R
+// before it (its consumed count). Every wait on a flag is bounded, and a CTA
+// that gives up raises the launch's abort word so the others stop waiting.
 //
 // The output is formed transposed (value rows on the 128 tensor-memory
 // lanes, tokens on 64 columns) so that no product pads 64 tokens to M = 128;
@@ -59,6 +61,8 @@
 // Gam_C / Gam_t, Gam_C) is at most 1. Exact in fp32 while every alpha >=
 // 2^-15. The prep CTAs write Q o Gam and K o Gam_C / Gam into the slot, so
 // the chain CTAs load no q or k tiles of their own.
+#include <atomic>
+
 #include "prefill.h"
 #include "prefill_impl.cuh"
 #include "launch.cuh"
@@ -75,10 +79,11 @@ using chunk::st_shared_v4;
 using chunk::store_row32_bf16;
 
 constexpr int kConv = 256;              // converting threads (8 warps)
-constexpr int kThreads = kConv + 32;    // + one control warp
+constexpr int kThreads = kConv + 64;    // + a control warp and a flag warp (chain CTAs)
 constexpr uint32_t kBarConv = 1;        // named barrier of the converting warps
 
 __host__ __device__ constexpr uint32_t align1024(uint32_t x) { return (x + 1023u) & ~1023u; }
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // One chunk's intermediates, byte-identical in the workspace and in shared
 // memory. Tiles are bf16 with the 128-byte swizzle (1024-aligned offsets).
@@ -198,19 +203,33 @@ struct Params {
     const float* state_in;  // [BH, DV, DK] or NULL (zeros)
     float* state_out;       // [BH, DV, DK] or NULL
     __nv_bfloat16* out;     // [BH, T, DV]
-    float* ws_state;        // [G, DV, DK]: the state between launches
-    uint8_t* ws_slot;       // [2][G][W] slots
+    uint8_t* ws_slot;       // [G][R] slots: ring of the chunks of each sequence-head
+    // Hand-off flags (each value = epoch | count): ready[G*R] (chunk c's
+    // slot stored: c + 1), then per head consumed[G] at a stride of 16 words
+    // (chunks whose slot the chain has loaded), then the abort word (= epoch
+    // once a CTA of this launch gave up).
+    unsigned long long* ws_flag;
+    unsigned long long epoch;   // this launch's epoch, in the upper 32 bits
     int T;
+    int nch;                // chunks per sequence
     int h0;                 // first sequence-head of the group
     int G;                  // sequence-heads in the group
-    int W;                  // chunks per window (slot ring stride)
-    int chain_c0, chain_n, chain_buf, chain_first, chain_last;
-    int prep_c0, prep_n, prep_buf;
+    int R;                  // ring depth in chunks
     int n_chain;            // CTAs [0, n_chain) walk the chain, the others prepare
-    int early;              // prep CTAs may read the inputs before the previous launch completes
     unsigned flags;
     int* status;
+    __device__ unsigned long long* ready(int g, int c) const { return ws_flag + static_cast<size_t>(g) * R + c % R; }
+    __device__ unsigned long long* consumed(int g) const { return ws_flag + static_cast<size_t>(G) * R + 16 * g; }
+    __device__ unsigned long long* abort_word() const { return ws_flag + static_cast<size_t>(G) * R + 16 * G; }
+    __device__ void abort_all() const {
+        *reinterpret_cast<volatile unsigned long long*>(abort_word()) = epoch;
+    }
+    __device__ bool wait_flag(const unsigned long long* f, unsigned long long count) const {
+        return flag_wait(f, epoch | count, abort_word(), epoch);
+    }
 };
+// Flag words the launcher reserves in front of the slots (ready, consumed, abort).
+constexpr size_t flag_words(int G, int R) { return static_cast<size_t>(G) * R + 16 * (G + 1); }
 
 __device__ __forceinline__ void st_global_b32(void* p, uint32_t v) {
     asm volatile("st.global.b32 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(v) : "memory");
@@ -227,13 +246,14 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
     constexpr int KA = L::KA, DKH = DK / 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool control = warp == kConv / 32;
+    const bool flagw = warp == kConv / 32 + 1;
     const int r = 32 * (warp & 3) + lane;   // tensor-memory lane = value row (converting warps)
     const int hh = (warp >> 2) & 1;         // column half
     const int g = blockIdx.x;
     const int bh = p.h0 + g;
-    const int n = p.chain_n;
+    const int n = p.nch;
     const int T = p.T;
-    const bool own = !control && r < DV;
+    const bool own = warp < kConv / 32 && r < DV;
 
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint64_t* bar_full = bar;        // [2] stage loaded (control expects the bytes)
@@ -246,6 +266,8 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
     uint64_t* bar_test = bar + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 10);
+    uint64_t* bar_rdy = bar + 11;    // [2] flag warp: the chunk's slot is in the ring
+    uint64_t* bar_cons = bar + 13;   // [2] control: the chunk's slot has been loaded
     const uint32_t aSS = sbase + L::OFF_SS, aUS = sbase + L::OFF_US, aUS2 = sbase + L::OFF_US2;
     float* sVec = reinterpret_cast<float*>(sm + L::OFF_VEC);
 
@@ -253,6 +275,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
         for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         for (int i = 5; i < 8; ++i) mbar_init(&bar[i], kConv / 32);
         mbar_init(bar_test, 1);
+        for (int i = 11; i < 15; ++i) mbar_init(&bar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -266,10 +289,6 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    // The previous window launch has written this window's slots and the
-    // state; only then may the next launch be dispatched.
-    griddep_wait();
-    griddep_launch_dependents();
 
     int status_bits = 0;
     bool failed = false;
@@ -287,9 +306,22 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
         // ======================= control warp (lane 0) =========================
         if (lane == 0 && !failed && n > 0) {
             bool pending[2] = {false, false};
-            int load_idx[2] = {0, 0};   // window chunk of the load last issued on each stage
-            auto issue_load = [&](int i, int s) {
-                const int c = p.chain_c0 + i;
+            int load_idx[2] = {0, 0};   // chunk of the load last issued on each stage
+            bool fail = false;
+            auto give_up = [&](int bit) {
+                fail = true;
+                status_bits |= bit;
+                *abort_flag = 1;
+                p.abort_all();
+            };
+            // Load chunk c into stage s once the flag warp has seen its slot
+            // stored (stage s = c & 1, the (c >> 1)-th hand-off on bar_rdy[s]).
+            auto issue_load = [&](int c, int s) {
+                if (fail) return;
+                if (!mbar_wait_or_abort(&bar_rdy[s], (c >> 1) & 1, abort_flag)) {
+                    give_up(kStatusFlagWait);
+                    return;
+                }
                 uint8_t* stg = sm + s * L::STAGE;
                 mbar_arrive_expect_tx(&bar_full[s], L::TX);
                 if (!KDA) {
@@ -299,11 +331,13 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                         tma_load_3d(tmk, &bar_full[s], stg + L::K_OFF + a * 8192, a * 64, c * C, bh);
                     }
                 }
-                const uint8_t* src = p.ws_slot + (static_cast<size_t>(p.chain_buf * p.G + g) * p.W + i) * S::BYTES;
+                const uint8_t* src = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES;
                 bulk_load(stg + L::SLOT_OFF, src, S::BYTES, &bar_full[s]);
                 pending[s] = true;
-                load_idx[s] = i;
+                load_idx[s] = c;
             };
+            // The slot of chunk c has arrived: the flag warp tells the prep CTAs.
+            auto consumed = [&](int c) { mbar_arrive(&bar_cons[c & 1]); };
             // Commits issued so far per MMA barrier: the k-th completes phase k.
             int n_u = 0, n_c = 0, n_o = 0;
             // X_0 W^T into COL_U (commit) and X_0 Q^T into the chunk's O1 buffer.
@@ -325,14 +359,9 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                                 kmaj(stg + L::Q_OFF + (kk / 4) * 8192 + (kk % 4) * 32), ID_O, kk > 0);
                 }
             };
-            bool fail = false;
             auto wait = [&](uint64_t* b, uint32_t parity, int bit) {
                 if (fail) return;
-                if (!mbar_wait_or_abort(b, parity, abort_flag)) {
-                    fail = true;
-                    status_bits |= bit;
-                    *abort_flag = 1;
-                }
+                if (!mbar_wait_or_abort(b, parity, abort_flag)) give_up(bit);
             };
             issue_load(0, 0);
             if (n > 1) issue_load(1, 1);
@@ -340,6 +369,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
             wait(&bar_full[0], 0, kStatusTmaWait);
             if (!fail) {
                 pending[0] = false;
+                consumed(0);
                 tc_fence_after();
                 issue_state_mmas(0);
             }
@@ -366,9 +396,12 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                 ++n_o;
                 if (it + 1 < n) {
                     wait(&bar_full[s ^ 1], ((it + 1) >> 1) & 1, kStatusTmaWait);
+                    if (!fail) {
+                        pending[s ^ 1] = false;
+                        consumed(it + 1);
+                    }
                     wait(bar_x, (it + 1) & 1, kStatusMmaWait);
                     if (fail) break;
-                    pending[s ^ 1] = false;
                     tc_fence_after();
                     issue_state_mmas(it + 1);
                 }
@@ -376,6 +409,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                     wait(bar_o, it & 1, kStatusMmaWait);   // every reader of stage s is done
                     if (fail) break;
                     issue_load(it + 2, s);
+                    if (fail) break;
                 }
             }
             if (fail) {
@@ -389,10 +423,33 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                 if (n_o > 0) mbar_wait(bar_o, (n_o - 1) & 1, 100000000ull);
             }
         }
+    } else if (flagw) {
+        // ======================= flag warp (lane 0) ============================
+        // Keeps the global hand-off off the control thread: waits for each
+        // chunk's ready flag (then hands the chunk to the control thread), and
+        // publishes the consumed count once the control thread has loaded a
+        // slot. Hand-off c on bar_rdy[c & 1] only follows the consumption of
+        // chunk c - 2, so neither barrier runs more than one phase ahead.
+        if (lane == 0 && !failed) {
+            for (int c = 0; c < n; ++c) {
+                if (c >= 2) {
+                    if (!mbar_wait_or_abort(&bar_cons[c & 1], ((c - 2) >> 1) & 1, abort_flag)) break;
+                    st_release_u64(p.consumed(g), p.epoch | static_cast<unsigned long long>(c - 1));
+                }
+                if (!p.wait_flag(p.ready(g, c), static_cast<unsigned long long>(c) + 1)) {
+                    status_bits |= kStatusFlagWait;
+                    *abort_flag = 1;
+                    p.abort_all();
+                    break;
+                }
+                fence_proxy_async_global();
+                mbar_arrive(&bar_rdy[c & 1]);
+            }
+        }
     } else {
         // ======================= converting warps ==============================
         // initial state: thread (r, hh) owns X[r][hh*DK/2 .. +DK/2)
-        const float* sin = p.chain_first ? (p.state_in ? p.state_in + bh * ssz : nullptr) : p.ws_state + g * ssz;
+        const float* sin = p.state_in ? p.state_in + bh * ssz : nullptr;
         float st[DKH];
 #pragma unroll
         for (int i = 0; i < DKH; i += 4) {
@@ -433,7 +490,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
         int it = 0;
         for (; it < n; ++it) {
             const int s = it & 1;
-            const int t0 = (p.chain_c0 + it) * C;
+            const int t0 = it * C;
             const float* vec = reinterpret_cast<const float*>(sm + s * L::STAGE + L::SLOT_OFF + S::V_OFF);
             float* sv = sVec + 128 * s;
             // ---- U^T = Ut^T - X_0 W^T; bf16 copies U^T and U^T diag(gam_C/gam) ----
@@ -532,24 +589,25 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
             if (lane == 0) mbar_arrive(bar_ep);
             bad |= !ok;
         }
-        // ---- state for the next launch, or the final state ----------------------
+        // ---- the final state -----------------------------------------------------
         bad = named_sync_or(kBarConv, kConv, bad);
         if (!bad) {
-            float* dst = p.chain_last ? (p.state_out ? p.state_out + bh * ssz : nullptr) : p.ws_state + g * ssz;
+            float* dst = p.state_out ? p.state_out + bh * ssz : nullptr;
             if (dst && own) {
 #pragma unroll
                 for (int i = 0; i < DKH; i += 4)
                     *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * DK + hh * DKH + i) =
                         make_float4(st[i], st[i + 1], st[i + 2], st[i + 3]);
             }
-        } else if (tid == 0 && !failed) {
-            status_bits |= kStatusMmaWait;
+        } else if (tid == 0) {
+            if (!failed) status_bits |= kStatusMmaWait;
+            p.abort_all();
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
-    if (status_bits && (tid == 0 || (control && lane == 0))) atomicOr(p.status, status_bits);
+    if (status_bits && (tid == 0 || ((control || flagw) && lane == 0))) atomicOr(p.status, status_bits);
 }
 
 // ============================================================================
@@ -653,7 +711,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     const int hh = warp >> 2;
     const int pid = blockIdx.x - p.n_chain;
     const int np = gridDim.x - p.n_chain;
-    const int nunits = p.G * p.prep_n;
+    const int nunits = p.G * p.nch;
     const int T = p.T;
 
     float* As = reinterpret_cast<float*>(sm + L::OFF_AS);
@@ -680,18 +738,6 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    // Programmatic dependent launch. The first launch of a call waits for
-    // the kernels before it at once (they may have produced the inputs). A
-    // later launch may only be dispatched after every CTA of the previous one
-    // passed this point, so its inputs are complete; it computes its first
-    // unit while the previous launch finishes and waits only before its
-    // first write to the slot ring, whose buffer that launch's chain reads.
-    bool waited = false;
-    if (!p.early) {
-        griddep_wait();
-        griddep_launch_dependents();
-        waited = true;
-    }
 
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
         const bool ok = mbar_wait(b, parity, kWaitLimitNs);
@@ -712,13 +758,43 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         if (named_sync_or(kBarConv, kConv, !ok)) { status_bits |= kStatusTestHook; failed = true; }
     }
 
-    // unit u -> (head g = u % G, chunk prep_c0 + u / G)
+    // unit u -> (head g = u % G, chunk u / G): the units go chunk by chunk
     auto unit_g = [&](int u) { return u % p.G; };
     auto unit_i = [&](int u) { return u / p.G; };
+    // Slot hand-off (thread 0). The slot of unit u goes to ring position
+    // chunk % R of its head once the chain has loaded the chunk R before it;
+    // its ready flag is raised when the store has completed, which thread 0
+    // checks early in its next unit (or after the last one).
+    int st_g = -1, st_c = 0;   // the stored slot whose flag is still down
+    auto release_stored = [&]() {
+        if (tid == 0 && st_g >= 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            st_release_u64(p.ready(st_g, st_c), p.epoch | (static_cast<unsigned long long>(st_c) + 1));
+            st_g = -1;
+        }
+    };
+    auto store_slot = [&](int u, uint32_t src) -> bool {
+        bool ok = true;
+        if (tid == 0) {
+            const int g = unit_g(u), c = unit_i(u);
+            if (c >= p.R) ok = p.wait_flag(p.consumed(g), static_cast<unsigned long long>(c - p.R) + 1);
+            if (ok) {
+                uint8_t* dst = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES;
+                bulk_store(dst, src, S::BYTES);
+                bulk_commit();
+                st_g = g;
+                st_c = c;
+            } else {
+                p.abort_all();
+            }
+        }
+        return !named_sync_or(kBarConv, kConv, !ok);
+    };
     bool pending[2] = {false, false};
     auto issue_load = [&](int u, int s) {
         const int bh = p.h0 + unit_g(u);
-        const int y = (p.prep_c0 + unit_i(u)) * C;
+        const int y = unit_i(u) * C;
         uint8_t* stg = sm + s * L::STAGE;
         mbar_arrive_expect_tx(&bar_full[s], L::TX);
 #pragma unroll
@@ -736,7 +812,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         bv = 0.f;
         if (u < nunits && tid < 64) {
             const int bh = p.h0 + unit_g(u);
-            const int t = (p.prep_c0 + unit_i(u)) * C + tid;
+            const int t = unit_i(u) * C + tid;
             if (t < T) {
                 gv = p.gate[static_cast<size_t>(bh) * T + t];
                 bv = p.beta[static_cast<size_t>(bh) * T + t];
@@ -788,9 +864,8 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
                 mma_bf16_ss(tmem + L::COL_G, d, d, ID_G, kk > 0);
             }
             mma_commit(bar_m);
-            // the slot buffer written below was last stored two units ago
-            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         }
+        release_stored();   // the previous unit's slot (also frees its buffer)
         sync_conv();
         if (tid >= 32 && tid < 64) sG2[tid] += sG2[31];
         sync_conv();
@@ -883,23 +958,16 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         fence_proxy_async_smem();
         tc_fence_before();
         sync_conv();
-        if (!waited) {
-            griddep_wait();
-            griddep_launch_dependents();
-            waited = true;
-        }
-        if (tid == 0) {
-            uint8_t* dst = p.ws_slot + (static_cast<size_t>(p.prep_buf * p.G + unit_g(u)) * p.W + unit_i(u)) * S::BYTES;
-            bulk_store(dst, aOut, S::BYTES);
-            bulk_commit();
-        }
+        if (!store_slot(u, aOut)) { status_bits |= kStatusFlagWait; failed = true; break; }
     }
 
     if (failed && tid == 0) {
         for (int s2 = 0; s2 < 2; ++s2)
             if (pending[s2]) mbar_wait(&bar_full[s2], ((s2 == (k & 1) ? k : k + 1) >> 1) & 1, 100000000ull);
     }
+    if (!failed) release_stored();
     if (tid == 0) bulk_wait_all();
+    if (failed && tid == 0) p.abort_all();
     tc_fence_before();
     sync_conv();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
@@ -936,7 +1004,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     const int hh = warp >> 2;
     const int pid = blockIdx.x - p.n_chain;
     const int np = gridDim.x - p.n_chain;
-    const int nunits = p.G * p.prep_n;
+    const int nunits = p.G * p.nch;
     const int T = p.T;
     // element pass: thread (cp, seg) owns channels c0, c0 + 1 of tokens
     // [seg*SL, seg*SL + SL), all inside sub-chunk sa
@@ -976,14 +1044,6 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    // Programmatic dependent launch as in the scalar-gate prep role: a later
-    // window launch computes its first unit before it waits.
-    bool waited = false;
-    if (!p.early) {
-        griddep_wait();
-        griddep_launch_dependents();
-        waited = true;
-    }
 
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
         const bool ok = mbar_wait(b, parity, kWaitLimitNs);
@@ -1004,15 +1064,45 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         if (named_sync_or(kBarConv, kConv, !ok)) { status_bits |= kStatusTestHook; failed = true; }
     }
 
-    auto unit_g = [&](int u) { return u % p.G; };
+    auto unit_g = [&](int u) { return u % p.G; };   // as in the scalar-gate role
     auto unit_i = [&](int u) { return u / p.G; };
+    // Slot hand-off (thread 0). The slot of unit u goes to ring position
+    // chunk % R of its head once the chain has loaded the chunk R before it;
+    // its ready flag is raised when the store has completed, which thread 0
+    // checks early in its next unit (or after the last one).
+    int st_g = -1, st_c = 0;   // the stored slot whose flag is still down
+    auto release_stored = [&]() {
+        if (tid == 0 && st_g >= 0) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            st_release_u64(p.ready(st_g, st_c), p.epoch | (static_cast<unsigned long long>(st_c) + 1));
+            st_g = -1;
+        }
+    };
+    auto store_slot = [&](int u, uint32_t src) -> bool {
+        bool ok = true;
+        if (tid == 0) {
+            const int g = unit_g(u), c = unit_i(u);
+            if (c >= p.R) ok = p.wait_flag(p.consumed(g), static_cast<unsigned long long>(c - p.R) + 1);
+            if (ok) {
+                uint8_t* dst = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES;
+                bulk_store(dst, src, S::BYTES);
+                bulk_commit();
+                st_g = g;
+                st_c = c;
+            } else {
+                p.abort_all();
+            }
+        }
+        return !named_sync_or(kBarConv, kConv, !ok);
+    };
     // Copies in flight (thread 0): the k/q stages, and the single V and gate
     // buffers (one load at a time each, the n-th completing phase n).
     bool pend_qk[2] = {false, false};
     int v_issued = 0, v_done = 0, g_issued = 0, g_done = 0;
     auto issue_qk = [&](int u, int s) {
         const int bh = p.h0 + unit_g(u);
-        const int y = (p.prep_c0 + unit_i(u)) * C;
+        const int y = unit_i(u) * C;
         uint8_t* stg = sm + s * L::QK_BYTES;
         mbar_arrive_expect_tx(&bar_qk[s], L::QK_BYTES);
 #pragma unroll
@@ -1024,7 +1114,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     };
     auto issue_v = [&](int u) {
         const int bh = p.h0 + unit_g(u);
-        const int y = (p.prep_c0 + unit_i(u)) * C;
+        const int y = unit_i(u) * C;
         mbar_arrive_expect_tx(bar_v, VA * 8192);
 #pragma unroll
         for (int a = 0; a < VA; ++a) tma_load_3d(tmv, bar_v, sm + L::OFF_V + a * 8192, a * 64, y, bh);
@@ -1033,7 +1123,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     // the gate rows of a chunk are contiguous: one bulk copy of the valid rows
     auto issue_g = [&](int u) {
         const int bh = p.h0 + unit_g(u);
-        const int y = (p.prep_c0 + unit_i(u)) * C;
+        const int y = unit_i(u) * C;
         const int rows = T - y < C ? T - y : C;
         const uint32_t bytes = static_cast<uint32_t>(rows) * DK * 4;
         mbar_arrive_expect_tx(bar_g, bytes);
@@ -1044,7 +1134,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         bv = 0.f;
         if (u < nunits && tid < 64) {
             const int bh = p.h0 + unit_g(u);
-            const int t = (p.prep_c0 + unit_i(u)) * C + tid;
+            const int t = unit_i(u) * C + tid;
             if (t < T) bv = p.beta[static_cast<size_t>(bh) * T + t];
         }
     };
@@ -1066,7 +1156,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         const int s = k & 1;
         const int un = u + np;
         const uint32_t stg = sbase + s * L::QK_BYTES;
-        const int nvalid = T - (p.prep_c0 + unit_i(u)) * C;   // tokens of the unit inside the sequence
+        const int nvalid = T - unit_i(u) * C;   // tokens of the unit inside the sequence
         if (tid == 0 && un < nunits) {
             fence_proxy_async_smem();
             issue_qk(un, s ^ 1);   // stage s^1's MMAs finished with the previous unit
@@ -1094,8 +1184,9 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         }
         if (tid < 64) sB[tid] = b_nx;
         load_b(un, b_nx);
-        // the slot buffer is written below: the store of the previous unit has read it
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        // the slot buffer is written below: the previous unit's store completes
+        // here and its flag goes up
+        release_stored();
         sync_conv();
         // ---- cumulative log2 at the block ends: segment offset, the sub-chunk
         //      references r_a (end of block 2a), G_C ---------------------------------
@@ -1276,16 +1367,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         fence_proxy_async_smem();
         tc_fence_before();
         sync_conv();
-        if (!waited) {
-            griddep_wait();
-            griddep_launch_dependents();
-            waited = true;
-        }
-        if (tid == 0) {
-            uint8_t* dst = p.ws_slot + (static_cast<size_t>(p.prep_buf * p.G + unit_g(u)) * p.W + unit_i(u)) * S::BYTES;
-            bulk_store(dst, aOut, S::BYTES);
-            bulk_commit();
-        }
+        if (!store_slot(u, aOut)) { status_bits |= kStatusFlagWait; failed = true; break; }
     }
 
     if (failed && tid == 0) {
@@ -1294,7 +1376,9 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         if (v_issued > v_done) mbar_wait(bar_v, (v_issued - 1) & 1, 100000000ull);
         if (g_issued > g_done) mbar_wait(bar_g, (g_issued - 1) & 1, 100000000ull);
     }
+    if (!failed) release_stored();
     if (tid == 0) bulk_wait_all();
+    if (failed && tid == 0) p.abort_all();
     tc_fence_before();
     sync_conv();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
@@ -1320,68 +1404,49 @@ gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     }
 }
 
+// Every launch takes a fresh epoch (the upper half of each flag value), so a
+// flag of an earlier launch is never mistaken for one of this launch.
+std::atomic<unsigned> g_epoch{0};
+
 template <int DK, int DV, bool KDA>
-cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int W, cudaStream_t s) {
+cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int R, cudaStream_t s) {
     constexpr uint32_t smem = smem_alloc<DK, DV, KDA>();
     static_assert(smem <= 232448, "shared memory budget");
     auto kern = gdn_kernel<DK, DV, KDA>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nch = (a.T + C - 1) / C;
-    // Windows of 2, 4, 8 chunks, then W: the chain starts after a short
-    // prep-only first launch, and the prep of each window fits in the walk
-    // of the previous one.
-    int wstart[130];
-    int NW = 0;
-    for (int c0 = 0, w = 2; c0 < nch; c0 += w, w *= 2) {
-        if (w > W) w = W;
-        wstart[NW++] = c0;
-        if (NW == 129) return cudaErrorInvalidValue;
-    }
-    wstart[NW] = nch;
-    const size_t state_bytes = static_cast<size_t>(G) * DK * DV * sizeof(float);
     Params p;
     p.gate = a.gate;
     p.beta = a.beta;
     p.state_in = a.state_in;
     p.state_out = a.state_out;
     p.out = static_cast<__nv_bfloat16*>(a.out);
-    p.ws_state = a.workspace;
-    p.ws_slot = reinterpret_cast<uint8_t*>(a.workspace) + state_bytes;
+    p.ws_flag = reinterpret_cast<unsigned long long*>(a.workspace);
+    p.ws_slot = reinterpret_cast<uint8_t*>(a.workspace) + align_up(flag_words(G, R) * 8, 1024);
     p.T = a.T;
-    p.W = W;
+    p.nch = nch;
+    p.R = R;
     p.flags = a.flags;
     p.status = a.status;
+    // One cooperative launch per group of sequence-heads: every CTA is
+    // resident, so the chain and prep CTAs may wait on each other's flags.
     for (int h0 = 0; h0 < a.BH; h0 += G) {
         p.h0 = h0;
         p.G = a.BH - h0 < G ? a.BH - h0 : G;
-        for (int j = 0; j <= NW; ++j) {
-            p.chain_n = 0;
-            p.prep_n = 0;
-            if (j >= 1) {
-                p.chain_c0 = wstart[j - 1];
-                p.chain_n = wstart[j] - wstart[j - 1];
-                p.chain_buf = (j - 1) & 1;
-                p.chain_first = (j == 1);
-                p.chain_last = (j == NW);
-            }
-            if (j < NW) {
-                p.prep_c0 = wstart[j];
-                p.prep_n = wstart[j + 1] - wstart[j];
-                p.prep_buf = j & 1;
-            }
-            p.early = (j >= 1);
-            p.n_chain = p.chain_n > 0 ? p.G : 0;
-            int n_prep = 0;
-            if (p.prep_n > 0) {
-                const int units = p.G * p.prep_n;
-                n_prep = a.sm_count - p.n_chain > 0 ? a.sm_count - p.n_chain : a.sm_count;
-                if (n_prep > units) n_prep = units;
-            }
-            e = launch_pdl(kern, static_cast<unsigned>(p.n_chain + n_prep), kThreads, smem, s, m.q, m.k, m.v, p);
-            if (e != cudaSuccess) return e;
-            if (a.nlaunch) ++*a.nlaunch;
-        }
+        p.n_chain = p.G;
+        p.epoch = static_cast<unsigned long long>(g_epoch.fetch_add(1) + 1) << 32;
+        // The workspace is shared with the other variants' scratch: clear the
+        // flag words so that no stale value reads as raised.
+        e = cudaMemsetAsync(p.ws_flag, 0, flag_words(G, R) * 8, s);
+        if (e != cudaSuccess) return e;
+        const int units = p.G * nch;
+        int n_prep = a.sm_count - p.n_chain;
+        if (n_prep > units) n_prep = units;
+        if (n_prep < 1) return cudaErrorInvalidConfiguration;
+        e = launch_coop(kern, static_cast<unsigned>(p.n_chain + n_prep), kThreads, smem, s, m.q, m.k, m.v, p);
+        if (e != cudaSuccess) return e;
+        if (a.nlaunch) ++*a.nlaunch;
     }
     return cudaSuccess;
 }
@@ -1396,34 +1461,36 @@ size_t gdn_slot_bytes(int dk, int dv, bool kda) {
 
 int gdn_group(int BH) { return BH < kGdnMaxGroup ? BH : kGdnMaxGroup; }
 
+// Flag words, then a ring of R chunks per sequence-head of a group of G.
+static size_t ring_bytes(int G, int R, int dk, int dv, bool kda) {
+    return gdn::align_up(gdn::flag_words(G, R) * 8, 1024) + static_cast<size_t>(G) * R * gdn_slot_bytes(dk, dv, kda);
+}
+
 size_t gdn_workspace_bytes(int BH, int dk, int dv, int W, bool kda) {
-    const int G = gdn_group(BH);
-    return static_cast<size_t>(G) * dk * dv * sizeof(float) +
-           2 * static_cast<size_t>(G) * W * gdn_slot_bytes(dk, dv, kda);
+    return ring_bytes(gdn_group(BH), 2 * W, dk, dv, kda);
 }
 
 cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     const int G = gdn_group(a.BH);
-    const size_t state_bytes = static_cast<size_t>(G) * a.dk * a.dv * sizeof(float);
     const bool kda = a.variant == kKda;
-    const size_t per_w = 2 * static_cast<size_t>(G) * gdn_slot_bytes(a.dk, a.dv, kda);
-    if (!a.workspace || a.ws_bytes < state_bytes + per_w) return cudaErrorInvalidValue;
     const int nch = (a.T + C - 1) / C;
-    size_t W = (a.ws_bytes - state_bytes) / per_w;
-    if (W > static_cast<size_t>(kGdnWindow)) W = kGdnWindow;
-    if (W > static_cast<size_t>(nch)) W = nch;
-    const int w = static_cast<int>(W);
+    // the deepest ring (up to 2 kGdnWindow chunks, no deeper than the
+    // sequence) that the workspace holds
+    int R = 2 * kGdnWindow;
+    if (R > nch) R = nch < 2 ? 2 : nch;
+    while (R > 2 && ring_bytes(G, R, a.dk, a.dv, kda) > a.ws_bytes) --R;
+    if (!a.workspace || ring_bytes(G, R, a.dk, a.dv, kda) > a.ws_bytes) return cudaErrorInvalidValue;
     if (kda) {
-        if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, true>(m, a, G, w, s);
-        if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, true>(m, a, G, w, s);
-        if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, true>(m, a, G, w, s);
-        if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, true>(m, a, G, w, s);
+        if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, true>(m, a, G, R, s);
+        if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, true>(m, a, G, R, s);
+        if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, true>(m, a, G, R, s);
+        if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, true>(m, a, G, R, s);
         return cudaErrorInvalidValue;
     }
-    if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, false>(m, a, G, w, s);
-    if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, false>(m, a, G, w, s);
-    if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, false>(m, a, G, w, s);
-    if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, false>(m, a, G, w, s);
+    if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, false>(m, a, G, R, s);
+    if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, false>(m, a, G, R, s);
+    if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, false>(m, a, G, R, s);
+    if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, false>(m, a, G, R, s);
     return cudaErrorInvalidValue;
 }
 

@@ -26,6 +26,7 @@ enum : int {
     kStatusTmaWait = 1,    // a TMA completion wait expired
     kStatusMmaWait = 2,    // an MMA completion wait expired
     kStatusTestHook = 4,   // the test hook's never-signalled wait expired (expected)
+    kStatusFlagWait = 8,   // a hand-off flag from another CTA of the launch never came
 };
 
 // Default limit of every bounded wait: 2 s. A healthy wait here ends in
@@ -180,6 +181,38 @@ __device__ __forceinline__ float lg2(float x) {
 // (tensor core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// The same between the proxies for global memory: bulk copies that wrote
+// (or will read) global memory against generic flag accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- flags in global memory
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Wait until *f >= want, giving up after kWaitLimitNs or as soon as *abort
+// equals abort_val. Only for CTAs of one launch that are all resident
+// (cooperative launch). Returns true when the value arrived.
+__device__ __forceinline__ bool flag_wait(const unsigned long long* f, unsigned long long want,
+                                          const unsigned long long* abort, unsigned long long abort_val) {
+    if (ld_acquire_u64(f) >= want) return true;
+    const uint64_t t0 = globaltimer_ns();
+    unsigned sleep = 32;   // back off to 512 ns between polls of the line
+    while (true) {
+        __nanosleep(sleep);
+        if (sleep < 512) sleep *= 2;
+        if (ld_acquire_u64(f) >= want) return true;
+        if (*reinterpret_cast<const volatile unsigned long long*>(abort) == abort_val) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -67,11 +67,11 @@
  * states do not fit takes the sequential kernel instead), for segment
  * summaries when B*H is too small to fill the GPU ((SM count) x
  * (d_k*d_v + d_k) floats) and, for
- * LA_GDN and LA_KDA, for the fp32 states of a group of G = min(B*H, 32)
- * sequence-heads plus two windows of 16 chunks of per-chunk intermediates
- * (G*d_k*d_v*4 + 2*G*16*((d_k+d_v)*128 + 8704 [+ 256*d_k for LA_KDA])
- * bytes; 78 MB at G = 32, d_k = d_v = 128, sized for LA_KDA; a smaller
- * workspace only shortens the windows). The largest of these is allocated when the
+ * LA_GDN and LA_KDA, for the hand-off flags and a ring of up to 32 chunks
+ * of per-chunk intermediates for each of a group of G = min(B*H, 32)
+ * sequence-heads (G*32*((d_k+d_v)*128 + 8704 [+ 256*d_k for LA_KDA]) bytes
+ * plus a few KB; 76 MB at G = 32, d_k = d_v = 128, sized for LA_KDA; a
+ * smaller workspace only makes the ring shallower). The largest of these is allocated when the
  * configuration can take the tensor-core path (bf16, d_k, d_v in {64, 128}).
  * Calls that overlap on the GPU through the same handle (different streams)
  * would share that workspace: serialize them.
@@ -239,9 +239,8 @@ const char* la_last_error(const la_handle* h);
  * enqueued (0 after a failed or a T = 0 call, or for a NULL handle). A
  * diagnostic: which algorithm the library picked shows in this count (1: the
  * recurrent kernel or a decode step; 1 or 2: the chunk kernel, with segment
- * summaries when B*H is small; 3: the three-phase parallel form; for LA_GDN
- * and LA_KDA one per window of chunks plus one, for each group of 32
- * sequence-heads). */
+ * summaries when B*H is small; 3: the three-phase parallel form; LA_GDN and
+ * LA_KDA: one per group of 32 sequence-heads). */
 int la_last_launches(const la_handle* h);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */

@@ -464,12 +464,12 @@ def test_rejected_calls_do_not_launch():
     ("gla", 200, 0, 64, 3),
     ("norm", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 2),      # segment summaries + chunk kernel
     ("norm", 100, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),      # too short to split
-    ("gdn", 200, 0, 64, 3),                                  # windows of 2 and 2 chunks, + 1
-    ("gdn", 64 * 40, 0, 64, 6),                              # windows of 2, 4, 8, 16, 10, + 1
+    ("gdn", 200, 0, 64, 1),                                  # one cooperative launch per 32 heads
+    ("gdn", 64 * 40, 0, 64, 1),
     ("gla", 200, 0, 1, 1),                                   # the recurrent kernel
     ("norm_decay", 200, 0, 64, 3),                           # decayed: the three-phase form
     ("norm_decay", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),  # decayed, not three-phase: recurrent
-    ("kda", 200, 0, 0, 3),                                   # per-channel delta rule: as gdn
+    ("kda", 200, 0, 0, 1),                                   # per-channel delta rule: as gdn
     ("kda", 200, 0, 1, 1),                                   # per-channel delta rule: recurrent
 ])
 def test_launch_counts(variant, T, flags, chunk, expect):
