@@ -256,9 +256,7 @@ int la_create(const la_config* cfg, la_handle** out) {
     h->ws_bytes = static_cast<size_t>(h->sm_count) * (static_cast<size_t>(cfg->d_k) * cfg->d_v + cfg->d_k) * sizeof(float);
     const bool tc_shape = cfg->io == LA_BF16 && (cfg->d_k == 64 || cfg->d_k == 128) && (cfg->d_v == 64 || cfg->d_v == 128);
     if (tc_shape) {
-        // (sized for the per-channel decay, whose slots are the larger)
-        const size_t gdn =
-            la::chunk::gdn_workspace_bytes(cfg->B * cfg->H, cfg->d_k, cfg->d_v, la::chunk::kGdnWindow, true);
+        const size_t gdn = la::chunk::gdn_workspace_bytes(cfg->B * cfg->H, cfg->d_k, cfg->d_v, la::chunk::kGdnWindow);
         if (gdn > h->ws_bytes) h->ws_bytes = gdn;
         // three-phase normalized / gated prefill: per-chunk states of up to
         // 128 chunks (T = 8192) per sequence-head, capped at the L2 budget

@@ -85,7 +85,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // delta rule's launcher accepts (it sizes its windows to the scratch).
 size_t scratch_needed(int variant, int BH, int T, int dk, int dv, int sms) {
     const int nch = (T + 63) / 64;
-    if (variant == LA_GDN) return la::chunk::gdn_workspace_bytes(BH, dk, dv, 1, false);
+    if (variant == LA_GDN) return la::chunk::gdn_workspace_bytes(BH, dk, dv, 1);
     if (BH >= sms || nch < 4) return 0;
     int nseg = sms / BH;
     if (nseg > nch / 2) nseg = nch / 2;

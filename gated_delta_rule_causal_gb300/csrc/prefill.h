@@ -26,10 +26,10 @@ cudaError_t launch_gla(int dk, int dv, const Maps& m, const Params& p, int BH, c
 // most, as deep as the workspace allows).
 constexpr int kGdnMaxGroup = 32;   // chain CTAs per launch
 constexpr int kGdnWindow = 16;     // half the deepest ring, in chunks
-size_t gdn_slot_bytes(int dk, int dv, bool kda);
+size_t gdn_slot_bytes(int dk, int dv);
 int gdn_group(int BH);
 // Workspace for a ring of 2W chunks (W >= 1 is the least the launcher accepts).
-size_t gdn_workspace_bytes(int BH, int dk, int dv, int W, bool kda);
+size_t gdn_workspace_bytes(int BH, int dk, int dv, int W);
 cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s);
 
 // Normalized / per-channel gated: three fully parallel phases (chunk

@@ -81,51 +81,42 @@ using chunk::store_row32_bf16;
 constexpr int kConv = 256;              // converting threads (8 warps)
 constexpr int kThreads = kConv + 64;    // + a control warp and a flag warp (chain CTAs)
 constexpr uint32_t kBarConv = 1;        // named barrier of the converting warps
+constexpr uint32_t kBarInit = 2;        // prep CTAs: converting warps and the store warp, once
 
 __host__ __device__ constexpr uint32_t align1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // One chunk's intermediates, byte-identical in the workspace and in shared
 // memory. Tiles are bf16 with the 128-byte swizzle (1024-aligned offsets).
-// With the per-channel decay (KDA) the slot also carries Q o Gam and
-// K o Gam_C / Gam ([64][DK] K-major tiles, KA atoms of 8 KB), and its vector
-// is Gam_C [DK].
-template <int DK, int DV, bool KDA>
+// The same layout serves both decays: with a scalar gate Gam_t = gam_t on
+// every channel, so Q o Gam = diag(gam) Q and K o Gam_C/Gam = diag(gam_C/gam) K.
+template <int DK, int DV>
 struct Slot {
     static constexpr int KA = DK / 64;
     static constexpr uint32_t W_OFF = 0;                  // W^T [dk][64 t]: MN-major B operand
     static constexpr uint32_t U_OFF = DK * 128;           // Ut^T [dv][64 t]
     static constexpr uint32_t P_OFF = U_OFF + DV * 128;   // P [64 t][64 j]: K-major B operand
-    static constexpr uint32_t QG_OFF = P_OFF + 8192;      // KDA: Q o Gam        [64 t][DK]
-    static constexpr uint32_t KP_OFF = QG_OFF + (KDA ? KA * 8192 : 0);   // KDA: K o Gam_C/Gam [64 j][DK]
-    static constexpr uint32_t V_OFF = KP_OFF + (KDA ? KA * 8192 : 0);
-    // gdn: gam_t [64], gam_C/gam_t [64]; KDA: Gam_C [DK] (fp32)
+    static constexpr uint32_t QG_OFF = P_OFF + 8192;      // Q o Gam          [64 t][DK], KA atoms of 8 KB
+    static constexpr uint32_t KP_OFF = QG_OFF + KA * 8192;   // K o Gam_C/Gam [64 j][DK]
+    static constexpr uint32_t V_OFF = KP_OFF + KA * 8192;    // Gam_C [DK] (fp32)
     static constexpr uint32_t BYTES = V_OFF + 512;
     static_assert(BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
 
-template <int DK, int DV, bool KDA>
+template <int DK, int DV>
 struct ChainLayout {
     static constexpr int KA = DK / 64;
-    using S = Slot<DK, DV, KDA>;
-    // gdn: q and k come by TMA in front of the slot; KDA: the slot holds
-    // their rescaled forms.
-    static constexpr uint32_t QK_BYTES = KDA ? 0 : 2 * KA * 8192;
-    static constexpr uint32_t Q_OFF = KDA ? S::QG_OFF : 0;              // q [64 t][DK], KA atoms of 8 KB
-    static constexpr uint32_t K_OFF = KDA ? S::KP_OFF : KA * 8192;      // k [64 j][DK]
-    static constexpr uint32_t SLOT_OFF = QK_BYTES;
-    static constexpr uint32_t STAGE = align1024(SLOT_OFF + S::BYTES);
-    static constexpr uint32_t TX = QK_BYTES + S::BYTES;
+    using S = Slot<DK, DV>;
+    static constexpr uint32_t STAGE = align1024(S::BYTES);      // one slot per stage
     static constexpr uint32_t OFF_SS = 2 * STAGE;               // X_0 bf16 [128 rows][DK]
     static constexpr uint32_t OFF_US = OFF_SS + KA * 16384;     // U^T bf16 [128 rows][64 j]
-    static constexpr uint32_t OFF_US2 = KDA ? OFF_US : OFF_US + 16384;   // U^T diag(gam_C/gam) (gdn)
-    static constexpr uint32_t OFF_VEC = OFF_US2 + 16384;        // the slot vector per stage
+    static constexpr uint32_t OFF_VEC = OFF_US + 16384;         // the slot vector per stage
     static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 512;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
     // TMEM columns (lanes = value rows)
-    static constexpr uint32_t COL_U = 0;        // X_0 W^T           [dv][64]
-    static constexpr uint32_t COL_O = 64;       // two buffers of [O1 | O2], 128 columns each
-    static constexpr uint32_t COL_S = 320;      // U^T K'            [dv][DK]
+    static constexpr uint32_t COL_U = 0;        // X_0 W^T                          [dv][64]
+    static constexpr uint32_t COL_O = 64;       // two buffers of X_0 QG^T + U^T P^T [dv][64], 128 apart
+    static constexpr uint32_t COL_S = 320;      // U^T K'                           [dv][DK]
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(COL_S + DK <= TMEM_COLS, "tensor memory budget");
 };
@@ -134,16 +125,15 @@ template <int DK, int DV>
 struct PrepLayout {
     static constexpr int KA = DK / 64;
     static constexpr int VA = DV / 64;
-    using S = Slot<DK, DV, false>;
+    using S = Slot<DK, DV>;
     static constexpr uint32_t QK_BYTES = KA * 16384;    // per k-atom: rows 0-63 k, rows 64-127 q
     static constexpr uint32_t V_BYTES = VA * 8192;
     static constexpr uint32_t STAGE = QK_BYTES + V_BYTES;
     static constexpr uint32_t TX = STAGE;
     static constexpr uint32_t OFF_TB1 = 2 * STAGE;       // T diag(beta)     bf16 [t][j]
     static constexpr uint32_t OFF_TB2 = OFF_TB1 + 8192;  // T diag(beta gam) bf16 [t][j]
-    static constexpr uint32_t OUT_STRIDE = align1024(S::BYTES);
-    static constexpr uint32_t OFF_OUT = OFF_TB2 + 8192;  // two slots being assembled / stored
-    static constexpr uint32_t OFF_AS = OFF_OUT + 2 * OUT_STRIDE;        // fp32 [64][kAStride]
+    static constexpr uint32_t OFF_OUT = OFF_TB2 + 8192;  // the slot being assembled / stored
+    static constexpr uint32_t OFF_AS = OFF_OUT + align1024(S::BYTES);   // fp32 [64][kAStride]
     static constexpr uint32_t OFF_RS = OFF_AS + C * kAStride * 4;       // fp32 [32][kRStride]
     static constexpr uint32_t OFF_MISC = OFF_RS + 32 * 40 * 4;          // log2 prefix, beta, beta gam
     static constexpr uint32_t OFF_BAR = OFF_MISC + 3 * 64 * 4;
@@ -166,7 +156,7 @@ template <int DK, int DV>
 struct PrepLayoutKda {
     static constexpr int KA = DK / 64;
     static constexpr int VA = DV / 64;
-    using S = Slot<DK, DV, true>;
+    using S = Slot<DK, DV>;
     static constexpr uint32_t QK_BYTES = KA * 16384;     // per k-atom: rows 0-63 k, rows 64-127 q
     static constexpr uint32_t OFF_V = 2 * QK_BYTES;      // V [64 t][DV]
     static constexpr uint32_t OFF_GATE = OFF_V + VA * 8192;   // alpha fp32 [64 t][DK]
@@ -193,7 +183,7 @@ struct PrepLayoutKda {
 template <int DK, int DV, bool KDA>
 constexpr uint32_t smem_alloc() {
     constexpr uint32_t prep = KDA ? PrepLayoutKda<DK, DV>::BYTES : PrepLayout<DK, DV>::BYTES;
-    constexpr uint32_t chain = ChainLayout<DK, DV, KDA>::BYTES;
+    constexpr uint32_t chain = ChainLayout<DK, DV>::BYTES;
     return (chain > prep ? chain : prep) + 1024;
 }
 
@@ -231,6 +221,13 @@ struct Params {
 // Flag words the launcher reserves in front of the slots (ready, consumed, abort).
 constexpr size_t flag_words(int G, int R) { return static_cast<size_t>(G) * R + 16 * (G + 1); }
 
+__device__ __forceinline__ void st_shared_v4_u4(uint32_t addr, uint4 v) { st_shared_v4(addr, v.x, v.y, v.z, v.w); }
+// Eight bf16 values scaled by f, rounded back to bf16.
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 u, float f) {
+    const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y), c = unpack_bf16(u.z), d = unpack_bf16(u.w);
+    return make_uint4(pack_bf16(a.x * f, a.y * f), pack_bf16(b.x * f, b.y * f), pack_bf16(c.x * f, c.y * f),
+                      pack_bf16(d.x * f, d.y * f));
+}
 __device__ __forceinline__ void st_global_b32(void* p, uint32_t v) {
     asm volatile("st.global.b32 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(v) : "memory");
 }
@@ -238,12 +235,11 @@ __device__ __forceinline__ void st_global_b32(void* p, uint32_t v) {
 // ============================================================================
 // chain CTA: the state-dependent part of every chunk of one window
 // ============================================================================
-template <int DK, int DV, bool KDA>
-__device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtensorMap* tmk, const Params& p,
-                                           uint8_t* sm, uint32_t sbase) {
-    using L = ChainLayout<DK, DV, KDA>;
-    using S = Slot<DK, DV, KDA>;
-    constexpr int KA = L::KA, DKH = DK / 2;
+template <int DK, int DV>
+__device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_t sbase) {
+    using L = ChainLayout<DK, DV>;
+    using S = Slot<DK, DV>;
+    constexpr int DKH = DK / 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool control = warp == kConv / 32;
     const bool flagw = warp == kConv / 32 + 1;
@@ -268,7 +264,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 10);
     uint64_t* bar_rdy = bar + 11;    // [2] flag warp: the chunk's slot is in the ring
     uint64_t* bar_cons = bar + 13;   // [2] control: the chunk's slot has been loaded
-    const uint32_t aSS = sbase + L::OFF_SS, aUS = sbase + L::OFF_US, aUS2 = sbase + L::OFF_US2;
+    const uint32_t aSS = sbase + L::OFF_SS, aUS = sbase + L::OFF_US;
     float* sVec = reinterpret_cast<float*>(sm + L::OFF_VEC);
 
     if (tid == 0) {
@@ -278,10 +274,6 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
         for (int i = 11; i < 15; ++i) mbar_init(&bar[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
-    }
-    if (!KDA && control && lane == 0) {
-        tma_prefetch_desc(tmq);
-        tma_prefetch_desc(tmk);
     }
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
@@ -323,16 +315,9 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                     return;
                 }
                 uint8_t* stg = sm + s * L::STAGE;
-                mbar_arrive_expect_tx(&bar_full[s], L::TX);
-                if (!KDA) {
-#pragma unroll
-                    for (int a = 0; a < KA; ++a) {
-                        tma_load_3d(tmq, &bar_full[s], stg + L::Q_OFF + a * 8192, a * 64, c * C, bh);
-                        tma_load_3d(tmk, &bar_full[s], stg + L::K_OFF + a * 8192, a * 64, c * C, bh);
-                    }
-                }
+                mbar_arrive_expect_tx(&bar_full[s], S::BYTES);
                 const uint8_t* src = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES;
-                bulk_load(stg + L::SLOT_OFF, src, S::BYTES, &bar_full[s]);
+                bulk_load(stg, src, S::BYTES, &bar_full[s]);
                 pending[s] = true;
                 load_idx[s] = c;
             };
@@ -340,11 +325,11 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
             auto consumed = [&](int c) { mbar_arrive(&bar_cons[c & 1]); };
             // Commits issued so far per MMA barrier: the k-th completes phase k.
             int n_u = 0, n_c = 0, n_o = 0;
-            // X_0 W^T into COL_U (commit) and X_0 Q^T into the chunk's O1 buffer.
+            // X_0 W^T into COL_U (commit) and X_0 QG^T into the chunk's output buffer.
             auto issue_state_mmas = [&](int i) {
                 const int s = i & 1;
                 const uint32_t stg = sbase + s * L::STAGE;
-                const uint32_t aW = stg + L::SLOT_OFF + S::W_OFF;
+                const uint32_t aW = stg + S::W_OFF;
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint64_t sa = kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32);
@@ -356,7 +341,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint64_t sa = kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32);
                     mma_bf16_ss(tmem + L::COL_O + 128 * s, sa,
-                                kmaj(stg + L::Q_OFF + (kk / 4) * 8192 + (kk % 4) * 32), ID_O, kk > 0);
+                                kmaj(stg + S::QG_OFF + (kk / 4) * 8192 + (kk % 4) * 32), ID_O, kk > 0);
                 }
             };
             auto wait = [&](uint64_t* b, uint32_t parity, int bit) {
@@ -380,18 +365,17 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                 if (it >= 1) wait(bar_ep, (it - 1) & 1, kStatusMmaWait);
                 if (fail) break;
                 tc_fence_after();
-                // dX = U^T K' (commit), O2 = U^T P^T (commit); K' is the raw k
-                // tile (gdn, its token factors sit on U^T) or K o Gam_C / Gam (KDA)
+                // dX = U^T K' (commit), then U^T P^T onto X_0 QG^T (commit)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + L::COL_S, kmaj(aUS2 + kk * 32), mnmaj(stg + L::K_OFF + kk * 2048, 8192), ID_S,
+                    mma_bf16_ss(tmem + L::COL_S, kmaj(aUS + kk * 32), mnmaj(stg + S::KP_OFF + kk * 2048, 8192), ID_S,
                                 kk > 0);
                 mma_commit(bar_c);
                 ++n_c;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + L::COL_O + 128 * s + 64, kmaj(aUS + kk * 32),
-                                kmaj(stg + L::SLOT_OFF + S::P_OFF + kk * 32), ID_O, kk > 0);
+                    mma_bf16_ss(tmem + L::COL_O + 128 * s, kmaj(aUS + kk * 32), kmaj(stg + S::P_OFF + kk * 32), ID_O,
+                                true);
                 mma_commit(bar_o);
                 ++n_o;
                 if (it + 1 < n) {
@@ -475,7 +459,6 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
 #pragma unroll
             for (int i = 0; i < 32; ++i) z[i] = 0.f;
             store_row32_bf16(aUS, r, 4 * hh, z);
-            store_row32_bf16(aUS2, r, 4 * hh, z);
         }
         auto signal = [&](uint64_t* b) {   // this warp's writes / TMEM reads are done
             fence_proxy_async_smem();
@@ -491,9 +474,9 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
         for (; it < n; ++it) {
             const int s = it & 1;
             const int t0 = it * C;
-            const float* vec = reinterpret_cast<const float*>(sm + s * L::STAGE + L::SLOT_OFF + S::V_OFF);
+            const float* vec = reinterpret_cast<const float*>(sm + s * L::STAGE + S::V_OFF);
             float* sv = sVec + 128 * s;
-            // ---- U^T = Ut^T - X_0 W^T; bf16 copies U^T and U^T diag(gam_C/gam) ----
+            // ---- U^T = Ut^T - X_0 W^T, as the bf16 operand of both U products --------
             bool ok = !bad && mbar_wait_or_abort(&bar_full[s], (it >> 1) & 1, abort_flag) &&
                       mbar_wait_or_abort(bar_u, ph_u, abort_flag);
             ph_u ^= 1u;
@@ -501,7 +484,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
             if (ok) {
                 if (tid < 128) sv[tid] = vec[tid];
                 if (own) {
-                    const uint32_t aUt = sbase + s * L::STAGE + L::SLOT_OFF + S::U_OFF;
+                    const uint32_t aUt = sbase + s * L::STAGE + S::U_OFF;
                     float x[32];
                     tmem_ld32(tlane + L::COL_U + 32 * hh, x);
                     tmem_ld_wait();
@@ -521,11 +504,6 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                         y[7] = a3.y - y[7];
                     }
                     store_row32_bf16(aUS, r, 4 * hh, x);
-                    if (!KDA) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) x[i] *= vec[64 + 32 * hh + i];
-                        store_row32_bf16(aUS2, r, 4 * hh, x);
-                    }
                 }
             }
             fence_proxy_async_smem();
@@ -536,26 +514,24 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
                 break;
             }
             if (lane == 0) mbar_arrive(bar_us);
-            // ---- X = gam_C X_0 + dX (KDA: X_0 Diag(Gam_C) + dX), republished -----
+            // ---- X = X_0 Diag(Gam_C) + dX, republished as the bf16 operand ----------
             ok = mbar_wait_or_abort(bar_c, ph_c, abort_flag);
             ph_c ^= 1u;
             tc_fence_after();
             if (ok && own) {
-                const float gC = sv[63];
 #pragma unroll
                 for (int b = 0; b < DKH / 32; ++b) {
                     float x[32];
                     tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        st[32 * b + i] = (KDA ? sv[hh * DKH + 32 * b + i] : gC) * st[32 * b + i] + x[i];
+                    for (int i = 0; i < 32; ++i) st[32 * b + i] = sv[hh * DKH + 32 * b + i] * st[32 * b + i] + x[i];
                 }
                 publish_state();
             }
             signal(bar_x);
             bad |= !ok;
-            // ---- output: o_t = gam_t O1[t] + O2[t] (KDA: Gam_t is inside O1) -----
+            // ---- output: o_t = (X_0 QG^T + U^T P^T)[:, t] ------------------------------
             ok = mbar_wait_or_abort(bar_o, ph_o, abort_flag);
             ph_o ^= 1u;
             tc_fence_after();
@@ -568,12 +544,9 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmq, const CUtenso
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int tb = 32 * hh + 16 * q;   // first token of these 16 columns
-                    float o1[16], o2[16];
+                    float o1[16];
                     tmem_ld16(tlane + L::COL_O + 128 * s + tb, o1);
-                    tmem_ld16(tlane + L::COL_O + 128 * s + 64 + tb, o2);
                     tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) o1[i] = (KDA ? o1[i] : sv[tb + i] * o1[i]) + o2[i];
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
                         const float send = odd ? o1[2 * m] : o1[2 * m + 1];
@@ -700,11 +673,48 @@ __device__ __forceinline__ void invert_unit_lower(float* As, float* Rs, int warp
     }
 }
 
+// Store warp of a prep CTA (lane 0 of warp 8). For each unit of the CTA, in
+// order: waits until the converting warps have assembled its slot
+// (slot_full), waits until the chain has loaded the chunk R before it from
+// the same ring position, stores the slot, hands the buffer back
+// (slot_free) once the copy has read it, and raises the chunk's ready flag
+// once the copy has completed. Keeps every global hand-off off the
+// converting warps.
+template <uint32_t BYTES>
+__device__ __forceinline__ void store_loop(const Params& p, uint64_t* slot_full, uint64_t* slot_free,
+                                           const uint8_t* out, volatile int* abort_smem, int& status_bits) {
+    const int pid = blockIdx.x - p.n_chain, np = gridDim.x - p.n_chain, nunits = p.G * p.nch;
+    for (int k = 0;; ++k) {
+        const int u = pid + k * np;
+        if (u >= nunits) break;
+        if (!mbar_wait_or_abort(slot_full, k & 1, abort_smem)) {
+            if (!*abort_smem) status_bits |= kStatusFlagWait;   // else the converting warps recorded it
+            break;
+        }
+        const int g = u % p.G, c = u / p.G;
+        if (c >= p.R && !p.wait_flag(p.consumed(g), static_cast<unsigned long long>(c - p.R) + 1)) {
+            status_bits |= kStatusFlagWait;
+            *abort_smem = 1;
+            p.abort_all();
+            break;
+        }
+        uint8_t* dst = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * BYTES;
+        bulk_store(dst, smem_u32(out), BYTES);
+        bulk_commit();
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        mbar_arrive(slot_free);
+        bulk_wait_all();
+        fence_proxy_async_global();
+        st_release_u64(p.ready(g, c), p.epoch | (static_cast<unsigned long long>(c) + 1));
+    }
+    bulk_wait_all();
+}
+
 template <int DK, int DV>
 __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                           const Params& p, uint8_t* sm, uint32_t sbase) {
     using L = PrepLayout<DK, DV>;
-    using S = Slot<DK, DV, false>;
+    using S = Slot<DK, DV>;
     constexpr int KA = L::KA, VA = L::VA;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r = 32 * (warp & 3) + lane;
@@ -723,10 +733,15 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     uint64_t* bar_m = bar_full + 2;
     uint64_t* bar_test = bar_full + 3;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_full + 4);
+    uint64_t* slot_full = bar_full + 5;   // converting warps: the slot buffer is assembled
+    uint64_t* slot_free = bar_full + 6;   // store warp: the slot buffer was read by its store
+    volatile int* abort_smem = reinterpret_cast<volatile int*>(bar_full + 7);
     const uint32_t aTB1 = sbase + L::OFF_TB1, aTB2 = sbase + L::OFF_TB2;
 
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(&bar_full[i], 1);
+        for (int i = 5; i < 7; ++i) mbar_init(&bar_full[i], 1);
+        *abort_smem = 0;
         fence_mbar_init();
         tma_prefetch_desc(tmq);
         tma_prefetch_desc(tmk);
@@ -734,14 +749,26 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     }
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
-    sync_conv();
+    named_sync(kBarInit, kConv + 32);
     tc_fence_after();
+    if (warp == kConv / 32) {
+        int sbits = 0;
+        if (lane == 0 && !(p.flags & 0x100u))
+            store_loop<S::BYTES>(p, slot_full, slot_free, sm + L::OFF_OUT, abort_smem, sbits);
+        if (sbits) atomicOr(p.status, sbits);
+        return;
+    }
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
 
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
         const bool ok = mbar_wait(b, parity, kWaitLimitNs);
         tc_fence_after();
+        return !named_sync_or(kBarConv, kConv, !ok);
+    };
+    // the same, also giving up when the store warp has given up
+    auto wait_all_abort = [&](uint64_t* b, uint32_t parity) -> bool {
+        const bool ok = mbar_wait_or_abort(b, parity, abort_smem);
         return !named_sync_or(kBarConv, kConv, !ok);
     };
     auto publish = [&]() {
@@ -761,36 +788,6 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     // unit u -> (head g = u % G, chunk u / G): the units go chunk by chunk
     auto unit_g = [&](int u) { return u % p.G; };
     auto unit_i = [&](int u) { return u / p.G; };
-    // Slot hand-off (thread 0). The slot of unit u goes to ring position
-    // chunk % R of its head once the chain has loaded the chunk R before it;
-    // its ready flag is raised when the store has completed, which thread 0
-    // checks early in its next unit (or after the last one).
-    int st_g = -1, st_c = 0;   // the stored slot whose flag is still down
-    auto release_stored = [&]() {
-        if (tid == 0 && st_g >= 0) {
-            bulk_wait_all();
-            fence_proxy_async_global();
-            st_release_u64(p.ready(st_g, st_c), p.epoch | (static_cast<unsigned long long>(st_c) + 1));
-            st_g = -1;
-        }
-    };
-    auto store_slot = [&](int u, uint32_t src) -> bool {
-        bool ok = true;
-        if (tid == 0) {
-            const int g = unit_g(u), c = unit_i(u);
-            if (c >= p.R) ok = p.wait_flag(p.consumed(g), static_cast<unsigned long long>(c - p.R) + 1);
-            if (ok) {
-                uint8_t* dst = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES;
-                bulk_store(dst, src, S::BYTES);
-                bulk_commit();
-                st_g = g;
-                st_c = c;
-            } else {
-                p.abort_all();
-            }
-        }
-        return !named_sync_or(kBarConv, kConv, !ok);
-    };
     bool pending[2] = {false, false};
     auto issue_load = [&](int u, int s) {
         const int bh = p.h0 + unit_g(u);
@@ -834,9 +831,8 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         const int s = k & 1;
         const int un = u + np;
         const uint32_t stg = sbase + s * L::STAGE;
-        const uint32_t aOut = sbase + L::OFF_OUT + s * L::OUT_STRIDE;
-        float* oGam = reinterpret_cast<float*>(sm + L::OFF_OUT + s * L::OUT_STRIDE + S::V_OFF);   // gam_t
-        float* oKf = oGam + 64;                                                                // gam_C / gam_t
+        const uint32_t aOut = sbase + L::OFF_OUT;
+        float* oVec = reinterpret_cast<float*>(sm + L::OFF_OUT + S::V_OFF);   // gam_C per channel
         if (tid == 0 && un < nunits) {
             fence_proxy_async_smem();
             issue_load(un, s ^ 1);   // stage s^1's MMAs finished with the previous unit
@@ -865,16 +861,30 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
             }
             mma_commit(bar_m);
         }
-        release_stored();   // the previous unit's slot (also frees its buffer)
         sync_conv();
         if (tid >= 32 && tid < 64) sG2[tid] += sG2[31];
-        sync_conv();
-        if (tid < 64) {
-            const float G = sG2[tid];
-            const float gam = ex2(G);
-            sBG[tid] = sB[tid] * gam;
-            oGam[tid] = gam;
-            oKf[tid] = ex2(sG2[63] - G);
+        // the slot buffer is written from here on: the previous unit's store has read it
+        if (k >= 1) {
+            if (!wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
+        } else {
+            sync_conv();
+        }
+        if (tid < 64) sBG[tid] = sB[tid] * ex2(sG2[tid]);
+        if (tid < DK) oVec[tid] = ex2(sG2[63]);
+        // ---- the chain's operands Q o Gam = diag(gam) Q and K o Gam_C/Gam =
+        //      diag(gam_C/gam) K: thread (t, part) scales DK/4 channels of row t
+        {
+            const int t = tid >> 2, part = tid & 3;
+            const float fq = ex2(sG2[t]), fk = ex2(sG2[63] - sG2[t]);
+#pragma unroll
+            for (int i = 0; i < DK / 32; ++i) {
+                const int cidx = part * (DK / 32) + i;   // 16-byte chunk of the row
+                const int a = cidx / 8, c8 = cidx % 8;
+                const uint32_t ro = sw128_off(t, c8);
+                st_shared_v4_u4(aOut + S::KP_OFF + a * 8192 + ro, scale_bf16x8(ld_shared_v4(stg + a * 16384 + ro), fk));
+                st_shared_v4_u4(aOut + S::QG_OFF + a * 8192 + ro,
+                                scale_bf16x8(ld_shared_v4(stg + a * 16384 + sw128_off(64 + t, c8)), fq));
+            }
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;
@@ -958,16 +968,17 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         fence_proxy_async_smem();
         tc_fence_before();
         sync_conv();
-        if (!store_slot(u, aOut)) { status_bits |= kStatusFlagWait; failed = true; break; }
+        if (tid == 0) mbar_arrive(&slot_full[0]);   // to the store warp
     }
 
     if (failed && tid == 0) {
         for (int s2 = 0; s2 < 2; ++s2)
             if (pending[s2]) mbar_wait(&bar_full[s2], ((s2 == (k & 1) ? k : k + 1) >> 1) & 1, 100000000ull);
     }
-    if (!failed) release_stored();
-    if (tid == 0) bulk_wait_all();
-    if (failed && tid == 0) p.abort_all();
+    if (failed && tid == 0) {
+        *abort_smem = 1;
+        p.abort_all();
+    }
     tc_fence_before();
     sync_conv();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
@@ -993,7 +1004,7 @@ template <int DK, int DV>
 __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                               const Params& p, uint8_t* sm, uint32_t sbase) {
     using L = PrepLayoutKda<DK, DV>;
-    using S = Slot<DK, DV, true>;
+    using S = Slot<DK, DV>;
     constexpr int KA = L::KA, VA = L::VA;
     constexpr int NCP = DK / 2;          // channel pairs
     constexpr int NSEG = kConv / NCP;    // token segments of the element pass
@@ -1029,10 +1040,16 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     uint64_t* bar_m = bar + 4;    // MMAs
     uint64_t* bar_test = bar + 5;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 6);
+    uint64_t* slot_full = bar + 7;   // converting warps: the slot buffer is assembled
+    uint64_t* slot_free = bar + 8;   // store warp: the slot buffer was read by its store
+    volatile int* abort_smem = reinterpret_cast<volatile int*>(bar + 9);
     const uint32_t aTB1 = sbase + L::OFF_TB1, aOut = sbase + L::OFF_OUT, aV = sbase + L::OFF_V;
 
     if (tid == 0) {
         for (int i = 0; i < 6; ++i) mbar_init(&bar[i], 1);
+        mbar_init(slot_full, 1);
+        mbar_init(slot_free, 1);
+        *abort_smem = 0;
         fence_mbar_init();
         tma_prefetch_desc(tmq);
         tma_prefetch_desc(tmk);
@@ -1040,14 +1057,26 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     }
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
-    sync_conv();
+    named_sync(kBarInit, kConv + 32);
     tc_fence_after();
+    if (warp == kConv / 32) {
+        int sbits = 0;
+        if (lane == 0 && !(p.flags & 0x100u))
+            store_loop<S::BYTES>(p, slot_full, slot_free, sm + L::OFF_OUT, abort_smem, sbits);
+        if (sbits) atomicOr(p.status, sbits);
+        return;
+    }
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
 
     auto wait_all = [&](uint64_t* b, uint32_t parity) -> bool {
         const bool ok = mbar_wait(b, parity, kWaitLimitNs);
         tc_fence_after();
+        return !named_sync_or(kBarConv, kConv, !ok);
+    };
+    // the same, also giving up when the store warp has given up
+    auto wait_all_abort = [&](uint64_t* b, uint32_t parity) -> bool {
+        const bool ok = mbar_wait_or_abort(b, parity, abort_smem);
         return !named_sync_or(kBarConv, kConv, !ok);
     };
     auto publish = [&]() {
@@ -1066,36 +1095,6 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
 
     auto unit_g = [&](int u) { return u % p.G; };   // as in the scalar-gate role
     auto unit_i = [&](int u) { return u / p.G; };
-    // Slot hand-off (thread 0). The slot of unit u goes to ring position
-    // chunk % R of its head once the chain has loaded the chunk R before it;
-    // its ready flag is raised when the store has completed, which thread 0
-    // checks early in its next unit (or after the last one).
-    int st_g = -1, st_c = 0;   // the stored slot whose flag is still down
-    auto release_stored = [&]() {
-        if (tid == 0 && st_g >= 0) {
-            bulk_wait_all();
-            fence_proxy_async_global();
-            st_release_u64(p.ready(st_g, st_c), p.epoch | (static_cast<unsigned long long>(st_c) + 1));
-            st_g = -1;
-        }
-    };
-    auto store_slot = [&](int u, uint32_t src) -> bool {
-        bool ok = true;
-        if (tid == 0) {
-            const int g = unit_g(u), c = unit_i(u);
-            if (c >= p.R) ok = p.wait_flag(p.consumed(g), static_cast<unsigned long long>(c - p.R) + 1);
-            if (ok) {
-                uint8_t* dst = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES;
-                bulk_store(dst, src, S::BYTES);
-                bulk_commit();
-                st_g = g;
-                st_c = c;
-            } else {
-                p.abort_all();
-            }
-        }
-        return !named_sync_or(kBarConv, kConv, !ok);
-    };
     // Copies in flight (thread 0): the k/q stages, and the single V and gate
     // buffers (one load at a time each, the n-th completing phase n).
     bool pend_qk[2] = {false, false};
@@ -1184,10 +1183,9 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         }
         if (tid < 64) sB[tid] = b_nx;
         load_b(un, b_nx);
-        // the slot buffer is written below: the previous unit's store completes
-        // here and its flag goes up
-        release_stored();
         sync_conv();
+        // the slot buffer is written below: the previous unit's store has read it
+        if (k >= 1 && !wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
         // ---- cumulative log2 at the block ends: segment offset, the sub-chunk
         //      references r_a (end of block 2a), G_C ---------------------------------
         float off0 = 0.f, off1 = 0.f, rr0[4], rr1[4], GC0, GC1;
@@ -1367,7 +1365,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         fence_proxy_async_smem();
         tc_fence_before();
         sync_conv();
-        if (!store_slot(u, aOut)) { status_bits |= kStatusFlagWait; failed = true; break; }
+        if (tid == 0) mbar_arrive(&slot_full[0]);   // to the store warp
     }
 
     if (failed && tid == 0) {
@@ -1376,9 +1374,10 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         if (v_issued > v_done) mbar_wait(bar_v, (v_issued - 1) & 1, 100000000ull);
         if (g_issued > g_done) mbar_wait(bar_g, (g_issued - 1) & 1, 100000000ull);
     }
-    if (!failed) release_stored();
-    if (tid == 0) bulk_wait_all();
-    if (failed && tid == 0) p.abort_all();
+    if (failed && tid == 0) {
+        *abort_smem = 1;
+        p.abort_all();
+    }
     tc_fence_before();
     sync_conv();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
@@ -1394,9 +1393,9 @@ gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (sbase - raw);
     if (static_cast<int>(blockIdx.x) < p.n_chain) {
-        chain_role<DK, DV, KDA>(&tmq, &tmk, p, sm, sbase);
+        chain_role<DK, DV>(p, sm, sbase);
     } else {
-        if (threadIdx.x >= kConv) return;   // the prep role runs on eight warps
+        if (threadIdx.x >= kConv + 32) return;   // the prep role: eight converting warps and a store warp
         if constexpr (KDA)
             prep_role_kda<DK, DV>(&tmq, &tmk, &tmv, p, sm, sbase);
         else
@@ -1455,20 +1454,16 @@ cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int R, cudaStream
 
 namespace chunk {
 
-size_t gdn_slot_bytes(int dk, int dv, bool kda) {
-    return static_cast<size_t>(dk + dv) * 128 + 8192 + (kda ? static_cast<size_t>(dk) * 256 : 0) + 512;
-}
+size_t gdn_slot_bytes(int dk, int dv) { return static_cast<size_t>(3 * dk + dv) * 128 + 8192 + 512; }
 
 int gdn_group(int BH) { return BH < kGdnMaxGroup ? BH : kGdnMaxGroup; }
 
 // Flag words, then a ring of R chunks per sequence-head of a group of G.
-static size_t ring_bytes(int G, int R, int dk, int dv, bool kda) {
-    return gdn::align_up(gdn::flag_words(G, R) * 8, 1024) + static_cast<size_t>(G) * R * gdn_slot_bytes(dk, dv, kda);
+static size_t ring_bytes(int G, int R, int dk, int dv) {
+    return gdn::align_up(gdn::flag_words(G, R) * 8, 1024) + static_cast<size_t>(G) * R * gdn_slot_bytes(dk, dv);
 }
 
-size_t gdn_workspace_bytes(int BH, int dk, int dv, int W, bool kda) {
-    return ring_bytes(gdn_group(BH), 2 * W, dk, dv, kda);
-}
+size_t gdn_workspace_bytes(int BH, int dk, int dv, int W) { return ring_bytes(gdn_group(BH), 2 * W, dk, dv); }
 
 cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     const int G = gdn_group(a.BH);
@@ -1478,8 +1473,8 @@ cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     // sequence) that the workspace holds
     int R = 2 * kGdnWindow;
     if (R > nch) R = nch < 2 ? 2 : nch;
-    while (R > 2 && ring_bytes(G, R, a.dk, a.dv, kda) > a.ws_bytes) --R;
-    if (!a.workspace || ring_bytes(G, R, a.dk, a.dv, kda) > a.ws_bytes) return cudaErrorInvalidValue;
+    while (R > 2 && ring_bytes(G, R, a.dk, a.dv) > a.ws_bytes) --R;
+    if (!a.workspace || ring_bytes(G, R, a.dk, a.dv) > a.ws_bytes) return cudaErrorInvalidValue;
     if (kda) {
         if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, true>(m, a, G, R, s);
         if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, true>(m, a, G, R, s);
