@@ -150,8 +150,9 @@ constexpr int kRStride = 40;   // fp32 row stride of the merge scratch (conflict
 // are single-buffered (V and the gates of the next unit are loaded once the
 // MMAs that read their buffer are done; the slot store of the previous unit
 // has drained before the buffer is written again). The column operands of
-// the four sub-chunks (16, 32, 48, 64 rows) are written over the gate tile
-// and TB1, both of which are dead while they live.
+// the four sub-chunks (16, 32, 48, 64 rows) are stacked into one 160-row
+// operand, written over the gate tile and TB1, both of which are dead while
+// it lives.
 template <int DK, int DV>
 struct PrepLayoutKda {
     static constexpr int KA = DK / 64;
@@ -162,7 +163,8 @@ struct PrepLayoutKda {
     static constexpr uint32_t OFF_GATE = OFF_V + VA * 8192;   // alpha fp32 [64 t][DK]
     static constexpr uint32_t OFF_TB1 = OFF_GATE + DK * 256;  // T diag(beta) bf16 [t][j]
     static constexpr uint32_t OFF_B = OFF_GATE;               // column operands, over gate + TB1
-    static constexpr uint32_t B_BYTES = 160 * 128 * KA;
+    static constexpr uint32_t B_ATOM = 160 * 128;             // 160 rows of one 64-channel atom
+    static constexpr uint32_t B_BYTES = B_ATOM * KA;
     static_assert(B_BYTES <= DK * 256 + 8192, "column operands fit over the gate tile and TB1");
     static constexpr uint32_t OFF_OUT = align1024(OFF_TB1 + 8192);
     static constexpr uint32_t OFF_AS = OFF_OUT + align1024(S::BYTES);   // fp32 [64][kAStride]
@@ -172,9 +174,10 @@ struct PrepLayoutKda {
     static constexpr uint32_t OFF_MISC = OFF_PR + 4 * DK * 4;            // beta [64]
     static constexpr uint32_t OFF_BAR = OFF_MISC + 64 * 4;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
-    // Column operand of sub-chunk a: rows j < 16(a+1), KA atoms of 2048(a+1) bytes.
-    static __host__ __device__ constexpr uint32_t b_off(int a) { return OFF_B + 1024u * KA * a * (a + 1); }
-    static constexpr uint32_t COL_G = 0;     // [K;Q] B_a^T, four blocks of 64 columns
+    // First row (and product column) of sub-chunk a's column operand: its
+    // rows j < 16(a+1) follow the operands of the sub-chunks before it.
+    static __host__ __device__ constexpr int b_row(int a) { return 8 * a * (a + 1); }
+    static constexpr uint32_t COL_G = 0;     // [K;Q] B^T, 160 columns (block a at b_row(a))
     static constexpr uint32_t COL_W = 0;     // W^T per sub-chunk (four blocks; the products above are read by then)
     static constexpr uint32_t COL_UT = 256;  // Ut^T [dv][64]
     static constexpr uint32_t TMEM_COLS = 512;
@@ -1186,9 +1189,11 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         sync_conv();
         // the slot buffer is written below: the previous unit's store has read it
         if (k >= 1 && !wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
-        // ---- cumulative log2 at the block ends: segment offset, the sub-chunk
-        //      references r_a (end of block 2a), G_C ---------------------------------
+        // ---- cumulative log2 at the 8-token block ends Bc[b]: the segment offset,
+        //      the sub-chunk references r_a = Bc[2a] (its 8th token), its start
+        //      S_a = Bc[2a-1] and end E_a = Bc[2a+1], G_C = Bc[7] ----------------------
         float off0 = 0.f, off1 = 0.f, rr0[4], rr1[4], GC0, GC1;
+        float Sa0 = 0.f, Sa1 = 0.f, Ea0 = 0.f, Ea1 = 0.f;
         {
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -1198,6 +1203,8 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 s1 += x.y;
                 if (b + 1 == blk0) { off0 = s0; off1 = s1; }
                 if ((b & 1) == 0) { rr0[b / 2] = s0; rr1[b / 2] = s1; }
+                if (b + 1 == 2 * sa) { Sa0 = s0; Sa1 = s1; }
+                if (b == 2 * sa + 1) { Ea0 = s0; Ea1 = s1; }
             }
             GC0 = s0;
             GC1 = s1;
@@ -1206,6 +1213,23 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
 #pragma unroll
         for (int a = 1; a < 4; ++a)
             if (a == sa) { ra0 = rr0[a]; ra1 = rr1[a]; }
+        // Per-channel factors, every exponent <= 0: Q o Gam = q h 2^S_a and
+        // K o Gam_C/Gam = k f 2^(G_C - E_a), columns of a later sub-chunk b
+        // k f 2^(r_b - E_a), with h = 2^(G - S_a) and f = 2^(E_a - G) per
+        // element. Up to the reference token h is taken directly and f as
+        // 2^(r_a - G) 2^(E_a - r_a); after it f directly and h as
+        // 2^(G - r_a) 2^(r_a - S_a): each product joins two factors <= 1, so
+        // an underflow only hides values that are themselves negligible.
+        const float cS0 = ex2(Sa0), cS1 = ex2(Sa1);
+        const float cK0 = ex2(GC0 - Ea0), cK1 = ex2(GC1 - Ea1);
+        const float cF0 = ex2(Ea0 - ra0), cF1 = ex2(Ea1 - ra1);
+        const float cH0 = ex2(ra0 - Sa0), cH1 = ex2(ra1 - Sa1);
+        float cB0[4], cB1[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            cB0[b] = b > sa ? ex2(rr0[b] - Ea0) : 0.f;
+            cB1[b] = b > sa ? ex2(rr1[b] - Ea1) : 0.f;
+        }
         if (seg == 0) {
             *reinterpret_cast<float2*>(outp + S::V_OFF + c0 * 4) = make_float2(ex2(GC0), ex2(GC1));
 #pragma unroll
@@ -1220,6 +1244,8 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         //      Q o Gam and K o Gam_C/Gam into the slot ------------------------------
         {
             const uint32_t aKQ = stg + ka * 16384;
+            const uint32_t aB = sbase + L::OFF_B + ka * L::B_ATOM;
+            const int ref = 16 * sa + 7;
 #pragma unroll
             for (int i = 0; i < SL; ++i) {
                 const int t = seg * SL + i;
@@ -1231,30 +1257,40 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 const float G0 = off0 + lp0[i], G1 = off1 + lp1[i];
                 const float e10 = ex2c(G0 - ra0), e11 = ex2c(G1 - ra1);
                 const float e20 = ex2c(ra0 - G0), e21 = ex2c(ra1 - G1);
+                float h0, h1, f0, f1;
+                if (t <= ref) {
+                    h0 = ex2(G0 - Sa0);
+                    h1 = ex2(G1 - Sa1);
+                    f0 = e20 * cF0;
+                    f1 = e21 * cF1;
+                } else {
+                    f0 = ex2(Ea0 - G0);
+                    f1 = ex2(Ea1 - G1);
+                    h0 = e10 * cH0;
+                    h1 = e11 * cH1;
+                }
                 st_shared_b32(ak, pack_bf16(kv.x * e10, kv.y * e11));
                 st_shared_b32(aq, pack_bf16(qv.x * e10, qv.y * e11));
-                st_shared_b32(aOut + S::QG_OFF + ka * 8192 + ro, pack_bf16(qv.x * ex2(G0), qv.y * ex2(G1)));
-                st_shared_b32(aOut + S::KP_OFF + ka * 8192 + ro,
-                              pack_bf16(kv.x * ex2(GC0 - G0), kv.y * ex2(GC1 - G1)));
+                st_shared_b32(aOut + S::QG_OFF + ka * 8192 + ro, pack_bf16(qv.x * h0 * cS0, qv.y * h1 * cS1));
+                const float kf0 = kv.x * f0, kf1 = kv.y * f1;
+                st_shared_b32(aOut + S::KP_OFF + ka * 8192 + ro, pack_bf16(kf0 * cK0, kf1 * cK1));
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
-                    const uint32_t ab = sbase + L::b_off(b) + ka * 2048 * (b + 1) + ro;
+                    const uint32_t ab = aB + sw128_off(L::b_row(b) + t, ch) + bo;
                     if (b == sa) st_shared_b32(ab, pack_bf16(kv.x * e20, kv.y * e21));
-                    if (b > sa) st_shared_b32(ab, pack_bf16(kv.x * ex2(rr0[b] - G0), kv.y * ex2(rr1[b] - G1)));
+                    if (b > sa) st_shared_b32(ab, pack_bf16(kf0 * cB0[b], kf1 * cB1[b]));
                 }
             }
         }
         publish();
-        // ---- [K;Q] B_a^T on the tensor cores, one product per sub-chunk a ------------
+        // ---- [K;Q] B^T on the tensor cores: the four column operands stacked
+        //      into one N = 160 product ------------------------------------------------
         if (tid == 0) {
+            constexpr uint32_t idg = idesc_bf16(128, 160, false, false);
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const uint32_t idg = idesc_bf16(128, 16 * (a + 1), false, false);
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk)
-                    mma_bf16_ss(tmem + L::COL_G + 64 * a, kmaj(stg + (kk / 4) * 16384 + (kk % 4) * 32),
-                                kmaj(sbase + L::b_off(a) + (kk / 4) * 2048 * (a + 1) + (kk % 4) * 32), idg, kk > 0);
-            }
+            for (int kk = 0; kk < DK / 16; ++kk)
+                mma_bf16_ss(tmem + L::COL_G, kmaj(stg + (kk / 4) * 16384 + (kk % 4) * 32),
+                            kmaj(sbase + L::OFF_B + (kk / 4) * L::B_ATOM + (kk % 4) * 32), idg, kk > 0);
             mma_commit(bar_m);
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
@@ -1271,8 +1307,8 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
             float x[32];
             {
                 float y[32];
-                tmem_ld32(tlane + L::COL_G + 64 * a0 + 32 * hh, x);
-                tmem_ld32(tlane + L::COL_G + 64 * (a0 + 1) + 32 * hh, y);
+                tmem_ld32(tlane + L::COL_G + L::b_row(a0) + 32 * hh, x);
+                tmem_ld32(tlane + L::COL_G + L::b_row(a0 + 1) + 32 * hh, y);
                 tmem_ld_wait();
                 const bool hi = lane >= 16;
 #pragma unroll
