@@ -110,7 +110,8 @@ struct ChainLayout {
     static constexpr uint32_t STAGE = align1024(S::BYTES);      // one slot per stage
     static constexpr uint32_t OFF_SS = 2 * STAGE;               // X_0 bf16 [128 rows][DK]
     static constexpr uint32_t OFF_US = OFF_SS + KA * 16384;     // U^T bf16 [128 rows][64 j]
-    static constexpr uint32_t OFF_VEC = OFF_US + 16384;         // the slot vector per stage
+    static constexpr uint32_t OFF_OT = OFF_US + 16384;          // output tile bf16 [64 t][DV] for the TMA store
+    static constexpr uint32_t OFF_VEC = OFF_OT + DV * 128;      // the slot vector per stage
     static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 512;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
     // TMEM columns (lanes = value rows)
@@ -231,15 +232,20 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 u, float f) {
     return make_uint4(pack_bf16(a.x * f, a.y * f), pack_bf16(b.x * f, b.y * f), pack_bf16(c.x * f, c.y * f),
                       pack_bf16(d.x * f, d.y * f));
 }
-__device__ __forceinline__ void st_global_b32(void* p, uint32_t v) {
-    asm volatile("st.global.b32 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(v) : "memory");
+__device__ __forceinline__ uint32_t ld_shared_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // ============================================================================
 // chain CTA: the state-dependent part of every chunk of one window
 // ============================================================================
 template <int DK, int DV>
-__device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_t sbase) {
+__device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params& p, uint8_t* sm, uint32_t sbase) {
     using L = ChainLayout<DK, DV>;
     using S = Slot<DK, DV>;
     constexpr int DKH = DK / 2;
@@ -251,7 +257,6 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
     const int g = blockIdx.x;
     const int bh = p.h0 + g;
     const int n = p.nch;
-    const int T = p.T;
     const bool own = warp < kConv / 32 && r < DV;
 
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
@@ -265,8 +270,8 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
     uint64_t* bar_test = bar + 8;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 10);
-    uint64_t* bar_rdy = bar + 11;    // [2] flag warp: the chunk's slot is in the ring
-    uint64_t* bar_cons = bar + 13;   // [2] control: the chunk's slot has been loaded
+    uint64_t* bar_sfree = bar + 11;  // [2] control: every MMA reading the stage is done
+    uint64_t* bar_ofree = bar + 15;  // copy warp: the output tile's store has read it
     const uint32_t aSS = sbase + L::OFF_SS, aUS = sbase + L::OFF_US;
     float* sVec = reinterpret_cast<float*>(sm + L::OFF_VEC);
 
@@ -274,10 +279,12 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
         for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
         for (int i = 5; i < 8; ++i) mbar_init(&bar[i], kConv / 32);
         mbar_init(bar_test, 1);
-        for (int i = 11; i < 15; ++i) mbar_init(&bar[i], 1);
+        for (int i = 11; i < 13; ++i) mbar_init(&bar[i], 1);
+        mbar_init(bar_ofree, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
+    if (flagw && lane == 0) tma_prefetch_desc(tmo);
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -299,9 +306,9 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
 
     if (control) {
         // ======================= control warp (lane 0) =========================
+        // Issues every MMA. Copies belong to the copy warp; the control thread
+        // tells it when a stage's last reader is done (bar_sfree).
         if (lane == 0 && !failed && n > 0) {
-            bool pending[2] = {false, false};
-            int load_idx[2] = {0, 0};   // chunk of the load last issued on each stage
             bool fail = false;
             auto give_up = [&](int bit) {
                 fail = true;
@@ -309,23 +316,6 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
                 *abort_flag = 1;
                 p.abort_all();
             };
-            // Load chunk c into stage s once the flag warp has seen its slot
-            // stored (stage s = c & 1, the (c >> 1)-th hand-off on bar_rdy[s]).
-            auto issue_load = [&](int c, int s) {
-                if (fail) return;
-                if (!mbar_wait_or_abort(&bar_rdy[s], (c >> 1) & 1, abort_flag)) {
-                    give_up(kStatusFlagWait);
-                    return;
-                }
-                uint8_t* stg = sm + s * L::STAGE;
-                mbar_arrive_expect_tx(&bar_full[s], S::BYTES);
-                const uint8_t* src = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES;
-                bulk_load(stg, src, S::BYTES, &bar_full[s]);
-                pending[s] = true;
-                load_idx[s] = c;
-            };
-            // The slot of chunk c has arrived: the flag warp tells the prep CTAs.
-            auto consumed = [&](int c) { mbar_arrive(&bar_cons[c & 1]); };
             // Commits issued so far per MMA barrier: the k-th completes phase k.
             int n_u = 0, n_c = 0, n_o = 0;
             // X_0 W^T into COL_U (commit) and X_0 QG^T into the chunk's output buffer.
@@ -351,13 +341,9 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
                 if (fail) return;
                 if (!mbar_wait_or_abort(b, parity, abort_flag)) give_up(bit);
             };
-            issue_load(0, 0);
-            if (n > 1) issue_load(1, 1);
             wait(bar_x, 0, kStatusMmaWait);
             wait(&bar_full[0], 0, kStatusTmaWait);
             if (!fail) {
-                pending[0] = false;
-                consumed(0);
                 tc_fence_after();
                 issue_state_mmas(0);
             }
@@ -383,54 +369,97 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
                 ++n_o;
                 if (it + 1 < n) {
                     wait(&bar_full[s ^ 1], ((it + 1) >> 1) & 1, kStatusTmaWait);
-                    if (!fail) {
-                        pending[s ^ 1] = false;
-                        consumed(it + 1);
-                    }
                     wait(bar_x, (it + 1) & 1, kStatusMmaWait);
                     if (fail) break;
                     tc_fence_after();
                     issue_state_mmas(it + 1);
                 }
                 if (it + 2 < n) {
-                    wait(bar_o, it & 1, kStatusMmaWait);   // every reader of stage s is done
+                    wait(bar_o, it & 1, kStatusMmaWait);   // every MMA reading stage s is done
                     if (fail) break;
-                    issue_load(it + 2, s);
-                    if (fail) break;
+                    mbar_arrive(&bar_sfree[s]);             // the copy warp may refill it
                 }
             }
             if (fail) {
-                // Let copies and MMAs in flight finish before the CTA exits
-                // (bounded: 100 ms each). MMAs complete in issue order, so the
-                // newest commit of each barrier covers the ones before it.
-                for (int s2 = 0; s2 < 2; ++s2)
-                    if (pending[s2]) mbar_wait(&bar_full[s2], (load_idx[s2] >> 1) & 1, 100000000ull);
+                // Let MMAs in flight finish before the CTA exits (bounded: 100 ms
+                // each). MMAs complete in issue order, so the newest commit of
+                // each barrier covers the ones before it.
                 if (n_u > 0) mbar_wait(bar_u, (n_u - 1) & 1, 100000000ull);
                 if (n_c > 0) mbar_wait(bar_c, (n_c - 1) & 1, 100000000ull);
                 if (n_o > 0) mbar_wait(bar_o, (n_o - 1) & 1, 100000000ull);
             }
         }
     } else if (flagw) {
-        // ======================= flag warp (lane 0) ============================
-        // Keeps the global hand-off off the control thread: waits for each
-        // chunk's ready flag (then hands the chunk to the control thread), and
-        // publishes the consumed count once the control thread has loaded a
-        // slot. Hand-off c on bar_rdy[c & 1] only follows the consumption of
-        // chunk c - 2, so neither barrier runs more than one phase ahead.
-        if (lane == 0 && !failed) {
-            for (int c = 0; c < n; ++c) {
+        // ======================= copy warp (lane 0) ============================
+        // Keeps copies and global hand-offs off the control thread. For chunk
+        // c, in order: once the ring holds the chunk (its ready flag) and
+        // stage c & 1 is free (bar_sfree, relayed by the control thread after
+        // the last MMA reading it), loads the slot; hands the output tile back
+        // (bar_ofree) once chunk c - 2's store has read it; then, for chunk
+        // c - 1, waits for its slot to arrive and publishes the consumed count,
+        // waits for its output tile (bar_ep) and stores it. Each barrier waited on here can only
+        // advance one more phase after a step this warp takes later, so no
+        // parity wait is ever two phases behind.
+        if (lane == 0 && !failed && n > 0) {
+            bool fail = false;
+            bool pending[2] = {false, false};
+            int load_idx[2] = {0, 0};   // chunk of the load last issued on each stage
+            auto give_up = [&](int bit) {
+                fail = true;
+                status_bits |= bit;
+                *abort_flag = 1;
+                p.abort_all();
+            };
+            auto wait = [&](uint64_t* b, uint32_t parity, int bit) {
+                if (fail) return;
+                if (!mbar_wait_or_abort(b, parity, abort_flag)) give_up(bit);
+            };
+            for (int c = 0; c <= n && !fail; ++c) {
+                if (c < n) {
+                    // the ready flag first: it is usually up long before the
+                    // stage frees, so its load latency hides behind that wait
+                    const int s = c & 1;
+                    if (!p.wait_flag(p.ready(g, c), static_cast<unsigned long long>(c) + 1)) {
+                        give_up(kStatusFlagWait);
+                        break;
+                    }
+                    if (c >= 2) wait(&bar_sfree[s], ((c - 2) >> 1) & 1, kStatusMmaWait);
+                    if (fail) break;
+                    fence_proxy_async_global();
+                    mbar_arrive_expect_tx(&bar_full[s], S::BYTES);
+                    bulk_load(sm + s * L::STAGE, p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES,
+                              S::BYTES, &bar_full[s]);
+                    pending[s] = true;
+                    load_idx[s] = c;
+                }
+                // chunk c - 2's output store (the only one in flight) has long
+                // read its tile: hand it back for chunk c - 1's epilogue
                 if (c >= 2) {
-                    if (!mbar_wait_or_abort(&bar_cons[c & 1], ((c - 2) >> 1) & 1, abort_flag)) break;
-                    st_release_u64(p.consumed(g), p.epoch | static_cast<unsigned long long>(c - 1));
+                    bulk_wait_read_all();
+                    mbar_arrive(bar_ofree);
                 }
-                if (!p.wait_flag(p.ready(g, c), static_cast<unsigned long long>(c) + 1)) {
-                    status_bits |= kStatusFlagWait;
-                    *abort_flag = 1;
-                    p.abort_all();
-                    break;
+                if (c >= 1) {
+                    const int c1 = c - 1, s1 = c1 & 1;
+                    wait(&bar_full[s1], (c1 >> 1) & 1, kStatusTmaWait);
+                    if (fail) break;
+                    pending[s1] = false;
+                    // Chunks 0..c-1 are in shared memory. The wait above
+                    // (acquire) orders this store after the completed copy, so
+                    // a relaxed store suffices: a release would also wait for
+                    // the copy just issued.
+                    st_relaxed_u64(p.consumed(g), p.epoch | static_cast<unsigned long long>(c));
+                    wait(bar_ep, c1 & 1, kStatusMmaWait);
+                    if (fail) break;
+                    // rows past T are clipped by the tensor map
+#pragma unroll
+                    for (int a = 0; a < DV / 64; ++a) tma_store_3d(tmo, sm + L::OFF_OT + a * 8192, a * 64, c1 * C, bh);
+                    bulk_commit();
                 }
-                fence_proxy_async_global();
-                mbar_arrive(&bar_rdy[c & 1]);
+            }
+            bulk_wait_all();   // every output store has completed
+            if (fail) {
+                for (int s2 = 0; s2 < 2; ++s2)
+                    if (pending[s2]) mbar_wait(&bar_full[s2], (load_idx[s2] >> 1) & 1, 100000000ull);
             }
         }
     } else {
@@ -476,7 +505,6 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
         int it = 0;
         for (; it < n; ++it) {
             const int s = it & 1;
-            const int t0 = it * C;
             const float* vec = reinterpret_cast<const float*>(sm + s * L::STAGE + S::V_OFF);
             float* sv = sVec + 128 * s;
             // ---- U^T = Ut^T - X_0 W^T, as the bf16 operand of both U products --------
@@ -535,15 +563,18 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
             signal(bar_x);
             bad |= !ok;
             // ---- output: o_t = (X_0 QG^T + U^T P^T)[:, t] ------------------------------
-            ok = mbar_wait_or_abort(bar_o, ph_o, abort_flag);
+            ok = mbar_wait_or_abort(bar_o, ph_o, abort_flag) &&
+                 (it == 0 || mbar_wait_or_abort(bar_ofree, (it - 1) & 1, abort_flag));
             ph_o ^= 1u;
             tc_fence_after();
             if (ok && own) {
                 // Lane pairs (r even, r + 1) exchange values so that each
-                // stores two adjacent columns of one token row in one word.
+                // writes two adjacent columns of one token row of the output
+                // tile in one word; the control warp stores the tile.
                 const bool odd = lane & 1;
                 const int col = r & ~1;
-                __nv_bfloat16* ob = p.out + (static_cast<size_t>(bh) * T + t0) * DV + col;
+                const uint32_t aot = sbase + L::OFF_OT + (col / 64) * 8192 + (col % 8) * 2;
+                const uint32_t c8 = (col % 64) / 8;
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int tb = 32 * hh + 16 * q;   // first token of these 16 columns
@@ -556,10 +587,11 @@ __device__ __forceinline__ void chain_role(const Params& p, uint8_t* sm, uint32_
                         const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
                         const int t = tb + 2 * m + (odd ? 1 : 0);
                         const uint32_t w = odd ? pack_bf16(recv, o1[2 * m + 1]) : pack_bf16(o1[2 * m], recv);
-                        if (t0 + t < T) st_global_b32(ob + static_cast<size_t>(t) * DV, w);
+                        st_shared_b32(aot + sw128_off(t, c8), w);
                     }
                 }
             }
+            fence_proxy_async_smem();   // the tile is read by the TMA store
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_ep);
@@ -991,14 +1023,6 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
 // ============================================================================
 // prep CTA of the per-channel decay (8 warps)
 // ============================================================================
-__device__ __forceinline__ uint32_t ld_shared_b32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 // Exponent kept inside the fp32 range, so that a factor stays finite even
 // for decays below the form's stated limit.
 __device__ __forceinline__ float ex2c(float x) { return ex2(fminf(fmaxf(x, -126.f), 126.f)); }
@@ -1423,13 +1447,13 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
 template <int DK, int DV, bool KDA>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-           const __grid_constant__ CUtensorMap tmv, const Params p) {
+           const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (sbase - raw);
     if (static_cast<int>(blockIdx.x) < p.n_chain) {
-        chain_role<DK, DV>(p, sm, sbase);
+        chain_role<DK, DV>(&tmo, p, sm, sbase);
     } else {
         if (threadIdx.x >= kConv + 32) return;   // the prep role: eight converting warps and a store warp
         if constexpr (KDA)
@@ -1479,7 +1503,7 @@ cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int R, cudaStream
         int n_prep = a.sm_count - p.n_chain;
         if (n_prep > units) n_prep = units;
         if (n_prep < 1) return cudaErrorInvalidConfiguration;
-        e = launch_coop(kern, static_cast<unsigned>(p.n_chain + n_prep), kThreads, smem, s, m.q, m.k, m.v, p);
+        e = launch_coop(kern, static_cast<unsigned>(p.n_chain + n_prep), kThreads, smem, s, m.q, m.k, m.v, m.o, p);
         if (e != cudaSuccess) return e;
         if (a.nlaunch) ++*a.nlaunch;
     }
