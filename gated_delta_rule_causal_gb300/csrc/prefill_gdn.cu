@@ -73,6 +73,7 @@ namespace gdn {
 using chunk::C;
 using chunk::kAStride;
 using chunk::kmaj;
+using chunk::ld_shared_bf16;
 using chunk::ld_shared_v4;
 using chunk::mnmaj;
 using chunk::st_shared_v4;
@@ -88,38 +89,44 @@ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // One chunk's intermediates, byte-identical in the workspace and in shared
 // memory. Tiles are bf16 with the 128-byte swizzle (1024-aligned offsets).
-// The same layout serves both decays: with a scalar gate Gam_t = gam_t on
-// every channel, so Q o Gam = diag(gam) Q and K o Gam_C/Gam = diag(gam_C/gam) K.
+// The same layout serves both decays (with a scalar gate Gam_t = gam_t on
+// every channel). With N_c = W^T K' and E_c = QG^T - W^T P^T the chunk's
+// effect on the state and its output are affine in X_0:
+//    X   = X_0 Diag(Gam_C) + Ut^T K' - X_0 N_c
+//    O^T = Ut^T P^T + X_0 E_c
+// so the chain needs no U^T = Ut^T - X_0 W^T of its own.
 template <int DK, int DV>
 struct Slot {
     static constexpr int KA = DK / 64;
-    static constexpr uint32_t W_OFF = 0;                  // W^T [dk][64 t]: MN-major B operand
-    static constexpr uint32_t U_OFF = DK * 128;           // Ut^T [dv][64 t]
-    static constexpr uint32_t P_OFF = U_OFF + DV * 128;   // P [64 t][64 j]: K-major B operand
-    static constexpr uint32_t QG_OFF = P_OFF + 8192;      // Q o Gam          [64 t][DK], KA atoms of 8 KB
-    static constexpr uint32_t KP_OFF = QG_OFF + KA * 8192;   // K o Gam_C/Gam [64 j][DK]
-    static constexpr uint32_t V_OFF = KP_OFF + KA * 8192;    // Gam_C [DK] (fp32)
+    static constexpr uint32_t NC_OFF = 0;                   // -N_c [DK c][DK c']: MN-major B, KA atoms of [DK][64]
+    static constexpr uint32_t E_OFF = DK * DK * 2;          // E_c  [DK c][64 t]: MN-major B
+    static constexpr uint32_t U_OFF = E_OFF + DK * 128;     // Ut^T [DV][64 j]: K-major A
+    static constexpr uint32_t KP_OFF = U_OFF + DV * 128;    // K' = K o Gam_C/Gam [64 j][DK]: MN-major B, KA atoms of 8 KB
+    static constexpr uint32_t P_OFF = KP_OFF + KA * 8192;   // P [64 t][64 j]: K-major B
+    static constexpr uint32_t TILES = P_OFF + 8192;
+    static constexpr uint32_t V_OFF = TILES;                // Gam_C [DK] (fp32)
     static constexpr uint32_t BYTES = V_OFF + 512;
-    static_assert(BYTES % 16 == 0, "bulk copies move multiples of 16 bytes");
+    // The chain loads the slot in two parts: B = [-N_c | E_c] (read by the
+    // state product) and A = the rest (read by the products issued earlier).
+    static constexpr uint32_t B_BYTES = U_OFF;
+    static constexpr uint32_t A_BYTES = BYTES - U_OFF;
+    static_assert(TILES % 1024 == 0 && BYTES % 16 == 0, "tile alignment, bulk copy sizes");
 };
 
 template <int DK, int DV>
 struct ChainLayout {
     static constexpr int KA = DK / 64;
     using S = Slot<DK, DV>;
-    static constexpr uint32_t STAGE = align1024(S::BYTES);      // one slot per stage
-    static constexpr uint32_t OFF_SS = 2 * STAGE;               // X_0 bf16 [128 rows][DK]
-    static constexpr uint32_t OFF_US = OFF_SS + KA * 16384;     // U^T bf16 [128 rows][64 j]
-    static constexpr uint32_t OFF_OT = OFF_US + 16384;          // output tile bf16 [64 t][DV] for the TMA store
-    static constexpr uint32_t OFF_VEC = OFF_OT + DV * 128;      // the slot vector per stage
-    static constexpr uint32_t OFF_BAR = OFF_VEC + 2 * 512;
-    static constexpr uint32_t BYTES = OFF_BAR + 128;
-    // TMEM columns (lanes = value rows)
-    static constexpr uint32_t COL_U = 0;        // X_0 W^T                          [dv][64]
-    static constexpr uint32_t COL_O = 64;       // two buffers of X_0 QG^T + U^T P^T [dv][64], 128 apart
-    static constexpr uint32_t COL_S = 320;      // U^T K'                           [dv][DK]
+    static constexpr uint32_t STAGE = S::TILES;                 // the slot's tiles, per stage
+    static constexpr uint32_t OFF_VEC = 2 * STAGE;              // the slot's vector, per stage (512 B)
+    static constexpr uint32_t OFF_SS = OFF_VEC + 1024;          // X_0 bf16 [128 rows][DK]
+    static constexpr uint32_t OFF_OT = OFF_SS + KA * 16384;     // output tile bf16 [64 t][DV] for the TMA store
+    static constexpr uint32_t OFF_BAR = OFF_OT + DV * 128;
+    static constexpr uint32_t BYTES = OFF_BAR + 256;
+    // TMEM columns (lanes = value rows); buffer b = chunk & 1
+    static constexpr uint32_t COL_S = 0;        // Ut^T K' - X_0 N_c   [dv][DK], two buffers 128 apart
+    static constexpr uint32_t COL_O = 256;      // Ut^T P^T + X_0 E_c  [dv][64], two buffers 64 apart
     static constexpr uint32_t TMEM_COLS = 512;
-    static_assert(COL_S + DK <= TMEM_COLS, "tensor memory budget");
 };
 
 template <int DK, int DV>
@@ -136,13 +143,19 @@ struct PrepLayout {
     static constexpr uint32_t OFF_OUT = OFF_TB2 + 8192;  // the slot being assembled / stored
     static constexpr uint32_t OFF_AS = OFF_OUT + align1024(S::BYTES);   // fp32 [64][kAStride]
     static constexpr uint32_t OFF_RS = OFF_AS + C * kAStride * 4;       // fp32 [32][kRStride]
-    static constexpr uint32_t OFF_MISC = OFF_RS + 32 * 40 * 4;          // log2 prefix, beta, beta gam
-    static constexpr uint32_t OFF_BAR = OFF_MISC + 3 * 64 * 4;
+    static constexpr uint32_t OFF_MISC = OFF_RS + 32 * 40 * 4;          // log2 prefix, beta, beta gam, gam
+    static constexpr uint32_t OFF_BAR = OFF_MISC + 4 * 64 * 4;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
+    // W^T as a bf16 K-major A operand [dk][64 j] goes over the solve matrix,
+    // which is dead by then
+    static constexpr uint32_t OFF_WT = OFF_AS;
+    static_assert(DK * 128 <= C * kAStride * 4, "W^T fits over the solve matrix");
     static constexpr uint32_t COL_G = 0;     // [K;Q] K^T  [128][64]
     static constexpr uint32_t COL_W = 64;    // W^T        [dk][64]
     static constexpr uint32_t COL_UT = 128;  // Ut^T       [dv][64]
-    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t COL_N = 192;   // -W^T K'    [dk][DK]
+    static constexpr uint32_t COL_E = 320;   // W^T P^T    [dk][64]
+    static constexpr uint32_t TMEM_COLS = 512;
 };
 constexpr int kRStride = 40;   // fp32 row stride of the merge scratch (conflict-free fragment reads)
 
@@ -160,7 +173,7 @@ struct PrepLayoutKda {
     static constexpr int VA = DV / 64;
     using S = Slot<DK, DV>;
     static constexpr uint32_t QK_BYTES = KA * 16384;     // per k-atom: rows 0-63 k, rows 64-127 q
-    static constexpr uint32_t OFF_V = 2 * QK_BYTES;      // V [64 t][DV]
+    static constexpr uint32_t OFF_V = QK_BYTES;          // V [64 t][DV]
     static constexpr uint32_t OFF_GATE = OFF_V + VA * 8192;   // alpha fp32 [64 t][DK]
     static constexpr uint32_t OFF_TB1 = OFF_GATE + DK * 256;  // T diag(beta) bf16 [t][j]
     static constexpr uint32_t OFF_B = OFF_GATE;               // column operands, over gate + TB1
@@ -171,16 +184,22 @@ struct PrepLayoutKda {
     static constexpr uint32_t OFF_AS = OFF_OUT + align1024(S::BYTES);   // fp32 [64][kAStride]
     static constexpr uint32_t OFF_RS = OFF_AS + C * kAStride * 4;        // fp32 [32][kRStride]
     static constexpr uint32_t OFF_BLK = OFF_RS + 32 * 40 * 4;            // log2-gate sums of 8-token blocks [8][DK]
-    static constexpr uint32_t OFF_PR = OFF_BLK + 8 * DK * 4;             // 2^r_a [4][DK]
-    static constexpr uint32_t OFF_MISC = OFF_PR + 4 * DK * 4;            // beta [64]
+    static constexpr uint32_t OFF_MISC = OFF_BLK + 8 * DK * 4;           // beta [64]
     static constexpr uint32_t OFF_BAR = OFF_MISC + 64 * 4;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
+    // W^T as a bf16 K-major A operand goes over the solve matrix (dead by
+    // then); K o Gam (the W product's operand) and Q o Gam wait in the slot
+    // buffer's -N_c and E_c tiles until those are written.
+    static constexpr uint32_t OFF_WT = OFF_AS;
+    static_assert(DK * 128 <= C * kAStride * 4, "W^T fits over the solve matrix");
     // First row (and product column) of sub-chunk a's column operand: its
     // rows j < 16(a+1) follow the operands of the sub-chunks before it.
     static __host__ __device__ constexpr int b_row(int a) { return 8 * a * (a + 1); }
     static constexpr uint32_t COL_G = 0;     // [K;Q] B^T, 160 columns (block a at b_row(a))
-    static constexpr uint32_t COL_W = 0;     // W^T per sub-chunk (four blocks; the products above are read by then)
-    static constexpr uint32_t COL_UT = 256;  // Ut^T [dv][64]
+    static constexpr uint32_t COL_W = 160;   // W^T    [dk][64]
+    static constexpr uint32_t COL_UT = 224;  // Ut^T   [dv][64]
+    static constexpr uint32_t COL_N = 288;   // -W^T K' [dk][DK]
+    static constexpr uint32_t COL_E = 416;   // W^T P^T [dk][64]
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -242,8 +261,15 @@ __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
 }
 
 // ============================================================================
-// chain CTA: the state-dependent part of every chunk of one window
+// chain CTA: the state-dependent part of every chunk of one sequence-head
 // ============================================================================
+// Per chunk c (buffer b = c & 1 of tensor memory, stage b of shared memory):
+//   pre(c):   S_b = Ut^T K',  O_b = Ut^T P^T          (no state: issued early)
+//   state(c): [S_b | O_b] += X_c [-N_c | E_c]           (one MMA chain, N = DK + 64)
+//   converters: X_{c+1} = X_c Diag(Gam_C) + S_b (fp32 registers), republished
+//               as the bf16 operand; o = O_b through the output tile.
+// Only state(c) and the state update lie on the path from one chunk to the
+// next.
 template <int DK, int DV>
 __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params& p, uint8_t* sm, uint32_t sbase) {
     using L = ChainLayout<DK, DV>;
@@ -251,7 +277,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
     constexpr int DKH = DK / 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool control = warp == kConv / 32;
-    const bool flagw = warp == kConv / 32 + 1;
+    const bool copyw = warp == kConv / 32 + 1;
     const int r = 32 * (warp & 3) + lane;   // tensor-memory lane = value row (converting warps)
     const int hh = (warp >> 2) & 1;         // column half
     const int g = blockIdx.x;
@@ -260,31 +286,37 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
     const bool own = warp < kConv / 32 && r < DV;
 
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
-    uint64_t* bar_full = bar;        // [2] stage loaded (control expects the bytes)
-    uint64_t* bar_u = bar + 2;       // MMA: X_0 W^T done
-    uint64_t* bar_c = bar + 3;       // MMA: U^T K' done
-    uint64_t* bar_o = bar + 4;       // MMA: U^T P^T done (and everything before it)
-    uint64_t* bar_us = bar + 5;      // converters: U^T written          (8 arrivals)
-    uint64_t* bar_x = bar + 6;       // converters: X_0 written          (8 arrivals)
-    uint64_t* bar_ep = bar + 7;      // converters: output columns read  (8 arrivals)
-    uint64_t* bar_test = bar + 8;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 9);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 10);
-    uint64_t* bar_sfree = bar + 11;  // [2] control: every MMA reading the stage is done
-    uint64_t* bar_ofree = bar + 15;  // copy warp: the output tile's store has read it
-    const uint32_t aSS = sbase + L::OFF_SS, aUS = sbase + L::OFF_US;
-    float* sVec = reinterpret_cast<float*>(sm + L::OFF_VEC);
+    uint64_t* bar_full = bar;        // [2] copy warp: part A of the stage's slot (and its vector) has arrived
+    uint64_t* bar_fullb = bar + 13;  // [2] copy warp: part B (-N_c, E_c) has arrived
+    uint64_t* bar_donea = bar + 15;  // [2] MMA: pre(c) done, part A of stage c & 1 is read
+    uint64_t* bar_s = bar + 2;       // MMA: state(c) and everything before it done
+    uint64_t* bar_fin = bar + 3;     // MMA: all issued MMAs done (after a failure)
+    uint64_t* bar_x = bar + 4;       // converters: X_c written          (8 arrivals)
+    uint64_t* bar_ep = bar + 5;      // [2] converters: chunk c's output tile written, buffer c & 1 read (8 arrivals)
+    uint64_t* bar_sfree = bar + 7;   // [2] control: state(c) done, part B of stage c & 1 is read
+    uint64_t* bar_ofree = bar + 9;   // copy warp: the output tile's store has read it
+    uint64_t* bar_test = bar + 10;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 11);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 12);
+    const uint32_t aSS = sbase + L::OFF_SS;
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(&bar[i], 1);
-        for (int i = 5; i < 8; ++i) mbar_init(&bar[i], kConv / 32);
-        mbar_init(bar_test, 1);
-        for (int i = 11; i < 13; ++i) mbar_init(&bar[i], 1);
+        mbar_init(&bar_full[0], 1);
+        mbar_init(&bar_full[1], 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_fin, 1);
+        mbar_init(bar_x, kConv / 32);
+        mbar_init(&bar_ep[0], kConv / 32);
+        mbar_init(&bar_ep[1], kConv / 32);
+        mbar_init(&bar_sfree[0], 1);
+        mbar_init(&bar_sfree[1], 1);
+        for (int i = 13; i < 17; ++i) mbar_init(&bar[i], 1);
         mbar_init(bar_ofree, 1);
+        mbar_init(bar_test, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (flagw && lane == 0) tma_prefetch_desc(tmo);
+    if (copyw && lane == 0) tma_prefetch_desc(tmo);
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
@@ -300,14 +332,14 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
     }
 
     const size_t ssz = static_cast<size_t>(DK) * DV;
-    constexpr uint32_t ID_U = idesc_bf16(128, 64, false, true);     // X_0 W^T
-    constexpr uint32_t ID_O = idesc_bf16(128, 64, false, false);    // X_0 Q^T, U^T P^T
-    constexpr uint32_t ID_S = idesc_bf16(128, DK, false, true);     // U^T K'
+    constexpr uint32_t ID_K = idesc_bf16(128, DK, false, true);        // Ut^T K'
+    constexpr uint32_t ID_P = idesc_bf16(128, 64, false, false);       // Ut^T P^T
+    constexpr uint32_t ID_X = idesc_bf16(128, DK + 64, false, true);   // X_c [-N_c | E_c]
+    auto col_s = [](int b) { return L::COL_S + 256u * b; };             // S_b; O_b follows at + DK
 
     if (control) {
         // ======================= control warp (lane 0) =========================
-        // Issues every MMA. Copies belong to the copy warp; the control thread
-        // tells it when a stage's last reader is done (bar_sfree).
+        // Issues every MMA. Copies belong to the copy warp.
         if (lane == 0 && !failed && n > 0) {
             bool fail = false;
             auto give_up = [&](int bit) {
@@ -316,94 +348,81 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                 *abort_flag = 1;
                 p.abort_all();
             };
-            // Commits issued so far per MMA barrier: the k-th completes phase k.
-            int n_u = 0, n_c = 0, n_o = 0;
-            // X_0 W^T into COL_U (commit) and X_0 QG^T into the chunk's output buffer.
-            auto issue_state_mmas = [&](int i) {
-                const int s = i & 1;
-                const uint32_t stg = sbase + s * L::STAGE;
-                const uint32_t aW = stg + S::W_OFF;
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint64_t sa = kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32);
-                    mma_bf16_ss(tmem + L::COL_U, sa, mnmaj(aW + kk * 2048, 8192), ID_U, kk > 0);
-                }
-                mma_commit(bar_u);
-                ++n_u;
-#pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                    const uint64_t sa = kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32);
-                    mma_bf16_ss(tmem + L::COL_O + 128 * s, sa,
-                                kmaj(stg + S::QG_OFF + (kk / 4) * 8192 + (kk % 4) * 32), ID_O, kk > 0);
-                }
-            };
             auto wait = [&](uint64_t* b, uint32_t parity, int bit) {
                 if (fail) return;
                 if (!mbar_wait_or_abort(b, parity, abort_flag)) give_up(bit);
             };
-            wait(bar_x, 0, kStatusMmaWait);
+            int n_s = 0;   // commits of bar_s issued: the k-th completes phase k
+            auto issue_pre = [&](int c) {
+                const int b = c & 1;
+                const uint32_t stg = sbase + b * L::STAGE;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + col_s(b), kmaj(stg + S::U_OFF + kk * 32), mnmaj(stg + S::KP_OFF + kk * 2048, 8192),
+                                ID_K, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(tmem + col_s(b) + DK, kmaj(stg + S::U_OFF + kk * 32), kmaj(stg + S::P_OFF + kk * 32),
+                                ID_P, kk > 0);
+                mma_commit(&bar_donea[b]);   // part A of stage b may be reloaded once these are done
+            };
+            auto issue_state = [&](int c) {
+                const int b = c & 1;
+                const uint32_t stg = sbase + b * L::STAGE;
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk)
+                    mma_bf16_ss(tmem + col_s(b), kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
+                                mnmaj(stg + S::NC_OFF + kk * 2048, DK * 128), ID_X, true);
+                mma_commit(bar_s);
+                ++n_s;
+            };
             wait(&bar_full[0], 0, kStatusTmaWait);
             if (!fail) {
                 tc_fence_after();
-                issue_state_mmas(0);
+                issue_pre(0);
             }
             for (int it = 0; it < n && !fail; ++it) {
-                const int s = it & 1;
-                const uint32_t stg = sbase + s * L::STAGE;
-                wait(bar_us, it & 1, kStatusMmaWait);
-                if (it >= 1) wait(bar_ep, (it - 1) & 1, kStatusMmaWait);
+                wait(bar_x, it & 1, kStatusMmaWait);   // X_it published, so state(it-1) was done
+                if (fail) break;
+                // every MMA reading stage (it-1) & 1 finished with state(it-1):
+                // the copy warp may load chunk it+1 there
+                if (it >= 1 && it + 1 < n) mbar_arrive(&bar_sfree[(it - 1) & 1]);
+                wait(&bar_fullb[it & 1], (it >> 1) & 1, kStatusTmaWait);
                 if (fail) break;
                 tc_fence_after();
-                // dX = U^T K' (commit), then U^T P^T onto X_0 QG^T (commit)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + L::COL_S, kmaj(aUS + kk * 32), mnmaj(stg + S::KP_OFF + kk * 2048, 8192), ID_S,
-                                kk > 0);
-                mma_commit(bar_c);
-                ++n_c;
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(tmem + L::COL_O + 128 * s, kmaj(aUS + kk * 32), kmaj(stg + S::P_OFF + kk * 32), ID_O,
-                                true);
-                mma_commit(bar_o);
-                ++n_o;
+                issue_state(it);
                 if (it + 1 < n) {
-                    wait(&bar_full[s ^ 1], ((it + 1) >> 1) & 1, kStatusTmaWait);
-                    wait(bar_x, (it + 1) & 1, kStatusMmaWait);
+                    // buffer (it+1) & 1: its S was read before bar_x(it), its O
+                    // before chunk it-1's epilogue (bar_ep[(it-1) & 1])
+                    wait(&bar_full[(it + 1) & 1], ((it + 1) >> 1) & 1, kStatusTmaWait);
+                    if (it >= 1) wait(&bar_ep[(it - 1) & 1], ((it - 1) >> 1) & 1, kStatusMmaWait);
                     if (fail) break;
                     tc_fence_after();
-                    issue_state_mmas(it + 1);
-                }
-                if (it + 2 < n) {
-                    wait(bar_o, it & 1, kStatusMmaWait);   // every MMA reading stage s is done
-                    if (fail) break;
-                    mbar_arrive(&bar_sfree[s]);             // the copy warp may refill it
+                    issue_pre(it + 1);
                 }
             }
-            if (fail) {
-                // Let MMAs in flight finish before the CTA exits (bounded: 100 ms
-                // each). MMAs complete in issue order, so the newest commit of
-                // each barrier covers the ones before it.
-                if (n_u > 0) mbar_wait(bar_u, (n_u - 1) & 1, 100000000ull);
-                if (n_c > 0) mbar_wait(bar_c, (n_c - 1) & 1, 100000000ull);
-                if (n_o > 0) mbar_wait(bar_o, (n_o - 1) & 1, 100000000ull);
+            if (fail && n_s + (n > 0 ? 1 : 0) > 0) {
+                // Let every MMA issued finish before the CTA exits (bounded:
+                // 100 ms): one more commit covers them all, in issue order.
+                mma_commit(bar_fin);
+                mbar_wait(bar_fin, 0, 100000000ull);
             }
         }
-    } else if (flagw) {
+    } else if (copyw) {
         // ======================= copy warp (lane 0) ============================
         // Keeps copies and global hand-offs off the control thread. For chunk
         // c, in order: once the ring holds the chunk (its ready flag) and
-        // stage c & 1 is free (bar_sfree, relayed by the control thread after
-        // the last MMA reading it), loads the slot; hands the output tile back
+        // stage c & 1 is free (bar_sfree), loads the slot (tiles into the
+        // stage, the vector beside it); hands the output tile back
         // (bar_ofree) once chunk c - 2's store has read it; then, for chunk
         // c - 1, waits for its slot to arrive and publishes the consumed count,
-        // waits for its output tile (bar_ep) and stores it. Each barrier waited on here can only
-        // advance one more phase after a step this warp takes later, so no
-        // parity wait is ever two phases behind.
+        // waits for its output tile (bar_ep) and stores it. Each barrier waited
+        // on here can only advance one more phase after a step this warp takes
+        // later, so no parity wait is ever two phases behind.
         if (lane == 0 && !failed && n > 0) {
             bool fail = false;
-            bool pending[2] = {false, false};
-            int load_idx[2] = {0, 0};   // chunk of the load last issued on each stage
+            bool pending[2] = {false, false}, pendb[2] = {false, false};
+            int load_idx[2] = {0, 0};   // chunk of the loads last issued on each stage
             auto give_up = [&](int bit) {
                 fail = true;
                 status_bits |= bit;
@@ -423,14 +442,23 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                         give_up(kStatusFlagWait);
                         break;
                     }
-                    if (c >= 2) wait(&bar_sfree[s], ((c - 2) >> 1) & 1, kStatusMmaWait);
-                    if (fail) break;
+                    const uint8_t* src = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES;
+                    uint8_t* stg = sm + s * L::STAGE;
                     fence_proxy_async_global();
-                    mbar_arrive_expect_tx(&bar_full[s], S::BYTES);
-                    bulk_load(sm + s * L::STAGE, p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * S::BYTES,
-                              S::BYTES, &bar_full[s]);
+                    // part A once pre(c - 2) has read it (long done), then part B
+                    // once state(c - 2) has (relayed by the control thread)
+                    if (c >= 2) wait(&bar_donea[s], ((c - 2) >> 1) & 1, kStatusMmaWait);
+                    if (fail) break;
+                    mbar_arrive_expect_tx(&bar_full[s], S::A_BYTES);
+                    bulk_load(stg + S::U_OFF, src + S::U_OFF, S::TILES - S::U_OFF, &bar_full[s]);
+                    bulk_load(sm + L::OFF_VEC + s * 512, src + S::V_OFF, 512, &bar_full[s]);
                     pending[s] = true;
                     load_idx[s] = c;
+                    if (c >= 2) wait(&bar_sfree[s], ((c - 2) >> 1) & 1, kStatusMmaWait);
+                    if (fail) break;
+                    mbar_arrive_expect_tx(&bar_fullb[s], S::B_BYTES);
+                    bulk_load(stg, src, S::B_BYTES, &bar_fullb[s]);
+                    pendb[s] = true;
                 }
                 // chunk c - 2's output store (the only one in flight) has long
                 // read its tile: hand it back for chunk c - 1's epilogue
@@ -441,14 +469,16 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                 if (c >= 1) {
                     const int c1 = c - 1, s1 = c1 & 1;
                     wait(&bar_full[s1], (c1 >> 1) & 1, kStatusTmaWait);
+                    wait(&bar_fullb[s1], (c1 >> 1) & 1, kStatusTmaWait);
                     if (fail) break;
                     pending[s1] = false;
+                    pendb[s1] = false;
                     // Chunks 0..c-1 are in shared memory. The wait above
                     // (acquire) orders this store after the completed copy, so
                     // a relaxed store suffices: a release would also wait for
                     // the copy just issued.
                     st_relaxed_u64(p.consumed(g), p.epoch | static_cast<unsigned long long>(c));
-                    wait(bar_ep, c1 & 1, kStatusMmaWait);
+                    wait(&bar_ep[s1], (c1 >> 1) & 1, kStatusMmaWait);
                     if (fail) break;
                     // rows past T are clipped by the tensor map
 #pragma unroll
@@ -458,8 +488,10 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
             }
             bulk_wait_all();   // every output store has completed
             if (fail) {
-                for (int s2 = 0; s2 < 2; ++s2)
+                for (int s2 = 0; s2 < 2; ++s2) {
                     if (pending[s2]) mbar_wait(&bar_full[s2], (load_idx[s2] >> 1) & 1, 100000000ull);
+                    if (pendb[s2]) mbar_wait(&bar_fullb[s2], (load_idx[s2] >> 1) & 1, 100000000ull);
+                }
             }
         }
     } else {
@@ -476,6 +508,8 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
             st[i + 2] = x.z;
             st[i + 3] = x.w;
         }
+        // Every row of the bf16 operand is written (rows >= d_v as zeros) so
+        // that padded MMA rows never see stale bits.
         auto publish_state = [&]() {
 #pragma unroll
             for (int b = 0; b < DKH / 32; ++b) {
@@ -483,94 +517,43 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                 store_row32_bf16(aSS + (cb / 64) * 16384, r, (cb % 64) / 8, st + 32 * b);
             }
         };
-        // Every row is written once (rows >= d_v as zeros) so that padded MMA
-        // rows never see stale bits.
-        publish_state();
-        {
-            float z[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) z[i] = 0.f;
-            store_row32_bf16(aUS, r, 4 * hh, z);
-        }
         auto signal = [&](uint64_t* b) {   // this warp's writes / TMEM reads are done
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(b);
         };
+        publish_state();
         signal(bar_x);
 
-        uint32_t ph_u = 0, ph_c = 0, ph_o = 0;
         bool bad = failed;
-        int it = 0;
-        for (; it < n; ++it) {
-            const int s = it & 1;
-            const float* vec = reinterpret_cast<const float*>(sm + s * L::STAGE + S::V_OFF);
-            float* sv = sVec + 128 * s;
-            // ---- U^T = Ut^T - X_0 W^T, as the bf16 operand of both U products --------
-            bool ok = !bad && mbar_wait_or_abort(&bar_full[s], (it >> 1) & 1, abort_flag) &&
-                      mbar_wait_or_abort(bar_u, ph_u, abort_flag);
-            ph_u ^= 1u;
-            tc_fence_after();
-            if (ok) {
-                if (tid < 128) sv[tid] = vec[tid];
-                if (own) {
-                    const uint32_t aUt = sbase + s * L::STAGE + S::U_OFF;
-                    float x[32];
-                    tmem_ld32(tlane + L::COL_U + 32 * hh, x);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint4 u = ld_shared_v4(aUt + sw128_off(r, 4 * hh + m));
-                        const float2 a0 = unpack_bf16(u.x), a1 = unpack_bf16(u.y), a2 = unpack_bf16(u.z),
-                                     a3 = unpack_bf16(u.w);
-                        float* y = x + 8 * m;
-                        y[0] = a0.x - y[0];
-                        y[1] = a0.y - y[1];
-                        y[2] = a1.x - y[2];
-                        y[3] = a1.y - y[3];
-                        y[4] = a2.x - y[4];
-                        y[5] = a2.y - y[5];
-                        y[6] = a3.x - y[6];
-                        y[7] = a3.y - y[7];
-                    }
-                    store_row32_bf16(aUS, r, 4 * hh, x);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            // agreement point of the converting warps (also publishes sVec)
-            if (named_sync_or(kBarConv, kConv, !ok)) {
-                bad = true;
-                break;
-            }
-            if (lane == 0) mbar_arrive(bar_us);
-            // ---- X = X_0 Diag(Gam_C) + dX, republished as the bf16 operand ----------
-            ok = mbar_wait_or_abort(bar_c, ph_c, abort_flag);
-            ph_c ^= 1u;
+        for (int it = 0; it < n && !bad; ++it) {
+            const int b = it & 1;
+            // ---- X_{it+1} = X_it Diag(Gam_C) + S_b, republished ------------------
+            bool ok = mbar_wait_or_abort(&bar_full[b], (it >> 1) & 1, abort_flag) &&
+                      mbar_wait_or_abort(bar_s, it & 1, abort_flag);
             tc_fence_after();
             if (ok && own) {
+                const float* vec = reinterpret_cast<const float*>(sm + L::OFF_VEC + b * 512);
 #pragma unroll
-                for (int b = 0; b < DKH / 32; ++b) {
+                for (int b2 = 0; b2 < DKH / 32; ++b2) {
                     float x[32];
-                    tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
+                    tmem_ld32(tlane + col_s(b) + hh * DKH + 32 * b2, x);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) st[32 * b + i] = sv[hh * DKH + 32 * b + i] * st[32 * b + i] + x[i];
+                    for (int i = 0; i < 32; ++i)
+                        st[32 * b2 + i] = vec[hh * DKH + 32 * b2 + i] * st[32 * b2 + i] + x[i];
                 }
                 publish_state();
             }
             signal(bar_x);
             bad |= !ok;
-            // ---- output: o_t = (X_0 QG^T + U^T P^T)[:, t] ------------------------------
-            ok = mbar_wait_or_abort(bar_o, ph_o, abort_flag) &&
-                 (it == 0 || mbar_wait_or_abort(bar_ofree, (it - 1) & 1, abort_flag));
-            ph_o ^= 1u;
-            tc_fence_after();
+            // ---- output: o_t = O_b[:, t], through the output tile ----------------
+            ok = ok && (it == 0 || mbar_wait_or_abort(bar_ofree, (it - 1) & 1, abort_flag));
             if (ok && own) {
                 // Lane pairs (r even, r + 1) exchange values so that each
-                // writes two adjacent columns of one token row of the output
-                // tile in one word; the control warp stores the tile.
+                // writes two adjacent columns of one token row of the tile in
+                // one word; the copy warp stores the tile.
                 const bool odd = lane & 1;
                 const int col = r & ~1;
                 const uint32_t aot = sbase + L::OFF_OT + (col / 64) * 8192 + (col % 8) * 2;
@@ -579,7 +562,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                 for (int q = 0; q < 2; ++q) {
                     const int tb = 32 * hh + 16 * q;   // first token of these 16 columns
                     float o1[16];
-                    tmem_ld16(tlane + L::COL_O + 128 * s + tb, o1);
+                    tmem_ld16(tlane + col_s(b) + DK + tb, o1);
                     tmem_ld_wait();
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
@@ -591,13 +574,10 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                     }
                 }
             }
-            fence_proxy_async_smem();   // the tile is read by the TMA store
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_ep);
+            signal(&bar_ep[b]);   // also orders the tile for the TMA store
             bad |= !ok;
         }
-        // ---- the final state -----------------------------------------------------
+        // ---- the final state ---------------------------------------------------
         bad = named_sync_or(kBarConv, kConv, bad);
         if (!bad) {
             float* dst = p.state_out ? p.state_out + bh * ssz : nullptr;
@@ -609,13 +589,14 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
             }
         } else if (tid == 0) {
             if (!failed) status_bits |= kStatusMmaWait;
+            *abort_flag = 1;
             p.abort_all();
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
-    if (status_bits && (tid == 0 || ((control || flagw) && lane == 0))) atomicOr(p.status, status_bits);
+    if (status_bits && (tid == 0 || ((control || copyw) && lane == 0))) atomicOr(p.status, status_bits);
 }
 
 // ============================================================================
@@ -708,6 +689,20 @@ __device__ __forceinline__ void invert_unit_lower(float* As, float* Rs, int warp
     }
 }
 
+// Row r of -N_c from tensor memory (columns hh*DK/2 ..) into the slot's
+// MN-major tile: the 64-column atom of column c' at c' / 64, DK rows each.
+template <int DK>
+__device__ __forceinline__ void store_neg_nc(uint32_t tcol, int hh, uint32_t aNC, int r) {
+#pragma unroll
+    for (int b2 = 0; b2 < DK / 64; ++b2) {
+        float x[32];
+        const int col = hh * (DK / 2) + 32 * b2;
+        tmem_ld32(tcol + col, x);
+        tmem_ld_wait();
+        store_row32_bf16(aNC + (col / 64) * (DK * 128), r, (col % 64) / 8, x);
+    }
+}
+
 // Store warp of a prep CTA (lane 0 of warp 8). For each unit of the CTA, in
 // order: waits until the converting warps have assembled its slot
 // (slot_full), waits until the chain has loaded the chunk R before it from
@@ -764,6 +759,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     float* sG2 = reinterpret_cast<float*>(sm + L::OFF_MISC);   // cumulative log2-gate
     float* sB = sG2 + 64;                                        // beta (0 on padded tokens)
     float* sBG = sB + 64;                                        // beta_t gam_t
+    float* sGam = sBG + 64;                                      // gam_t
     uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint64_t* bar_m = bar_full + 2;
     uint64_t* bar_test = bar_full + 3;
@@ -854,6 +850,8 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
 
     constexpr uint32_t ID_G = idesc_bf16(128, 64, false, false);   // [K;Q] K^T
     constexpr uint32_t ID_WU = idesc_bf16(128, 64, true, false);   // K^T TB2^T, V^T TB1^T
+    constexpr uint32_t ID_NEG_N = idesc_bf16(128, DK, false, true, true);   // -(W^T K')
+    constexpr uint32_t ID_EP = idesc_bf16(128, 64, false, false);            // W^T P^T
 
     float g_nx, b_nx;
     load_gb(pid, g_nx, b_nx);
@@ -868,6 +866,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         const uint32_t stg = sbase + s * L::STAGE;
         const uint32_t aOut = sbase + L::OFF_OUT;
         float* oVec = reinterpret_cast<float*>(sm + L::OFF_OUT + S::V_OFF);   // gam_C per channel
+        uint32_t pw[16];   // this thread's row of P (rows 64-127), bf16 pairs
         if (tid == 0 && un < nunits) {
             fence_proxy_async_smem();
             issue_load(un, s ^ 1);   // stage s^1's MMAs finished with the previous unit
@@ -898,28 +897,11 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         }
         sync_conv();
         if (tid >= 32 && tid < 64) sG2[tid] += sG2[31];
-        // the slot buffer is written from here on: the previous unit's store has read it
-        if (k >= 1) {
-            if (!wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
-        } else {
-            sync_conv();
-        }
-        if (tid < 64) sBG[tid] = sB[tid] * ex2(sG2[tid]);
-        if (tid < DK) oVec[tid] = ex2(sG2[63]);
-        // ---- the chain's operands Q o Gam = diag(gam) Q and K o Gam_C/Gam =
-        //      diag(gam_C/gam) K: thread (t, part) scales DK/4 channels of row t
-        {
-            const int t = tid >> 2, part = tid & 3;
-            const float fq = ex2(sG2[t]), fk = ex2(sG2[63] - sG2[t]);
-#pragma unroll
-            for (int i = 0; i < DK / 32; ++i) {
-                const int cidx = part * (DK / 32) + i;   // 16-byte chunk of the row
-                const int a = cidx / 8, c8 = cidx % 8;
-                const uint32_t ro = sw128_off(t, c8);
-                st_shared_v4_u4(aOut + S::KP_OFF + a * 8192 + ro, scale_bf16x8(ld_shared_v4(stg + a * 16384 + ro), fk));
-                st_shared_v4_u4(aOut + S::QG_OFF + a * 8192 + ro,
-                                scale_bf16x8(ld_shared_v4(stg + a * 16384 + sw128_off(64 + t, c8)), fq));
-            }
+        sync_conv();
+        if (tid < 64) {
+            const float gam = ex2(sG2[tid]);
+            sGam[tid] = gam;
+            sBG[tid] = sB[tid] * gam;
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;
@@ -941,21 +923,45 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
                 *reinterpret_cast<float4*>(As + t * kAStride + j) = o;
             }
         } else {
-            // rows 64-127: P_tj = 2^(G_t - G_j) q_t.k_j for j <= t
+            // rows 64-127: P_tj = 2^(G_t - G_j) q_t.k_j for j <= t, held as bf16
+            // pairs until the slot buffer is free
             const int t = r - 64;
             const float Gt = sG2[t];
             float x[32];
             tmem_ld32(tlane + L::COL_G + 32 * hh, x);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int j = 32 * hh + i;
-                x[i] = (j <= t) ? ex2(Gt - sG2[j]) * x[i] : 0.f;
+            for (int i = 0; i < 16; ++i) {
+                const int j = 32 * hh + 2 * i;
+                pw[i] = pack_bf16((j <= t) ? ex2(Gt - sG2[j]) * x[2 * i] : 0.f,
+                                  (j + 1 <= t) ? ex2(Gt - sG2[j + 1]) * x[2 * i + 1] : 0.f);
             }
-            store_row32_bf16(aOut + S::P_OFF, t, 4 * hh, x);
         }
         sync_conv();
         invert_unit_lower(As, Rs, warp, lane);
+        // the slot buffer is written from here on: the previous unit's store has
+        // long read it
+        if (k >= 1 && !wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
+        if ((warp & 3) >= 2) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                st_shared_v4(aOut + S::P_OFF + sw128_off(r - 64, 4 * hh + m), pw[4 * m], pw[4 * m + 1], pw[4 * m + 2],
+                             pw[4 * m + 3]);
+        }
+        if (tid < DK) oVec[tid] = ex2(sG2[63]);
+        // ---- K' = K o Gam_C/Gam = diag(gam_C/gam) K: thread (t, part) scales
+        //      DK/4 channels of row t ------------------------------------------------
+        {
+            const int t = tid >> 2, part = tid & 3;
+            const float fk = ex2(sG2[63] - sG2[t]);
+#pragma unroll
+            for (int i = 0; i < DK / 32; ++i) {
+                const int cidx = part * (DK / 32) + i;   // 16-byte chunk of the row
+                const int a = cidx / 8, c8 = cidx % 8;
+                const uint32_t ro = sw128_off(t, c8);
+                st_shared_v4_u4(aOut + S::KP_OFF + a * 8192 + ro, scale_bf16x8(ld_shared_v4(stg + a * 16384 + ro), fk));
+            }
+        }
         // ---- T diag(beta) and T diag(beta gam) as bf16 MMA operands --------------
         {
             const int t = tid >> 2, q4 = tid & 3;
@@ -988,17 +994,48 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;
+        // W^T as the bf16 A operand of the two products below; Ut^T into the slot
         if (r < DK) {
             float x[32];
             tmem_ld32(tlane + L::COL_W + 32 * hh, x);
             tmem_ld_wait();
-            store_row32_bf16(aOut + S::W_OFF, r, 4 * hh, x);
+            store_row32_bf16(sbase + L::OFF_WT, r, 4 * hh, x);
         }
         if (r < DV) {
             float x[32];
             tmem_ld32(tlane + L::COL_UT + 32 * hh, x);
             tmem_ld_wait();
             store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, x);
+        }
+        publish();
+        // ---- -N_c = -(W^T K') and W^T P^T ------------------------------------------
+        if (tid == 0) {
+            const uint32_t aWT = sbase + L::OFF_WT;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + L::COL_N, kmaj(aWT + kk * 32), mnmaj(aOut + S::KP_OFF + kk * 2048, 8192), ID_NEG_N,
+                            kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + L::COL_E, kmaj(aWT + kk * 32), kmaj(aOut + S::P_OFF + kk * 32), ID_EP, kk > 0);
+            mma_commit(bar_m);
+        }
+        if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        mph ^= 1u;
+        if (r < DK) {
+            store_neg_nc<DK>(tlane + L::COL_N, hh, aOut + S::NC_OFF, r);
+            // E_c[r][t] = gam_t q_t[r] - (W^T P^T)[r][t]; q from the stage
+            float x[32];
+            tmem_ld32(tlane + L::COL_E + 32 * hh, x);
+            tmem_ld_wait();
+            const uint32_t aq = stg + (r / 64) * 16384 + (r % 8) * 2;
+            const uint32_t c8 = (r % 64) / 8;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int t = 32 * hh + i;
+                x[i] = sGam[t] * ld_shared_bf16(aq + sw128_off(64 + t, c8)) - x[i];
+            }
+            store_row32_bf16(aOut + S::E_OFF, r, 4 * hh, x);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -1056,12 +1093,11 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     float* As = reinterpret_cast<float*>(sm + L::OFF_AS);
     float* Rs = reinterpret_cast<float*>(sm + L::OFF_RS);
     float* sBlk = reinterpret_cast<float*>(sm + L::OFF_BLK);   // log2-gate sum of each 8-token block [8][DK]
-    float* sPr = reinterpret_cast<float*>(sm + L::OFF_PR);     // 2^r_a [4][DK]
     float* sB = reinterpret_cast<float*>(sm + L::OFF_MISC);    // beta (0 on padded tokens)
     const float* sGate = reinterpret_cast<const float*>(sm + L::OFF_GATE);
     uint8_t* outp = sm + L::OFF_OUT;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
-    uint64_t* bar_qk = bar;       // [2] k and q of a unit
+    uint64_t* bar_qk = bar;       // k and q of a unit
     uint64_t* bar_v = bar + 2;    // v of a unit
     uint64_t* bar_g = bar + 3;    // gate tile of a unit
     uint64_t* bar_m = bar + 4;    // MMAs
@@ -1122,21 +1158,19 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
 
     auto unit_g = [&](int u) { return u % p.G; };   // as in the scalar-gate role
     auto unit_i = [&](int u) { return u / p.G; };
-    // Copies in flight (thread 0): the k/q stages, and the single V and gate
-    // buffers (one load at a time each, the n-th completing phase n).
-    bool pend_qk[2] = {false, false};
-    int v_issued = 0, v_done = 0, g_issued = 0, g_done = 0;
-    auto issue_qk = [&](int u, int s) {
+    // Copies in flight (thread 0): the single k/q, V and gate buffers (one
+    // load at a time each, the n-th completing phase n).
+    int qk_issued = 0, qk_done = 0, v_issued = 0, v_done = 0, g_issued = 0, g_done = 0;
+    auto issue_qk = [&](int u) {
         const int bh = p.h0 + unit_g(u);
         const int y = unit_i(u) * C;
-        uint8_t* stg = sm + s * L::QK_BYTES;
-        mbar_arrive_expect_tx(&bar_qk[s], L::QK_BYTES);
+        mbar_arrive_expect_tx(bar_qk, L::QK_BYTES);
 #pragma unroll
         for (int a = 0; a < KA; ++a) {
-            tma_load_3d(tmk, &bar_qk[s], stg + a * 16384, a * 64, y, bh);
-            tma_load_3d(tmq, &bar_qk[s], stg + a * 16384 + 8192, a * 64, y, bh);
+            tma_load_3d(tmk, bar_qk, sm + a * 16384, a * 64, y, bh);
+            tma_load_3d(tmq, bar_qk, sm + a * 16384 + 8192, a * 64, y, bh);
         }
-        pend_qk[s] = true;
+        ++qk_issued;
     };
     auto issue_v = [&](int u) {
         const int bh = p.h0 + unit_g(u);
@@ -1165,12 +1199,14 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         }
     };
 
-    constexpr uint32_t ID_WU = idesc_bf16(128, 64, true, false);   // K^T TB1^T per sub-chunk, V^T TB1^T
+    constexpr uint32_t ID_WU = idesc_bf16(128, 64, true, false);   // (K o Gam)^T TB1^T, V^T TB1^T
+    constexpr uint32_t ID_NEG_N = idesc_bf16(128, DK, false, true, true);   // -(W^T K')
+    constexpr uint32_t ID_EP = idesc_bf16(128, 64, false, false);            // W^T P^T
 
     float b_nx;
     load_b(pid, b_nx);
     if (!failed && tid == 0 && pid < nunits) {
-        issue_qk(pid, 0);
+        issue_qk(pid);
         issue_v(pid);
         issue_g(pid);
     }
@@ -1179,14 +1215,9 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     for (; !failed; ++k) {
         const int u = pid + k * np;
         if (u >= nunits) break;
-        const int s = k & 1;
         const int un = u + np;
-        const uint32_t stg = sbase + s * L::QK_BYTES;
+        const uint32_t stg = sbase;   // [K;Q], rescaled in place into the row operand
         const int nvalid = T - unit_i(u) * C;   // tokens of the unit inside the sequence
-        if (tid == 0 && un < nunits) {
-            fence_proxy_async_smem();
-            issue_qk(un, s ^ 1);   // stage s^1's MMAs finished with the previous unit
-        }
         // ---- log2 gates: prefix sums inside each segment, 8-token block sums -----
         if (!wait_all(bar_g, k & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
         if (tid == 0) ++g_done;
@@ -1254,18 +1285,14 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
             cB0[b] = b > sa ? ex2(rr0[b] - Ea0) : 0.f;
             cB1[b] = b > sa ? ex2(rr1[b] - Ea1) : 0.f;
         }
-        if (seg == 0) {
-            *reinterpret_cast<float2*>(outp + S::V_OFF + c0 * 4) = make_float2(ex2(GC0), ex2(GC1));
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-                *reinterpret_cast<float2*>(sPr + a * DK + c0) = make_float2(ex2(rr0[a]), ex2(rr1[a]));
-        }
-        if (!wait_all(&bar_qk[s], (k >> 1) & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
-        if (tid == 0) pend_qk[s] = false;
+        if (seg == 0) *reinterpret_cast<float2*>(outp + S::V_OFF + c0 * 4) = make_float2(ex2(GC0), ex2(GC1));
+        if (!wait_all(bar_qk, k & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
+        if (tid == 0) ++qk_done;
         // ---- element pass over the thread's tokens and channel pair:
         //      [K;Q] o 2^(G - r_a) in place (row operand), K o 2^(r_a - G) (own
         //      column operand), K o 2^(r_b - G) (columns of later sub-chunks b),
-        //      Q o Gam and K o Gam_C/Gam into the slot ------------------------------
+        //      K o Gam_C/Gam into the slot, K o Gam and Q o Gam into the slot
+        //      buffer's -N_c and E_c tiles until those are written -----------------
         {
             const uint32_t aKQ = stg + ka * 16384;
             const uint32_t aB = sbase + L::OFF_B + ka * L::B_ATOM;
@@ -1295,7 +1322,8 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 }
                 st_shared_b32(ak, pack_bf16(kv.x * e10, kv.y * e11));
                 st_shared_b32(aq, pack_bf16(qv.x * e10, qv.y * e11));
-                st_shared_b32(aOut + S::QG_OFF + ka * 8192 + ro, pack_bf16(qv.x * h0 * cS0, qv.y * h1 * cS1));
+                st_shared_b32(aOut + S::E_OFF + ka * 8192 + ro, pack_bf16(qv.x * h0 * cS0, qv.y * h1 * cS1));
+                st_shared_b32(aOut + S::NC_OFF + ka * 8192 + ro, pack_bf16(kv.x * h0 * cS0, kv.y * h1 * cS1));
                 const float kf0 = kv.x * f0, kf1 = kv.y * f1;
                 st_shared_b32(aOut + S::KP_OFF + ka * 8192 + ro, pack_bf16(kf0 * cK0, kf1 * cK1));
 #pragma unroll
@@ -1321,7 +1349,8 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         mph ^= 1u;
         if (tid == 0 && un < nunits) {
             fence_proxy_async_smem();
-            issue_g(un);   // the column operands over the gate tile are read
+            issue_g(un);    // the column operands over the gate tile are read
+            issue_qk(un);   // and so is the row operand: the stage is free
         }
         // ---- A (rows 0-63) and P (rows 64-127). A warp's lanes 0-15 and 16-31
         //      lie in consecutive sub-chunks a0, a0 + 1: it reads both products and
@@ -1383,13 +1412,12 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         if (!wait_all(bar_v, k & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
         if (tid == 0) ++v_done;
         publish();
-        // ---- W^T = sum_a Diag(2^r_a) Kr_a^T (T diag(beta))_a^T, one product per
-        //      sub-chunk a (Kr = the row operand's k rows); Ut^T = V^T (T diag(beta))^T
+        // ---- W^T = (K o Gam)^T (T diag(beta))^T, Ut^T = V^T (T diag(beta))^T ---------
         if (tid == 0) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-                mma_bf16_ss(tmem + L::COL_W + 64 * kk, mnmaj(stg + kk * 2048, 16384), kmaj(aTB1 + kk * 32), ID_WU,
-                            false);
+                mma_bf16_ss(tmem + L::COL_W, mnmaj(aOut + S::NC_OFF + kk * 2048, 8192), kmaj(aTB1 + kk * 32), ID_WU,
+                            kk > 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16_ss(tmem + L::COL_UT, mnmaj(aV + kk * 2048, 8192), kmaj(aTB1 + kk * 32), ID_WU, kk > 0);
@@ -1401,26 +1429,49 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
             fence_proxy_async_smem();
             issue_v(un);
         }
+        // W^T as the bf16 A operand of the two products below, Ut^T into the
+        // slot; Q o Gam (column r, this thread's tokens) read before its tile is
+        // overwritten by E_c
+        float qg[32];
         if (r < DK) {
-            float w[32];
+            float x[32];
+            tmem_ld32(tlane + L::COL_W + 32 * hh, x);
+            tmem_ld_wait();
+            store_row32_bf16(sbase + L::OFF_WT, r, 4 * hh, x);
+            const uint32_t aq = aOut + S::E_OFF + (r / 64) * 8192 + (r % 8) * 2;
+            const uint32_t c8 = (r % 64) / 8;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] = 0.f;
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                float x[32];
-                tmem_ld32(tlane + L::COL_W + 64 * a + 32 * hh, x);
-                tmem_ld_wait();
-                const float f = sPr[a * DK + r];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) w[i] += f * x[i];
-            }
-            store_row32_bf16(aOut + S::W_OFF, r, 4 * hh, w);
+            for (int i = 0; i < 32; ++i) qg[i] = ld_shared_bf16(aq + sw128_off(32 * hh + i, c8));
         }
         if (r < DV) {
             float x[32];
             tmem_ld32(tlane + L::COL_UT + 32 * hh, x);
             tmem_ld_wait();
             store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, x);
+        }
+        publish();
+        // ---- -N_c = -(W^T K') and W^T P^T ------------------------------------------
+        if (tid == 0) {
+            const uint32_t aWT = sbase + L::OFF_WT;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + L::COL_N, kmaj(aWT + kk * 32), mnmaj(aOut + S::KP_OFF + kk * 2048, 8192), ID_NEG_N,
+                            kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_bf16_ss(tmem + L::COL_E, kmaj(aWT + kk * 32), kmaj(aOut + S::P_OFF + kk * 32), ID_EP, kk > 0);
+            mma_commit(bar_m);
+        }
+        if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        mph ^= 1u;
+        if (r < DK) {
+            store_neg_nc<DK>(tlane + L::COL_N, hh, aOut + S::NC_OFF, r);   // over K o Gam, read by now
+            float x[32];
+            tmem_ld32(tlane + L::COL_E + 32 * hh, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = qg[i] - x[i];
+            store_row32_bf16(aOut + S::E_OFF, r, 4 * hh, x);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -1429,8 +1480,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     }
 
     if (failed && tid == 0) {
-        for (int s2 = 0; s2 < 2; ++s2)
-            if (pend_qk[s2]) mbar_wait(&bar_qk[s2], ((s2 == (k & 1) ? k : k + 1) >> 1) & 1, 100000000ull);
+        if (qk_issued > qk_done) mbar_wait(bar_qk, (qk_issued - 1) & 1, 100000000ull);
         if (v_issued > v_done) mbar_wait(bar_v, (v_issued - 1) & 1, 100000000ull);
         if (g_issued > g_done) mbar_wait(bar_g, (g_issued - 1) & 1, 100000000ull);
     }
@@ -1514,7 +1564,9 @@ cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int R, cudaStream
 
 namespace chunk {
 
-size_t gdn_slot_bytes(int dk, int dv) { return static_cast<size_t>(3 * dk + dv) * 128 + 8192 + 512; }
+size_t gdn_slot_bytes(int dk, int dv) {
+    return 2 * static_cast<size_t>(dk) * dk + static_cast<size_t>(2 * dk + dv) * 128 + 8192 + 512;
+}
 
 int gdn_group(int BH) { return BH < kGdnMaxGroup ? BH : kGdnMaxGroup; }
 

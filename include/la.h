@@ -69,9 +69,9 @@
  * (d_k*d_v + d_k) floats) and, for
  * LA_GDN and LA_KDA, for the hand-off flags and a ring of up to 32 chunks
  * of per-chunk intermediates for each of a group of G = min(B*H, 32)
- * sequence-heads (G*32*((3*d_k+d_v)*128 + 8704) bytes plus a few KB; 76 MB
- * at G = 32, d_k = d_v = 128; a smaller workspace only makes the ring
- * shallower). The largest of these is allocated when the
+ * sequence-heads (G*32*(2*d_k*d_k + (2*d_k+d_v)*128 + 8704) bytes plus a few
+ * KB; 93 MB at G = 32, d_k = d_v = 128; a smaller workspace only makes the
+ * ring shallower). The largest of these is allocated when the
  * configuration can take the tensor-core path (bf16, d_k, d_v in {64, 128}).
  * Calls that overlap on the GPU through the same handle (different streams)
  * would share that workspace: serialize them.
