@@ -1242,8 +1242,6 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         if (tid < 64) sB[tid] = b_nx;
         load_b(un, b_nx);
         sync_conv();
-        // the slot buffer is written below: the previous unit's store has read it
-        if (k >= 1 && !wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
         // ---- cumulative log2 at the 8-token block ends Bc[b]: the segment offset,
         //      the sub-chunk references r_a = Bc[2a] (its 8th token), its start
         //      S_a = Bc[2a-1] and end E_a = Bc[2a+1], G_C = Bc[7] ----------------------
@@ -1268,31 +1266,23 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
 #pragma unroll
         for (int a = 1; a < 4; ++a)
             if (a == sa) { ra0 = rr0[a]; ra1 = rr1[a]; }
-        // Per-channel factors, every exponent <= 0: Q o Gam = q h 2^S_a and
-        // K o Gam_C/Gam = k f 2^(G_C - E_a), columns of a later sub-chunk b
-        // k f 2^(r_b - E_a), with h = 2^(G - S_a) and f = 2^(E_a - G) per
-        // element. Up to the reference token h is taken directly and f as
-        // 2^(r_a - G) 2^(E_a - r_a); after it f directly and h as
-        // 2^(G - r_a) 2^(r_a - S_a): each product joins two factors <= 1, so
-        // an underflow only hides values that are themselves negligible.
-        const float cS0 = ex2(Sa0), cS1 = ex2(Sa1);
-        const float cK0 = ex2(GC0 - Ea0), cK1 = ex2(GC1 - Ea1);
+        // Per-channel factors, every exponent <= 0: the columns of a later
+        // sub-chunk b are k f 2^(r_b - E_a) with f = 2^(E_a - G) per element,
+        // taken up to the reference token as 2^(r_a - G) 2^(E_a - r_a) and
+        // directly after it: each product joins two factors <= 1, so an
+        // underflow only hides values that are themselves negligible.
         const float cF0 = ex2(Ea0 - ra0), cF1 = ex2(Ea1 - ra1);
-        const float cH0 = ex2(ra0 - Sa0), cH1 = ex2(ra1 - Sa1);
         float cB0[4], cB1[4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             cB0[b] = b > sa ? ex2(rr0[b] - Ea0) : 0.f;
             cB1[b] = b > sa ? ex2(rr1[b] - Ea1) : 0.f;
         }
-        if (seg == 0) *reinterpret_cast<float2*>(outp + S::V_OFF + c0 * 4) = make_float2(ex2(GC0), ex2(GC1));
         if (!wait_all(bar_qk, k & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
         if (tid == 0) ++qk_done;
         // ---- element pass over the thread's tokens and channel pair:
         //      [K;Q] o 2^(G - r_a) in place (row operand), K o 2^(r_a - G) (own
-        //      column operand), K o 2^(r_b - G) (columns of later sub-chunks b),
-        //      K o Gam_C/Gam into the slot, K o Gam and Q o Gam into the slot
-        //      buffer's -N_c and E_c tiles until those are written -----------------
+        //      column operand), K o 2^(r_b - G) (columns of later sub-chunks b) ----
         {
             const uint32_t aKQ = stg + ka * 16384;
             const uint32_t aB = sbase + L::OFF_B + ka * L::B_ATOM;
@@ -1308,24 +1298,17 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 const float G0 = off0 + lp0[i], G1 = off1 + lp1[i];
                 const float e10 = ex2c(G0 - ra0), e11 = ex2c(G1 - ra1);
                 const float e20 = ex2c(ra0 - G0), e21 = ex2c(ra1 - G1);
-                float h0, h1, f0, f1;
+                float f0, f1;
                 if (t <= ref) {
-                    h0 = ex2(G0 - Sa0);
-                    h1 = ex2(G1 - Sa1);
                     f0 = e20 * cF0;
                     f1 = e21 * cF1;
                 } else {
                     f0 = ex2(Ea0 - G0);
                     f1 = ex2(Ea1 - G1);
-                    h0 = e10 * cH0;
-                    h1 = e11 * cH1;
                 }
                 st_shared_b32(ak, pack_bf16(kv.x * e10, kv.y * e11));
                 st_shared_b32(aq, pack_bf16(qv.x * e10, qv.y * e11));
-                st_shared_b32(aOut + S::E_OFF + ka * 8192 + ro, pack_bf16(qv.x * h0 * cS0, qv.y * h1 * cS1));
-                st_shared_b32(aOut + S::NC_OFF + ka * 8192 + ro, pack_bf16(kv.x * h0 * cS0, kv.y * h1 * cS1));
                 const float kf0 = kv.x * f0, kf1 = kv.y * f1;
-                st_shared_b32(aOut + S::KP_OFF + ka * 8192 + ro, pack_bf16(kf0 * cK0, kf1 * cK1));
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     const uint32_t ab = aB + sw128_off(L::b_row(b) + t, ch) + bo;
@@ -1347,10 +1330,52 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;
+        // the slot buffer is written from here on: the previous unit's store has read it
+        if (k >= 1 && !wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
+        // ---- slot pass: K o Gam and Q o Gam are the row operand times 2^r_a, and
+        //      K o Gam_C/Gam is the last sub-chunk's column operand (k 2^(r_3 - G),
+        //      all 64 rows) times 2^(G_C - r_3). Each joins a factor <= 1 to one
+        //      within eight tokens of decay of 1, so every value stays in range
+        //      (or is negligible where a factor underflows). K o Gam and Q o Gam
+        //      wait in the -N_c and E_c tiles until those are written. ----------------
+        {
+            // r_a, r_3 and G_C again from the block sums (fewer live registers)
+            float ra0s = 0.f, ra1s = 0.f, r30 = 0.f, r31 = 0.f, gc0 = 0.f, gc1 = 0.f;
+            {
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    const float2 x = *reinterpret_cast<const float2*>(sBlk + b * DK + c0);
+                    s0 += x.x;
+                    s1 += x.y;
+                    if (b == 2 * sa) { ra0s = s0; ra1s = s1; }
+                    if (b == 6) { r30 = s0; r31 = s1; }
+                }
+                gc0 = s0;
+                gc1 = s1;
+            }
+            const float ca0 = ex2(ra0s), ca1 = ex2(ra1s);
+            const float cz0 = ex2(gc0 - r30), cz1 = ex2(gc1 - r31);
+            const uint32_t aKQ = stg + ka * 16384;
+            const uint32_t aB3 = sbase + L::OFF_B + ka * L::B_ATOM;
+#pragma unroll
+            for (int i = 0; i < SL; ++i) {
+                const int t = seg * SL + i;
+                const uint32_t ro = sw128_off(t, ch) + bo;
+                const float2 rk = unpack_bf16(ld_shared_b32(aKQ + ro));
+                const float2 rq = unpack_bf16(ld_shared_b32(aKQ + sw128_off(64 + t, ch) + bo));
+                const float2 b3 = unpack_bf16(ld_shared_b32(aB3 + sw128_off(L::b_row(3) + t, ch) + bo));
+                st_shared_b32(aOut + S::NC_OFF + ka * 8192 + ro, pack_bf16(rk.x * ca0, rk.y * ca1));
+                st_shared_b32(aOut + S::E_OFF + ka * 8192 + ro, pack_bf16(rq.x * ca0, rq.y * ca1));
+                st_shared_b32(aOut + S::KP_OFF + ka * 8192 + ro, pack_bf16(b3.x * cz0, b3.y * cz1));
+            }
+            if (seg == 0) *reinterpret_cast<float2*>(outp + S::V_OFF + c0 * 4) = make_float2(ex2(gc0), ex2(gc1));
+        }
+        sync_conv();   // the stage and the column operands are read
         if (tid == 0 && un < nunits) {
             fence_proxy_async_smem();
-            issue_g(un);    // the column operands over the gate tile are read
-            issue_qk(un);   // and so is the row operand: the stage is free
+            issue_g(un);    // into the gate tile, under the column operands
+            issue_qk(un);   // into the stage
         }
         // ---- A (rows 0-63) and P (rows 64-127). A warp's lanes 0-15 and 16-31
         //      lie in consecutive sub-chunks a0, a0 + 1: it reads both products and
