@@ -83,6 +83,7 @@ constexpr int kConv = 256;              // converting threads (8 warps)
 constexpr int kThreads = kConv + 64;    // + a control warp and a flag warp (chain CTAs)
 constexpr uint32_t kBarConv = 1;        // named barrier of the converting warps
 constexpr uint32_t kBarInit = 2;        // prep CTAs: converting warps and the store warp, once
+constexpr int kIssuer = 64;             // prep CTAs: the thread issuing the first MMA of a unit
 
 __host__ __device__ constexpr uint32_t align1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -143,8 +144,8 @@ struct PrepLayout {
     static constexpr uint32_t OFF_OUT = OFF_TB2 + 8192;  // the slot being assembled / stored
     static constexpr uint32_t OFF_AS = OFF_OUT + align1024(S::BYTES);   // fp32 [64][kAStride]
     static constexpr uint32_t OFF_RS = OFF_AS + C * kAStride * 4;       // fp32 [32][kRStride]
-    static constexpr uint32_t OFF_MISC = OFF_RS + 32 * 40 * 4;          // log2 prefix, beta, beta gam, gam
-    static constexpr uint32_t OFF_BAR = OFF_MISC + 4 * 64 * 4;
+    static constexpr uint32_t OFF_MISC = OFF_RS + 32 * 40 * 4;          // log2 prefix, beta, beta gam, gam, next gates and betas
+    static constexpr uint32_t OFF_BAR = OFF_MISC + 6 * 64 * 4;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
     // W^T as a bf16 K-major A operand [dk][64 j] goes over the solve matrix,
     // which is dead by then
@@ -184,8 +185,8 @@ struct PrepLayoutKda {
     static constexpr uint32_t OFF_AS = OFF_OUT + align1024(S::BYTES);   // fp32 [64][kAStride]
     static constexpr uint32_t OFF_RS = OFF_AS + C * kAStride * 4;        // fp32 [32][kRStride]
     static constexpr uint32_t OFF_BLK = OFF_RS + 32 * 40 * 4;            // log2-gate sums of 8-token blocks [8][DK]
-    static constexpr uint32_t OFF_MISC = OFF_BLK + 8 * DK * 4;           // beta [64]
-    static constexpr uint32_t OFF_BAR = OFF_MISC + 64 * 4;
+    static constexpr uint32_t OFF_MISC = OFF_BLK + 8 * DK * 4;           // beta [64], next unit's beta [64]
+    static constexpr uint32_t OFF_BAR = OFF_MISC + 2 * 64 * 4;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
     // W^T as a bf16 K-major A operand goes over the solve matrix (dead by
     // then); K o Gam (the W product's operand) and Q o Gam wait in the slot
@@ -760,6 +761,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     float* sB = sG2 + 64;                                        // beta (0 on padded tokens)
     float* sBG = sB + 64;                                        // beta_t gam_t
     float* sGam = sBG + 64;                                      // gam_t
+    float* sGin = sGam + 64;                                     // next unit's gates, then betas [2][64]
     uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint64_t* bar_m = bar_full + 2;
     uint64_t* bar_test = bar_full + 3;
@@ -834,17 +836,20 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         for (int a = 0; a < VA; ++a) tma_load_3d(tmv, &bar_full[s], stg + L::QK_BYTES + a * 8192, a * 64, y, bh);
         pending[s] = true;
     };
-    // gate and beta of a unit, one token per thread (threads 0-63)
-    auto load_gb = [&](int u, float& gv, float& bv) {
-        gv = 1.f;
-        bv = 0.f;
+    // gate and beta of a unit, one token per thread (threads 0-63), copied
+    // asynchronously into shared memory a unit ahead (padded tokens: 1 and 0)
+    auto load_gb = [&](int u) {
         if (u < nunits && tid < 64) {
             const int bh = p.h0 + unit_g(u);
             const int t = unit_i(u) * C + tid;
             if (t < T) {
-                gv = p.gate[static_cast<size_t>(bh) * T + t];
-                bv = p.beta[static_cast<size_t>(bh) * T + t];
+                cp_async4(smem_u32(sGin + tid), p.gate + static_cast<size_t>(bh) * T + t);
+                cp_async4(smem_u32(sGin + 64 + tid), p.beta + static_cast<size_t>(bh) * T + t);
+            } else {
+                sGin[tid] = 1.f;
+                sGin[64 + tid] = 0.f;
             }
+            cp_async_commit();
         }
     };
 
@@ -853,8 +858,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     constexpr uint32_t ID_NEG_N = idesc_bf16(128, DK, false, true, true);   // -(W^T K')
     constexpr uint32_t ID_EP = idesc_bf16(128, 64, false, false);            // W^T P^T
 
-    float g_nx, b_nx;
-    load_gb(pid, g_nx, b_nx);
+    load_gb(pid);
     if (!failed && tid == 0 && pid < nunits) issue_load(pid, 0);
     uint32_t mph = 0;
     int k = 0;
@@ -873,10 +877,20 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         }
         if (!wait_all(&bar_full[s], (k >> 1) & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
         if (tid == 0) pending[s] = false;
+        // [K;Q] K^T, issued by a thread outside the warps of the gate prefix
+        if (tid == kIssuer) {
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+                const uint64_t d = kmaj(stg + (kk / 4) * 16384 + (kk % 4) * 32);
+                mma_bf16_ss(tmem + L::COL_G, d, d, ID_G, kk > 0);
+            }
+            mma_commit(bar_m);
+        }
 
-        // ---- gate prefix sums (log2 domain) and [K;Q] K^T --------------------------
+        // ---- gate prefix sums (log2 domain) -----------------------------------------
         if (tid < 64) {
-            const float gv = g_nx, bv = b_nx;
+            cp_async_wait();   // this thread's own copies
+            const float gv = sGin[tid], bv = sGin[64 + tid];
             float lg = lg2(gv);
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -886,15 +900,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
             sG2[tid] = lg;
             sB[tid] = bv;
         }
-        load_gb(un, g_nx, b_nx);
-        if (tid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < DK / 16; ++kk) {
-                const uint64_t d = kmaj(stg + (kk / 4) * 16384 + (kk % 4) * 32);
-                mma_bf16_ss(tmem + L::COL_G, d, d, ID_G, kk > 0);
-            }
-            mma_commit(bar_m);
-        }
+        load_gb(un);   // the values above are read
         sync_conv();
         if (tid >= 32 && tid < 64) sG2[tid] += sG2[31];
         sync_conv();
@@ -994,21 +1000,15 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;
-        // W^T as the bf16 A operand of the two products below; Ut^T into the slot
+        // W^T as the bf16 A operand of the two products below
         if (r < DK) {
             float x[32];
             tmem_ld32(tlane + L::COL_W + 32 * hh, x);
             tmem_ld_wait();
             store_row32_bf16(sbase + L::OFF_WT, r, 4 * hh, x);
         }
-        if (r < DV) {
-            float x[32];
-            tmem_ld32(tlane + L::COL_UT + 32 * hh, x);
-            tmem_ld_wait();
-            store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, x);
-        }
         publish();
-        // ---- -N_c = -(W^T K') and W^T P^T ------------------------------------------
+        // ---- -N_c = -(W^T K') and W^T P^T; Ut^T into the slot meanwhile -------------
         if (tid == 0) {
             const uint32_t aWT = sbase + L::OFF_WT;
 #pragma unroll
@@ -1019,6 +1019,12 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16_ss(tmem + L::COL_E, kmaj(aWT + kk * 32), kmaj(aOut + S::P_OFF + kk * 32), ID_EP, kk > 0);
             mma_commit(bar_m);
+        }
+        if (r < DV) {
+            float x[32];
+            tmem_ld32(tlane + L::COL_UT + 32 * hh, x);
+            tmem_ld_wait();
+            store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, x);
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;
@@ -1094,6 +1100,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     float* Rs = reinterpret_cast<float*>(sm + L::OFF_RS);
     float* sBlk = reinterpret_cast<float*>(sm + L::OFF_BLK);   // log2-gate sum of each 8-token block [8][DK]
     float* sB = reinterpret_cast<float*>(sm + L::OFF_MISC);    // beta (0 on padded tokens)
+    float* sBin = sB + 64;                                      // next unit's beta, copied ahead
     const float* sGate = reinterpret_cast<const float*>(sm + L::OFF_GATE);
     uint8_t* outp = sm + L::OFF_OUT;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
@@ -1190,12 +1197,16 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         bulk_load(sm + L::OFF_GATE, p.gate + (static_cast<size_t>(bh) * T + y) * DK, bytes, bar_g);
         ++g_issued;
     };
-    auto load_b = [&](int u, float& bv) {
-        bv = 0.f;
+    auto load_b = [&](int u) {   // asynchronously, one token per thread (threads 0-63)
         if (u < nunits && tid < 64) {
             const int bh = p.h0 + unit_g(u);
             const int t = unit_i(u) * C + tid;
-            if (t < T) bv = p.beta[static_cast<size_t>(bh) * T + t];
+            if (t < T) {
+                cp_async4(smem_u32(sBin + tid), p.beta + static_cast<size_t>(bh) * T + t);
+                cp_async_commit();
+            } else {
+                sBin[tid] = 0.f;
+            }
         }
     };
 
@@ -1203,8 +1214,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     constexpr uint32_t ID_NEG_N = idesc_bf16(128, DK, false, true, true);   // -(W^T K')
     constexpr uint32_t ID_EP = idesc_bf16(128, 64, false, false);            // W^T P^T
 
-    float b_nx;
-    load_b(pid, b_nx);
+    load_b(pid);
     if (!failed && tid == 0 && pid < nunits) {
         issue_qk(pid);
         issue_v(pid);
@@ -1239,8 +1249,11 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 *reinterpret_cast<float2*>(sBlk + (blk0 + 1) * DK + c0) =
                     make_float2(lp0[SL - 1] - lp0[7], lp1[SL - 1] - lp1[7]);
         }
-        if (tid < 64) sB[tid] = b_nx;
-        load_b(un, b_nx);
+        if (tid < 64) {
+            cp_async_wait();   // this thread's own copy
+            sB[tid] = sBin[tid];
+        }
+        load_b(un);
         sync_conv();
         // ---- cumulative log2 at the 8-token block ends Bc[b]: the segment offset,
         //      the sub-chunk references r_a = Bc[2a] (its 8th token), its start
@@ -1319,7 +1332,8 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         }
         publish();
         // ---- [K;Q] B^T on the tensor cores: the four column operands stacked
-        //      into one N = 160 product ------------------------------------------------
+        //      into one N = 160 product; the slot pass below reads the same
+        //      operands meanwhile --------------------------------------------------------
         if (tid == 0) {
             constexpr uint32_t idg = idesc_bf16(128, 160, false, false);
 #pragma unroll
@@ -1328,8 +1342,6 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                             kmaj(sbase + L::OFF_B + (kk / 4) * L::B_ATOM + (kk % 4) * 32), idg, kk > 0);
             mma_commit(bar_m);
         }
-        if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
-        mph ^= 1u;
         // the slot buffer is written from here on: the previous unit's store has read it
         if (k >= 1 && !wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
         // ---- slot pass: K o Gam and Q o Gam are the row operand times 2^r_a, and
@@ -1371,7 +1383,10 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
             }
             if (seg == 0) *reinterpret_cast<float2*>(outp + S::V_OFF + c0 * 4) = make_float2(ex2(gc0), ex2(gc1));
         }
-        sync_conv();   // the stage and the column operands are read
+        // the pair products are done, and the slot pass has read the stage and
+        // the column operands (the barrier inside)
+        if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        mph ^= 1u;
         if (tid == 0 && un < nunits) {
             fence_proxy_async_smem();
             issue_g(un);    // into the gate tile, under the column operands
@@ -1454,9 +1469,8 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
             fence_proxy_async_smem();
             issue_v(un);
         }
-        // W^T as the bf16 A operand of the two products below, Ut^T into the
-        // slot; Q o Gam (column r, this thread's tokens) read before its tile is
-        // overwritten by E_c
+        // W^T as the bf16 A operand of the two products below; Q o Gam (column
+        // r, this thread's tokens) read before its tile is overwritten by E_c
         float qg[32];
         if (r < DK) {
             float x[32];
@@ -1467,12 +1481,6 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
             const uint32_t c8 = (r % 64) / 8;
 #pragma unroll
             for (int i = 0; i < 32; ++i) qg[i] = ld_shared_bf16(aq + sw128_off(32 * hh + i, c8));
-        }
-        if (r < DV) {
-            float x[32];
-            tmem_ld32(tlane + L::COL_UT + 32 * hh, x);
-            tmem_ld_wait();
-            store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, x);
         }
         publish();
         // ---- -N_c = -(W^T K') and W^T P^T ------------------------------------------
@@ -1486,6 +1494,12 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16_ss(tmem + L::COL_E, kmaj(aWT + kk * 32), kmaj(aOut + S::P_OFF + kk * 32), ID_EP, kk > 0);
             mma_commit(bar_m);
+        }
+        if (r < DV) {   // Ut^T into the slot while the products run
+            float x[32];
+            tmem_ld32(tlane + L::COL_UT + 32 * hh, x);
+            tmem_ld_wait();
+            store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, x);
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;

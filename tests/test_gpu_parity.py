@@ -238,6 +238,14 @@ def test_kda_strong_and_mixed_decays(d):
     assert_parity(w, inp, chunk=64)
 
 
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_two_head_groups(variant):
+    # 40 sequence-heads: one cooperative launch for the first 32, one for the
+    # other 8, each with a fresh hand-off epoch over the same workspace
+    w = base(variant, 64).with_(B=5, H=8, T=130)
+    assert_parity(w, W.draw(w, seed=40), chunk=64, launches=2)
+
+
 # ------------------------------------------------------------- prefill from host memory
 
 @pytest.mark.parametrize("variant", ["norm", "gla", "gdn", "norm_decay", "kda"])

@@ -71,6 +71,17 @@ def test_noalloc_matches_la_forward_twice(variant):
             assert float(np.max(np.abs(den - den_ref) / den_ref)) <= TOL["bf16"]
 
 
+def test_noalloc_gdn_shallow_ring_is_bit_identical():
+    # 32 sequence-heads of d = 128 leave the 16 MiB static scratch room for a
+    # ring of only a few chunks per head, so the prep CTAs wait for ring
+    # positions the chain CTAs free; la_forward's ring is 16 chunks deep. The
+    # arithmetic of every chunk is the same either way.
+    w = W.small(W.GDN_B2H16_T8192_D128, B=2, H=16, T=1000, dk=128, dv=128)
+    o, s, _, o_ref, s_ref, _ = _run_both(w, 3)
+    assert np.array_equal(o, o_ref)
+    assert np.array_equal(s, s_ref)
+
+
 def test_noalloc_rejects_what_it_cannot_run():
     dev = torch.cuda.current_device()
     x = torch.zeros(16, device="cuda")
