@@ -154,6 +154,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, dist, device: str) -> float:
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step: float, steps: int, n_ranks: int, max_ms: float) -> float:
+    """Units all ranks processed (each rank runs the whole workload: replicas)
+    per second of the slowest rank."""
+    return units_per_step * steps * n_ranks / (max_ms * 1e-3)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -392,13 +408,9 @@ def gpu_arm(args):
             r.step()
         torch.cuda.synchronize()
     clocks = sampler.stop()
-    max_ms = total_ms
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
+    max_ms = max_over_ranks(total_ms, dist, "cuda")
     n = ws
-    value = w.tokens * args.steps * n / (max_ms * 1e-3)
+    value = job_throughput(w.tokens, args.steps, n, max_ms)
     line = {
         "metric": "prefill tokens/s (B*T)", "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": n, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
