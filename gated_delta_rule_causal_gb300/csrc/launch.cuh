@@ -42,4 +42,24 @@ cudaError_t launch_coop(Kern kern, unsigned grid, unsigned block, size_t smem, c
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Launch in thread-block clusters of `cluster` CTAs along x (the grid is a
+// multiple of it); the CTAs of one cluster are resident together.
+template <typename Kern, typename... Args>
+cudaError_t launch_cluster(Kern kern, unsigned grid, unsigned cluster, unsigned block, size_t smem, cudaStream_t s,
+                           Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace la

@@ -47,6 +47,11 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
         *what = "chunked prefill launch";
         return chunk::launch_gdn(a, m, s);
     }
+    if (a.variant == kNorm && !a.gate && !(a.flags & 0x2u) &&
+        chunk::seg_fits(a.BH, a.T, a.dk, a.dv, a.sm_count)) {
+        *what = "chunked prefill launch";
+        return chunk::launch_seg(a, m, s);
+    }
     if (!(a.flags & 0x2u) && a.workspace && chunk::par_fits(a.BH, a.T, a.dk, a.dv, a.ws_bytes)) {
         *what = "chunked prefill launch";
         return chunk::launch_par(a, m, s);

@@ -32,6 +32,14 @@ int gdn_group(int BH);
 size_t gdn_workspace_bytes(int BH, int dk, int dv, int W);
 cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s);
 
+// Normalized, d_k = d_v = 64, no decay: one launch in which each CTA runs a
+// segment of up to four 128-token blocks of one sequence-head, and the
+// segments of a sequence-head (a thread-block cluster of at most 8) pass
+// their totals through distributed shared memory. Fits when every
+// sequence-head splits into such segments; needs no workspace.
+bool seg_fits(int BH, int T, int dk, int dv, int sm_count);
+cudaError_t launch_seg(const FwdArgs& a, const Maps& m, cudaStream_t s);
+
 // Normalized / per-channel gated: three fully parallel phases (chunk
 // summaries, a scan over the chunks, outputs) when the per-chunk states of
 // the whole problem fit in the workspace and comfortably in L2.

@@ -1,0 +1,462 @@
+// Normalized elu+1 prefill (d_k = d_v = 64) in one cooperative launch.
+//
+// "Linear attention and Hyena" §11.2-11.3: with phi = elu + 1, the state
+// S_t = S_{t-1} + phi(k_t) v_t^T and z_t = z_{t-1} + phi(k_t) give
+// o_t = phi(q_t)^T S_t / phi(q_t)^T z_t, and over a block of tokens the
+// same outputs come from the block's causal scores plus the state that
+// entered it. Here every CTA owns one segment of at most kMaxSub blocks of
+// B = 128 tokens of one sequence-head. With X = S^T ([d_v][d_k]) and, per
+// block j of the segment,
+//   A_j = [V_j | 1]^T phi(K_j)             (rows 0..63: dX^T, rows 64..: dz)
+//   P_j = L o phi(Q_j) phi(K_j)^T          (L: the causal mask)
+//   O_j = phi(Q_j) [X_loc | z_loc]^T + P_j [V_j | 1]
+// where X_loc, z_loc sum A_i over the segment's earlier blocks (and the
+// initial state in the first segment), kept in fp32 registers. Column d_v of
+// O_j is the normalizer of each token, so the quotient needs no extra pass.
+// The "1" columns and rows come from a block of ones in shared memory that
+// the MN-major operand descriptors reach through their leading-byte offset.
+//
+// The segments of one sequence-head form one thread-block cluster (at most
+// kMaxSeg CTAs). Each leaves its total (X, z) in its shared memory; after one
+// cluster barrier, segment s sums the totals of segments 0..s-1 through
+// distributed shared memory (the state entering it), then adds
+// phi(Q_j) [X_in | z_in]^T to the outputs it held in tensor memory. Clusters
+// never wait on one another, every other wait is bounded, and a CTA that
+// failed says so next to its total.
+
+#include "prefill.h"
+#include "prefill_impl.cuh"
+#include "launch.cuh"
+
+namespace la {
+namespace seg {
+
+using chunk::elu1;
+using chunk::kmaj;
+using chunk::ld_shared_v4;
+using chunk::mnmaj;
+using chunk::st_shared_v4;
+using chunk::store_row32_bf16;
+
+constexpr int B = 128;        // tokens per block
+constexpr int D = 64;         // d_k = d_v
+constexpr int kMaxSub = 4;    // blocks per segment: four held outputs + scores fill tensor memory
+constexpr int kMaxSeg = 8;    // segments per sequence-head: the portable cluster size
+constexpr int kWorkers = 256;             // 8 warps: conversions and tensor-memory reads
+constexpr int kThreads = kWorkers + 32;   // + the warp that issues every MMA and TMA copy
+constexpr int SSZ = D * D + D;   // one state: X or S plus z
+
+struct Params {
+    const float* state_in;     // S [BH][D][D] then z [D] per head, or NULL
+    float* state_out;          // same layout, or NULL
+    float* den_out;            // [BH][T], or NULL
+    int BH, T, nsub, nseg, per;   // blocks per head, segments (= cluster size) per head, blocks per segment
+    unsigned flags;
+    int* status;
+};
+
+// Shared memory (offsets from the 1024-aligned base).
+struct Layout {
+    static constexpr uint32_t Q = 0;                        // phi(Q_j), kMaxSub tiles [128 t][64] K-major
+    static constexpr uint32_t STG = Q + kMaxSub * 16384;    // 3 stages of K (phi(K) in place) and V, then the output tiles
+    static constexpr uint32_t STAGE = 32768;
+    static constexpr int NSTAGE = 3;
+    static constexpr uint32_t P = STG + NSTAGE * STAGE;     // scores bf16, 2 atoms [128 t][64 i]; then the
+                                                            // segment's total fp32 [65][64] and its ok word
+    static constexpr uint32_t X = P + 32768;                // [X_loc | z_loc]^T, [80 rows][64] K-major; then [X_in | z_in]^T
+    static constexpr uint32_t ONES = X + 10240;             // 16 KB of bf16 ones
+    static constexpr uint32_t BAR = ONES + 16384;
+    static constexpr uint32_t BYTES = BAR + 128;
+    static constexpr uint32_t SMEM = BYTES + 1024;
+    // tensor memory: O_j at 96 j (80 columns); the scores at COL_PA. A_j goes
+    // to the next block's output columns (still free), the last one to COL_PA.
+    static constexpr uint32_t COL_PA = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+static_assert(Layout::SMEM <= 232448, "shared memory budget");
+static_assert(Layout::ONES > Layout::STG + (Layout::NSTAGE - 1) * Layout::STAGE + 16384, "ones block above every value tile");
+static_assert(kMaxSub <= Layout::NSTAGE + 1, "a block reloads a stage at most once");
+
+// barriers
+enum { kBarQ = 0, kBarLd = kMaxSub, kBarP = kMaxSub + Layout::NSTAGE, kBarO, kBarFin, kBarHook, kNumBar };
+
+__global__ void __launch_bounds__(kThreads, 1)
+seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+           const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const Params p) {
+    using L = Layout;
+    constexpr int NS = L::NSTAGE;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (sbase - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool worker = tid < kWorkers;
+    const bool issuer = tid == kWorkers;     // lane 0 of the last warp
+    const int r = 32 * (warp & 3) + lane;    // tensor-memory lane: token, or state row
+    const int hh = (warp >> 2) & 1;          // column half
+    const bool rowv = worker && (warp & 3) < 2;    // state rows v = r < 64
+    const bool rowz = worker && (warp & 3) == 2;   // normalizer rows (all alike); r == 64 writes
+    const int bh = blockIdx.x / p.nseg, sg = static_cast<int>(cluster_ctarank());   // = blockIdx.x % nseg
+    const int j0 = sg * p.per;
+    const int nj = min(p.per, p.nsub - j0);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumBar);
+    const uint32_t aP = sbase + L::P, aX = sbase + L::X, aONES = sbase + L::ONES;
+    const bool hook = (p.flags & 0x100u) != 0;   // test hook: a wait nothing will satisfy, 1 ms limit
+
+    // loads in flight, for a clean exit after a failed wait (issuing thread): Q
+    // tiles not yet waited for, and per stage the loads issued and waited for
+    unsigned q_pending = 0;
+    int kv_iss[NS] = {0, 0, 0}, kv_done[NS] = {0, 0, 0};
+    auto load_kv = [&](int j) {
+        const int t0 = (j0 + j) * B, st = j % NS;
+        ++kv_iss[st];
+        uint8_t* stg = sm + L::STG + st * L::STAGE;
+        mbar_arrive_expect_tx(&bar[kBarLd + st], 32768);
+        tma_load_3d(&tmk, &bar[kBarLd + st], stg, 0, t0, bh);
+        tma_load_3d(&tmk, &bar[kBarLd + st], stg + 8192, 0, t0 + 64, bh);
+        tma_load_3d(&tmv, &bar[kBarLd + st], stg + 16384, 0, t0, bh);
+        tma_load_3d(&tmv, &bar[kBarLd + st], stg + 24576, 0, t0 + 64, bh);
+    };
+    auto load_q = [&](int j) {
+        const int t0 = (j0 + j) * B;
+        mbar_arrive_expect_tx(&bar[kBarQ + j], 16384);
+        tma_load_3d(&tmq, &bar[kBarQ + j], sm + L::Q + j * 16384, 0, t0, bh);
+        tma_load_3d(&tmq, &bar[kBarQ + j], sm + L::Q + j * 16384 + 8192, 0, t0 + 64, bh);
+    };
+    if (issuer) {   // barriers, then the first tiles on their way before anything else
+        for (int i = 0; i < kNumBar; ++i) mbar_init(&bar[i], 1);
+        fence_mbar_init();
+        if (!hook) {
+            load_q(0);
+            load_kv(0);
+            for (int j = 1; j < nj && j < NS; ++j) load_kv(j);
+            for (int j = 1; j < nj; ++j) load_q(j);
+            q_pending = (1u << nj) - 1u;
+        }
+    }
+    {   // ones block; the state tile starts at zero (rows past 64 stay zero)
+        const uint32_t one2 = 0x3F803F80u;
+        for (int i = tid; i < 16384 / 16; i += kThreads) st_shared_v4(aONES + 16 * i, one2, one2, one2, one2);
+        for (int i = tid; i < 10240 / 16; i += kThreads) st_shared_v4(aX + 16 * i, 0u, 0u, 0u, 0u);
+        if (issuer) {
+            tma_prefetch_desc(&tmo);
+        }
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+
+    int status_bits = 0;
+    bool failed = false;
+    if (hook) {
+        const bool ok = mbar_wait(&bar[kBarHook], 0, 1000000ull);
+        if (__syncthreads_or(!ok)) { status_bits |= kStatusTestHook; failed = true; }
+    }
+
+    // running total of this thread's state row (columns hh*32..hh*32+31):
+    // X rows v = r (rowv) or z (rowz); the first segment starts from state_in
+    float R[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) R[i] = 0.f;
+    if (sg == 0 && p.state_in && (rowv || rowz)) {
+        const float* si = p.state_in + static_cast<size_t>(bh) * SSZ;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) R[i] = rowv ? si[(hh * 32 + i) * D + r] : si[D * D + hh * 32 + i];
+    }
+    auto write_state_tile = [&](const float* x) {
+        if (rowv) store_row32_bf16(aX, r, 4 * hh, x);
+        else if (rowz && lane == 0) store_row32_bf16(aX, 64, 4 * hh, x);
+    };
+    auto read_a = [&](uint32_t col) {   // R += A (tensor memory rows 0..95 at `col`)
+        if (rowv || rowz) {
+            float a[32];
+            tmem_ld32(tlane + col + hh * 32, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) R[i] += a[i];
+        }
+    };
+    // phi(Q_j), phi(K_j) in place once block j has landed; key rows past T
+    // are zero (phi(0) = 1)
+    auto convert = [&](int j) -> bool {
+        const bool ok = !worker || (mbar_wait(&bar[kBarQ + j], 0, kWaitLimitNs) &&
+                                    mbar_wait(&bar[kBarLd + j % NS], (j / NS) & 1, kWaitLimitNs));
+        if (__syncthreads_or(!ok)) return false;
+        if (issuer) { q_pending &= ~(1u << j); ++kv_done[j % NS]; }
+        if (!worker) return true;
+        const int nvalid = min(B, p.T - (j0 + j) * B);
+        const uint32_t aQ = sbase + L::Q + j * 16384, aK = sbase + L::STG + (j % NS) * L::STAGE;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + kWorkers * i;   // 16-byte chunk: row e / 8
+            const uint32_t qa = aQ + 16 * e, ka = aK + 16 * e;
+            const uint4 uq = ld_shared_v4(qa), uk = ld_shared_v4(ka);
+            const float2 a0 = unpack_bf16(uq.x), a1 = unpack_bf16(uq.y), a2 = unpack_bf16(uq.z), a3 = unpack_bf16(uq.w);
+            st_shared_v4(qa, pack_bf16(elu1(a0.x), elu1(a0.y)), pack_bf16(elu1(a1.x), elu1(a1.y)),
+                         pack_bf16(elu1(a2.x), elu1(a2.y)), pack_bf16(elu1(a3.x), elu1(a3.y)));
+            if ((e >> 3) < nvalid) {
+                const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z),
+                             b3 = unpack_bf16(uk.w);
+                st_shared_v4(ka, pack_bf16(elu1(b0.x), elu1(b0.y)), pack_bf16(elu1(b1.x), elu1(b1.y)),
+                             pack_bf16(elu1(b2.x), elu1(b2.y)), pack_bf16(elu1(b3.x), elu1(b3.y)));
+            } else {
+                st_shared_v4(ka, 0u, 0u, 0u, 0u);
+            }
+        }
+        return true;
+    };
+    auto sync_mma = [&]() {   // generic smem writes and tensor-memory reads before the next MMAs
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+
+    const uint32_t ID_P = idesc_bf16(128, 128, false, false);
+    const uint32_t ID_O = idesc_bf16(128, 80, false, false);
+    const uint32_t ID_PV = idesc_bf16(128, 80, false, true);
+    const uint32_t ID_A = idesc_bf16(128, 64, true, true);
+    auto issue_batch1 = [&](int j) {   // scores, the state part of O_j and (not last) A_j
+        const uint32_t aQ = sbase + L::Q + j * 16384;
+        const uint32_t aK = sbase + L::STG + (j % NS) * L::STAGE, aV = aK + 16384;
+        const uint32_t dO = tmem + 96 * j;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + L::COL_PA, kmaj(aQ + kk * 32), kmaj(aK + kk * 32), ID_P, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dO, kmaj(aQ + kk * 32), kmaj(aX + kk * 32), ID_O, kk > 0);
+        if (j + 1 < nj) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ss(dO + 96, mnmaj(aV + kk * 2048, aONES - aV), mnmaj(aK + kk * 2048, 8192), ID_A, kk > 0);
+        }
+        mma_commit(&bar[kBarP]);
+    };
+    auto issue_batch2 = [&](int j) {   // the score part of O_j (and the last block's A_j)
+        const uint32_t aK = sbase + L::STG + (j % NS) * L::STAGE, aV = aK + 16384;
+        const uint32_t dO = tmem + 96 * j;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(dO, kmaj(aP + (kk / 4) * 16384 + (kk % 4) * 32), mnmaj(aV + kk * 2048, aONES - aV), ID_PV, 1);
+        if (j + 1 == nj) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ss(tmem + L::COL_PA, mnmaj(aV + kk * 2048, aONES - aV), mnmaj(aK + kk * 2048, 8192), ID_A, kk > 0);
+        }
+        mma_commit(&bar[kBarO]);
+    };
+    if (!failed) {
+        write_state_tile(R);
+        if (!convert(0)) { status_bits |= kStatusTmaWait; failed = true; }
+    }
+    if (!failed) {
+        sync_mma();
+        if (issuer) issue_batch1(0);
+    }
+    // Block j: while batch 1 runs, block j+1 converts; then the masked
+    // scores, A_j into the running total and the next state tile; then the
+    // issuer queues batch 2 of block j and batch 1 of block j+1 together.
+    for (int j = 0; j < nj && !failed; ++j) {
+        const bool last = j + 1 == nj;
+        if (!last && !convert(j + 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
+        {
+            // batch 1 of block j done, and with it batch 2 of block j-1
+            bool ok = true;
+            if (worker || (j >= 1 && j + 2 < nj)) {
+                ok = mbar_wait(&bar[kBarP], j & 1, kWaitLimitNs);
+                if (j > 0) ok = ok && mbar_wait(&bar[kBarO], (j - 1) & 1, kWaitLimitNs);
+            }
+            tc_fence_after();
+            if (issuer && ok && j >= 1 && j + 2 < nj) load_kv(j + 2);   // into block j-1's stage
+            if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; break; }
+        }
+        if (worker) {   // causal mask, bf16 scores: thread (t, hh) holds key columns hh*64..hh*64+63
+            const int t = r;
+            float x[32];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                tmem_ld32(tlane + L::COL_PA + hh * 64 + 32 * b, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (hh * 64 + 32 * b + i > t) x[i] = 0.f;
+                store_row32_bf16(aP + hh * 16384, t, 4 * b, x);
+            }
+        }
+        if (!last) {   // the state entering block j+1
+            read_a(96 * (j + 1));
+            write_state_tile(R);
+        }
+        sync_mma();
+        if (issuer) {
+            issue_batch2(j);
+            if (!last) issue_batch1(j + 1);
+        }
+    }
+
+    // ---- the segment's total, the state entering it, and the outputs
+    if (!failed) {
+        const bool ok = !worker || mbar_wait(&bar[kBarO], (nj - 1) & 1, kWaitLimitNs);
+        tc_fence_after();
+        if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; }
+    }
+    if (!failed) read_a(L::COL_PA);
+    // the total to this CTA's shared memory as [16 column groups][65 rows][4]
+    // floats (rows 0..63 X, row 64 z; a warp's 16-byte accesses fall on
+    // consecutive addresses), then whether it is valid; the scores are done with
+    const uint32_t aTOT = sbase + L::P;
+    float* tot = reinterpret_cast<float*>(sm + L::P);
+    if (!failed && (rowv || (rowz && lane == 0))) {
+        const int row = rowv ? r : D;
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(tot + ((hh * 8 + i / 4) * (D + 1) + row) * 4) =
+                make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
+    }
+    if (tid == 0) tot[SSZ] = failed ? 0.f : 1.f;
+    cluster_sync();
+    float Sin[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) Sin[i] = 0.f;
+    if (!failed && sg > 0) {
+        const bool ok = tid >= sg || ld_cluster_f32(mapa_cluster(aTOT + SSZ * 4, tid)) != 0.f;
+        if (__syncthreads_or(!ok)) { status_bits |= kStatusFlagWait; failed = true; }
+        if (!failed && (rowv || rowz)) {
+            const uint32_t off = aTOT + (hh * 8 * (D + 1) + (rowv ? r : D)) * 16;   // z follows the D rows of X
+            for (int s2 = 0; s2 < sg; ++s2) {
+                const uint32_t src = mapa_cluster(off, s2);
+                float4 v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = ld_cluster_v4(src + i * (D + 1) * 16);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    Sin[4 * i] += v[i].x;
+                    Sin[4 * i + 1] += v[i].y;
+                    Sin[4 * i + 2] += v[i].z;
+                    Sin[4 * i + 3] += v[i].w;
+                }
+            }
+            write_state_tile(Sin);   // the last batch 1 that read the tile is done
+        }
+        if (!failed) {
+            sync_mma();
+            if (issuer) {   // O_j += phi(Q_j) [X_in | z_in]^T
+                for (int jj = 0; jj < nj; ++jj)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + 96 * jj, kmaj(sbase + L::Q + jj * 16384 + kk * 32), kmaj(aX + kk * 32), ID_O, 1);
+                mma_commit(&bar[kBarFin]);
+            }
+            const bool ok2 = !worker || mbar_wait(&bar[kBarFin], 0, kWaitLimitNs);
+            tc_fence_after();
+            if (__syncthreads_or(!ok2)) { status_bits |= kStatusMmaWait; failed = true; }
+        }
+    }
+    if (!failed && sg + 1 == p.nseg && p.state_out && (rowv || (rowz && lane == 0))) {
+        float* so = p.state_out + static_cast<size_t>(bh) * SSZ;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float v = R[i] + Sin[i];
+            if (rowv) so[(hh * 32 + i) * D + r] = v;
+            else so[D * D + hh * 32 + i] = v;
+        }
+    }
+    if (!failed) {
+        // outputs: column 64 of O_j is the normalizer; tiles in the free stage area
+        for (int jj = 0; jj < nj && worker; ++jj) {
+            const int t0 = (j0 + jj) * B;
+            float x[32], dn[16];
+            tmem_ld32(tlane + 96 * jj + hh * 32, x);
+            tmem_ld16(tlane + 96 * jj + 64, dn);
+            tmem_ld_wait();
+            const float inv = __fdividef(1.f, dn[0]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] *= inv;
+            store_row32_bf16(sbase + L::STG + jj * 16384, r, 4 * hh, x);
+            if (p.den_out && hh == 0 && t0 + r < p.T) p.den_out[static_cast<size_t>(bh) * p.T + t0 + r] = dn[0];
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (issuer) {
+            for (int jj = 0; jj < nj; ++jj) {
+                const int t0 = (j0 + jj) * B;
+                tma_store_3d(&tmo, sm + L::STG + jj * 16384, 0, t0, bh);
+                if (t0 + 64 < p.T) tma_store_3d(&tmo, sm + L::STG + jj * 16384 + 8192, 0, t0 + 64, bh);
+            }
+            bulk_commit();
+        }
+    }
+    cluster_sync();   // no CTA leaves while another may still read its total
+    if (failed && issuer) {   // let loads and MMAs in flight finish before the CTA exits
+        for (int jj = 0; jj < kMaxSub; ++jj)
+            if (q_pending & (1u << jj)) mbar_wait(&bar[kBarQ + jj], 0, 100000000ull);
+        for (int s2 = 0; s2 < NS; ++s2)   // at most one load per stage is outstanding
+            if (kv_iss[s2] > kv_done[s2]) mbar_wait(&bar[kBarLd + s2], (kv_iss[s2] - 1) & 1, 100000000ull);
+        mma_commit(&bar[kBarHook]);   // phase 0 of this barrier is never completed otherwise
+        mbar_wait(&bar[kBarHook], 0, 100000000ull);
+    }
+    if (issuer) bulk_wait_read_all();   // the output tiles have left shared memory
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);
+    if (status_bits && tid == 0) atomicOr(p.status, status_bits);
+}
+
+// The split of one sequence-head into segments: as many as the SMs hold side
+// by side (at most kMaxSeg, one cluster), each at most kMaxSub blocks.
+struct Split {
+    int nsub, nseg, per;
+};
+bool split(int BH, int T, int sm_count, Split* out) {
+    const int nsub = (T + B - 1) / B;
+    int nseg = sm_count / BH;
+    if (nseg < 1) nseg = 1;
+    if (nseg > kMaxSeg) nseg = kMaxSeg;
+    if (nseg > nsub) nseg = nsub;
+    const int per = (nsub + nseg - 1) / nseg;
+    if (per > kMaxSub) return false;
+    out->nsub = nsub;
+    out->per = per;
+    out->nseg = (nsub + per - 1) / per;
+    return true;
+}
+
+}  // namespace seg
+
+namespace chunk {
+
+bool seg_fits(int BH, int T, int dk, int dv, int sm_count) {
+    seg::Split sp;
+    return dk == seg::D && dv == seg::D && seg::split(BH, T, sm_count, &sp);
+}
+
+cudaError_t launch_seg(const FwdArgs& a, const Maps& m, cudaStream_t s) {
+    seg::Split sp;
+    if (!seg::split(a.BH, a.T, a.sm_count, &sp)) return cudaErrorInvalidValue;
+    seg::Params p;
+    p.state_in = a.state_in;
+    p.state_out = a.state_out;
+    p.den_out = a.den_out;
+    p.BH = a.BH;
+    p.T = a.T;
+    p.nsub = sp.nsub;
+    p.nseg = sp.nseg;
+    p.per = sp.per;
+    p.flags = a.flags;
+    p.status = a.status;
+    auto kern = seg::seg_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, seg::Layout::SMEM);
+    if (e != cudaSuccess) return e;
+    if (a.nlaunch) *a.nlaunch += 1;
+    const unsigned grid = static_cast<unsigned>(a.BH) * sp.nseg;
+    return launch_cluster(kern, grid, static_cast<unsigned>(sp.nseg), seg::kThreads, seg::Layout::SMEM, s, m.q, m.k,
+                          m.v, m.o, p);
+}
+
+}  // namespace chunk
+}  // namespace la

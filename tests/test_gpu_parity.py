@@ -120,6 +120,29 @@ def test_segmented_prefill_parity(variant, T, flags):
     assert_parity(w, inp, chunk=64, state_in=sin, flags=flags)
 
 
+@pytest.mark.parametrize("B,H,T,launches", [
+    (1, 2, 2053, 1),     # 17 segments of one block each, ragged tail
+    (4, 8, 1000, 1),     # 4 segments of 2 blocks
+    (2, 16, 1500, 1),    # 4 segments of 3 blocks, ragged tail
+    (1, 40, 777, 1),     # 3 segments of 3 blocks (the last one short)
+    (8, 20, 300, 1),     # B*H above the SM count: one segment per head, no waits
+    (4, 16, 2048, 2),    # would need 8 blocks per segment (and the per-chunk states pass the
+                         # three-phase budget): segment summaries + the chunk kernel
+])
+@pytest.mark.parametrize("with_state", [False, True], ids=["zero", "state"])
+def test_single_launch_normalized_parity(B, H, T, launches, with_state):
+    # normalized, d = 64: segments of 128-token blocks in one launch, each
+    # starting from the totals its predecessors published
+    w = base("norm", 64).with_(B=B, H=H, T=T)
+    inp = W.draw(w, seed=T + B)
+    sin = None
+    if with_state:
+        rng = np.random.default_rng(T)
+        sin = (rng.standard_normal((w.B, w.H, oracle.state_size("norm", 64, 64))) * 0.1).astype(np.float32)
+        sin[..., 64 * 64:] = np.abs(sin[..., 64 * 64:]) * 50 + 1.0
+    assert_parity(w, inp, chunk=64, state_in=sin, launches=launches)
+
+
 def test_gla_identity_feature_map():
     w = base("gla", 128).with_(T=100)
     inp = W.draw(w, seed=4)
@@ -468,7 +491,7 @@ def test_rejected_calls_do_not_launch():
 
 
 @pytest.mark.parametrize("variant,T,flags,chunk,expect", [
-    ("norm", 200, 0, 64, 3),                                 # three-phase parallel form
+    ("norm", 200, 0, 64, 1),                                 # d = 64: segments of 128-token blocks, one launch
     ("gla", 200, 0, 64, 3),
     ("norm", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 2),      # segment summaries + chunk kernel
     ("norm", 100, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),      # too short to split
@@ -492,11 +515,12 @@ def test_launch_counts(variant, T, flags, chunk, expect):
 
 
 @pytest.mark.filterwarnings("ignore::RuntimeWarning")   # the aborted call leaves `out` unwritten
-@pytest.mark.parametrize("variant", ["gdn", "kda"])
-def test_bounded_wait_expires_cleanly(variant):
+@pytest.mark.parametrize("variant,d,T", [("gdn", 128, 128), ("kda", 128, 128), ("norm", 64, 512)])
+def test_bounded_wait_expires_cleanly(variant, d, T):
     # The test hook makes the chunked kernel wait on a barrier nothing signals;
-    # the wait gives up after 1 ms, the kernel records it and exits cleanly.
-    w = base(variant, 128).with_(T=128)
+    # the wait gives up after 1 ms, the kernel records it and exits cleanly
+    # (for norm: every segment tags its flag as failed, so none waits on another).
+    w = base(variant, d).with_(T=T)
     inp = W.draw(w, 0)
     h = handle(w, flags=la.LA_FLAG_TEST_TIMEOUT)
     run_gpu_prefill(h, w, inp, 64)
