@@ -34,7 +34,7 @@ cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s);
 
 // Normalized, d_k = d_v = 64, no decay: one launch in which each CTA runs a
 // segment of up to four 128-token blocks of one sequence-head, and the
-// segments of a sequence-head (a thread-block cluster of at most 8) pass
+// segments of a sequence-head (a thread-block cluster of at most 6) pass
 // their totals through distributed shared memory. Fits when every
 // sequence-head splits into such segments; needs no workspace.
 bool seg_fits(int BH, int T, int dk, int dv, int sm_count);

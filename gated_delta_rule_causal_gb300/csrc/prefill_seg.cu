@@ -17,12 +17,13 @@
 // the MN-major operand descriptors reach through their leading-byte offset.
 //
 // The segments of one sequence-head form one thread-block cluster (at most
-// kMaxSeg CTAs). Each leaves its total (X, z) in its shared memory; after one
-// cluster barrier, segment s sums the totals of segments 0..s-1 through
-// distributed shared memory (the state entering it), then adds
-// phi(Q_j) [X_in | z_in]^T to the outputs it held in tensor memory. Clusters
-// never wait on one another, every other wait is bounded, and a CTA that
-// failed says so next to its total.
+// kMaxSeg CTAs). Once its blocks are done, a CTA tells its predecessors that
+// its stage area is free; each predecessor then copies its total (X, z) into
+// that area with one distributed-shared-memory bulk copy per successor, and
+// segment s sums the totals of segments 0..s-1 (the state entering it) from
+// its own shared memory, then adds phi(Q_j) [X_in | z_in]^T to the outputs it
+// held in tensor memory. Clusters never wait on one another, every wait is
+// bounded, and a CTA that failed still sends its total, marked as invalid.
 
 #include "prefill.h"
 #include "prefill_impl.cuh"
@@ -41,10 +42,11 @@ using chunk::store_row32_bf16;
 constexpr int B = 128;        // tokens per block
 constexpr int D = 64;         // d_k = d_v
 constexpr int kMaxSub = 4;    // blocks per segment: four held outputs + scores fill tensor memory
-constexpr int kMaxSeg = 8;    // segments per sequence-head: the portable cluster size
+constexpr int kMaxSeg = 6;    // segments per sequence-head (cluster size): 5 totals fit the stage area
 constexpr int kWorkers = 256;             // 8 warps: conversions and tensor-memory reads
 constexpr int kThreads = kWorkers + 32;   // + the warp that issues every MMA and TMA copy
 constexpr int SSZ = D * D + D;   // one state: X or S plus z
+constexpr uint32_t kTotBytes = SSZ * 4 + 16;   // a total as sent: [16 column groups][65 rows][4] floats, ok word
 
 struct Params {
     const float* state_in;     // S [BH][D][D] then z [D] per head, or NULL
@@ -57,12 +59,12 @@ struct Params {
 
 // Shared memory (offsets from the 1024-aligned base).
 struct Layout {
-    static constexpr uint32_t Q = 0;                        // phi(Q_j), kMaxSub tiles [128 t][64] K-major
-    static constexpr uint32_t STG = Q + kMaxSub * 16384;    // 3 stages of K (phi(K) in place) and V, then the output tiles
+    static constexpr uint32_t Q = 0;                        // phi(Q_j), kMaxSub tiles [128 t][64] K-major; then the output tiles
+    static constexpr uint32_t STG = Q + kMaxSub * 16384;    // 3 stages of K (phi(K) in place) and V; then the predecessors' totals
     static constexpr uint32_t STAGE = 32768;
     static constexpr int NSTAGE = 3;
-    static constexpr uint32_t P = STG + NSTAGE * STAGE;     // scores bf16, 2 atoms [128 t][64 i]; then the
-                                                            // segment's total fp32 [65][64] and its ok word
+    static constexpr uint32_t P = STG + NSTAGE * STAGE;     // scores bf16, 2 atoms [128 t][64 i]; then this
+                                                            // segment's total as sent (kTotBytes)
     static constexpr uint32_t X = P + 32768;                // [X_loc | z_loc]^T, [80 rows][64] K-major; then [X_in | z_in]^T
     static constexpr uint32_t ONES = X + 10240;             // 16 KB of bf16 ones
     static constexpr uint32_t BAR = ONES + 16384;
@@ -76,9 +78,11 @@ struct Layout {
 static_assert(Layout::SMEM <= 232448, "shared memory budget");
 static_assert(Layout::ONES > Layout::STG + (Layout::NSTAGE - 1) * Layout::STAGE + 16384, "ones block above every value tile");
 static_assert(kMaxSub <= Layout::NSTAGE + 1, "a block reloads a stage at most once");
+static_assert((kMaxSeg - 1) * kTotBytes <= Layout::NSTAGE * Layout::STAGE, "predecessors' totals fit the stage area");
+static_assert(kTotBytes <= 32768 && kTotBytes % 16 == 0, "this CTA's total fits the score area");
 
 // barriers
-enum { kBarQ = 0, kBarLd = kMaxSub, kBarP = kMaxSub + Layout::NSTAGE, kBarO, kBarFin, kBarHook, kNumBar };
+enum { kBarQ = 0, kBarLd = kMaxSub, kBarP = kMaxSub + Layout::NSTAGE, kBarO, kBarFin, kBarHook, kBarReady, kBarInbox, kBarDone, kNumBar };
 
 __global__ void __launch_bounds__(kThreads, 1)
 seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -124,9 +128,12 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
         tma_load_3d(&tmq, &bar[kBarQ + j], sm + L::Q + j * 16384, 0, t0, bh);
         tma_load_3d(&tmq, &bar[kBarQ + j], sm + L::Q + j * 16384 + 8192, 0, t0 + 64, bh);
     };
+    const int nsucc = p.nseg - 1 - sg;
     if (issuer) {   // barriers, then the first tiles on their way before anything else
-        for (int i = 0; i < kNumBar; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < kNumBar; ++i)
+            mbar_init(&bar[i], (i == kBarReady || i == kBarDone) && nsucc > 0 ? nsucc : 1);
         fence_mbar_init();
+        if (sg > 0) mbar_arrive_expect_tx(&bar[kBarInbox], static_cast<uint32_t>(sg) * kTotBytes);
         if (!hook) {
             load_q(0);
             load_kv(0);
@@ -148,6 +155,7 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    cluster_arrive_relaxed();   // waited for before the first access to another CTA's barriers
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
 
@@ -306,10 +314,10 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
         if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; }
     }
     if (!failed) read_a(L::COL_PA);
-    // the total to this CTA's shared memory as [16 column groups][65 rows][4]
+    // this CTA's total in the score area as [16 column groups][65 rows][4]
     // floats (rows 0..63 X, row 64 z; a warp's 16-byte accesses fall on
-    // consecutive addresses), then whether it is valid; the scores are done with
-    const uint32_t aTOT = sbase + L::P;
+    // consecutive addresses) and whether it is valid
+    const uint32_t aTOT = sbase + L::P, aIN = sbase + L::STG;
     float* tot = reinterpret_cast<float*>(sm + L::P);
     if (!failed && (rowv || (rowz && lane == 0))) {
         const int row = rowv ? r : D;
@@ -319,26 +327,42 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
                 make_float4(R[i], R[i + 1], R[i + 2], R[i + 3]);
     }
     if (tid == 0) tot[SSZ] = failed ? 0.f : 1.f;
-    cluster_sync();
+    fence_proxy_async_smem();   // the total, for the bulk copies
+    __syncthreads();
+    cluster_wait();   // every CTA of the cluster has its barriers initialized
+    if (issuer) {
+        // this CTA's stage area is free: the predecessors may send their totals
+        for (int s2 = 0; s2 < sg; ++s2) mbar_arrive_remote(mapa_cluster(smem_u32(&bar[kBarReady]), s2));
+        if (nsucc > 0) {
+            if (mbar_wait(&bar[kBarReady], 0, kWaitLimitNs)) {
+                for (int d = p.nseg - 1; d > sg; --d)   // the last segment, which waits on the most, first
+                    bulk_push_cluster(mapa_cluster(aIN + sg * kTotBytes, d), aTOT, kTotBytes,
+                                      mapa_cluster(smem_u32(&bar[kBarInbox]), d));
+            } else {
+                status_bits |= kStatusFlagWait;
+            }
+        }
+    }
     float Sin[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) Sin[i] = 0.f;
-    if (!failed && sg > 0) {
-        const bool ok = tid >= sg || ld_cluster_f32(mapa_cluster(aTOT + SSZ * 4, tid)) != 0.f;
-        if (__syncthreads_or(!ok)) { status_bits |= kStatusFlagWait; failed = true; }
+    if (sg > 0) {
+        // the predecessors' totals (each arrives whether or not it is valid)
+        bool ok = mbar_wait(&bar[kBarInbox], 0, kWaitLimitNs);
+        if (issuer)   // the predecessors' copies are done with their shared memory
+            for (int s2 = 0; s2 < sg; ++s2) mbar_arrive_remote(mapa_cluster(smem_u32(&bar[kBarDone]), s2));
+        if (ok && tid < sg) ok = reinterpret_cast<const float*>(sm + L::STG + tid * kTotBytes)[SSZ] != 0.f;
+        if (__syncthreads_or(!ok) && !failed) { status_bits |= kStatusFlagWait; failed = true; }
         if (!failed && (rowv || rowz)) {
-            const uint32_t off = aTOT + (hh * 8 * (D + 1) + (rowv ? r : D)) * 16;   // z follows the D rows of X
+            const uint32_t off = aIN + (hh * 8 * (D + 1) + (rowv ? r : D)) * 16;   // z follows the D rows of X
             for (int s2 = 0; s2 < sg; ++s2) {
-                const uint32_t src = mapa_cluster(off, s2);
-                float4 v[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = ld_cluster_v4(src + i * (D + 1) * 16);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    Sin[4 * i] += v[i].x;
-                    Sin[4 * i + 1] += v[i].y;
-                    Sin[4 * i + 2] += v[i].z;
-                    Sin[4 * i + 3] += v[i].w;
+                    const uint4 u = ld_shared_v4(off + s2 * kTotBytes + i * (D + 1) * 16);
+                    Sin[4 * i] += __uint_as_float(u.x);
+                    Sin[4 * i + 1] += __uint_as_float(u.y);
+                    Sin[4 * i + 2] += __uint_as_float(u.z);
+                    Sin[4 * i + 3] += __uint_as_float(u.w);
                 }
             }
             write_state_tile(Sin);   // the last batch 1 that read the tile is done
@@ -367,7 +391,7 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
         }
     }
     if (!failed) {
-        // outputs: column 64 of O_j is the normalizer; tiles in the free stage area
+        // outputs: column 64 of O_j is the normalizer; tiles where phi(Q) was
         for (int jj = 0; jj < nj && worker; ++jj) {
             const int t0 = (j0 + jj) * B;
             float x[32], dn[16];
@@ -377,7 +401,7 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
             const float inv = __fdividef(1.f, dn[0]);
 #pragma unroll
             for (int i = 0; i < 32; ++i) x[i] *= inv;
-            store_row32_bf16(sbase + L::STG + jj * 16384, r, 4 * hh, x);
+            store_row32_bf16(sbase + L::Q + jj * 16384, r, 4 * hh, x);
             if (p.den_out && hh == 0 && t0 + r < p.T) p.den_out[static_cast<size_t>(bh) * p.T + t0 + r] = dn[0];
         }
         fence_proxy_async_smem();
@@ -385,13 +409,13 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
         if (issuer) {
             for (int jj = 0; jj < nj; ++jj) {
                 const int t0 = (j0 + jj) * B;
-                tma_store_3d(&tmo, sm + L::STG + jj * 16384, 0, t0, bh);
-                if (t0 + 64 < p.T) tma_store_3d(&tmo, sm + L::STG + jj * 16384 + 8192, 0, t0 + 64, bh);
+                tma_store_3d(&tmo, sm + L::Q + jj * 16384, 0, t0, bh);
+                if (t0 + 64 < p.T) tma_store_3d(&tmo, sm + L::Q + jj * 16384 + 8192, 0, t0 + 64, bh);
             }
             bulk_commit();
         }
     }
-    cluster_sync();   // no CTA leaves while another may still read its total
+    if (issuer && nsucc > 0) mbar_wait(&bar[kBarDone], 0, kWaitLimitNs);   // no CTA leaves before its total arrived
     if (failed && issuer) {   // let loads and MMAs in flight finish before the CTA exits
         for (int jj = 0; jj < kMaxSub; ++jj)
             if (q_pending & (1u << jj)) mbar_wait(&bar[kBarQ + jj], 0, 100000000ull);

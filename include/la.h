@@ -150,7 +150,7 @@ int la_create(const la_config* cfg, la_handle** out);
  *             fp32 io and head sizes 16/32 always use the recurrent kernel.
  *             LA_NORM_ELU1 with d_k = d_v = 64 computes its chunkwise form
  *             in blocks of 128 tokens, in one launch, when each
- *             sequence-head splits into at most min(8, SM count / (B*H))
+ *             sequence-head splits into at most min(6, SM count / (B*H))
  *             segments (one segment when B*H > SM count) of at most 4 blocks
  *             each; the segments of a sequence-head form one thread-block
  *             cluster. Otherwise it takes the forms described under the
