@@ -187,11 +187,13 @@ la::FwdArgs make_args(la_handle* h, const void* q, const void* k, const void* v,
 int enqueue_forward(la_handle* h, la::FwdArgs& a, int variant, int chunk, cudaStream_t s) {
     const la_config& c = h->cfg;
     const bool tc_ok = c.io == LA_BF16 && (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
-    // the decayed normalized variant runs chunkwise only in the three-phase form
+    // the decayed normalized variant runs chunkwise only in the single-launch
+    // or the three-phase form
     const bool chunked = tc_ok && chunk != 1 &&
                          (variant != LA_NORM_DECAY ||
                           (!(c.flags & LA_FLAG_SEQUENTIAL_CHUNKS) &&
-                           la::chunk::par_fits(a.BH, a.T, c.d_k, c.d_v, h->ws_bytes)));
+                           (la::chunk::seg_fits(a.BH, a.T, c.d_k, c.d_v, h->sm_count) ||
+                            la::chunk::par_fits(a.BH, a.T, c.d_k, c.d_v, h->ws_bytes))));
     cudaError_t e;
     if (chunked) {
         const char* what = "";

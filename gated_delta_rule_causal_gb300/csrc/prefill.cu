@@ -47,7 +47,7 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
         *what = "chunked prefill launch";
         return chunk::launch_gdn(a, m, s);
     }
-    if (a.variant == kNorm && !a.gate && !(a.flags & 0x2u) &&
+    if (a.variant == kNorm && !(a.flags & 0x2u) &&   // with or without a fixed decay
         chunk::seg_fits(a.BH, a.T, a.dk, a.dv, a.sm_count)) {
         *what = "chunked prefill launch";
         return chunk::launch_seg(a, m, s);

@@ -24,6 +24,15 @@
 // its own shared memory, then adds phi(Q_j) [X_in | z_in]^T to the outputs it
 // held in tensor memory. Clusters never wait on one another, every wait is
 // bounded, and a CTA that failed still sends its total, marked as invalid.
+//
+// With a fixed decay gamma per sequence-head (S_t = gamma S_{t-1} +
+// phi(k_t) v_t^T, z likewise), every factor is a power gamma^n with n >= 0:
+// score (t, i) takes gamma^(t-i); once the scores are read, phi(Q_j) rows
+// take gamma^(t+1) for the state part and phi(K_j) rows gamma^(L-1-i) for
+// A_j (L tokens in the block), so the state part of O_j and A_j move to the
+// second batch; the running total becomes gamma^L X + A_j, a predecessor's
+// total is weighted by the tokens between it and this segment, and the
+// closing product of block j by gamma^(128 j).
 
 #include "prefill.h"
 #include "prefill_impl.cuh"
@@ -49,6 +58,7 @@ constexpr int SSZ = D * D + D;   // one state: X or S plus z
 constexpr uint32_t kTotBytes = SSZ * 4 + 16;   // a total as sent: [16 column groups][65 rows][4] floats, ok word
 
 struct Params {
+    const float* gamma;        // [BH] fixed decay per sequence-head in (0, 1] (decayed form only)
     const float* state_in;     // S [BH][D][D] then z [D] per head, or NULL
     float* state_out;          // same layout, or NULL
     float* den_out;            // [BH][T], or NULL
@@ -84,6 +94,7 @@ static_assert(kTotBytes <= 32768 && kTotBytes % 16 == 0, "this CTA's total fits 
 // barriers
 enum { kBarQ = 0, kBarLd = kMaxSub, kBarP = kMaxSub + Layout::NSTAGE, kBarO, kBarFin, kBarHook, kBarReady, kBarInbox, kBarDone, kNumBar };
 
+template <bool DECAY>
 __global__ void __launch_bounds__(kThreads, 1)
 seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
            const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const Params p) {
@@ -107,6 +118,8 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumBar);
     const uint32_t aP = sbase + L::P, aX = sbase + L::X, aONES = sbase + L::ONES;
     const bool hook = (p.flags & 0x100u) != 0;   // test hook: a wait nothing will satisfy, 1 ms limit
+    const float gam = DECAY ? __ldg(p.gamma + bh) : 1.f;
+    const float lg = DECAY ? lg2(gam) : 0.f;   // gamma^n = ex2(n lg), n >= 0 throughout
 
     // loads in flight, for a clean exit after a failed wait (issuing thread): Q
     // tiles not yet waited for, and per stage the loads issued and waited for
@@ -236,6 +249,10 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             mma_bf16_ss(tmem + L::COL_PA, kmaj(aQ + kk * 32), kmaj(aK + kk * 32), ID_P, kk > 0);
+        if (DECAY) {   // scores alone: the rest waits for the decayed operands
+            mma_commit(&bar[kBarP]);
+            return;
+        }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dO, kmaj(aQ + kk * 32), kmaj(aX + kk * 32), ID_O, kk > 0);
         if (j + 1 < nj) {
@@ -246,12 +263,21 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
         mma_commit(&bar[kBarP]);
     };
     auto issue_batch2 = [&](int j) {   // the score part of O_j (and the last block's A_j)
+        const uint32_t aQ = sbase + L::Q + j * 16384;
         const uint32_t aK = sbase + L::STG + (j % NS) * L::STAGE, aV = aK + 16384;
         const uint32_t dO = tmem + 96 * j;
+        if (DECAY) {   // decayed: the state part of O_j and A_j (into the next block's columns) too
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_bf16_ss(dO, kmaj(aQ + kk * 32), kmaj(aX + kk * 32), ID_O, kk > 0);
+        }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
             mma_bf16_ss(dO, kmaj(aP + (kk / 4) * 16384 + (kk % 4) * 32), mnmaj(aV + kk * 2048, aONES - aV), ID_PV, 1);
-        if (j + 1 == nj) {
+        if (DECAY) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_ss(dO + 96, mnmaj(aV + kk * 2048, aONES - aV), mnmaj(aK + kk * 2048, 8192), ID_A, kk > 0);
+        } else if (j + 1 == nj) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 mma_bf16_ss(tmem + L::COL_PA, mnmaj(aV + kk * 2048, aONES - aV), mnmaj(aK + kk * 2048, 8192), ID_A, kk > 0);
@@ -288,15 +314,48 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
             float x[32];
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
-                tmem_ld32(tlane + L::COL_PA + hh * 64 + 32 * b, x);
+                const int i0 = hh * 64 + 32 * b;
+                tmem_ld32(tlane + L::COL_PA + i0, x);
                 tmem_ld_wait();
+                if (DECAY) {
+                    // gamma^(t-i), walking down from the diagonal (factors <= 1)
+                    float f = (t >= i0 + 31) ? ex2(static_cast<float>(t - i0 - 31) * lg) : 1.f;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (hh * 64 + 32 * b + i > t) x[i] = 0.f;
+                    for (int i = 31; i >= 0; --i) {
+                        if (i0 + i <= t) {
+                            x[i] *= f;
+                            f *= gam;
+                        } else {
+                            x[i] = 0.f;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i0 + i > t) x[i] = 0.f;
+                }
                 store_row32_bf16(aP + hh * 16384, t, 4 * b, x);
             }
         }
-        if (!last) {   // the state entering block j+1
+        if (DECAY) {
+            if (j > 0) {   // the state entering block j: gamma^L X + A_{j-1}
+                const float gL = ex2(static_cast<float>(B) * lg);   // block j-1 was full
+#pragma unroll
+                for (int i = 0; i < 32; ++i) R[i] *= gL;
+                read_a(96 * j);
+                write_state_tile(R);
+            }
+            if (worker) {   // phi(Q_j) rows by gamma^(t+1), phi(K_j) rows by gamma^(L-1-i)
+                const int nvalid = min(B, p.T - (j0 + j) * B);
+                const uint32_t aQ = sbase + L::Q + j * 16384, aK = sbase + L::STG + (j % NS) * L::STAGE;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = tid + kWorkers * i, row = e >> 3;
+                    chunk::scale_chunk(aQ + 16 * e, ex2(static_cast<float>(row + 1) * lg));
+                    if (row < nvalid) chunk::scale_chunk(aK + 16 * e, ex2(static_cast<float>(nvalid - 1 - row) * lg));
+                }
+            }
+        } else if (!last) {   // the state entering block j+1
             read_a(96 * (j + 1));
             write_state_tile(R);
         }
@@ -313,7 +372,17 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
         tc_fence_after();
         if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; }
     }
-    if (!failed) read_a(L::COL_PA);
+    if (!failed) {
+        if (DECAY) {
+            const int nvalid = min(B, p.T - (j0 + nj - 1) * B);
+            const float gL = ex2(static_cast<float>(nvalid) * lg);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) R[i] *= gL;
+            read_a(96 * nj);
+        } else {
+            read_a(L::COL_PA);
+        }
+    }
     // this CTA's total in the score area as [16 column groups][65 rows][4]
     // floats (rows 0..63 X, row 64 z; a warp's 16-byte accesses fall on
     // consecutive addresses) and whether it is valid
@@ -356,16 +425,24 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
         if (!failed && (rowv || rowz)) {
             const uint32_t off = aIN + (hh * 8 * (D + 1) + (rowv ? r : D)) * 16;   // z follows the D rows of X
             for (int s2 = 0; s2 < sg; ++s2) {
+                // decayed: over the (sg - s2 - 1) full segments between them
+                const float w = DECAY ? ex2(static_cast<float>((sg - s2 - 1) * p.per * B) * lg) : 1.f;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const uint4 u = ld_shared_v4(off + s2 * kTotBytes + i * (D + 1) * 16);
-                    Sin[4 * i] += __uint_as_float(u.x);
-                    Sin[4 * i + 1] += __uint_as_float(u.y);
-                    Sin[4 * i + 2] += __uint_as_float(u.z);
-                    Sin[4 * i + 3] += __uint_as_float(u.w);
+                    Sin[4 * i] += w * __uint_as_float(u.x);
+                    Sin[4 * i + 1] += w * __uint_as_float(u.y);
+                    Sin[4 * i + 2] += w * __uint_as_float(u.z);
+                    Sin[4 * i + 3] += w * __uint_as_float(u.w);
                 }
             }
             write_state_tile(Sin);   // the last batch 1 that read the tile is done
+        }
+        if (DECAY && !failed && worker) {   // block j's tokens are 128 j further from the segment's start
+            for (int jj = 1; jj < nj; ++jj) {
+                const float f = ex2(static_cast<float>(B * jj) * lg);
+                for (int e = tid; e < 1024; e += kWorkers) chunk::scale_chunk(sbase + L::Q + jj * 16384 + 16 * e, f);
+            }
         }
         if (!failed) {
             sync_mma();
@@ -383,9 +460,10 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     }
     if (!failed && sg + 1 == p.nseg && p.state_out && (rowv || (rowz && lane == 0))) {
         float* so = p.state_out + static_cast<size_t>(bh) * SSZ;
+        const float gS = DECAY ? ex2(static_cast<float>(min(p.T, (j0 + nj) * B) - j0 * B) * lg) : 1.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const float v = R[i] + Sin[i];
+            const float v = R[i] + gS * Sin[i];
             if (rowv) so[(hh * 32 + i) * D + r] = v;
             else so[D * D + hh * 32 + i] = v;
         }
@@ -454,7 +532,7 @@ bool split(int BH, int T, int sm_count, Split* out) {
 
 namespace chunk {
 
-bool seg_fits(int BH, int T, int dk, int dv, int sm_count) {
+bool seg_fits(int BH, int T, int dk, int dv, int sm_count) {   // with or without a fixed decay
     seg::Split sp;
     return dk == seg::D && dv == seg::D && seg::split(BH, T, sm_count, &sp);
 }
@@ -463,6 +541,7 @@ cudaError_t launch_seg(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     seg::Split sp;
     if (!seg::split(a.BH, a.T, a.sm_count, &sp)) return cudaErrorInvalidValue;
     seg::Params p;
+    p.gamma = a.gate;   // the normalized variant's fixed decay, or NULL
     p.state_in = a.state_in;
     p.state_out = a.state_out;
     p.den_out = a.den_out;
@@ -473,7 +552,7 @@ cudaError_t launch_seg(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     p.per = sp.per;
     p.flags = a.flags;
     p.status = a.status;
-    auto kern = seg::seg_kernel;
+    auto kern = a.gate ? seg::seg_kernel<true> : seg::seg_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, seg::Layout::SMEM);
     if (e != cudaSuccess) return e;
     if (a.nlaunch) *a.nlaunch += 1;

@@ -148,18 +148,19 @@ int la_create(const la_config* cfg, la_handle** out);
  *   chunk     0 = default (64). 1 = token-by-token recurrent kernel. 64 =
  *             chunkwise tensor-core kernel (bf16 io, d_k and d_v in {64, 128}).
  *             fp32 io and head sizes 16/32 always use the recurrent kernel.
- *             LA_NORM_ELU1 with d_k = d_v = 64 computes its chunkwise form
- *             in blocks of 128 tokens, in one launch, when each
- *             sequence-head splits into at most min(6, SM count / (B*H))
- *             segments (one segment when B*H > SM count) of at most 4 blocks
- *             each; the segments of a sequence-head form one thread-block
- *             cluster. Otherwise it takes the forms described under the
- *             workspace below.
+ *             LA_NORM_ELU1 and LA_NORM_DECAY with d_k = d_v = 64 compute
+ *             their chunkwise form in blocks of 128 tokens, in one launch,
+ *             when each sequence-head splits into at most
+ *             min(6, SM count / (B*H)) segments (one segment when B*H > SM
+ *             count) of at most 4 blocks each; the segments of a
+ *             sequence-head form one thread-block cluster. Otherwise they
+ *             take the forms described under the workspace below.
  *             Other values: LA_ERR_UNSUPPORTED.
  *   den_out   optional, LA_NORM_ELU1 and LA_NORM_DECAY only.
  * Every pointer must be 16-byte aligned (LA_ERR_MISALIGNED otherwise).
- * LA_NORM_DECAY runs chunkwise only in the three-phase form; a call whose
- * per-chunk states do not fit the workspace runs the recurrent kernel.
+ * LA_NORM_DECAY runs chunkwise in the single-launch form (d_k = d_v = 64,
+ * as above) or the three-phase form; a call that fits neither runs the
+ * recurrent kernel.
  */
 int la_forward(la_handle* h, const void* q, const void* k, const void* v,
                const float* gate, const float* beta, const float* state_in,

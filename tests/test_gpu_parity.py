@@ -121,26 +121,39 @@ def test_segmented_prefill_parity(variant, T, flags):
 
 
 @pytest.mark.parametrize("B,H,T,launches", [
-    (1, 2, 2053, 1),     # 17 segments of one block each, ragged tail
+    (1, 2, 2053, 1),     # 6 segments of 3 blocks, ragged tail
     (4, 8, 1000, 1),     # 4 segments of 2 blocks
     (2, 16, 1500, 1),    # 4 segments of 3 blocks, ragged tail
     (1, 40, 777, 1),     # 3 segments of 3 blocks (the last one short)
-    (8, 20, 300, 1),     # B*H above the SM count: one segment per head, no waits
-    (4, 16, 2048, 2),    # would need 8 blocks per segment (and the per-chunk states pass the
-                         # three-phase budget): segment summaries + the chunk kernel
+    (8, 20, 300, 1),     # B*H above the SM count: one segment per head, no hand-off
+    (4, 16, 2048, None), # would need 8 blocks per segment: another form (norm: segment
+                         # summaries + the chunk kernel; decayed: the recurrent kernel)
 ])
 @pytest.mark.parametrize("with_state", [False, True], ids=["zero", "state"])
-def test_single_launch_normalized_parity(B, H, T, launches, with_state):
-    # normalized, d = 64: segments of 128-token blocks in one launch, each
-    # starting from the totals its predecessors published
-    w = base("norm", 64).with_(B=B, H=H, T=T)
+@pytest.mark.parametrize("variant", ["norm", "norm_decay"])
+def test_single_launch_normalized_parity(variant, B, H, T, launches, with_state):
+    # normalized, d = 64, with or without a fixed decay: segments of 128-token
+    # blocks in one launch, each starting from its predecessors' totals
+    w = base(variant, 64).with_(B=B, H=H, T=T)
     inp = W.draw(w, seed=T + B)
     sin = None
     if with_state:
         rng = np.random.default_rng(T)
-        sin = (rng.standard_normal((w.B, w.H, oracle.state_size("norm", 64, 64))) * 0.1).astype(np.float32)
+        sin = (rng.standard_normal((w.B, w.H, oracle.state_size(variant, 64, 64))) * 0.1).astype(np.float32)
         sin[..., 64 * 64:] = np.abs(sin[..., 64 * 64:]) * 50 + 1.0
+    if launches is None:
+        launches = 2 if variant == "norm" else 1
     assert_parity(w, inp, chunk=64, state_in=sin, launches=launches)
+
+
+@pytest.mark.parametrize("gamma", [1.0, 0.999, 0.5, 1e-3])
+def test_single_launch_decay_edges(gamma):
+    # decays from none to forgetting at once, across 4 segments of 3 blocks
+    # (every decay factor is a power gamma^n with n >= 0: nothing overflows)
+    w = base("norm_decay", 64).with_(B=2, H=16, T=1500)
+    inp = W.draw(w, seed=9)
+    inp.gate[...] = gamma
+    assert_parity(w, inp, chunk=64, launches=1)
 
 
 def test_gla_identity_feature_map():
@@ -498,8 +511,8 @@ def test_rejected_calls_do_not_launch():
     ("gdn", 200, 0, 64, 1),                                  # one cooperative launch per 32 heads
     ("gdn", 64 * 40, 0, 64, 1),
     ("gla", 200, 0, 1, 1),                                   # the recurrent kernel
-    ("norm_decay", 200, 0, 64, 3),                           # decayed: the three-phase form
-    ("norm_decay", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),  # decayed, not three-phase: recurrent
+    ("norm_decay", 200, 0, 64, 1),                           # decayed, d = 64: the single launch
+    ("norm_decay", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),  # decayed, not in parallel: recurrent
     ("kda", 200, 0, 0, 1),                                   # per-channel delta rule: as gdn
     ("kda", 200, 0, 1, 1),                                   # per-channel delta rule: recurrent
 ])

@@ -56,13 +56,14 @@ def _rel(x, r):
     return float(np.max(np.abs(x - r)) / max(np.max(np.abs(r)), 1e-30))
 
 
-@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
-def test_noalloc_matches_la_forward_twice(variant):
-    # B*H = 2 with 16 chunks: norm and gla split into segments, so their
-    # summaries go through the static scratch; two calls in a row with
-    # different data must both match la_forward.
+@pytest.mark.parametrize("variant,d", [("norm", 128), ("norm", 64), ("gla", 128), ("gdn", 128)])
+def test_noalloc_matches_la_forward_twice(variant, d):
+    # B*H = 2 with 16 chunks: norm (d = 128) and gla split into segments, so
+    # their summaries go through the static scratch; norm at d = 64 runs the
+    # single cluster launch; two calls in a row with different data must both
+    # match la_forward.
     base = {"norm": W.NORM_B4H8_T2048_D64, "gla": W.GLA_B4H16_T4096_D128, "gdn": W.GDN_B2H16_T8192_D128}[variant]
-    w = W.small(base, B=1, H=2, T=1000, dk=128, dv=128)
+    w = W.small(base, B=1, H=2, T=1000, dk=d, dv=d)
     for seed in (1, 2):
         o, s, den, o_ref, s_ref, den_ref = _run_both(w, seed)
         assert _rel(o, o_ref) <= TOL["bf16"]
