@@ -202,34 +202,40 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
             for (int i = 0; i < 32; ++i) R[i] += a[i];
         }
     };
-    // phi(Q_j), phi(K_j) in place once block j has landed; key rows past T
-    // are zero (phi(0) = 1)
+    // phi(Q_j), phi(K_j) in place once block j has landed (workers; no CTA
+    // barrier, so the conversion overlaps the issuing warp's MMA queueing);
+    // key rows past T are zero (phi(0) = 1). Returns whether the wait succeeded.
     auto convert = [&](int j) -> bool {
-        const bool ok = !worker || (mbar_wait(&bar[kBarQ + j], 0, kWaitLimitNs) &&
-                                    mbar_wait(&bar[kBarLd + j % NS], (j / NS) & 1, kWaitLimitNs));
-        if (__syncthreads_or(!ok)) return false;
-        if (issuer) { q_pending &= ~(1u << j); ++kv_done[j % NS]; }
-        if (!worker) return true;
+        const bool ok = mbar_wait(&bar[kBarQ + j], 0, kWaitLimitNs) &&
+                        mbar_wait(&bar[kBarLd + j % NS], (j / NS) & 1, kWaitLimitNs);
         const int nvalid = min(B, p.T - (j0 + j) * B);
         const uint32_t aQ = sbase + L::Q + j * 16384, aK = sbase + L::STG + (j % NS) * L::STAGE;
+        // all eight 16-byte chunks in flight before any is converted (the
+        // shared-memory accesses keep their program order)
+        uint4 uq[4], uk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int e = tid + kWorkers * i;   // 16-byte chunk: row e / 8
-            const uint32_t qa = aQ + 16 * e, ka = aK + 16 * e;
-            const uint4 uq = ld_shared_v4(qa), uk = ld_shared_v4(ka);
-            const float2 a0 = unpack_bf16(uq.x), a1 = unpack_bf16(uq.y), a2 = unpack_bf16(uq.z), a3 = unpack_bf16(uq.w);
-            st_shared_v4(qa, pack_bf16(elu1(a0.x), elu1(a0.y)), pack_bf16(elu1(a1.x), elu1(a1.y)),
+            uq[i] = ld_shared_v4(aQ + 16 * e);
+            uk[i] = ld_shared_v4(aK + 16 * e);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = tid + kWorkers * i;
+            const float2 a0 = unpack_bf16(uq[i].x), a1 = unpack_bf16(uq[i].y), a2 = unpack_bf16(uq[i].z),
+                         a3 = unpack_bf16(uq[i].w);
+            st_shared_v4(aQ + 16 * e, pack_bf16(elu1(a0.x), elu1(a0.y)), pack_bf16(elu1(a1.x), elu1(a1.y)),
                          pack_bf16(elu1(a2.x), elu1(a2.y)), pack_bf16(elu1(a3.x), elu1(a3.y)));
             if ((e >> 3) < nvalid) {
-                const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z),
-                             b3 = unpack_bf16(uk.w);
-                st_shared_v4(ka, pack_bf16(elu1(b0.x), elu1(b0.y)), pack_bf16(elu1(b1.x), elu1(b1.y)),
+                const float2 b0 = unpack_bf16(uk[i].x), b1 = unpack_bf16(uk[i].y), b2 = unpack_bf16(uk[i].z),
+                             b3 = unpack_bf16(uk[i].w);
+                st_shared_v4(aK + 16 * e, pack_bf16(elu1(b0.x), elu1(b0.y)), pack_bf16(elu1(b1.x), elu1(b1.y)),
                              pack_bf16(elu1(b2.x), elu1(b2.y)), pack_bf16(elu1(b3.x), elu1(b3.y)));
             } else {
-                st_shared_v4(ka, 0u, 0u, 0u, 0u);
+                st_shared_v4(aK + 16 * e, 0u, 0u, 0u, 0u);
             }
         }
-        return true;
+        return ok;
     };
     auto sync_mma = [&]() {   // generic smem writes and tensor-memory reads before the next MMAs
         fence_proxy_async_smem();
@@ -286,7 +292,9 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     };
     if (!failed) {
         write_state_tile(R);
-        if (!convert(0)) { status_bits |= kStatusTmaWait; failed = true; }
+        const bool ok = !worker || convert(0);
+        if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; }
+        if (issuer && !failed) { q_pending &= ~1u; ++kv_done[0]; }
     }
     if (!failed) {
         sync_mma();
@@ -297,7 +305,7 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     // issuer queues batch 2 of block j and batch 1 of block j+1 together.
     for (int j = 0; j < nj && !failed; ++j) {
         const bool last = j + 1 == nj;
-        if (!last && !convert(j + 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
+        const bool cok = !worker || last || convert(j + 1);
         {
             // batch 1 of block j done, and with it batch 2 of block j-1
             bool ok = true;
@@ -307,16 +315,20 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
             }
             tc_fence_after();
             if (issuer && ok && j >= 1 && j + 2 < nj) load_kv(j + 2);   // into block j-1's stage
+            if (__syncthreads_or(!cok)) { status_bits |= kStatusTmaWait; failed = true; break; }
+            if (issuer && !last) { q_pending &= ~(1u << (j + 1)); ++kv_done[(j + 1) % NS]; }
             if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; break; }
         }
         if (worker) {   // causal mask, bf16 scores: thread (t, hh) holds key columns hh*64..hh*64+63
             const int t = r;
-            float x[32];
+            float xs[2][32];
+            tmem_ld32(tlane + L::COL_PA + hh * 64, xs[0]);
+            tmem_ld32(tlane + L::COL_PA + hh * 64 + 32, xs[1]);
+            tmem_ld_wait();
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
                 const int i0 = hh * 64 + 32 * b;
-                tmem_ld32(tlane + L::COL_PA + i0, x);
-                tmem_ld_wait();
+                float* x = xs[b];
                 if (DECAY) {
                     // gamma^(t-i), walking down from the diagonal (factors <= 1)
                     float f = (t >= i0 + 31) ? ex2(static_cast<float>(t - i0 - 31) * lg) : 1.f;
@@ -348,11 +360,26 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
             if (worker) {   // phi(Q_j) rows by gamma^(t+1), phi(K_j) rows by gamma^(L-1-i)
                 const int nvalid = min(B, p.T - (j0 + j) * B);
                 const uint32_t aQ = sbase + L::Q + j * 16384, aK = sbase + L::STG + (j % NS) * L::STAGE;
+                uint4 uq[4], uk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = tid + kWorkers * i;
+                    uq[i] = ld_shared_v4(aQ + 16 * e);
+                    uk[i] = ld_shared_v4(aK + 16 * e);
+                }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int e = tid + kWorkers * i, row = e >> 3;
-                    chunk::scale_chunk(aQ + 16 * e, ex2(static_cast<float>(row + 1) * lg));
-                    if (row < nvalid) chunk::scale_chunk(aK + 16 * e, ex2(static_cast<float>(nvalid - 1 - row) * lg));
+                    const float fq = ex2(static_cast<float>(row + 1) * lg);
+                    const float fk = row < nvalid ? ex2(static_cast<float>(nvalid - 1 - row) * lg) : 0.f;
+                    const float2 a0 = unpack_bf16(uq[i].x), a1 = unpack_bf16(uq[i].y), a2 = unpack_bf16(uq[i].z),
+                                 a3 = unpack_bf16(uq[i].w);
+                    const float2 b0 = unpack_bf16(uk[i].x), b1 = unpack_bf16(uk[i].y), b2 = unpack_bf16(uk[i].z),
+                                 b3 = unpack_bf16(uk[i].w);
+                    st_shared_v4(aQ + 16 * e, pack_bf16(a0.x * fq, a0.y * fq), pack_bf16(a1.x * fq, a1.y * fq),
+                                 pack_bf16(a2.x * fq, a2.y * fq), pack_bf16(a3.x * fq, a3.y * fq));
+                    st_shared_v4(aK + 16 * e, pack_bf16(b0.x * fk, b0.y * fk), pack_bf16(b1.x * fk, b1.y * fk),
+                                 pack_bf16(b2.x * fk, b2.y * fk), pack_bf16(b3.x * fk, b3.y * fk));
                 }
             }
         } else if (!last) {   // the state entering block j+1
