@@ -1,0 +1,82 @@
+"""Float64 gradients of the normalized elu+1 recurrence (test infrastructure).
+
+TEST INFRASTRUCTURE, like the rest of ``oracle``: only ``tests/`` and
+``bench.py``'s CPU legs use it.
+
+The pages define the forward operator only ("Transformers are RNNs" as
+summarized in "Beyond — Linear attention and recurrent memory": phi = elu + 1,
+S_t = S_{t-1} + phi(k_t) v_t^T, z_t = z_{t-1} + phi(k_t), o_t = S_t^T
+phi(q_t) / phi(q_t)^T z_t, update first) and name chunked training without
+giving gradients. This module applies the chain rule to that recurrence, token
+by token, in plain float64:
+
+    f_t = phi(k_t), p_t = phi(q_t), num_t = S_t^T p_t, den_t = p_t . z_t
+    dnum_t = do_t / den_t,  dden_t = -(do_t . num_t) / den_t^2
+    dp_t   = S_t dnum_t + z_t dden_t
+    GS_t   = dS_T + sum_{tau >= t} p_tau dnum_tau^T   (gradient reaching f_t v_t^T)
+    Gz_t   = dz_T + sum_{tau >= t} p_tau dden_tau
+    df_t   = GS_t v_t + Gz_t,  dv_t = GS_t^T f_t
+    dq_t   = dp_t * phi'(q_t),  dk_t = df_t * phi'(k_t),  phi'(x) = 1 (x > 0), e^x (x <= 0)
+    dS_0   = GS_0,  dz_0 = Gz_0
+
+``tests/test_oracle_pins.py`` pins every output against central finite
+differences of the C forward oracle (``oracle.run``), which shares no
+arithmetic with this module.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _phi(x):
+    return np.where(x > 0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def _dphi(x):
+    return np.where(x > 0, 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def norm_backward(q, k, v, do, state_in=None, dstate_out=None):
+    """Gradients of the normalized recurrence.
+
+    q, k [B,H,T,dk]; v, do [B,H,T,dv]; state_in, dstate_out [B,H,dk*dv+dk]
+    (S [dk,dv] then z [dk]) or None (zero state / no gradient on the final
+    state). Returns (dq, dk, dv, dstate_in) in float64.
+    """
+    q, k, v, do = (np.asarray(a, np.float64) for a in (q, k, v, do))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    ss = dk * dv + dk
+    sin = np.zeros((B, H, ss)) if state_in is None else np.asarray(state_in, np.float64).reshape(B, H, ss)
+    dso = np.zeros((B, H, ss)) if dstate_out is None else np.asarray(dstate_out, np.float64).reshape(B, H, ss)
+    f, p = _phi(k), _phi(q)
+    # forward, keeping every state (update first)
+    S = np.empty((B, H, T, dk, dv))
+    z = np.empty((B, H, T, dk))
+    s_prev = sin[..., :dk * dv].reshape(B, H, dk, dv).copy()
+    z_prev = sin[..., dk * dv:].copy()
+    for t in range(T):
+        s_prev = s_prev + f[:, :, t, :, None] * v[:, :, t, None, :]
+        z_prev = z_prev + f[:, :, t]
+        S[:, :, t] = s_prev
+        z[:, :, t] = z_prev
+    num = np.einsum("bhtkv,bhtk->bhtv", S, p)
+    den = np.einsum("bhtk,bhtk->bht", z, p)
+    # reverse
+    GS = dso[..., :dk * dv].reshape(B, H, dk, dv).copy()
+    Gz = dso[..., dk * dv:].copy()
+    dq = np.empty_like(q)
+    dkk = np.empty_like(k)
+    dvv = np.empty_like(v)
+    for t in range(T - 1, -1, -1):
+        dnum = do[:, :, t] / den[:, :, t, None]
+        dden = -np.einsum("bhv,bhv->bh", do[:, :, t], num[:, :, t]) / den[:, :, t] ** 2
+        dp = np.einsum("bhkv,bhv->bhk", S[:, :, t], dnum) + z[:, :, t] * dden[..., None]
+        GS = GS + p[:, :, t, :, None] * dnum[:, :, None, :]
+        Gz = Gz + p[:, :, t] * dden[..., None]
+        df = np.einsum("bhkv,bhv->bhk", GS, v[:, :, t]) + Gz
+        dvv[:, :, t] = np.einsum("bhkv,bhk->bhv", GS, f[:, :, t])
+        dq[:, :, t] = dp * _dphi(q[:, :, t])
+        dkk[:, :, t] = df * _dphi(k[:, :, t])
+    dsin = np.concatenate([GS.reshape(B, H, dk * dv), Gz], axis=-1)
+    return dq, dkk, dvv, dsin

@@ -472,3 +472,59 @@ def test_oracle_batches_are_independent():
             o, S, _ = one("gdn", q[bb, hh], unit(k[bb, hh]), v[bb, hh], g[bb, hh], be[bb, hh])
             assert np.array_equal(res.o[bb, hh], o)
             assert np.array_equal(res.state[bb, hh], S)
+
+
+# ------------------------------------------------------------- gradients of (a)
+
+def _fd_loss(q, k, v, sin, W, Ws):
+    r = oracle.run("norm", q, k, v, None, None, sin)
+    return float(np.sum(r.o * W) + np.sum(r.state * Ws))
+
+
+@pytest.mark.parametrize("with_state", [False, True])
+def test_norm_backward_matches_finite_differences(with_state):
+    # Every gradient of the float64 backward against central differences of
+    # the C forward recurrence, entry by entry, on a tiny problem with a
+    # cotangent on the outputs and on the final state (S and z).
+    from oracle import backward
+    g = rng(41 + with_state)
+    B, H, T, dk, dv = 1, 2, 6, 3, 4
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    ss = dk * dv + dk
+    sin = None
+    if with_state:
+        sin = g.standard_normal((B, H, ss)) * 0.3
+        sin[..., dk * dv:] = np.abs(sin[..., dk * dv:]) + 1.0
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, ss))
+    dq, dk_, dv_, dsin = backward.norm_backward(q, k, v, W, sin, Ws)
+    eps = 1e-6
+    for name, arr, grad in (("q", q, dq), ("k", k, dk_), ("v", v, dv_)) + ((("s", sin, dsin),) if with_state else ()):
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = _fd_loss(q, k, v, sin, W, Ws)
+            arr[idx] = a0 - eps
+            lm = _fd_loss(q, k, v, sin, W, Ws)
+            arr[idx] = a0
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_norm_backward_state_only_closed_form():
+    # With a cotangent on the final state alone, the gradient reaching token t
+    # is the constant dS_T (and dz_T): dv_t = dS_T^T phi(k_t),
+    # dk_t = (dS_T v_t + dz_T) * phi'(k_t), dq = 0, dstate_in = dstate_out.
+    from oracle import backward
+    g = rng(43)
+    B, H, T, dk, dv = 2, 1, 5, 4, 3
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    dso = g.standard_normal((B, H, dk * dv + dk))
+    dq, dk_, dv_, dsin = backward.norm_backward(q, k, v, np.zeros((B, H, T, dv)), None, dso)
+    dS = dso[..., :dk * dv].reshape(B, H, dk, dv)
+    dz = dso[..., dk * dv:]
+    phi = np.where(k > 0, k + 1, np.exp(np.minimum(k, 0)))
+    dphi = np.where(k > 0, 1.0, np.exp(np.minimum(k, 0)))
+    assert np.allclose(dq, 0.0)
+    assert np.allclose(dv_, np.einsum("bhkv,bhtk->bhtv", dS, phi), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dk_, (np.einsum("bhkv,bhtv->bhtk", dS, v) + dz[:, :, None, :]) * dphi, rtol=1e-12, atol=1e-12)
+    assert np.allclose(dsin, dso)
