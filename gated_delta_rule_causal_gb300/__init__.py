@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
             L.la_forward_host.argtypes = [vp, vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, i, vp]
             L.la_forward_host.restype = i
             L.la_decode_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, vp, fp, fp, i, vp]
+            L.la_backward.restype = i
+            L.la_backward.argtypes = [vp, vp, vp, vp, fp, vp, fp, vp, vp, vp, fp, i, i, vp]
             L.la_decode_step.restype = i
             L.la_status.argtypes = [vp, vp]
             L.la_status.restype = i
@@ -284,6 +286,30 @@ class Handle:
                             _ptr(out), _ptr(state_out), _ptr(den_out), var, _stream_ptr(stream))
         self._check(rc)
         return out, state_out, den_out
+
+    def backward(self, q, k, v, dout, state_in=None, dstate_out=None, *, variant="norm",
+                 dq=None, dk=None, dv=None, dstate_in=None, return_dstate=True, stream=None):
+        """Gradients of a normalized prefill: q,k [B,H,T,d_k], v and dout
+        [B,H,T,d_v]; dstate_out optional. Returns (dq, dk, dv, dstate_in)."""
+        import torch
+        var = VARIANTS[variant]
+        B, H, T = q.shape[0], q.shape[1], q.shape[2]
+        if (B, H) != (self.B, self.H):
+            raise ValueError("q batch/heads differ from the handle's")
+        for name, t, d in (("q", q, self.d_k), ("k", k, self.d_k), ("v", v, self.d_v), ("dout", dout, self.d_v)):
+            self._expect(name, t, (B, H, T, d), self.dtype)
+        ss = state_size(variant, self.d_k, self.d_v)
+        self._expect("state_in", state_in, (B, H, ss), torch.float32)
+        self._expect("dstate_out", dstate_out, (B, H, ss), torch.float32)
+        dq = torch.empty_like(q) if dq is None else dq
+        dk = torch.empty_like(k) if dk is None else dk
+        dv = torch.empty_like(v) if dv is None else dv
+        if dstate_in is None and return_dstate:
+            dstate_in = torch.empty((B, H, ss), dtype=torch.float32, device=self.device)
+        rc = lib().la_backward(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(state_in), _ptr(dout), _ptr(dstate_out),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dstate_in), var, T, _stream_ptr(stream))
+        self._check(rc)
+        return dq, dk, dv, dstate_in
 
     def last_launches(self) -> int:
         """Kernels the last forward / decode_step call enqueued."""

@@ -511,6 +511,50 @@ int la_decode_step(la_handle* h, const void* q, const void* k, const void* v, co
     return LA_OK;
 }
 
+int la_backward(la_handle* h, const void* q, const void* k, const void* v, const float* state_in, const void* dout,
+                const float* dstate_out, void* dq, void* dk, void* dv, float* dstate_in, int variant, int T,
+                void* cuda_stream) {
+    if (!h) return LA_ERR_INVALID_ARG;
+    h->last_error.clear();
+    h->last_launches = 0;
+    if (variant != LA_NORM_ELU1) return fail(h, LA_ERR_UNSUPPORTED, "la_backward supports LA_NORM_ELU1 only");
+    if (T < 1) return fail(h, LA_ERR_INVALID_ARG, "T must be >= 1");
+    if (!q || !k || !v || !dout || !dq || !dk || !dv)
+        return fail(h, LA_ERR_INVALID_ARG, "q, k, v, dout, dq, dk and dv are required");
+    const la_config& c = h->cfg;
+    if (!((c.d_k == 16 || c.d_k == 32 || c.d_k == 64) && (c.d_v == 16 || c.d_v == 32 || c.d_v == 64)))
+        return fail(h, LA_ERR_UNSUPPORTED, "la_backward supports d_k, d_v in {16, 32, 64}");
+    if (static_cast<long long>(T) * (c.d_k > c.d_v ? c.d_k : c.d_v) > (1LL << 31) - 1)
+        return fail(h, LA_ERR_UNSUPPORTED, "T * d exceeds 2^31 - 1");
+    const void* ptrs[] = {q, k, v, state_in, dout, dstate_out, dq, dk, dv, dstate_in};
+    const char* names[] = {"q", "k", "v", "state_in", "dout", "dstate_out", "dq", "dk", "dv", "dstate_in"};
+    for (int i = 0; i < 10; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(h, LA_ERR_MISALIGNED, std::string(names[i]) + " is not 16-byte aligned");
+    DeviceGuard g(c.device);
+    if (!g.ok) return fail(h, LA_ERR_CUDA, "cannot select the handle's device");
+    la::BwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.state_in = state_in;
+    a.dout = dout;
+    a.dstate_out = dstate_out;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dstate_in = dstate_in;
+    a.BH = c.B * c.H;
+    a.T = T;
+    a.dk_dim = c.d_k;
+    a.dv_dim = c.d_v;
+    a.io = c.io == LA_FP32 ? la::kFp32 : la::kBf16;
+    const cudaError_t e = la::launch_norm_backward(a, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "backward kernel launch");
+    h->last_launches = 1;
+    return LA_OK;
+}
+
 int la_last_launches(const la_handle* h) { return h ? h->last_launches : 0; }
 
 int la_status(la_handle* h, void* cuda_stream) {

@@ -45,4 +45,23 @@ cudaError_t launch_decode(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEncodeTiled_v12000 encode,
                            const char** what);
 
+// Gradients of the normalized elu+1 recurrence (see backward.cu).
+struct BwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* state_in;    // NULL: zero initial state
+    const void* dout;         // gradient of the outputs [BH][T][dv]
+    const float* dstate_out;  // gradient of the final state (S then z), or NULL
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dstate_in;         // gradient of the initial state, or NULL
+    int BH, T, dk_dim, dv_dim;
+    int io;                   // Io
+};
+
+// One CTA per sequence-head on CUDA cores; d_k, d_v in {16, 32, 64}.
+cudaError_t launch_norm_backward(const BwdArgs& a, cudaStream_t s);
+
 }  // namespace la

@@ -243,6 +243,26 @@ void la_destroy(la_handle* h);
 /* Text of the last failure on h ("" if none). Valid until the next call on h. */
 const char* la_last_error(const la_handle* h);
 
+/*
+ * Backward of the prefill (LA_NORM_ELU1 only; d_k, d_v in {16, 32, 64}; bf16
+ * or fp32 io). Given the same q, k, v, state_in as a forward call and the
+ * gradients of its outputs (dout [B,H,T,d_v], io dtype) and, optionally, of
+ * its final state (dstate_out, fp32, S then z as above; NULL means zero),
+ * writes the gradients dq, dk [B,H,T,d_k], dv [B,H,T,d_v] (io dtype) and,
+ * if dstate_in is not NULL, the gradient of the initial state (fp32, same
+ * layout). The pages give the forward operator only; the gradients follow
+ * from the chain rule through the update-first recurrence (phi'(x) = 1 for
+ * x > 0, e^x otherwise). One CUDA-core kernel: it runs the recurrence
+ * forward to the final state, then backward, recovering earlier states by
+ * subtracting each token's update, so its fp32 rounding grows with T.
+ * Errors as for la_forward: LA_ERR_UNSUPPORTED for another variant or head
+ * size, LA_ERR_INVALID_ARG, LA_ERR_MISALIGNED, LA_ERR_CUDA.
+ */
+int la_backward(la_handle* h, const void* q, const void* k, const void* v,
+                const float* state_in, const void* dout, const float* dstate_out,
+                void* dq, void* dk, void* dv, float* dstate_in,
+                int variant, int T, void* cuda_stream);
+
 /* Number of CUDA kernels the last successful la_forward / la_decode_step on h
  * enqueued (0 after a failed or a T = 0 call, or for a NULL handle). A
  * diagnostic: which algorithm the library picked shows in this count (1: the
