@@ -64,6 +64,11 @@ def prefill_bytes(w: W.Workload) -> int:
     return b + w.B * w.H * state_elems(w) * 4
 
 
+def backward_bytes(w: W.Workload) -> int:
+    """la_backward: q, k, v and the outputs' gradient read; dq, dk, dv written."""
+    return w.B * w.H * w.T * (4 * w.dk + 3 * w.dv) * io_bytes(w)
+
+
 def prefill_flops(w: W.Workload) -> float:
     """Dense chunk contractions per sequence-head-token at C = 64."""
     C, dk, dv = C_FLOPS, w.dk, w.dv
@@ -237,6 +242,33 @@ class PrefillRunner:
     @property
     def launches_per_step(self):
         return self.h.last_launches()   # kernels the library enqueued for one forward
+
+
+class BackwardRunner:
+    """Rotating device copies of the normalized workload's inputs and an
+    output gradient; one la_backward per step."""
+
+    def __init__(self, w: W.Workload, seed: int, l2_bytes: int, torch, la):
+        self.w, self.torch = w, torch
+        self.h = la.Handle(w.B, w.H, w.dk, w.dv, io=w.io)
+        x = W.draw(w, seed)
+        do = W.round_io(np.random.default_rng(seed + 1).standard_normal((w.B, w.H, w.T, w.dv)), w.io)
+        self.copies = max(2, int(np.ceil(2.5 * l2_bytes / backward_bytes(w))))
+        dev = self.h.device
+        base = [PrefillRunner._dev(a, dev) for a in (x.q, x.k, x.v, do)]
+        self.sets = [base] + [[t.clone() for t in base] for _ in range(self.copies - 1)]
+        self.grads = [torch.empty_like(base[0]), torch.empty_like(base[1]), torch.empty_like(base[2])]
+        self.i = 0
+
+    def step(self):
+        q, k, v, do = self.sets[self.i % self.copies]
+        self.i += 1
+        dq, dk, dv = self.grads
+        self.h.backward(q, k, v, do, dq=dq, dk=dk, dv=dv, return_dstate=False)
+
+    @property
+    def launches_per_step(self):
+        return self.h.last_launches()
 
 
 class DecodeRunner:
@@ -460,6 +492,23 @@ def gpu_arm(args):
                               "gpu_launches": args.steps * pr.launches_per_step})
                 del pr
             torch.cuda.empty_cache()
+        # the backward of the normalized prefill on the headline's shapes
+        br = BackwardRunner(HEADLINE, 0, l2, torch, la)
+        tot, per = time_steps(br, args.steps, args.warmup, torch, dist)
+        kms = statistics.mean(per)
+        byts = backward_bytes(HEADLINE)
+        gbs = byts / (kms * 1e-3) / 1e9
+        suite.append({"workload": "norm_backward_" + HEADLINE.name.split("_", 1)[1], "metric": "backward tokens/s (B*T)",
+                      "value": round(HEADLINE.tokens * args.steps / (tot * 1e-3), 1), "unit": "tokens/s",
+                      "ms_per_step": round(tot / args.steps, 4),
+                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                   "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None, "algorithmic_bytes": byts,
+                                   "kernel_ms": round(kms, 4),
+                                   "peak_source": pk["source"] + " (burst copy bandwidth)",
+                                   "note": "one CTA per sequence-head on CUDA cores: latency-bound"},
+                      "gpu_launches": args.steps * br.launches_per_step})
+        del br
+        torch.cuda.empty_cache()
         line["suite"] = suite
     line["wall_s"] = round(time.perf_counter() - t_wall0, 2)
     if rank == 0:
