@@ -138,10 +138,10 @@ __global__ void __launch_bounds__(kThreads) norm_backward_kernel(BwdArgs a) {
         // A: num_t (columns, stepping S back to the tile's start) and p_t z_t
         if (col) {
             for (int t = nt - 1; t >= 0; --t) {
-                float num = 0.f;
+                float nm[4] = {0.f, 0.f, 0.f, 0.f};   // four partial sums: shorter dependent chains
 #pragma unroll
-                for (int e = 0; e < DK; ++e) num += sp[t][e] * S[e];
-                pn[t][j] = sdo[t][j] * num;
+                for (int e = 0; e < DK; ++e) nm[e & 3] += sp[t][e] * S[e];
+                pn[t][j] = sdo[t][j] * ((nm[0] + nm[1]) + (nm[2] + nm[3]));
                 const float vj = sv[t][j];
 #pragma unroll
                 for (int e = 0; e < DK; ++e) S[e] -= sf[t][e] * vj;
@@ -169,25 +169,26 @@ __global__ void __launch_bounds__(kThreads) norm_backward_kernel(BwdArgs a) {
             const size_t tt = static_cast<size_t>(t0 + t);
             if (col) {
                 const float dnum = sdo[t][j] * rden;
-                float dvj = 0.f;
+                float dvp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < DK; ++e) {
                     G[e] += sp[t][e] * dnum;
-                    dvj += G[e] * sf[t][e];
+                    dvp[e & 3] += G[e] * sf[t][e];
                 }
-                st_io(dv, tt * DV + j, dvj);
+                st_io(dv, tt * DV + j, (dvp[0] + dvp[1]) + (dvp[2] + dvp[3]));
             } else if (row) {
                 const float pi = sp[t][i], fi = sf[t][i];
-                float dpi = z * dden, dfi = 0.f;
+                float dpp[4] = {0.f, 0.f, 0.f, 0.f}, dfp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < DV; ++e) {
                     const float dnum = sdo[t][e] * rden;
-                    dpi += S[e] * dnum;
+                    dpp[e & 3] += S[e] * dnum;
                     G[e] += pi * dnum;
-                    dfi += G[e] * sv[t][e];
+                    dfp[e & 3] += G[e] * sv[t][e];
                 }
                 gz += pi * dden;
-                dfi += gz;
+                const float dpi = z * dden + ((dpp[0] + dpp[1]) + (dpp[2] + dpp[3]));
+                const float dfi = gz + ((dfp[0] + dfp[1]) + (dfp[2] + dfp[3]));
                 st_io(dq, tt * DK + i, dpi * sdp[t][i]);
                 st_io(dk, tt * DK + i, dfi * sdf[t][i]);
 #pragma unroll
