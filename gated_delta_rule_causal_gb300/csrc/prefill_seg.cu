@@ -1,4 +1,4 @@
-// Normalized elu+1 prefill (d_k = d_v = 64) in one cooperative launch.
+// Normalized elu+1 prefill (d_k = d_v = 64), with or without a fixed decay, in one cluster launch.
 //
 // "Linear attention and Hyena" §11.2-11.3: with phi = elu + 1, the state
 // S_t = S_{t-1} + phi(k_t) v_t^T and z_t = z_{t-1} + phi(k_t) give
