@@ -1,0 +1,86 @@
+"""The backward oracle's finite-difference pin must catch plausible mistakes.
+
+Each case plants one mistake in a copy of ``oracle/backward.py`` (a dropped
+term, a wrong operand, a wrong feature-map derivative, a lost cotangent),
+loads the copy, and compares its gradients with central differences of the
+(unmutated) C forward oracle: every mutant must disagree.
+"""
+import os
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "backward.py")
+
+MUTANTS = {
+    "drops_normalizer_gradient": ("dden = -np.einsum", "dden = 0.0 * np.einsum"),
+    "drops_z_term_of_dp": ("+ z[:, :, t] * dden[..., None]", ""),
+    "wrong_phi_derivative": ("return np.where(x > 0, 1.0, np.exp(np.minimum(x, 0.0)))", "return np.ones_like(x)"),
+    "df_from_state_not_gradient": ('df = np.einsum("bhkv,bhv->bhk", GS, v[:, :, t]) + Gz',
+                                   'df = np.einsum("bhkv,bhv->bhk", S[:, :, t], v[:, :, t]) + Gz'),
+    "dv_with_query_features": ('dvv[:, :, t] = np.einsum("bhkv,bhk->bhv", GS, f[:, :, t])',
+                               'dvv[:, :, t] = np.einsum("bhkv,bhk->bhv", GS, p[:, :, t])'),
+    "drops_final_state_cotangent": ("GS = dso[..., :dk * dv].reshape(B, H, dk, dv).copy()",
+                                    "GS = np.zeros((B, H, dk, dv))"),
+    "z_gradient_with_key_features": ("Gz = Gz + p[:, :, t] * dden[..., None]", "Gz = Gz + f[:, :, t] * dden[..., None]"),
+}
+
+
+def _load(text):
+    mod = types.ModuleType("backward_mutant")
+    exec(compile(text, "backward_mutant.py", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.fixture(scope="module")
+def case():
+    g = np.random.default_rng(53)
+    B, H, T, dk, dv = 1, 1, 5, 3, 2
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    ss = dk * dv + dk
+    sin = g.standard_normal((B, H, ss)) * 0.3
+    sin[..., dk * dv:] = np.abs(sin[..., dk * dv:]) + 1.0
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, ss))
+
+    def loss():
+        r = oracle.run("norm", q, k, v, None, None, sin)
+        return float(np.sum(r.o * W) + np.sum(r.state * Ws))
+
+    eps = 1e-6
+    fd = []
+    for arr in (q, k, v, sin):
+        grad = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = loss()
+            arr[idx] = a0 - eps
+            lm = loss()
+            arr[idx] = a0
+            grad[idx] = (lp - lm) / (2 * eps)
+        fd.append(grad)
+    return (q, k, v, W, sin, Ws), fd
+
+
+def _agrees(mod, case):
+    (q, k, v, W, sin, Ws), fd = case
+    got = mod.norm_backward(q, k, v, W, sin, Ws)
+    return all(np.allclose(gr, f, rtol=1e-6, atol=1e-6) for gr, f in zip(got, fd))
+
+
+def test_unmutated_backward_agrees(case):
+    with open(SRC) as fh:
+        assert _agrees(_load(fh.read()), case)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, case):
+    old, new = MUTANTS[name]
+    with open(SRC) as fh:
+        text = fh.read()
+    assert text.count(old) == 1, name
+    assert not _agrees(_load(text.replace(old, new)), case), name

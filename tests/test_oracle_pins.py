@@ -528,3 +528,27 @@ def test_norm_backward_state_only_closed_form():
     assert np.allclose(dv_, np.einsum("bhkv,bhtk->bhtv", dS, phi), rtol=1e-12, atol=1e-12)
     assert np.allclose(dk_, (np.einsum("bhkv,bhtv->bhtk", dS, v) + dz[:, :, None, :]) * dphi, rtol=1e-12, atol=1e-12)
     assert np.allclose(dsin, dso)
+
+
+def test_norm_backward_matches_autograd_of_the_parallel_form():
+    # The same gradients from a different association order: torch autograd
+    # (float64, CPU) through the explicit masked parallel form num = (L o
+    # Q_phi K_phi^T) V, den = (L o Q_phi K_phi^T) 1, against the reverse
+    # recurrence of oracle/backward.py (zero initial state).
+    torch = pytest.importorskip("torch")
+    from oracle import backward
+    g = rng(47)
+    B, H, T, dk, dv = 1, 2, 9, 4, 3
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    W = g.standard_normal((B, H, T, dv))
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+
+    def phi(x):
+        return torch.where(x > 0, x + 1.0, torch.exp(torch.clamp(x, max=0.0)))
+
+    A = torch.tril(phi(tq) @ phi(tk).transpose(-1, -2))
+    o = (A @ tv) / A.sum(-1, keepdim=True)
+    (o * torch.tensor(W)).sum().backward()
+    dq, dk_, dv_, _ = backward.norm_backward(q, k, v, W)
+    for got, ref in ((dq, tq.grad), (dk_, tk.grad), (dv_, tv.grad)):
+        assert np.allclose(got, ref.numpy(), rtol=1e-10, atol=1e-12)
