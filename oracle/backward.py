@@ -80,3 +80,59 @@ def norm_backward(q, k, v, do, state_in=None, dstate_out=None):
         dkk[:, :, t] = df * _dphi(k[:, :, t])
     dsin = np.concatenate([GS.reshape(B, H, dk * dv), Gz], axis=-1)
     return dq, dkk, dvv, dsin
+
+
+def norm_decay_backward(q, k, v, gamma, do, state_in=None, dstate_out=None):
+    """Gradients of the normalized recurrence with a fixed decay per
+    sequence-head (S_t = gamma S_{t-1} + phi(k_t) v_t^T, z likewise; the
+    normalized variant with one gamma in (0, 1] per (b,h), as
+    "Beyond — Linear attention and recurrent memory" states for a fixed
+    decay). With G_t, g_t the whole gradients reaching S_t, z_t:
+
+        G_t = p_t dnum_t^T + gamma G_{t+1},   g_t = p_t dden_t + gamma g_{t+1}
+        (G_{T-1} and g_{T-1} also take dS_T, dz_T)
+        df_t = G_t v_t + g_t,  dv_t = G_t^T f_t,  dp_t = S_t dnum_t + z_t dden_t
+        dS_0 = gamma G_0,  dz_0 = gamma g_0
+        dgamma = sum_t <G_t, S_{t-1}> + <g_t, z_{t-1}>
+
+    gamma [B,H]; the rest as ``norm_backward``. Returns (dq, dk, dv,
+    dstate_in, dgamma) in float64.
+    """
+    q, k, v, do = (np.asarray(a, np.float64) for a in (q, k, v, do))
+    gm = np.asarray(gamma, np.float64)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    ss = dk * dv + dk
+    sin = np.zeros((B, H, ss)) if state_in is None else np.asarray(state_in, np.float64).reshape(B, H, ss)
+    dso = np.zeros((B, H, ss)) if dstate_out is None else np.asarray(dstate_out, np.float64).reshape(B, H, ss)
+    f, p = _phi(k), _phi(q)
+    S = np.empty((B, H, T + 1, dk, dv))   # S[:, :, t + 1] is the state after token t
+    z = np.empty((B, H, T + 1, dk))
+    S[:, :, 0] = sin[..., :dk * dv].reshape(B, H, dk, dv)
+    z[:, :, 0] = sin[..., dk * dv:]
+    for t in range(T):
+        S[:, :, t + 1] = gm[..., None, None] * S[:, :, t] + f[:, :, t, :, None] * v[:, :, t, None, :]
+        z[:, :, t + 1] = gm[..., None] * z[:, :, t] + f[:, :, t]
+    num = np.einsum("bhtkv,bhtk->bhtv", S[:, :, 1:], p)
+    den = np.einsum("bhtk,bhtk->bht", z[:, :, 1:], p)
+    G = dso[..., :dk * dv].reshape(B, H, dk, dv).copy()   # gradient arriving from after token t
+    g = dso[..., dk * dv:].copy()
+    dq = np.empty_like(q)
+    dkk = np.empty_like(k)
+    dvv = np.empty_like(v)
+    dgam = np.zeros((B, H))
+    for t in range(T - 1, -1, -1):
+        dnum = do[:, :, t] / den[:, :, t, None]
+        dden = -np.einsum("bhv,bhv->bh", do[:, :, t], num[:, :, t]) / den[:, :, t] ** 2
+        G = G + p[:, :, t, :, None] * dnum[:, :, None, :]
+        g = g + p[:, :, t] * dden[..., None]
+        dp = np.einsum("bhkv,bhv->bhk", S[:, :, t + 1], dnum) + z[:, :, t + 1] * dden[..., None]
+        df = np.einsum("bhkv,bhv->bhk", G, v[:, :, t]) + g
+        dvv[:, :, t] = np.einsum("bhkv,bhk->bhv", G, f[:, :, t])
+        dq[:, :, t] = dp * _dphi(q[:, :, t])
+        dkk[:, :, t] = df * _dphi(k[:, :, t])
+        dgam += np.einsum("bhkv,bhkv->bh", G, S[:, :, t]) + np.einsum("bhk,bhk->bh", g, z[:, :, t])
+        G = gm[..., None, None] * G   # through S_t = gamma S_{t-1} + ...
+        g = gm[..., None] * g
+    dsin = np.concatenate([G.reshape(B, H, dk * dv), g], axis=-1)
+    return dq, dkk, dvv, dsin, dgam

@@ -1,9 +1,10 @@
-"""The backward oracle's finite-difference pin must catch plausible mistakes.
+"""The backward oracle's finite-difference pins must catch plausible mistakes.
 
 Each case plants one mistake in a copy of ``oracle/backward.py`` (a dropped
-term, a wrong operand, a wrong feature-map derivative, a lost cotangent),
-loads the copy, and compares its gradients with central differences of the
-(unmutated) C forward oracle: every mutant must disagree.
+term, a wrong operand, a wrong feature-map derivative, a lost cotangent, a
+lost decay), inside the function it targets, loads the copy, and compares its
+gradients with central differences of the (unmutated) C forward oracle:
+every mutant must disagree.
 """
 import os
 import types
@@ -28,6 +29,20 @@ MUTANTS = {
                                     "GS = np.zeros((B, H, dk, dv))"),
     "z_gradient_with_key_features": ("Gz = Gz + p[:, :, t] * dden[..., None]", "Gz = Gz + f[:, :, t] * dden[..., None]"),
 }
+# planted in norm_decay_backward
+MUTANTS_DECAY = {
+    "state_gradient_not_decayed": ("G = gm[..., None, None] * G   # through", "G = G   # through"),
+    "gamma_gradient_against_later_state": ('np.einsum("bhkv,bhkv->bh", G, S[:, :, t])',
+                                          'np.einsum("bhkv,bhkv->bh", G, S[:, :, t + 1])'),
+    "normalizer_gradient_not_decayed": ("g = gm[..., None] * g", "g = g"),
+}
+
+
+def _split(text):
+    """(head, norm_backward, norm_decay_backward) sources."""
+    a = text.index("def norm_backward(")
+    b = text.index("def norm_decay_backward(")
+    return text[:a], text[a:b], text[b:]
 
 
 def _load(text):
@@ -66,21 +81,73 @@ def case():
     return (q, k, v, W, sin, Ws), fd
 
 
+@pytest.fixture(scope="module")
+def case_decay():
+    g = np.random.default_rng(67)
+    B, H, T, dk, dv = 1, 1, 5, 2, 2
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    gm = np.array([[0.7]])
+    ss = dk * dv + dk
+    sin = g.standard_normal((B, H, ss)) * 0.3
+    sin[..., dk * dv:] = np.abs(sin[..., dk * dv:]) + 1.0
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, ss))
+
+    def loss():
+        r = oracle.run("norm_decay", q, k, v, gm, None, sin)
+        return float(np.sum(r.o * W) + np.sum(r.state * Ws))
+
+    eps = 1e-6
+    fd = []
+    for arr in (q, k, v, sin, gm):
+        grad = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = loss()
+            arr[idx] = a0 - eps
+            lm = loss()
+            arr[idx] = a0
+            grad[idx] = (lp - lm) / (2 * eps)
+        fd.append(grad)
+    return (q, k, v, gm, W, sin, Ws), fd
+
+
 def _agrees(mod, case):
     (q, k, v, W, sin, Ws), fd = case
     got = mod.norm_backward(q, k, v, W, sin, Ws)
     return all(np.allclose(gr, f, rtol=1e-6, atol=1e-6) for gr, f in zip(got, fd))
 
 
-def test_unmutated_backward_agrees(case):
+def _agrees_decay(mod, case):
+    (q, k, v, gm, W, sin, Ws), fd = case
+    got = mod.norm_decay_backward(q, k, v, gm, W, sin, Ws)
+    return all(np.allclose(gr, f, rtol=1e-6, atol=1e-6) for gr, f in zip(got, fd))
+
+
+def test_unmutated_backward_agrees(case, case_decay):
     with open(SRC) as fh:
-        assert _agrees(_load(fh.read()), case)
+        mod = _load(fh.read())
+    assert _agrees(mod, case)
+    assert _agrees_decay(mod, case_decay)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, case):
     old, new = MUTANTS[name]
     with open(SRC) as fh:
-        text = fh.read()
-    assert text.count(old) == 1, name
-    assert not _agrees(_load(text.replace(old, new)), case), name
+        head, plain, decay = _split(fh.read())
+    if head.count(old) == 1:   # a helper both functions share
+        head = head.replace(old, new)
+    else:
+        assert plain.count(old) == 1, name
+        plain = plain.replace(old, new)
+    assert not _agrees(_load(head + plain + decay), case), name
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS_DECAY))
+def test_decay_mutant_is_caught(name, case_decay):
+    old, new = MUTANTS_DECAY[name]
+    with open(SRC) as fh:
+        head, plain, decay = _split(fh.read())
+    assert decay.count(old) == 1, name
+    assert not _agrees_decay(_load(head + plain + decay.replace(old, new)), case_decay), name

@@ -552,3 +552,48 @@ def test_norm_backward_matches_autograd_of_the_parallel_form():
     dq, dk_, dv_, _ = backward.norm_backward(q, k, v, W)
     for got, ref in ((dq, tq.grad), (dk_, tk.grad), (dv_, tv.grad)):
         assert np.allclose(got, ref.numpy(), rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("gamma", [0.9, 0.35])
+def test_norm_decay_backward_matches_finite_differences(gamma):
+    # The decayed gradients (q, k, v, the initial state and gamma itself)
+    # against central differences of the C forward recurrence.
+    from oracle import backward
+    g = rng(59)
+    B, H, T, dk, dv = 1, 2, 6, 3, 2
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    gm = np.array([[gamma, gamma * 0.8]])
+    ss = dk * dv + dk
+    sin = g.standard_normal((B, H, ss)) * 0.3
+    sin[..., dk * dv:] = np.abs(sin[..., dk * dv:]) + 1.0
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, ss))
+
+    def loss():
+        r = oracle.run("norm_decay", q, k, v, gm, None, sin)
+        return float(np.sum(r.o * W) + np.sum(r.state * Ws))
+
+    dq, dk_, dv_, dsin, dgam = backward.norm_decay_backward(q, k, v, gm, W, sin, Ws)
+    eps = 1e-6
+    for name, arr, grad in (("q", q, dq), ("k", k, dk_), ("v", v, dv_), ("s", sin, dsin), ("gamma", gm, dgam)):
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = loss()
+            arr[idx] = a0 - eps
+            lm = loss()
+            arr[idx] = a0
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_norm_decay_backward_at_one_is_undecayed():
+    # gamma = 1 gives the undecayed gradients exactly
+    from oracle import backward
+    g = rng(61)
+    B, H, T, dk, dv = 2, 1, 7, 3, 4
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    W = g.standard_normal((B, H, T, dv))
+    a = backward.norm_backward(q, k, v, W)
+    b = backward.norm_decay_backward(q, k, v, np.ones((B, H)), W)
+    for x, y in zip(a, b[:4]):
+        assert np.allclose(x, y, rtol=1e-12, atol=1e-12)
