@@ -136,3 +136,66 @@ def norm_decay_backward(q, k, v, gamma, do, state_in=None, dstate_out=None):
         g = gm[..., None] * g
     dsin = np.concatenate([G.reshape(B, H, dk * dv), g], axis=-1)
     return dq, dkk, dvv, dsin, dgam
+
+
+def norm_backward_chunked(q, k, v, do, C=64, state_in=None, dstate_out=None):
+    """The same gradients as ``norm_backward``, by chunks of C tokens: the
+    form a tensor-core backward computes. Per chunk c (Q, K the feature-mapped
+    tiles, S_in, z_in the state entering it, P = L o Q K^T):
+
+        num = P V + Q S_in,  den = P 1 + Q z_in
+        dnum = dO / den,  dden = -rowsum(dO o num) / den^2
+        dP = L o (dnum V^T + dden 1^T)
+        dQ = dP K + dnum S_in^T + dden z_in^T
+        dK = dP^T Q + V G^T + 1 g^T,   dV = P^T dnum + K G
+
+    where G, g are the gradients of the state and normalizer after the chunk
+    (the final-state cotangent plus Q^T dnum and Q^T dden of every later
+    chunk), carried from the last chunk to the first; the initial state
+    receives G, g after chunk 0 has added its own. dq = dQ o phi'(q),
+    dk = dK o phi'(k).
+    """
+    q, k, v, do = (np.asarray(a, np.float64) for a in (q, k, v, do))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    ss = dk * dv + dk
+    sin = np.zeros((B, H, ss)) if state_in is None else np.asarray(state_in, np.float64).reshape(B, H, ss)
+    dso = np.zeros((B, H, ss)) if dstate_out is None else np.asarray(dstate_out, np.float64).reshape(B, H, ss)
+    Qf, Kf = _phi(q), _phi(k)
+    nch = (T + C - 1) // C
+    # states entering every chunk (forward, by chunks)
+    S_in = np.empty((B, H, nch, dk, dv))
+    z_in = np.empty((B, H, nch, dk))
+    S = sin[..., :dk * dv].reshape(B, H, dk, dv).copy()
+    z = sin[..., dk * dv:].copy()
+    for c in range(nch):
+        sl = slice(c * C, min(T, (c + 1) * C))
+        S_in[:, :, c], z_in[:, :, c] = S, z
+        S = S + np.einsum("bhtk,bhtv->bhkv", Kf[:, :, sl], v[:, :, sl])
+        z = z + Kf[:, :, sl].sum(axis=2)
+    G = dso[..., :dk * dv].reshape(B, H, dk, dv).copy()
+    g = dso[..., dk * dv:].copy()
+    dq, dkk, dvv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    for c in range(nch - 1, -1, -1):
+        sl = slice(c * C, min(T, (c + 1) * C))
+        Q, K, V, dO = Qf[:, :, sl], Kf[:, :, sl], v[:, :, sl], do[:, :, sl]
+        n = Q.shape[2]
+        L = np.tril(np.ones((n, n)))
+        P = L * np.einsum("bhtk,bhjk->bhtj", Q, K)
+        num = np.einsum("bhtj,bhjv->bhtv", P, V) + np.einsum("bhtk,bhkv->bhtv", Q, S_in[:, :, c])
+        den = P.sum(-1) + np.einsum("bhtk,bhk->bht", Q, z_in[:, :, c])
+        dnum = dO / den[..., None]
+        dden = -np.einsum("bhtv,bhtv->bht", dO, num) / den ** 2
+        dP = L * (np.einsum("bhtv,bhjv->bhtj", dnum, V) + dden[..., None])
+        dQ = (np.einsum("bhtj,bhjk->bhtk", dP, K) + np.einsum("bhtv,bhkv->bhtk", dnum, S_in[:, :, c])
+              + dden[..., None] * z_in[:, :, c][:, :, None, :])
+        dK = np.einsum("bhtj,bhtk->bhjk", dP, Q) + np.einsum("bhjv,bhkv->bhjk", V, G) + g[:, :, None, :]
+        dV = np.einsum("bhtj,bhtv->bhjv", P, dnum) + np.einsum("bhjk,bhkv->bhjv", K, G)
+        dq[:, :, sl] = dQ * _dphi(q[:, :, sl])
+        dkk[:, :, sl] = dK * _dphi(k[:, :, sl])
+        dvv[:, :, sl] = dV
+        # the state entering this chunk also reaches this chunk's outputs
+        G = G + np.einsum("bhtk,bhtv->bhkv", Q, dnum)
+        g = g + np.einsum("bhtk,bht->bhk", Q, dden)
+    dsin = np.concatenate([G.reshape(B, H, dk * dv), g], axis=-1)
+    return dq, dkk, dvv, dsin

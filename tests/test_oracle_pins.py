@@ -597,3 +597,21 @@ def test_norm_decay_backward_at_one_is_undecayed():
     b = backward.norm_decay_backward(q, k, v, np.ones((B, H)), W)
     for x, y in zip(a, b[:4]):
         assert np.allclose(x, y, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("C,T", [(4, 13), (8, 16), (64, 37)])
+def test_norm_backward_chunked_equals_token_by_token(C, T):
+    # The chunkwise form of the gradients (the tensor-core algebra) equals the
+    # token-by-token reverse recurrence, ragged tail and start state included.
+    from oracle import backward
+    g = rng(71 + C)
+    B, H, dk, dv = 1, 2, 3, 5
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    ss = dk * dv + dk
+    sin = g.standard_normal((B, H, ss)) * 0.3
+    sin[..., dk * dv:] = np.abs(sin[..., dk * dv:]) + 1.0
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, ss))
+    a = backward.norm_backward(q, k, v, W, sin, Ws)
+    b = backward.norm_backward_chunked(q, k, v, W, C, sin, Ws)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-11, atol=1e-12)
