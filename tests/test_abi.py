@@ -72,3 +72,21 @@ def test_create_without_gpu_reports_cuda(lib):
 def test_create_null_config(lib):
     out = ctypes.c_void_p()
     assert lib.la_create(None, ctypes.byref(out)) == la.LA_ERR_INVALID_ARG
+
+
+def test_header_is_plain_c(tmp_path):
+    # The boundary is a C ABI: la.h compiles as C99 (pedantic, warnings as
+    # errors), with every declared entry point referenced from C.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = declared_functions()
+    src = tmp_path / "use_la.c"
+    src.write_text('#include "la.h"\ntypedef void (*any_fn)(void);\n' +
+                   "".join(f"any_fn ref_{n}(void) {{ return (any_fn)&{n}; }}\n" for n in names))
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                        "-I", inc, "-c", str(src), "-o", str(tmp_path / "use_la.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
