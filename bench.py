@@ -4,10 +4,11 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload NAME] [--no-suite]
 
 One step = one la_forward over the whole workload (every (b,h) sequence,
-all chunks). The headline workload is normalized elu+1 attention, B=4 H=8
-T=2048 d=64, bf16. The same JSON line carries a suite of the other
-workloads measured the same way: the per-channel gated and gated-delta
-prefills and the 1024-step gated-delta decode.
+all chunks). The headline workload is the gated delta rule, B=2 H=16
+T=8192 d_k=d_v=128, bf16 (the largest single-GPU prefill by FLOPs). The same
+JSON line carries a suite of the other workloads measured the same way: the
+normalized and per-channel gated prefills, the per-channel-decay delta rule,
+and the 1024-step gated-delta decodes.
 
 Timing: W untimed steps, then K steps bracketed by a barrier and a device
 synchronize, timed with CUDA events on the launching stream. Each step reads
@@ -33,9 +34,10 @@ import numpy as np  # noqa: E402
 
 import workloads as W  # noqa: E402
 
-HEADLINE = W.NORM_B4H8_T2048_D64
-SUITE = (W.GLA_B4H16_T4096_D128, W.GDN_B2H16_T8192_D128, W.GDN_DECODE_N256H16_D128, W.NORM_DECAY_B4H8_T2048_D64,
+HEADLINE = W.GDN_B2H16_T8192_D128
+SUITE = (W.NORM_B4H8_T2048_D64, W.GLA_B4H16_T4096_D128, W.GDN_DECODE_N256H16_D128, W.NORM_DECAY_B4H8_T2048_D64,
          W.KDA_B2H16_T8192_D128, W.KDA_DECODE_N256H16_D128)
+BACKWARD = W.NORM_B4H8_T2048_D64   # the backward is timed on the normalized workload's shapes
 C_FLOPS = 64   # chunk size the algorithmic FLOP count is quoted at
 
 
@@ -405,6 +407,7 @@ def cpu_oracle_baseline(w: W.Workload, budget_s: float = 2.0):
         if el >= budget_s:
             break
     return {"value": round(w.tokens * reps / el, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"whole workload ({w.B * w.H} sequence-heads x {w.T} tokens) x {reps}, "
                       f"{el:.2f} s wall, float64 C recurrence with OpenMP over sequence-heads"}
 
@@ -492,14 +495,14 @@ def gpu_arm(args):
                               "gpu_launches": args.steps * pr.launches_per_step})
                 del pr
             torch.cuda.empty_cache()
-        # the backward of the normalized prefill on the headline's shapes
-        br = BackwardRunner(HEADLINE, 0, l2, torch, la)
+        # the backward of the normalized prefill on the normalized workload's shapes
+        br = BackwardRunner(BACKWARD, 0, l2, torch, la)
         tot, per = time_steps(br, args.steps, args.warmup, torch, dist)
         kms = statistics.mean(per)
-        byts = backward_bytes(HEADLINE)
+        byts = backward_bytes(BACKWARD)
         gbs = byts / (kms * 1e-3) / 1e9
-        suite.append({"workload": "norm_backward_" + HEADLINE.name.split("_", 1)[1], "metric": "backward tokens/s (B*T)",
-                      "value": round(HEADLINE.tokens * args.steps / (tot * 1e-3), 1), "unit": "tokens/s",
+        suite.append({"workload": "norm_backward_" + BACKWARD.name.split("_", 1)[1], "metric": "backward tokens/s (B*T)",
+                      "value": round(BACKWARD.tokens * args.steps / (tot * 1e-3), 1), "unit": "tokens/s",
                       "ms_per_step": round(tot / args.steps, 4),
                       "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                                    "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None, "algorithmic_bytes": byts,
@@ -534,8 +537,24 @@ def kernel_only(args):
                       "kernel_ms": [round(x, 5) for x in per]}), flush=True)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (/proc/cpuinfo; Arm hosts name the part)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            txt = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "CPU part"):
+        for line in txt.splitlines():
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    return "unknown"
+
+
 def reference_arm(args):
-    """The float64 CPU oracle, timed on the host cores (rank 0 only)."""
+    """The float64 CPU oracle, timed on the host cores (rank 0 only): every
+    step runs the whole workload (all sequence-heads, all tokens) with OpenMP
+    over the sequence-heads on every core the process may use."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
@@ -547,26 +566,39 @@ def reference_arm(args):
     g = None if x.gate is None else x.gate.astype(np.float64)
     b = None if x.beta is None else x.beta.astype(np.float64)
     cores = host_cores()
-    # each step: a bounded sample, the first 4 sequence-heads of the workload
-    nb = min(4, w.B * w.H)
-    sel = lambda a: None if a is None else a.reshape((w.B * w.H,) + a.shape[2:])[:nb][None]
-    qs, ks, vs, gs, bs = (sel(a) for a in (q, k, v, g, b))
-    for _ in range(max(1, args.warmup)):
-        oracle.run(w.variant, qs, ks, vs, gs, bs, nthreads=cores)
+    # the whole workload is one step; keep the run within a few minutes
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.run(w.variant, qs, ks, vs, gs, bs, nthreads=cores)
+    oracle.run(w.variant, q, k, v, g, b, nthreads=cores)
+    one = time.perf_counter() - t0
+    steps = args.steps
+    warm = max(0, args.warmup - 1)
+    budget = 150.0
+    if one * (steps + warm) > budget:
+        steps = max(1, int(budget / one) - warm)
+    for _ in range(warm):
+        oracle.run(w.variant, q, k, v, g, b, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.run(w.variant, q, k, v, g, b, nthreads=cores)
     el = time.perf_counter() - t0
-    tokens = nb * w.T / w.H * args.steps          # sequence-head tokens expressed as B*T tokens
-    val = tokens / el
+    val = w.tokens * steps / el
+    # one thread, on one sequence-head, scaled to the workload's tokens
+    sel = lambda a: None if a is None else a.reshape((w.B * w.H,) + a.shape[2:])[:1][None]
+    t1 = time.perf_counter()
+    oracle.run(w.variant, sel(q), sel(k), sel(v), sel(g), sel(b), nthreads=1)
+    # B*T tokens count one token of every head: one sequence-head's T tokens are T/H of them
+    one_thread = w.T / w.H / (time.perf_counter() - t1)
     line = {"impl": "reference", "metric": "prefill tokens/s (B*T)", "value": round(val, 2), "unit": "tokens/s",
-            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "n_gpus": ws, "steps": steps, "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy PCG64)",
             "config": {"workload": w.name, "variant": w.variant, "B": w.B, "H": w.H, "T": w.T, "d_k": w.dk,
                        "d_v": w.dv},
             "cpu_baseline": {"value": round(val, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{nb} of {w.B * w.H} sequence-heads x {w.T} tokens per step"},
+                             "cpu_model": cpu_model(),
+                             "one_thread_tokens_per_s": round(one_thread, 2),
+                             "sample": f"whole workload per step ({w.B * w.H} sequence-heads x {w.T} tokens), "
+                                       f"{steps} steps; float64 C recurrence, OpenMP over sequence-heads"},
             "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

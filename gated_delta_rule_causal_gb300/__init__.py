@@ -8,7 +8,7 @@ calls raise.
 
 Low level (same names as the C ABI): ``la_create``, ``la_forward``, ``la_forward_host``,
 ``la_decode_step``, ``la_status``, ``la_destroy``, ``la_last_error``,
-``la_last_launches``, ``la_version``, ``la_forward_noalloc``. Convenience: ``Handle`` takes torch
+``la_last_launches``, ``la_version``, ``la_forward_noalloc``, ``la_noalloc_status``. Convenience: ``Handle`` takes torch
 tensors.
 """
 from __future__ import annotations
@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.la_version.restype = i
             L.la_forward_noalloc.argtypes = [ctypes.POINTER(la_config), vp, vp, vp, fp, fp, fp, vp, fp, fp, i, i, vp]
             L.la_forward_noalloc.restype = i
+            L.la_noalloc_status.argtypes = [i, vp]
+            L.la_noalloc_status.restype = i
             _lib = L
     return _lib
 
@@ -114,6 +116,11 @@ def la_forward_noalloc(cfg: la_config, q, k, v, gate, beta, state_in, out, state
     """Prefill without any device allocation by the library (see la.h)."""
     return lib().la_forward_noalloc(ctypes.byref(cfg), q, k, v, gate, beta, state_in, out, state_out,
                                     den_out, variant, T, stream)
+
+
+def la_noalloc_status(device: int, stream) -> int:
+    """Read and clear the status word of la_forward_noalloc calls on `device` (see la.h)."""
+    return lib().la_noalloc_status(device, stream)
 
 
 def la_status(h, stream) -> int:

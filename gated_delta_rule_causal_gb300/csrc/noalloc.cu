@@ -10,7 +10,8 @@
 //
 // The scratch is one file-scope array of kScratchBytes per GPU that loads the
 // library; it stays allocated until the process exits. Its first 256 bytes
-// hold the status word the kernels set when a bounded wait expires; the rest
+// hold the status word the kernels set when a bounded wait expires
+// (la_noalloc_status reads and clears it); the rest
 // holds segment summaries (normalized / gated), which the summary kernel fully
 // writes before the chunk kernel reads them, or the gated delta rule's states
 // and per-chunk slots, each written by one launch before the next reads it,
@@ -135,7 +136,9 @@ extern "C" int la_forward_noalloc(const la_config* cfg, const void* q, const voi
     a.q = q;
     a.k = k;
     a.v = v;
-    a.gate = gate;
+    // Plain LA_NORM_ELU1 carries no gate, as in la_forward: the normalized
+    // kernels read a non-NULL gate as a per-(b,h) decay.
+    a.gate = (variant == LA_NORM_ELU1) ? nullptr : gate;
     a.beta = beta;
     a.state_in = state_in;
     a.out = out;
@@ -159,4 +162,34 @@ extern "C" int la_forward_noalloc(const la_config* cfg, const void* q, const voi
         return LA_ERR_CUDA;
     }
     return LA_OK;
+}
+
+extern "C" int la_noalloc_status(int device, void* cuda_stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return LA_ERR_CUDA;
+    }
+    if (dev != device) return LA_ERR_INVALID_ARG;  // the caller makes `device` current
+    void* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        base = g_addr[dev];
+    }
+    if (!base) return LA_OK;  // no call has run on this device: nothing can have failed
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return LA_ERR_CUDA;
+    }
+    int word = 0;
+    if (cudaMemcpy(&word, base, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return LA_ERR_CUDA;
+    }
+    if (word == 0) return LA_OK;
+    if (cudaMemset(base, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return LA_ERR_CUDA;
+    }
+    return LA_ERR_TIMEOUT;
 }

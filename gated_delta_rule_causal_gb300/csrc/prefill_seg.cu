@@ -530,6 +530,11 @@ seg_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
         mbar_wait(&bar[kBarHook], 0, 100000000ull);
     }
     if (issuer) bulk_wait_read_all();   // the output tiles have left shared memory
+    // No CTA leaves the cluster while another may still reach its shared
+    // memory: a successor whose inbox wait ran out may yet arrive remotely on
+    // this CTA's barriers. Every wait above is bounded, so every CTA gets here.
+    cluster_arrive_release();
+    cluster_wait();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);

@@ -238,6 +238,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
+// Arrive on the cluster barrier, ordering this thread's earlier memory
+// operations (remote arrives and writes included) before the arrival.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Arrive once on an mbarrier of another CTA of the cluster (address from mapa_cluster).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {

@@ -216,7 +216,8 @@ int la_decode_step(la_handle* h, const void* q, const void* k, const void* v,
  * Scratch: a file-scope device array of 16 MiB in the library's own image,
  * held on every GPU that loads the library until the process exits. It holds
  * the segment summaries of the normalized and per-channel gated variants and
- * a status word for expired device waits (not reported by this call). A shape
+ * a status word for expired device waits, which this call does not read
+ * (it returns before its kernels run): la_noalloc_status reports it. A shape
  * whose summaries would not fit returns LA_ERR_UNSUPPORTED; on a GB300 every
  * supported shape fits. Every call shares the array: calls that overlap on
  * the GPU (different streams, or other host threads) race on it and must be
@@ -231,6 +232,15 @@ int la_forward_noalloc(const la_config* cfg, const void* q, const void* k, const
                        const float* gate, const float* beta, const float* state_in,
                        void* out, float* state_out, float* den_out,
                        int variant, int T, void* cuda_stream);
+
+/* The status of la_forward_noalloc calls on `device` (which must be the
+ * current device): synchronize cuda_stream, then read and clear the status
+ * word in the static scratch. Returns LA_OK, LA_ERR_TIMEOUT if one of those
+ * calls' kernels recorded an expired bounded wait since the word was last
+ * cleared (its outputs are then not valid), LA_ERR_INVALID_ARG or
+ * LA_ERR_CUDA. Allocates nothing. The word is shared by every such call on
+ * the device, whatever the stream. */
+int la_noalloc_status(int device, void* cuda_stream);
 
 /* Synchronize cuda_stream, then read and clear the device status word.
  * Returns LA_OK, LA_ERR_TIMEOUT if a kernel recorded an expired wait since

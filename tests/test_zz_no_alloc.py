@@ -8,8 +8,9 @@ failure has already run every other test."""
 import numpy as np
 import pytest
 
+import oracle
 import workloads as W
-from _helpers import TOL, from_torch, to_torch
+from _helpers import TOL, from_torch, oracle_inputs, slice_rel_err, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -23,11 +24,14 @@ def built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-def _run_both(w, seed):
+def _run_both(w, seed, gate_for_norm=False):
     x = W.draw(w, seed)
     dev = torch.device("cuda", torch.cuda.current_device())
     q, k, v = (to_torch(a, dev) for a in (x.q, x.k, x.v))
     g, b = to_torch(x.gate, dev), to_torch(x.beta, dev)
+    if gate_for_norm:
+        # a stray gate pointer with the undecayed variant must be ignored, as la_forward ignores it
+        g = torch.full((w.B, w.H), 0.5, device=dev)
     var = la.VARIANTS[w.variant]
     ss = la.state_size(w.variant, w.dk, w.dv)
     sin = torch.randn((w.B, w.H, ss), device=dev) * 0.1
@@ -46,6 +50,7 @@ def _run_both(w, seed):
     rc = la.la_forward_noalloc(cfg, P(q), P(k), P(v), P(g), P(b), P(sin), P(o), P(s), P(den), var, w.T,
                                la._stream_ptr(None))
     assert rc == la.LA_OK
+    assert la.la_noalloc_status(dev.index, la._stream_ptr(None)) == la.LA_OK
     torch.cuda.synchronize()
     h.close()
     return (from_torch(o), s.cpu().numpy(), None if den is None else den.cpu().numpy(),
@@ -93,3 +98,68 @@ def test_noalloc_rejects_what_it_cannot_run():
     bf = la.la_config(1, 1, 64, 64, la.LA_BF16, 0, dev)
     assert la.la_forward_noalloc(bf, P, P, P, None, None, None, P, None, None, la.LA_GDN, 8, st) == la.LA_ERR_INVALID_ARG
     assert la.la_forward_noalloc(bf, P + 4, P, P, None, None, None, P, None, None, la.LA_NORM_ELU1, 8, st) == la.LA_ERR_MISALIGNED
+
+
+def test_noalloc_ignores_a_gate_for_the_undecayed_normalized_variant():
+    w = W.small(W.NORM_B4H8_T2048_D64, B=1, H=2, T=1000, dk=128, dv=128)
+    o, s, den, o_ref, s_ref, den_ref = _run_both(w, 4, gate_for_norm=True)
+    assert _rel(o, o_ref) <= TOL["bf16"]
+    assert _rel(s, s_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("variant", ["norm", "gla", "gdn"])
+def test_noalloc_matches_the_oracle(variant):
+    # One call per variant against the float64 oracle directly, on the same
+    # seeded inputs (T with a ragged tail; the norm and gla shapes split
+    # into segments whose summaries live in the static scratch).
+    base = {"norm": W.NORM_B4H8_T2048_D64, "gla": W.GLA_B4H16_T4096_D128, "gdn": W.GDN_B2H16_T8192_D128}[variant]
+    w = W.small(base, B=1, H=2, T=777, dk=128, dv=128)
+    x = W.draw(w, 5)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v = (to_torch(a, dev) for a in (x.q, x.k, x.v))
+    g, b = to_torch(x.gate, dev), to_torch(x.beta, dev)
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=torch.bfloat16, device=dev)
+    s = torch.empty((w.B, w.H, la.state_size(w.variant, w.dk, w.dv)), device=dev)
+    den = torch.empty((w.B, w.H, w.T), device=dev) if variant == "norm" else None
+    cfg = la.la_config(w.B, w.H, w.dk, w.dv, la.LA_BF16, 0, dev.index)
+    P = lambda t: None if t is None else t.data_ptr()
+    st = la._stream_ptr(None)
+    assert la.la_forward_noalloc(cfg, P(q), P(k), P(v), P(g), P(b), None, P(o), P(s), P(den),
+                                 la.VARIANTS[variant], w.T, st) == la.LA_OK
+    assert la.la_noalloc_status(dev.index, st) == la.LA_OK
+    ref = oracle.run(w.variant, *oracle_inputs(x))
+    assert slice_rel_err(from_torch(o), ref.o) <= TOL["bf16"]
+    assert slice_rel_err(s.cpu().numpy(), ref.state) <= TOL["bf16"]
+    if den is not None:
+        assert float(np.max(np.abs(den.cpu().numpy() - ref.den) / ref.den)) <= TOL["bf16"]
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("variant,T", [("gdn", 128), ("norm", 512)])
+def test_noalloc_status_reports_an_expired_wait(variant, T):
+    # The test hook makes the chunked kernel wait once on a barrier nothing
+    # signals; the wait gives up after 1 ms and records it in the status word
+    # of the static scratch. la_noalloc_status reports it once, then the word
+    # is clear, and the next call computes normally.
+    base = {"norm": W.NORM_B4H8_T2048_D64, "gdn": W.GDN_B2H16_T8192_D128}[variant]
+    w = W.small(base, B=1, H=2, T=T, dk=64, dv=64)
+    x = W.draw(w, 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v = (to_torch(a, dev) for a in (x.q, x.k, x.v))
+    g, b = to_torch(x.gate, dev), to_torch(x.beta, dev)
+    o = torch.empty((w.B, w.H, w.T, w.dv), dtype=torch.bfloat16, device=dev)
+    s = torch.empty((w.B, w.H, la.state_size(w.variant, w.dk, w.dv)), device=dev)
+    P = lambda t: None if t is None else t.data_ptr()
+    st = la._stream_ptr(None)
+    hook = la.la_config(w.B, w.H, w.dk, w.dv, la.LA_BF16, la.LA_FLAG_TEST_TIMEOUT, dev.index)
+    assert la.la_forward_noalloc(hook, P(q), P(k), P(v), P(g), P(b), None, P(o), P(s), None,
+                                 la.VARIANTS[variant], w.T, st) == la.LA_OK
+    assert la.la_noalloc_status(dev.index, st) == la.LA_ERR_TIMEOUT
+    assert la.la_noalloc_status(dev.index, st) == la.LA_OK      # read once, then cleared
+    plain = la.la_config(w.B, w.H, w.dk, w.dv, la.LA_BF16, 0, dev.index)
+    assert la.la_forward_noalloc(plain, P(q), P(k), P(v), P(g), P(b), None, P(o), P(s), None,
+                                 la.VARIANTS[variant], w.T, st) == la.LA_OK
+    assert la.la_noalloc_status(dev.index, st) == la.LA_OK
+    ref = oracle.run(w.variant, *oracle_inputs(x))
+    assert slice_rel_err(from_torch(o), ref.o) <= TOL["bf16"]
+    assert la.la_noalloc_status(dev.index + 1000, st) == la.LA_ERR_INVALID_ARG
