@@ -86,7 +86,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // delta rule's launcher accepts (it sizes its windows to the scratch).
 size_t scratch_needed(int variant, int BH, int T, int dk, int dv, int sms) {
     const int nch = (T + 63) / 64;
-    if (variant == LA_GDN) return la::chunk::gdn_workspace_bytes(BH, dk, dv, 1);
+    // the gated delta rule, and the gated variant when the three-phase form
+    // does not fit: the least ring the prep/chain launcher accepts
+    if (variant == LA_GDN || variant == LA_GLA) return la::chunk::gdn_workspace_bytes(BH, dk, dv, 1);
     if (BH >= sms || nch < 4) return 0;
     int nseg = sms / BH;
     if (nseg > nch / 2) nseg = nch / 2;

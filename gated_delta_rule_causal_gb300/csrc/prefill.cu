@@ -18,17 +18,6 @@ CUresult map_qkv(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const vo
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// 3-D map over the per-channel gates [BH, T, dk] fp32, full-width boxes.
-CUresult map_gate(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base, int dk, int T, int BH) {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(dk), static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(dk) * 4, static_cast<cuuint64_t>(dk) * 4 * T};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(dk), static_cast<cuuint32_t>(chunk::C), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-}
-
 }  // namespace
 
 cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEncodeTiled_v12000 enc, const char** what) {
@@ -38,12 +27,11 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     if (map_qkv(enc, &m.k, a.k, a.dk, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (map_qkv(enc, &m.v, a.v, a.dv, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (map_qkv(enc, &m.o, a.out, a.dv, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (a.variant == kGla) {
-        if (map_gate(enc, &m.g, a.gate, a.dk, a.T, a.BH) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    } else {
-        m.g = m.q;
-    }
-    if (a.variant == kGdn || a.variant == kKda) {
+    // The gated delta rule, its per-channel-decay form and the per-channel
+    // gated variant (the delta rule's chunk algebra with T = I and W = 0) run
+    // on the prep/chain kernel, whose in-chunk decay factors are taken
+    // against 16-token sub-chunk references and so stay in the fp32 range.
+    if (a.variant == kGdn || a.variant == kKda || a.variant == kGla) {
         *what = "chunked prefill launch";
         return chunk::launch_gdn(a, m, s);
     }
@@ -92,11 +80,8 @@ cudaError_t launch_chunked(const FwdArgs& a, cudaStream_t s, PFN_cuTensorMapEnco
     }
     *what = "chunked prefill launch";
     if (a.nlaunch) *a.nlaunch += (p.nseg > 1) ? 2 : 1;   // segment summaries + chunk kernel
-    switch (a.variant) {
-        case kNorm: return chunk::launch_norm(a.dk, a.dv, m, p, a.BH, s);
-        case kGla: return chunk::launch_gla(a.dk, a.dv, m, p, a.BH, s);
-        default: return cudaErrorInvalidValue;
-    }
+    if (a.variant != kNorm) return cudaErrorInvalidValue;
+    return chunk::launch_norm(a.dk, a.dv, m, p, a.BH, s);
 }
 
 }  // namespace la

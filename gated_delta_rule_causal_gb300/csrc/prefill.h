@@ -11,15 +11,16 @@ namespace la {
 namespace chunk {
 
 struct Maps {
-    CUtensorMap q, k, v, g, o;
+    CUtensorMap q, k, v, o;
 };
 
 struct Params;
 
+// Normalized variant: the sequential chunk kernel (with segment summaries).
 cudaError_t launch_norm(int dk, int dv, const Maps& m, const Params& p, int BH, cudaStream_t s);
-cudaError_t launch_gla(int dk, int dv, const Maps& m, const Params& p, int BH, cudaStream_t s);
 
-// Gated delta rule, scalar or per-channel (kda) decay: one cooperative
+// Gated delta rule (scalar or per-channel decay) and per-channel gated
+// attention (the same kernel with T = I and W = 0): one cooperative
 // launch per group of at most kGdnMaxGroup sequence-heads, in which prep CTAs
 // feed a ring of per-chunk slots to one chain CTA per head; the workspace
 // holds the hand-off flags and the ring (2 kGdnWindow chunks per head at
@@ -40,7 +41,7 @@ cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s);
 bool seg_fits(int BH, int T, int dk, int dv, int sm_count);
 cudaError_t launch_seg(const FwdArgs& a, const Maps& m, cudaStream_t s);
 
-// Normalized / per-channel gated: three fully parallel phases (chunk
+// Normalized: three fully parallel phases (chunk
 // summaries, a scan over the chunks, outputs) when the per-chunk states of
 // the whole problem fit in the workspace and comfortably in L2.
 constexpr size_t kParL2Bytes = size_t(48) << 20;

@@ -58,9 +58,19 @@
 // [K;Q] o 2^(G_t - r_a) and the column operand K o 2^(r_a - G_j) of the
 // pair products span at most eight tokens of decay each; columns of later
 // sub-chunks b > a(j) use 2^(r_b - G_j) <= 1. Every other factor (Gam_t,
-// Gam_C / Gam_t, Gam_C) is at most 1. Exact in fp32 while every alpha >=
-// 2^-15. The prep CTAs write Q o Gam and K o Gam_C / Gam into the slot, so
-// the chain CTAs load no q or k tiles of their own.
+// Gam_C / Gam_t, Gam_C) is at most 1. A per-token decay below 2^-15 is
+// taken as 2^-15, which keeps eight tokens of decay within 2^120: the
+// factors are exact in fp32 for every decay, and the only departure from the
+// recurrence is that what crosses a token of decay alpha < 2^-15 is scaled
+// by 2^-15 instead of alpha. The prep CTAs write Q o Gam and K o Gam_C / Gam
+// into the slot, so the chain CTAs load no q or k tiles of their own.
+//
+// Per-channel gated attention (GLA / RetNet family, "Linear attention and
+// Hyena" 11.3: S_t = diag(gamma_t) S_{t-1} + phi(k_t) v_t^T) is the same
+// per-channel chunk algebra without the delta rule: T = I, W = 0, so
+// Ut = V, N_c = 0 and E_c = (phi(Q) o Gam)^T. It runs through the prep CTAs
+// of the per-channel decay (no inverse) and the chain CTAs with the state
+// product X_c E_c alone.
 #include <atomic>
 
 #include "prefill.h"
@@ -71,6 +81,7 @@ namespace la {
 namespace gdn {
 
 using chunk::C;
+using chunk::elu1;
 using chunk::kAStride;
 using chunk::kmaj;
 using chunk::ld_shared_bf16;
@@ -204,9 +215,11 @@ struct PrepLayoutKda {
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
-template <int DK, int DV, bool KDA>
+// MODE: 0 = scalar gate (gated delta rule), 1 = per-channel decay delta rule,
+// 2 = per-channel gated attention without the delta rule.
+template <int DK, int DV, int MODE>
 constexpr uint32_t smem_alloc() {
-    constexpr uint32_t prep = KDA ? PrepLayoutKda<DK, DV>::BYTES : PrepLayout<DK, DV>::BYTES;
+    constexpr uint32_t prep = MODE ? PrepLayoutKda<DK, DV>::BYTES : PrepLayout<DK, DV>::BYTES;
     constexpr uint32_t chain = ChainLayout<DK, DV>::BYTES;
     return (chain > prep ? chain : prep) + 1024;
 }
@@ -271,7 +284,10 @@ __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
 //               as the bf16 operand; o = O_b through the output tile.
 // Only state(c) and the state update lie on the path from one chunk to the
 // next.
-template <int DK, int DV>
+// GLA: the per-channel gated variant without the delta rule. N_c = 0, so the
+// state product is X_c E_c alone and part B of the slot is E_c; the state is
+// read and written in that variant's orientation S = X^T [DK][DV].
+template <int DK, int DV, bool GLA>
 __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params& p, uint8_t* sm, uint32_t sbase) {
     using L = ChainLayout<DK, DV>;
     using S = Slot<DK, DV>;
@@ -336,6 +352,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
     constexpr uint32_t ID_K = idesc_bf16(128, DK, false, true);        // Ut^T K'
     constexpr uint32_t ID_P = idesc_bf16(128, 64, false, false);       // Ut^T P^T
     constexpr uint32_t ID_X = idesc_bf16(128, DK + 64, false, true);   // X_c [-N_c | E_c]
+    constexpr uint32_t ID_E = idesc_bf16(128, 64, false, true);        // X_c E_c (GLA)
     auto col_s = [](int b) { return L::COL_S + 256u * b; };             // S_b; O_b follows at + DK
 
     if (control) {
@@ -371,9 +388,14 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                 const int b = c & 1;
                 const uint32_t stg = sbase + b * L::STAGE;
 #pragma unroll
-                for (int kk = 0; kk < DK / 16; ++kk)
-                    mma_bf16_ss(tmem + col_s(b), kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
-                                mnmaj(stg + S::NC_OFF + kk * 2048, DK * 128), ID_X, true);
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                    if (GLA)
+                        mma_bf16_ss(tmem + col_s(b) + DK, kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
+                                    mnmaj(stg + S::E_OFF + kk * 2048, 8192), ID_E, true);
+                    else
+                        mma_bf16_ss(tmem + col_s(b), kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
+                                    mnmaj(stg + S::NC_OFF + kk * 2048, DK * 128), ID_X, true);
+                }
                 mma_commit(bar_s);
                 ++n_s;
             };
@@ -457,8 +479,13 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                     load_idx[s] = c;
                     if (c >= 2) wait(&bar_sfree[s], ((c - 2) >> 1) & 1, kStatusMmaWait);
                     if (fail) break;
-                    mbar_arrive_expect_tx(&bar_fullb[s], S::B_BYTES);
-                    bulk_load(stg, src, S::B_BYTES, &bar_fullb[s]);
+                    if (GLA) {   // part B is E_c alone
+                        mbar_arrive_expect_tx(&bar_fullb[s], DK * 128);
+                        bulk_load(stg + S::E_OFF, src + S::E_OFF, DK * 128, &bar_fullb[s]);
+                    } else {
+                        mbar_arrive_expect_tx(&bar_fullb[s], S::B_BYTES);
+                        bulk_load(stg, src, S::B_BYTES, &bar_fullb[s]);
+                    }
                     pendb[s] = true;
                 }
                 // chunk c - 2's output store (the only one in flight) has long
@@ -503,7 +530,14 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
 #pragma unroll
         for (int i = 0; i < DKH; i += 4) {
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (own && sin) x = *reinterpret_cast<const float4*>(sin + static_cast<size_t>(r) * DK + hh * DKH + i);
+            if (own && sin) {
+                if (GLA) {   // S[c][r]: a warp reads 32 consecutive r of each row c
+                    const float* sc = sin + static_cast<size_t>(hh * DKH + i) * DV + r;
+                    x = make_float4(sc[0], sc[DV], sc[2 * DV], sc[3 * DV]);
+                } else {
+                    x = *reinterpret_cast<const float4*>(sin + static_cast<size_t>(r) * DK + hh * DKH + i);
+                }
+            }
             st[i] = x.x;
             st[i + 1] = x.y;
             st[i + 2] = x.z;
@@ -583,10 +617,15 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
         if (!bad) {
             float* dst = p.state_out ? p.state_out + bh * ssz : nullptr;
             if (dst && own) {
+                if (GLA) {
 #pragma unroll
-                for (int i = 0; i < DKH; i += 4)
-                    *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * DK + hh * DKH + i) =
-                        make_float4(st[i], st[i + 1], st[i + 2], st[i + 3]);
+                    for (int i = 0; i < DKH; ++i) dst[static_cast<size_t>(hh * DKH + i) * DV + r] = st[i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < DKH; i += 4)
+                        *reinterpret_cast<float4*>(dst + static_cast<size_t>(r) * DK + hh * DKH + i) =
+                            make_float4(st[i], st[i + 1], st[i + 2], st[i + 3]);
+                }
             }
         } else if (tid == 0) {
             if (!failed) status_bits |= kStatusMmaWait;
@@ -1066,11 +1105,19 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
 // ============================================================================
 // prep CTA of the per-channel decay (8 warps)
 // ============================================================================
-// Exponent kept inside the fp32 range, so that a factor stays finite even
-// for decays below the form's stated limit.
+// Per-token log2 decays are floored here, so that the factors of the
+// 16-token sub-chunk references (at most eight tokens of decay each) stay
+// inside the fp32 exponent range.
+constexpr float kLog2DecayFloor = -15.f;
+// Exponent kept inside the fp32 range (a guard: with the floor above no
+// factor reaches it).
 __device__ __forceinline__ float ex2c(float x) { return ex2(fminf(fmaxf(x, -126.f), 126.f)); }
 
-template <int DK, int DV>
+// GLA: the per-channel gated variant without the delta rule (no beta, T = I,
+// W = 0). q and k pass through the feature map phi (elu + 1, or the identity
+// under the flag) first; the unit then needs only P, Ut^T = V^T, K' and
+// E_c = (phi(Q) o Gam)^T, no inverse and no product after P.
+template <int DK, int DV, bool GLA>
 __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                               const Params& p, uint8_t* sm, uint32_t sbase) {
     using L = PrepLayoutKda<DK, DV>;
@@ -1087,6 +1134,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     const int np = gridDim.x - p.n_chain;
     const int nunits = p.G * p.nch;
     const int T = p.T;
+    const bool phi_on = GLA && !(p.flags & 0x1u);   // the GLA feature map elu + 1 unless disabled
     // element pass: thread (cp, seg) owns channels c0, c0 + 1 of tokens
     // [seg*SL, seg*SL + SL), all inside sub-chunk sa
     const int cp = tid % NCP, seg = tid / NCP;
@@ -1198,7 +1246,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
         ++g_issued;
     };
     auto load_b = [&](int u) {   // asynchronously, one token per thread (threads 0-63)
-        if (u < nunits && tid < 64) {
+        if (!GLA && u < nunits && tid < 64) {
             const int bh = p.h0 + unit_g(u);
             const int t = unit_i(u) * C + tid;
             if (t < T) {
@@ -1239,8 +1287,12 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 const int t = seg * SL + i;
                 float2 g = make_float2(1.f, 1.f);
                 if (t < nvalid) g = *reinterpret_cast<const float2*>(sGate + t * DK + c0);
-                a0 += lg2(g.x);
-                a1 += lg2(g.y);
+                // A decay below 2^-15 acts as 2^-15 (kLog2DecayFloor): eight
+                // tokens of decay then span at most 2^120, so every factor
+                // below is exact in fp32; what crosses such a token is still
+                // scaled down by 2^-15 or more.
+                a0 += fmaxf(lg2(g.x), kLog2DecayFloor);
+                a1 += fmaxf(lg2(g.y), kLog2DecayFloor);
                 lp0[i] = a0;
                 lp1[i] = a1;
             }
@@ -1249,7 +1301,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 *reinterpret_cast<float2*>(sBlk + (blk0 + 1) * DK + c0) =
                     make_float2(lp0[SL - 1] - lp0[7], lp1[SL - 1] - lp1[7]);
         }
-        if (tid < 64) {
+        if (!GLA && tid < 64) {
             cp_async_wait();   // this thread's own copy
             sB[tid] = sBin[tid];
         }
@@ -1306,8 +1358,15 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 const uint32_t ro = sw128_off(t, ch) + bo;   // in [64][DK] tiles of 8 KB atoms
                 const uint32_t ak = aKQ + ro;
                 const uint32_t aq = aKQ + sw128_off(64 + t, ch) + bo;
-                const float2 kv = unpack_bf16(ld_shared_b32(ak));
-                const float2 qv = unpack_bf16(ld_shared_b32(aq));
+                float2 kv = unpack_bf16(ld_shared_b32(ak));
+                float2 qv = unpack_bf16(ld_shared_b32(aq));
+                if (GLA) {
+                    if (phi_on) {
+                        kv = make_float2(elu1(kv.x), elu1(kv.y));
+                        qv = make_float2(elu1(qv.x), elu1(qv.y));
+                    }
+                    if (t >= nvalid) kv = make_float2(0.f, 0.f);   // phi(0) = 1: padded keys write nothing
+                }
                 const float G0 = off0 + lp0[i], G1 = off1 + lp1[i];
                 const float e10 = ex2c(G0 - ra0), e11 = ex2c(G1 - ra1);
                 const float e20 = ex2c(ra0 - G0), e21 = ex2c(ra1 - G1);
@@ -1408,18 +1467,20 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 for (int i = 0; i < 32; ++i) x[i] = hi ? y[i] : x[i];
             }
             if ((warp & 3) < 2) {
-                // A_tj = beta_t (k_t o Gam_t).(k_j / Gam_j) for j < t
-                const int t = r;
-                const float bt = sB[t];
+                if (!GLA) {   // (no A without the delta rule)
+                    // A_tj = beta_t (k_t o Gam_t).(k_j / Gam_j) for j < t
+                    const int t = r;
+                    const float bt = sB[t];
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int j = 32 * hh + 4 * m;
-                    float4 o;
-                    o.x = (j + 0 < t) ? bt * x[4 * m + 0] : 0.f;
-                    o.y = (j + 1 < t) ? bt * x[4 * m + 1] : 0.f;
-                    o.z = (j + 2 < t) ? bt * x[4 * m + 2] : 0.f;
-                    o.w = (j + 3 < t) ? bt * x[4 * m + 3] : 0.f;
-                    *reinterpret_cast<float4*>(As + t * kAStride + j) = o;
+                    for (int m = 0; m < 8; ++m) {
+                        const int j = 32 * hh + 4 * m;
+                        float4 o;
+                        o.x = (j + 0 < t) ? bt * x[4 * m + 0] : 0.f;
+                        o.y = (j + 1 < t) ? bt * x[4 * m + 1] : 0.f;
+                        o.z = (j + 2 < t) ? bt * x[4 * m + 2] : 0.f;
+                        o.w = (j + 3 < t) ? bt * x[4 * m + 3] : 0.f;
+                        *reinterpret_cast<float4*>(As + t * kAStride + j) = o;
+                    }
                 }
             } else {
                 // P_tj = (q_t o Gam_t).(k_j / Gam_j) for j <= t
@@ -1431,6 +1492,37 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
                 }
                 store_row32_bf16(aOut + S::P_OFF, t, 4 * hh, x);
             }
+        }
+        if constexpr (GLA) {
+            // ---- Ut^T = V^T and E_c = (phi(Q) o Gam)^T, both by transposing in
+            //      shared memory: thread (r, hh) gathers column r of 32 tokens --------
+            if (!wait_all(bar_v, k & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
+            if (tid == 0) ++v_done;
+            float qg[32], vt[32];
+            if (r < DK) {
+                const uint32_t aq = aOut + S::E_OFF + (r / 64) * 8192 + (r % 8) * 2;
+                const uint32_t c8 = (r % 64) / 8;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) qg[i] = ld_shared_bf16(aq + sw128_off(32 * hh + i, c8));
+            }
+            if (r < DV) {
+                const uint32_t av = aV + (r / 64) * 8192 + (r % 8) * 2;
+                const uint32_t c8 = (r % 64) / 8;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) vt[i] = ld_shared_bf16(av + sw128_off(32 * hh + i, c8));
+            }
+            sync_conv();   // Q o Gam and V are read
+            if (tid == 0 && un < nunits) {
+                fence_proxy_async_smem();
+                issue_v(un);
+            }
+            if (r < DK) store_row32_bf16(aOut + S::E_OFF, r, 4 * hh, qg);
+            if (r < DV) store_row32_bf16(aOut + S::U_OFF, r, 4 * hh, vt);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            sync_conv();
+            if (tid == 0) mbar_arrive(&slot_full[0]);   // to the store warp
+            continue;
         }
         sync_conv();
         invert_unit_lower(As, Rs, warp, lane);
@@ -1533,7 +1625,7 @@ __device__ __forceinline__ void prep_role_kda(const CUtensorMap* tmq, const CUte
     if (status_bits && tid == 0) atomicOr(p.status, status_bits);
 }
 
-template <int DK, int DV, bool KDA>
+template <int DK, int DV, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
            const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const Params p) {
@@ -1542,11 +1634,11 @@ gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (sbase - raw);
     if (static_cast<int>(blockIdx.x) < p.n_chain) {
-        chain_role<DK, DV>(&tmo, p, sm, sbase);
+        chain_role<DK, DV, MODE == 2>(&tmo, p, sm, sbase);
     } else {
         if (threadIdx.x >= kConv + 32) return;   // the prep role: eight converting warps and a store warp
-        if constexpr (KDA)
-            prep_role_kda<DK, DV>(&tmq, &tmk, &tmv, p, sm, sbase);
+        if constexpr (MODE != 0)
+            prep_role_kda<DK, DV, MODE == 2>(&tmq, &tmk, &tmv, p, sm, sbase);
         else
             prep_role<DK, DV>(&tmq, &tmk, &tmv, p, sm, sbase);
     }
@@ -1556,11 +1648,11 @@ gdn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUte
 // flag of an earlier launch is never mistaken for one of this launch.
 std::atomic<unsigned> g_epoch{0};
 
-template <int DK, int DV, bool KDA>
+template <int DK, int DV, int MODE>
 cudaError_t run(const chunk::Maps& m, const FwdArgs& a, int G, int R, cudaStream_t s) {
-    constexpr uint32_t smem = smem_alloc<DK, DV, KDA>();
+    constexpr uint32_t smem = smem_alloc<DK, DV, MODE>();
     static_assert(smem <= 232448, "shared memory budget");
-    auto kern = gdn_kernel<DK, DV, KDA>;
+    auto kern = gdn_kernel<DK, DV, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nch = (a.T + C - 1) / C;
@@ -1618,7 +1710,7 @@ size_t gdn_workspace_bytes(int BH, int dk, int dv, int W) { return ring_bytes(gd
 
 cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     const int G = gdn_group(a.BH);
-    const bool kda = a.variant == kKda;
+    const int mode = a.variant == kKda ? 1 : a.variant == kGla ? 2 : 0;
     const int nch = (a.T + C - 1) / C;
     // the deepest ring (up to 2 kGdnWindow chunks, no deeper than the
     // sequence) that the workspace holds
@@ -1626,17 +1718,24 @@ cudaError_t launch_gdn(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     if (R > nch) R = nch < 2 ? 2 : nch;
     while (R > 2 && ring_bytes(G, R, a.dk, a.dv) > a.ws_bytes) --R;
     if (!a.workspace || ring_bytes(G, R, a.dk, a.dv) > a.ws_bytes) return cudaErrorInvalidValue;
-    if (kda) {
-        if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, true>(m, a, G, R, s);
-        if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, true>(m, a, G, R, s);
-        if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, true>(m, a, G, R, s);
-        if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, true>(m, a, G, R, s);
+    if (mode == 2) {
+        if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, 2>(m, a, G, R, s);
+        if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, 2>(m, a, G, R, s);
+        if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, 2>(m, a, G, R, s);
+        if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, 2>(m, a, G, R, s);
         return cudaErrorInvalidValue;
     }
-    if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, false>(m, a, G, R, s);
-    if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, false>(m, a, G, R, s);
-    if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, false>(m, a, G, R, s);
-    if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, false>(m, a, G, R, s);
+    if (mode == 1) {
+        if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, 1>(m, a, G, R, s);
+        if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, 1>(m, a, G, R, s);
+        if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, 1>(m, a, G, R, s);
+        if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, 1>(m, a, G, R, s);
+        return cudaErrorInvalidValue;
+    }
+    if (a.dk == 64 && a.dv == 64) return gdn::run<64, 64, 0>(m, a, G, R, s);
+    if (a.dk == 64 && a.dv == 128) return gdn::run<64, 128, 0>(m, a, G, R, s);
+    if (a.dk == 128 && a.dv == 64) return gdn::run<128, 64, 0>(m, a, G, R, s);
+    if (a.dk == 128 && a.dv == 128) return gdn::run<128, 128, 0>(m, a, G, R, s);
     return cudaErrorInvalidValue;
 }
 

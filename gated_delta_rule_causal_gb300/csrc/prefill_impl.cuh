@@ -1,39 +1,31 @@
-// Chunkwise prefill on the tcgen05 tensor cores (sm_103a): normalized and
-// per-channel gated variants (the gated delta rule is in prefill_gdn.cu and
-// shares the helpers below).
+// Chunkwise prefill on the tcgen05 tensor cores (sm_103a): the normalized
+// variant's sequential chunk kernel and its segment summaries (the gated
+// variants run on the prep/chain kernel of prefill_gdn.cu, which shares the
+// helpers below). VAR is kNorm.
 //
 // One CTA per (b,h) sequence-head walks its sequence in chunks of C = 64
-// tokens. TMA stages the q/k/v tiles (and the per-channel gate tile of the
-// gated variant) of chunk c+1 while chunk c is computed. The dense products
+// tokens. TMA stages the q/k/v tiles of chunk c+1 while chunk c is computed. The dense products
 // run as tcgen05 bf16 MMAs with fp32 accumulators in tensor memory. The
 // fp32 state lives in registers and is re-published each chunk as a bf16 MMA
 // operand in shared memory. Outputs leave through a shared-memory tile and a
 // TMA store.
 //
 // Inside the kernel the state is held as X = S^T [d_v rows][d_k cols] (S is
-// d_k x d_v for these variants). With that orientation the state products have M = 128 (value rows, padded when
+// d_k x d_v for this variant). With that orientation the state products have M = 128 (value rows, padded when
 // d_v = 64); the output products put the 64 tokens on M (rows 64-127 of
 // those accumulators are unused) so each thread writes whole output rows. The 256 threads pair up on the 128
 // tensor-memory lanes: thread (r, h) owns row r and the h-th half of the
 // columns of whatever it reads (warp w serves lanes 32*(w%4).., h = w/4).
 //
-// Chunk algebra (G_t = sum of log-gates inside the chunk up to t, Gam_t =
-// exp(G_t), L = causal mask including the diagonal):
-//
-//  norm / gla ("Linear attention and Hyena" 11.2-11.3, secondary rescaling):
-//    q~_t = phi(q_t) * Gam_t,  k~_j = phi(k_j) / Gam_j
+// Chunk algebra ("Linear attention and Hyena" 11.2, L = causal mask
+// including the diagonal, q~ = phi(q), k~ = phi(k)):
 //    O    = Q~ X_0^T + (L o Q~ K~^T) V
-//    X    = diag-cols(Gam_C) (X_0 + V^T K~)
-//    norm adds den_t = q~_t . z_0 + sum_{j<=t} q~_t . k~_j, o_t = num_t / den_t.
+//    X    = X_0 + V^T K~
+//    den_t = q~_t . z_0 + sum_{j<=t} q~_t . k~_j, o_t = num_t / den_t.
 //
 // Tail chunks (T not a multiple of 64): TMA zero-fills rows past the end.
-// phi(0) = 1, so padded keys are zeroed explicitly and padded gates read as 1,
-// which makes padded tokens leave the state untouched; the TMA store clips
-// rows past the end.
-//
-// Limit of the per-channel gated variant: the in-chunk rescaling divides by
-// Gam_j, so the product of 64 consecutive gates of one channel must stay
-// above ~1e-38 (fp32 range); per-token gates >= 0.25 always satisfy it.
+// phi(0) = 1, so padded keys are zeroed explicitly, which makes padded
+// tokens leave the state untouched; the TMA store clips rows past the end.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -61,8 +53,7 @@ struct Params {
     // last segment are also cut into nsub summary runs of sub_len chunks
     // (sub_len divides seg_len). scratch holds, for every (b,h) and every
     // summary run, the state that run produces from a zero start: X [DV][DK]
-    // followed by DK floats (gla: the run's per-channel decay; norm: its sum
-    // of phi(k)).
+    // followed by DK floats (its sum of phi(k)).
     int nseg;
     int seg_len;
     int nsub;
@@ -77,20 +68,17 @@ struct Layout {
     // q/k tile pair: per k-atom, rows 0-63 hold block 0 and rows 64-127 block 1.
     static constexpr uint32_t QK_BYTES = KA * 16384;
     static constexpr uint32_t V_BYTES = VA * 8192;
-    static constexpr uint32_t G_BYTES = (VAR == kGla) ? C * DK * 4 : 0;
-    static constexpr uint32_t STAGE = QK_BYTES + V_BYTES + G_BYTES;
-    static constexpr uint32_t TX_BYTES = 2 * KA * 8192 + V_BYTES + G_BYTES;
+    static constexpr uint32_t STAGE = QK_BYTES + V_BYTES;
+    static constexpr uint32_t TX_BYTES = 2 * KA * 8192 + V_BYTES;
     // bf16 P [64 t][64 j]. The P V product reads it as a 128-row A operand,
     // so the 8 KB after it (rows 64-127, whose results are unused) must be
     // shared memory of this CTA: the state tile follows.
     static constexpr uint32_t OFF_PS = 2 * STAGE;
     static constexpr uint32_t OFF_SS = OFF_PS + 8192;             // bf16 state [128 rows][DK]
-    // output tile [64 t][DV] (norm: own buffer; gla: the current stage's gate
-    // tile, free once the gates are consumed)
-    static constexpr uint32_t OFF_OT = OFF_SS + KA * 16384;
-    static constexpr uint32_t OT_BYTES = (VAR == kNorm) ? VA * 8192 : 0;
+    static constexpr uint32_t OFF_OT = OFF_SS + KA * 16384;       // output tile [64 t][DV]
+    static constexpr uint32_t OT_BYTES = VA * 8192;
     static constexpr uint32_t OFF_MISC = OFF_OT + OT_BYTES;
-    static constexpr uint32_t MISC_BYTES = (128 + 3 * 128 + 256) * 4;
+    static constexpr uint32_t MISC_BYTES = 3 * 128 * 4;            // den, z, this chunk's sum of phi(k)
     static constexpr uint32_t OFF_BAR = OFF_MISC + MISC_BYTES;
     static constexpr uint32_t BYTES = OFF_BAR + 64;
     static constexpr uint32_t SMEM_ALLOC = BYTES + 1024;  // slack to align the base to 1024
@@ -162,9 +150,8 @@ __device__ __forceinline__ void scale_chunk(uint32_t addr, float f) {
 template <int VAR, int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-             const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
-             const __grid_constant__ CUtensorMap tmo, const Params p) {
-    static_assert(VAR == kNorm || VAR == kGla, "the gated delta rule has its own kernel");
+             const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo, const Params p) {
+    static_assert(VAR == kNorm, "the gated variants have their own kernel");
     using L = Layout<VAR, DK, DV>;
     constexpr int KA = L::KA, VA = L::VA;
     constexpr int DKH = DK / 2;   // state columns per thread
@@ -181,13 +168,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
     const int T = p.T, nch = p.nchunks;
     const int c_begin = seg * p.seg_len;
     const int nloc = min(nch, c_begin + p.seg_len) - c_begin;
-    const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
 
-    float* sDen = reinterpret_cast<float*>(sm + L::OFF_MISC);   // norm: denominators of the chunk
-    float* sGC = sDen + 128;   // gla: Gam_C per channel (128)
-    float* sZ = sGC + 128;     // norm: z (128)
-    float* sDz = sZ + 128;     // norm: this chunk's sum of phi(k) (128)
-    float* sPart = sDz + 128;  // gla: partial gate products of the scan (256)
+    float* sDen = reinterpret_cast<float*>(sm + L::OFF_MISC);   // denominators of the chunk
+    float* sZ = sDen + 128;    // z (128)
+    float* sDz = sZ + 128;     // this chunk's sum of phi(k) (128)
     uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint64_t* bar_mma = bar_full + 2;
     uint64_t* bar_test = bar_full + 3;
@@ -205,13 +189,12 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
         tma_prefetch_desc(&tmo);
-        if (VAR == kGla) tma_prefetch_desc(&tmg);
     }
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
 
     // ---- initial state: thread (r, hh) owns X[r][hh*DK/2 .. +DK/2) ----------------
     const bool own = r < DV;
-    const size_t ssz = static_cast<size_t>(DK) * DV + (VAR == kNorm ? DK : 0);
+    const size_t ssz = static_cast<size_t>(DK) * DV + DK;
     const float* sin = p.state_in ? p.state_in + bh * ssz : nullptr;
     float st[DKH];
 #pragma unroll
@@ -221,24 +204,21 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         if (own && sin) x = sin[static_cast<size_t>(c) * DV + r];
         st[i] = x;
     }
-    // Later segments start from the states of the summary runs before them,
-    // in order: X = D_u X + X_u.
+    // Later segments start from the states of the summary runs before them:
+    // X = X + X_u.
     const size_t sblk = static_cast<size_t>(DV) * DK + DK;
     const float* sc0 = p.scratch + static_cast<size_t>(bh) * p.nsub * sblk;
     const int nprev = seg * (p.seg_len / p.sub_len);
     if (own) {
         for (int s2 = 0; s2 < nprev; ++s2) {
             const float* xs = sc0 + s2 * sblk + static_cast<size_t>(r) * DK + hh * DKH;
-            const float* ds = sc0 + s2 * sblk + static_cast<size_t>(DV) * DK + hh * DKH;
 #pragma unroll
             for (int i = 0; i < DKH; i += 4) {
                 const float4 x4 = *reinterpret_cast<const float4*>(xs + i);
-                float4 d4 = make_float4(1.f, 1.f, 1.f, 1.f);
-                if (VAR == kGla) d4 = *reinterpret_cast<const float4*>(ds + i);
-                st[i + 0] = d4.x * st[i + 0] + x4.x;
-                st[i + 1] = d4.y * st[i + 1] + x4.y;
-                st[i + 2] = d4.z * st[i + 2] + x4.z;
-                st[i + 3] = d4.w * st[i + 3] + x4.w;
+                st[i + 0] += x4.x;
+                st[i + 1] += x4.y;
+                st[i + 2] += x4.z;
+                st[i + 3] += x4.w;
             }
         }
     }
@@ -250,7 +230,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         }
     };
     publish_state();
-    if (VAR == kNorm && tid < DK) {
+    if (tid < DK) {
         float z = sin ? sin[static_cast<size_t>(DK) * DV + tid] : 0.f;
         for (int s2 = 0; s2 < nprev; ++s2) z += sc0[s2 * sblk + static_cast<size_t>(DV) * DK + tid];
         sZ[tid] = z;
@@ -282,7 +262,6 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         }
 #pragma unroll
         for (int a = 0; a < VA; ++a) tma_load_3d(&tmv, bar, stg + L::QK_BYTES + a * 8192, a * 64, y, bh);
-        if (VAR == kGla) tma_load_3d(&tmg, bar, stg + L::QK_BYTES + L::V_BYTES, 0, y, bh);
     };
 
     if (!failed && tid == 0 && nloc > 0) issue_tma(c_begin, 0);
@@ -305,22 +284,20 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         tc_fence_after();
     };
     // Output epilogue: rows t < 64 of O (thread (t, hh) holds columns
-    // [hh*DV/2, (hh+1)*DV/2)), scaled by 1/den for norm, into the swizzled
+    // [hh*DV/2, (hh+1)*DV/2)), scaled by 1/den, into the swizzled
     // [64 t][DV] tile at `ot`, then one TMA store per 64-column atom.
     auto store_output = [&](uint32_t ot, int t0) {
         if ((warp & 3) < 2) {
             const int t = r;
-            const float sc = (VAR == kNorm) ? __fdividef(1.f, sDen[t]) : 1.f;
+            const float sc = __fdividef(1.f, sDen[t]);
 #pragma unroll
             for (int b = 0; b < DV / 64; ++b) {
                 const int cb = hh * (DV / 2) + 32 * b;
                 float x[32];
                 tmem_ld32(tlane + L::COL_O + cb, x);
                 tmem_ld_wait();
-                if (VAR == kNorm) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] *= sc;
-                }
+                for (int i = 0; i < 32; ++i) x[i] *= sc;
                 store_row32_bf16(ot + (cb / 64) * 8192, t, (cb % 64) / 8, x);
             }
         }
@@ -350,7 +327,6 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         const uint32_t aV = aQK + L::QK_BYTES;
         uint8_t* stg = sm + s * L::STAGE;
         if (tid == 0 && it + 1 < nloc) {
-            if (VAR == kGla) bulk_wait_read_all();  // the output store of chunk c-1 read stage s^1
             fence_proxy_async_smem();
             issue_tma(c + 1, s ^ 1);
         }
@@ -360,48 +336,13 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             tc_fence_after();
         }
 
-        if constexpr (VAR == kGla) {
-            // Running products Gam_t = prod_{i<=t} gamma_i per channel, in place.
-            // 256/DK threads per channel each scan a contiguous part of the chunk.
-            constexpr int NP = kThreads / DK, TP = C / NP;
-            float* gt = reinterpret_cast<float*>(stg + L::QK_BYTES + L::V_BYTES);
-            const int ch = tid % DK, part = tid / DK;
-            float gv[TP];
-#pragma unroll
-            for (int i = 0; i < TP; ++i) {
-                const int t = part * TP + i;
-                gv[i] = (t < nvalid) ? gt[t * DK + ch] : 1.f;
-            }
-            float G = 1.f;
-#pragma unroll
-            for (int i = 0; i < TP; ++i) {
-                G *= gv[i];
-                gv[i] = G;
-            }
-            sPart[part * DK + ch] = G;
-            __syncthreads();
-            float pre = 1.f, tot = 1.f;
-#pragma unroll
-            for (int q = 0; q < NP; ++q) {
-                const float v = sPart[q * DK + ch];
-                if (q < part) pre *= v;
-                tot *= v;
-            }
-#pragma unroll
-            for (int i = 0; i < TP; ++i) gt[(part * TP + i) * DK + ch] = gv[i] * pre;
-            if (part == 0) sGC[ch] = tot;
-            __syncthreads();
-        }
-        if (VAR == kNorm && tid < DK) sDz[tid] = 0.f;
+        if (tid < DK) sDz[tid] = 0.f;
         // q~ (block 0), k~ (block 1) in place, 8 channels per chunk.
         {
-            const float* gt = reinterpret_cast<const float*>(stg + L::QK_BYTES + L::V_BYTES);
 #pragma unroll
             for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
                 const int e = tid + kThreads * i;
                 const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-                const int lc = pc ^ (row & 7);
-                const int c0 = a * 64 + lc * 8;
                 const uint32_t off = (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
                 const uint32_t qa = aQK + a * 16384 + off, ka = qa + 8192;
                 const uint4 uq = ld_shared_v4(qa), uk = ld_shared_v4(ka);
@@ -415,22 +356,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                     k8[4] = b2.x; k8[5] = b2.y; k8[6] = b3.x; k8[7] = b3.y;
                 }
                 const bool valid = row < nvalid;
-                float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
-                if constexpr (VAR == kGla) {
-                    g0 = *reinterpret_cast<const float4*>(gt + row * DK + c0);
-                    g1 = *reinterpret_cast<const float4*>(gt + row * DK + c0 + 4);
-                }
-                const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                 for (int m = 0; m < 8; ++m) {
-                    float qq = phi_on ? elu1(q8[m]) : q8[m];
-                    float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
-                    if constexpr (VAR == kGla) {
-                        qq *= gg[m];
-                        kv *= __fdividef(1.f, gg[m]);
-                    }
-                    q8[m] = qq;
-                    k8[m] = kv;
+                    q8[m] = elu1(q8[m]);
+                    k8[m] = valid ? elu1(k8[m]) : 0.f;
                 }
                 st_shared_v4(qa, pack_bf16(q8[0], q8[1]), pack_bf16(q8[2], q8[3]), pack_bf16(q8[4], q8[5]),
                              pack_bf16(q8[6], q8[7]));
@@ -454,7 +383,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                             ID_128xDK_MM, kk > 0);
             mma_commit(bar_mma);
         }
-        if constexpr (VAR == kNorm) {
+        {
             // While the MMAs run: den_t = q~_t . z_0, and this chunk's sum of phi(k).
             {
                 const int t = tid >> 2, q4 = tid & 3;
@@ -486,7 +415,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
         }
         if (!mma_wait()) { failed = true; break; }
         if ((warp & 3) < 2) {
-            // masked scores of rows t = 0..63 -> bf16 P; norm adds the row sums to den.
+            // masked scores of rows t = 0..63 -> bf16 P; the row sums add to den.
             const int t = r;
             float x[32];
             tmem_ld32(tlane + L::COL_G + 32 * hh, x);
@@ -498,7 +427,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 rs += x[i];
             }
             store_row32_bf16(aPS, t, 4 * hh, x);
-            if (VAR == kNorm) atomicAdd(&sDen[t], rs);
+            atomicAdd(&sDen[t], rs);
         }
         if (own) {
 #pragma unroll
@@ -507,16 +436,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 tmem_ld32(tlane + L::COL_S + hh * DKH + 32 * b, x);
                 tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    if constexpr (VAR == kGla)
-                        st[32 * b + i] = sGC[hh * DKH + 32 * b + i] * (st[32 * b + i] + x[i]);
-                    else
-                        st[32 * b + i] += x[i];
-                }
+                for (int i = 0; i < 32; ++i) st[32 * b + i] += x[i];
             }
             publish_state();
         }
-        if (VAR == kNorm && tid < DK) sZ[tid] += sDz[tid];
+        if (tid < DK) sZ[tid] += sDz[tid];
         publish();
         // ---- O += P V ----------------------------------------------------------
         if (tid == 0) {
@@ -524,13 +448,12 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
             for (int kk = 0; kk < 4; ++kk)
                 mma_bf16_ss(tmem + L::COL_O, kmaj(aPS + kk * 32), mnmaj(aV + kk * 2048, v_lbo), ID_128xDV_KM, 1);
             mma_commit(bar_mma);
-            if (VAR == kNorm) bulk_wait_read_all();  // the previous output store read the tile
+            bulk_wait_read_all();  // the previous output store read the tile
         }
-        if (VAR == kNorm && p.den_out && tid < nvalid)
+        if (p.den_out && tid < nvalid)
             p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
         if (!mma_wait()) { failed = true; break; }
-        const uint32_t ot = (VAR == kGla) ? sbase + s * L::STAGE + L::QK_BYTES + L::V_BYTES : sbase + L::OFF_OT;
-        store_output(ot, t0);
+        store_output(sbase + L::OFF_OT, t0);
     }
 
     // ---- on failure, let an in-flight prefetch land before the CTA exits -----
@@ -549,7 +472,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
                 so[static_cast<size_t>(cc) * DV + r] = st[i];
             }
         }
-        if (VAR == kNorm && tid < DK) so[static_cast<size_t>(DK) * DV + tid] = sZ[tid];
+        if (tid < DK) so[static_cast<size_t>(DK) * DV + tid] = sZ[tid];
     }
     if (tid == 0) bulk_wait_all();
     tc_fence_before();
@@ -560,15 +483,12 @@ chunk_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CU
 
 
 // ---------------------------------------------------------------------------
-// Segment summaries (normalized and per-channel gated variants).
+// Segment summaries of the normalized variant.
 //
 // For summary run u of sequence-head bh (the runs tile every segment but the
 // last), compute the state the run's chunks produce from a zero state,
-//   X_s = sum_c (prod_{c' > c} Gam_C(c')) o (V_c^T K^_c),
-// its per-channel decay D_s = prod_c Gam_C(c) (gla) and its sum of phi(k)
-// (norm), and store them in p.scratch. The chunks are walked last to first so
-// the decay to the run's end folds into K^ (column scaling commutes with
-// V^T K^), and every chunk accumulates into one TMEM accumulator.
+// X_s = sum_c V_c^T phi(K_c), and its sum of phi(k), and store them in
+// p.scratch. Every chunk accumulates into one TMEM accumulator.
 // ---------------------------------------------------------------------------
 template <int VAR, int DK, int DV>
 struct SLayout {
@@ -576,12 +496,11 @@ struct SLayout {
     static constexpr int VA = DV / 64;
     static constexpr uint32_t K_BYTES = KA * 8192;
     static constexpr uint32_t V_BYTES = VA * 8192;
-    static constexpr uint32_t G_BYTES = (VAR == kGla) ? C * DK * 4 : 0;
-    static constexpr uint32_t STAGE = K_BYTES + V_BYTES + G_BYTES;
-    static constexpr uint32_t TX_BYTES = K_BYTES + V_BYTES + G_BYTES;
-    static constexpr uint32_t OFF_KH = 2 * STAGE;                  // k^ [64 j][DK]
+    static constexpr uint32_t STAGE = K_BYTES + V_BYTES;
+    static constexpr uint32_t TX_BYTES = K_BYTES + V_BYTES;
+    static constexpr uint32_t OFF_KH = 2 * STAGE;                  // phi(k) [64 j][DK]
     static constexpr uint32_t OFF_MISC = OFF_KH + KA * 8192;
-    static constexpr uint32_t MISC_BYTES = (128 + 128 + 256 + 128) * 4;   // R, Gam_C, scan parts, z
+    static constexpr uint32_t MISC_BYTES = 128 * 4;                // z
     static constexpr uint32_t OFF_BAR = OFF_MISC + MISC_BYTES;
     static constexpr uint32_t SMEM_ALLOC = OFF_BAR + 64 + 1024;
     static constexpr uint32_t TMEM_COLS = DK <= 64 ? 64 : 128;
@@ -590,8 +509,8 @@ struct SLayout {
 
 template <int VAR, int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-               const __grid_constant__ CUtensorMap tmg, const Params p) {
+summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Params p) {
+    static_assert(VAR == kNorm, "the gated variants have their own kernel");
     using L = SLayout<VAR, DK, DV>;
     constexpr int KA = L::KA, VA = L::VA, DKH = DK / 2;
     extern __shared__ uint8_t smem_raw[];
@@ -605,12 +524,8 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     const int T = p.T;
     const int c_begin = seg * p.sub_len;
     const int nloc = p.sub_len;   // runs lie before the last segment, so they are full
-    const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
 
-    float* sR = reinterpret_cast<float*>(sm + L::OFF_MISC);   // decay from the chunk end to the run's end
-    float* sGC = sR + 128;
-    float* sPart = sGC + 128;
-    float* sZ = sPart + 256;
+    float* sZ = reinterpret_cast<float*>(sm + L::OFF_MISC);
     uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint64_t* bar_mma = bar_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_full + 3);
@@ -623,10 +538,7 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
-    if (tid < DK) {
-        sR[tid] = 1.f;
-        sZ[tid] = 0.f;
-    }
+    if (tid < DK) sZ[tid] = 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -640,7 +552,6 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         for (int a = 0; a < KA; ++a) tma_load_3d(&tmk, &bar_full[s], stg + a * 8192, a * 64, cc * C, bh);
 #pragma unroll
         for (int a = 0; a < VA; ++a) tma_load_3d(&tmv, &bar_full[s], stg + L::K_BYTES + a * 8192, a * 64, cc * C, bh);
-        if (VAR == kGla) tma_load_3d(&tmg, &bar_full[s], stg + L::K_BYTES + L::V_BYTES, 0, cc * C, bh);
     };
     if (tid == 0) issue_tma(c_begin + nloc - 1, 0);
 
@@ -654,7 +565,6 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         const int s = it & 1;
         const int t0 = c * C;
         const int nvalid = min(C, T - t0);
-        uint8_t* stg = sm + s * L::STAGE;
         const uint32_t aK = sbase + s * L::STAGE, aV = aK + L::K_BYTES;
         if (tid == 0 && it + 1 < nloc) {
             fence_proxy_async_smem();
@@ -664,53 +574,18 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             const bool ok = mbar_wait(&bar_full[s], (it >> 1) & 1, kWaitLimitNs);
             if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; break; }
         }
-        float* gt = reinterpret_cast<float*>(stg + L::K_BYTES + L::V_BYTES);
-        if constexpr (VAR == kGla) {
-            constexpr int NP = kThreads / DK, TP = C / NP;
-            const int ch = tid % DK, part = tid / DK;
-            float gv[TP];
-#pragma unroll
-            for (int i = 0; i < TP; ++i) {
-                const int t = part * TP + i;
-                gv[i] = (t < nvalid) ? gt[t * DK + ch] : 1.f;
-            }
-            float G = 1.f;
-#pragma unroll
-            for (int i = 0; i < TP; ++i) {
-                G *= gv[i];
-                gv[i] = G;
-            }
-            sPart[part * DK + ch] = G;
-            __syncthreads();
-            float pre = 1.f, tot = 1.f;
-#pragma unroll
-            for (int q = 0; q < NP; ++q) {
-                const float v = sPart[q * DK + ch];
-                if (q < part) pre *= v;
-                tot *= v;
-            }
-#pragma unroll
-            for (int i = 0; i < TP; ++i) gt[(part * TP + i) * DK + ch] = gv[i] * pre;
-            if (part == 0) sGC[ch] = tot;
-            __syncthreads();
-        }
-        // k^'_j = phi(k_j) * Gam_C / Gam_j * R (gla), phi(k_j) (norm); padded rows 0.
+        // phi(k_j); padded rows 0.
 #pragma unroll
         for (int i = 0; i < (64 * 8 * KA) / kThreads; ++i) {
             const int e = tid + kThreads * i;
             const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-            const int c0 = a * 64 + (pc ^ (row & 7)) * 8;
             const uint32_t off = a * 8192 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
             const uint4 uk = ld_shared_v4(aK + off);
             const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z), b3 = unpack_bf16(uk.w);
             float k8[8] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y, b3.x, b3.y};
             const bool valid = row < nvalid;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
-                if constexpr (VAR == kGla) kv *= sGC[c0 + m] * sR[c0 + m] * __fdividef(1.f, gt[row * DK + c0 + m]);
-                k8[m] = kv;
-            }
+            for (int m = 0; m < 8; ++m) k8[m] = valid ? elu1(k8[m]) : 0.f;
             st_shared_v4(aKH + off, pack_bf16(k8[0], k8[1]), pack_bf16(k8[2], k8[3]), pack_bf16(k8[4], k8[5]),
                          pack_bf16(k8[6], k8[7]));
         }
@@ -724,7 +599,7 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 mma_bf16_ss(tmem, mnmaj(aV + kk * 2048, 8192), mnmaj(aKH + kk * 2048, 8192), ID_MM, (it > 0 || kk > 0));
             mma_commit(bar_mma);
         }
-        if constexpr (VAR == kNorm) {
+        {
             // sum of phi(k) over this chunk: each thread sums a strip of rows of one channel
             constexpr int NP = kThreads / DK, RP = C / NP;
             const int ch = tid % DK, part = tid / DK;
@@ -741,7 +616,6 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             tc_fence_after();
             if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; break; }
         }
-        if (VAR == kGla && tid < DK) sR[tid] *= sGC[tid];
         __syncthreads();
     }
     if (failed && it + 1 < nloc) mbar_wait(&bar_full[(it + 1) & 1], ((it + 1) >> 1) & 1, 100000000ull);
@@ -759,7 +633,7 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
             }
         }
-        if (tid < DK) out[static_cast<size_t>(DV) * DK + tid] = (VAR == kGla) ? sR[tid] : sZ[tid];
+        if (tid < DK) out[static_cast<size_t>(DV) * DK + tid] = sZ[tid];
     }
     tc_fence_before();
     __syncthreads();

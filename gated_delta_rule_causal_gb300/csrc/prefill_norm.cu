@@ -1,4 +1,5 @@
-// Instantiations of the chunkwise prefill kernel for one variant.
+// Instantiations of the normalized variant's sequential chunk kernel and its
+// segment summaries.
 #include "prefill.h"
 #include "prefill_impl.cuh"
 
@@ -15,14 +16,14 @@ cudaError_t run(const Maps& m, const Params& p, int BH, cudaStream_t s) {
         auto sk = summary_kernel<kNorm, DK, DV>;
         e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, SL::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        sk<<<BH * p.nsub, kThreads, SL::SMEM_ALLOC, s>>>(m.k, m.v, m.g, p);
+        sk<<<BH * p.nsub, kThreads, SL::SMEM_ALLOC, s>>>(m.k, m.v, p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     auto kern = chunk_kernel<kNorm, DK, DV>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    kern<<<BH * p.nseg, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.g, m.o, p);
+    kern<<<BH * p.nseg, kThreads, L::SMEM_ALLOC, s>>>(m.q, m.k, m.v, m.o, p);
     return cudaGetLastError();
 }
 

@@ -1,22 +1,19 @@
-// Chunkwise prefill of the normalized and per-channel gated variants in three
-// fully parallel phases, for problems whose per-chunk states fit in L2.
+// Chunkwise prefill of the normalized variant (with or without a fixed decay
+// per sequence-head) in three fully parallel phases, for problems whose
+// per-chunk states fit in L2.
 //
-// The state recurrence of these two variants does not depend on the
-// outputs. With X = S^T [d_v][d_k] and, per chunk c of C = 64 tokens
-// ("Linear attention and Hyena" §11.2-11.3, chunked with the secondary
-// rescaling; Gam_t = running product of the gates inside the chunk, 1 for
-// norm):
-//    dX_c = V_c^T K^_c,   k^_t = phi(k_t) Gam_C / Gam_t
-//    X_c  = D_c o X_{c-1} + dX_c,   D_c = Gam_C per d_k column (1 for norm)
+// The state recurrence does not depend on the outputs. With X = S^T
+// [d_v][d_k] and, per chunk c of C = 64 tokens ("Linear attention and
+// Hyena" §11.2):
+//    dX_c = V_c^T phi(K_c),   X_c = D_c X_{c-1} + dX_c   (D_c = gamma^nvalid, 1 undecayed)
 // so the work splits into
-//  1. summary (per (head, chunk)): dX_c, and D_c (gla) or the chunk's sum
-//     of phi(k) (norm);
+//  1. summary (per (head, chunk)): dX_c and the chunk's sum of phi(k);
 //  2. scan (one thread per 2 state elements): the state entering every
 //     chunk, stored as the bf16 operand tile the output phase loads as is,
-//     the normalizer entering every chunk (norm) and the final state;
+//     the normalizer entering every chunk and the final state;
 //  3. output (per (head, chunk)): O = Q~ X_{c-1}^T + (L o Q~ K~^T) V
-//     with q~_t = phi(q_t) Gam_t, k~_j = phi(k_j) / Gam_j; norm divides
-//     row t by den_t = q~_t . z_{c-1} + sum_{j<=t} q~_t . k~_j.
+//     with q~ = phi(q), k~ = phi(k), row t divided by
+//     den_t = q~_t . z_{c-1} + sum_{j<=t} q~_t . k~_j.
 // Phases 1 and 3 are independent over all (head, chunk) units, so the GPU
 // fills even when B*H is small. They run as persistent CTAs (a few per SM,
 // each looping over units with the next unit's tiles in flight) because
@@ -41,15 +38,15 @@ using chunk::st_shared_v4;
 using chunk::store_row32_bf16;
 
 struct Params {
-    const float* state_in;  // S [BH][DK][DV] (+ z [BH][DK] for norm) or NULL
+    const float* state_in;  // S [BH][DK][DV] + z [BH][DK], or NULL
     float* state_out;       // same layout, or NULL
-    float* den_out;         // norm: [BH][T], or NULL
+    float* den_out;         // [BH][T], or NULL
     float* dx;              // [BH][nch][DV][DK] fp32 chunk summaries
-    float* dd;              // [BH][nch][DK]: gla Gam_C, norm sum of phi(k)
+    float* dd;              // [BH][nch][DK]: the chunk's sum of phi(k)
     uint8_t* xs;            // [BH][nch] state entering the chunk, bf16 MMA tile (DK*DV*2 bytes)
-    float* zs;              // norm: [BH][nch][DK] normalizer entering the chunk
-    uint8_t* kh;            // norm: [BH][nch] phi(k) as the bf16 operand tile (DK*128 bytes)
-    const float* gamma;     // norm: [BH] fixed decay per sequence-head, or NULL (none)
+    float* zs;              // [BH][nch][DK] normalizer entering the chunk
+    uint8_t* kh;            // [BH][nch] phi(k) as the bf16 operand tile (DK*128 bytes)
+    const float* gamma;     // [BH] fixed decay per sequence-head, or NULL (none)
     int BH, T, nch;
     unsigned flags;
     int* status;
@@ -63,12 +60,10 @@ struct Params {
 template <int VAR, int DK, int DV>
 struct SumLayout {
     static constexpr int KA = DK / 64, VA = DV / 64;
-    static constexpr uint32_t G_BYTES = (VAR == kGla) ? C * DK * 4 : 0;
     static constexpr uint32_t K_OFF = 0;                       // within a stage
     static constexpr uint32_t V_OFF = KA * 8192;
-    static constexpr uint32_t G_OFF = V_OFF + VA * 8192;
-    static constexpr uint32_t STAGE = G_OFF + G_BYTES;         // multiple of 1024
-    static constexpr uint32_t KH_OFF = 2 * STAGE;              // k^ [64 j][DK]
+    static constexpr uint32_t STAGE = V_OFF + VA * 8192;       // multiple of 1024
+    static constexpr uint32_t KH_OFF = 2 * STAGE;              // phi(k) [64 j][DK]
     static constexpr uint32_t MISC_OFF = KH_OFF + KA * 8192;   // sTot[DK], sPart[128]
     static constexpr uint32_t BAR_OFF = MISC_OFF + (DK + 128) * 4;
     static constexpr uint32_t SMEM = BAR_OFF + 64 + 1024;
@@ -79,8 +74,8 @@ constexpr int kSumThreads = 256;
 
 template <int VAR, int DK, int DV>
 __global__ void __launch_bounds__(kSumThreads, 3)
-summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-               const __grid_constant__ CUtensorMap tmg, const Params p) {
+summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const Params p) {
+    static_assert(VAR == kNorm, "the gated variants have their own kernel");
     using L = SumLayout<VAR, DK, DV>;
     constexpr int KA = L::KA, VA = L::VA;
     griddep_launch_dependents();
@@ -90,8 +85,7 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     uint8_t* sm = smem_raw + (sbase - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int units = p.BH * p.nch;
-    const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
-    float* sTot = reinterpret_cast<float*>(sm + L::MISC_OFF);   // gla: Gam_C; norm: sum of phi(k)
+    float* sTot = reinterpret_cast<float*>(sm + L::MISC_OFF);   // sum of phi(k)
     float* sPart = sTot + DK;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);   // [0,1] stages, [2] MMA, [3] test hook
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
@@ -102,7 +96,6 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         fence_mbar_init();
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
-        if (VAR == kGla) tma_prefetch_desc(&tmg);
     }
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
@@ -125,7 +118,6 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         for (int a = 0; a < KA; ++a) tma_load_3d(&tmk, &bar[s], stg + L::K_OFF + a * 8192, a * 64, t0, bh);
 #pragma unroll
         for (int a = 0; a < VA; ++a) tma_load_3d(&tmv, &bar[s], stg + L::V_OFF + a * 8192, a * 64, t0, bh);
-        if (VAR == kGla) tma_load_3d(&tmg, &bar[s], stg + L::G_OFF, 0, t0, bh);
     };
     bool pending[2] = {false, false};
     if (!failed && tid == 0 && static_cast<int>(blockIdx.x) < units) {
@@ -138,73 +130,36 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         const int bh = u / p.nch, c = u % p.nch;
         const int nvalid = min(C, p.T - c * C);
         const uint32_t aK = sbase + s * L::STAGE + L::K_OFF, aV = sbase + s * L::STAGE + L::V_OFF;
-        float* gt = reinterpret_cast<float*>(sm + s * L::STAGE + L::G_OFF);
         if (tid == 0 && u + static_cast<int>(gridDim.x) < units) {
             issue_load(u + gridDim.x, s ^ 1);   // the previous unit is done with stage s^1
             pending[s ^ 1] = true;
         }
-        if (VAR == kNorm && tid == 0) bulk_wait_read_all();   // the previous phi(k) tile has left
+        if (tid == 0) bulk_wait_read_all();   // the previous phi(k) tile has left
         {
             const bool ok = mbar_wait(&bar[s], (k >> 1) & 1, kWaitLimitNs);
             if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; break; }
             if (tid == 0) pending[s] = false;
         }
-        if constexpr (VAR == kGla) {
-            // Exclusive suffix products prod_{t' > t} gamma_t' per channel, in
-            // place (= Gam_C / Gam_t without a division); Gam_C into sTot.
-            constexpr int NP = kSumThreads / DK, TP = C / NP;
-            const int ch = tid % DK, part = tid / DK;
-            float gv[TP];
-            float P = 1.f;
-#pragma unroll
-            for (int i = 0; i < TP; ++i) {
-                const int t = part * TP + i;
-                gv[i] = (t < nvalid) ? gt[t * DK + ch] : 1.f;
-                P *= gv[i];
-            }
-            sPart[part * DK + ch] = P;
-            __syncthreads();
-            float after = 1.f, tot = 1.f;
-#pragma unroll
-            for (int q = 0; q < NP; ++q) {
-                const float v = sPart[q * DK + ch];
-                if (q > part) after *= v;
-                tot *= v;
-            }
-            float S = after;
-#pragma unroll
-            for (int i = TP - 1; i >= 0; --i) {
-                gt[(part * TP + i) * DK + ch] = S;
-                S *= gv[i];
-            }
-            if (part == 0) sTot[ch] = tot;
-            __syncthreads();
-        }
-        // k^ = phi(k) (times the suffix products for gla); rows past T are zero.
+        // phi(k); rows past T are zero.
 #pragma unroll
         for (int i = 0; i < (64 * 8 * KA) / kSumThreads; ++i) {
             const int e = tid + kSumThreads * i;
             const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-            const int c0 = a * 64 + (pc ^ (row & 7)) * 8;
             const uint32_t off = a * 8192 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
             const uint4 uk = ld_shared_v4(aK + off);
             const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z), b3 = unpack_bf16(uk.w);
             float k8[8] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y, b3.x, b3.y};
             const bool valid = row < nvalid;
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
-                if constexpr (VAR == kGla) kv *= gt[row * DK + c0 + m];
-                k8[m] = kv;
-            }
+            for (int m = 0; m < 8; ++m) k8[m] = valid ? elu1(k8[m]) : 0.f;
             st_shared_v4(aKH + off, pack_bf16(k8[0], k8[1]), pack_bf16(k8[2], k8[3]), pack_bf16(k8[4], k8[5]),
                          pack_bf16(k8[6], k8[7]));
         }
         // norm with a fixed decay: token j of the chunk reaches the chunk's
         // end decayed by gamma^(nvalid-1-j); the weight goes on v_j (the
         // phi(k) tile stays as the output phase reads it)
-        const float lg2g = (VAR == kNorm && p.gamma) ? lg2(__ldg(p.gamma + bh)) : 0.f;
-        if (VAR == kNorm && p.gamma) {
+        const float lg2g = p.gamma ? lg2(__ldg(p.gamma + bh)) : 0.f;
+        if (p.gamma) {
 #pragma unroll
             for (int i = 0; i < (64 * 8 * VA) / kSumThreads; ++i) {
                 const int e = tid + kSumThreads * i;
@@ -228,12 +183,11 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 mma_bf16_ss(tmem, mnmaj(aV + kk * 2048, 8192), mnmaj(aKH + kk * 2048, 8192),
                             idesc_bf16(128, DK, true, true), kk > 0);
             mma_commit(&bar[2]);
-            if (VAR == kNorm) {   // phi(k) for the output phase, as the operand tile it reads
-                bulk_store(p.kh + static_cast<size_t>(u) * KA * 8192, aKH, KA * 8192);
-                bulk_commit();
-            }
+            // phi(k) for the output phase, as the operand tile it reads
+            bulk_store(p.kh + static_cast<size_t>(u) * KA * 8192, aKH, KA * 8192);
+            bulk_commit();
         }
-        if constexpr (VAR == kNorm) {
+        {
             // sum of phi(k) per channel, from the bf16 operand the MMA reads
             constexpr int NP = kSumThreads / DK, RP = C / NP;
             const int ch = tid % DK, part = tid / DK;
@@ -303,10 +257,11 @@ constexpr int kScanBatch = 32;   // chunks whose loads are in flight together
 // up to 32 chunks costs one round trip to L2.
 template <int VAR, int DK, int DV>
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
-    constexpr int E2 = DV * DK / 2;                   // column pairs of X
-    constexpr int Z2 = (VAR == kNorm) ? DK / 2 : 0;   // channel pairs of z
+    static_assert(VAR == kNorm, "the gated variants have their own kernel");
+    constexpr int E2 = DV * DK / 2;   // column pairs of X
+    constexpr int Z2 = DK / 2;        // channel pairs of z
     constexpr int PER = E2 + Z2;
-    constexpr size_t SSZ = static_cast<size_t>(DK) * DV + (VAR == kNorm ? DK : 0);
+    constexpr size_t SSZ = static_cast<size_t>(DK) * DV + DK;
     constexpr size_t XS_BYTES = static_cast<size_t>(DK) * DV * 2;
     griddep_launch_dependents();
     griddep_wait();   // the chunk summaries are complete
@@ -314,10 +269,10 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
     const int bh = gi / PER, e = gi % PER;
     if (bh >= p.BH) return;
     const int nch = p.nch;
-    // norm with a fixed decay: each chunk decays what enters it by gamma^nvalid
-    const float lg2g = (VAR == kNorm && p.gamma) ? lg2(__ldg(p.gamma + bh)) : 0.f;
+    // with a fixed decay: each chunk decays what enters it by gamma^nvalid
+    const float lg2g = p.gamma ? lg2(__ldg(p.gamma + bh)) : 0.f;
     auto chunk_decay = [&](int c) -> float {
-        return (VAR == kNorm && p.gamma) ? ex2(static_cast<float>(min(C, p.T - c * C)) * lg2g) : 1.f;
+        return p.gamma ? ex2(static_cast<float>(min(C, p.T - c * C)) * lg2g) : 1.f;
     };
     if (e < E2) {
         const int r = e / (DK / 2), col = 2 * (e % (DK / 2));   // value row r, columns col, col+1
@@ -327,25 +282,18 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
             x = make_float2(si[static_cast<size_t>(col) * DV], si[static_cast<size_t>(col + 1) * DV]);
         }
         const float* dx = p.dx + (static_cast<size_t>(bh) * nch * DV + r) * DK + col;
-        const float* dd = p.dd + static_cast<size_t>(bh) * nch * DK + col;
         uint8_t* xs = p.xs + static_cast<size_t>(bh) * nch * XS_BYTES + (col / 64) * (DV * 128) +
                       sw128_off(r, (col % 64) / 8) + (col % 8) * 2;
         for (int c = 0; c < nch; c += kScanBatch) {
-            float2 a[kScanBatch], d[kScanBatch];
+            float2 a[kScanBatch];
 #pragma unroll
-            for (int u = 0; u < kScanBatch; ++u) {
-                if (c + u < nch) {
-                    a[u] = *reinterpret_cast<const float2*>(dx + static_cast<size_t>(c + u) * DV * DK);
-                    if (VAR == kGla) d[u] = *reinterpret_cast<const float2*>(dd + static_cast<size_t>(c + u) * DK);
-                }
-            }
+            for (int u = 0; u < kScanBatch; ++u)
+                if (c + u < nch) a[u] = *reinterpret_cast<const float2*>(dx + static_cast<size_t>(c + u) * DV * DK);
 #pragma unroll
             for (int u = 0; u < kScanBatch; ++u) {
                 if (c + u < nch) {
                     *reinterpret_cast<uint32_t*>(xs + (c + u) * XS_BYTES) = pack_bf16(x.x, x.y);
-                    if constexpr (VAR == kGla) {
-                        x = make_float2(d[u].x * x.x + a[u].x, d[u].y * x.y + a[u].y);
-                    } else if (p.gamma) {
+                    if (p.gamma) {
                         const float dc = chunk_decay(c + u);
                         x = make_float2(dc * x.x + a[u].x, dc * x.y + a[u].y);
                     } else {
@@ -360,7 +308,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
             so[static_cast<size_t>(col + 1) * DV] = x.y;
         }
     } else {
-        // norm: the normalizer entering every chunk
+        // the normalizer entering every chunk
         const int ch = 2 * (e - E2);
         float2 z = make_float2(0.f, 0.f);
         if (p.state_in) z = *reinterpret_cast<const float2*>(p.state_in + bh * SSZ + static_cast<size_t>(DK) * DV + ch);
@@ -388,24 +336,22 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const Params p) {
 template <int VAR, int DK, int DV>
 struct OutLayout {
     static constexpr int KA = DK / 64, VA = DV / 64;
-    // one stage: q/k pair (per k-atom rows 0-63 q, 64-127 k), v, the state
-    // entering the chunk (bf16 [DV rows][DK], KA atoms), gates (gla), z (norm)
+    // one stage: q/k pair (per k-atom rows 0-63 q, 64-127 phi(k)), v, the
+    // state entering the chunk (bf16 [DV rows][DK], KA atoms), z
     static constexpr uint32_t QK_OFF = 0;
     static constexpr uint32_t V_OFF = KA * 16384;
     static constexpr uint32_t XS_OFF = V_OFF + VA * 8192;
     static constexpr uint32_t XS_BYTES = DK * DV * 2;
-    static constexpr uint32_t G_OFF = XS_OFF + XS_BYTES;
-    static constexpr uint32_t G_BYTES = (VAR == kGla) ? C * DK * 4 : 0;
-    static constexpr uint32_t Z_OFF = G_OFF + G_BYTES;
-    static constexpr uint32_t Z_BYTES = (VAR == kNorm) ? DK * 4 : 0;
+    static constexpr uint32_t Z_OFF = XS_OFF + XS_BYTES;
+    static constexpr uint32_t Z_BYTES = DK * 4;
     static constexpr uint32_t STAGE = ((Z_OFF + Z_BYTES) + 1023u) & ~1023u;
-    static constexpr uint32_t TX = 2 * KA * 8192 + VA * 8192 + XS_BYTES + G_BYTES + Z_BYTES;
-    static constexpr uint32_t FIXED = 8192 + VA * 8192 + (64 + 256) * 4 + 64;   // P, output tile, misc, barriers
+    static constexpr uint32_t TX = 2 * KA * 8192 + VA * 8192 + XS_BYTES + Z_BYTES;
+    static constexpr uint32_t FIXED = 8192 + VA * 8192 + 64 * 4 + 64;   // P, output tile, misc, barriers
     static constexpr int NSTAGE = (2 * STAGE + FIXED + 1024 <= 232448) ? 2 : 1;
     static constexpr uint32_t PS_OFF = NSTAGE * STAGE;           // P bf16 [64 t][64 j]
     static constexpr uint32_t OT_OFF = PS_OFF + 8192;            // output tile [64 t][DV] (also rows 64-127 of the M=128 P read)
-    static constexpr uint32_t MISC_OFF = OT_OFF + VA * 8192;     // sDen[64], sPart[256]
-    static constexpr uint32_t BAR_OFF = MISC_OFF + (64 + 256) * 4;
+    static constexpr uint32_t MISC_OFF = OT_OFF + VA * 8192;     // sDen[64]
+    static constexpr uint32_t BAR_OFF = MISC_OFF + 64 * 4;
     static constexpr uint32_t SMEM = BAR_OFF + 64 + 1024;
     static constexpr uint32_t COL_G = 0;    // P [t][64]
     static constexpr uint32_t COL_O = 64;   // O [t][DV]
@@ -415,9 +361,9 @@ constexpr int kOutThreads = 256;
 
 template <int VAR, int DK, int DV>
 __global__ void __launch_bounds__(kOutThreads, 2)
-output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-              const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmg,
+output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmv,
               const __grid_constant__ CUtensorMap tmo, const Params p) {
+    static_assert(VAR == kNorm, "the gated variants have their own kernel");
     using L = OutLayout<VAR, DK, DV>;
     constexpr int KA = L::KA, VA = L::VA, NS = L::NSTAGE;
     griddep_launch_dependents();
@@ -430,9 +376,7 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
     const int hh = warp >> 2;               // column half
     const int units = p.BH * p.nch;
     const int T = p.T;
-    const bool phi_on = !(VAR == kGla && (p.flags & 0x1u));
     float* sDen = reinterpret_cast<float*>(sm + L::MISC_OFF);
-    float* sPart = sDen + 64;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);   // [0,1] stages, [2] MMA, [3] test hook
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
     const uint32_t aPS = sbase + L::PS_OFF, aOT = sbase + L::OT_OFF;
@@ -441,10 +385,8 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
         for (int i = 0; i < 4; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
-        tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
         tma_prefetch_desc(&tmo);
-        if (VAR == kGla) tma_prefetch_desc(&tmg);
     }
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
@@ -467,17 +409,13 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
 #pragma unroll
         for (int a = 0; a < KA; ++a) {
             tma_load_3d(&tmq, &bar[s], stg + L::QK_OFF + a * 16384, a * 64, t0, bh);
-            if (VAR == kNorm)   // phi(k) as the summary phase stored it
-                bulk_load(stg + L::QK_OFF + a * 16384 + 8192, p.kh + (static_cast<size_t>(u) * KA + a) * 8192, 8192,
-                          &bar[s]);
-            else
-                tma_load_3d(&tmk, &bar[s], stg + L::QK_OFF + a * 16384 + 8192, a * 64, t0, bh);
+            // phi(k) as the summary phase stored it
+            bulk_load(stg + L::QK_OFF + a * 16384 + 8192, p.kh + (static_cast<size_t>(u) * KA + a) * 8192, 8192, &bar[s]);
         }
 #pragma unroll
         for (int a = 0; a < VA; ++a) tma_load_3d(&tmv, &bar[s], stg + L::V_OFF + a * 8192, a * 64, t0, bh);
         bulk_load(stg + L::XS_OFF, p.xs + static_cast<size_t>(u) * L::XS_BYTES, L::XS_BYTES, &bar[s]);
-        if (VAR == kGla) tma_load_3d(&tmg, &bar[s], stg + L::G_OFF, 0, t0, bh);
-        if (VAR == kNorm) bulk_load(stg + L::Z_OFF, p.zs + static_cast<size_t>(u) * DK, DK * 4, &bar[s]);
+        bulk_load(stg + L::Z_OFF, p.zs + static_cast<size_t>(u) * DK, DK * 4, &bar[s]);
     };
     bool pending[2] = {false, false};
     if (!failed && tid == 0 && static_cast<int>(blockIdx.x) < units) {
@@ -490,11 +428,10 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
         const int s = (NS == 2) ? (k & 1) : 0;
         const uint32_t par_full = (NS == 2) ? ((k >> 1) & 1) : (k & 1);
         const int bh = u / p.nch, c = u % p.nch;
-        const float lg2g = (VAR == kNorm && p.gamma) ? lg2(__ldg(p.gamma + bh)) : 0.f;   // norm: log2 of the decay
+        const float lg2g = p.gamma ? lg2(__ldg(p.gamma + bh)) : 0.f;   // log2 of the decay
         const int t0 = c * C, nvalid = min(C, T - t0);
         const uint32_t aQK = sbase + s * L::STAGE + L::QK_OFF, aV = sbase + s * L::STAGE + L::V_OFF;
         const uint32_t aXS = sbase + s * L::STAGE + L::XS_OFF;
-        float* gt = reinterpret_cast<float*>(sm + s * L::STAGE + L::G_OFF);
         const float* sZ = reinterpret_cast<const float*>(sm + s * L::STAGE + L::Z_OFF);
         if (NS == 2 && tid == 0 && u + static_cast<int>(gridDim.x) < units) {
             issue_load(u + gridDim.x, s ^ 1);   // the previous unit is done with stage s^1
@@ -505,31 +442,9 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
             if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; break; }
             if (tid == 0) pending[s] = false;
         }
-        if constexpr (VAR == kGla) {
-            // Gam_t = prod_{i<=t} gamma_i per channel, in place.
-            constexpr int NP = kOutThreads / DK, TP = C / NP;
-            const int ch = tid % DK, part = tid / DK;
-            float gv[TP];
-            float G = 1.f;
-#pragma unroll
-            for (int i = 0; i < TP; ++i) {
-                const int t = part * TP + i;
-                G *= (t < nvalid) ? gt[t * DK + ch] : 1.f;
-                gv[i] = G;
-            }
-            sPart[part * DK + ch] = G;
-            __syncthreads();
-            float pre = 1.f;
-#pragma unroll
-            for (int q = 0; q < NP; ++q)
-                if (q < part) pre *= sPart[q * DK + ch];
-#pragma unroll
-            for (int i = 0; i < TP; ++i) gt[(part * TP + i) * DK + ch] = gv[i] * pre;
-            __syncthreads();
-        }
-        // q~ (rows 0-63), k~ (rows 64-127) in place, 8 channels per 16 bytes
-        // (norm: k~ = phi(k) arrived ready from the summary phase).
-        if constexpr (VAR == kNorm) {
+        // q~ = phi(q) (rows 0-63) in place, 8 channels per 16 bytes; k~ = phi(k)
+        // (rows 64-127) arrived ready from the summary phase.
+        {
 #pragma unroll
             for (int i = 0; i < (64 * 8 * KA) / kOutThreads; ++i) {
                 const int e = tid + kOutThreads * i;
@@ -541,35 +456,6 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
                 st_shared_v4(qa, pack_bf16(elu1(a0.x), elu1(a0.y)), pack_bf16(elu1(a1.x), elu1(a1.y)),
                              pack_bf16(elu1(a2.x), elu1(a2.y)), pack_bf16(elu1(a3.x), elu1(a3.y)));
             }
-        }
-#pragma unroll
-        for (int i = 0; i < ((VAR == kNorm) ? 0 : (64 * 8 * KA) / kOutThreads); ++i) {
-            const int e = tid + kOutThreads * i;
-            const int row = e / (8 * KA), a = (e / 8) % KA, pc = e % 8;
-            const int c0 = a * 64 + (pc ^ (row & 7)) * 8;
-            const uint32_t qa = aQK + a * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16, ka = qa + 8192;
-            const uint4 uq = ld_shared_v4(qa), uk = ld_shared_v4(ka);
-            const float2 a0 = unpack_bf16(uq.x), a1 = unpack_bf16(uq.y), a2 = unpack_bf16(uq.z), a3 = unpack_bf16(uq.w);
-            const float2 b0 = unpack_bf16(uk.x), b1 = unpack_bf16(uk.y), b2 = unpack_bf16(uk.z), b3 = unpack_bf16(uk.w);
-            float q8[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
-            float k8[8] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y, b3.x, b3.y};
-            const bool valid = row < nvalid;
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float qq = phi_on ? elu1(q8[m]) : q8[m];
-                float kv = valid ? (phi_on ? elu1(k8[m]) : k8[m]) : 0.f;
-                if constexpr (VAR == kGla) {
-                    const float gm = gt[row * DK + c0 + m];
-                    qq *= gm;
-                    kv *= __fdividef(1.f, gm);
-                }
-                q8[m] = qq;
-                k8[m] = kv;
-            }
-            st_shared_v4(qa, pack_bf16(q8[0], q8[1]), pack_bf16(q8[2], q8[3]), pack_bf16(q8[4], q8[5]),
-                         pack_bf16(q8[6], q8[7]));
-            st_shared_v4(ka, pack_bf16(k8[0], k8[1]), pack_bf16(k8[2], k8[3]), pack_bf16(k8[4], k8[5]),
-                         pack_bf16(k8[6], k8[7]));
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -586,7 +472,7 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
             }
             mma_commit(&bar[2]);
         }
-        if constexpr (VAR == kNorm) {
+        {
             // den_t = q~_t . z_{c-1} while the MMAs run (4 threads per token)
             const int t = tid >> 2, q4 = tid & 3;
             float d = 0.f;
@@ -611,14 +497,14 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
             if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; break; }
         }
         if ((warp & 3) < 2) {
-            // masked scores of rows t = 0..63 -> bf16 P; norm adds the row sums to den.
+            // masked scores of rows t = 0..63 -> bf16 P; the row sums add to den.
             const int t = r;
             float x[32];
             tmem_ld32(tlane + L::COL_G + 32 * hh, x);
             tmem_ld_wait();
             float rs = 0.f;
-            if (VAR == kNorm && p.gamma) {
-                // norm with a fixed decay: score (t, j) weighs gamma^(t-j), and
+            if (p.gamma) {
+                // with a fixed decay: score (t, j) weighs gamma^(t-j), and
                 // the product with the state entering the chunk gamma^(t+1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -646,7 +532,7 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
                 }
             }
             store_row32_bf16(aPS, t, 4 * hh, x);
-            if (VAR == kNorm) atomicAdd(&sDen[t], rs);
+            atomicAdd(&sDen[t], rs);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -661,7 +547,7 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
             mma_commit(&bar[2]);
             bulk_wait_read_all();   // the previous unit's output store has left the tile
         }
-        if (VAR == kNorm && p.den_out && tid < nvalid) p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
+        if (p.den_out && tid < nvalid) p.den_out[static_cast<size_t>(bh) * T + t0 + tid] = sDen[tid];
         {
             const bool ok = mbar_wait(&bar[2], mph, kWaitLimitNs);
             mph ^= 1u;
@@ -669,20 +555,18 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
             if (__syncthreads_or(!ok)) { status_bits |= kStatusMmaWait; failed = true; break; }
         }
         // rows t < 64 of O (thread (t, hh) holds columns [hh*DV/2, (hh+1)*DV/2)),
-        // divided by den for norm, into the [64 t][DV] tile, then TMA stores.
+        // divided by den, into the [64 t][DV] tile, then TMA stores.
         if ((warp & 3) < 2) {
             const int t = r;
-            const float sc = (VAR == kNorm) ? __fdividef(1.f, sDen[t]) : 1.f;
+            const float sc = __fdividef(1.f, sDen[t]);
 #pragma unroll
             for (int b = 0; b < DV / 64; ++b) {
                 const int cb = hh * (DV / 2) + 32 * b;
                 float x[32];
                 tmem_ld32(tlane + L::COL_O + cb, x);
                 tmem_ld_wait();
-                if (VAR == kNorm) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] *= sc;
-                }
+                for (int i = 0; i < 32; ++i) x[i] *= sc;
                 store_row32_bf16(aOT + (cb / 64) * 8192, t, (cb % 64) / 8, x);
             }
         }
@@ -741,13 +625,13 @@ cudaError_t run(const chunk::Maps& m, const Params& p, int sm_count, cudaStream_
     int g3 = sm_count * per_sm(S3::SMEM, S3::TMEM_COLS, kOutThreads, 2);
     if (g1 > units) g1 = units;
     if (g3 > units) g3 = units;
-    e = launch_pdl(k1, g1, kSumThreads, S1::SMEM, s, m.k, m.v, m.g, p);
+    e = launch_pdl(k1, g1, kSumThreads, S1::SMEM, s, m.k, m.v, p);
     if (e != cudaSuccess) return e;
-    constexpr int PER = DV * DK / 2 + (VAR == kNorm ? DK / 2 : 0);
+    constexpr int PER = DV * DK / 2 + DK / 2;
     const long long threads = static_cast<long long>(p.BH) * PER;
     e = launch_pdl(k2, static_cast<unsigned>((threads + kScanThreads - 1) / kScanThreads), kScanThreads, 0, s, p);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k3, g3, kOutThreads, S3::SMEM, s, m.q, m.k, m.v, m.g, m.o, p);
+    return launch_pdl(k3, g3, kOutThreads, S3::SMEM, s, m.q, m.v, m.o, p);
 }
 
 template <int VAR>
@@ -764,7 +648,7 @@ cudaError_t dispatch(int dk, int dv, const chunk::Maps& m, const Params& p, int 
 namespace chunk {
 
 size_t par_chunk_bytes(int dk, int dv) {
-    // dX fp32 + start state bf16 + dd + zs + phi(k) tile (norm)
+    // dX fp32 + start state bf16 + dd + zs + phi(k) tile
     return static_cast<size_t>(dk) * dv * 6 + static_cast<size_t>(dk) * 8 + static_cast<size_t>(dk) * 128;
 }
 
@@ -792,7 +676,7 @@ cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     p.zs = reinterpret_cast<float*>(w);
     w += units * a.dk * sizeof(float);
     p.kh = w;
-    p.gamma = (a.variant == kNorm) ? a.gate : nullptr;   // the normalized variant's decay, if any
+    p.gamma = a.gate;   // the normalized variant's fixed decay, or NULL
     p.BH = a.BH;
     p.T = a.T;
     p.nch = static_cast<int>(nch);
@@ -800,7 +684,6 @@ cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     p.status = a.status;
     if (a.nlaunch) *a.nlaunch += 3;   // summary, scan, output
     if (a.variant == kNorm) return par::dispatch<kNorm>(a.dk, a.dv, m, p, a.sm_count, s);
-    if (a.variant == kGla) return par::dispatch<kGla>(a.dk, a.dv, m, p, a.sm_count, s);
     return cudaErrorInvalidValue;
 }
 

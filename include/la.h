@@ -29,9 +29,12 @@
  *                   S_t = S_{t-1} Diag(alpha_t) (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
  *                 alpha_t in (0,1]^{d_k}. ("Linear attention and recurrent
  *                 memory", From fixed decay to KDA's gated delta write.)
- *                 The chunkwise kernel is exact in fp32 while every alpha >= 2^-15
- *                 (smaller values stay finite but lose accuracy); the recurrent
- *                 kernel (chunk 1) has no such limit.
+ *
+ * Decays of LA_GLA and LA_KDA below 2^-15 act as 2^-15 in the chunkwise
+ * kernel (16-token sub-chunk references keep every factor exact in fp32
+ * down to there): what crosses such a token is scaled by 2^-15 instead of
+ * the decay, a departure of at most 2^-15 of the quantity crossing it. The
+ * recurrent kernel (chunk 1) uses every decay as given.
  *
  * Every variant updates first and then reads, so token t attends to itself.
  *
@@ -62,19 +65,21 @@
  * resident on the device). The library never frees or retains them after a
  * call returns. la_create allocates the handle, one device status word and a
  * fixed workspace; la_destroy frees all three. The chunked prefill uses the
- * workspace for the per-chunk states of the three-phase form (LA_NORM_ELU1,
- * LA_GLA: up to 128 chunks per sequence-head, at most 48 MB; a call whose
- * states do not fit takes the sequential kernel instead), for segment
- * summaries when B*H is too small to fill the GPU ((SM count) x
- * (d_k*d_v + d_k) floats) and, for
- * LA_GDN and LA_KDA, for the hand-off flags and a ring of up to 32 chunks
- * of per-chunk intermediates for each of a group of G = min(B*H, 32)
- * sequence-heads (G*32*(2*d_k*d_k + (2*d_k+d_v)*128 + 8704) bytes plus a few
- * KB; 93 MB at G = 32, d_k = d_v = 128; a smaller workspace only makes the
- * ring shallower). The largest of these is allocated when the
- * configuration can take the tensor-core path (bf16, d_k, d_v in {64, 128}).
- * Calls that overlap on the GPU through the same handle (different streams)
- * would share that workspace: serialize them.
+ * workspace
+ *   - LA_NORM_ELU1: for the per-chunk states of the three-phase form (up to
+ *     128 chunks per sequence-head, at most 48 MB; a call whose states do
+ *     not fit takes the sequential kernel instead) and for segment summaries
+ *     when B*H is too small to fill the GPU ((SM count) x (d_k*d_v + d_k)
+ *     floats);
+ *   - LA_GDN, LA_KDA, LA_GLA: for the hand-off flags and a ring of up to 16
+ *     chunks of per-chunk intermediates for each of a group of
+ *     G = min(B*H, 32) sequence-heads: G*16*(2*d_k*d_k + 256*d_k + 128*d_v
+ *     + 8704) bytes plus a few KB, 45.3 MB at G = 32, d_k = d_v = 128 (a
+ *     smaller workspace only makes the ring shallower).
+ * The largest of these is allocated when the configuration can take the
+ * tensor-core path (bf16, d_k, d_v in {64, 128}). Calls that overlap on the
+ * GPU through the same handle (different streams) would share that
+ * workspace: serialize them.
  *
  * EXECUTION. Calls are asynchronous on the given CUDA stream (NULL = the
  * legacy default stream) and never synchronize the device, except
@@ -114,7 +119,7 @@ enum {
 
 /* la_config.flags */
 #define LA_FLAG_IDENTITY_PHI 0x1u   /* LA_GLA without the feature map (phi = identity) */
-#define LA_FLAG_SEQUENTIAL_CHUNKS 0x2u /* LA_NORM_ELU1 / LA_GLA chunked prefill: always walk the
+#define LA_FLAG_SEQUENTIAL_CHUNKS 0x2u /* LA_NORM_ELU1 chunked prefill: always walk the
                                           chunks of a sequence-head in order (split into segments
                                           when B*H is small) instead of the three-phase parallel
                                           form the library picks when the per-chunk states fit
@@ -154,7 +159,9 @@ int la_create(const la_config* cfg, la_handle** out);
  *             min(6, SM count / (B*H)) segments (one segment when B*H > SM
  *             count) of at most 4 blocks each; the segments of a
  *             sequence-head form one thread-block cluster. Otherwise they
- *             take the forms described under the workspace below.
+ *             take the forms described under the workspace below. LA_GDN,
+ *             LA_KDA and LA_GLA run one cooperative launch per group of up
+ *             to 32 sequence-heads.
  *             Other values: LA_ERR_UNSUPPORTED.
  *   den_out   optional, LA_NORM_ELU1 and LA_NORM_DECAY only.
  * Every pointer must be 16-byte aligned (LA_ERR_MISALIGNED otherwise).
@@ -277,8 +284,8 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
  * enqueued (0 after a failed or a T = 0 call, or for a NULL handle). A
  * diagnostic: which algorithm the library picked shows in this count (1: the
  * recurrent kernel or a decode step; 1 or 2: the chunk kernel, with segment
- * summaries when B*H is small; 3: the three-phase parallel form; LA_GDN and
- * LA_KDA: one per group of 32 sequence-heads). */
+ * summaries when B*H is small; 3: the three-phase parallel form; LA_GDN,
+ * LA_KDA and LA_GLA: one per group of 32 sequence-heads). */
 int la_last_launches(const la_handle* h);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */

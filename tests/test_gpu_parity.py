@@ -174,6 +174,49 @@ def test_gla_small_gates():
     assert_parity(w, inp, chunk=64)
 
 
+@pytest.mark.parametrize("gamma", [0.2, 0.05, 1e-3])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [65, 200, 1000])
+def test_gla_strong_gates(gamma, d, T):
+    # A constant decay on every channel: 64 tokens of gamma = 1e-3 multiply
+    # to 1e-192, far outside fp32; the in-chunk factors must stay in range
+    # and the results finite and within tolerance.
+    w = base("gla", d).with_(T=T)
+    inp = W.draw(w, seed=T + d)
+    inp.gate[...] = gamma
+    assert_parity(w, inp, chunk=64)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [65, 200, 1000])
+def test_gla_mixed_strong_and_weak_channels(d, T):
+    # Per channel: a third near 1 (slow), a third at 1e-3, the rest drawn;
+    # on some tokens a channel drops to 1e-5 for one step.
+    w = base("gla", d).with_(T=T)
+    inp = W.draw(w, seed=2 * T + d)
+    g = inp.gate
+    g[..., 0::3] = 0.9995
+    g[..., 1::3] = 1e-3
+    rng = np.random.default_rng(T)
+    drop = rng.random(g.shape) < 0.02
+    g[drop] = 1e-5
+    assert_parity(w, inp, chunk=64)
+
+
+@pytest.mark.parametrize("variant", ["gla", "kda"])
+def test_decays_below_the_floor_stay_finite(variant):
+    # Decays far below 2^-15 (down to 1e-30) act as 2^-15 in the chunkwise
+    # kernel: results stay finite, and what they change is scaled by 2^-15
+    # of the quantity crossing such a token, well inside the tolerance.
+    w = base(variant, 128).with_(T=300)
+    inp = W.draw(w, seed=17)
+    g = inp.gate
+    rng = np.random.default_rng(5)
+    g[rng.random(g.shape) < 0.05] = 1e-30
+    g[rng.random(g.shape) < 0.05] = 1e-8
+    assert_parity(w, inp, chunk=64)
+
+
 def test_gdn_small_gates_and_full_beta():
     w = base("gdn", 128).with_(T=200)
     inp = W.draw(w, seed=9)
@@ -542,7 +585,7 @@ def test_rejected_calls_do_not_launch():
 
 @pytest.mark.parametrize("variant,T,flags,chunk,expect", [
     ("norm", 200, 0, 64, 1),                                 # d = 64: segments of 128-token blocks, one launch
-    ("gla", 200, 0, 64, 3),
+    ("gla", 200, 0, 64, 1),                                  # the prep/chain kernel, as gdn
     ("norm", 200, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 2),      # segment summaries + chunk kernel
     ("norm", 100, la.LA_FLAG_SEQUENTIAL_CHUNKS, 64, 1),      # too short to split
     ("gdn", 200, 0, 64, 1),                                  # one cooperative launch per 32 heads
