@@ -26,7 +26,7 @@ cudaError_t launch_norm(int dk, int dv, const Maps& m, const Params& p, int BH, 
 // holds the hand-off flags and the ring (2 kGdnWindow chunks per head at
 // most, as deep as the workspace allows).
 constexpr int kGdnMaxGroup = 32;   // chain CTAs per launch
-constexpr int kGdnWindow = 8;      // half the deepest ring, in chunks
+constexpr int kGdnWindow = 4;      // half the deepest ring, in chunks (8: a deeper ring spills L2)
 size_t gdn_slot_bytes(int dk, int dv);
 int gdn_group(int BH);
 // Workspace for a ring of 2W chunks (W >= 1 is the least the launcher accepts).

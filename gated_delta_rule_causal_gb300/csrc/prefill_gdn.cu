@@ -155,8 +155,9 @@ struct PrepLayout {
     static constexpr uint32_t OFF_OUT = OFF_TB2 + 8192;  // the slot being assembled / stored
     static constexpr uint32_t OFF_AS = OFF_OUT + align1024(S::BYTES);   // fp32 [64][kAStride]
     static constexpr uint32_t OFF_RS = OFF_AS + C * kAStride * 4;       // fp32 [32][kRStride]
-    static constexpr uint32_t OFF_MISC = OFF_RS + 32 * 40 * 4;          // log2 prefix, beta, beta gam, gam, next gates and betas
-    static constexpr uint32_t OFF_BAR = OFF_MISC + 6 * 64 * 4;
+    // two gate buffers (units k and k + 1), each: log2 prefix, beta, beta gam, gam
+    static constexpr uint32_t OFF_MISC = OFF_RS + 32 * 40 * 4;
+    static constexpr uint32_t OFF_BAR = OFF_MISC + 2 * 4 * 64 * 4;
     static constexpr uint32_t BYTES = OFF_BAR + 128;
     // W^T as a bf16 K-major A operand [dk][64 j] goes over the solve matrix,
     // which is dead by then
@@ -780,6 +781,78 @@ __device__ __forceinline__ void store_loop(const Params& p, uint64_t* slot_full,
     bulk_wait_all();
 }
 
+// Gate preparation of one unit by the whole store warp (scalar decay): lane l
+// takes tokens 2l and 2l + 1 and writes, into gate buffer gb ([4][64] floats),
+// the cumulative log2 gate G_t, beta_t (0 on padded tokens), beta_t gam_t
+// and gam_t = 2^G_t; then every lane arrives on gates_full (32 arrivals).
+__device__ __forceinline__ void prepare_gates(const Params& p, int u, float* gb, uint64_t* gates_full) {
+    const int lane = threadIdx.x & 31;
+    const int bh = p.h0 + u % p.G;
+    const int t0 = (u / p.G) * C + 2 * lane;
+    const size_t base = static_cast<size_t>(bh) * p.T;
+    float g0 = 1.f, g1 = 1.f, b0 = 0.f, b1 = 0.f;
+    if (t0 < p.T) { g0 = __ldg(p.gate + base + t0); b0 = __ldg(p.beta + base + t0); }
+    if (t0 + 1 < p.T) { g1 = __ldg(p.gate + base + t0 + 1); b1 = __ldg(p.beta + base + t0 + 1); }
+    const float l0 = lg2(g0), l1 = lg2(g1);
+    float sum = l0 + l1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, sum, o);
+        if (lane >= o) sum += y;
+    }
+    const float G0 = sum - l1, G1 = sum;   // inclusive prefix at tokens 2l, 2l + 1
+    const float gam0 = ex2(G0), gam1 = ex2(G1);
+    *reinterpret_cast<float2*>(gb + 2 * lane) = make_float2(G0, G1);
+    *reinterpret_cast<float2*>(gb + 64 + 2 * lane) = make_float2(b0, b1);
+    *reinterpret_cast<float2*>(gb + 128 + 2 * lane) = make_float2(b0 * gam0, b1 * gam1);
+    *reinterpret_cast<float2*>(gb + 192 + 2 * lane) = make_float2(gam0, gam1);
+    mbar_arrive(gates_full);   // release: this lane's writes precede the waiters' reads
+}
+
+// Store warp of a scalar-decay prep CTA (all 32 lanes): prepares the gates of
+// the CTA's first unit, then per unit k prepares unit k + 1's gates (into the
+// buffer unit k - 1 used, free since its slot was assembled) and stores unit
+// k's slot (lane 0, as store_loop does).
+template <uint32_t BYTES>
+__device__ __forceinline__ void store_gate_loop(const Params& p, uint64_t* slot_full, uint64_t* slot_free,
+                                                uint64_t* gates_full, float* gbuf, const uint8_t* out,
+                                                volatile int* abort_smem, int& status_bits) {
+    const int lane = threadIdx.x & 31;
+    const int pid = blockIdx.x - p.n_chain, np = gridDim.x - p.n_chain, nunits = p.G * p.nch;
+    if (pid < nunits) prepare_gates(p, pid, gbuf, &gates_full[0]);
+    for (int k = 0;; ++k) {
+        const int u = pid + k * np;
+        if (u >= nunits) break;
+        if (u + np < nunits) prepare_gates(p, u + np, gbuf + ((k + 1) & 1) * 256, &gates_full[(k + 1) & 1]);
+        bool stop = false;
+        if (lane == 0) {
+            if (!mbar_wait_or_abort(slot_full, k & 1, abort_smem)) {
+                if (!*abort_smem) status_bits |= kStatusFlagWait;   // else the converting warps recorded it
+                stop = true;
+            }
+            const int g = u % p.G, c = u / p.G;
+            if (!stop && c >= p.R && !p.wait_flag(p.consumed(g), static_cast<unsigned long long>(c - p.R) + 1)) {
+                status_bits |= kStatusFlagWait;
+                *abort_smem = 1;
+                p.abort_all();
+                stop = true;
+            }
+            if (!stop) {
+                uint8_t* dst = p.ws_slot + (static_cast<size_t>(g) * p.R + c % p.R) * BYTES;
+                bulk_store(dst, smem_u32(out), BYTES);
+                bulk_commit();
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                mbar_arrive(slot_free);
+                bulk_wait_all();
+                fence_proxy_async_global();
+                st_release_u64(p.ready(g, c), p.epoch | (static_cast<unsigned long long>(c) + 1));
+            }
+        }
+        if (__shfl_sync(0xffffffffu, stop ? 1 : 0, 0)) break;
+    }
+    if (lane == 0) bulk_wait_all();
+}
+
 template <int DK, int DV>
 __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                           const Params& p, uint8_t* sm, uint32_t sbase) {
@@ -796,11 +869,10 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
 
     float* As = reinterpret_cast<float*>(sm + L::OFF_AS);
     float* Rs = reinterpret_cast<float*>(sm + L::OFF_RS);
-    float* sG2 = reinterpret_cast<float*>(sm + L::OFF_MISC);   // cumulative log2-gate
-    float* sB = sG2 + 64;                                        // beta (0 on padded tokens)
-    float* sBG = sB + 64;                                        // beta_t gam_t
-    float* sGam = sBG + 64;                                      // gam_t
-    float* sGin = sGam + 64;                                     // next unit's gates, then betas [2][64]
+    // gate buffer of unit k: gbuf + (k & 1) * 256 = cumulative log2 gate,
+    // beta (0 on padded tokens), beta_t gam_t, gam_t (64 each), written by
+    // the store warp a unit ahead
+    float* gbuf = reinterpret_cast<float*>(sm + L::OFF_MISC);
     uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
     uint64_t* bar_m = bar_full + 2;
     uint64_t* bar_test = bar_full + 3;
@@ -808,11 +880,16 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     uint64_t* slot_full = bar_full + 5;   // converting warps: the slot buffer is assembled
     uint64_t* slot_free = bar_full + 6;   // store warp: the slot buffer was read by its store
     volatile int* abort_smem = reinterpret_cast<volatile int*>(bar_full + 7);
+    uint64_t* gates_full = bar_full + 8;  // [2] store warp: a unit's gate buffer is written (32 arrivals)
+    uint64_t* drain = bar_full + 10;      // after a failure: the MMAs of both issuing threads are done
     const uint32_t aTB1 = sbase + L::OFF_TB1, aTB2 = sbase + L::OFF_TB2;
 
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(&bar_full[i], 1);
         for (int i = 5; i < 7; ++i) mbar_init(&bar_full[i], 1);
+        mbar_init(&gates_full[0], 32);
+        mbar_init(&gates_full[1], 32);
+        mbar_init(drain, 2);
         *abort_smem = 0;
         fence_mbar_init();
         tma_prefetch_desc(tmq);
@@ -825,9 +902,9 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     tc_fence_after();
     if (warp == kConv / 32) {
         int sbits = 0;
-        if (lane == 0 && !(p.flags & 0x100u))
-            store_loop<S::BYTES>(p, slot_full, slot_free, sm + L::OFF_OUT, abort_smem, sbits);
-        if (sbits) atomicOr(p.status, sbits);
+        if (!(p.flags & 0x100u))
+            store_gate_loop<S::BYTES>(p, slot_full, slot_free, gates_full, gbuf, sm + L::OFF_OUT, abort_smem, sbits);
+        if (sbits && lane == 0) atomicOr(p.status, sbits);
         return;
     }
     const uint32_t tmem = *tmem_slot;
@@ -877,27 +954,11 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
     };
     // gate and beta of a unit, one token per thread (threads 0-63), copied
     // asynchronously into shared memory a unit ahead (padded tokens: 1 and 0)
-    auto load_gb = [&](int u) {
-        if (u < nunits && tid < 64) {
-            const int bh = p.h0 + unit_g(u);
-            const int t = unit_i(u) * C + tid;
-            if (t < T) {
-                cp_async4(smem_u32(sGin + tid), p.gate + static_cast<size_t>(bh) * T + t);
-                cp_async4(smem_u32(sGin + 64 + tid), p.beta + static_cast<size_t>(bh) * T + t);
-            } else {
-                sGin[tid] = 1.f;
-                sGin[64 + tid] = 0.f;
-            }
-            cp_async_commit();
-        }
-    };
-
     constexpr uint32_t ID_G = idesc_bf16(128, 64, false, false);   // [K;Q] K^T
     constexpr uint32_t ID_WU = idesc_bf16(128, 64, true, false);   // K^T TB2^T, V^T TB1^T
     constexpr uint32_t ID_NEG_N = idesc_bf16(128, DK, false, true, true);   // -(W^T K')
     constexpr uint32_t ID_EP = idesc_bf16(128, 64, false, false);            // W^T P^T
 
-    load_gb(pid);
     if (!failed && tid == 0 && pid < nunits) issue_load(pid, 0);
     uint32_t mph = 0;
     int k = 0;
@@ -909,6 +970,10 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         const uint32_t stg = sbase + s * L::STAGE;
         const uint32_t aOut = sbase + L::OFF_OUT;
         float* oVec = reinterpret_cast<float*>(sm + L::OFF_OUT + S::V_OFF);   // gam_C per channel
+        const float* sG2 = gbuf + (k & 1) * 256;   // cumulative log2 gate (from the store warp)
+        const float* sB = sG2 + 64;                // beta (0 on padded tokens)
+        const float* sBG = sB + 64;                // beta_t gam_t
+        const float* sGam = sBG + 64;              // gam_t
         uint32_t pw[16];   // this thread's row of P (rows 64-127), bf16 pairs
         if (tid == 0 && un < nunits) {
             fence_proxy_async_smem();
@@ -916,7 +981,7 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         }
         if (!wait_all(&bar_full[s], (k >> 1) & 1)) { status_bits |= kStatusTmaWait; failed = true; break; }
         if (tid == 0) pending[s] = false;
-        // [K;Q] K^T, issued by a thread outside the warps of the gate prefix
+        // [K;Q] K^T
         if (tid == kIssuer) {
 #pragma unroll
             for (int kk = 0; kk < DK / 16; ++kk) {
@@ -925,29 +990,8 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
             }
             mma_commit(bar_m);
         }
-
-        // ---- gate prefix sums (log2 domain) -----------------------------------------
-        if (tid < 64) {
-            cp_async_wait();   // this thread's own copies
-            const float gv = sGin[tid], bv = sGin[64 + tid];
-            float lg = lg2(gv);
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, lg, o);
-                if (lane >= o) lg += y;
-            }
-            sG2[tid] = lg;
-            sB[tid] = bv;
-        }
-        load_gb(un);   // the values above are read
-        sync_conv();
-        if (tid >= 32 && tid < 64) sG2[tid] += sG2[31];
-        sync_conv();
-        if (tid < 64) {
-            const float gam = ex2(sG2[tid]);
-            sGam[tid] = gam;
-            sBG[tid] = sB[tid] * gam;
-        }
+        // the unit's gates, prepared by the store warp meanwhile
+        if (!wait_all_abort(&gates_full[k & 1], (k >> 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;
         if ((warp & 3) < 2) {
@@ -984,6 +1028,37 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         }
         sync_conv();
         invert_unit_lower(As, Rs, warp, lane);
+        // ---- T diag(beta) and T diag(beta gam) as bf16 MMA operands --------------
+        {
+            const int t = tid >> 2, q4 = tid & 3;
+            const float* trow = As + t * kAStride + 16 * q4;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const float4 t0 = *reinterpret_cast<const float4*>(trow + 8 * cc);
+                const float4 t1 = *reinterpret_cast<const float4*>(trow + 8 * cc + 4);
+                const float4 b0 = *reinterpret_cast<const float4*>(sB + 16 * q4 + 8 * cc);
+                const float4 b1 = *reinterpret_cast<const float4*>(sB + 16 * q4 + 8 * cc + 4);
+                const float4 c0 = *reinterpret_cast<const float4*>(sBG + 16 * q4 + 8 * cc);
+                const float4 c1 = *reinterpret_cast<const float4*>(sBG + 16 * q4 + 8 * cc + 4);
+                const int c8 = 2 * q4 + cc;
+                st_shared_v4(aTB1 + sw128_off(t, c8), pack_bf16(t0.x * b0.x, t0.y * b0.y), pack_bf16(t0.z * b0.z, t0.w * b0.w),
+                             pack_bf16(t1.x * b1.x, t1.y * b1.y), pack_bf16(t1.z * b1.z, t1.w * b1.w));
+                st_shared_v4(aTB2 + sw128_off(t, c8), pack_bf16(t0.x * c0.x, t0.y * c0.y), pack_bf16(t0.z * c0.z, t0.w * c0.w),
+                             pack_bf16(t1.x * c1.x, t1.y * c1.y), pack_bf16(t1.z * c1.z, t1.w * c1.w));
+            }
+        }
+        publish();
+        // ---- W^T = K^T (T diag(beta gam))^T, Ut^T = V^T (T diag(beta))^T, issued
+        //      before the slot buffer is free; its stores below overlap them ----------
+        if (tid == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                mma_bf16_ss(tmem + L::COL_W, mnmaj(stg + kk * 2048, 16384), kmaj(aTB2 + kk * 32), ID_WU, kk > 0);
+                mma_bf16_ss(tmem + L::COL_UT, mnmaj(stg + L::QK_BYTES + kk * 2048, 8192), kmaj(aTB1 + kk * 32),
+                            ID_WU, kk > 0);
+            }
+            mma_commit(bar_m);
+        }
         // the slot buffer is written from here on: the previous unit's store has
         // long read it
         if (k >= 1 && !wait_all_abort(slot_free, (k - 1) & 1)) { status_bits |= kStatusFlagWait; failed = true; break; }
@@ -1006,36 +1081,6 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
                 const uint32_t ro = sw128_off(t, c8);
                 st_shared_v4_u4(aOut + S::KP_OFF + a * 8192 + ro, scale_bf16x8(ld_shared_v4(stg + a * 16384 + ro), fk));
             }
-        }
-        // ---- T diag(beta) and T diag(beta gam) as bf16 MMA operands --------------
-        {
-            const int t = tid >> 2, q4 = tid & 3;
-            const float* trow = As + t * kAStride + 16 * q4;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const float4 t0 = *reinterpret_cast<const float4*>(trow + 8 * cc);
-                const float4 t1 = *reinterpret_cast<const float4*>(trow + 8 * cc + 4);
-                const float4 b0 = *reinterpret_cast<const float4*>(sB + 16 * q4 + 8 * cc);
-                const float4 b1 = *reinterpret_cast<const float4*>(sB + 16 * q4 + 8 * cc + 4);
-                const float4 c0 = *reinterpret_cast<const float4*>(sBG + 16 * q4 + 8 * cc);
-                const float4 c1 = *reinterpret_cast<const float4*>(sBG + 16 * q4 + 8 * cc + 4);
-                const int c8 = 2 * q4 + cc;
-                st_shared_v4(aTB1 + sw128_off(t, c8), pack_bf16(t0.x * b0.x, t0.y * b0.y), pack_bf16(t0.z * b0.z, t0.w * b0.w),
-                             pack_bf16(t1.x * b1.x, t1.y * b1.y), pack_bf16(t1.z * b1.z, t1.w * b1.w));
-                st_shared_v4(aTB2 + sw128_off(t, c8), pack_bf16(t0.x * c0.x, t0.y * c0.y), pack_bf16(t0.z * c0.z, t0.w * c0.w),
-                             pack_bf16(t1.x * c1.x, t1.y * c1.y), pack_bf16(t1.z * c1.z, t1.w * c1.w));
-            }
-        }
-        publish();
-        // ---- W^T = K^T (T diag(beta gam))^T, Ut^T = V^T (T diag(beta))^T --------
-        if (tid == 0) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                mma_bf16_ss(tmem + L::COL_W, mnmaj(stg + kk * 2048, 16384), kmaj(aTB2 + kk * 32), ID_WU, kk > 0);
-                mma_bf16_ss(tmem + L::COL_UT, mnmaj(stg + L::QK_BYTES + kk * 2048, 8192), kmaj(aTB1 + kk * 32),
-                            ID_WU, kk > 0);
-            }
-            mma_commit(bar_m);
         }
         if (!wait_all(bar_m, mph)) { status_bits |= kStatusMmaWait; failed = true; break; }
         mph ^= 1u;
@@ -1096,6 +1141,11 @@ __device__ __forceinline__ void prep_role(const CUtensorMap* tmq, const CUtensor
         *abort_smem = 1;
         p.abort_all();
     }
+    // after a failure, MMAs of the last unit may still be in flight: the two
+    // issuing threads commit them to one barrier and it completes before the
+    // tensor memory is released (bounded: 100 ms)
+    if (failed && (tid == 0 || tid == kIssuer)) mma_commit(drain);
+    if (failed && tid == 0) mbar_wait(drain, 0, 100000000ull);
     tc_fence_before();
     sync_conv();
     if (warp == 0) tmem_dealloc(tmem, L::TMEM_COLS);

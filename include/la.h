@@ -71,10 +71,10 @@
  *     not fit takes the sequential kernel instead) and for segment summaries
  *     when B*H is too small to fill the GPU ((SM count) x (d_k*d_v + d_k)
  *     floats);
- *   - LA_GDN, LA_KDA, LA_GLA: for the hand-off flags and a ring of up to 16
+ *   - LA_GDN, LA_KDA, LA_GLA: for the hand-off flags and a ring of up to 8
  *     chunks of per-chunk intermediates for each of a group of
- *     G = min(B*H, 32) sequence-heads: G*16*(2*d_k*d_k + 256*d_k + 128*d_v
- *     + 8704) bytes plus a few KB, 45.3 MB at G = 32, d_k = d_v = 128 (a
+ *     G = min(B*H, 32) sequence-heads: G*8*(2*d_k*d_k + 256*d_k + 128*d_v
+ *     + 8704) bytes plus a few KB, 22.7 MB at G = 32, d_k = d_v = 128 (a
  *     smaller workspace only makes the ring shallower).
  * The largest of these is allocated when the configuration can take the
  * tensor-core path (bf16, d_k, d_v in {64, 128}). Calls that overlap on the

@@ -80,7 +80,7 @@ def test_noalloc_matches_la_forward_twice(variant, d):
 def test_noalloc_gdn_shallow_ring_is_bit_identical():
     # 32 sequence-heads of d = 128 leave the 16 MiB static scratch room for a
     # ring of only a few chunks per head, so the prep CTAs wait for ring
-    # positions the chain CTAs free; la_forward's ring is 16 chunks deep. The
+    # positions the chain CTAs free; la_forward's ring is 8 chunks deep. The
     # arithmetic of every chunk is the same either way.
     w = W.small(W.GDN_B2H16_T8192_D128, B=2, H=16, T=1000, dk=128, dv=128)
     o, s, _, o_ref, s_ref, _ = _run_both(w, 3)
