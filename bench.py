@@ -508,7 +508,7 @@ def gpu_arm(args):
                                    "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None, "algorithmic_bytes": byts,
                                    "kernel_ms": round(kms, 4),
                                    "peak_source": pk["source"] + " (burst copy bandwidth)",
-                                   "note": "one CTA per sequence-head on CUDA cores: latency-bound"},
+                                   "note": "chunkwise tcgen05 chain (five launches per head group)"},
                       "gpu_launches": args.steps * br.launches_per_step})
         del br
         torch.cuda.empty_cache()

@@ -1,5 +1,6 @@
 // C ABI of the library (declared in include/la.h): argument validation,
 // kernel selection and the device status word.
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -549,6 +550,43 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v, const
     a.dk_dim = c.d_k;
     a.dv_dim = c.d_v;
     a.io = c.io == LA_FP32 ? la::kFp32 : la::kBf16;
+    a.flags = c.flags;
+    // The chunkwise tensor-core backward where the shape allows it and the
+    // per-chunk states of at least one sequence-head fit the workspace: the
+    // sequence-heads run in groups whose states fit it, one five-launch chain
+    // per group. Otherwise the token-serial kernel.
+    const size_t per_head = la::chunk::bwd_chunk_bytes(1, T);
+    if (c.io == LA_BF16 && c.d_k == 64 && c.d_v == 64 && h->d_ws && per_head <= h->ws_bytes) {
+        const int group = static_cast<int>(std::min<size_t>(h->ws_bytes / per_head, static_cast<size_t>(a.BH)));
+        const size_t ss = static_cast<size_t>(c.d_k) * c.d_v + c.d_k;   // floats per state
+        const size_t row = static_cast<size_t>(T) * 64 * 2;            // bytes of one head's q (= k, v, dout)
+        auto off = [](const void* p, size_t bytes) -> const void* {
+            return p ? static_cast<const uint8_t*>(p) + bytes : nullptr;
+        };
+        int launches = 0;
+        for (int h0 = 0; h0 < a.BH; h0 += group) {
+            la::BwdArgs g = a;
+            g.BH = std::min(group, a.BH - h0);
+            const size_t hb = static_cast<size_t>(h0) * row;
+            const size_t sb = static_cast<size_t>(h0) * ss * sizeof(float);
+            g.q = off(q, hb);
+            g.k = off(k, hb);
+            g.v = off(v, hb);
+            g.dout = off(dout, hb);
+            g.dq = const_cast<void*>(off(dq, hb));
+            g.dk = const_cast<void*>(off(dk, hb));
+            g.dv = const_cast<void*>(off(dv, hb));
+            g.state_in = static_cast<const float*>(off(state_in, sb));
+            g.dstate_out = static_cast<const float*>(off(dstate_out, sb));
+            g.dstate_in = static_cast<float*>(const_cast<void*>(off(dstate_in, sb)));
+            const cudaError_t e = la::chunk::launch_norm_backward_chunked(
+                g, h->d_ws, h->ws_bytes, h->d_status, h->sm_count, h->encode, static_cast<cudaStream_t>(cuda_stream));
+            if (e != cudaSuccess) return cuda_fail(h, e, "chunkwise backward launch");
+            launches += 5;
+        }
+        h->last_launches = launches;
+        return LA_OK;
+    }
     const cudaError_t e = la::launch_norm_backward(a, static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "backward kernel launch");
     h->last_launches = 1;

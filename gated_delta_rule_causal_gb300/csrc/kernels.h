@@ -59,6 +59,7 @@ struct BwdArgs {
     float* dstate_in;         // gradient of the initial state, or NULL
     int BH, T, dk_dim, dv_dim;
     int io;                   // Io
+    unsigned flags = 0;       // LA_FLAG_* (the test hook)
 };
 
 // One CTA per sequence-head on CUDA cores; d_k, d_v in {16, 32, 64}.

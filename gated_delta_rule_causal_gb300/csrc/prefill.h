@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "kernels.h"
 
@@ -48,6 +49,30 @@ constexpr size_t kParL2Bytes = size_t(48) << 20;
 size_t par_chunk_bytes(int dk, int dv);
 bool par_fits(int BH, int T, int dk, int dv, size_t ws_bytes);
 cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s);
+
+// The first two phases alone (undecayed, d_k = d_v = 64), for the chunkwise
+// backward: per chunk, the state entering it (bf16 [d_v][d_k] operand tile
+// in xs, z in zs), phi(k) as an operand tile (kh); dx and dd hold the chunk
+// summaries and are free afterwards. `end` is the first byte of the
+// workspace past these arrays.
+struct ParStates {
+    float* dx;
+    float* dd;
+    uint8_t* xs;
+    float* zs;
+    uint8_t* kh;
+    uint8_t* end;
+    int nch;
+};
+cudaError_t launch_par_states(const FwdArgs& a, const Maps& m, cudaStream_t s, ParStates* st);
+
+// Chunkwise backward of the normalized variant (d_k = d_v = 64, bf16 io):
+// workspace it needs, and the launch (five kernels: the two state phases
+// above, then per-chunk normalizer gradients, the reverse scan of the state
+// gradient, and the per-chunk input gradients).
+size_t bwd_chunk_bytes(int BH, int T);
+cudaError_t launch_norm_backward_chunked(const BwdArgs& a, float* workspace, size_t ws_bytes, int* status,
+                                         int sm_count, PFN_cuTensorMapEncodeTiled_v12000 enc, cudaStream_t s);
 
 }  // namespace chunk
 }  // namespace la

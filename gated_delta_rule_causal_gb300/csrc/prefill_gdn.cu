@@ -569,6 +569,9 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
             bool ok = mbar_wait_or_abort(&bar_full[b], (it >> 1) & 1, abort_flag) &&
                       mbar_wait_or_abort(bar_s, it & 1, abort_flag);
             tc_fence_after();
+            // warp-uniform before the warp-collective tensor-memory loads: a
+            // wait that gives up may give up in some lanes only
+            ok = __all_sync(0xffffffffu, ok);
             if (ok && own) {
                 const float* vec = reinterpret_cast<const float*>(sm + L::OFF_VEC + b * 512);
 #pragma unroll
@@ -586,6 +589,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
             bad |= !ok;
             // ---- output: o_t = O_b[:, t], through the output tile ----------------
             ok = ok && (it == 0 || mbar_wait_or_abort(bar_ofree, (it - 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, ok);
             if (ok && own) {
                 // Lane pairs (r even, r + 1) exchange values so that each
                 // writes two adjacent columns of one token row of the tile in

@@ -19,7 +19,9 @@
 // each looping over units with the next unit's tiles in flight) because
 // dispatching one short CTA per unit costs more than the work. The three
 // kernels are chained with programmatic dependent launch, so each one's
-// dispatch and prologue overlap the previous one's tail. The intermediates
+// dispatch and prologue (barriers, tensor-map prefetch) overlap the previous
+// one's tail; tensor memory is allocated only after the wait on the previous
+// kernel. The intermediates
 // (fp32 dX, bf16 states) stay in L2 between the phases.
 #include "prefill.h"
 #include "prefill_impl.cuh"
@@ -97,12 +99,15 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
     }
+    // The previous kernel first, then tensor memory: a CTA never holds
+    // columns while it waits on another grid (whose CTAs may still need
+    // columns of this SM to finish).
+    griddep_wait();   // inputs and the workspace are free to use from here on
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    griddep_wait();   // inputs and the workspace are free to use from here on
 
     int status_bits = 0;
     bool failed = false;
@@ -388,13 +393,13 @@ output_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ C
         tma_prefetch_desc(&tmv);
         tma_prefetch_desc(&tmo);
     }
+    griddep_wait();   // the scan's start states are complete (then tensor memory, as above)
     if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    griddep_wait();   // the scan's start states are complete
 
     int status_bits = 0;
     bool failed = false;
@@ -609,28 +614,38 @@ int per_sm(uint32_t smem, uint32_t tmem_cols, int threads, int cap) {
     return n < 1 ? 1 : n;
 }
 
+// Phases 1 and 2 (chunk summaries, then the scan), chained by programmatic
+// dependent launch; the states entering every chunk are in p.xs and p.zs
+// afterwards.
 template <int VAR, int DK, int DV>
-cudaError_t run(const chunk::Maps& m, const Params& p, int sm_count, cudaStream_t s) {
+cudaError_t run_states(const chunk::Maps& m, const Params& p, int sm_count, cudaStream_t s) {
     using S1 = SumLayout<VAR, DK, DV>;
-    using S3 = OutLayout<VAR, DK, DV>;
-    static_assert(S1::SMEM <= 232448 && S3::SMEM <= 232448, "shared memory budget");
+    static_assert(S1::SMEM <= 232448, "shared memory budget");
     auto k1 = summary_kernel<VAR, DK, DV>;
     auto k2 = scan_kernel<VAR, DK, DV>;
-    auto k3 = output_kernel<VAR, DK, DV>;
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, S1::SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, S3::SMEM);
     if (e != cudaSuccess) return e;
     const int units = p.BH * p.nch;
     int g1 = sm_count * per_sm(S1::SMEM, S1::TMEM_COLS, kSumThreads, 3);
-    int g3 = sm_count * per_sm(S3::SMEM, S3::TMEM_COLS, kOutThreads, 2);
     if (g1 > units) g1 = units;
-    if (g3 > units) g3 = units;
     e = launch_pdl(k1, g1, kSumThreads, S1::SMEM, s, m.k, m.v, p);
     if (e != cudaSuccess) return e;
     constexpr int PER = DV * DK / 2 + DK / 2;
     const long long threads = static_cast<long long>(p.BH) * PER;
-    e = launch_pdl(k2, static_cast<unsigned>((threads + kScanThreads - 1) / kScanThreads), kScanThreads, 0, s, p);
+    return launch_pdl(k2, static_cast<unsigned>((threads + kScanThreads - 1) / kScanThreads), kScanThreads, 0, s, p);
+}
+
+template <int VAR, int DK, int DV>
+cudaError_t run(const chunk::Maps& m, const Params& p, int sm_count, cudaStream_t s) {
+    using S3 = OutLayout<VAR, DK, DV>;
+    static_assert(S3::SMEM <= 232448, "shared memory budget");
+    auto k3 = output_kernel<VAR, DK, DV>;
+    cudaError_t e = run_states<VAR, DK, DV>(m, p, sm_count, s);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, S3::SMEM);
     if (e != cudaSuccess) return e;
+    const int units = p.BH * p.nch;
+    int g3 = sm_count * per_sm(S3::SMEM, S3::TMEM_COLS, kOutThreads, 2);
+    if (g3 > units) g3 = units;
     return launch_pdl(k3, g3, kOutThreads, S3::SMEM, s, m.q, m.v, m.o, p);
 }
 
@@ -658,14 +673,17 @@ bool par_fits(int BH, int T, int dk, int dv, size_t ws_bytes) {
     return need <= ws_bytes && need <= kParL2Bytes;
 }
 
-cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
+namespace {
+
+// The three-phase form's workspace: dX | dd | start states | start
+// normalizers | phi(k) tiles (each a multiple of 256 bytes per unit).
+par::Params carve(const FwdArgs& a, ParStates* st) {
     par::Params p;
     const size_t nch = static_cast<size_t>((a.T + C - 1) / C);
     const size_t units = static_cast<size_t>(a.BH) * nch;
     p.state_in = a.state_in;
     p.state_out = a.state_out;
     p.den_out = a.den_out;
-    // workspace: dX | dd | start states | start normalizers (each 256-byte aligned)
     uint8_t* w = reinterpret_cast<uint8_t*>(a.workspace);
     p.dx = reinterpret_cast<float*>(w);
     w += units * a.dk * a.dv * sizeof(float);
@@ -676,14 +694,38 @@ cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
     p.zs = reinterpret_cast<float*>(w);
     w += units * a.dk * sizeof(float);
     p.kh = w;
+    w += units * a.dk * 128;
     p.gamma = a.gate;   // the normalized variant's fixed decay, or NULL
     p.BH = a.BH;
     p.T = a.T;
     p.nch = static_cast<int>(nch);
     p.flags = a.flags;
     p.status = a.status;
+    if (st) {
+        st->dx = p.dx;
+        st->dd = p.dd;
+        st->xs = p.xs;
+        st->zs = p.zs;
+        st->kh = p.kh;
+        st->end = w;
+        st->nch = p.nch;
+    }
+    return p;
+}
+
+}  // namespace
+
+cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
+    const par::Params p = carve(a, nullptr);
     if (a.nlaunch) *a.nlaunch += 3;   // summary, scan, output
     if (a.variant == kNorm) return par::dispatch<kNorm>(a.dk, a.dv, m, p, a.sm_count, s);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_par_states(const FwdArgs& a, const Maps& m, cudaStream_t s, ParStates* st) {
+    const par::Params p = carve(a, st);
+    if (a.variant != kNorm || a.gate) return cudaErrorInvalidValue;
+    if (a.dk == 64 && a.dv == 64) return par::run_states<kNorm, 64, 64>(m, p, a.sm_count, s);
     return cudaErrorInvalidValue;
 }
 

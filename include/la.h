@@ -269,9 +269,18 @@ const char* la_last_error(const la_handle* h);
  * if dstate_in is not NULL, the gradient of the initial state (fp32, same
  * layout). The pages give the forward operator only; the gradients follow
  * from the chain rule through the update-first recurrence (phi'(x) = 1 for
- * x > 0, e^x otherwise). One CUDA-core kernel: it runs the recurrence
- * forward to the final state, then backward, recovering earlier states by
- * subtracting each token's update, so its fp32 rounding grows with T.
+ * x > 0, e^x otherwise).
+ * bf16 io with d_k = d_v = 64: the chunkwise tensor-core form (chunks of 64
+ * tokens), five kernels per group of sequence-heads whose per-chunk states
+ * fit the handle's workspace (about 50 KB per chunk of each sequence-head):
+ * the states entering every chunk, per-chunk normalizer gradients, a reverse
+ * scan of the state gradient, and the per-chunk input gradients. Other
+ * shapes, fp32 io, or a single sequence-head whose chunk states exceed the
+ * workspace: one CUDA-core kernel that runs the recurrence forward to the
+ * final state, then backward, recovering earlier states by subtracting each
+ * token's update, so its fp32 rounding grows with T. la_last_launches tells
+ * which ran (a multiple of 5, or 1). An expired bounded wait in the
+ * chunkwise kernels is reported by la_status.
  * Errors as for la_forward: LA_ERR_UNSUPPORTED for another variant or head
  * size, LA_ERR_INVALID_ARG, LA_ERR_MISALIGNED, LA_ERR_CUDA.
  */
@@ -280,12 +289,13 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
                 void* dq, void* dk, void* dv, float* dstate_in,
                 int variant, int T, void* cuda_stream);
 
-/* Number of CUDA kernels the last successful la_forward / la_decode_step on h
- * enqueued (0 after a failed or a T = 0 call, or for a NULL handle). A
- * diagnostic: which algorithm the library picked shows in this count (1: the
- * recurrent kernel or a decode step; 1 or 2: the chunk kernel, with segment
- * summaries when B*H is small; 3: the three-phase parallel form; LA_GDN,
- * LA_KDA and LA_GLA: one per group of 32 sequence-heads). */
+/* Number of CUDA kernels the last successful la_forward / la_decode_step /
+ * la_backward on h enqueued (0 after a failed or a T = 0 call, or for a NULL
+ * handle). A diagnostic: which algorithm the library picked shows in this
+ * count (1: the recurrent kernel or a decode step; 1 or 2: the chunk kernel,
+ * with segment summaries when B*H is small; 3: the three-phase parallel form;
+ * LA_GDN, LA_KDA and LA_GLA: one per group of 32 sequence-heads; la_backward:
+ * 5 per head group for the chunkwise form, 1 for the token-serial kernel). */
 int la_last_launches(const la_handle* h);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */

@@ -1,6 +1,8 @@
 """Gradients of the normalized prefill (la_backward) against the float64
 oracle's (oracle/backward.py, itself pinned by finite differences of the
-forward oracle), on the same seeded inputs."""
+forward oracle), on the same seeded inputs. bf16 io with d_k = d_v = 64 takes
+the chunkwise tensor-core backward (five launches); other shapes and fp32 io
+take the token-serial kernel (one launch)."""
 import numpy as np
 import pytest
 
@@ -36,7 +38,11 @@ def _case(B, H, T, dk, dv, io, seed, with_state, with_dstate):
     gdso = None if dso is None else torch.from_numpy(dso).to(dev)
     dq, dk_, dv_, dsin = h.backward(tq, tk, tv, to_torch(do_s, dev), gsin, gdso)
     torch.cuda.synchronize()
-    assert h.last_launches() == 1
+    chunked = io == "bf16" and dk == 64 and dv == 64
+    n = h.last_launches()
+    # chunkwise: one five-launch chain per group of sequence-heads whose
+    # per-chunk states fit the handle's workspace
+    assert (n >= 5 and n % 5 == 0) if chunked else n == 1, n
     assert h.status() == la.LA_OK
     h.close()
     rq, rk, rv, rs = backward.norm_backward(q, k, v, do64, sin, dso)
@@ -61,11 +67,23 @@ def test_backward_optional_states(with_state, with_dstate):
         assert slice_rel_err(g, r) <= TOL["bf16"], (name, slice_rel_err(g, r))
 
 
-def test_backward_long_sequence():
-    # 2048 tokens: the earlier states are recovered by subtracting 2048
-    # updates in fp32; the gradients still meet the bf16 bound
-    got, ref = _case(1, 2, 2048, 64, 64, "bf16", seed=7, with_state=False, with_dstate=True)
+@pytest.mark.parametrize("io", ["bf16", "fp32"])
+def test_backward_long_sequence(io):
+    # 2048 tokens: 32 chunks carried by the chunkwise form (bf16), or the
+    # earlier states recovered by subtracting 2048 updates in fp32 (the
+    # token-serial kernel); the gradients meet the io dtype's bound
+    got, ref = _case(1, 2, 2048, 64, 64, io, seed=7, with_state=False, with_dstate=True)
+    tol = TOL["bf16"]   # the fp32 kernel's subtraction drift at this length is above 1e-4
     for name, g, r in zip(("dq", "dk", "dv", "dstate_in"), got, ref):
+        assert slice_rel_err(g, r) <= tol, (name, slice_rel_err(g, r))
+
+
+def test_backward_workload_shape():
+    # the normalized workload's shapes, B4 H8 T2048 d64, every head (their
+    # per-chunk states exceed the handle's workspace: two head groups)
+    got, ref = _case(4, 8, 2048, 64, 64, "bf16", seed=11, with_state=True, with_dstate=True)
+    for name, g, r in zip(("dq", "dk", "dv", "dstate_in"), got, ref):
+        assert np.all(np.isfinite(g)), name
         assert slice_rel_err(g, r) <= TOL["bf16"], (name, slice_rel_err(g, r))
 
 
