@@ -526,14 +526,16 @@ def kernel_only(args):
     import torch
     import gated_delta_rule_causal_gb300 as la
     la.build()
-    w = W.BY_NAME[args.workload] if args.workload else HEADLINE
-    if w.decode_steps:
+    w = BACKWARD if args.backward else W.BY_NAME[args.workload] if args.workload else HEADLINE
+    props = torch.cuda.get_device_properties(0)
+    if args.backward:
+        r = BackwardRunner(w, 0, int(getattr(props, "L2_cache_size", 126 * 2 ** 20)), torch, la)
+    elif w.decode_steps:
         r = DecodeRunner(w.with_(decode_steps=8), 0, torch, la)
     else:
-        props = torch.cuda.get_device_properties(0)
         r = PrefillRunner(w, 0, int(getattr(props, "L2_cache_size", 126 * 2 ** 20)), torch, la)
     total_ms, per = time_steps(r, args.steps, args.warmup, torch)
-    print(json.dumps({"workload": w.name, "steps": args.steps, "ms_per_step": round(total_ms / args.steps, 5),
+    print(json.dumps({"workload": ("backward/" if args.backward else "") + w.name, "steps": args.steps, "ms_per_step": round(total_ms / args.steps, 5),
                       "kernel_ms": [round(x, 5) for x in per]}), flush=True)
 
 
@@ -613,6 +615,8 @@ def main():
     ap.add_argument("--no-suite", action="store_true")
     ap.add_argument("--only-kernel", action="store_true",
                     help="run warmup + steps of the workload's kernel and nothing else (for ncu)")
+    ap.add_argument("--backward", action="store_true",
+                    help="with --only-kernel: the normalized backward on its workload's shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

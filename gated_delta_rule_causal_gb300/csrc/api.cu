@@ -557,7 +557,9 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v, const
     // per group. Otherwise the token-serial kernel.
     const size_t per_head = la::chunk::bwd_chunk_bytes(1, T);
     if (c.io == LA_BF16 && c.d_k == 64 && c.d_v == 64 && h->d_ws && per_head <= h->ws_bytes) {
-        const int group = static_cast<int>(std::min<size_t>(h->ws_bytes / per_head, static_cast<size_t>(a.BH)));
+        const int most = static_cast<int>(std::min<size_t>(h->ws_bytes / per_head, static_cast<size_t>(a.BH)));
+        const int ngroups = (a.BH + most - 1) / most;
+        const int group = (a.BH + ngroups - 1) / ngroups;   // groups of even size
         const size_t ss = static_cast<size_t>(c.d_k) * c.d_v + c.d_k;   // floats per state
         const size_t row = static_cast<size_t>(T) * 64 * 2;            // bytes of one head's q (= k, v, dout)
         auto off = [](const void* p, size_t bytes) -> const void* {

@@ -35,9 +35,9 @@
 // 64-127 are the next 8 KB tile of shared memory (finite data, results
 // unused).
 //
-// Tail chunks: TMA zero-fills q, v and dO rows past T, and the forward summary
-// zeroes phi(k) there, so padded tokens have dnum = 0 and dden = 0 and add
-// nothing; their gradient rows are not stored.
+// Tail chunks: TMA zero-fills q, k, v and dO rows past T, and phi(k) is set
+// to zero there, so padded tokens have dnum = 0 and dden = 0 and add nothing;
+// their gradient rows are not stored.
 #include <cuda_bf16.h>
 
 #include "prefill.h"
@@ -69,7 +69,6 @@ struct Params {
     __nv_bfloat16* dv;
     const uint8_t* xs;         // [units] X_in = S_in^T tiles [v][k]
     const float* zs;           // [units][D] z_in
-    const uint8_t* kh;         // [units] phi(k) tiles [j][k]
     float* dG;                 // [units][v][k] fp32: dnum^T Q~ of the chunk
     float* dg;                 // [units][D]: Q~^T dden of the chunk
     uint8_t* dn;               // [units] dnum tiles [t][v]
@@ -99,17 +98,20 @@ __device__ __forceinline__ void load8(uint32_t tile, int row, int c, float* out)
     out[4] = d.x; out[5] = d.y; out[6] = e.x; out[7] = e.y;
 }
 
-// phi(q) in place over a [64][64] tile (two 16-byte chunks per thread).
-__device__ __forceinline__ void phi_tile(uint32_t tile, int tid) {
+// phi in place over the q and k tiles ([64][64] each, two 16-byte chunks
+// per thread and tile); k rows at or past `nvalid` (tokens past T) become 0.
+__device__ __forceinline__ void phi_tiles(uint32_t tq, uint32_t tk, int nvalid, int tid) {
 #pragma unroll
-    for (int i = 0; i < (64 * 8) / kThreads; ++i) {
+    for (int i = 0; i < (2 * 64 * 8) / kThreads; ++i) {
         const int e = tid + kThreads * i;
-        const int row = e / 8, pc = e % 8;
-        const uint32_t a = tile + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
+        const bool isk = e >= 64 * 8;
+        const int row = (e / 8) % 64, pc = e % 8;
+        const uint32_t a = (isk ? tk : tq) + (row >> 3) * 1024 + (row & 7) * 128 + pc * 16;
         const uint4 u = ld_shared_v4(a);
         const float2 x0 = unpack_bf16(u.x), x1 = unpack_bf16(u.y), x2 = unpack_bf16(u.z), x3 = unpack_bf16(u.w);
-        st_shared_v4(a, pack_bf16(elu1(x0.x), elu1(x0.y)), pack_bf16(elu1(x1.x), elu1(x1.y)),
-                     pack_bf16(elu1(x2.x), elu1(x2.y)), pack_bf16(elu1(x3.x), elu1(x3.y)));
+        const float m = (isk && row >= nvalid) ? 0.f : 1.f;
+        st_shared_v4(a, pack_bf16(m * elu1(x0.x), m * elu1(x0.y)), pack_bf16(m * elu1(x1.x), m * elu1(x1.y)),
+                     pack_bf16(m * elu1(x2.x), m * elu1(x2.y)), pack_bf16(m * elu1(x3.x), m * elu1(x3.y)));
     }
 }
 
@@ -128,14 +130,16 @@ struct SumL {
                               DN = 6 * TILE, PAD = 7 * TILE, MISC = 8 * TILE;
     // misc: z_in, den, rowsum(dO o num), dden, dg (fp32, 64 each)
     static constexpr uint32_t BAR = MISC + 5 * VEC;
-    // at least 80 KB, so that no more than two CTAs (2 x 256 columns of
-    // tensor memory) share an SM
-    static constexpr uint32_t SMEM = (BAR + 64 + 1024) > 81920 ? (BAR + 64 + 1024) : 81920;
-    static constexpr uint32_t COL_P = 0, COL_O = 64, COL_G = 128;
-    static constexpr uint32_t TMEM_COLS = 256;
+    // 67.9 KB: three CTAs (3 x 128 columns of tensor memory) share an SM
+    static constexpr uint32_t SMEM = BAR + 64 + 1024;
+    // dG^T reuses P's columns: P has been read out before the MMA that
+    // completes num is issued
+    static constexpr uint32_t COL_P = 0, COL_O = 64, COL_G = 0;
+    static constexpr uint32_t TMEM_COLS = 128;
 };
 
-__global__ void __launch_bounds__(kThreads) bw_sum_kernel(const __grid_constant__ CUtensorMap tmq,
+__global__ void __launch_bounds__(kThreads, 3) bw_sum_kernel(const __grid_constant__ CUtensorMap tmq,
+                                                          const __grid_constant__ CUtensorMap tmk,
                                                           const __grid_constant__ CUtensorMap tmv,
                                                           const __grid_constant__ CUtensorMap tmdo, const Params p) {
     using L = SumL;
@@ -164,6 +168,7 @@ __global__ void __launch_bounds__(kThreads) bw_sum_kernel(const __grid_constant_
         for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
         tma_prefetch_desc(&tmdo);
     }
@@ -193,7 +198,7 @@ __global__ void __launch_bounds__(kThreads) bw_sum_kernel(const __grid_constant_
     if (!failed && tid == 0) {
         mbar_arrive_expect_tx(&bar[0], 5 * TILE + VEC);
         tma_load_3d(&tmq, &bar[0], sm + L::Q, 0, t0, bh);
-        bulk_load(sm + L::K, p.kh + static_cast<size_t>(u) * TILE, TILE, &bar[0]);
+        tma_load_3d(&tmk, &bar[0], sm + L::K, 0, t0, bh);
         tma_load_3d(&tmv, &bar[0], sm + L::V, 0, t0, bh);
         bulk_load(sm + L::XS, p.xs + static_cast<size_t>(u) * TILE, TILE, &bar[0]);
         tma_load_3d(&tmdo, &bar[0], sm + L::DO, 0, t0, bh);
@@ -211,8 +216,9 @@ __global__ void __launch_bounds__(kThreads) bw_sum_kernel(const __grid_constant_
         if (__syncthreads_or(!ok)) { status_bits |= kStatusTmaWait; failed = true; }
         else loading = false;
     }
+    const int nvalid = min(C, p.T - t0);
     if (!failed) {
-        phi_tile(aQ, tid);
+        phi_tiles(aQ, aK, nvalid, tid);
         publish();
         // P = Q~ K~^T, O = Q~ X_in^T (tokens on the lanes)
         if (tid == 0) {
@@ -430,6 +436,7 @@ struct GradL {
 };
 
 __global__ void __launch_bounds__(kThreads) bw_grad_kernel(const __grid_constant__ CUtensorMap tmq,
+                                                           const __grid_constant__ CUtensorMap tmk,
                                                            const __grid_constant__ CUtensorMap tmv, const Params p) {
     using L = GradL;
     griddep_launch_dependents();
@@ -455,6 +462,7 @@ __global__ void __launch_bounds__(kThreads) bw_grad_kernel(const __grid_constant
         for (int i = 0; i < 3; ++i) mbar_init(&bar[i], 1);
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
     }
     griddep_wait();   // G and g after every chunk are complete (then tensor memory, as above)
@@ -475,7 +483,7 @@ __global__ void __launch_bounds__(kThreads) bw_grad_kernel(const __grid_constant
     if (!failed && tid == 0) {
         mbar_arrive_expect_tx(&bar[0], 6 * TILE + 3 * VEC);
         tma_load_3d(&tmq, &bar[0], sm + L::Q, 0, t0, bh);
-        bulk_load(sm + L::K, p.kh + static_cast<size_t>(u) * TILE, TILE, &bar[0]);
+        tma_load_3d(&tmk, &bar[0], sm + L::K, 0, t0, bh);
         tma_load_3d(&tmv, &bar[0], sm + L::V, 0, t0, bh);
         bulk_load(sm + L::DN, p.dn + static_cast<size_t>(u) * TILE, TILE, &bar[0]);
         bulk_load(sm + L::XS, p.xs + static_cast<size_t>(u) * TILE, TILE, &bar[0]);
@@ -500,7 +508,7 @@ __global__ void __launch_bounds__(kThreads) bw_grad_kernel(const __grid_constant
     constexpr uint32_t ID_KM = idesc_bf16(128, 64, false, true);
     constexpr uint32_t ID_MM = idesc_bf16(128, 64, true, true);
     if (!failed) {
-        phi_tile(aQ, tid);
+        phi_tiles(aQ, aK, min(C, p.T - t0), tid);
         publish();
         // P = Q~ K~^T and dnum V^T (tokens on the lanes)
         if (tid == 0) {
@@ -633,7 +641,7 @@ namespace chunk {
 
 size_t bwd_chunk_bytes(int BH, int T) {
     const size_t units = static_cast<size_t>(BH) * ((T + C - 1) / C);
-    return units * (par_chunk_bytes(bwd::D, bwd::D) + bwd::kExtraPerUnit);
+    return units * (par_state_bytes(bwd::D, bwd::D) + bwd::kExtraPerUnit);
 }
 
 cudaError_t launch_norm_backward_chunked(const BwdArgs& a, float* workspace, size_t ws_bytes, int* status,
@@ -680,7 +688,6 @@ cudaError_t launch_norm_backward_chunked(const BwdArgs& a, float* workspace, siz
     p.dv = static_cast<__nv_bfloat16*>(a.dv);
     p.xs = st.xs;
     p.zs = st.zs;
-    p.kh = st.kh;
     p.dG = st.dx;   // the chunk summaries are dead once the scan has run
     p.dg = st.dd;
     uint8_t* w = st.end;
@@ -700,13 +707,13 @@ cudaError_t launch_norm_backward_chunked(const BwdArgs& a, float* workspace, siz
     e = cudaFuncSetAttribute(bw_sum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SumL::SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(bw_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GradL::SMEM);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(bw_sum_kernel, static_cast<unsigned>(units), kThreads, SumL::SMEM, s, m.q, m.v, m.o, p);
+    e = launch_pdl(bw_sum_kernel, static_cast<unsigned>(units), kThreads, SumL::SMEM, s, m.q, m.k, m.v, m.o, p);
     if (e != cudaSuccess) return e;
     constexpr int PER = D * D / 2 + D / 2;
     const long long nthr = static_cast<long long>(a.BH) * PER;
     e = launch_pdl(bw_scan_kernel, static_cast<unsigned>((nthr + kScanThreads - 1) / kScanThreads), kScanThreads, 0, s, p);
     if (e != cudaSuccess) return e;
-    return launch_pdl(bw_grad_kernel, static_cast<unsigned>(units), kThreads, GradL::SMEM, s, m.q, m.v, p);
+    return launch_pdl(bw_grad_kernel, static_cast<unsigned>(units), kThreads, GradL::SMEM, s, m.q, m.k, m.v, p);
 }
 
 }  // namespace chunk

@@ -47,20 +47,20 @@ cudaError_t launch_seg(const FwdArgs& a, const Maps& m, cudaStream_t s);
 // the whole problem fit in the workspace and comfortably in L2.
 constexpr size_t kParL2Bytes = size_t(48) << 20;
 size_t par_chunk_bytes(int dk, int dv);
+size_t par_state_bytes(int dk, int dv);   // the same without the phi(k) tile
 bool par_fits(int BH, int T, int dk, int dv, size_t ws_bytes);
 cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s);
 
 // The first two phases alone (undecayed, d_k = d_v = 64), for the chunkwise
 // backward: per chunk, the state entering it (bf16 [d_v][d_k] operand tile
-// in xs, z in zs), phi(k) as an operand tile (kh); dx and dd hold the chunk
-// summaries and are free afterwards. `end` is the first byte of the
+// in xs, z in zs); dx and dd hold the chunk summaries and are free
+// afterwards. phi(k) tiles are not kept. `end` is the first byte of the
 // workspace past these arrays.
 struct ParStates {
     float* dx;
     float* dd;
     uint8_t* xs;
     float* zs;
-    uint8_t* kh;
     uint8_t* end;
     int nch;
 };

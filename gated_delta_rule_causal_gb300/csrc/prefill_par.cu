@@ -189,8 +189,11 @@ summary_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                             idesc_bf16(128, DK, true, true), kk > 0);
             mma_commit(&bar[2]);
             // phi(k) for the output phase, as the operand tile it reads
-            bulk_store(p.kh + static_cast<size_t>(u) * KA * 8192, aKH, KA * 8192);
-            bulk_commit();
+            // (not kept when only the chunk states are wanted)
+            if (p.kh) {
+                bulk_store(p.kh + static_cast<size_t>(u) * KA * 8192, aKH, KA * 8192);
+                bulk_commit();
+            }
         }
         {
             // sum of phi(k) per channel, from the bf16 operand the MMA reads
@@ -662,9 +665,13 @@ cudaError_t dispatch(int dk, int dv, const chunk::Maps& m, const Params& p, int 
 
 namespace chunk {
 
+size_t par_state_bytes(int dk, int dv) {
+    // dX fp32 + start state bf16 + dd + zs
+    return static_cast<size_t>(dk) * dv * 6 + static_cast<size_t>(dk) * 8;
+}
+
 size_t par_chunk_bytes(int dk, int dv) {
-    // dX fp32 + start state bf16 + dd + zs + phi(k) tile
-    return static_cast<size_t>(dk) * dv * 6 + static_cast<size_t>(dk) * 8 + static_cast<size_t>(dk) * 128;
+    return par_state_bytes(dk, dv) + static_cast<size_t>(dk) * 128;   // + the phi(k) tile
 }
 
 bool par_fits(int BH, int T, int dk, int dv, size_t ws_bytes) {
@@ -677,7 +684,7 @@ namespace {
 
 // The three-phase form's workspace: dX | dd | start states | start
 // normalizers | phi(k) tiles (each a multiple of 256 bytes per unit).
-par::Params carve(const FwdArgs& a, ParStates* st) {
+par::Params carve(const FwdArgs& a, ParStates* st, bool keep_kh = true) {
     par::Params p;
     const size_t nch = static_cast<size_t>((a.T + C - 1) / C);
     const size_t units = static_cast<size_t>(a.BH) * nch;
@@ -693,8 +700,8 @@ par::Params carve(const FwdArgs& a, ParStates* st) {
     w += units * a.dk * a.dv * 2;
     p.zs = reinterpret_cast<float*>(w);
     w += units * a.dk * sizeof(float);
-    p.kh = w;
-    w += units * a.dk * 128;
+    p.kh = keep_kh ? w : nullptr;
+    if (keep_kh) w += units * a.dk * 128;
     p.gamma = a.gate;   // the normalized variant's fixed decay, or NULL
     p.BH = a.BH;
     p.T = a.T;
@@ -706,7 +713,6 @@ par::Params carve(const FwdArgs& a, ParStates* st) {
         st->dd = p.dd;
         st->xs = p.xs;
         st->zs = p.zs;
-        st->kh = p.kh;
         st->end = w;
         st->nch = p.nch;
     }
@@ -723,7 +729,7 @@ cudaError_t launch_par(const FwdArgs& a, const Maps& m, cudaStream_t s) {
 }
 
 cudaError_t launch_par_states(const FwdArgs& a, const Maps& m, cudaStream_t s, ParStates* st) {
-    const par::Params p = carve(a, st);
+    const par::Params p = carve(a, st, false);
     if (a.variant != kNorm || a.gate) return cudaErrorInvalidValue;
     if (a.dk == 64 && a.dv == 64) return par::run_states<kNorm, 64, 64>(m, p, a.sm_count, s);
     return cudaErrorInvalidValue;
