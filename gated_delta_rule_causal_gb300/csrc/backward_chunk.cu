@@ -430,12 +430,14 @@ struct GradL {
                               PS = 6 * TILE, DP = 7 * TILE, PAD = 8 * TILE, MISC = 9 * TILE;
     // misc: z_in, g, dden (fp32, 64 each)
     static constexpr uint32_t BAR = MISC + 3 * VEC;
-    static constexpr uint32_t SMEM = (BAR + 64 + 1024) > 81920 ? (BAR + 64 + 1024) : 81920;   // <= 2 CTAs per SM
+    // 75.6 KB: three CTAs share an SM, two of which hold tensor memory
+    // (2 x 256 columns) while the third has its tiles landing
+    static constexpr uint32_t SMEM = BAR + 64 + 1024;
     static constexpr uint32_t COL_A = 0, COL_B = 64, COL_DV = 128;   // P then dQ~; dnum V^T then dK~; dV
     static constexpr uint32_t TMEM_COLS = 256;
 };
 
-__global__ void __launch_bounds__(kThreads) bw_grad_kernel(const __grid_constant__ CUtensorMap tmq,
+__global__ void __launch_bounds__(kThreads, 3) bw_grad_kernel(const __grid_constant__ CUtensorMap tmq,
                                                            const __grid_constant__ CUtensorMap tmk,
                                                            const __grid_constant__ CUtensorMap tmv, const Params p) {
     using L = GradL;
@@ -465,22 +467,11 @@ __global__ void __launch_bounds__(kThreads) bw_grad_kernel(const __grid_constant
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
     }
-    griddep_wait();   // G and g after every chunk are complete (then tensor memory, as above)
-    if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-
-    int status_bits = 0;
-    bool failed = false;
-    if (p.flags & 0x100u) {
-        const bool ok = mbar_wait(&bar[2], 0, 1000000ull);
-        if (__syncthreads_or(!ok)) { status_bits |= kStatusTestHook; failed = true; }
-    }
+    griddep_wait();   // G and g after every chunk are complete
+    // The tiles first: they need no tensor memory, so a CTA that waits in
+    // tcgen05.alloc for another CTA of the SM to finish has them landing.
     bool loading = false;
-    if (!failed && tid == 0) {
+    if (tid == 0) {
         mbar_arrive_expect_tx(&bar[0], 6 * TILE + 3 * VEC);
         tma_load_3d(&tmq, &bar[0], sm + L::Q, 0, t0, bh);
         tma_load_3d(&tmk, &bar[0], sm + L::K, 0, t0, bh);
@@ -492,6 +483,19 @@ __global__ void __launch_bounds__(kThreads) bw_grad_kernel(const __grid_constant
         bulk_load(sG, p.gz + static_cast<size_t>(u) * D, VEC, &bar[0]);
         bulk_load(sDden, p.ddn + static_cast<size_t>(u) * C, VEC, &bar[0]);
         loading = true;
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+
+    int status_bits = 0;
+    bool failed = false;
+    if (p.flags & 0x100u) {   // test hook: a wait nothing will satisfy, 1 ms limit
+        const bool ok = mbar_wait(&bar[2], 0, 1000000ull);
+        if (__syncthreads_or(!ok)) { status_bits |= kStatusTestHook; failed = true; }
     }
     int nmma = 0;
     auto mma_wait = [&](uint32_t parity) {
