@@ -35,7 +35,17 @@ struct la_handle {
 
 namespace {
 
-constexpr int kHostGroups = 2;   // la_forward_host: groups of sequence-heads in flight (2 measured best of 1, 2, 4, 8)
+// la_forward_host: groups of sequence-heads in flight, and how they cross the
+// host link. Below kLargeCall bytes per call: two groups (best of 1, 2, 4, 8
+// on the normalized B4 H8 T2048 call) moved by copy kernels. From there on:
+// four groups (best of 1, 2, 4, 8 on the gated-delta B2 H16 T8192 call) moved
+// by the copy engines, which need no SM: the chunkwise kernels of the gated
+// variants fill each SM's shared memory, so a copy kernel's CTAs could not
+// run beside them and the copies of one group would not overlap the
+// kernels of another.
+constexpr int kHostGroupsSmall = 2;
+constexpr int kHostGroupsLarge = 4;
+constexpr size_t kLargeCall = size_t(64) << 20;
 constexpr int kCopyCtas = 64;    // CTAs of one gather / scatter over the host link
 
 // Up to six contiguous byte ranges copied by one launch: the inputs of a
@@ -380,12 +390,9 @@ int la_forward_host(la_handle* h, const void* q, const void* k, const void* v, c
         h->host_ready = true;
     }
 
-    // Sequence-heads in up to kHostGroups groups; per group the bytes of
-    // every staged tensor, each slice 256-byte aligned.
+    // Sequence-heads in groups; per group the bytes of every staged tensor,
+    // each slice 256-byte aligned.
     const int BH = c.B * c.H;
-    const int G0 = BH < kHostGroups ? BH : kHostGroups;
-    const int gbh = (BH + G0 - 1) / G0;
-    const int G = (BH + gbh - 1) / gbh;
     const size_t io = (c.io == LA_BF16) ? 2 : 4;
     const size_t ss = state_elems(c, variant);
     const size_t tok = static_cast<size_t>(T);
@@ -395,6 +402,13 @@ int la_forward_host(la_handle* h, const void* q, const void* k, const void* v, c
         tok * c.d_k * io, tok * c.d_k * io, tok * c.d_v * io,                    // q, k, v
         gate ? gate_per_head * 4 : 0, beta ? tok * 4 : 0, state_in ? ss * 4 : 0,  // gate, beta, state_in
         tok * c.d_v * io, state_out ? ss * 4 : 0, den_out ? tok * 4 : 0};         // out, state_out, den_out
+    size_t call_bytes = 0;
+    for (int i = 0; i < 9; ++i) call_bytes += per_head[i] * BH;
+    const bool large = call_bytes >= kLargeCall;
+    const int want = large ? kHostGroupsLarge : kHostGroupsSmall;
+    const int G0 = BH < want ? BH : want;
+    const int gbh = (BH + G0 - 1) / G0;
+    const int G = (BH + gbh - 1) / gbh;
     size_t off[9], buf = 0;
     for (int i = 0; i < 9; ++i) {
         off[i] = buf;
@@ -416,10 +430,11 @@ int la_forward_host(la_handle* h, const void* q, const void* k, const void* v, c
     }
     const void* src[6] = {q, k, v, gate, beta, state_in};
     void* dst[3] = {out, state_out, den_out};
-    // copy kernels when the GPU can address every host buffer, else the copy engine
+    // copy kernels for a small call when the GPU can address every host
+    // buffer, else the copy engines
     const uint8_t* msrc[6];
     uint8_t* mdst[3];
-    bool by_kernel = true;
+    bool by_kernel = !large;
     for (int i = 0; i < 6; ++i) {
         msrc[i] = mapped(src[i]);
         if (src[i] && !msrc[i]) by_kernel = false;
