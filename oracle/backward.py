@@ -1,4 +1,6 @@
-"""Float64 gradients of the normalized elu+1 recurrence (test infrastructure).
+"""Float64 gradients of the normalized elu+1 recurrence (with and without a
+fixed decay) and of the gated delta rule (scalar or per-channel decay), as
+test infrastructure.
 
 TEST INFRASTRUCTURE, like the rest of ``oracle``: only ``tests/`` and
 ``bench.py``'s CPU legs use it.
@@ -21,7 +23,9 @@ by token, in plain float64:
 
 ``tests/test_oracle_pins.py`` pins every output against central finite
 differences of the C forward oracle (``oracle.run``), which shares no
-arithmetic with this module.
+arithmetic with this module; ``tests/test_backward_mutations.py`` plants
+mistakes in copies of each function and checks that those pins catch them.
+``delta_backward`` states its own chain rule.
 """
 from __future__ import annotations
 
@@ -199,3 +203,74 @@ def norm_backward_chunked(q, k, v, do, C=64, state_in=None, dstate_out=None):
         g = g + np.einsum("bhtk,bht->bhk", Q, dden)
     dsin = np.concatenate([G.reshape(B, H, dk * dv), g], axis=-1)
     return dq, dkk, dvv, dsin
+
+
+def delta_backward(q, k, v, decay, beta, do, state_in=None, dstate_out=None):
+    """Gradients of the gated delta rule, scalar or per-channel decay.
+
+    The forward operator is the gated delta rule with the decay applied to
+    the state before the error is taken ("Beyond attention" §18.2 for a
+    scalar gate; "Linear attention and recurrent memory", from fixed decay to
+    KDA, for a decay per key channel), S in R^{dv x dk}:
+
+        S~_t = S_{t-1} Diag(a_t)      (a_t = g_t 1 for the scalar gate)
+        u_t  = beta_t (v_t - S~_t k_t),   S_t = S~_t + u_t k_t^T,   o_t = S_t q_t
+
+    The pages give no gradients. By the chain rule, with D_t the whole
+    gradient reaching S_t (the final-state cotangent, then carried back) and
+    every term taken at token t:
+
+        D_t  += do_t q_t^T,                  dq_t = S_t^T do_t
+        du    = D_t k_t
+        dv_t  = beta_t du,                   dbeta_t = (v_t - S~_t k_t) . du
+        dk_t  = D_t^T u_t - beta_t S~_t^T du
+        dS~   = D_t - beta_t du k_t^T
+        D_{t-1} = dS~ Diag(a_t)
+        da_t  = column sums of dS~ o S_{t-1}   (their total for a scalar g_t)
+
+    and dstate_in = D_0. q, k [B,H,T,dk]; v, do [B,H,T,dv]; decay [B,H,T]
+    (scalar gate g) or [B,H,T,dk] (per-channel alpha); beta [B,H,T];
+    state_in, dstate_out [B,H,dv*dk] (S row-major) or None. Returns
+    (dq, dk, dv, ddecay, dbeta, dstate_in) in float64, ddecay shaped like
+    decay.
+
+    ``tests/test_oracle_pins.py`` pins every output against central finite
+    differences of the C forward oracle (``oracle.run``), which shares no
+    arithmetic with this module.
+    """
+    q, k, v, do = (np.asarray(a, np.float64) for a in (q, k, v, do))
+    a = np.asarray(decay, np.float64)
+    bt = np.asarray(beta, np.float64)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    per_channel = a.ndim == 4
+    av = a if per_channel else np.broadcast_to(a[..., None], (B, H, T, dk))
+    sin = np.zeros((B, H, dv, dk)) if state_in is None else np.asarray(state_in, np.float64).reshape(B, H, dv, dk)
+    # forward, keeping every state: S[:, :, t + 1] is the state after token t
+    S = np.empty((B, H, T + 1, dv, dk))
+    S[:, :, 0] = sin
+    for t in range(T):
+        st = S[:, :, t] * av[:, :, t, None, :]
+        u = bt[:, :, t, None] * (v[:, :, t] - np.einsum("bhvk,bhk->bhv", st, k[:, :, t]))
+        S[:, :, t + 1] = st + u[..., None] * k[:, :, t, None, :]
+    D = np.zeros((B, H, dv, dk)) if dstate_out is None else np.asarray(dstate_out, np.float64).reshape(B, H, dv, dk).copy()
+    dq, dkk, dvv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    da = np.empty((B, H, T, dk))
+    db = np.empty((B, H, T))
+    for t in range(T - 1, -1, -1):
+        kt, qt = k[:, :, t], q[:, :, t]
+        D = D + do[:, :, t, :, None] * qt[:, :, None, :]
+        dq[:, :, t] = np.einsum("bhvk,bhv->bhk", S[:, :, t + 1], do[:, :, t])
+        st = S[:, :, t] * av[:, :, t, None, :]
+        err = v[:, :, t] - np.einsum("bhvk,bhk->bhv", st, kt)
+        u = bt[:, :, t, None] * err
+        du = np.einsum("bhvk,bhk->bhv", D, kt)
+        dvv[:, :, t] = bt[:, :, t, None] * du
+        db[:, :, t] = np.einsum("bhv,bhv->bh", err, du)
+        dkk[:, :, t] = (np.einsum("bhvk,bhv->bhk", D, u)
+                        - bt[:, :, t, None] * np.einsum("bhvk,bhv->bhk", st, du))
+        dst = D - bt[:, :, t, None, None] * du[..., None] * kt[:, :, None, :]
+        da[:, :, t] = np.einsum("bhvk,bhvk->bhk", dst, S[:, :, t])
+        D = dst * av[:, :, t, None, :]
+    dgate = da if per_channel else da.sum(axis=-1)
+    return dq, dkk, dvv, dgate, db, D.reshape(B, H, dv * dk)

@@ -38,6 +38,24 @@ MUTANTS_DECAY = {
 }
 
 
+# planted in delta_backward (gated delta rule, scalar and per-channel decay)
+MUTANTS_DELTA = {
+    "drops_write_correction_of_state_gradient": ("dst = D - bt[:, :, t, None, None] * du[..., None] * kt[:, :, None, :]",
+                                                 "dst = D"),
+    "dk_without_state_term": ('''
+                        - bt[:, :, t, None] * np.einsum("bhvk,bhv->bhk", st, du))''', ")"),
+    "dk_with_undecayed_state": ('np.einsum("bhvk,bhv->bhk", st, du)', 'np.einsum("bhvk,bhv->bhk", S[:, :, t], du)'),
+    "dbeta_with_value_not_error": ('db[:, :, t] = np.einsum("bhv,bhv->bh", err, du)',
+                                   'db[:, :, t] = np.einsum("bhv,bhv->bh", v[:, :, t], du)'),
+    "decay_gradient_against_new_state": ('np.einsum("bhvk,bhvk->bhk", dst, S[:, :, t])',
+                                         'np.einsum("bhvk,bhvk->bhk", dst, S[:, :, t + 1])'),
+    "state_gradient_not_decayed": ("D = dst * av[:, :, t, None, :]", "D = dst"),
+    "dq_from_previous_state": ('np.einsum("bhvk,bhv->bhk", S[:, :, t + 1], do[:, :, t])',
+                               'np.einsum("bhvk,bhv->bhk", S[:, :, t], do[:, :, t])'),
+    "dv_without_beta": ("dvv[:, :, t] = bt[:, :, t, None] * du", "dvv[:, :, t] = du"),
+}
+
+
 def _split(text):
     """(head, norm_backward, norm_decay_backward) sources."""
     a = text.index("def norm_backward(")
@@ -151,3 +169,64 @@ def test_decay_mutant_is_caught(name, case_decay):
         head, plain, decay = _split(fh.read())
     assert decay.count(old) == 1, name
     assert not _agrees_decay(_load(head + plain + decay.replace(old, new)), case_decay), name
+
+
+def _delta_fd_case(variant, seed):
+    g = np.random.default_rng(seed)
+    B, H, T, dk, dv = 1, 1, 5, 3, 2
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    k = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    a = g.uniform(0.5, 1.0, (B, H, T, dk) if variant == "kda" else (B, H, T))
+    b = g.uniform(0.1, 0.9, (B, H, T))
+    sin = g.standard_normal((B, H, dv * dk)) * 0.3
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, dv * dk))
+
+    def loss():
+        r = oracle.run(variant, q, k, v, a, b, sin)
+        return float(np.sum(r.o * W) + np.sum(r.state * Ws))
+
+    eps = 1e-6
+    fd = []
+    for arr in (q, k, v, a, b, sin):
+        grad = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = loss()
+            arr[idx] = a0 - eps
+            lm = loss()
+            arr[idx] = a0
+            grad[idx] = (lp - lm) / (2 * eps)
+        fd.append(grad)
+    return (q, k, v, a, b, W, sin, Ws), fd
+
+
+@pytest.fixture(scope="module")
+def delta_cases():
+    return {"gdn": _delta_fd_case("gdn", 103), "kda": _delta_fd_case("kda", 107)}
+
+
+def _agrees_delta(mod, case):
+    (q, k, v, a, b, W, sin, Ws), fd = case
+    got = mod.delta_backward(q, k, v, a, b, W, sin, Ws)
+    return all(np.allclose(gr, f, rtol=1e-6, atol=1e-6) for gr, f in zip(got, fd))
+
+
+def test_unmutated_delta_backward_agrees(delta_cases):
+    with open(SRC) as fh:
+        mod = _load(fh.read())
+    for case in delta_cases.values():
+        assert _agrees_delta(mod, case)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS_DELTA))
+def test_delta_mutant_is_caught(name, delta_cases):
+    old, new = MUTANTS_DELTA[name]
+    with open(SRC) as fh:
+        text = fh.read()
+    i = text.index("def delta_backward(")
+    head, body = text[:i], text[i:]
+    assert body.count(old) == 1, name
+    mod = _load(head + body.replace(old, new))
+    # caught when it disagrees with the finite differences on either decay
+    assert not all(_agrees_delta(mod, c) for c in delta_cases.values()), name

@@ -615,3 +615,76 @@ def test_norm_backward_chunked_equals_token_by_token(C, T):
     b = backward.norm_backward_chunked(q, k, v, W, C, sin, Ws)
     for x, y in zip(a, b):
         assert np.allclose(x, y, rtol=1e-11, atol=1e-12)
+
+
+# ------------------------------------------------------------- gradients of (c) and its per-channel form
+
+def _delta_case(g, per_channel, B=1, H=2, T=6, dk=3, dv=2):
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    k = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    a = g.uniform(0.5, 1.0, (B, H, T, dk) if per_channel else (B, H, T))
+    b = g.uniform(0.1, 0.9, (B, H, T))
+    sin = g.standard_normal((B, H, dv * dk)) * 0.3
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, dv * dk))
+    return q, k, v, a, b, sin, W, Ws
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_delta_backward_matches_finite_differences(variant):
+    # Every gradient of the float64 backward (q, k, v, the decay, beta and the
+    # initial state) against central differences of the C forward recurrence,
+    # entry by entry, with cotangents on the outputs and the final state.
+    from oracle import backward
+    q, k, v, a, b, sin, W, Ws = _delta_case(rng(83 if variant == "gdn" else 89), variant == "kda")
+
+    def loss():
+        r = oracle.run(variant, q, k, v, a, b, sin)
+        return float(np.sum(r.o * W) + np.sum(r.state * Ws))
+
+    grads = backward.delta_backward(q, k, v, a, b, W, sin, Ws)
+    eps = 1e-6
+    for name, arr, grad in zip(("q", "k", "v", "decay", "beta", "s"), (q, k, v, a, b, sin), grads):
+        assert grad.shape == arr.shape, name
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = loss()
+            arr[idx] = a0 - eps
+            lm = loss()
+            arr[idx] = a0
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_delta_backward_frozen_state_closed_form():
+    # beta = 0 and a decay of 1 leave the state at S_0, so o_t = S_0 q_t: the
+    # gradient reaching token t is D_t = dS_T + sum_{tau >= t} do_tau q_tau^T,
+    # and dq_t = S_0^T do_t, dv = dk = 0, dbeta_t = (v_t - S_0 k_t) . D_t k_t,
+    # dg_t = <D_t, S_0>, dstate_in = D_0.
+    from oracle import backward
+    g = rng(97)
+    B, H, T, dk, dv = 2, 1, 5, 4, 3
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    S0 = g.standard_normal((B, H, dv, dk))
+    do, dso = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, dv, dk))
+    dq, dk_, dv_, dg, db, dsin = backward.delta_backward(q, k, v, np.ones((B, H, T)), np.zeros((B, H, T)), do,
+                                                         S0.reshape(B, H, -1), dso.reshape(B, H, -1))
+    D = dso[:, :, None] + np.cumsum(np.einsum("bhtv,bhtk->bhtvk", do, q)[:, :, ::-1], axis=2)[:, :, ::-1]   # D_t
+    assert np.allclose(dq, np.einsum("bhvk,bhtv->bhtk", S0, do), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dv_, 0.0) and np.allclose(dk_, 0.0)
+    err = v - np.einsum("bhvk,bhtk->bhtv", S0, k)
+    assert np.allclose(db, np.einsum("bhtv,bhtvk,bhtk->bht", err, D, k), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dg, np.einsum("bhtvk,bhvk->bht", D, S0), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dsin.reshape(B, H, dv, dk), D[:, :, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_delta_backward_uniform_channels_is_scalar_gate():
+    # A per-channel decay equal on every channel is the scalar gate: the same
+    # gradients, the scalar gate's being the sum over channels.
+    from oracle import backward
+    q, k, v, a, b, sin, W, Ws = _delta_case(rng(101), False, B=2, H=1, T=7, dk=4, dv=3)
+    s = backward.delta_backward(q, k, v, a, b, W, sin, Ws)
+    c = backward.delta_backward(q, k, v, np.repeat(a[..., None], 4, axis=-1), b, W, sin, Ws)
+    for i in (0, 1, 2, 4, 5):
+        assert np.allclose(s[i], c[i], rtol=1e-12, atol=1e-12)
+    assert np.allclose(s[3], c[3].sum(-1), rtol=1e-12, atol=1e-12)
