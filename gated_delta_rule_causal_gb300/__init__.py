@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.la_decode_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, vp, fp, fp, i, vp]
             L.la_backward.restype = i
             L.la_backward.argtypes = [vp, vp, vp, vp, fp, vp, fp, vp, vp, vp, fp, i, i, vp]
+            L.la_backward_gated.restype = i
+            L.la_backward_gated.argtypes = [vp, vp, vp, vp, fp, fp, fp, vp, fp, vp, vp, vp, fp, fp, fp, i, i, vp]
             L.la_decode_step.restype = i
             L.la_status.argtypes = [vp, vp]
             L.la_status.restype = i
@@ -317,6 +319,33 @@ class Handle:
                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dstate_in), var, T, _stream_ptr(stream))
         self._check(rc)
         return dq, dk, dv, dstate_in
+
+    def backward_gated(self, q, k, v, gate, beta, dout, state_in=None, dstate_out=None, *, variant="gdn",
+                       return_dstate=True, stream=None):
+        """Gradients of a gated delta rule prefill (variant "gdn": gate
+        [B,H,T]; "kda": gate [B,H,T,d_k]); beta [B,H,T]. Returns (dq, dk, dv,
+        dgate, dbeta, dstate_in)."""
+        import torch
+        var = VARIANTS[variant]
+        B, H, T = q.shape[0], q.shape[1], q.shape[2]
+        if (B, H) != (self.B, self.H):
+            raise ValueError("q batch/heads differ from the handle's")
+        for name, t, d in (("q", q, self.d_k), ("k", k, self.d_k), ("v", v, self.d_v), ("dout", dout, self.d_v)):
+            self._expect(name, t, (B, H, T, d), self.dtype)
+        gshape = (B, H, T, self.d_k) if variant == "kda" else (B, H, T)
+        self._expect("gate", gate, gshape, torch.float32)
+        self._expect("beta", beta, (B, H, T), torch.float32)
+        ss = state_size(variant, self.d_k, self.d_v)
+        self._expect("state_in", state_in, (B, H, ss), torch.float32)
+        self._expect("dstate_out", dstate_out, (B, H, ss), torch.float32)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dgate, dbeta = torch.empty_like(gate), torch.empty_like(beta)
+        dstate_in = torch.empty((B, H, ss), dtype=torch.float32, device=self.device) if return_dstate else None
+        rc = lib().la_backward_gated(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(beta), _ptr(state_in),
+                                     _ptr(dout), _ptr(dstate_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgate),
+                                     _ptr(dbeta), _ptr(dstate_in), var, T, _stream_ptr(stream))
+        self._check(rc)
+        return dq, dk, dv, dgate, dbeta, dstate_in
 
     def last_launches(self) -> int:
         """Kernels the last forward / decode_step call enqueued."""

@@ -19,7 +19,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblacausal.so")
 SOURCES = ["api.cu", "recurrent.cu", "decode.cu", "prefill.cu",
            "prefill_norm.cu", "prefill_gdn.cu", "prefill_par.cu",
-           "prefill_seg.cu", "noalloc.cu", "backward.cu", "backward_chunk.cu"]
+           "prefill_seg.cu", "noalloc.cu", "backward.cu", "backward_chunk.cu",
+           "backward_delta.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
          "-I" + os.path.join(ROOT, "include")]

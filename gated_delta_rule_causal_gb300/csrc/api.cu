@@ -31,6 +31,10 @@ struct la_handle {
     cudaStream_t s_in, s_comp, s_out;
     cudaEvent_t ev_start, ev_done, ev_in[2], ev_comp[2], ev_out[2];
     bool host_ready;
+    // la_backward_gated: checkpoints and accumulators (allocated on first
+    // use, grown when a call needs more)
+    float* d_bws;
+    size_t bws_bytes;
 };
 
 namespace {
@@ -253,6 +257,8 @@ int la_create(const la_config* cfg, la_handle** out) {
     h->d_stage = nullptr;
     h->stage_bytes = 0;
     h->host_ready = false;
+    h->d_bws = nullptr;
+    h->bws_bytes = 0;
     DeviceGuard g(cfg->device);
     if (!g.ok) { delete h; return LA_ERR_CUDA; }
     if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess || cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
@@ -314,6 +320,7 @@ void la_destroy(la_handle* h) {
                 cudaEventDestroy(e);
         }
         if (h->d_stage) cudaFree(h->d_stage);
+        if (h->d_bws) cudaFree(h->d_bws);
         if (h->d_status) cudaFree(h->d_status);
         if (h->d_ws) cudaFree(h->d_ws);
     }
@@ -607,6 +614,71 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v, const
     const cudaError_t e = la::launch_norm_backward(a, static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "backward kernel launch");
     h->last_launches = 1;
+    return LA_OK;
+}
+
+int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v, const float* gate, const float* beta,
+                      const float* state_in, const void* dout, const float* dstate_out, void* dq, void* dk, void* dv,
+                      float* dgate, float* dbeta, float* dstate_in, int variant, int T, void* cuda_stream) {
+    if (!h) return LA_ERR_INVALID_ARG;
+    h->last_error.clear();
+    h->last_launches = 0;
+    if (variant != LA_GDN && variant != LA_KDA)
+        return fail(h, LA_ERR_UNSUPPORTED, "la_backward_gated supports LA_GDN and LA_KDA");
+    if (T < 1) return fail(h, LA_ERR_INVALID_ARG, "T must be >= 1");
+    if (!q || !k || !v || !gate || !beta || !dout || !dq || !dk || !dv || !dgate || !dbeta)
+        return fail(h, LA_ERR_INVALID_ARG, "q, k, v, gate, beta, dout, dq, dk, dv, dgate and dbeta are required");
+    const la_config& c = h->cfg;
+    if (!((c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128)))
+        return fail(h, LA_ERR_UNSUPPORTED, "la_backward_gated supports d_k, d_v in {64, 128}");
+    if (static_cast<long long>(T) * (c.d_k > c.d_v ? c.d_k : c.d_v) > (1LL << 31) - 1)
+        return fail(h, LA_ERR_UNSUPPORTED, "T * d exceeds 2^31 - 1");
+    const void* ptrs[] = {q, k, v, gate, beta, state_in, dout, dstate_out, dq, dk, dv, dgate, dbeta, dstate_in};
+    const char* names[] = {"q", "k", "v", "gate", "beta", "state_in", "dout", "dstate_out", "dq", "dk", "dv",
+                           "dgate", "dbeta", "dstate_in"};
+    for (int i = 0; i < 14; ++i)
+        if (ptrs[i] && !aligned16(ptrs[i]))
+            return fail(h, LA_ERR_MISALIGNED, std::string(names[i]) + " is not 16-byte aligned");
+    DeviceGuard g(c.device);
+    if (!g.ok) return fail(h, LA_ERR_CUDA, "cannot select the handle's device");
+    const int BH = c.B * c.H;
+    const size_t need = la::delta_backward_bytes(BH, T, c.d_k, c.d_v);
+    if (need > h->bws_bytes) {
+        if (h->d_bws) {
+            cudaFree(h->d_bws);   // waits for the work that used it
+            h->d_bws = nullptr;
+            h->bws_bytes = 0;
+        }
+        const cudaError_t e = cudaMalloc(&h->d_bws, need);
+        if (e != cudaSuccess) return cuda_fail(h, e, "backward workspace allocation");
+        h->bws_bytes = need;
+    }
+    la::DeltaBwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.gate = gate;
+    a.beta = beta;
+    a.state_in = state_in;
+    a.dout = dout;
+    a.dstate_out = dstate_out;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dgate = dgate;
+    a.dbeta = dbeta;
+    a.dstate_in = dstate_in;
+    a.BH = BH;
+    a.T = T;
+    a.dk_dim = c.d_k;
+    a.dv_dim = c.d_v;
+    a.io = c.io == LA_FP32 ? la::kFp32 : la::kBf16;
+    a.per_channel = variant == LA_KDA;
+    a.sm_count = h->sm_count;
+    a.workspace = h->d_bws;
+    const cudaError_t e = la::launch_delta_backward(a, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail(h, e, "gated backward launch");
+    h->last_launches = 2;   // the token-serial kernel and the dq / dk conversion
     return LA_OK;
 }
 

@@ -1,0 +1,298 @@
+// Gradients of the gated delta rule (scalar or per-channel decay) on CUDA
+// cores, token by token, in fp32.
+//
+// Forward operator ("Beyond attention" §18.2 for the scalar gate; "Linear
+// attention and recurrent memory", from fixed decay to KDA, for a decay per
+// key channel), S in R^{dv x dk}:
+//    S~_t = S_{t-1} Diag(a_t)   (a_t = g_t 1 for the scalar gate)
+//    u_t  = beta_t (v_t - S~_t k_t),   S_t = S~_t + u_t k_t^T,   o_t = S_t q_t
+// The pages give no gradients. By the chain rule, with D the whole gradient
+// reaching S_t (the final-state cotangent, then carried back):
+//    D += do_t q_t^T,            dq_t = S_t^T do_t
+//    du = D k_t,                 dv_t = beta_t du,   dbeta_t = (v_t - S~_t k_t) . du
+//    dk_t = D^T u_t - beta_t S~_t^T du
+//    dS~ = D - beta_t du k_t^T,  da_t = column sums of dS~ o S_{t-1} (their total for g_t)
+//    D <- dS~ Diag(a_t);         dstate_in = D after token 0.
+//
+// Every value row of S (and of D) evolves on its own given k, a and beta, so
+// the work splits by rows: one CTA per (sequence-head, block of kRows rows),
+// one warp per row, each lane holding DK/32 adjacent columns. Each CTA first
+// runs its rows forward and stores them at the start of every segment of
+// kSeg tokens (workspace). It then walks the segments from the last: it
+// reloads the segment's starting rows, recomputes the kSeg + 1 row states in
+// registers, and takes the tokens in reverse. The row-local gradients (dv)
+// are written directly; the sums over rows (dq, dk, the decay and beta
+// gradients) go through shared memory once per token and then into fp32
+// accumulators with one atomic add per column per CTA. A second kernel
+// writes dq and dk in the io dtype.
+//
+// This is the correctness path of the gated variants' gradients: its cost is
+// the token-serial walk (2 T dependent steps per row) and the per-token
+// reduction, not memory bandwidth.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace la {
+namespace {
+
+constexpr int kRows = 16;             // value rows per CTA (one warp each)
+constexpr int kSeg = 16;              // tokens per recomputed segment
+constexpr int kThreads = kRows * 32;
+
+template <typename T> __device__ __forceinline__ float ld_io(const T* p, size_t i);
+template <> __device__ __forceinline__ float ld_io<float>(const float* p, size_t i) { return p[i]; }
+template <> __device__ __forceinline__ float ld_io<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) {
+    return __bfloat162float(p[i]);
+}
+template <typename T> __device__ __forceinline__ void st_io(T* p, size_t i, float x);
+template <> __device__ __forceinline__ void st_io<float>(float* p, size_t i, float x) { p[i] = x; }
+template <> __device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16* p, size_t i, float x) {
+    p[i] = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Shared memory of one CTA.
+template <int DK, bool PC>
+struct Smem {
+    static constexpr int NV = PC ? 3 : 2;           // column sums per token: dq, dk (, da)
+    static constexpr int RED = NV * DK + 2;         // + dbeta and (scalar gate) dg
+    float k[kSeg][DK];
+    float q[kSeg][DK];
+    float a[PC ? kSeg : 1][DK];                     // per-channel decay
+    float g[kSeg];                                  // scalar decay
+    float b[kSeg];
+    float v[kSeg][kRows];
+    float dout[kSeg][kRows];
+    float dv[kSeg][kRows];
+    float red[2][kRows][RED];
+};
+
+template <int DK, int DV, bool PC, typename IO>
+__global__ void __launch_bounds__(kThreads, 1) delta_backward_kernel(DeltaBwdArgs p) {
+    constexpr int NC = DK / 32;   // columns per lane
+    constexpr int NRB = DV / kRows;
+    using SM = Smem<DK, PC>;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SM& sm = *reinterpret_cast<SM*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x / NRB, rb = blockIdx.x % NRB;
+    const int r = rb * kRows + warp;   // this warp's value row
+    const int c0 = lane * NC;          // this lane's first column
+    const int T = p.T;
+    const int nseg = (T + kSeg - 1) / kSeg;
+    const size_t tok0 = static_cast<size_t>(bh) * T;
+    const IO* q = static_cast<const IO*>(p.q);
+    const IO* k = static_cast<const IO*>(p.k);
+    const IO* v = static_cast<const IO*>(p.v);
+    const IO* dout = static_cast<const IO*>(p.dout);
+    const size_t ssz = static_cast<size_t>(DV) * DK;
+    float* ck = p.ckpt + (static_cast<size_t>(bh) * nseg * DV + r) * DK + c0;   // + seg * DV * DK
+
+    // Stage the inputs of tokens [t0, t0 + n) that every warp reads.
+    auto stage = [&](int t0, int n, bool with_q) {
+        for (int x = tid; x < kSeg * DK; x += kThreads) {
+            const int i = x / DK, c = x % DK;
+            const bool in = i < n;
+            const size_t e = (tok0 + t0 + i) * DK + c;
+            sm.k[i][c] = in ? ld_io(k, e) : 0.f;
+            if (with_q) sm.q[i][c] = in ? ld_io(q, e) : 0.f;
+            if (PC) sm.a[i][c] = in ? p.gate[e] : 1.f;
+        }
+        for (int x = tid; x < kSeg; x += kThreads) {
+            const bool in = x < n;
+            if (!PC) sm.g[x] = in ? p.gate[tok0 + t0 + x] : 1.f;
+            sm.b[x] = in ? p.beta[tok0 + t0 + x] : 0.f;
+        }
+        for (int x = tid; x < kSeg * kRows; x += kThreads) {
+            const int i = x / kRows, w = x % kRows;
+            const bool in = i < n;
+            const size_t e = (tok0 + t0 + i) * DV + rb * kRows + w;
+            sm.v[i][w] = in ? ld_io(v, e) : 0.f;
+            if (with_q) sm.dout[i][w] = in ? ld_io(dout, e) : 0.f;
+        }
+    };
+    // One token forward on this lane's columns of row r: s <- S_t, returns
+    // the error v_t - S~_t k_t (the same on every lane).
+    auto step = [&](int i, float* s) -> float {
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+            s[j] *= PC ? sm.a[i][c0 + j] : sm.g[i];
+            part += s[j] * sm.k[i][c0 + j];
+        }
+        const float err = sm.v[i][warp] - warp_sum(part);
+        const float u = sm.b[i] * err;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) s[j] += u * sm.k[i][c0 + j];
+        return err;
+    };
+
+    // ---- forward: the rows at the start of every segment -------------------
+    float s[NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) s[j] = p.state_in ? p.state_in[bh * ssz + static_cast<size_t>(r) * DK + c0 + j] : 0.f;
+    for (int sg = 0; sg < nseg; ++sg) {
+        const int t0 = sg * kSeg, n = min(kSeg, T - t0);
+        float* dst = ck + static_cast<size_t>(sg) * DV * DK;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) dst[j] = s[j];
+        __syncthreads();   // the previous segment's inputs are no longer read
+        stage(t0, n, false);
+        __syncthreads();
+        for (int i = 0; i < n; ++i) step(i, s);
+    }
+
+    // ---- backward: segments from the last ---------------------------------
+    float D[NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) D[j] = p.dstate_out ? p.dstate_out[bh * ssz + static_cast<size_t>(r) * DK + c0 + j] : 0.f;
+    int buf = 0;
+    for (int sg = nseg - 1; sg >= 0; --sg) {
+        const int t0 = sg * kSeg, n = min(kSeg, T - t0);
+        __syncthreads();   // the previous segment's inputs and dv are no longer read
+        stage(t0, n, true);
+        __syncthreads();
+        // the kSeg + 1 row states of the segment, and each token's error
+        float st[kSeg + 1][NC];
+        float err[kSeg];
+        const float* src = ck + static_cast<size_t>(sg) * DV * DK;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) st[0][j] = src[j];
+#pragma unroll
+        for (int i = 0; i < kSeg; ++i) {
+#pragma unroll
+            for (int j = 0; j < NC; ++j) st[i + 1][j] = st[i][j];
+            err[i] = (i < n) ? step(i, st[i + 1]) : 0.f;
+        }
+#pragma unroll
+        for (int i = kSeg - 1; i >= 0; --i) {
+            if (i < n) {   // uniform over the CTA
+                float* red = &sm.red[buf][warp][0];
+                const float dor = sm.dout[i][warp], bt = sm.b[i];
+                float part = 0.f;
+#pragma unroll
+                for (int j = 0; j < NC; ++j) {
+                    D[j] += dor * sm.q[i][c0 + j];
+                    red[c0 + j] = st[i + 1][j] * dor;   // dq_t = S_t^T do_t
+                    part += D[j] * sm.k[i][c0 + j];
+                }
+                const float du = warp_sum(part);
+                const float u = bt * err[i];
+                float dg = 0.f;
+#pragma unroll
+                for (int j = 0; j < NC; ++j) {
+                    const float dec = PC ? sm.a[i][c0 + j] : sm.g[i];
+                    const float sd = st[i][j] * dec;                       // S~_t
+                    red[DK + c0 + j] = D[j] * u - bt * sd * du;            // dk_t
+                    const float dsd = D[j] - bt * du * sm.k[i][c0 + j];    // dS~
+                    const float da = dsd * st[i][j];
+                    if (PC) red[2 * DK + c0 + j] = da;
+                    else dg += da;
+                    D[j] = dsd * dec;
+                }
+                if (!PC) dg = warp_sum(dg);
+                if (lane == 0) {
+                    red[SM::NV * DK] = err[i] * du;   // dbeta_t
+                    red[SM::NV * DK + 1] = dg;
+                    sm.dv[i][warp] = bt * du;
+                }
+                __syncthreads();
+                // sums over the CTA's rows, added to the totals over all rows
+                const size_t t = tok0 + t0 + i;
+                for (int x = tid; x < SM::RED; x += kThreads) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kRows; ++w) acc += sm.red[buf][w][x];
+                    if (x < DK) atomicAdd(p.dq_acc + t * DK + x, acc);
+                    else if (x < 2 * DK) atomicAdd(p.dk_acc + t * DK + x - DK, acc);
+                    else if (PC && x < 3 * DK) atomicAdd(p.dgate + t * DK + x - 2 * DK, acc);
+                    else if (x == SM::NV * DK) atomicAdd(p.dbeta + t, acc);
+                    else if (!PC) atomicAdd(p.dgate + t, acc);
+                }
+                buf ^= 1;   // the next token fills the other buffer while this one is read
+            }
+        }
+        __syncthreads();
+        IO* dvo = static_cast<IO*>(p.dv);
+        for (int x = tid; x < n * kRows; x += kThreads) {
+            const int i = x / kRows, w = x % kRows;
+            st_io(dvo, (tok0 + t0 + i) * DV + rb * kRows + w, sm.dv[i][w]);
+        }
+    }
+    if (p.dstate_in) {
+#pragma unroll
+        for (int j = 0; j < NC; ++j) p.dstate_in[bh * ssz + static_cast<size_t>(r) * DK + c0 + j] = D[j];
+    }
+}
+
+// dq and dk from the fp32 accumulators, in the io dtype.
+template <typename IO>
+__global__ void write_qk_kernel(const float* dq_acc, const float* dk_acc, IO* dq, IO* dk, size_t n) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+        st_io(dq, i, dq_acc[i]);
+        st_io(dk, i, dk_acc[i]);
+    }
+}
+
+template <int DK, int DV, bool PC, typename IO>
+cudaError_t run(const DeltaBwdArgs& p, cudaStream_t s) {
+    auto kern = delta_backward_kernel<DK, DV, PC, IO>;
+    constexpr size_t smem = sizeof(Smem<DK, PC>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<p.BH * (DV / kRows), kThreads, smem, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t n = static_cast<size_t>(p.BH) * p.T * DK;
+    write_qk_kernel<IO><<<p.sm_count * 4, 256, 0, s>>>(p.dq_acc, p.dk_acc, static_cast<IO*>(p.dq),
+                                                        static_cast<IO*>(p.dk), n);
+    return cudaGetLastError();
+}
+
+template <int DK, int DV, bool PC>
+cudaError_t run_io(const DeltaBwdArgs& p, cudaStream_t s) {
+    return p.io == kBf16 ? run<DK, DV, PC, __nv_bfloat16>(p, s) : run<DK, DV, PC, float>(p, s);
+}
+
+template <bool PC>
+cudaError_t run_dims(const DeltaBwdArgs& p, cudaStream_t s) {
+    if (p.dk_dim == 64 && p.dv_dim == 64) return run_io<64, 64, PC>(p, s);
+    if (p.dk_dim == 64 && p.dv_dim == 128) return run_io<64, 128, PC>(p, s);
+    if (p.dk_dim == 128 && p.dv_dim == 64) return run_io<128, 64, PC>(p, s);
+    if (p.dk_dim == 128 && p.dv_dim == 128) return run_io<128, 128, PC>(p, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+size_t delta_backward_bytes(int BH, int T, int dk, int dv) {
+    const size_t nseg = static_cast<size_t>((T + kSeg - 1) / kSeg);
+    return static_cast<size_t>(BH) * (nseg * dv * dk + 2 * static_cast<size_t>(T) * dk) * sizeof(float);
+}
+
+cudaError_t launch_delta_backward(const DeltaBwdArgs& args, cudaStream_t s) {
+    if (!args.workspace) return cudaErrorInvalidValue;
+    DeltaBwdArgs a = args;
+    const size_t nseg = static_cast<size_t>((a.T + kSeg - 1) / kSeg);
+    a.ckpt = a.workspace;
+    a.dq_acc = a.ckpt + static_cast<size_t>(a.BH) * nseg * a.dv_dim * a.dk_dim;
+    a.dk_acc = a.dq_acc + static_cast<size_t>(a.BH) * a.T * a.dk_dim;
+    // the column sums are accumulated: clear their totals first
+    const size_t qk = static_cast<size_t>(a.BH) * a.T * a.dk_dim * sizeof(float);
+    cudaError_t e = cudaMemsetAsync(a.dq_acc, 0, qk, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dk_acc, 0, qk, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(a.dgate, 0, static_cast<size_t>(a.BH) * a.T * (a.per_channel ? a.dk_dim : 1) * sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dbeta, 0, static_cast<size_t>(a.BH) * a.T * sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    return a.per_channel ? run_dims<true>(a, s) : run_dims<false>(a, s);
+}
+
+}  // namespace la

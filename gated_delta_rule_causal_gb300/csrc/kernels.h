@@ -62,6 +62,42 @@ struct BwdArgs {
     unsigned flags = 0;       // LA_FLAG_* (the test hook)
 };
 
+// Gradients of the gated delta rule, scalar (gate [BH][T]) or per-channel
+// (gate [BH][T][dk]) decay; state S [dv][dk] per sequence-head. Pointers are
+// device pointers; dgate, dbeta and the accumulators are overwritten.
+struct DeltaBwdArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* gate;
+    const float* beta;
+    const float* state_in;     // NULL: zero initial state
+    const void* dout;
+    const float* dstate_out;   // NULL: no gradient on the final state
+    void* dq;
+    void* dk;
+    void* dv;
+    float* dgate;
+    float* dbeta;
+    float* dstate_in;          // NULL: not wanted
+    int BH, T, dk_dim, dv_dim;
+    int io;                    // Io
+    bool per_channel;
+    int sm_count;
+    float* workspace;          // delta_backward_bytes(BH, T, dk, dv) bytes
+    // carved from the workspace by the launch: rows at every segment start,
+    // fp32 totals of dq and dk
+    float* ckpt;
+    float* dq_acc;
+    float* dk_acc;
+};
+
+// Workspace bytes launch_delta_backward needs (checkpoints + accumulators).
+size_t delta_backward_bytes(int BH, int T, int dk, int dv);
+// Token-serial CUDA-core kernel, rows split over CTAs (see backward_delta.cu);
+// d_k, d_v in {64, 128}.
+cudaError_t launch_delta_backward(const DeltaBwdArgs& a, cudaStream_t s);
+
 // One CTA per sequence-head on CUDA cores; d_k, d_v in {16, 32, 64}.
 cudaError_t launch_norm_backward(const BwdArgs& a, cudaStream_t s);
 

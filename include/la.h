@@ -291,6 +291,37 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
                 void* dq, void* dk, void* dv, float* dstate_in,
                 int variant, int T, void* cuda_stream);
 
+/*
+ * Backward of the prefill of the gated delta rule (LA_GDN) and of its
+ * per-channel-decay form (LA_KDA); d_k, d_v in {64, 128}; bf16 or fp32 io.
+ * Given the forward call's q, k, v, gate, beta and state_in (same layouts as
+ * la_forward: gate [B,H,T] for LA_GDN, [B,H,T,d_k] for LA_KDA; beta
+ * [B,H,T]; state_in [B,H,d_v*d_k] fp32 or NULL for zero), the gradient of
+ * its outputs (dout [B,H,T,d_v], io dtype) and optionally of its final state
+ * (dstate_out, fp32, same layout as the state; NULL means zero), writes dq,
+ * dk [B,H,T,d_k] and dv [B,H,T,d_v] (io dtype), dgate (fp32, the gate's
+ * shape), dbeta [B,H,T] (fp32) and, if dstate_in is not NULL, the gradient
+ * of the initial state (fp32). The pages give the forward operator only; the
+ * gradients follow from the chain rule through the decay-first delta rule
+ * (S~ = S Diag(a), u = beta (v - S~ k), S = S~ + u k^T, o = S q).
+ * Token-serial CUDA-core kernel: the state's value rows are split over CTAs
+ * of 16 rows, run forward with checkpoints every 16 tokens, then walked back
+ * segment by segment; sums over rows are accumulated in fp32 (the order of
+ * those additions varies from run to run, so the last bits of dq, dk, dgate
+ * and dbeta may too). Its workspace (4 * B*H * (ceil(T/16) * d_v*d_k +
+ * 2*T*d_k) bytes) is allocated by the handle on first use and grown when a
+ * call needs more (la_destroy frees it). la_last_launches reports 2 (plus
+ * memsets of the accumulated outputs, not counted).
+ * Errors: LA_ERR_UNSUPPORTED for another variant or head size,
+ * LA_ERR_INVALID_ARG (T < 1, a required pointer NULL), LA_ERR_MISALIGNED,
+ * LA_ERR_CUDA.
+ */
+int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
+                      const float* gate, const float* beta, const float* state_in,
+                      const void* dout, const float* dstate_out,
+                      void* dq, void* dk, void* dv, float* dgate, float* dbeta, float* dstate_in,
+                      int variant, int T, void* cuda_stream);
+
 /* Number of CUDA kernels the last successful la_forward / la_decode_step /
  * la_backward on h enqueued (0 after a failed or a T = 0 call, or for a NULL
  * handle). A diagnostic: which algorithm the library picked shows in this

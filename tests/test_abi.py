@@ -44,6 +44,8 @@ def test_null_handle_is_rejected(lib):
     assert la.la_status(None, None) == la.LA_ERR_INVALID_ARG
     assert la.lib().la_backward(None, None, None, None, None, None, None, None, None, None, None, 0, 8,
                                 None) == la.LA_ERR_INVALID_ARG
+    assert la.lib().la_backward_gated(None, None, None, None, None, None, None, None, None, None, None, None,
+                                      None, None, None, 2, 8, None) == la.LA_ERR_INVALID_ARG
     la.la_destroy(None)                     # allowed
     assert la.la_last_error(None) == "null handle"
     assert la.la_last_launches(None) == 0

@@ -1,0 +1,86 @@
+"""Gradients of the gated delta rule prefill (la_backward_gated, scalar gate
+and per-channel decay) against the float64 oracle's (oracle/backward.py,
+``delta_backward``, itself pinned by finite differences of the forward
+oracle), on the same seeded inputs."""
+import numpy as np
+import pytest
+
+import workloads as W
+from _helpers import TOL, oracle_inputs, slice_rel_err, to_torch
+
+pytestmark = pytest.mark.gpu
+
+la = pytest.importorskip("gated_delta_rule_causal_gb300")
+
+
+def _workload(variant, B, H, T, d, io):
+    base = {"gdn": W.GDN_B2H16_T8192_D128,
+            "kda": W.KDA_DECODE_N256H16_D128.with_(B=4, H=16, T=2048, decode_steps=0, state_std=0.0)}[variant]
+    return W.small(base, B=B, H=H, T=T, dk=d, dv=d).with_(io=io)
+
+
+def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True):
+    import torch
+    from oracle import backward
+    w = _workload(variant, B, H, T, d, io)
+    inp = W.draw(w, seed)
+    q, k, v, g, b = oracle_inputs(inp)
+    rng = np.random.default_rng(seed + 1000)
+    ss = d * d
+    do_s = W.round_io(rng.standard_normal((B, H, T, d)), io)
+    do64 = W.as_f64(do_s)
+    sin = (rng.standard_normal((B, H, ss)) * 0.1).astype(np.float32) if with_state else None
+    dso = (rng.standard_normal((B, H, ss)) * 0.05).astype(np.float32) if with_dstate else None
+    h = la.Handle(B, H, d, d, io=io)
+    dev = h.device
+    t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    got = h.backward_gated(to_torch(inp.q, dev), to_torch(inp.k, dev), to_torch(inp.v, dev),
+                           to_torch(inp.gate, dev), to_torch(inp.beta, dev), to_torch(do_s, dev), t(sin), t(dso),
+                           variant=variant)
+    torch.cuda.synchronize()
+    assert h.last_launches() == 2
+    assert h.status() == la.LA_OK
+    h.close()
+    ref = backward.delta_backward(q, k, v, g, b, do64, sin, dso)
+    return [x.float().cpu().numpy() for x in got], ref
+
+
+NAMES = ("dq", "dk", "dv", "dgate", "dbeta", "dstate_in")
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("io", ["bf16", "fp32"])
+@pytest.mark.parametrize("T", [1, 37, 200])
+def test_backward_gated_parity(variant, d, io, T):
+    got, ref = _case(variant, 1, 2, T, d, io, seed=T + d + (7 if variant == "kda" else 0))
+    for name, x, r in zip(NAMES, got, ref):
+        assert x.shape == r.shape, name
+        assert np.all(np.isfinite(x)), name
+        assert slice_rel_err(x, r) <= TOL[io], (name, slice_rel_err(x, r))
+
+
+@pytest.mark.parametrize("with_state,with_dstate", [(False, False), (True, False), (False, True)])
+def test_backward_gated_optional_states(with_state, with_dstate):
+    got, ref = _case("gdn", 2, 3, 65, 64, "bf16", seed=5, with_state=with_state, with_dstate=with_dstate)
+    for name, x, r in zip(NAMES, got, ref):
+        assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def test_backward_gated_long_sequence(variant):
+    # 2048 tokens: 128 segments walked back through their checkpoints
+    got, ref = _case(variant, 1, 2, 2048, 64, "bf16", seed=17)
+    for name, x, r in zip(NAMES, got, ref):
+        assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
+
+
+def test_backward_gated_rejects_what_it_cannot_run():
+    import torch
+    h = la.Handle(1, 1, 32, 32)
+    z = torch.zeros((1, 1, 4, 32), dtype=torch.bfloat16, device=h.device)
+    g = torch.ones((1, 1, 4), device=h.device)
+    with pytest.raises(la.LAError) as e:
+        h.backward_gated(z, z, z, g, g, z)
+    assert e.value.code == la.LA_ERR_UNSUPPORTED
+    h.close()
