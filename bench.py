@@ -38,6 +38,7 @@ HEADLINE = W.GDN_B2H16_T8192_D128
 SUITE = (W.NORM_B4H8_T2048_D64, W.GLA_B4H16_T4096_D128, W.GDN_DECODE_N256H16_D128, W.NORM_DECAY_B4H8_T2048_D64,
          W.KDA_B2H16_T8192_D128, W.KDA_DECODE_N256H16_D128)
 BACKWARD = W.NORM_B4H8_T2048_D64   # the backward is timed on the normalized workload's shapes
+GATED_BACKWARD = W.GDN_B2H16_T8192_D128   # and the gated delta rule's on the headline's
 C_FLOPS = 64   # chunk size the algorithmic FLOP count is quoted at
 
 
@@ -69,6 +70,13 @@ def prefill_bytes(w: W.Workload) -> int:
 def backward_bytes(w: W.Workload) -> int:
     """la_backward: q, k, v and the outputs' gradient read; dq, dk, dv written."""
     return w.B * w.H * w.T * (4 * w.dk + 3 * w.dv) * io_bytes(w)
+
+
+def gated_backward_bytes(w: W.Workload) -> int:
+    """la_backward_gated: q, k, v, the outputs' gradient, gate and beta read;
+    dq, dk, dv, dgate and dbeta written."""
+    gate = w.dk if w.variant == "kda" else 1
+    return w.B * w.H * w.T * ((4 * w.dk + 3 * w.dv) * io_bytes(w) + 2 * (gate + 1) * 4)
 
 
 def prefill_flops(w: W.Workload) -> float:
@@ -185,7 +193,22 @@ def host_cores() -> int:
 
 
 def kernel_source_hash() -> str:
-    """sha1 (12 hex) of the CUDA sources and the C header."""
+    """sha1 (12 hex) of the CUDA sources of the forward and decode paths
+    (every file in csrc/ but the backward kernels, which none of the traffic
+    keys covers) and the C header."""
+    import glob
+    import hashlib
+    h = hashlib.sha1()
+    files = sorted(f for f in glob.glob(os.path.join(ROOT, "gated_delta_rule_causal_gb300", "csrc", "*"))
+                   if not os.path.basename(f).startswith("backward"))
+    for f in files + [os.path.join(ROOT, "include", "la.h")]:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+def all_source_hash() -> str:
+    """sha1 (12 hex) of every CUDA source and the C header."""
     import glob
     import hashlib
     h = hashlib.sha1()
@@ -198,13 +221,17 @@ def kernel_source_hash() -> str:
 
 def traffic_from_profiles(key: str):
     """DRAM bytes (read + write) per unit from the committed ncu capture, or
-    None when the kernels changed since the counters were taken."""
+    None when the kernels changed since the counters were taken (forward and
+    decode keys: their sources; "backward/" keys: every source)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("source_hash") != kernel_source_hash():
+    if key.startswith("backward/"):
+        if d.get("all_source_hash") != all_source_hash():
+            return None
+    elif d.get("source_hash") != kernel_source_hash():
         return None
     return d.get(key)
 
@@ -244,6 +271,30 @@ class PrefillRunner:
     @property
     def launches_per_step(self):
         return self.h.last_launches()   # kernels the library enqueued for one forward
+
+
+class GatedBackwardRunner:
+    """The gated delta rule's inputs and an output gradient (two rotating
+    device copies, each larger than L2); one la_backward_gated per step."""
+
+    def __init__(self, w: W.Workload, seed: int, torch, la):
+        self.w, self.torch = w, torch
+        self.h = la.Handle(w.B, w.H, w.dk, w.dv, io=w.io)
+        x = W.draw(w, seed)
+        do = W.round_io(np.random.default_rng(seed + 1).standard_normal((w.B, w.H, w.T, w.dv)), w.io)
+        dev = self.h.device
+        base = [PrefillRunner._dev(a, dev) for a in (x.q, x.k, x.v, x.gate, x.beta, do)]
+        self.sets = [base, [t.clone() for t in base]]
+        self.i = 0
+
+    def step(self):
+        q, k, v, g, b, do = self.sets[self.i % 2]
+        self.i += 1
+        self.h.backward_gated(q, k, v, g, b, do, variant=self.w.variant, return_dstate=False)
+
+    @property
+    def launches_per_step(self):
+        return self.h.last_launches()
 
 
 class BackwardRunner:
@@ -505,12 +556,33 @@ def gpu_arm(args):
                       "value": round(BACKWARD.tokens * args.steps / (tot * 1e-3), 1), "unit": "tokens/s",
                       "ms_per_step": round(tot / args.steps, 4),
                       "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                   "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": None, "algorithmic_bytes": byts,
+                                   "frac": round(gbs / pk["hbm_gbs"], 4),
+                                   "traffic": traffic_from_profiles("backward/norm"), "algorithmic_bytes": byts,
                                    "kernel_ms": round(kms, 4),
                                    "peak_source": pk["source"] + " (burst copy bandwidth)",
                                    "note": "chunkwise tcgen05 chain (five launches per head group)"},
                       "gpu_launches": args.steps * br.launches_per_step})
         del br
+        torch.cuda.empty_cache()
+        # the gated delta rule's backward on the headline's shapes (token-serial)
+        gs = max(3, args.steps // 4)
+        gr = GatedBackwardRunner(GATED_BACKWARD, 0, torch, la)
+        tot, per = time_steps(gr, gs, args.warmup, torch)
+        kms = statistics.mean(per)
+        byts = gated_backward_bytes(GATED_BACKWARD)
+        gbs = byts / (kms * 1e-3) / 1e9
+        suite.append({"workload": "gdn_backward_" + GATED_BACKWARD.name.split("_", 1)[1],
+                      "metric": "backward tokens/s (B*T)",
+                      "value": round(GATED_BACKWARD.tokens * gs / (tot * 1e-3), 1), "unit": "tokens/s",
+                      "ms_per_step": round(tot / gs, 4), "steps": gs,
+                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                   "frac": round(gbs / pk["hbm_gbs"], 4),
+                                   "traffic": traffic_from_profiles("backward/gdn"), "algorithmic_bytes": byts,
+                                   "kernel_ms": round(kms, 4),
+                                   "peak_source": pk["source"] + " (burst copy bandwidth)",
+                                   "note": "token-serial CUDA-core kernel (rows split over CTAs): latency-bound"},
+                      "gpu_launches": gs * gr.launches_per_step})
+        del gr
         torch.cuda.empty_cache()
         line["suite"] = suite
     line["wall_s"] = round(time.perf_counter() - t_wall0, 2)
@@ -526,16 +598,22 @@ def kernel_only(args):
     import torch
     import gated_delta_rule_causal_gb300 as la
     la.build()
-    w = BACKWARD if args.backward else W.BY_NAME[args.workload] if args.workload else HEADLINE
+    w = (BACKWARD if args.backward else GATED_BACKWARD if args.gated_backward
+         else W.BY_NAME[args.workload] if args.workload else HEADLINE)
+    if args.gated_backward and args.workload:
+        w = W.BY_NAME[args.workload]   # a smaller gated workload, for ncu captures
     props = torch.cuda.get_device_properties(0)
     if args.backward:
         r = BackwardRunner(w, 0, int(getattr(props, "L2_cache_size", 126 * 2 ** 20)), torch, la)
+    elif args.gated_backward:
+        r = GatedBackwardRunner(w, 0, torch, la)
     elif w.decode_steps:
         r = DecodeRunner(w.with_(decode_steps=8), 0, torch, la)
     else:
         r = PrefillRunner(w, 0, int(getattr(props, "L2_cache_size", 126 * 2 ** 20)), torch, la)
     total_ms, per = time_steps(r, args.steps, args.warmup, torch)
-    print(json.dumps({"workload": ("backward/" if args.backward else "") + w.name, "steps": args.steps, "ms_per_step": round(total_ms / args.steps, 5),
+    print(json.dumps({"workload": ("backward/" if args.backward or args.gated_backward else "") + w.name,
+                      "steps": args.steps, "ms_per_step": round(total_ms / args.steps, 5),
                       "kernel_ms": [round(x, 5) for x in per]}), flush=True)
 
 
@@ -617,6 +695,8 @@ def main():
                     help="run warmup + steps of the workload's kernel and nothing else (for ncu)")
     ap.add_argument("--backward", action="store_true",
                     help="with --only-kernel: the normalized backward on its workload's shapes")
+    ap.add_argument("--gated-backward", action="store_true",
+                    help="with --only-kernel: the gated delta rule's backward (headline shapes, or --workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
