@@ -131,13 +131,16 @@ struct ChainLayout {
     using S = Slot<DK, DV>;
     static constexpr uint32_t STAGE = S::TILES;                 // the slot's tiles, per stage
     static constexpr uint32_t OFF_VEC = 2 * STAGE;              // the slot's vector, per stage (512 B)
-    static constexpr uint32_t OFF_SS = OFF_VEC + 1024;          // X_0 bf16 [128 rows][DK]
-    static constexpr uint32_t OFF_OT = OFF_SS + KA * 16384;     // output tile bf16 [64 t][DV] for the TMA store
+    static constexpr uint32_t OFF_OT = OFF_VEC + 1024;          // output tile bf16 [64 t][DV] for the TMA store
     static constexpr uint32_t OFF_BAR = OFF_OT + DV * 128;
     static constexpr uint32_t BYTES = OFF_BAR + 256;
     // TMEM columns (lanes = value rows); buffer b = chunk & 1
     static constexpr uint32_t COL_S = 0;        // Ut^T K' - X_0 N_c   [dv][DK], two buffers 128 apart
     static constexpr uint32_t COL_O = 256;      // Ut^T P^T + X_0 E_c  [dv][64], two buffers 64 apart
+    // X_c as the bf16 A operand of the state product [dv rows][DK / 2
+    // columns], after buffer 0's S and O
+    static constexpr uint32_t COL_A = DK + 64;
+    static_assert(COL_A + DK / 2 <= 256, "the A operand fits before buffer 1");
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -281,8 +284,9 @@ __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
 // Per chunk c (buffer b = c & 1 of tensor memory, stage b of shared memory):
 //   pre(c):   S_b = Ut^T K',  O_b = Ut^T P^T          (no state: issued early)
 //   state(c): [S_b | O_b] += X_c [-N_c | E_c]           (one MMA chain, N = DK + 64)
-//   converters: X_{c+1} = X_c Diag(Gam_C) + S_b (fp32 registers), republished
-//               as the bf16 operand; o = O_b through the output tile.
+//   converters: X_{c+1} = X_c Diag(Gam_C) + S_b (fp32 registers), stored as
+//               the bf16 A operand in tensor memory (no shared-memory copy, no
+//               async-proxy fence); o = O_b through the output tile.
 // Only state(c) and the state update lie on the path from one chunk to the
 // next.
 // GLA: the per-channel gated variant without the delta rule. N_c = 0, so the
@@ -316,7 +320,6 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
     uint64_t* bar_test = bar + 10;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 11);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 12);
-    const uint32_t aSS = sbase + L::OFF_SS;
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
@@ -391,10 +394,10 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
 #pragma unroll
                 for (int kk = 0; kk < DK / 16; ++kk) {
                     if (GLA)
-                        mma_bf16_ss(tmem + col_s(b) + DK, kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
+                        mma_bf16_ts(tmem + col_s(b) + DK, tmem + L::COL_A + 8 * kk,
                                     mnmaj(stg + S::E_OFF + kk * 2048, 8192), ID_E, true);
                     else
-                        mma_bf16_ss(tmem + col_s(b), kmaj(aSS + (kk / 4) * 16384 + (kk % 4) * 32),
+                        mma_bf16_ts(tmem + col_s(b), tmem + L::COL_A + 8 * kk,
                                     mnmaj(stg + S::NC_OFF + kk * 2048, DK * 128), ID_X, true);
                 }
                 mma_commit(bar_s);
@@ -544,14 +547,29 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
             st[i + 2] = x.z;
             st[i + 3] = x.w;
         }
-        // Every row of the bf16 operand is written (rows >= d_v as zeros) so
-        // that padded MMA rows never see stale bits.
+        // The bf16 state as the A operand in tensor memory: thread (r, hh)
+        // writes its DK/2 values of row r as DK/4 packed columns of lane r.
+        // Rows >= d_v are written once, as zeros, before the first chunk (their
+        // warps own no row after that).
         auto publish_state = [&]() {
+            if constexpr (DKH == 64) {
+                uint32_t u[32];
 #pragma unroll
-            for (int b = 0; b < DKH / 32; ++b) {
-                const int cb = hh * DKH + 32 * b;
-                store_row32_bf16(aSS + (cb / 64) * 16384, r, (cb % 64) / 8, st + 32 * b);
+                for (int i = 0; i < 32; ++i) u[i] = pack_bf16(st[2 * i], st[2 * i + 1]);
+                tmem_st32(tlane + L::COL_A + hh * 32, u);
+            } else {
+                static_assert(DKH == 32, "d_k in {64, 128}");
+                uint32_t u[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) u[i] = pack_bf16(st[2 * i], st[2 * i + 1]);
+                tmem_st16(tlane + L::COL_A + hh * 16, u);
             }
+            tmem_st_wait();
+        };
+        auto signal_x = [&]() {   // this warp's part of X is in tensor memory
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_x);
         };
         auto signal = [&](uint64_t* b) {   // this warp's writes / TMEM reads are done
             fence_proxy_async_smem();
@@ -560,7 +578,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
             if (lane == 0) mbar_arrive(b);
         };
         publish_state();
-        signal(bar_x);
+        signal_x();
 
         bool bad = failed;
         for (int it = 0; it < n && !bad; ++it) {
@@ -585,7 +603,7 @@ __device__ __forceinline__ void chain_role(const CUtensorMap* tmo, const Params&
                 }
                 publish_state();
             }
-            signal(bar_x);
+            signal_x();
             bad |= !ok;
             // ---- output: o_t = O_b[:, t], through the output tile ----------------
             ok = ok && (it == 0 || mbar_wait_or_abort(bar_ofree, (it - 1) & 1, abort_flag));
