@@ -1,6 +1,6 @@
 """Float64 gradients of the normalized elu+1 recurrence (with and without a
-fixed decay) and of the gated delta rule (scalar or per-channel decay), as
-test infrastructure.
+fixed decay), of the per-channel gated recurrence and of the gated delta rule
+(scalar or per-channel decay), as test infrastructure.
 
 TEST INFRASTRUCTURE, like the rest of ``oracle``: only ``tests/`` and
 ``bench.py``'s CPU legs use it.
@@ -25,7 +25,7 @@ by token, in plain float64:
 differences of the C forward oracle (``oracle.run``), which shares no
 arithmetic with this module; ``tests/test_backward_mutations.py`` plants
 mistakes in copies of each function and checks that those pins catch them.
-``delta_backward`` states its own chain rule.
+``gla_backward`` and ``delta_backward`` state their own chain rules.
 """
 from __future__ import annotations
 
@@ -274,3 +274,51 @@ def delta_backward(q, k, v, decay, beta, do, state_in=None, dstate_out=None):
         D = dst * av[:, :, t, None, :]
     dgate = da if per_channel else da.sum(axis=-1)
     return dq, dkk, dvv, dgate, db, D.reshape(B, H, dv * dk)
+
+
+def gla_backward(q, k, v, gamma, do, state_in=None, dstate_out=None, identity_phi=False):
+    """Gradients of the per-channel gated recurrence (GLA / RetNet family,
+    "Linear attention and Hyena" §11.3), S in R^{dk x dv}:
+
+        S_t = diag(gamma_t) S_{t-1} + f_t v_t^T,   o_t = S_t^T p_t,
+        f = phi(k), p = phi(q) (the identity under identity_phi)
+
+    The pages give no gradients. By the chain rule, with D the whole gradient
+    reaching S_t (the final-state cotangent, then carried back):
+
+        D += p_t do_t^T,          dp_t = S_t do_t
+        df_t = D v_t,             dv_t = D^T f_t
+        dgamma_t = rowsums of D o S_{t-1}  (one per key channel)
+        D <- diag(gamma_t) D;     dstate_in = D after token 0
+        dq = dp o phi'(q), dk = df o phi'(k)
+
+    q, k [B,H,T,dk]; v, do [B,H,T,dv]; gamma [B,H,T,dk]; state_in,
+    dstate_out [B,H,dk*dv] (S row-major) or None. Returns (dq, dk, dv,
+    dgamma, dstate_in) in float64.
+    """
+    q, k, v, do = (np.asarray(a, np.float64) for a in (q, k, v, do))
+    gm = np.asarray(gamma, np.float64)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    if identity_phi:
+        f, p = k, q
+        dfk, dpq = np.ones_like(k), np.ones_like(q)
+    else:
+        f, p = _phi(k), _phi(q)
+        dfk, dpq = _dphi(k), _dphi(q)
+    sin = np.zeros((B, H, dk, dv)) if state_in is None else np.asarray(state_in, np.float64).reshape(B, H, dk, dv)
+    S = np.empty((B, H, T + 1, dk, dv))   # S[:, :, t + 1] is the state after token t
+    S[:, :, 0] = sin
+    for t in range(T):
+        S[:, :, t + 1] = gm[:, :, t, :, None] * S[:, :, t] + f[:, :, t, :, None] * v[:, :, t, None, :]
+    D = np.zeros((B, H, dk, dv)) if dstate_out is None else np.asarray(dstate_out, np.float64).reshape(B, H, dk, dv).copy()
+    dq, dkk, dvv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    dg = np.empty((B, H, T, dk))
+    for t in range(T - 1, -1, -1):
+        D = D + p[:, :, t, :, None] * do[:, :, t, None, :]
+        dq[:, :, t] = np.einsum("bhkv,bhv->bhk", S[:, :, t + 1], do[:, :, t]) * dpq[:, :, t]
+        dkk[:, :, t] = np.einsum("bhkv,bhv->bhk", D, v[:, :, t]) * dfk[:, :, t]
+        dvv[:, :, t] = np.einsum("bhkv,bhk->bhv", D, f[:, :, t])
+        dg[:, :, t] = np.einsum("bhkv,bhkv->bhk", D, S[:, :, t])
+        D = gm[:, :, t, :, None] * D
+    return dq, dkk, dvv, dg, D.reshape(B, H, dk * dv)

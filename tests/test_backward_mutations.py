@@ -56,6 +56,23 @@ MUTANTS_DELTA = {
 }
 
 
+# planted in gla_backward (per-channel gated attention)
+MUTANTS_GLA = {
+    "gate_gradient_against_new_state": ('dg[:, :, t] = np.einsum("bhkv,bhkv->bhk", D, S[:, :, t])',
+                                        'dg[:, :, t] = np.einsum("bhkv,bhkv->bhk", D, S[:, :, t + 1])'),
+    "state_gradient_not_decayed": ("D = gm[:, :, t, :, None] * D", "D = D"),
+    "dq_from_previous_state": ('dq[:, :, t] = np.einsum("bhkv,bhv->bhk", S[:, :, t + 1], do[:, :, t])',
+                               'dq[:, :, t] = np.einsum("bhkv,bhv->bhk", S[:, :, t], do[:, :, t])'),
+    "dv_with_query_features": ('dvv[:, :, t] = np.einsum("bhkv,bhk->bhv", D, f[:, :, t])',
+                               'dvv[:, :, t] = np.einsum("bhkv,bhk->bhv", D, p[:, :, t])'),
+    "dk_without_feature_map_derivative": ("v[:, :, t]) * dfk[:, :, t]", "v[:, :, t])"),
+    "output_cotangent_with_key_features": ("D = D + p[:, :, t, :, None] * do[:, :, t, None, :]",
+                                           "D = D + f[:, :, t, :, None] * do[:, :, t, None, :]"),
+    "drops_final_state_cotangent": ("D = np.zeros((B, H, dk, dv)) if dstate_out is None else np.asarray(dstate_out, np.float64).reshape(B, H, dk, dv).copy()",
+                                    "D = np.zeros((B, H, dk, dv))"),
+}
+
+
 def _split(text):
     """(head, norm_backward, norm_decay_backward) sources."""
     a = text.index("def norm_backward(")
@@ -230,3 +247,54 @@ def test_delta_mutant_is_caught(name, delta_cases):
     mod = _load(head + body.replace(old, new))
     # caught when it disagrees with the finite differences on either decay
     assert not all(_agrees_delta(mod, c) for c in delta_cases.values()), name
+
+
+@pytest.fixture(scope="module")
+def gla_case():
+    g = np.random.default_rng(127)
+    B, H, T, dk, dv = 1, 1, 5, 3, 2
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    gm = g.uniform(0.4, 1.0, (B, H, T, dk))
+    sin = g.standard_normal((B, H, dk * dv)) * 0.3
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, dk * dv))
+
+    def loss():
+        r = oracle.run("gla", q, k, v, gm, None, sin)
+        return float(np.sum(r.o * W) + np.sum(r.state * Ws))
+
+    eps = 1e-6
+    fd = []
+    for arr in (q, k, v, gm, sin):
+        grad = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = loss()
+            arr[idx] = a0 - eps
+            lm = loss()
+            arr[idx] = a0
+            grad[idx] = (lp - lm) / (2 * eps)
+        fd.append(grad)
+    return (q, k, v, gm, W, sin, Ws), fd
+
+
+def _agrees_gla(mod, case):
+    (q, k, v, gm, W, sin, Ws), fd = case
+    got = mod.gla_backward(q, k, v, gm, W, sin, Ws)
+    return all(np.allclose(gr, f, rtol=1e-6, atol=1e-6) for gr, f in zip(got, fd))
+
+
+def test_unmutated_gla_backward_agrees(gla_case):
+    with open(SRC) as fh:
+        assert _agrees_gla(_load(fh.read()), gla_case)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS_GLA))
+def test_gla_mutant_is_caught(name, gla_case):
+    old, new = MUTANTS_GLA[name]
+    with open(SRC) as fh:
+        text = fh.read()
+    i = text.index("def gla_backward(")
+    head, body = text[:i], text[i:]
+    assert body.count(old) == 1, name
+    assert not _agrees_gla(_load(head + body.replace(old, new)), gla_case), name

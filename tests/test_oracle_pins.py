@@ -688,3 +688,60 @@ def test_delta_backward_uniform_channels_is_scalar_gate():
     for i in (0, 1, 2, 4, 5):
         assert np.allclose(s[i], c[i], rtol=1e-12, atol=1e-12)
     assert np.allclose(s[3], c[3].sum(-1), rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- gradients of (b)
+
+@pytest.mark.parametrize("identity_phi", [False, True])
+def test_gla_backward_matches_finite_differences(identity_phi):
+    # Every gradient of the float64 backward (q, k, v, the per-channel gate,
+    # the initial state) against central differences of the C forward
+    # recurrence, entry by entry, with cotangents on the outputs and the
+    # final state.
+    from oracle import backward
+    g = rng(109 + identity_phi)
+    B, H, T, dk, dv = 1, 2, 6, 3, 2
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    gm = g.uniform(0.4, 1.0, (B, H, T, dk))
+    sin = g.standard_normal((B, H, dk * dv)) * 0.3
+    W, Ws = g.standard_normal((B, H, T, dv)), g.standard_normal((B, H, dk * dv))
+
+    def loss():
+        r = oracle.run("gla", q, k, v, gm, None, sin, identity_phi=identity_phi)
+        return float(np.sum(r.o * W) + np.sum(r.state * Ws))
+
+    grads = backward.gla_backward(q, k, v, gm, W, sin, Ws, identity_phi=identity_phi)
+    eps = 1e-6
+    for name, arr, grad in zip(("q", "k", "v", "gamma", "s"), (q, k, v, gm, sin), grads):
+        assert grad.shape == arr.shape, name
+        for idx in np.ndindex(arr.shape):
+            a0 = arr[idx]
+            arr[idx] = a0 + eps
+            lp = loss()
+            arr[idx] = a0 - eps
+            lm = loss()
+            arr[idx] = a0
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, grad[idx])
+
+
+def test_gla_backward_state_only_closed_form():
+    # Gate 1 and a cotangent on the final state alone: the gradient reaching
+    # every token is dS_T, so dv_t = dS_T^T phi(k_t), dk_t = (dS_T v_t) o
+    # phi'(k_t), dq = 0, dgamma_t = rowsums(dS_T o S_{t-1}), dstate_in = dS_T.
+    from oracle import backward
+    g = rng(113)
+    B, H, T, dk, dv = 2, 1, 5, 4, 3
+    q, k, v = g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dk)), g.standard_normal((B, H, T, dv))
+    S0 = g.standard_normal((B, H, dk, dv))
+    dS = g.standard_normal((B, H, dk, dv))
+    dq, dk_, dv_, dg, dsin = backward.gla_backward(q, k, v, np.ones((B, H, T, dk)), np.zeros((B, H, T, dv)),
+                                                   S0.reshape(B, H, -1), dS.reshape(B, H, -1))
+    phi = np.where(k > 0, k + 1, np.exp(np.minimum(k, 0)))
+    dphi = np.where(k > 0, 1.0, np.exp(np.minimum(k, 0)))
+    prev = S0[:, :, None] + np.cumsum(phi[..., :, None] * v[..., None, :], axis=2) - phi[..., :, None] * v[..., None, :]
+    assert np.allclose(dq, 0.0)
+    assert np.allclose(dv_, np.einsum("bhkv,bhtk->bhtv", dS, phi), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dk_, np.einsum("bhkv,bhtv->bhtk", dS, v) * dphi, rtol=1e-12, atol=1e-12)
+    assert np.allclose(dg, np.einsum("bhkv,bhtkv->bhtk", dS, prev), rtol=1e-11, atol=1e-11)
+    assert np.allclose(dsin.reshape(B, H, dk, dv), dS)
