@@ -323,8 +323,9 @@ class Handle:
     def backward_gated(self, q, k, v, gate, beta, dout, state_in=None, dstate_out=None, *, variant="gdn",
                        return_dstate=True, stream=None):
         """Gradients of a gated delta rule prefill (variant "gdn": gate
-        [B,H,T]; "kda": gate [B,H,T,d_k]); beta [B,H,T]. Returns (dq, dk, dv,
-        dgate, dbeta, dstate_in)."""
+        [B,H,T]; "kda": gate [B,H,T,d_k]; beta [B,H,T]) or of a per-channel
+        gated one ("gla": gate [B,H,T,d_k], beta None). Returns (dq, dk, dv,
+        dgate, dbeta, dstate_in); dbeta is None for "gla"."""
         import torch
         var = VARIANTS[variant]
         B, H, T = q.shape[0], q.shape[1], q.shape[2]
@@ -332,14 +333,17 @@ class Handle:
             raise ValueError("q batch/heads differ from the handle's")
         for name, t, d in (("q", q, self.d_k), ("k", k, self.d_k), ("v", v, self.d_v), ("dout", dout, self.d_v)):
             self._expect(name, t, (B, H, T, d), self.dtype)
-        gshape = (B, H, T, self.d_k) if variant == "kda" else (B, H, T)
+        gshape = (B, H, T, self.d_k) if variant in ("kda", "gla") else (B, H, T)
         self._expect("gate", gate, gshape, torch.float32)
+        if variant == "gla":
+            beta = None
         self._expect("beta", beta, (B, H, T), torch.float32)
         ss = state_size(variant, self.d_k, self.d_v)
         self._expect("state_in", state_in, (B, H, ss), torch.float32)
         self._expect("dstate_out", dstate_out, (B, H, ss), torch.float32)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        dgate, dbeta = torch.empty_like(gate), torch.empty_like(beta)
+        dgate = torch.empty_like(gate)
+        dbeta = None if beta is None else torch.empty_like(beta)
         dstate_in = torch.empty((B, H, ss), dtype=torch.float32, device=self.device) if return_dstate else None
         rc = lib().la_backward_gated(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(beta), _ptr(state_in),
                                      _ptr(dout), _ptr(dstate_out), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgate),

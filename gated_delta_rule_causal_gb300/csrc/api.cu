@@ -623,11 +623,13 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
     if (!h) return LA_ERR_INVALID_ARG;
     h->last_error.clear();
     h->last_launches = 0;
-    if (variant != LA_GDN && variant != LA_KDA)
-        return fail(h, LA_ERR_UNSUPPORTED, "la_backward_gated supports LA_GDN and LA_KDA");
+    if (variant != LA_GDN && variant != LA_KDA && variant != LA_GLA)
+        return fail(h, LA_ERR_UNSUPPORTED, "la_backward_gated supports LA_GDN, LA_KDA and LA_GLA");
     if (T < 1) return fail(h, LA_ERR_INVALID_ARG, "T must be >= 1");
-    if (!q || !k || !v || !gate || !beta || !dout || !dq || !dk || !dv || !dgate || !dbeta)
-        return fail(h, LA_ERR_INVALID_ARG, "q, k, v, gate, beta, dout, dq, dk, dv, dgate and dbeta are required");
+    const bool gla = variant == LA_GLA;
+    if (!q || !k || !v || !gate || !dout || !dq || !dk || !dv || !dgate)
+        return fail(h, LA_ERR_INVALID_ARG, "q, k, v, gate, dout, dq, dk, dv and dgate are required");
+    if (!gla && (!beta || !dbeta)) return fail(h, LA_ERR_INVALID_ARG, "beta and dbeta are required");
     const la_config& c = h->cfg;
     if (!((c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128)))
         return fail(h, LA_ERR_UNSUPPORTED, "la_backward_gated supports d_k, d_v in {64, 128}");
@@ -642,7 +644,7 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
     DeviceGuard g(c.device);
     if (!g.ok) return fail(h, LA_ERR_CUDA, "cannot select the handle's device");
     const int BH = c.B * c.H;
-    const size_t need = la::delta_backward_bytes(BH, T, c.d_k, c.d_v);
+    const size_t need = la::delta_backward_bytes(BH, T, c.d_k, c.d_v, gla);
     if (need > h->bws_bytes) {
         if (h->d_bws) {
             cudaFree(h->d_bws);   // waits for the work that used it
@@ -673,7 +675,14 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
     a.dk_dim = c.d_k;
     a.dv_dim = c.d_v;
     a.io = c.io == LA_FP32 ? la::kFp32 : la::kBf16;
-    a.per_channel = variant == LA_KDA;
+    a.per_channel = variant != LA_GDN;
+    a.gla = gla;
+    a.identity_phi = gla && (c.flags & LA_FLAG_IDENTITY_PHI);
+    a.dq_acc = a.dk_acc = a.dv_acc = nullptr;
+    if (gla) {
+        a.beta = nullptr;
+        a.dbeta = nullptr;
+    }
     a.sm_count = h->sm_count;
     a.workspace = h->d_bws;
     const cudaError_t e = la::launch_delta_backward(a, static_cast<cudaStream_t>(cuda_stream));

@@ -26,6 +26,13 @@
 // accumulators with one atomic add per column per CTA. A second kernel
 // writes dq and dk in the io dtype.
 //
+// The per-channel gated recurrence ("Linear attention and Hyena" §11.3,
+// S in R^{dk x dv}: S_t = diag(gamma_t) S_{t-1} + f_t v_t^T, o_t = S_t^T p_t
+// with f = phi(k), p = phi(q)) runs through the same scheme with the key
+// channels as rows: D += p_t do_t^T, dq = (S_t do_t) o phi'(q), dk = (D v_t)
+// o phi'(k), dgamma = rowsums of D o S_{t-1} (all row-local), dv_t = D^T f_t
+// (the one sum over rows), D <- diag(gamma_t) D.
+//
 // This is the correctness path of the gated variants' gradients: its cost is
 // the token-serial walk (2 T dependent steps per row) and the per-token
 // reduction, not memory bandwidth.
@@ -50,6 +57,9 @@ template <> __device__ __forceinline__ void st_io<float>(float* p, size_t i, flo
 template <> __device__ __forceinline__ void st_io<__nv_bfloat16>(__nv_bfloat16* p, size_t i, float x) {
     p[i] = __float2bfloat16_rn(x);
 }
+
+__device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.f : expf(x); }
+__device__ __forceinline__ float dphi(float x) { return x > 0.f ? 1.f : expf(x); }
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -231,6 +241,200 @@ __global__ void __launch_bounds__(kThreads, 1) delta_backward_kernel(DeltaBwdArg
     }
 }
 
+// ---------------------------------------------------------------------------
+// per-channel gated recurrence: rows = key channels
+// ---------------------------------------------------------------------------
+template <int DV>
+struct SmemGla {
+    float v[kSeg][DV];
+    float dout[kSeg][DV];
+    float f[kSeg][kRows];     // phi(k) of the CTA's channels
+    float df[kSeg][kRows];    // phi'(k)
+    float p[kSeg][kRows];     // phi(q)
+    float dp[kSeg][kRows];    // phi'(q)
+    float g[kSeg][kRows];     // gamma
+    float dq[kSeg][kRows];
+    float dk[kSeg][kRows];
+    float dg[kSeg][kRows];
+    float red[2][kRows][DV];
+};
+
+template <int DK, int DV, typename IO, bool IDPHI>
+__global__ void __launch_bounds__(kThreads, 1) gla_backward_kernel(DeltaBwdArgs p) {
+    constexpr int NC = DV / 32;   // value columns per lane
+    constexpr int NRB = DK / kRows;
+    using SM = SmemGla<DV>;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SM& sm = *reinterpret_cast<SM*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x / NRB, rb = blockIdx.x % NRB;
+    const int r = rb * kRows + warp;   // this warp's key channel
+    const int c0 = lane * NC;
+    const int T = p.T;
+    const int nseg = (T + kSeg - 1) / kSeg;
+    const size_t tok0 = static_cast<size_t>(bh) * T;
+    const IO* q = static_cast<const IO*>(p.q);
+    const IO* k = static_cast<const IO*>(p.k);
+    const IO* v = static_cast<const IO*>(p.v);
+    const IO* dout = static_cast<const IO*>(p.dout);
+    const size_t ssz = static_cast<size_t>(DK) * DV;
+    float* ck = p.ckpt + (static_cast<size_t>(bh) * nseg * DK + r) * DV + c0;   // + seg * DK * DV
+
+    auto stage = [&](int t0, int n, bool with_q) {
+        for (int x = tid; x < kSeg * DV; x += kThreads) {
+            const int i = x / DV, c = x % DV;
+            const bool in = i < n;
+            const size_t e = (tok0 + t0 + i) * DV + c;
+            sm.v[i][c] = in ? ld_io(v, e) : 0.f;
+            if (with_q) sm.dout[i][c] = in ? ld_io(dout, e) : 0.f;
+        }
+        for (int x = tid; x < kSeg * kRows; x += kThreads) {
+            const int i = x / kRows, w = x % kRows;
+            const bool in = i < n;
+            const size_t e = (tok0 + t0 + i) * DK + rb * kRows + w;
+            const float kk = in ? ld_io(k, e) : 0.f;
+            sm.f[i][w] = in ? (IDPHI ? kk : phi(kk)) : 0.f;
+            sm.df[i][w] = IDPHI ? 1.f : dphi(kk);
+            sm.g[i][w] = in ? p.gate[e] : 1.f;
+            if (with_q) {
+                const float qq = in ? ld_io(q, e) : 0.f;
+                sm.p[i][w] = in ? (IDPHI ? qq : phi(qq)) : 0.f;
+                sm.dp[i][w] = IDPHI ? 1.f : dphi(qq);
+            }
+        }
+    };
+    auto step = [&](int i, float* s) {
+        const float g = sm.g[i][warp], f = sm.f[i][warp];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) s[j] = g * s[j] + f * sm.v[i][c0 + j];
+    };
+
+    // ---- forward: the rows at the start of every segment -------------------
+    float s[NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) s[j] = p.state_in ? p.state_in[bh * ssz + static_cast<size_t>(r) * DV + c0 + j] : 0.f;
+    for (int sg = 0; sg < nseg; ++sg) {
+        const int t0 = sg * kSeg, n = min(kSeg, T - t0);
+        float* dst = ck + static_cast<size_t>(sg) * DK * DV;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) dst[j] = s[j];
+        __syncthreads();
+        stage(t0, n, false);
+        __syncthreads();
+        for (int i = 0; i < n; ++i) step(i, s);
+    }
+
+    // ---- backward: segments from the last ---------------------------------
+    float D[NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) D[j] = p.dstate_out ? p.dstate_out[bh * ssz + static_cast<size_t>(r) * DV + c0 + j] : 0.f;
+    int buf = 0;
+    for (int sg = nseg - 1; sg >= 0; --sg) {
+        const int t0 = sg * kSeg, n = min(kSeg, T - t0);
+        __syncthreads();
+        stage(t0, n, true);
+        __syncthreads();
+        float st[kSeg + 1][NC];
+        const float* src = ck + static_cast<size_t>(sg) * DK * DV;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) st[0][j] = src[j];
+#pragma unroll
+        for (int i = 0; i < kSeg; ++i) {
+#pragma unroll
+            for (int j = 0; j < NC; ++j) st[i + 1][j] = st[i][j];
+            if (i < n) step(i, st[i + 1]);
+        }
+#pragma unroll
+        for (int i = kSeg - 1; i >= 0; --i) {
+            if (i < n) {   // uniform over the CTA
+                float* red = &sm.red[buf][warp][0];
+                const float pr = sm.p[i][warp], f = sm.f[i][warp];
+                float a = 0.f, b = 0.f, c = 0.f;
+#pragma unroll
+                for (int j = 0; j < NC; ++j) {
+                    const float dor = sm.dout[i][c0 + j];
+                    D[j] += pr * dor;
+                    a += st[i + 1][j] * dor;              // (S_t do_t) row r
+                    b += D[j] * sm.v[i][c0 + j];           // (D v_t) row r
+                    c += D[j] * st[i][j];                  // rowsum of D o S_{t-1}
+                    red[c0 + j] = D[j] * f;                // dv_t, this row's part
+                }
+                a = warp_sum(a);
+                b = warp_sum(b);
+                c = warp_sum(c);
+                if (lane == 0) {
+                    sm.dq[i][warp] = a * sm.dp[i][warp];
+                    sm.dk[i][warp] = b * sm.df[i][warp];
+                    sm.dg[i][warp] = c;
+                }
+                const float g = sm.g[i][warp];
+#pragma unroll
+                for (int j = 0; j < NC; ++j) D[j] *= g;
+                __syncthreads();
+                const size_t t = tok0 + t0 + i;
+                for (int x = tid; x < DV; x += kThreads) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kRows; ++w) acc += sm.red[buf][w][x];
+                    atomicAdd(p.dv_acc + t * DV + x, acc);
+                }
+                buf ^= 1;
+            }
+        }
+        __syncthreads();
+        IO* dqo = static_cast<IO*>(p.dq);
+        IO* dko = static_cast<IO*>(p.dk);
+        for (int x = tid; x < n * kRows; x += kThreads) {
+            const int i = x / kRows, w = x % kRows;
+            const size_t e = (tok0 + t0 + i) * DK + rb * kRows + w;
+            st_io(dqo, e, sm.dq[i][w]);
+            st_io(dko, e, sm.dk[i][w]);
+            p.dgate[e] = sm.dg[i][w];
+        }
+    }
+    if (p.dstate_in) {
+#pragma unroll
+        for (int j = 0; j < NC; ++j) p.dstate_in[bh * ssz + static_cast<size_t>(r) * DV + c0 + j] = D[j];
+    }
+}
+
+// dv from its fp32 accumulator, in the io dtype.
+template <typename IO>
+__global__ void write_v_kernel(const float* dv_acc, IO* dv, size_t n) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        st_io(dv, i, dv_acc[i]);
+}
+
+template <int DK, int DV, typename IO, bool IDPHI>
+cudaError_t run_gla(const DeltaBwdArgs& p, cudaStream_t s) {
+    auto kern = gla_backward_kernel<DK, DV, IO, IDPHI>;
+    constexpr size_t smem = sizeof(SmemGla<DV>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<p.BH * (DK / kRows), kThreads, smem, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t n = static_cast<size_t>(p.BH) * p.T * DV;
+    write_v_kernel<IO><<<p.sm_count * 4, 256, 0, s>>>(p.dv_acc, static_cast<IO*>(p.dv), n);
+    return cudaGetLastError();
+}
+
+template <int DK, int DV>
+cudaError_t run_gla_io(const DeltaBwdArgs& p, cudaStream_t s) {
+    if (p.identity_phi)
+        return p.io == kBf16 ? run_gla<DK, DV, __nv_bfloat16, true>(p, s) : run_gla<DK, DV, float, true>(p, s);
+    return p.io == kBf16 ? run_gla<DK, DV, __nv_bfloat16, false>(p, s) : run_gla<DK, DV, float, false>(p, s);
+}
+
+cudaError_t run_gla_dims(const DeltaBwdArgs& p, cudaStream_t s) {
+    if (p.dk_dim == 64 && p.dv_dim == 64) return run_gla_io<64, 64>(p, s);
+    if (p.dk_dim == 64 && p.dv_dim == 128) return run_gla_io<64, 128>(p, s);
+    if (p.dk_dim == 128 && p.dv_dim == 64) return run_gla_io<128, 64>(p, s);
+    if (p.dk_dim == 128 && p.dv_dim == 128) return run_gla_io<128, 128>(p, s);
+    return cudaErrorInvalidValue;
+}
+
 // dq and dk from the fp32 accumulators, in the io dtype.
 template <typename IO>
 __global__ void write_qk_kernel(const float* dq_acc, const float* dk_acc, IO* dq, IO* dk, size_t n) {
@@ -272,9 +476,10 @@ cudaError_t run_dims(const DeltaBwdArgs& p, cudaStream_t s) {
 
 }  // namespace
 
-size_t delta_backward_bytes(int BH, int T, int dk, int dv) {
+size_t delta_backward_bytes(int BH, int T, int dk, int dv, bool gla) {
     const size_t nseg = static_cast<size_t>((T + kSeg - 1) / kSeg);
-    return static_cast<size_t>(BH) * (nseg * dv * dk + 2 * static_cast<size_t>(T) * dk) * sizeof(float);
+    const size_t acc = gla ? static_cast<size_t>(T) * dv : 2 * static_cast<size_t>(T) * dk;
+    return static_cast<size_t>(BH) * (nseg * dv * dk + acc) * sizeof(float);
 }
 
 cudaError_t launch_delta_backward(const DeltaBwdArgs& args, cudaStream_t s) {
@@ -282,6 +487,12 @@ cudaError_t launch_delta_backward(const DeltaBwdArgs& args, cudaStream_t s) {
     DeltaBwdArgs a = args;
     const size_t nseg = static_cast<size_t>((a.T + kSeg - 1) / kSeg);
     a.ckpt = a.workspace;
+    if (a.gla) {   // rows at every segment start, then the fp32 total of dv
+        a.dv_acc = a.ckpt + static_cast<size_t>(a.BH) * nseg * a.dv_dim * a.dk_dim;
+        cudaError_t e = cudaMemsetAsync(a.dv_acc, 0, static_cast<size_t>(a.BH) * a.T * a.dv_dim * sizeof(float), s);
+        if (e != cudaSuccess) return e;
+        return run_gla_dims(a, s);
+    }
     a.dq_acc = a.ckpt + static_cast<size_t>(a.BH) * nseg * a.dv_dim * a.dk_dim;
     a.dk_acc = a.dq_acc + static_cast<size_t>(a.BH) * a.T * a.dk_dim;
     // the column sums are accumulated: clear their totals first

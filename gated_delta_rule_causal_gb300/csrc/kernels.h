@@ -63,8 +63,10 @@ struct BwdArgs {
 };
 
 // Gradients of the gated delta rule, scalar (gate [BH][T]) or per-channel
-// (gate [BH][T][dk]) decay; state S [dv][dk] per sequence-head. Pointers are
-// device pointers; dgate, dbeta and the accumulators are overwritten.
+// (gate [BH][T][dk]) decay, state S [dv][dk] per sequence-head; or of the
+// per-channel gated recurrence (gla: gate [BH][T][dk], no beta, state S
+// [dk][dv]). Pointers are device pointers; dgate, dbeta and the accumulators
+// are overwritten.
 struct DeltaBwdArgs {
     const void* q;
     const void* k;
@@ -83,6 +85,8 @@ struct DeltaBwdArgs {
     int BH, T, dk_dim, dv_dim;
     int io;                    // Io
     bool per_channel;
+    bool gla;                  // per-channel gated recurrence (no beta; rows = key channels)
+    bool identity_phi;         // gla without the feature map
     int sm_count;
     float* workspace;          // delta_backward_bytes(BH, T, dk, dv) bytes
     // carved from the workspace by the launch: rows at every segment start,
@@ -90,10 +94,11 @@ struct DeltaBwdArgs {
     float* ckpt;
     float* dq_acc;
     float* dk_acc;
+    float* dv_acc;             // gla: fp32 total of dv
 };
 
 // Workspace bytes launch_delta_backward needs (checkpoints + accumulators).
-size_t delta_backward_bytes(int BH, int T, int dk, int dv);
+size_t delta_backward_bytes(int BH, int T, int dk, int dv, bool gla);
 // Token-serial CUDA-core kernel, rows split over CTAs (see backward_delta.cu);
 // d_k, d_v in {64, 128}.
 cudaError_t launch_delta_backward(const DeltaBwdArgs& a, cudaStream_t s);

@@ -292,10 +292,11 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
                 int variant, int T, void* cuda_stream);
 
 /*
- * Backward of the prefill of the gated delta rule (LA_GDN) and of its
- * per-channel-decay form (LA_KDA); d_k, d_v in {64, 128}; bf16 or fp32 io.
+ * Backward of the prefill of the gated delta rule (LA_GDN), of its
+ * per-channel-decay form (LA_KDA) and of the per-channel gated variant
+ * (LA_GLA); d_k, d_v in {64, 128}; bf16 or fp32 io.
  * Given the forward call's q, k, v, gate, beta and state_in (same layouts as
- * la_forward: gate [B,H,T] for LA_GDN, [B,H,T,d_k] for LA_KDA; beta
+ * la_forward: gate [B,H,T] for LA_GDN, [B,H,T,d_k] for LA_KDA and LA_GLA; beta
  * [B,H,T]; state_in [B,H,d_v*d_k] fp32 or NULL for zero), the gradient of
  * its outputs (dout [B,H,T,d_v], io dtype) and optionally of its final state
  * (dstate_out, fp32, same layout as the state; NULL means zero), writes dq,
@@ -303,14 +304,20 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
  * shape), dbeta [B,H,T] (fp32) and, if dstate_in is not NULL, the gradient
  * of the initial state (fp32). The pages give the forward operator only; the
  * gradients follow from the chain rule through the decay-first delta rule
- * (S~ = S Diag(a), u = beta (v - S~ k), S = S~ + u k^T, o = S q).
- * Token-serial CUDA-core kernel: the state's value rows are split over CTAs
- * of 16 rows, run forward with checkpoints every 16 tokens, then walked back
- * segment by segment; sums over rows are accumulated in fp32 (the order of
- * those additions varies from run to run, so the last bits of dq, dk, dgate
- * and dbeta may too). Its workspace (4 * B*H * (ceil(T/16) * d_v*d_k +
- * 2*T*d_k) bytes) is allocated by the handle on first use and grown when a
- * call needs more (la_destroy frees it). la_last_launches reports 2 (plus
+ * (S~ = S Diag(a), u = beta (v - S~ k), S = S~ + u k^T, o = S q) and, for
+ * LA_GLA, through S_t = diag(gamma_t) S_{t-1} + phi(k_t) v_t^T,
+ * o_t = S_t^T phi(q_t) (phi = elu + 1, the identity under
+ * LA_FLAG_IDENTITY_PHI). LA_GLA takes no beta: beta and dbeta may be NULL
+ * and are ignored; its state_in, dstate_out and dstate_in are
+ * [B,H,d_k*d_v] (S [d_k][d_v]).
+ * Token-serial CUDA-core kernel: the state's value rows (LA_GLA: its key
+ * channels) are split over CTAs of 16 rows, run forward with checkpoints
+ * every 16 tokens, then walked back segment by segment; sums over rows are
+ * accumulated in fp32 (the order of those additions varies from run to run,
+ * so the last bits of dq, dk, dgate and dbeta, or of LA_GLA's dv, may too).
+ * Its workspace (4 * B*H * (ceil(T/16) * d_v*d_k + 2*T*d_k) bytes; LA_GLA:
+ * T*d_v in place of 2*T*d_k) is allocated by the handle on first use and
+ * grown when a call needs more (la_destroy frees it). la_last_launches reports 2 (plus
  * memsets of the accumulated outputs, not counted).
  * Errors: LA_ERR_UNSUPPORTED for another variant or head size,
  * LA_ERR_INVALID_ARG (T < 1, a required pointer NULL), LA_ERR_MISALIGNED,

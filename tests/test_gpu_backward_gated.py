@@ -1,7 +1,8 @@
-"""Gradients of the gated delta rule prefill (la_backward_gated, scalar gate
-and per-channel decay) against the float64 oracle's (oracle/backward.py,
-``delta_backward``, itself pinned by finite differences of the forward
-oracle), on the same seeded inputs."""
+"""Gradients of the gated prefills (la_backward_gated: the gated delta rule
+with a scalar gate or a per-channel decay, and the per-channel gated
+variant) against the float64 oracle's (oracle/backward.py, ``delta_backward``
+and ``gla_backward``, pinned by finite differences of the forward oracle), on
+the same seeded inputs."""
 import numpy as np
 import pytest
 
@@ -14,12 +15,12 @@ la = pytest.importorskip("gated_delta_rule_causal_gb300")
 
 
 def _workload(variant, B, H, T, d, io):
-    base = {"gdn": W.GDN_B2H16_T8192_D128,
+    base = {"gdn": W.GDN_B2H16_T8192_D128, "gla": W.GLA_B4H16_T4096_D128,
             "kda": W.KDA_DECODE_N256H16_D128.with_(B=4, H=16, T=2048, decode_steps=0, state_std=0.0)}[variant]
     return W.small(base, B=B, H=H, T=T, dk=d, dv=d).with_(io=io)
 
 
-def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True):
+def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True, flags=0):
     import torch
     from oracle import backward
     w = _workload(variant, B, H, T, d, io)
@@ -31,30 +32,41 @@ def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True):
     do64 = W.as_f64(do_s)
     sin = (rng.standard_normal((B, H, ss)) * 0.1).astype(np.float32) if with_state else None
     dso = (rng.standard_normal((B, H, ss)) * 0.05).astype(np.float32) if with_dstate else None
-    h = la.Handle(B, H, d, d, io=io)
+    h = la.Handle(B, H, d, d, io=io, flags=flags)
     dev = h.device
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     got = h.backward_gated(to_torch(inp.q, dev), to_torch(inp.k, dev), to_torch(inp.v, dev),
                            to_torch(inp.gate, dev), to_torch(inp.beta, dev), to_torch(do_s, dev), t(sin), t(dso),
                            variant=variant)
+    if variant == "gla":
+        assert got[4] is None
+        got = got[:4] + got[5:]
     torch.cuda.synchronize()
     assert h.last_launches() == 2
     assert h.status() == la.LA_OK
     h.close()
-    ref = backward.delta_backward(q, k, v, g, b, do64, sin, dso)
+    if variant == "gla":
+        ref = backward.gla_backward(q, k, v, g, do64, sin, dso, identity_phi=bool(flags & la.LA_FLAG_IDENTITY_PHI))
+    else:
+        ref = backward.delta_backward(q, k, v, g, b, do64, sin, dso)
     return [x.float().cpu().numpy() for x in got], ref
 
 
 NAMES = ("dq", "dk", "dv", "dgate", "dbeta", "dstate_in")
+NAMES_GLA = ("dq", "dk", "dv", "dgate", "dstate_in")
 
 
-@pytest.mark.parametrize("variant", ["gdn", "kda"])
+def names(variant):
+    return NAMES_GLA if variant == "gla" else NAMES
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda", "gla"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("io", ["bf16", "fp32"])
 @pytest.mark.parametrize("T", [1, 37, 200])
 def test_backward_gated_parity(variant, d, io, T):
-    got, ref = _case(variant, 1, 2, T, d, io, seed=T + d + (7 if variant == "kda" else 0))
-    for name, x, r in zip(NAMES, got, ref):
+    got, ref = _case(variant, 1, 2, T, d, io, seed=T + d + {"gdn": 0, "kda": 7, "gla": 13}[variant])
+    for name, x, r in zip(names(variant), got, ref):
         assert x.shape == r.shape, name
         assert np.all(np.isfinite(x)), name
         assert slice_rel_err(x, r) <= TOL[io], (name, slice_rel_err(x, r))
@@ -67,11 +79,19 @@ def test_backward_gated_optional_states(with_state, with_dstate):
         assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
 
 
-@pytest.mark.parametrize("variant", ["gdn", "kda"])
+@pytest.mark.parametrize("variant", ["gdn", "kda", "gla"])
 def test_backward_gated_long_sequence(variant):
     # 2048 tokens: 128 segments walked back through their checkpoints
     got, ref = _case(variant, 1, 2, 2048, 64, "bf16", seed=17)
-    for name, x, r in zip(NAMES, got, ref):
+    for name, x, r in zip(names(variant), got, ref):
+        assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_gla_identity_feature_map(d):
+    # LA_FLAG_IDENTITY_PHI: the per-channel gated variant without phi
+    got, ref = _case("gla", 1, 2, 100, d, "bf16", seed=29, flags=la.LA_FLAG_IDENTITY_PHI)
+    for name, x, r in zip(NAMES_GLA, got, ref):
         assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
 
 
