@@ -39,16 +39,24 @@ struct la_handle {
 
 namespace {
 
-// la_forward_host: groups of sequence-heads in flight, and how they cross the
-// host link. Below kLargeCall bytes per call: two groups (best of 1, 2, 4, 8
-// on the normalized B4 H8 T2048 call) moved by copy kernels. From there on:
-// four groups (best of 1, 2, 4, 8 on the gated-delta B2 H16 T8192 call) moved
-// by the copy engines, which need no SM: the chunkwise kernels of the gated
-// variants fill each SM's shared memory, so a copy kernel's CTAs could not
-// run beside them and the copies of one group would not overlap the
-// kernels of another.
+// la_forward_host: how a call crosses the host link. Below kLargeCall bytes
+// per call: two groups of sequence-heads (best of 1, 2, 4, 8 on the
+// normalized B4 H8 T2048 call) moved by copy kernels. From there on, by the
+// copy engines, which need no SM (the chunkwise kernels of the gated
+// variants fill each SM's shared memory, so copy kernels could not run
+// beside them):
+// - the sequence in kTimeSegments segments of every head (strided 2-D
+//   copies), the state handed from one segment's kernels to the next in
+//   device memory. Every launch keeps every head, so a segment's kernels take
+//   ~1/kTimeSegments of the call's, where a group of heads would still walk
+//   the whole sequence (gated delta B2 H16 T8192: 1.26 ms per call with 4
+//   segments, 1.27 with 8, 1.40 with 16; 1.43 with 4 head groups);
+// - LA_GLA alone in kHostGroupsLarge groups of heads: its calls run two
+//   launches of 32 heads per segment, and time segments measured slower
+//   (B4 H16 T4096: 1.91 ms with 4 groups, 2.02 with 4 segments).
 constexpr int kHostGroupsSmall = 2;
 constexpr int kHostGroupsLarge = 4;
+constexpr int kTimeSegments = 4;
 constexpr size_t kLargeCall = size_t(64) << 20;
 constexpr int kCopyCtas = 64;    // CTAs of one gather / scatter over the host link
 
@@ -218,6 +226,105 @@ int enqueue_forward(la_handle* h, la::FwdArgs& a, int variant, int chunk, cudaSt
         e = la::launch_recurrent(a, s);
         if (e != cudaSuccess) return cuda_fail(h, e, "recurrent kernel launch");
         h->last_launches += 1;
+    }
+    return LA_OK;
+}
+
+// la_forward_host for a large call: the sequence in segments of Ts tokens
+// (a multiple of the 64-token chunk) for all sequence-heads at once. Per
+// segment s, staging half b = s & 1: s_in copies the segment's slices of q,
+// k, v, gate and beta in (one strided copy each: BH rows of len tokens), s_comp
+// runs the prefill of len tokens from the state the previous segment left
+// (device buffer (s - 1) & 1; the caller's state_in is staged into buffer 1
+// for segment 0) into buffer s & 1, s_out copies the outputs (and den) out.
+// A half is refilled two segments later, after its kernels and its
+// copy-out. The final state leaves after the last segment.
+int host_time_split(la_handle* h, const void* q, const void* k, const void* v, const float* gate,
+                    const float* beta, const float* state_in, void* out, float* state_out, float* den_out,
+                    int variant, int T, int chunk) {
+    const la_config& c = h->cfg;
+    const int BH = c.B * c.H;
+    const size_t io = (c.io == LA_BF16) ? 2 : 4;
+    const size_t ss = state_elems(c, variant);
+    const bool per_token_gate = variant == LA_GLA || variant == LA_KDA || variant == LA_GDN;
+    const size_t gate_row = (variant == LA_GLA || variant == LA_KDA) ? c.d_k * 4 : 4;   // bytes per token
+    int Ts = (T + kTimeSegments - 1) / kTimeSegments;
+    Ts = (Ts + 63) / 64 * 64;
+    const int nseg = (T + Ts - 1) / Ts;
+    // bytes per token of every sequence-head: q, k, v, gate, beta, out, den
+    const size_t row[7] = {c.d_k * io, c.d_k * io, c.d_v * io, (gate && per_token_gate) ? gate_row : 0,
+                           beta ? 4 : 0, c.d_v * io, den_out ? 4 : 0};
+    size_t off[7], half = 0;
+    for (int i = 0; i < 7; ++i) {
+        off[i] = half;
+        half += (static_cast<size_t>(BH) * Ts * row[i] + 255) & ~static_cast<size_t>(255);
+    }
+    const size_t sbytes = (static_cast<size_t>(BH) * ss * 4 + 255) & ~static_cast<size_t>(255);
+    const size_t hgate = (variant == LA_NORM_DECAY && gate) ? ((BH * 4 + 255) & ~static_cast<size_t>(255)) : 0;
+    const size_t need = 2 * half + 2 * sbytes + hgate;
+    cudaError_t e;
+    if (need > h->stage_bytes) {
+        if (h->d_stage) {   // grow the staging (frees the old one after the work that used it)
+            cudaStreamSynchronize(h->s_in);
+            cudaStreamSynchronize(h->s_comp);
+            cudaStreamSynchronize(h->s_out);
+            cudaFree(h->d_stage);
+            h->d_stage = nullptr;
+            h->stage_bytes = 0;
+        }
+        e = cudaMalloc(&h->d_stage, need);
+        if (e != cudaSuccess) return cuda_fail(h, e, "staging allocation");
+        h->stage_bytes = need;
+    }
+    uint8_t* sbuf[2] = {h->d_stage + 2 * half, h->d_stage + 2 * half + sbytes};
+    float* dgate_head = reinterpret_cast<float*>(h->d_stage + 2 * half + 2 * sbytes);
+    // segment 0 reads the state from buffer 1; the per-head decay once
+    e = cudaSuccess;
+    if (state_in) e = cudaMemcpyAsync(sbuf[1], state_in, static_cast<size_t>(BH) * ss * 4, cudaMemcpyHostToDevice, h->s_in);
+    if (e == cudaSuccess && hgate)
+        e = cudaMemcpyAsync(dgate_head, gate, static_cast<size_t>(BH) * 4, cudaMemcpyHostToDevice, h->s_in);
+    if (e != cudaSuccess) return cuda_fail(h, e, "staging copy-in");
+    const void* src[5] = {q, k, v, per_token_gate ? gate : nullptr, beta};
+    for (int sg = 0; sg < nseg; ++sg) {
+        const int b = sg & 1;
+        const int t0 = sg * Ts;
+        const int len = (T - t0 < Ts) ? T - t0 : Ts;
+        uint8_t* st = h->d_stage + b * half;
+        if (sg >= 2) e = cudaStreamWaitEvent(h->s_in, h->ev_comp[b], 0);
+        for (int i = 0; i < 5 && e == cudaSuccess; ++i)
+            if (src[i] && row[i])
+                e = cudaMemcpy2DAsync(st + off[i], len * row[i], static_cast<const uint8_t*>(src[i]) + t0 * row[i],
+                                      static_cast<size_t>(T) * row[i], len * row[i], BH, cudaMemcpyHostToDevice,
+                                      h->s_in);
+        if (e == cudaSuccess) e = cudaEventRecord(h->ev_in[b], h->s_in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_comp, h->ev_in[b], 0);
+        if (e == cudaSuccess && sg >= 2) e = cudaStreamWaitEvent(h->s_comp, h->ev_out[b], 0);
+        if (e != cudaSuccess) return cuda_fail(h, e, "staging copy-in");
+        const float* g_arg = !gate ? nullptr : per_token_gate ? reinterpret_cast<const float*>(st + off[3])
+                           : (variant == LA_NORM_DECAY) ? dgate_head : nullptr;
+        const float* sin = (sg == 0 && !state_in) ? nullptr : reinterpret_cast<const float*>(sbuf[(sg + 1) & 1]);
+        la::FwdArgs a = make_args(h, st + off[0], st + off[1], st + off[2], g_arg,
+                                  beta ? reinterpret_cast<const float*>(st + off[4]) : nullptr, sin, st + off[5],
+                                  reinterpret_cast<float*>(sbuf[b]), den_out ? reinterpret_cast<float*>(st + off[6]) : nullptr,
+                                  variant, len);
+        int rc = enqueue_forward(h, a, variant, chunk, h->s_comp);
+        if (rc != LA_OK) return rc;
+        e = cudaEventRecord(h->ev_comp[b], h->s_comp);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_out, h->ev_comp[b], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(static_cast<uint8_t*>(out) + t0 * row[5], static_cast<size_t>(T) * row[5], st + off[5],
+                                  len * row[5], len * row[5], BH, cudaMemcpyDeviceToHost, h->s_out);
+        if (e == cudaSuccess && den_out)
+            e = cudaMemcpy2DAsync(reinterpret_cast<uint8_t*>(den_out) + t0 * row[6], static_cast<size_t>(T) * row[6],
+                                  st + off[6], len * row[6], len * row[6], BH, cudaMemcpyDeviceToHost, h->s_out);
+        if (e == cudaSuccess) e = cudaEventRecord(h->ev_out[b], h->s_out);
+        if (e != cudaSuccess) return cuda_fail(h, e, "staging copy-out");
+    }
+    // s_out follows the last segment's kernels: the final state leaves now
+    if (state_out) {
+        e = cudaMemcpyAsync(state_out, sbuf[(nseg - 1) & 1], static_cast<size_t>(BH) * ss * 4, cudaMemcpyDeviceToHost,
+                            h->s_out);
+        if (e != cudaSuccess) return cuda_fail(h, e, "state copy-out");
     }
     return LA_OK;
 }
@@ -412,6 +519,19 @@ int la_forward_host(la_handle* h, const void* q, const void* k, const void* v, c
     size_t call_bytes = 0;
     for (int i = 0; i < 9; ++i) call_bytes += per_head[i] * BH;
     const bool large = call_bytes >= kLargeCall;
+    if (large && variant != LA_GLA) {
+        e = cudaEventRecord(h->ev_start, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_in, h->ev_start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_comp, h->ev_start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->s_out, h->ev_start, 0);
+        if (e != cudaSuccess) return cuda_fail(h, e, "stream ordering");
+        rc = host_time_split(h, q, k, v, gate, beta, state_in, out, state_out, den_out, variant, T, chunk);
+        if (rc != LA_OK) return rc;
+        e = cudaEventRecord(h->ev_done, h->s_out);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, h->ev_done, 0);
+        if (e != cudaSuccess) return cuda_fail(h, e, "stream ordering");
+        return LA_OK;
+    }
     const int want = large ? kHostGroupsLarge : kHostGroupsSmall;
     const int G0 = BH < want ? BH : want;
     const int gbh = (BH + G0 - 1) / G0;

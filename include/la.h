@@ -178,15 +178,19 @@ int la_forward(la_handle* h, const void* q, const void* k, const void* v,
  * Prefill from host memory: the same operation and arguments as la_forward,
  * but q, k, v, gate, beta, state_in, out, state_out and den_out are host
  * pointers (page-locked memory, cudaHostAlloc or cudaHostRegister, for the
- * copies to run asynchronously). The library splits the B*H sequence-heads
- * into groups and, on three streams of its own, copies group i + 1 in, runs
- * the kernels of group i and copies group i - 1 out at the same time. A call
- * that moves less than 64 MiB over the host link runs as up to 2 groups and,
- * when the GPU can address every buffer (page-locked memory under unified
- * addressing), one copy kernel per group and direction moves the data;
- * otherwise the copy engine does, one copy per tensor. A call of 64 MiB or
- * more runs as up to 4 groups moved by the copy engines, which leave every
- * SM to the kernels. la_last_launches counts the copy kernels too. Staging for two
+ * copies to run asynchronously). The library splits the call into pieces
+ * and, on three streams of its own, copies piece i + 1 in, runs the kernels
+ * of piece i and copies piece i - 1 out at the same time. A call that moves
+ * less than 64 MiB over the host link runs as up to 2 groups of
+ * sequence-heads and, when the GPU can address every buffer (page-locked
+ * memory under unified addressing), one copy kernel per group and direction
+ * moves the data; otherwise the copy engine does, one copy per tensor. A
+ * call of 64 MiB or more is moved by the copy engines, which leave every SM
+ * to the kernels: split along the sequence into 4 segments of every
+ * sequence-head (multiples of 64 tokens, one strided copy per tensor and
+ * segment, the state handed from segment to segment in device memory), or,
+ * for LA_GLA, into up to 4 groups of sequence-heads. la_last_launches counts
+ * the copy kernels too. Staging for two
  * groups lives in device memory that the handle allocates on
  * first use and grows when a call needs more (la_destroy frees it). The call
  * is ordered after the work already enqueued on cuda_stream, and the work

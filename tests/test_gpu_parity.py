@@ -359,29 +359,37 @@ def test_forward_host_parity(variant, H, T, chunk):
     h.close()
 
 
-@pytest.mark.parametrize("variant,d,H,T", [("gdn", 128, 12, 6000), ("norm", 64, 24, 8192)])
+@pytest.mark.parametrize("variant,d,H,T", [("gdn", 128, 12, 6000), ("norm", 64, 24, 8192), ("gla", 128, 16, 3000)])
 def test_forward_host_large_call_parity(variant, d, H, T):
-    # A call that moves 64 MiB or more over the host link runs as 4 groups
-    # of sequence-heads moved by the copy engines (no copy kernels); every
-    # head against the oracle.
+    # A call that moves 64 MiB or more over the host link runs as 4 time
+    # segments of every sequence-head (multiples of 64 tokens), moved by the
+    # copy engines, the state handed from segment to segment on the device;
+    # every head against the oracle.
     w = base(variant, d).with_(B=1, H=H, T=T)
     inp = W.draw(w, seed=T + H)
     moved = sum(a.nbytes for a in (inp.q, inp.k, inp.v, inp.gate, inp.beta) if a is not None)
     moved += w.B * w.H * w.T * w.dv * 2 + w.B * w.H * oracle.state_size(variant, w.dk, w.dv) * 4
     assert moved >= 64 << 20
     pin = lambda a: None if a is None else to_torch(a, "cpu").pin_memory()
+    rng = np.random.default_rng(H)
+    sin = (rng.standard_normal((w.B, w.H, oracle.state_size(variant, w.dk, w.dv))) * 0.1).astype(np.float32)
+    if variant in NORMED:
+        sin[..., w.dk * w.dv:] = np.abs(sin[..., w.dk * w.dv:]) * 50 + 1.0
+    den = torch.zeros((w.B, w.H, w.T), dtype=torch.float32).pin_memory() if variant in NORMED else None
     h = handle(w)
-    out, st, _ = h.forward_host(pin(inp.q), pin(inp.k), pin(inp.v), pin(inp.gate), pin(inp.beta), None,
-                                variant=variant, chunk=0)
+    out, st, den = h.forward_host(pin(inp.q), pin(inp.k), pin(inp.v), pin(inp.gate), pin(inp.beta),
+                                  torch.from_numpy(sin).pin_memory(), variant=variant, chunk=0, den_out=den)
     torch.cuda.synchronize()
     assert h.status() == la.LA_OK
-    per_group = 1 if variant == "gdn" else None   # one cooperative launch per group of 3 heads
-    if per_group is not None:
-        assert h.last_launches() == 4 * per_group
+    if variant == "gdn":   # one cooperative launch per time segment
+        ts = -(-(-(-T // 4)) // 64) * 64
+        assert h.last_launches() == -(-T // ts)
     h.close()
-    ref = oracle_run(w, inp, None)
+    ref = oracle_run(w, inp, sin)
     assert slice_rel_err(from_torch(out), ref.o) <= TOL[w.io]
     assert slice_rel_err(st.numpy().astype(np.float64), ref.state) <= TOL[w.io]
+    if den is not None:
+        assert np.max(np.abs(den.numpy() - ref.den) / ref.den) <= TOL[w.io]
 
 
 # ------------------------------------------------------------- state passing
