@@ -323,9 +323,10 @@ class Handle:
     def backward_gated(self, q, k, v, gate, beta, dout, state_in=None, dstate_out=None, *, variant="gdn",
                        return_dstate=True, stream=None):
         """Gradients of a gated delta rule prefill (variant "gdn": gate
-        [B,H,T]; "kda": gate [B,H,T,d_k]; beta [B,H,T]) or of a per-channel
-        gated one ("gla": gate [B,H,T,d_k], beta None). Returns (dq, dk, dv,
-        dgate, dbeta, dstate_in); dbeta is None for "gla"."""
+        [B,H,T]; "kda": gate [B,H,T,d_k]; beta [B,H,T]), of a per-channel
+        gated one ("gla": gate [B,H,T,d_k]) or of a normalized one with a fixed
+        decay ("norm_decay": gate [B,H]); the last two take no beta. Returns
+        (dq, dk, dv, dgate, dbeta, dstate_in); dbeta is None without beta."""
         import torch
         var = VARIANTS[variant]
         B, H, T = q.shape[0], q.shape[1], q.shape[2]
@@ -333,9 +334,10 @@ class Handle:
             raise ValueError("q batch/heads differ from the handle's")
         for name, t, d in (("q", q, self.d_k), ("k", k, self.d_k), ("v", v, self.d_v), ("dout", dout, self.d_v)):
             self._expect(name, t, (B, H, T, d), self.dtype)
-        gshape = (B, H, T, self.d_k) if variant in ("kda", "gla") else (B, H, T)
+        gshape = ((B, H, T, self.d_k) if variant in ("kda", "gla") else (B, H) if variant == "norm_decay"
+                  else (B, H, T))
         self._expect("gate", gate, gshape, torch.float32)
-        if variant == "gla":
+        if variant in ("gla", "norm_decay"):
             beta = None
         self._expect("beta", beta, (B, H, T), torch.float32)
         ss = state_size(variant, self.d_k, self.d_v)

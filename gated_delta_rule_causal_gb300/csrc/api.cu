@@ -329,6 +329,69 @@ int host_time_split(la_handle* h, const void* q, const void* k, const void* v, c
     return LA_OK;
 }
 
+// Grow the handle's backward workspace to `need` bytes (frees the old one
+// after the work that used it).
+int grow_bws(la_handle* h, size_t need) {
+    if (need <= h->bws_bytes) return LA_OK;
+    if (h->d_bws) {
+        cudaFree(h->d_bws);   // waits for the work that used it
+        h->d_bws = nullptr;
+        h->bws_bytes = 0;
+    }
+    const cudaError_t e = cudaMalloc(&h->d_bws, need);
+    if (e != cudaSuccess) return cuda_fail(h, e, "backward workspace allocation");
+    h->bws_bytes = need;
+    return LA_OK;
+}
+
+// Gradients of the normalized variant (gamma NULL) or of its fixed-decay form
+// on the row-split CUDA-core kernel (d_k, d_v in {64, 128}): the forward
+// first, its outputs and normalizers into the backward workspace, then the
+// token-serial rows. Arguments validated by the caller.
+int norm_rows_backward(la_handle* h, const void* q, const void* k, const void* v, const float* gamma,
+                       const float* state_in, const void* dout, const float* dstate_out, void* dq, void* dk,
+                       void* dv, float* dgamma, float* dstate_in, int variant, int T, cudaStream_t s) {
+    const la_config& c = h->cfg;
+    const int BH = c.B * c.H;
+    const int io = c.io == LA_FP32 ? la::kFp32 : la::kBf16;
+    const size_t fwd = la::norm_rows_fwd_bytes(BH, T, c.d_v, io);
+    const size_t o_bytes = (static_cast<size_t>(BH) * T * c.d_v * (io == la::kBf16 ? 2 : 4) + 255) & ~static_cast<size_t>(255);
+    int rc = grow_bws(h, fwd + la::norm_rows_bytes(BH, T, c.d_k, c.d_v));
+    if (rc != LA_OK) return rc;
+    uint8_t* ws = reinterpret_cast<uint8_t*>(h->d_bws);
+    float* den = reinterpret_cast<float*>(ws + o_bytes);
+    la::FwdArgs f = make_args(h, q, k, v, gamma, nullptr, state_in, ws, nullptr, den, variant, T);
+    rc = enqueue_forward(h, f, variant, 0, s);
+    if (rc != LA_OK) return rc;
+    la::DeltaBwdArgs a = {};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.gate = gamma;
+    a.state_in = state_in;
+    a.dout = dout;
+    a.dstate_out = dstate_out;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dgate = dgamma;
+    a.dstate_in = dstate_in;
+    a.BH = BH;
+    a.T = T;
+    a.dk_dim = c.d_k;
+    a.dv_dim = c.d_v;
+    a.io = io;
+    a.norm = true;
+    a.fwd_out = ws;
+    a.fwd_den = den;
+    a.sm_count = h->sm_count;
+    a.workspace = reinterpret_cast<float*>(ws + fwd);
+    const cudaError_t e = la::launch_delta_backward(a, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "normalized backward launch");
+    h->last_launches += 2;   // the row kernel and the dv conversion, after the forward's
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -665,8 +728,10 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v, const
     if (!q || !k || !v || !dout || !dq || !dk || !dv)
         return fail(h, LA_ERR_INVALID_ARG, "q, k, v, dout, dq, dk and dv are required");
     const la_config& c = h->cfg;
-    if (!((c.d_k == 16 || c.d_k == 32 || c.d_k == 64) && (c.d_v == 16 || c.d_v == 32 || c.d_v == 64)))
-        return fail(h, LA_ERR_UNSUPPORTED, "la_backward supports d_k, d_v in {16, 32, 64}");
+    const bool small_d = (c.d_k == 16 || c.d_k == 32 || c.d_k == 64) && (c.d_v == 16 || c.d_v == 32 || c.d_v == 64);
+    const bool rows_d = (c.d_k == 64 || c.d_k == 128) && (c.d_v == 64 || c.d_v == 128);
+    if (!small_d && !rows_d)
+        return fail(h, LA_ERR_UNSUPPORTED, "la_backward supports d_k, d_v in {16, 32, 64} or in {64, 128}");
     if (static_cast<long long>(T) * (c.d_k > c.d_v ? c.d_k : c.d_v) > (1LL << 31) - 1)
         return fail(h, LA_ERR_UNSUPPORTED, "T * d exceeds 2^31 - 1");
     const void* ptrs[] = {q, k, v, state_in, dout, dstate_out, dq, dk, dv, dstate_in};
@@ -731,6 +796,12 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v, const
         h->last_launches = launches;
         return LA_OK;
     }
+    // d_k, d_v in {64, 128}: the row-split kernel after a forward (it keeps
+    // checkpoints, so its rounding does not grow with T); smaller heads: the
+    // one-CTA-per-head kernel
+    if (rows_d)
+        return norm_rows_backward(h, q, k, v, nullptr, state_in, dout, dstate_out, dq, dk, dv, nullptr, dstate_in,
+                                  LA_NORM_ELU1, T, static_cast<cudaStream_t>(cuda_stream));
     const cudaError_t e = la::launch_norm_backward(a, static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "backward kernel launch");
     h->last_launches = 1;
@@ -743,10 +814,10 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
     if (!h) return LA_ERR_INVALID_ARG;
     h->last_error.clear();
     h->last_launches = 0;
-    if (variant != LA_GDN && variant != LA_KDA && variant != LA_GLA)
-        return fail(h, LA_ERR_UNSUPPORTED, "la_backward_gated supports LA_GDN, LA_KDA and LA_GLA");
+    if (variant != LA_GDN && variant != LA_KDA && variant != LA_GLA && variant != LA_NORM_DECAY)
+        return fail(h, LA_ERR_UNSUPPORTED, "la_backward_gated supports LA_GDN, LA_KDA, LA_GLA and LA_NORM_DECAY");
     if (T < 1) return fail(h, LA_ERR_INVALID_ARG, "T must be >= 1");
-    const bool gla = variant == LA_GLA;
+    const bool gla = variant == LA_GLA || variant == LA_NORM_DECAY;   // no beta
     if (!q || !k || !v || !gate || !dout || !dq || !dk || !dv || !dgate)
         return fail(h, LA_ERR_INVALID_ARG, "q, k, v, gate, dout, dq, dk, dv and dgate are required");
     if (!gla && (!beta || !dbeta)) return fail(h, LA_ERR_INVALID_ARG, "beta and dbeta are required");
@@ -763,19 +834,13 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
             return fail(h, LA_ERR_MISALIGNED, std::string(names[i]) + " is not 16-byte aligned");
     DeviceGuard g(c.device);
     if (!g.ok) return fail(h, LA_ERR_CUDA, "cannot select the handle's device");
+    if (variant == LA_NORM_DECAY)
+        return norm_rows_backward(h, q, k, v, gate, state_in, dout, dstate_out, dq, dk, dv, dgate, dstate_in,
+                                  LA_NORM_DECAY, T, static_cast<cudaStream_t>(cuda_stream));
     const int BH = c.B * c.H;
-    const size_t need = la::delta_backward_bytes(BH, T, c.d_k, c.d_v, gla);
-    if (need > h->bws_bytes) {
-        if (h->d_bws) {
-            cudaFree(h->d_bws);   // waits for the work that used it
-            h->d_bws = nullptr;
-            h->bws_bytes = 0;
-        }
-        const cudaError_t e = cudaMalloc(&h->d_bws, need);
-        if (e != cudaSuccess) return cuda_fail(h, e, "backward workspace allocation");
-        h->bws_bytes = need;
-    }
-    la::DeltaBwdArgs a;
+    const int grc = grow_bws(h, la::delta_backward_bytes(BH, T, c.d_k, c.d_v, gla));
+    if (grc != LA_OK) return grc;
+    la::DeltaBwdArgs a = {};
     a.q = q;
     a.k = k;
     a.v = v;

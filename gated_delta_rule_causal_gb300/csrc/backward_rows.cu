@@ -33,9 +33,21 @@
 // o phi'(k), dgamma = rowsums of D o S_{t-1} (all row-local), dv_t = D^T f_t
 // (the one sum over rows), D <- diag(gamma_t) D.
 //
-// This is the correctness path of the gated variants' gradients: its cost is
-// the token-serial walk (2 T dependent steps per row) and the per-token
-// reduction, not memory bandwidth.
+// The normalized recurrence (S in R^{dk x dv} and z in R^{dk}: S_t = gamma
+// S_{t-1} + f_t v_t^T, z_t = gamma z_{t-1} + f_t, gamma = 1 or one decay per
+// sequence-head; o_t = S_t^T p_t / p_t.z_t) takes the key channels as rows
+// too. Its two per-token factors dnum_t = do_t / den_t and
+// dden_t = -(do_t.num_t) / den_t^2 = -(do_t.o_t) / den_t come from the
+// outputs and normalizers of a forward call the caller runs first. Then with
+// G, g the gradients reaching S_t, z_t: G += p_t dnum_t^T, g += p_t dden_t,
+// dq = (S_t dnum_t + z_t dden_t) o phi'(q), dk = (G v_t + g) o phi'(k) (both
+// row-local), dv_t = G^T f_t (the sum over rows), dgamma += <G, S_{t-1}> +
+// <g, z_{t-1}>, then G, g <- gamma G, gamma g.
+//
+// This is the correctness path of these gradients (and of the normalized
+// variant's wherever the chunkwise tensor-core backward does not apply): its
+// cost is the token-serial walk (2 T dependent steps per row) and the
+// per-token reduction, not memory bandwidth.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -435,6 +447,224 @@ cudaError_t run_gla_dims(const DeltaBwdArgs& p, cudaStream_t s) {
     return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------------------
+// normalized recurrence: rows = key channels, z alongside
+// ---------------------------------------------------------------------------
+template <int DV>
+struct SmemNorm {
+    float v[kSeg][DV];
+    float dnum[kSeg][DV];     // do / den
+    float dden[kSeg];         // -(do . o) / den
+    float f[kSeg][kRows];     // phi(k) of the CTA's channels
+    float df[kSeg][kRows];    // phi'(k)
+    float p[kSeg][kRows];     // phi(q)
+    float dp[kSeg][kRows];    // phi'(q)
+    float dq[kSeg][kRows];
+    float dk[kSeg][kRows];
+    float gsum[kRows];        // dgamma, per row
+    float red[2][kRows][DV];
+};
+
+template <int DK, int DV, typename IO, bool DECAY>
+__global__ void __launch_bounds__(kThreads, 1) norm_rows_backward_kernel(DeltaBwdArgs p) {
+    constexpr int NC = DV / 32;
+    constexpr int NRB = DK / kRows;
+    using SM = SmemNorm<DV>;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SM& sm = *reinterpret_cast<SM*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x / NRB, rb = blockIdx.x % NRB;
+    const int r = rb * kRows + warp;   // this warp's key channel
+    const int c0 = lane * NC;
+    const int T = p.T;
+    const int nseg = (T + kSeg - 1) / kSeg;
+    const size_t tok0 = static_cast<size_t>(bh) * T;
+    const IO* q = static_cast<const IO*>(p.q);
+    const IO* k = static_cast<const IO*>(p.k);
+    const IO* v = static_cast<const IO*>(p.v);
+    const IO* dout = static_cast<const IO*>(p.dout);
+    const IO* o = static_cast<const IO*>(p.fwd_out);
+    const size_t ssz = static_cast<size_t>(DK) * DV + DK;
+    const float gam = DECAY ? p.gate[bh] : 1.f;
+    float* ck = p.ckpt + (static_cast<size_t>(bh) * nseg * DK + r) * DV + c0;   // + seg * DK * DV
+    float* ckz = p.ckz + static_cast<size_t>(bh) * nseg * DK + r;              // + seg * DK
+
+    auto stage = [&](int t0, int n, bool bwd) {
+        for (int x = tid; x < kSeg * DV; x += kThreads) {
+            const int i = x / DV, c = x % DV;
+            const bool in = i < n;
+            const size_t e = (tok0 + t0 + i) * DV + c;
+            sm.v[i][c] = in ? ld_io(v, e) : 0.f;
+            if (bwd) sm.dnum[i][c] = in ? ld_io(dout, e) / p.fwd_den[tok0 + t0 + i] : 0.f;
+        }
+        if (bwd) {   // warp i: dden of token i
+            const int i = warp;
+            float d = 0.f;
+            if (i < n) {
+                const size_t e = (tok0 + t0 + i) * DV;
+                for (int c = lane; c < DV; c += 32) d += ld_io(dout, e + c) * ld_io(o, e + c);
+            }
+            d = warp_sum(d);
+            if (lane == 0) sm.dden[i] = (i < n) ? -d / p.fwd_den[tok0 + t0 + i] : 0.f;
+        }
+        for (int x = tid; x < kSeg * kRows; x += kThreads) {
+            const int i = x / kRows, w = x % kRows;
+            const bool in = i < n;
+            const size_t e = (tok0 + t0 + i) * DK + rb * kRows + w;
+            const float kk = in ? ld_io(k, e) : 0.f;
+            sm.f[i][w] = in ? phi(kk) : 0.f;
+            sm.df[i][w] = dphi(kk);
+            if (bwd) {
+                const float qq = in ? ld_io(q, e) : 0.f;
+                sm.p[i][w] = in ? phi(qq) : 0.f;
+                sm.dp[i][w] = dphi(qq);
+            }
+        }
+    };
+    static_assert(kSeg == kRows, "one warp per token of a segment for dden");
+    auto step = [&](int i, float* s, float& z) {
+        const float f = sm.f[i][warp];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) s[j] = gam * s[j] + f * sm.v[i][c0 + j];
+        z = gam * z + f;
+    };
+
+    // ---- forward: the rows (and z) at the start of every segment ----------
+    float s[NC];
+    float z = p.state_in ? p.state_in[bh * ssz + static_cast<size_t>(DK) * DV + r] : 0.f;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) s[j] = p.state_in ? p.state_in[bh * ssz + static_cast<size_t>(r) * DV + c0 + j] : 0.f;
+    for (int sg = 0; sg < nseg; ++sg) {
+        const int t0 = sg * kSeg, n = min(kSeg, T - t0);
+        float* dst = ck + static_cast<size_t>(sg) * DK * DV;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) dst[j] = s[j];
+        if (lane == 0) ckz[static_cast<size_t>(sg) * DK] = z;
+        __syncthreads();
+        stage(t0, n, false);
+        __syncthreads();
+        for (int i = 0; i < n; ++i) step(i, s, z);
+    }
+
+    // ---- backward: segments from the last ---------------------------------
+    float G[NC];
+    float gz = p.dstate_out ? p.dstate_out[bh * ssz + static_cast<size_t>(DK) * DV + r] : 0.f;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) G[j] = p.dstate_out ? p.dstate_out[bh * ssz + static_cast<size_t>(r) * DV + c0 + j] : 0.f;
+    float gacc = 0.f;   // dgamma: this lane's part of row r's sum
+    int buf = 0;
+    for (int sg = nseg - 1; sg >= 0; --sg) {
+        const int t0 = sg * kSeg, n = min(kSeg, T - t0);
+        __syncthreads();
+        stage(t0, n, true);
+        __syncthreads();
+        float st[kSeg + 1][NC];
+        float zs[kSeg + 1];
+        const float* src = ck + static_cast<size_t>(sg) * DK * DV;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) st[0][j] = src[j];
+        zs[0] = ckz[static_cast<size_t>(sg) * DK];
+#pragma unroll
+        for (int i = 0; i < kSeg; ++i) {
+#pragma unroll
+            for (int j = 0; j < NC; ++j) st[i + 1][j] = st[i][j];
+            zs[i + 1] = zs[i];
+            if (i < n) step(i, st[i + 1], zs[i + 1]);
+        }
+#pragma unroll
+        for (int i = kSeg - 1; i >= 0; --i) {
+            if (i < n) {   // uniform over the CTA
+                float* red = &sm.red[buf][warp][0];
+                const float pr = sm.p[i][warp], f = sm.f[i][warp], dd = sm.dden[i];
+                gz += pr * dd;
+                float a = 0.f, b = 0.f;
+#pragma unroll
+                for (int j = 0; j < NC; ++j) {
+                    const float dn = sm.dnum[i][c0 + j];
+                    G[j] += pr * dn;
+                    a += st[i + 1][j] * dn;               // (S_t dnum_t) row r
+                    b += G[j] * sm.v[i][c0 + j];           // (G v_t) row r
+                    if (DECAY) gacc += G[j] * st[i][j];    // <G, S_{t-1}> row r
+                    red[c0 + j] = G[j] * f;                // dv_t, this row's part
+                }
+                if (DECAY && lane == 0) gacc += gz * zs[i];   // <g, z_{t-1}> row r
+                a = warp_sum(a) + zs[i + 1] * dd;
+                b = warp_sum(b) + gz;
+                if (lane == 0) {
+                    sm.dq[i][warp] = a * sm.dp[i][warp];
+                    sm.dk[i][warp] = b * sm.df[i][warp];
+                }
+#pragma unroll
+                for (int j = 0; j < NC; ++j) G[j] *= gam;
+                gz *= gam;
+                __syncthreads();
+                const size_t t = tok0 + t0 + i;
+                for (int x = tid; x < DV; x += kThreads) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kRows; ++w) acc += sm.red[buf][w][x];
+                    atomicAdd(p.dv_acc + t * DV + x, acc);
+                }
+                buf ^= 1;
+            }
+        }
+        __syncthreads();
+        IO* dqo = static_cast<IO*>(p.dq);
+        IO* dko = static_cast<IO*>(p.dk);
+        for (int x = tid; x < n * kRows; x += kThreads) {
+            const int i = x / kRows, w = x % kRows;
+            const size_t e = (tok0 + t0 + i) * DK + rb * kRows + w;
+            st_io(dqo, e, sm.dq[i][w]);
+            st_io(dko, e, sm.dk[i][w]);
+        }
+    }
+    if (p.dstate_in) {
+#pragma unroll
+        for (int j = 0; j < NC; ++j) p.dstate_in[bh * ssz + static_cast<size_t>(r) * DV + c0 + j] = G[j];
+        if (lane == 0) p.dstate_in[bh * ssz + static_cast<size_t>(DK) * DV + r] = gz;
+    }
+    if (DECAY) {
+        gacc = warp_sum(gacc);
+        if (lane == 0) sm.gsum[warp] = gacc;
+        __syncthreads();
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w = 0; w < kRows; ++w) t += sm.gsum[w];
+            atomicAdd(p.dgate + bh, t);
+        }
+    }
+}
+
+template <int DK, int DV, typename IO, bool DECAY>
+cudaError_t run_norm_rows(const DeltaBwdArgs& p, cudaStream_t s) {
+    auto kern = norm_rows_backward_kernel<DK, DV, IO, DECAY>;
+    constexpr size_t smem = sizeof(SmemNorm<DV>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<p.BH * (DK / kRows), kThreads, smem, s>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t n = static_cast<size_t>(p.BH) * p.T * DV;
+    write_v_kernel<IO><<<p.sm_count * 4, 256, 0, s>>>(p.dv_acc, static_cast<IO*>(p.dv), n);
+    return cudaGetLastError();
+}
+
+template <int DK, int DV>
+cudaError_t run_norm_rows_io(const DeltaBwdArgs& p, cudaStream_t s) {
+    const bool decay = p.gate != nullptr;
+    if (decay)
+        return p.io == kBf16 ? run_norm_rows<DK, DV, __nv_bfloat16, true>(p, s) : run_norm_rows<DK, DV, float, true>(p, s);
+    return p.io == kBf16 ? run_norm_rows<DK, DV, __nv_bfloat16, false>(p, s) : run_norm_rows<DK, DV, float, false>(p, s);
+}
+
+cudaError_t run_norm_rows_dims(const DeltaBwdArgs& p, cudaStream_t s) {
+    if (p.dk_dim == 64 && p.dv_dim == 64) return run_norm_rows_io<64, 64>(p, s);
+    if (p.dk_dim == 64 && p.dv_dim == 128) return run_norm_rows_io<64, 128>(p, s);
+    if (p.dk_dim == 128 && p.dv_dim == 64) return run_norm_rows_io<128, 64>(p, s);
+    if (p.dk_dim == 128 && p.dv_dim == 128) return run_norm_rows_io<128, 128>(p, s);
+    return cudaErrorInvalidValue;
+}
+
 // dq and dk from the fp32 accumulators, in the io dtype.
 template <typename IO>
 __global__ void write_qk_kernel(const float* dq_acc, const float* dk_acc, IO* dq, IO* dk, size_t n) {
@@ -476,6 +706,17 @@ cudaError_t run_dims(const DeltaBwdArgs& p, cudaStream_t s) {
 
 }  // namespace
 
+size_t norm_rows_fwd_bytes(int BH, int T, int dv, int io) {
+    const size_t o = (static_cast<size_t>(BH) * T * dv * (io == kBf16 ? 2 : 4) + 255) & ~static_cast<size_t>(255);
+    const size_t den = (static_cast<size_t>(BH) * T * 4 + 255) & ~static_cast<size_t>(255);
+    return o + den;
+}
+
+size_t norm_rows_bytes(int BH, int T, int dk, int dv) {
+    const size_t nseg = static_cast<size_t>((T + kSeg - 1) / kSeg);
+    return static_cast<size_t>(BH) * (nseg * dk * (dv + 1) + static_cast<size_t>(T) * dv) * sizeof(float);
+}
+
 size_t delta_backward_bytes(int BH, int T, int dk, int dv, bool gla) {
     const size_t nseg = static_cast<size_t>((T + kSeg - 1) / kSeg);
     const size_t acc = gla ? static_cast<size_t>(T) * dv : 2 * static_cast<size_t>(T) * dk;
@@ -487,6 +728,14 @@ cudaError_t launch_delta_backward(const DeltaBwdArgs& args, cudaStream_t s) {
     DeltaBwdArgs a = args;
     const size_t nseg = static_cast<size_t>((a.T + kSeg - 1) / kSeg);
     a.ckpt = a.workspace;
+    if (a.norm) {   // rows and z at every segment start, then the fp32 total of dv
+        a.ckz = a.ckpt + static_cast<size_t>(a.BH) * nseg * a.dk_dim * a.dv_dim;
+        a.dv_acc = a.ckz + static_cast<size_t>(a.BH) * nseg * a.dk_dim;
+        cudaError_t e = cudaMemsetAsync(a.dv_acc, 0, static_cast<size_t>(a.BH) * a.T * a.dv_dim * sizeof(float), s);
+        if (e == cudaSuccess && a.gate && a.dgate) e = cudaMemsetAsync(a.dgate, 0, static_cast<size_t>(a.BH) * sizeof(float), s);
+        if (e != cudaSuccess) return e;
+        return run_norm_rows_dims(a, s);
+    }
     if (a.gla) {   // rows at every segment start, then the fp32 total of dv
         a.dv_acc = a.ckpt + static_cast<size_t>(a.BH) * nseg * a.dv_dim * a.dk_dim;
         cudaError_t e = cudaMemsetAsync(a.dv_acc, 0, static_cast<size_t>(a.BH) * a.T * a.dv_dim * sizeof(float), s);

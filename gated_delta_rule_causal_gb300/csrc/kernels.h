@@ -86,7 +86,11 @@ struct DeltaBwdArgs {
     int io;                    // Io
     bool per_channel;
     bool gla;                  // per-channel gated recurrence (no beta; rows = key channels)
+    bool norm;                 // normalized recurrence (rows = key channels; gate: one decay per
+                               // sequence-head or NULL; dgate [BH] or NULL)
     bool identity_phi;         // gla without the feature map
+    const void* fwd_out;       // norm: the forward's outputs [BH][T][dv] (io dtype)
+    const float* fwd_den;      // norm: the forward's normalizers [BH][T]
     int sm_count;
     float* workspace;          // delta_backward_bytes(BH, T, dk, dv) bytes
     // carved from the workspace by the launch: rows at every segment start,
@@ -94,12 +98,17 @@ struct DeltaBwdArgs {
     float* ckpt;
     float* dq_acc;
     float* dk_acc;
-    float* dv_acc;             // gla: fp32 total of dv
+    float* dv_acc;             // gla, norm: fp32 total of dv
+    float* ckz;                // norm: z at every segment start
 };
 
-// Workspace bytes launch_delta_backward needs (checkpoints + accumulators).
+// Workspace bytes launch_delta_backward needs (checkpoints + accumulators;
+// norm: the caller places the forward's outputs and normalizers first, see
+// norm_rows_fwd_bytes).
 size_t delta_backward_bytes(int BH, int T, int dk, int dv, bool gla);
-// Token-serial CUDA-core kernel, rows split over CTAs (see backward_delta.cu);
+size_t norm_rows_bytes(int BH, int T, int dk, int dv);
+size_t norm_rows_fwd_bytes(int BH, int T, int dv, int io);
+// Token-serial CUDA-core kernel, rows split over CTAs (see backward_rows.cu);
 // d_k, d_v in {64, 128}.
 cudaError_t launch_delta_backward(const DeltaBwdArgs& a, cudaStream_t s);
 

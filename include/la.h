@@ -267,8 +267,9 @@ void la_destroy(la_handle* h);
 const char* la_last_error(const la_handle* h);
 
 /*
- * Backward of the prefill (LA_NORM_ELU1 only; d_k, d_v in {16, 32, 64}; bf16
- * or fp32 io). Given the same q, k, v, state_in as a forward call and the
+ * Backward of the prefill (LA_NORM_ELU1 only; d_k, d_v both in {16, 32, 64}
+ * or both in {64, 128}; bf16 or fp32 io; the fixed-decay form's gradients
+ * are in la_backward_gated). Given the same q, k, v, state_in as a forward call and the
  * gradients of its outputs (dout [B,H,T,d_v], io dtype) and, optionally, of
  * its final state (dstate_out, fp32, S then z as above; NULL means zero),
  * writes the gradients dq, dk [B,H,T,d_k], dv [B,H,T,d_v] (io dtype) and,
@@ -278,15 +279,19 @@ const char* la_last_error(const la_handle* h);
  * x > 0, e^x otherwise).
  * bf16 io with d_k = d_v = 64: the chunkwise tensor-core form (chunks of 64
  * tokens), five kernels per group of sequence-heads whose per-chunk states
- * fit the handle's workspace (about 50 KB per chunk of each sequence-head):
+ * fit the handle's workspace (about 41 KB per chunk of each sequence-head):
  * the states entering every chunk, per-chunk normalizer gradients, a reverse
  * scan of the state gradient, and the per-chunk input gradients. Other
- * shapes, fp32 io, or a single sequence-head whose chunk states exceed the
- * workspace: one CUDA-core kernel that runs the recurrence forward to the
- * final state, then backward, recovering earlier states by subtracting each
- * token's update, so its fp32 rounding grows with T. la_last_launches tells
- * which ran (a multiple of 5, or 1). An expired bounded wait in the
- * chunkwise kernels is reported by la_status.
+ * shapes with d_k, d_v in {64, 128} (fp32 io, d = 128, or a single
+ * sequence-head whose chunk states exceed the workspace): a forward call
+ * (its outputs and normalizers into the backward workspace), then the
+ * token-serial row kernel of la_backward_gated (key channels as rows,
+ * checkpoints every 16 tokens). d_k, d_v in {16, 32}: one CUDA-core kernel
+ * per sequence-head that runs the recurrence forward to the final state,
+ * then backward, recovering earlier states by subtracting each token's
+ * update, so its fp32 rounding grows with T. la_last_launches tells which
+ * ran (a multiple of 5; the forward's launches + 2; or 1). An expired
+ * bounded wait in the chunkwise kernels is reported by la_status.
  * Errors as for la_forward: LA_ERR_UNSUPPORTED for another variant or head
  * size, LA_ERR_INVALID_ARG, LA_ERR_MISALIGNED, LA_ERR_CUDA.
  */
@@ -297,8 +302,11 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
 
 /*
  * Backward of the prefill of the gated delta rule (LA_GDN), of its
- * per-channel-decay form (LA_KDA) and of the per-channel gated variant
- * (LA_GLA); d_k, d_v in {64, 128}; bf16 or fp32 io.
+ * per-channel-decay form (LA_KDA), of the per-channel gated variant (LA_GLA)
+ * and of the normalized variant with a fixed decay per sequence-head
+ * (LA_NORM_DECAY: gate [B,H], dgate [B,H], state S then z as in la_forward;
+ * a forward call runs first, as for la_backward's larger heads); d_k, d_v in
+ * {64, 128}; bf16 or fp32 io.
  * Given the forward call's q, k, v, gate, beta and state_in (same layouts as
  * la_forward: gate [B,H,T] for LA_GDN, [B,H,T,d_k] for LA_KDA and LA_GLA; beta
  * [B,H,T]; state_in [B,H,d_v*d_k] fp32 or NULL for zero), the gradient of
@@ -311,9 +319,9 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
  * (S~ = S Diag(a), u = beta (v - S~ k), S = S~ + u k^T, o = S q) and, for
  * LA_GLA, through S_t = diag(gamma_t) S_{t-1} + phi(k_t) v_t^T,
  * o_t = S_t^T phi(q_t) (phi = elu + 1, the identity under
- * LA_FLAG_IDENTITY_PHI). LA_GLA takes no beta: beta and dbeta may be NULL
- * and are ignored; its state_in, dstate_out and dstate_in are
- * [B,H,d_k*d_v] (S [d_k][d_v]).
+ * LA_FLAG_IDENTITY_PHI). LA_GLA and LA_NORM_DECAY take no beta: beta and
+ * dbeta may be NULL and are ignored; LA_GLA's state_in, dstate_out and
+ * dstate_in are [B,H,d_k*d_v] (S [d_k][d_v]).
  * Token-serial CUDA-core kernel: the state's value rows (LA_GLA: its key
  * channels) are split over CTAs of 16 rows, run forward with checkpoints
  * every 16 tokens, then walked back segment by segment; sums over rows are

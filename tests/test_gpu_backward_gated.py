@@ -16,6 +16,7 @@ la = pytest.importorskip("gated_delta_rule_causal_gb300")
 
 def _workload(variant, B, H, T, d, io):
     base = {"gdn": W.GDN_B2H16_T8192_D128, "gla": W.GLA_B4H16_T4096_D128,
+            "norm_decay": W.NORM_DECAY_B4H8_T2048_D64,
             "kda": W.KDA_DECODE_N256H16_D128.with_(B=4, H=16, T=2048, decode_steps=0, state_std=0.0)}[variant]
     return W.small(base, B=B, H=H, T=T, dk=d, dv=d).with_(io=io)
 
@@ -27,10 +28,12 @@ def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True, flag
     inp = W.draw(w, seed)
     q, k, v, g, b = oracle_inputs(inp)
     rng = np.random.default_rng(seed + 1000)
-    ss = d * d
+    ss = d * d + (d if variant == "norm_decay" else 0)
     do_s = W.round_io(rng.standard_normal((B, H, T, d)), io)
     do64 = W.as_f64(do_s)
     sin = (rng.standard_normal((B, H, ss)) * 0.1).astype(np.float32) if with_state else None
+    if sin is not None and variant == "norm_decay":   # a positive normalizer state
+        sin[..., d * d:] = np.abs(sin[..., d * d:]) * 50 + 1.0
     dso = (rng.standard_normal((B, H, ss)) * 0.05).astype(np.float32) if with_dstate else None
     h = la.Handle(B, H, d, d, io=io, flags=flags)
     dev = h.device
@@ -38,15 +41,19 @@ def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True, flag
     got = h.backward_gated(to_torch(inp.q, dev), to_torch(inp.k, dev), to_torch(inp.v, dev),
                            to_torch(inp.gate, dev), to_torch(inp.beta, dev), to_torch(do_s, dev), t(sin), t(dso),
                            variant=variant)
-    if variant == "gla":
+    if variant in ("gla", "norm_decay"):
         assert got[4] is None
         got = got[:4] + got[5:]
     torch.cuda.synchronize()
-    assert h.last_launches() == 2
+    # two launches of the row kernel and its conversion (norm_decay: after the forward's)
+    assert h.last_launches() == 2 if variant != "norm_decay" else h.last_launches() >= 3
     assert h.status() == la.LA_OK
     h.close()
     if variant == "gla":
         ref = backward.gla_backward(q, k, v, g, do64, sin, dso, identity_phi=bool(flags & la.LA_FLAG_IDENTITY_PHI))
+    elif variant == "norm_decay":
+        rq, rk, rv, rs, rg = backward.norm_decay_backward(q, k, v, g, do64, sin, dso)
+        ref = (rq, rk, rv, rg, rs)
     else:
         ref = backward.delta_backward(q, k, v, g, b, do64, sin, dso)
     return [x.float().cpu().numpy() for x in got], ref
@@ -57,15 +64,15 @@ NAMES_GLA = ("dq", "dk", "dv", "dgate", "dstate_in")
 
 
 def names(variant):
-    return NAMES_GLA if variant == "gla" else NAMES
+    return NAMES_GLA if variant in ("gla", "norm_decay") else NAMES
 
 
-@pytest.mark.parametrize("variant", ["gdn", "kda", "gla"])
+@pytest.mark.parametrize("variant", ["gdn", "kda", "gla", "norm_decay"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("io", ["bf16", "fp32"])
 @pytest.mark.parametrize("T", [1, 37, 200])
 def test_backward_gated_parity(variant, d, io, T):
-    got, ref = _case(variant, 1, 2, T, d, io, seed=T + d + {"gdn": 0, "kda": 7, "gla": 13}[variant])
+    got, ref = _case(variant, 1, 2, T, d, io, seed=T + d + {"gdn": 0, "kda": 7, "gla": 13, "norm_decay": 19}[variant])
     for name, x, r in zip(names(variant), got, ref):
         assert x.shape == r.shape, name
         assert np.all(np.isfinite(x)), name
@@ -79,7 +86,7 @@ def test_backward_gated_optional_states(with_state, with_dstate):
         assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
 
 
-@pytest.mark.parametrize("variant", ["gdn", "kda", "gla"])
+@pytest.mark.parametrize("variant", ["gdn", "kda", "gla", "norm_decay"])
 def test_backward_gated_long_sequence(variant):
     # 2048 tokens: 128 segments walked back through their checkpoints
     got, ref = _case(variant, 1, 2, 2048, 64, "bf16", seed=17)
