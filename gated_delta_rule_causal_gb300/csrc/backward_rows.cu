@@ -56,7 +56,7 @@ namespace la {
 namespace {
 
 constexpr int kRows = 16;             // value rows per CTA (one warp each)
-constexpr int kSeg = 16;              // tokens per recomputed segment
+constexpr int kSeg = 8;               // tokens per recomputed segment
 constexpr int kThreads = kRows * 32;
 
 template <typename T> __device__ __forceinline__ float ld_io(const T* p, size_t i);
@@ -96,7 +96,7 @@ struct Smem {
 };
 
 template <int DK, int DV, bool PC, typename IO>
-__global__ void __launch_bounds__(kThreads, 1) delta_backward_kernel(DeltaBwdArgs p) {
+__global__ void __launch_bounds__(kThreads, 2) delta_backward_kernel(DeltaBwdArgs p) {
     constexpr int NC = DK / 32;   // columns per lane
     constexpr int NRB = DV / kRows;
     using SM = Smem<DK, PC>;
@@ -272,7 +272,7 @@ struct SmemGla {
 };
 
 template <int DK, int DV, typename IO, bool IDPHI>
-__global__ void __launch_bounds__(kThreads, 1) gla_backward_kernel(DeltaBwdArgs p) {
+__global__ void __launch_bounds__(kThreads, 2) gla_backward_kernel(DeltaBwdArgs p) {
     constexpr int NC = DV / 32;   // value columns per lane
     constexpr int NRB = DK / kRows;
     using SM = SmemGla<DV>;
@@ -466,7 +466,7 @@ struct SmemNorm {
 };
 
 template <int DK, int DV, typename IO, bool DECAY>
-__global__ void __launch_bounds__(kThreads, 1) norm_rows_backward_kernel(DeltaBwdArgs p) {
+__global__ void __launch_bounds__(kThreads, 2) norm_rows_backward_kernel(DeltaBwdArgs p) {
     constexpr int NC = DV / 32;
     constexpr int NRB = DK / kRows;
     using SM = SmemNorm<DV>;
@@ -498,14 +498,15 @@ __global__ void __launch_bounds__(kThreads, 1) norm_rows_backward_kernel(DeltaBw
             if (bwd) sm.dnum[i][c] = in ? ld_io(dout, e) / p.fwd_den[tok0 + t0 + i] : 0.f;
         }
         if (bwd) {   // warp i: dden of token i
-            const int i = warp;
-            float d = 0.f;
-            if (i < n) {
-                const size_t e = (tok0 + t0 + i) * DV;
-                for (int c = lane; c < DV; c += 32) d += ld_io(dout, e + c) * ld_io(o, e + c);
+            for (int i = warp; i < kSeg; i += kRows) {
+                float d = 0.f;
+                if (i < n) {
+                    const size_t e = (tok0 + t0 + i) * DV;
+                    for (int c = lane; c < DV; c += 32) d += ld_io(dout, e + c) * ld_io(o, e + c);
+                }
+                d = warp_sum(d);
+                if (lane == 0) sm.dden[i] = (i < n) ? -d / p.fwd_den[tok0 + t0 + i] : 0.f;
             }
-            d = warp_sum(d);
-            if (lane == 0) sm.dden[i] = (i < n) ? -d / p.fwd_den[tok0 + t0 + i] : 0.f;
         }
         for (int x = tid; x < kSeg * kRows; x += kThreads) {
             const int i = x / kRows, w = x % kRows;
@@ -521,7 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1) norm_rows_backward_kernel(DeltaBw
             }
         }
     };
-    static_assert(kSeg == kRows, "one warp per token of a segment for dden");
     auto step = [&](int i, float* s, float& z) {
         const float f = sm.f[i][warp];
 #pragma unroll

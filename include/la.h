@@ -286,7 +286,7 @@ const char* la_last_error(const la_handle* h);
  * sequence-head whose chunk states exceed the workspace): a forward call
  * (its outputs and normalizers into the backward workspace), then the
  * token-serial row kernel of la_backward_gated (key channels as rows,
- * checkpoints every 16 tokens). d_k, d_v in {16, 32}: one CUDA-core kernel
+ * checkpoints every 8 tokens). d_k, d_v in {16, 32}: one CUDA-core kernel
  * per sequence-head that runs the recurrence forward to the final state,
  * then backward, recovering earlier states by subtracting each token's
  * update, so its fp32 rounding grows with T. la_last_launches tells which
@@ -324,10 +324,10 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
  * dstate_in are [B,H,d_k*d_v] (S [d_k][d_v]).
  * Token-serial CUDA-core kernel: the state's value rows (LA_GLA: its key
  * channels) are split over CTAs of 16 rows, run forward with checkpoints
- * every 16 tokens, then walked back segment by segment; sums over rows are
+ * every 8 tokens, then walked back segment by segment; sums over rows are
  * accumulated in fp32 (the order of those additions varies from run to run,
  * so the last bits of dq, dk, dgate and dbeta, or of LA_GLA's dv, may too).
- * Its workspace (4 * B*H * (ceil(T/16) * d_v*d_k + 2*T*d_k) bytes; LA_GLA:
+ * Its workspace (4 * B*H * (ceil(T/8) * d_v*d_k + 2*T*d_k) bytes; LA_GLA:
  * T*d_v in place of 2*T*d_k) is allocated by the handle on first use and
  * grown when a call needs more (la_destroy frees it). la_last_launches reports 2 (plus
  * memsets of the accumulated outputs, not counted).
