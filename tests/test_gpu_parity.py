@@ -359,16 +359,18 @@ def test_forward_host_parity(variant, H, T, chunk):
     h.close()
 
 
-@pytest.mark.parametrize("variant,d,H,T", [("gdn", 128, 12, 6000), ("norm", 64, 24, 8192), ("gla", 128, 16, 3000)])
-def test_forward_host_large_call_parity(variant, d, H, T):
+@pytest.mark.parametrize("variant,d,H,T,io", [("gdn", 128, 12, 6000, "bf16"), ("norm", 64, 24, 8192, "bf16"),
+                                             ("gla", 128, 16, 3000, "bf16"), ("norm_decay", 64, 24, 8192, "bf16"),
+                                             ("kda", 64, 16, 5000, "fp32")])
+def test_forward_host_large_call_parity(variant, d, H, T, io):
     # A call that moves 64 MiB or more over the host link runs as 4 time
     # segments of every sequence-head (multiples of 64 tokens), moved by the
     # copy engines, the state handed from segment to segment on the device;
     # every head against the oracle.
-    w = base(variant, d).with_(B=1, H=H, T=T)
+    w = base(variant, d).with_(B=1, H=H, T=T, io=io)
     inp = W.draw(w, seed=T + H)
     moved = sum(a.nbytes for a in (inp.q, inp.k, inp.v, inp.gate, inp.beta) if a is not None)
-    moved += w.B * w.H * w.T * w.dv * 2 + w.B * w.H * oracle.state_size(variant, w.dk, w.dv) * 4
+    moved += w.B * w.H * w.T * w.dv * (2 if io == "bf16" else 4) + w.B * w.H * oracle.state_size(variant, w.dk, w.dv) * 4
     assert moved >= 64 << 20
     pin = lambda a: None if a is None else to_torch(a, "cpu").pin_memory()
     rng = np.random.default_rng(H)
