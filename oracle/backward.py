@@ -276,6 +276,121 @@ def delta_backward(q, k, v, decay, beta, do, state_in=None, dstate_out=None):
     return dq, dkk, dvv, dgate, db, D.reshape(B, H, dv * dk)
 
 
+def delta_backward_chunked(q, k, v, g, beta, do, C=64, state_in=None, dstate_out=None):
+    """The same gradients as ``delta_backward`` for a scalar gate, by chunks
+    of C tokens: the form a chunkwise backward computes. Inside a chunk
+    (rows r, s; b_r = sum of log g up to r, gam_r = e^{b_r}, gam_C and b_C
+    those of its last token, lam_s = gam_C / gam_s, E_rs = e^{b_r - b_s}) the
+    forward is the WY/UT chunk form of the rule ("Beyond attention" §18.2):
+
+        A  = strictly lower (diag(beta) o E o K K^T),   Ti = (I + A)^{-1}
+        W  = Ti diag(beta gam) K,   Ut = Ti diag(beta) V,   U = Ut - W S_0^T
+        P  = lower (E o Q K^T),     O  = diag(gam) Q S_0^T + P U
+        S_C = gam_C S_0 + U^T diag(lam) K
+
+    so that, across chunks, both the state and its gradient follow one linear
+    map X <- gam_C X - (X A'^T) B' + C'^T D' per chunk:
+    forward S with (A', B', C', D') = (W, lam K, Ut, lam K), backward dS (from
+    the last chunk) with (K, lam W, dO, Qh), Qh = diag(gam) Q - P W. With S_0
+    and dS_C (the gradient reaching the chunk's last state) known, the chain
+    rule through those four lines gives, per chunk:
+
+        dU  = P^T dO + diag(lam) K dS_C^T,    dW = -dU S_0
+        dRv = Ti^T dU,   dRk = Ti^T dW,       dA = -(dRv Ut^T + dRk W^T)  (strictly lower)
+        dV  = diag(beta) dRv
+        dP  = lower (dO U^T)
+        dQ  = diag(gam) dO S_0 + (dP o E) K
+        dK  = (dP o E)^T Q + diag(beta gam) dRk + F K + F^T K + diag(lam) U dS_C,
+              F = diag(beta) (dA o E)
+        dbeta_r = dRv_r . v_r + gam_r dRk_r . k_r + sum_s (dA o E o K K^T)_rs
+        db_r    = gam_r dO_r . (S_0 q_r) + beta_r gam_r dRk_r . k_r
+                  + rows minus columns of (dP o P) and of (dA o A)
+                  (+ at the last token: gam_C <dS_C, S_0> + sum_s c_s, and
+                  - c_s at s, c_s = lam_s (U dS_C)_s . k_s)
+        dlog g_t = sum_{r >= t} db_r (inside the chunk),   dg = dlog g / g
+
+    Padded rows of a ragged last chunk have k = q = v = do = 0, beta = 0 and
+    g = 1, which leaves every real row unchanged. q, k [B,H,T,dk]; v, do
+    [B,H,T,dv]; g, beta [B,H,T]; states [B,H,dv*dk] or None. Returns
+    (dq, dk, dv, dg, dbeta, dstate_in) in float64.
+    """
+    q, k, v, do = (np.asarray(a, np.float64) for a in (q, k, v, do))
+    g = np.asarray(g, np.float64)
+    bt = np.asarray(beta, np.float64)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    nch = (T + C - 1) // C
+    Tp = nch * C
+    pad = lambda a, fill=0.0: np.concatenate(
+        [a, np.full(a.shape[:2] + (Tp - T,) + a.shape[3:], fill)], axis=2) if Tp > T else a
+    Q, K, V, dO = (pad(a).reshape(B, H, nch, C, -1) for a in (q, k, v, do))
+    lg = pad(np.log(g)).reshape(B, H, nch, C)
+    be = pad(bt).reshape(B, H, nch, C)
+    ein = np.einsum
+    # per chunk, independent of the state
+    b = np.cumsum(lg, axis=-1)
+    gam = np.exp(b)
+    gC = gam[..., -1]
+    lam = np.exp(b[..., -1:] - b)
+    E = np.exp(b[..., :, None] - b[..., None, :])
+    lower = np.tril(np.ones((C, C)))
+    strict = np.tril(np.ones((C, C)), -1)
+    KK = ein("...rk,...sk->...rs", K, K)
+    A = strict * be[..., :, None] * E * KK
+    Ti = np.linalg.inv(np.eye(C) + A)
+    W = ein("...rs,...sk->...rk", Ti, (be * gam)[..., None] * K)
+    Ut = ein("...rs,...sv->...rv", Ti, be[..., None] * V)
+    P = lower * E * ein("...rk,...sk->...rs", Q, K)
+    Qh = gam[..., None] * Q - ein("...rs,...sk->...rk", P, W)
+    lK, lW = lam[..., None] * K, lam[..., None] * W
+
+    def chain(X, c, a_, b_, c_, d_):
+        # X <- gam_C X - (X a_^T) b_ + c_^T d_   for chunk c
+        Y = ein("bhik,bhrk->bhir", X, a_[:, :, c])
+        return (gC[:, :, c, None, None] * X - ein("bhir,bhrk->bhik", Y, b_[:, :, c])
+                + ein("bhri,bhrk->bhik", c_[:, :, c], d_[:, :, c]))
+
+    S0 = np.empty((B, H, nch, dv, dk))
+    X = np.zeros((B, H, dv, dk)) if state_in is None else np.asarray(state_in, np.float64).reshape(B, H, dv, dk)
+    for c in range(nch):
+        S0[:, :, c] = X
+        X = chain(X, c, W, lK, Ut, lK)
+    dSC = np.empty((B, H, nch, dv, dk))
+    X = np.zeros((B, H, dv, dk)) if dstate_out is None else np.asarray(dstate_out, np.float64).reshape(B, H, dv, dk)
+    for c in range(nch - 1, -1, -1):
+        dSC[:, :, c] = X
+        X = chain(X, c, K, lW, dO, Qh)
+    dstate_in = X.reshape(B, H, dv * dk)
+    # per chunk, with S_0 and dS_C
+    U = Ut - ein("...rk,...ik->...ri", W, S0)
+    dU = ein("...rs,...ri->...si", P, dO) + lam[..., None] * ein("...rk,...ik->...ri", K, dSC)
+    dWm = -ein("...ri,...ik->...rk", dU, S0)
+    dRv = ein("...sr,...si->...ri", Ti, dU)
+    dRk = ein("...sr,...sk->...rk", Ti, dWm)
+    dA = -strict * (ein("...ri,...si->...rs", dRv, Ut) + ein("...rk,...sk->...rs", dRk, W))
+    dP = lower * ein("...ri,...si->...rs", dO, U)
+    dPE = dP * E
+    F = be[..., :, None] * dA * E
+    dS0q = ein("...ri,...ik->...rk", dO, S0)            # dO S_0
+    dQ = gam[..., None] * dS0q + ein("...rs,...sk->...rk", dPE, K)
+    US = ein("...ri,...ik->...rk", U, dSC)               # U dS_C
+    dK = (ein("...rs,...rk->...sk", dPE, Q) + (be * gam)[..., None] * dRk
+          + ein("...rs,...sk->...rk", F, K) + ein("...rs,...rk->...sk", F, K) + lam[..., None] * US)
+    dV = be[..., None] * dRv
+    rk = ein("...rk,...rk->...r", dRk, K)
+    dbeta = ein("...rv,...rv->...r", dRv, V) + gam * rk + (dA * E * KK).sum(-1)
+    dPP, dAA = dP * P, dA * A
+    db = (gam * ein("...rk,...rk->...r", dS0q, Q) + be * gam * rk
+          + dPP.sum(-1) - dPP.sum(-2) + dAA.sum(-1) - dAA.sum(-2))
+    cs = lam * ein("...rk,...rk->...r", US, K)
+    db = db - cs
+    db[..., -1] += gC * ein("...ik,...ik->...", dSC, S0) + cs.sum(-1)
+    dlg = np.flip(np.cumsum(np.flip(db, -1), -1), -1)
+    unpad = lambda a: a.reshape((B, H, Tp) + a.shape[4:])[:, :, :T]
+    dg = unpad(dlg) / g
+    return unpad(dQ), unpad(dK), unpad(dV), dg, unpad(dbeta), dstate_in
+
+
 def gla_backward(q, k, v, gamma, do, state_in=None, dstate_out=None, identity_phi=False):
     """Gradients of the per-channel gated recurrence (GLA / RetNet family,
     "Linear attention and Hyena" §11.3), S in R^{dk x dv}:

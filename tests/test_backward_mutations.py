@@ -56,6 +56,22 @@ MUTANTS_DELTA = {
 }
 
 
+# planted in delta_backward_chunked (scalar gate, by chunks)
+MUTANTS_CHUNKED = {
+    "pair_gradient_without_transposed_term": ('+ ein("...rs,...sk->...rk", F, K) + ein("...rs,...rk->...sk", F, K)',
+                                              '+ ein("...rs,...sk->...rk", F, K)'),
+    "state_chain_without_decay": ("return (gC[:, :, c, None, None] * X", "return (X"),
+    "pseudo_value_weight_gradient_sign": ("dWm = -ein(", "dWm = ein("),
+    "dbeta_without_pair_term": (" + (dA * E * KK).sum(-1)", ""),
+    "gate_drops_carried_state_term": ('db[..., -1] += gC * ein("...ik,...ik->...", dSC, S0) + cs.sum(-1)',
+                                      "db[..., -1] += cs.sum(-1)"),
+    "inclusive_mask_in_solve": ("A = strict * be", "A = lower * be"),
+    "gate_prefix_sum_not_reversed": ("dlg = np.flip(np.cumsum(np.flip(db, -1), -1), -1)", "dlg = np.cumsum(db, -1)"),
+    "gradient_chain_without_intra_chunk_output": ('Qh = gam[..., None] * Q - ein("...rs,...sk->...rk", P, W)',
+                                                  "Qh = gam[..., None] * Q"),
+}
+
+
 # planted in gla_backward (per-channel gated attention)
 MUTANTS_GLA = {
     "gate_gradient_against_new_state": ('dg[:, :, t] = np.einsum("bhkv,bhkv->bhk", D, S[:, :, t])',
@@ -247,6 +263,33 @@ def test_delta_mutant_is_caught(name, delta_cases):
     mod = _load(head + body.replace(old, new))
     # caught when it disagrees with the finite differences on either decay
     assert not all(_agrees_delta(mod, c) for c in delta_cases.values()), name
+
+
+def _agrees_chunked(mod, case, C):
+    (q, k, v, a, b, W, sin, Ws), fd = case
+    got = mod.delta_backward_chunked(q, k, v, a, b, W, C, sin, Ws)
+    return all(np.allclose(gr, f, rtol=1e-6, atol=1e-6) for gr, f in zip(got, fd))
+
+
+def test_unmutated_delta_backward_chunked_agrees(delta_cases):
+    with open(SRC) as fh:
+        mod = _load(fh.read())
+    for C in (2, 4):
+        assert _agrees_chunked(mod, delta_cases["gdn"], C)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS_CHUNKED))
+def test_delta_chunked_mutant_is_caught(name, delta_cases):
+    old, new = MUTANTS_CHUNKED[name]
+    with open(SRC) as fh:
+        text = fh.read()
+    i = text.index("def delta_backward_chunked(")
+    j = text.index("def gla_backward(")
+    head, body, tail = text[:i], text[i:j], text[j:]
+    assert body.count(old) == 1, name
+    mod = _load(head + body.replace(old, new) + tail)
+    # caught when either chunk size (both leave a ragged last chunk) disagrees
+    assert not all(_agrees_chunked(mod, delta_cases["gdn"], C) for C in (2, 4)), name
 
 
 @pytest.fixture(scope="module")

@@ -690,6 +690,22 @@ def test_delta_backward_uniform_channels_is_scalar_gate():
     assert np.allclose(s[3], c[3].sum(-1), rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("C,T", [(4, 13), (8, 16), (16, 37), (64, 130)])
+def test_delta_backward_chunked_equals_token_by_token(C, T):
+    # The chunkwise form of the scalar-gate gradients (per-chunk UT inverse,
+    # the state and its gradient carried by chunks) equals the token-by-token
+    # reverse recurrence, which the finite-difference pin above holds to the C
+    # forward oracle: ragged tail, start state and final-state cotangent included.
+    from oracle import backward
+    q, k, v, a, b, sin, W, Ws = _delta_case(rng(103 + C), False, B=2, H=1, T=T, dk=6, dv=5)
+    a = 1.0 / (1.0 + np.exp(-(rng(107).standard_normal(a.shape) + 1.0)))   # gates down to ~0.05
+    x = backward.delta_backward(q, k, v, a, b, W, sin, Ws)
+    y = backward.delta_backward_chunked(q, k, v, a, b, W, C, sin, Ws)
+    for name, u, w in zip(("dq", "dk", "dv", "dg", "dbeta", "dstate_in"), x, y):
+        assert u.shape == w.shape, name
+        assert np.allclose(u, w, rtol=1e-11, atol=1e-12), (name, np.abs(u - w).max())
+
+
 # ------------------------------------------------------------- gradients of (b)
 
 @pytest.mark.parametrize("identity_phi", [False, True])
