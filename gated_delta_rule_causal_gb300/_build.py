@@ -20,7 +20,7 @@ LIB = os.path.join(BUILD, "liblacausal.so")
 SOURCES = ["api.cu", "recurrent.cu", "decode.cu", "prefill.cu",
            "prefill_norm.cu", "prefill_gdn.cu", "prefill_par.cu",
            "prefill_seg.cu", "noalloc.cu", "backward.cu", "backward_chunk.cu",
-           "backward_rows.cu"]
+           "backward_rows.cu", "backward_gdn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
          "-I" + os.path.join(ROOT, "include")]

@@ -838,7 +838,10 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
         return norm_rows_backward(h, q, k, v, gate, state_in, dout, dstate_out, dq, dk, dv, dgate, dstate_in,
                                   LA_NORM_DECAY, T, static_cast<cudaStream_t>(cuda_stream));
     const int BH = c.B * c.H;
-    const int grc = grow_bws(h, la::delta_backward_bytes(BH, T, c.d_k, c.d_v, gla));
+    // the scalar-gate rule in bf16 with square heads: chunkwise kernels
+    const bool chunked = variant == LA_GDN && c.io == LA_BF16 && c.d_k == c.d_v;
+    const int grc = grow_bws(h, chunked ? la::gdn_chunk_backward_bytes(BH, T, c.d_k)
+                                        : la::delta_backward_bytes(BH, T, c.d_k, c.d_v, gla));
     if (grc != LA_OK) return grc;
     la::DeltaBwdArgs a = {};
     a.q = q;
@@ -870,6 +873,12 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
     }
     a.sm_count = h->sm_count;
     a.workspace = h->d_bws;
+    if (chunked) {
+        const cudaError_t e = la::launch_gdn_chunk_backward(a, static_cast<cudaStream_t>(cuda_stream));
+        if (e != cudaSuccess) return cuda_fail(h, e, "gated backward launch");
+        h->last_launches = 5;   // prep, the two chunk chains, the two gradient kernels
+        return LA_OK;
+    }
     const cudaError_t e = la::launch_delta_backward(a, static_cast<cudaStream_t>(cuda_stream));
     if (e != cudaSuccess) return cuda_fail(h, e, "gated backward launch");
     h->last_launches = 2;   // the token-serial kernel and the dq / dk conversion
