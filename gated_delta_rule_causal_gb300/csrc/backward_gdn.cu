@@ -35,7 +35,8 @@
 // Five launches per call:
 //  1. prep, one CTA per (sequence-head, chunk): gate prefix sums, K K^T and
 //     Q K^T, Ti in fp32 (16x16 diagonal blocks by forward substitution, then
-//     two merge levels), W, Ut and Qh = gam Q - P W; fp32 into the workspace.
+//     two merge levels), W, Ut and Qh = gam Q - P W; fp32 into the workspace
+//     (W, lam W, lam K and Qh, only ever MMA operands, already rounded to tf32).
 //  2. the state chain, one CTA per (sequence-head, 32 value rows), walking the
 //     chunks with the rows in fp32 and storing every chunk's S_0 (bf16). It
 //     also forms the gate term gam_r dO_r.(S_0 q_r) from the fp32 rows (as
@@ -62,7 +63,6 @@ namespace gbw {
 
 constexpr int C = 64;            // tokens per chunk
 constexpr int kThreads = 256;    // eight warps
-constexpr int kRows = 32;        // value rows per chain CTA
 using bf16 = __nv_bfloat16;
 
 template <int D>
@@ -90,11 +90,13 @@ struct Params {
     float* dstate_in;
     int BH, T, NC;
     // workspace, per (sequence-head, chunk) unit
-    float* wb;     // [C]     ln-gate prefix sums
+    float* wb;     // [2C]    ln-gate prefix sums b, then gam = e^b
     float* wti;    // [C][C]  Ti
     float* ww;     // [C][D]  W
     float* wut;    // [C][D]  Ut
-    float* wqh;    // [C][D]  Qh
+    float* wqht;   // [D][C]  Qh^T
+    float* wlkt;   // [D][C]  (diag(lam) K)^T
+    float* wlwt;   // [D][C]  (diag(lam) W)^T
     bf16* ws0;     // [D][D]  S_0
     bf16* wsc;     // [D][D]  dS_C
     float* wdu;    // [C][D]  dU
@@ -106,32 +108,96 @@ struct Params {
 
 __device__ __forceinline__ float bf(const bf16* p, int i) { return __bfloat162float(p[i]); }
 
-// acc[MT][NT] (+)= sum over k in [k0, k1) of fa(m, k) fb(k, n) for the warp's
-// (16 MT) x (8 NT) tile at (m0, n0); k0, k1 multiples of 8.
-template <int MT, int NT, class FA, class FB>
+// An operand value as a tf32 register: rounded to nearest, or passed as it
+// is when it already fits tf32 (widened bf16, or rounded when stored).
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
+
+template <bool ROUND>
+__device__ __forceinline__ uint32_t tf32_of(float x) {
+    if constexpr (ROUND) return to_tf32(x);
+    else return __float_as_uint(x);
+}
+
+// Operand values two k at a time (k even): fa(m, k) = {A(m, k), A(m, k + 1)},
+// fb(k, n) = {B(k, n), B(k + 1, n)}. Inside an 8-wide k step lane t feeds
+// k + 2t and k + 2t + 1 into the slots t and t + 4 of the m16n8k8 fragments
+// (A: (g, t), (g + 8, t), (g, t + 4), (g + 8, t + 4); B: (t, g), (t + 4, g));
+// A and B take the same order, so the sum is unchanged, and a row-contiguous
+// operand loads its pair at once.
+__device__ __forceinline__ float2 rowf(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 rowh(const bf16* p) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+__device__ __forceinline__ float2 colf(const float* p, int ld) { return make_float2(p[0], p[ld]); }
+__device__ __forceinline__ float2 colh(const bf16* p, int ld) { return make_float2(bf(p, 0), bf(p, ld)); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return make_float2(a.x * b.x, a.y * b.y); }
+__device__ __forceinline__ float2 scale2(float2 a, float s) { return make_float2(a.x * s, a.y * s); }
+
+// acc[MT][NT] (+)= sum over k in [k0, k1) of A(m, k) B(k, n) for the warp's
+// (16 MT) x (8 NT) tile at (m0, n0); k0, k1 multiples of 8. RA, RB: round the
+// A, B values to tf32 (false where they already fit).
+template <int MT, int NT, bool RA = true, bool RB = true, class FA, class FB>
 __device__ __forceinline__ void warp_mma(float (&acc)[MT][NT][4], const FA& fa, const FB& fb, int m0, int n0, int k0,
                                          int k1) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 4
     for (int k = k0; k < k1; k += 8) {
         uint32_t a[MT][4], b[NT][2];
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
             const int m = m0 + 16 * i + g;
-            a[i][0] = to_tf32(fa(m, k + t));
-            a[i][1] = to_tf32(fa(m + 8, k + t));
-            a[i][2] = to_tf32(fa(m, k + t + 4));
-            a[i][3] = to_tf32(fa(m + 8, k + t + 4));
+            const float2 lo = fa(m, k + 2 * t), hi = fa(m + 8, k + 2 * t);
+            a[i][0] = tf32_of<RA>(lo.x);
+            a[i][1] = tf32_of<RA>(hi.x);
+            a[i][2] = tf32_of<RA>(lo.y);
+            a[i][3] = tf32_of<RA>(hi.y);
         }
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-            const int n = n0 + 8 * j + g;
-            b[j][0] = to_tf32(fb(k + t, n));
-            b[j][1] = to_tf32(fb(k + t + 4, n));
+            const float2 v = fb(k + 2 * t, n0 + 8 * j + g);
+            b[j][0] = tf32_of<RB>(v.x);
+            b[j][1] = tf32_of<RB>(v.y);
         }
 #pragma unroll
         for (int i = 0; i < MT; ++i)
 #pragma unroll
             for (int j = 0; j < NT; ++j) mma_tf32_m16n8k8(acc[i][j], a[i], b[j]);
+    }
+}
+
+// Two products sharing the A operand: acc1 += fa fb1, acc2 += fa fb2.
+template <int MT, int NT, bool RA, bool RB1, bool RB2, class FA, class FB1, class FB2>
+__device__ __forceinline__ void warp_mma2(float (&acc1)[MT][NT][4], float (&acc2)[MT][NT][4], const FA& fa,
+                                          const FB1& fb1, const FB2& fb2, int m0, int n0, int k0, int k1) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll 4
+    for (int k = k0; k < k1; k += 8) {
+        uint32_t a[MT][4], b1[NT][2], b2[NT][2];
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const int m = m0 + 16 * i + g;
+            const float2 lo = fa(m, k + 2 * t), hi = fa(m + 8, k + 2 * t);
+            a[i][0] = tf32_of<RA>(lo.x);
+            a[i][1] = tf32_of<RA>(hi.x);
+            a[i][2] = tf32_of<RA>(lo.y);
+            a[i][3] = tf32_of<RA>(hi.y);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const float2 v1 = fb1(k + 2 * t, n0 + 8 * j + g), v2 = fb2(k + 2 * t, n0 + 8 * j + g);
+            b1[j][0] = tf32_of<RB1>(v1.x);
+            b1[j][1] = tf32_of<RB1>(v1.y);
+            b2[j][0] = tf32_of<RB2>(v2.x);
+            b2[j][1] = tf32_of<RB2>(v2.y);
+        }
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                mma_tf32_m16n8k8(acc1[i][j], a[i], b1[j]);
+                mma_tf32_m16n8k8(acc2[i][j], a[i], b2[j]);
+            }
     }
 }
 
@@ -145,7 +211,9 @@ __device__ __forceinline__ void zero(float (&acc)[MT][NT][4]) {
             for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
 }
 
-// f(row, col, value&) for every accumulator element of the warp's tile.
+// f(row, col, value&, rs, cs) for every accumulator element of the warp's
+// tile; rs (< 2 MT) and cs (< 2 NT) are the element's row and column slots in
+// this lane, compile-time constants once unrolled.
 template <int MT, int NT, class F>
 __device__ __forceinline__ void for_acc(float (&acc)[MT][NT][4], int m0, int n0, const F& f) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -154,54 +222,42 @@ __device__ __forceinline__ void for_acc(float (&acc)[MT][NT][4], int m0, int n0,
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) f(m0 + 16 * i + g + 8 * (e >> 1), n0 + 8 * j + 2 * t + (e & 1), acc[i][j][e]);
+            for (int e = 0; e < 4; ++e)
+                f(m0 + 16 * i + g + 8 * (e >> 1), n0 + 8 * j + 2 * t + (e & 1), acc[i][j][e], 2 * i + (e >> 1),
+                  2 * j + (e & 1));
 }
 
-// Sum of per-row partials (h[i][0]: row m0+16i+g, h[i][1]: row +8) over the
+// Sum of per-row partials (slot rs = 2i + e: row m0 + 16i + g + 8e) over the
 // four lanes of a quad, added to s[row] by its first lane.
 template <int MT>
-__device__ __forceinline__ void add_rows(float (&h)[MT][2], int m0, float* s) {
+__device__ __forceinline__ void add_rows(float (&h)[2 * MT], int m0, float* s) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int i = 0; i < MT; ++i)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            float x = h[i][e];
+            float x = h[2 * i + e];
             x += __shfl_xor_sync(0xffffffffu, x, 1);
             x += __shfl_xor_sync(0xffffffffu, x, 2);
             if (t == 0) atomicAdd(s + m0 + 16 * i + g + 8 * e, x);
         }
 }
 
-// Sum of per-column partials (h[j][0]: col n0+8j+2t, h[j][1]: +1) over the
-// eight lanes sharing t, added to s[col] by the lanes with g = 0.
+// Sum of per-column partials (slot cs = 2j + e: col n0 + 8j + 2t + e) over
+// the eight lanes sharing t, added to s[col] by the lanes with g = 0.
 template <int NT>
-__device__ __forceinline__ void add_cols(float (&h)[NT][2], int n0, float* s) {
+__device__ __forceinline__ void add_cols(float (&h)[2 * NT], int n0, float* s) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            float x = h[j][e];
+            float x = h[2 * j + e];
             x += __shfl_xor_sync(0xffffffffu, x, 4);
             x += __shfl_xor_sync(0xffffffffu, x, 8);
             x += __shfl_xor_sync(0xffffffffu, x, 16);
             if (g == 0) atomicAdd(s + n0 + 8 * j + 2 * t + e, x);
         }
-}
-
-// rows x (cols) tile copy, global row stride gs, shared row stride ss (both in
-// elements of T), rows >= valid filled with zeros; 16-byte pieces.
-template <typename T>
-__device__ __forceinline__ void load_tile(T* dst, int ss, const T* src, size_t gs, int rows, int cols, int valid) {
-    constexpr int E = 16 / sizeof(T);
-    const int per = cols / E;
-    for (int x = threadIdx.x; x < rows * per; x += blockDim.x) {
-        const int r = x / per, c = (x % per) * E;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (r < valid) val = *reinterpret_cast<const uint4*>(src + r * gs + c);
-        *reinterpret_cast<uint4*>(dst + r * ss + c) = val;
-    }
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool full) {
@@ -211,7 +267,11 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool full
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// rows x cols tile copy, global row stride gs, shared row stride ss (both in
+// elements of T), rows >= valid filled with zeros; asynchronous 16-byte
+// pieces (the caller commits and waits).
 template <typename T>
 __device__ __forceinline__ void copy_tile_async(T* dst, int ss, const T* src, size_t gs, int rows, int cols,
                                                 int valid) {
@@ -286,11 +346,13 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Params p) {
     const int n = min(C, p.T - c * C);
     const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
 
-    load_tile(sQ, HD, p.q + tok0 * D, D, C, D, n);
-    load_tile(sK, HD, p.k + tok0 * D, D, C, D, n);
-    load_tile(sV, HD, p.v + tok0 * D, D, C, D, n);
+    copy_tile_async(sQ, HD, p.q + tok0 * D, D, C, D, n);
+    copy_tile_async(sK, HD, p.k + tok0 * D, D, C, D, n);
+    copy_tile_async(sV, HD, p.v + tok0 * D, D, C, D, n);
+    cp_async_commit();
     gate_sums(p, tok0, n, vb, vbeta);
     for (int x = tid; x < C * FC; x += kThreads) sT[x] = 0.f;
+    cp_async_wait0();
     __syncthreads();
     if (tid < C) {
         vgam[tid] = expf(vb[tid]);
@@ -302,15 +364,15 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Params p) {
         float kk[2][2][4], qk[2][2][4];
         zero(kk);
         zero(qk);
-        const auto fk = [&](int m, int k) { return bf(sK, m * HD + k); };
-        const auto fq = [&](int m, int k) { return bf(sQ, m * HD + k); };
-        const auto fkt = [&](int k, int nn) { return bf(sK, nn * HD + k); };
-        warp_mma<2, 2>(kk, fk, fkt, m0, n0, 0, D);
-        warp_mma<2, 2>(qk, fq, fkt, m0, n0, 0, D);
-        for_acc(kk, m0, n0, [&](int r, int s, float& x) {
+        const auto fk = [&](int m, int k) { return rowh(sK + m * HD + k); };
+        const auto fq = [&](int m, int k) { return rowh(sQ + m * HD + k); };
+        const auto fkt = [&](int k, int nn) { return rowh(sK + nn * HD + k); };
+        warp_mma<2, 2, false, false>(kk, fk, fkt, m0, n0, 0, D);
+        warp_mma<2, 2, false, false>(qk, fq, fkt, m0, n0, 0, D);
+        for_acc(kk, m0, n0, [&](int r, int s, float& x, int rs, int cs) {
             sA[r * FC + s] = s < r ? vbeta[r] * expf(vb[r] - vb[s]) * x : 0.f;
         });
-        for_acc(qk, m0, n0, [&](int r, int s, float& x) {
+        for_acc(qk, m0, n0, [&](int r, int s, float& x, int rs, int cs) {
             sP[r * FC + s] = s <= r ? expf(vb[r] - vb[s]) * x : 0.f;
         });
     }
@@ -361,26 +423,31 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Params p) {
         float w[2][NT][4], u[2][NT][4];
         zero(w);
         zero(u);
-        const auto fw = [&](int m, int k) { return sT[m * FC + k] * vbg[k]; };
-        const auto fu = [&](int m, int k) { return sT[m * FC + k] * vbeta[k]; };
-        const auto fK = [&](int k, int nn) { return bf(sK, k * HD + nn); };
-        const auto fV = [&](int k, int nn) { return bf(sV, k * HD + nn); };
-        warp_mma<2, NT>(w, fw, fK, m0, n0, 0, m0 + 32);
-        warp_mma<2, NT>(u, fu, fV, m0, n0, 0, m0 + 32);
+        const auto fw = [&](int m, int k) { return mul2(rowf(sT + m * FC + k), rowf(vbg + k)); };
+        const auto fu = [&](int m, int k) { return mul2(rowf(sT + m * FC + k), rowf(vbeta + k)); };
+        const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
+        const auto fV = [&](int k, int nn) { return colh(sV + k * HD + nn, HD); };
+        warp_mma<2, NT, true, false>(w, fw, fK, m0, n0, 0, m0 + 32);
+        warp_mma<2, NT, true, false>(u, fu, fV, m0, n0, 0, m0 + 32);
         float* gw = p.ww + ub * C * D;
         float* gu = p.wut + ub * C * D;
-        for_acc(w, m0, n0, [&](int r, int cc, float& x) { gw[r * D + cc] = x; });
-        for_acc(u, m0, n0, [&](int r, int cc, float& x) { gu[r * D + cc] = x; });
+        float* glw = p.wlwt + ub * C * D;
+        const float bC = vb[C - 1];
+        for_acc(w, m0, n0, [&](int r, int cc, float& x, int rs, int cs) {
+            gw[r * D + cc] = tf32r(x);
+            glw[cc * C + r] = tf32r(expf(bC - vb[r]) * x);
+        });
+        for_acc(u, m0, n0, [&](int r, int cc, float& x, int rs, int cs) { gu[r * D + cc] = x; });
     }
     // P Ti -> sA (A is no longer read)
     {
         const int m0 = (warp >> 2) * 32, n0 = (warp & 3) * 16;
         float pt[2][2][4];
         zero(pt);
-        const auto fp = [&](int m, int k) { return sP[m * FC + k]; };
-        const auto ft = [&](int k, int nn) { return sT[k * FC + nn]; };
+        const auto fp = [&](int m, int k) { return rowf(sP + m * FC + k); };
+        const auto ft = [&](int k, int nn) { return colf(sT + k * FC + nn, FC); };
         warp_mma<2, 2>(pt, fp, ft, m0, n0, 0, m0 + 32);
-        for_acc(pt, m0, n0, [&](int r, int s, float& x) { sA[r * FC + s] = x; });
+        for_acc(pt, m0, n0, [&](int r, int s, float& x, int rs, int cs) { sA[r * FC + s] = x; });
     }
     __syncthreads();
     // Qh = diag(gam) Q - (P Ti) diag(beta gam) K
@@ -389,171 +456,265 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Params p) {
         const int m0 = (warp >> 2) * 32, n0 = (warp & 3) * (D / 4);
         float qh[2][NT][4];
         zero(qh);
-        const auto fa = [&](int m, int k) { return sA[m * FC + k] * vbg[k]; };
-        const auto fK = [&](int k, int nn) { return bf(sK, k * HD + nn); };
-        warp_mma<2, NT>(qh, fa, fK, m0, n0, 0, m0 + 32);
-        float* gq = p.wqh + ub * C * D;
-        for_acc(qh, m0, n0, [&](int r, int cc, float& x) { gq[r * D + cc] = vgam[r] * bf(sQ, r * HD + cc) - x; });
+        const auto fa = [&](int m, int k) { return mul2(rowf(sA + m * FC + k), rowf(vbg + k)); };
+        const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
+        warp_mma<2, NT, true, false>(qh, fa, fK, m0, n0, 0, m0 + 32);
+        float* gq = p.wqht + ub * C * D;
+        for_acc(qh, m0, n0, [&](int r, int cc, float& x, int rs, int cs) {
+            gq[cc * C + r] = tf32r(vgam[r] * bf(sQ, r * HD + cc) - x);
+        });
+    }
+    {
+        float* gk = p.wlkt + ub * C * D;
+        const float bC = vb[C - 1];
+        for (int x = tid; x < C * D; x += kThreads) {
+            const int d = x / C, r = x % C;
+            gk[x] = tf32r(expf(bC - vb[r]) * bf(sK, r * HD + d));
+        }
     }
     float* gt = p.wti + ub * C * C;
     for (int x = tid; x < C * C; x += kThreads) gt[x] = sT[(x / C) * FC + x % C];
     if (tid < C) {
-        p.wb[ub * C + tid] = vb[tid];
+        p.wb[ub * 2 * C + tid] = vb[tid];
+        p.wb[ub * 2 * C + C + tid] = vgam[tid];
         p.wdb0[ub * C + tid] = 0.f;   // the state chain adds into it
     }
 }
 
 // ---------------------------------------------------------------------------
-// 2, 3. chains over the chunks, 32 value rows per CTA
+// 2, 3. both chains in one launch: one CTA per (sequence-head, direction),
+//       16 value rows per warp
 // ---------------------------------------------------------------------------
+// Each warp holds its 16 rows of X (fp32) as MMA accumulators. In the k-pair
+// order an accumulator tile (rows g, g + 8; columns 2t, 2t + 1 of each
+// 8-column block) is, register for register, the A fragment of the product
+// that contracts over those columns, so X and the chunk's Z = Ut^T - X W^T
+// (or -X K^T) never leave the registers:
+//    state chain:    Y = X W^T,  Z = Ut^T - Y,   X <- gam_C X + Z (lam K)
+//    gradient chain: Y = X K^T,  Z = -Y,         X <- gam_C X + Z (lam W) + dO^T Qh
+// The B operands come from double-buffered tiles (W, Q, K as stored; the
+// transposed lam K, lam W and Qh written by the prep), the Ut and dO slices
+// of the warp's rows from registers loaded a chunk ahead.
+
 template <int D>
 struct ChainSmem {
-    using Dm = Dims<D>;
-    static constexpr size_t F_TILE = size_t(C) * Dm::FD * 4;
-    static constexpr size_t H_TILE = size_t(C) * Dm::HD * 2;
-    static constexpr size_t S_TILE = size_t(C) * (kRows + 4) * 4;   // fp32 [C][R+4] or bf16 [C][R+8]
-    static constexpr size_t Q_TILE = H_TILE;                         // state chain: Q, then the dO slice
-    static_assert(Q_TILE + size_t(C) * (kRows + 8) * 2 <= F_TILE, "Q and the dO slice fit the Qh slot");
-    static constexpr size_t STAGE = 2 * F_TILE + H_TILE + S_TILE + C * 4;
-    static constexpr size_t OFF_X = 2 * STAGE;
-    static constexpr size_t OFF_Z = OFF_X + size_t(kRows) * Dm::FD * 4;
-    static constexpr size_t BYTES = OFF_Z + size_t(kRows) * Dm::FC * 4;
+    static constexpr int FW = D + 8;    // fp32 [C][FW]: W (pairs along d)
+    static constexpr int HD = D + 8;    // bf16 [C][HD]: Q, K (pairs along d)
+    static constexpr int FT = C + 8;    // fp32 [D][FT]: (lam K)^T, (lam W)^T, Qh^T (pairs along tokens)
+    static constexpr size_t W_T = size_t(C) * FW * 4, H_T = size_t(C) * HD * 2, T_T = size_t(D) * FT * 4;
+    // state chain: W, Q, (lam K)^T, gam; gradient chain: K, (lam W)^T, Qh^T, gam
+    static constexpr size_t FWD = W_T + H_T + T_T + C * 4;
+    static constexpr size_t REV = H_T + 2 * T_T + C * 4;
+    static constexpr size_t STAGE = ((FWD > REV ? FWD : REV) + 127) / 128 * 128;
+    static constexpr size_t BYTES = 2 * STAGE;
 };
 
-template <int D, bool REV>
-__global__ void __launch_bounds__(kThreads, 1) chain_kernel(const Params p) {
-    using Dm = Dims<D>;
+constexpr int kChainSplit = 2;   // CTAs per (sequence-head, direction), D / kChainSplit rows each
+
+template <int D, bool rev>
+__device__ __forceinline__ void chain_body(const Params& p, int bh, int part, uint8_t* smem) {
     using L = ChainSmem<D>;
-    constexpr int FD = Dm::FD, HD = Dm::HD, FC = Dm::FC, R = kRows;
-    constexpr int SF = R + 4, SH = R + 8;   // slice strides: fp32 Ut, bf16 dO
-    extern __shared__ __align__(16) uint8_t smem[];
-    float* sX = reinterpret_cast<float*>(smem + L::OFF_X);
-    float* sZ = reinterpret_cast<float*>(smem + L::OFF_Z);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int nrb = D / R, bh = blockIdx.x / nrb, row0 = (blockIdx.x % nrb) * R;
-    __shared__ float sdb[C];   // state chain: this CTA's part of gam_r dO_r.(S_0 q_r)
+    constexpr int FW = L::FW, HD = L::HD, FT = L::FT, NJ = D / 8;   // NJ column blocks of X
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int row0 = part * (D / kChainSplit) + 16 * warp;   // this warp's first row
     const int NC = p.NC;
     const size_t ss = static_cast<size_t>(D) * D;
 
-    // stage layout: F0 (W), F1 (Qh, gradient chain), H (K), S (Ut or dO slice), b
-    auto stage_ptr = [&](int buf, size_t off) { return smem + buf * L::STAGE + off; };
+    auto stage = [&](int buf) { return smem + buf * L::STAGE; };
     auto issue = [&](int j, int buf) {
-        const int c = REV ? NC - 1 - j : j;
+        const int c = rev ? NC - 1 - j : j;
         const int n = min(C, p.T - c * C);
         const size_t ub = static_cast<size_t>(bh) * NC + c;
         const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
-        copy_tile_async(reinterpret_cast<float*>(stage_ptr(buf, 0)), FD, p.ww + ub * C * D, D, C, D, C);
-        if (REV) {
-            copy_tile_async(reinterpret_cast<float*>(stage_ptr(buf, L::F_TILE)), FD, p.wqh + ub * C * D, D, C, D, C);
-            copy_tile_async(reinterpret_cast<bf16*>(stage_ptr(buf, 2 * L::F_TILE + L::H_TILE)), SH,
-                            p.dout + tok0 * D + row0, D, C, R, n);
+        uint8_t* b = stage(buf);
+        if (!rev) {
+            copy_tile_async(reinterpret_cast<float*>(b), FW, p.ww + ub * C * D, D, C, D, C);
+            copy_tile_async(reinterpret_cast<bf16*>(b + L::W_T), HD, p.q + tok0 * D, D, C, D, n);
+            copy_tile_async(reinterpret_cast<float*>(b + L::W_T + L::H_T), FT, p.wlkt + ub * C * D, C, D, C, D);
+            copy_tile_async(reinterpret_cast<float*>(b + L::FWD - C * 4), C, p.wb + ub * 2 * C + C, C, 1, C, 1);
         } else {
-            copy_tile_async(reinterpret_cast<float*>(stage_ptr(buf, 2 * L::F_TILE + L::H_TILE)), SF,
-                            p.wut + ub * C * D + row0, D, C, R, C);
-            copy_tile_async(reinterpret_cast<bf16*>(stage_ptr(buf, L::F_TILE)), HD, p.q + tok0 * D, D, C, D, n);
-            copy_tile_async(reinterpret_cast<bf16*>(stage_ptr(buf, L::F_TILE + L::Q_TILE)), SH,
-                            p.dout + tok0 * D + row0, D, C, R, n);
+            copy_tile_async(reinterpret_cast<bf16*>(b), HD, p.k + tok0 * D, D, C, D, n);
+            copy_tile_async(reinterpret_cast<float*>(b + L::H_T), FT, p.wlwt + ub * C * D, C, D, C, D);
+            copy_tile_async(reinterpret_cast<float*>(b + L::H_T + L::T_T), FT, p.wqht + ub * C * D, C, D, C, D);
+            copy_tile_async(reinterpret_cast<float*>(b + L::REV - C * 4), C, p.wb + ub * 2 * C + C, C, 1, C, 1);
         }
-        copy_tile_async(reinterpret_cast<bf16*>(stage_ptr(buf, 2 * L::F_TILE)), HD, p.k + tok0 * D, D, C, D, n);
-        copy_tile_async(reinterpret_cast<float*>(stage_ptr(buf, 2 * L::F_TILE + L::H_TILE + L::S_TILE)), C,
-                        p.wb + ub * C, C, 1, C, 1);
+    };
+    // the warp's slice of Ut (state chain) and of dO for chunk step j, in
+    // accumulator order: [block jb][row half h][pair e]; loaded once the
+    // previous step's are used, a little under a step ahead
+    float ut[8][2][2];
+    uint32_t dop[8][2];   // dO as bf16 pairs (tokens 8 jb + 2t, +1 at row g + 8h)
+    auto fetch = [&](int j, float (&u)[8][2][2], uint32_t (&o)[8][2]) {
+        const int c = rev ? NC - 1 - j : j;
+        const int n = min(C, p.T - c * C);
+        const size_t ub = static_cast<size_t>(bh) * NC + c;
+        const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
+        const uint16_t* dO = reinterpret_cast<const uint16_t*>(p.dout);
+#pragma unroll
+        for (int jb = 0; jb < 8; ++jb)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = row0 + g + 8 * h, tk = 8 * jb + 2 * t;
+                if (!rev) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) u[jb][h][e] = p.wut[(ub * C + tk + e) * D + row];
+                }
+                const uint32_t lo = tk < n ? dO[(tok0 + tk) * D + row] : 0u;
+                const uint32_t hi = tk + 1 < n ? dO[(tok0 + tk + 1) * D + row] : 0u;
+                o[jb][h] = lo | (hi << 16);
+            }
     };
 
-    const float* x0 = REV ? p.dstate_out : p.state_in;
-    for (int x = tid; x < R * D; x += kThreads) {
-        const int r = x / D, cc = x % D;
-        sX[r * FD + cc] = x0 ? x0[bh * ss + static_cast<size_t>(row0 + r) * D + cc] : 0.f;
+    float x[NJ][4];
+    {
+        const float* x0 = rev ? p.dstate_out : p.state_in;
+#pragma unroll
+        for (int jb = 0; jb < NJ; ++jb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = row0 + g + 8 * (e >> 1), col = 8 * jb + 2 * t + (e & 1);
+                x[jb][e] = x0 ? x0[bh * ss + static_cast<size_t>(row) * D + col] : 0.f;
+            }
     }
     issue(0, 0);
     cp_async_commit();
     if (NC > 1) issue(1, 1);
     cp_async_commit();
+    fetch(0, ut, dop);
 
-    bf16* gout = REV ? p.wsc : p.ws0;
+    bf16* gout = rev ? p.wsc : p.ws0;
     for (int j = 0; j < NC; ++j) {
         const int buf = j & 1;
-        const int c = REV ? NC - 1 - j : j;
-        const float* tW = reinterpret_cast<const float*>(stage_ptr(buf, 0));
-        const float* tQh = reinterpret_cast<const float*>(stage_ptr(buf, L::F_TILE));
-        const bf16* tK = reinterpret_cast<const bf16*>(stage_ptr(buf, 2 * L::F_TILE));
-        const float* tUt = reinterpret_cast<const float*>(stage_ptr(buf, 2 * L::F_TILE + L::H_TILE));
-        const bf16* tdO = reinterpret_cast<const bf16*>(stage_ptr(buf, 2 * L::F_TILE + L::H_TILE));
-        const float* tb = reinterpret_cast<const float*>(stage_ptr(buf, 2 * L::F_TILE + L::H_TILE + L::S_TILE));
+        const int c = rev ? NC - 1 - j : j;
+        const uint8_t* b = stage(buf);
+        const float* tgam = reinterpret_cast<const float*>(b + (rev ? L::REV : L::FWD) - C * 4);
+        // the rows entering this chunk
+        {
+            bf16* o = gout + (static_cast<size_t>(bh) * NC + c) * ss;
+#pragma unroll
+            for (int jb = 0; jb < NJ; ++jb)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<__nv_bfloat162*>(o + static_cast<size_t>(row0 + g + 8 * h) * D + 8 * jb + 2 * t) =
+                        __floats2bfloat162_rn(x[jb][2 * h], x[jb][2 * h + 1]);
+        }
         cp_async_wait1();
-        __syncthreads();   // this chunk's tiles and the rows' last update are visible
-        {
-            bf16* o = gout + (static_cast<size_t>(bh) * NC + c) * ss + static_cast<size_t>(row0) * D;
-            for (int x = tid; x < R * D / 2; x += kThreads) {
-                const int r = (2 * x) / D, cc = (2 * x) % D;
-                *reinterpret_cast<__nv_bfloat162*>(o + r * D + cc) =
-                    __floats2bfloat162_rn(sX[r * FD + cc], sX[r * FD + cc + 1]);
+        __syncthreads();   // this chunk's tiles are visible
+        // Y = X B1 (16 rows x C tokens); state chain also Y2 = X Q^T
+        float y[8][4], y2[8][4];
+#pragma unroll
+        for (int jb = 0; jb < 8; ++jb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[jb][e] = y2[jb][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < NJ; ++kk) {
+            const uint32_t a[4] = {to_tf32(x[kk][0]), to_tf32(x[kk][2]), to_tf32(x[kk][1]), to_tf32(x[kk][3])};
+#pragma unroll
+            for (int jb = 0; jb < 8; ++jb) {
+                const int tok = 8 * jb + g, d = 8 * kk + 2 * t;
+                if (!rev) {
+                    const float2 w = rowf(reinterpret_cast<const float*>(b) + tok * FW + d);
+                    const float2 qv = rowh(reinterpret_cast<const bf16*>(b + L::W_T) + tok * HD + d);
+                    const uint32_t b1[2] = {__float_as_uint(w.x), __float_as_uint(w.y)};
+                    const uint32_t b2[2] = {__float_as_uint(qv.x), __float_as_uint(qv.y)};
+                    mma_tf32_m16n8k8(y[jb], a, b1);
+                    mma_tf32_m16n8k8(y2[jb], a, b2);
+                } else {
+                    const float2 kv = rowh(reinterpret_cast<const bf16*>(b) + tok * HD + d);
+                    const uint32_t b1[2] = {__float_as_uint(kv.x), __float_as_uint(kv.y)};
+                    mma_tf32_m16n8k8(y[jb], a, b1);
+                }
             }
         }
-        const float bC = tb[C - 1];
-        // Y = X A'^T (32 x C), Z = (Ut^T - Y) diag(lam) or -Y diag(lam)
-        {
-            const int n0 = warp * 8;
-            float y[2][1][4];
-            zero(y);
-            const auto fx = [&](int m, int k) { return sX[m * FD + k]; };
-            if (REV) {
-                warp_mma<2, 1>(y, fx, [&](int k, int nn) { return bf(tK, nn * HD + k); }, 0, n0, 0, D);
-            } else {
-                warp_mma<2, 1>(y, fx, [&](int k, int nn) { return tW[nn * FD + k]; }, 0, n0, 0, D);
+        // Z = Ut^T - Y or -Y (in place); the state chain's gate term
+        // gam_r sum over rows of dO[r][row] (X Q^T)[row][r]
+        if (!rev) {
+            float part[8][2];
+#pragma unroll
+            for (int jb = 0; jb < 8; ++jb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float d0 = __uint_as_float((dop[jb][0] >> (16 * e)) << 16);
+                    const float d1 = __uint_as_float((dop[jb][1] >> (16 * e)) << 16);
+                    part[jb][e] = y2[jb][e] * d0 + y2[jb][2 + e] * d1;
+                    y[jb][e] = ut[jb][0][e] - y[jb][e];
+                    y[jb][2 + e] = ut[jb][1][e] - y[jb][2 + e];
+                }
+            if (j + 1 < NC) fetch(j + 1, ut, dop);
+            float* gdb = p.wdb0 + (static_cast<size_t>(bh) * NC + c) * C;
+#pragma unroll
+            for (int jb = 0; jb < 8; ++jb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float v = part[jb][e];
+                    v += __shfl_xor_sync(0xffffffffu, v, 4);
+                    v += __shfl_xor_sync(0xffffffffu, v, 8);
+                    v += __shfl_xor_sync(0xffffffffu, v, 16);
+                    const int tok = 8 * jb + 2 * t + e;
+                    if (g == 0) atomicAdd(gdb + tok, tgam[tok] * v);
+                }
+        } else {
+#pragma unroll
+            for (int jb = 0; jb < 8; ++jb)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[jb][e] = -y[jb][e];
+        }
+        // X <- gam_C X + Z B2 (+ dO^T Qh)
+        const float gC = tgam[C - 1];
+#pragma unroll
+        for (int jb = 0; jb < NJ; ++jb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[jb][e] *= gC;
+        const float* tB = reinterpret_cast<const float*>(b + (rev ? L::H_T : L::W_T + L::H_T));
+        const float* tQh = reinterpret_cast<const float*>(b + L::H_T + L::T_T);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {   // tokens 8 kk .. 8 kk + 7
+            const uint32_t a[4] = {to_tf32(y[kk][0]), to_tf32(y[kk][2]), to_tf32(y[kk][1]), to_tf32(y[kk][3])};
+            uint32_t a2[4];
+            if (rev) {   // dO^T: rows g, g + 8, tokens 8 kk + 2t, +1 (bf16: already tf32)
+                a2[0] = dop[kk][0] << 16;
+                a2[1] = dop[kk][1] << 16;
+                a2[2] = dop[kk][0] & 0xffff0000u;
+                a2[3] = dop[kk][1] & 0xffff0000u;
             }
-            for_acc(y, 0, n0, [&](int m, int s, float& x) {
-                const float lam = expf(bC - tb[s]);
-                sZ[m * FC + s] = REV ? -x * lam : (tUt[s * SF + m] - x) * lam;
-            });
-            if (!REV) {
-                // X Q^T with X = hi + lo (tf32 halves): fp32 accuracy; then the
-                // column sums of dO^T o (X Q^T) over this CTA's rows
-                const bf16* tQ = reinterpret_cast<const bf16*>(stage_ptr(buf, L::F_TILE));
-                const bf16* tO = reinterpret_cast<const bf16*>(stage_ptr(buf, L::F_TILE + L::Q_TILE));
-                if (tid < C) sdb[tid] = 0.f;
-                float y2[2][1][4];
-                zero(y2);
-                const auto fqt = [&](int k, int nn) { return bf(tQ, nn * HD + k); };
-                warp_mma<2, 1>(y2, fx, fqt, 0, n0, 0, D);
-                warp_mma<2, 1>(y2, [&](int m, int k) {
-                    const float x = sX[m * FD + k];
-                    return x - __uint_as_float(to_tf32(x));
-                }, fqt, 0, n0, 0, D);
-                float h[1][2] = {};
-                for_acc(y2, 0, n0, [&](int m, int r, float& x) { h[0][r & 1] += x * bf(tO, r * SH + m); });
-                __syncthreads();   // sdb zeroed
-                add_cols<1>(h, n0, sdb);
+#pragma unroll
+            for (int jb = 0; jb < NJ; ++jb) {
+                const float2 v = rowf(tB + (8 * jb + g) * FT + 8 * kk + 2 * t);
+                const uint32_t b1[2] = {__float_as_uint(v.x), __float_as_uint(v.y)};
+                mma_tf32_m16n8k8(x[jb], a, b1);
+            }
+            if (rev) {   // after the first pass, so that no two MMAs in a row share an accumulator
+#pragma unroll
+                for (int jb = 0; jb < NJ; ++jb) {
+                    const float2 qv = rowf(tQh + (8 * jb + g) * FT + 8 * kk + 2 * t);
+                    const uint32_t b2[2] = {__float_as_uint(qv.x), __float_as_uint(qv.y)};
+                    mma_tf32_m16n8k8(x[jb], a2, b2);
+                }
             }
         }
-        __syncthreads();
-        if (!REV && tid < C) atomicAdd(p.wdb0 + (static_cast<size_t>(bh) * NC + c) * C + tid, expf(tb[tid]) * sdb[tid]);
-        // X <- gam_C X + Z B' (+ dO^T Qh)
-        {
-            constexpr int NT = D / 64;
-            const int n0 = warp * (D / 8);
-            float acc[2][NT][4];
-            zero(acc);
-            const auto fz = [&](int m, int k) { return sZ[m * FC + k]; };
-            if (REV) {
-                warp_mma<2, NT>(acc, fz, [&](int k, int nn) { return tW[k * FD + nn]; }, 0, n0, 0, C);
-                warp_mma<2, NT>(acc, [&](int m, int k) { return bf(tdO, k * SH + m); },
-                                [&](int k, int nn) { return tQh[k * FD + nn]; }, 0, n0, 0, C);
-            } else {
-                warp_mma<2, NT>(acc, fz, [&](int k, int nn) { return bf(tK, k * HD + nn); }, 0, n0, 0, C);
-            }
-            const float gC = expf(bC);
-            for_acc(acc, 0, n0, [&](int m, int cc, float& x) { sX[m * FD + cc] = gC * sX[m * FD + cc] + x; });
-        }
+        if (rev && j + 1 < NC) fetch(j + 1, ut, dop);
         __syncthreads();   // every warp is done with this stage
         if (j + 2 < NC) issue(j + 2, buf);
         cp_async_commit();
     }
-    if (REV && p.dstate_in) {
-        for (int x = tid; x < R * D; x += kThreads) {
-            const int r = x / D, cc = x % D;
-            p.dstate_in[bh * ss + static_cast<size_t>(row0 + r) * D + cc] = sX[r * FD + cc];
-        }
+    if (rev && p.dstate_in) {
+#pragma unroll
+        for (int jb = 0; jb < NJ; ++jb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = row0 + g + 8 * (e >> 1), col = 8 * jb + 2 * t + (e & 1);
+                p.dstate_in[bh * ss + static_cast<size_t>(row) * D + col] = x[jb][e];
+            }
     }
+}
+
+template <int D>
+__global__ void __launch_bounds__(2 * D / kChainSplit, 1) chain_kernel(const Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int per_dir = p.BH * kChainSplit;
+    const int i = blockIdx.x % per_dir;
+    if (blockIdx.x < per_dir) chain_body<D, false>(p, i / kChainSplit, i % kChainSplit, smem);
+    else chain_body<D, true>(p, i / kChainSplit, i % kChainSplit, smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -598,18 +759,20 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
     const size_t ub = static_cast<size_t>(unit);
 
-    load_tile(sQ, HD, p.q + tok0 * D, D, C, D, n);
-    load_tile(sK, HD, p.k + tok0 * D, D, C, D, n);
-    load_tile(sO, HD, p.dout + tok0 * D, D, C, D, n);
-    load_tile(sS0, HD, p.ws0 + ub * D * D, D, D, D, D);
-    load_tile(sSC, HD, p.wsc + ub * D * D, D, D, D, D);
-    load_tile(sW, FD, p.ww + ub * C * D, D, C, D, C);
-    load_tile(sU, FD, p.wut + ub * C * D, D, C, D, C);
+    copy_tile_async(sQ, HD, p.q + tok0 * D, D, C, D, n);
+    copy_tile_async(sK, HD, p.k + tok0 * D, D, C, D, n);
+    copy_tile_async(sO, HD, p.dout + tok0 * D, D, C, D, n);
+    copy_tile_async(sS0, HD, p.ws0 + ub * D * D, D, D, D, D);
+    copy_tile_async(sSC, HD, p.wsc + ub * D * D, D, D, D, D);
+    copy_tile_async(sW, FD, p.ww + ub * C * D, D, C, D, C);
+    copy_tile_async(sU, FD, p.wut + ub * C * D, D, C, D, C);
+    cp_async_commit();
     if (tid < C) {
-        vb[tid] = p.wb[ub * C + tid];
+        vb[tid] = p.wb[ub * 2 * C + tid];
         vdb[tid] = 0.f;
     }
     if (tid == 0) vsum[0] = 0.f;
+    cp_async_wait0();
     __syncthreads();
     if (tid < C) {
         vgam[tid] = expf(vb[tid]);
@@ -618,42 +781,45 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     __syncthreads();
     const float gC = expf(vb[C - 1]);
     const int m0 = (warp >> 2) * 32, n0c = (warp & 3) * 16, n0d = (warp & 3) * (D / 4);
-    const auto fQ = [&](int m, int k) { return bf(sQ, m * HD + k); };
-    const auto fO = [&](int m, int k) { return bf(sO, m * HD + k); };
-    const auto fKt = [&](int k, int nn) { return bf(sK, nn * HD + k); };
-    const auto fK = [&](int k, int nn) { return bf(sK, k * HD + nn); };
-    const auto fS0 = [&](int k, int nn) { return bf(sS0, k * HD + nn); };
-    const auto fS0t = [&](int k, int nn) { return bf(sS0, nn * HD + k); };
-    const auto fSCt = [&](int k, int nn) { return bf(sSC, nn * HD + k); };
-    const auto fSC = [&](int k, int nn) { return bf(sSC, k * HD + nn); };
+    const auto fQ = [&](int m, int k) { return rowh(sQ + m * HD + k); };
+    const auto fQc = [&](int k, int nn) { return colh(sQ + k * HD + nn, HD); };
+    const auto fO = [&](int m, int k) { return rowh(sO + m * HD + k); };
+    const auto fOc = [&](int k, int nn) { return colh(sO + k * HD + nn, HD); };
+    const auto fKt = [&](int k, int nn) { return rowh(sK + nn * HD + k); };
+    const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
+    const auto fS0 = [&](int k, int nn) { return colh(sS0 + k * HD + nn, HD); };
+    const auto fS0t = [&](int k, int nn) { return rowh(sS0 + nn * HD + k); };
+    const auto fSCt = [&](int k, int nn) { return rowh(sSC + nn * HD + k); };
+    const auto fSC = [&](int k, int nn) { return colh(sSC + k * HD + nn, HD); };
 
     // P = lower(E o Q K^T); U = Ut - W S_0^T (in place); dQ <- gam dO S_0
     {
         float qk[2][2][4];
         zero(qk);
-        warp_mma<2, 2>(qk, fQ, fKt, m0, n0c, 0, D);
-        for_acc(qk, m0, n0c, [&](int r, int s, float& x) {
+        warp_mma<2, 2, false, false>(qk, fQ, fKt, m0, n0c, 0, D);
+        for_acc(qk, m0, n0c, [&](int r, int s, float& x, int rs, int cs) {
             sP[r * FC + s] = s <= r ? expf(vb[r] - vb[s]) * x : 0.f;
         });
         float ws[2][NT][4];
         zero(ws);
-        warp_mma<2, NT>(ws, [&](int m, int k) { return sW[m * FD + k]; }, fS0t, m0, n0d, 0, D);
-        for_acc(ws, m0, n0d, [&](int r, int i, float& x) { sU[r * FD + i] -= x; });
+        warp_mma<2, NT, true, false>(ws, [&](int m, int k) { return rowf(sW + m * FD + k); }, fS0t, m0, n0d, 0, D);
+        for_acc(ws, m0, n0d, [&](int r, int i, float& x, int rs, int cs) { sU[r * FD + i] -= x; });
     }
     float dq[2][NT][4];
     zero(dq);
-    warp_mma<2, NT>(dq, fO, fS0, m0, n0d, 0, D);
-    for_acc(dq, m0, n0d, [&](int r, int k, float& x) { x *= vgam[r]; });
+    warp_mma<2, NT, false, false>(dq, fO, fS0, m0, n0d, 0, D);
+    for_acc(dq, m0, n0d, [&](int r, int k, float& x, int rs, int cs) { x *= vgam[r]; });
     __syncthreads();   // sP, sU complete; W no longer read
     // dU = P^T dO + diag(lam) K dS_C^T -> sW and the workspace
     {
         float du[2][NT][4];
         zero(du);
-        warp_mma<2, NT>(du, [&](int m, int k) { return sP[k * FC + m]; }, [&](int k, int nn) { return fO(k, nn); },
+        warp_mma<2, NT, true, false>(du, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fOc,
                         m0, n0d, m0, C);
-        warp_mma<2, NT>(du, [&](int m, int k) { return vlam[m] * bf(sK, m * HD + k); }, fSCt, m0, n0d, 0, D);
+        warp_mma<2, NT, true, false>(du, [&](int m, int k) { return scale2(rowh(sK + m * HD + k), vlam[m]); }, fSCt, m0,
+                                     n0d, 0, D);
         float* g = p.wdu + ub * C * D;
-        for_acc(du, m0, n0d, [&](int r, int i, float& x) {
+        for_acc(du, m0, n0d, [&](int r, int i, float& x, int rs, int cs) {
             sW[r * FD + i] = x;
             g[r * D + i] = x;
         });
@@ -663,19 +829,19 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     {
         float dw[2][NT][4];
         zero(dw);
-        warp_mma<2, NT>(dw, [&](int m, int k) { return sW[m * FD + k]; }, fS0, m0, n0d, 0, D);
+        warp_mma<2, NT, true, false>(dw, [&](int m, int k) { return rowf(sW + m * FD + k); }, fS0, m0, n0d, 0, D);
         float* g = p.wdw + ub * C * D;
-        for_acc(dw, m0, n0d, [&](int r, int kk, float& x) { g[r * D + kk] = -x; });
+        for_acc(dw, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) { g[r * D + kk] = -x; });
         float dp[2][2][4];
         zero(dp);
-        warp_mma<2, 2>(dp, fO, [&](int k, int nn) { return sU[nn * FD + k]; }, m0, n0c, 0, D);
-        float hr[2][2] = {}, hc[2][2] = {};
-        for_acc(dp, m0, n0c, [&](int r, int s, float& x) {
+        warp_mma<2, 2, false, true>(dp, fO, [&](int k, int nn) { return rowf(sU + nn * FD + k); }, m0, n0c, 0, D);
+        float hr[4] = {}, hc[4] = {};
+        for_acc(dp, m0, n0c, [&](int r, int s, float& x, int rs, int cs) {
             float out = 0.f;
             if (s <= r) {
                 const float pp = x * sP[r * FC + s];
-                hr[(r - m0) >> 4][((r - m0) >> 3) & 1] += pp;
-                hc[(s - n0c) >> 3][(s - n0c) & 1] -= pp;
+                hr[rs] += pp;
+                hc[cs] -= pp;
                 out = x * expf(vb[r] - vb[s]);
             }
             sP[r * FC + s] = out;
@@ -685,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     }
     __syncthreads();   // dP o E complete
     // dQ += (dP o E) K -> global
-    warp_mma<2, NT>(dq, [&](int m, int k) { return sP[m * FC + k]; }, fK, m0, n0d, 0, m0 + 32);
+    warp_mma<2, NT, true, false>(dq, [&](int m, int k) { return rowf(sP + m * FC + k); }, fK, m0, n0d, 0, m0 + 32);
     {
         bf16* g = p.dq + tok0 * D;
 #pragma unroll
@@ -704,21 +870,22 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     {
         float dk[2][NT][4];
         zero(dk);
-        warp_mma<2, NT>(dk, [&](int m, int k) { return vlam[m] * sU[m * FD + k]; }, fSC, m0, n0d, 0, D);
-        float h[2][2] = {};
-        for_acc(dk, m0, n0d, [&](int r, int kk, float& x) {
-            h[(r - m0) >> 4][((r - m0) >> 3) & 1] -= x * bf(sK, r * HD + kk);
+        warp_mma<2, NT, true, false>(dk, [&](int m, int k) { return scale2(rowf(sU + m * FD + k), vlam[m]); }, fSC, m0,
+                                     n0d, 0, D);
+        float h[4] = {};
+        for_acc(dk, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) {
+            h[rs] -= x * bf(sK, r * HD + kk);
         });
         float tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) tot -= h[i][0] + h[i][1];
+        for (int i = 0; i < 4; ++i) tot -= h[i];
         add_rows<2>(h, m0, vdb);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
         if ((tid & 31) == 0) atomicAdd(vdb + C - 1, tot);
-        warp_mma<2, NT>(dk, [&](int m, int k) { return sP[k * FC + m]; }, fQ, m0, n0d, m0, C);
+        warp_mma<2, NT, true, false>(dk, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fQc, m0, n0d, m0, C);
         float* g = p.wdk + ub * C * D;
-        for_acc(dk, m0, n0d, [&](int r, int kk, float& x) { g[r * D + kk] = x; });
+        for_acc(dk, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) { g[r * D + kk] = x; });
     }
     // gam_C <dS_C, S_0>
     {
@@ -776,40 +943,42 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
     const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
     const size_t ub = static_cast<size_t>(unit);
 
-    load_tile(sT, FC, p.wti + ub * C * C, C, C, C, C);
-    load_tile(sW, FD, p.ww + ub * C * D, D, C, D, C);
-    load_tile(sUt, FD, p.wut + ub * C * D, D, C, D, C);
-    load_tile(sdU, FD, p.wdu + ub * C * D, D, C, D, C);
-    load_tile(sdW, FD, p.wdw + ub * C * D, D, C, D, C);
-    load_tile(sK, HD, p.k + tok0 * D, D, C, D, n);
-    load_tile(sV, HD, p.v + tok0 * D, D, C, D, n);
+    copy_tile_async(sT, FC, p.wti + ub * C * C, C, C, C, C);
+    copy_tile_async(sW, FD, p.ww + ub * C * D, D, C, D, C);
+    copy_tile_async(sUt, FD, p.wut + ub * C * D, D, C, D, C);
+    copy_tile_async(sdU, FD, p.wdu + ub * C * D, D, C, D, C);
+    copy_tile_async(sdW, FD, p.wdw + ub * C * D, D, C, D, C);
+    copy_tile_async(sK, HD, p.k + tok0 * D, D, C, D, n);
+    copy_tile_async(sV, HD, p.v + tok0 * D, D, C, D, n);
+    cp_async_commit();
     if (tid < C) {
-        vb[tid] = p.wb[ub * C + tid];
+        vb[tid] = p.wb[ub * 2 * C + tid];
         vbeta[tid] = tid < n ? p.beta[tok0 + tid] : 0.f;
         vdb[tid] = p.wdb[ub * C + tid];
         vdbeta[tid] = 0.f;
     }
+    cp_async_wait0();
     __syncthreads();
     if (tid < C) vgam[tid] = expf(vb[tid]);
     __syncthreads();
     const int m0 = (warp >> 2) * 32, n0c = (warp & 3) * 16, n0d = (warp & 3) * (D / 4);
-    const auto fK = [&](int k, int nn) { return bf(sK, k * HD + nn); };
+    const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
     // dRv = Ti^T dU, dRk = Ti^T dW (Ti^T upper: k >= m0); K K^T -> sA
     float rv[2][NT][4], rk[2][NT][4];
     zero(rv);
     zero(rk);
     {
-        const auto ftt = [&](int m, int k) { return sT[k * FC + m]; };
-        warp_mma<2, NT>(rv, ftt, [&](int k, int nn) { return sdU[k * FD + nn]; }, m0, n0d, m0, C);
-        warp_mma<2, NT>(rk, ftt, [&](int k, int nn) { return sdW[k * FD + nn]; }, m0, n0d, m0, C);
+        const auto ftt = [&](int m, int k) { return colf(sT + k * FC + m, FC); };
+        warp_mma<2, NT>(rv, ftt, [&](int k, int nn) { return colf(sdU + k * FD + nn, FD); }, m0, n0d, m0, C);
+        warp_mma<2, NT>(rk, ftt, [&](int k, int nn) { return colf(sdW + k * FD + nn, FD); }, m0, n0d, m0, C);
         float kk[2][2][4];
         zero(kk);
-        warp_mma<2, 2>(kk, [&](int m, int k) { return bf(sK, m * HD + k); },
-                       [&](int k, int nn) { return bf(sK, nn * HD + k); }, m0, n0c, 0, D);
-        for_acc(kk, m0, n0c, [&](int r, int s, float& x) { sA[r * FC + s] = x; });
+        warp_mma<2, 2, false, false>(kk, [&](int m, int k) { return rowh(sK + m * HD + k); },
+                                     [&](int k, int nn) { return rowh(sK + nn * HD + k); }, m0, n0c, 0, D);
+        for_acc(kk, m0, n0c, [&](int r, int s, float& x, int rs, int cs) { sA[r * FC + s] = x; });
         // dV = beta dRv; dbeta += dRv.v + gam dRk.k; db += beta gam dRk.k
         bf16* gv = p.dv + tok0 * D;
-        float hb[2][2] = {}, hg[2][2] = {};
+        float hb[4] = {}, hg[4] = {};
 #pragma unroll
         for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -823,33 +992,33 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
                     if (r < n) *reinterpret_cast<__nv_bfloat162*>(gv + r * D + cc) =
                         __floats2bfloat162_rn(vbeta[r] * a0, vbeta[r] * a1);
                     const float kr = k0 * bf(sK, r * HD + cc) + k1 * bf(sK, r * HD + cc + 1);
-                    hb[i][e2] += a0 * bf(sV, r * HD + cc) + a1 * bf(sV, r * HD + cc + 1) + vgam[r] * kr;
-                    hg[i][e2] += vbeta[r] * vgam[r] * kr;
+                    hb[2 * i + e2] += a0 * bf(sV, r * HD + cc) + a1 * bf(sV, r * HD + cc + 1) + vgam[r] * kr;
+                    hg[2 * i + e2] += vbeta[r] * vgam[r] * kr;
                 }
         add_rows<2>(hb, m0, vdbeta);
         add_rows<2>(hg, m0, vdb);
     }
     __syncthreads();   // dU, dW no longer read
-    for_acc(rv, m0, n0d, [&](int r, int i, float& x) { sdU[r * FD + i] = x; });
-    for_acc(rk, m0, n0d, [&](int r, int i, float& x) { sdW[r * FD + i] = x; });
+    for_acc(rv, m0, n0d, [&](int r, int i, float& x, int rs, int cs) { sdU[r * FD + i] = x; });
+    for_acc(rk, m0, n0d, [&](int r, int i, float& x, int rs, int cs) { sdW[r * FD + i] = x; });
     __syncthreads();
     // dA = -(dRv Ut^T + dRk W^T), strictly lower; F = beta dA o E in place of K K^T
     {
         float da[2][2][4];
         zero(da);
-        warp_mma<2, 2>(da, [&](int m, int k) { return sdU[m * FD + k]; }, [&](int k, int nn) { return sUt[nn * FD + k]; },
-                       m0, n0c, 0, D);
-        warp_mma<2, 2>(da, [&](int m, int k) { return sdW[m * FD + k]; }, [&](int k, int nn) { return sW[nn * FD + k]; },
-                       m0, n0c, 0, D);
-        float hr[2][2] = {}, hc[2][2] = {}, hb[2][2] = {};
-        for_acc(da, m0, n0c, [&](int r, int s, float& x) {
+        warp_mma<2, 2>(da, [&](int m, int k) { return rowf(sdU + m * FD + k); },
+                       [&](int k, int nn) { return rowf(sUt + nn * FD + k); }, m0, n0c, 0, D);
+        warp_mma<2, 2>(da, [&](int m, int k) { return rowf(sdW + m * FD + k); },
+                       [&](int k, int nn) { return rowf(sW + nn * FD + k); }, m0, n0c, 0, D);
+        float hr[4] = {}, hc[4] = {}, hb[4] = {};
+        for_acc(da, m0, n0c, [&](int r, int s, float& x, int rs, int cs) {
             float f = 0.f;
             if (s < r) {
                 const float d = -x, e = expf(vb[r] - vb[s]), kk = sA[r * FC + s];
                 const float aa = d * vbeta[r] * e * kk;
-                hr[(r - m0) >> 4][((r - m0) >> 3) & 1] += aa;
-                hc[(s - n0c) >> 3][(s - n0c) & 1] -= aa;
-                hb[(r - m0) >> 4][((r - m0) >> 3) & 1] += d * e * kk;
+                hr[rs] += aa;
+                hc[cs] -= aa;
+                hb[rs] += d * e * kk;
                 f = vbeta[r] * d * e;
             }
             sA[r * FC + s] = f;
@@ -861,11 +1030,21 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
     __syncthreads();   // F complete
     // dK = F K + F^T K + diag(beta gam) dRk + state terms
     {
+        const float* g1 = p.wdk + ub * C * D;
+        float2 pre[2][NT][2];   // state terms, loaded before the products
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int lane = tid & 31, r = m0 + 16 * i + (lane >> 2) + 8 * e2;
+                    pre[i][j][e2] = *reinterpret_cast<const float2*>(g1 + r * D + n0d + 8 * j + 2 * (lane & 3));
+                }
         float dk[2][NT][4];
         zero(dk);
-        warp_mma<2, NT>(dk, [&](int m, int k) { return sA[m * FC + k]; }, fK, m0, n0d, 0, m0 + 32);
-        warp_mma<2, NT>(dk, [&](int m, int k) { return sA[k * FC + m]; }, fK, m0, n0d, m0, C);
-        const float* g1 = p.wdk + ub * C * D;
+        warp_mma<2, NT, true, false>(dk, [&](int m, int k) { return rowf(sA + m * FC + k); }, fK, m0, n0d, 0, m0 + 32);
+        warp_mma<2, NT, true, false>(dk, [&](int m, int k) { return colf(sA + k * FC + m, FC); }, fK, m0, n0d, m0, C);
         bf16* gk = p.dk + tok0 * D;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
@@ -877,8 +1056,8 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
                     const int cc = n0d + 8 * j + 2 * (lane & 3);
                     if (r < n) {
                         const float bg = vbeta[r] * vgam[r];
-                        const float x0 = dk[i][j][2 * e2] + bg * sdW[r * FD + cc] + g1[r * D + cc];
-                        const float x1 = dk[i][j][2 * e2 + 1] + bg * sdW[r * FD + cc + 1] + g1[r * D + cc + 1];
+                        const float x0 = dk[i][j][2 * e2] + bg * sdW[r * FD + cc] + pre[i][j][e2].x;
+                        const float x1 = dk[i][j][2 * e2 + 1] + bg * sdW[r * FD + cc + 1] + pre[i][j][e2].y;
                         *reinterpret_cast<__nv_bfloat162*>(gk + r * D + cc) = __floats2bfloat162_rn(x0, x1);
                     }
                 }
@@ -913,17 +1092,16 @@ template <int D>
 cudaError_t launch_all(const Params& p, cudaStream_t s) {
     const int units = p.BH * p.NC;
     cudaError_t e;
-#define LA_GBW_LAUNCH(kern, grid, bytes)                                                                   \
+#define LA_GBW_LAUNCH(kern, grid, bytes, threads)                                                          \
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)); \
     if (e != cudaSuccess) return e;                                                                        \
-    kern<<<grid, kThreads, bytes, s>>>(p);                                                                 \
+    kern<<<grid, threads, bytes, s>>>(p);                                                                  \
     e = cudaGetLastError();                                                                                \
     if (e != cudaSuccess) return e;
-    LA_GBW_LAUNCH(prep_kernel<D>, units, PrepSmem<D>::BYTES)
-    LA_GBW_LAUNCH((chain_kernel<D, false>), p.BH * (D / kRows), ChainSmem<D>::BYTES)
-    LA_GBW_LAUNCH((chain_kernel<D, true>), p.BH * (D / kRows), ChainSmem<D>::BYTES)
-    LA_GBW_LAUNCH(grad_state_kernel<D>, units, GradASmem<D>::BYTES)
-    LA_GBW_LAUNCH(grad_rest_kernel<D>, units, GradBSmem<D>::BYTES)
+    LA_GBW_LAUNCH(prep_kernel<D>, units, PrepSmem<D>::BYTES, kThreads)
+    LA_GBW_LAUNCH(chain_kernel<D>, 2 * p.BH * kChainSplit, ChainSmem<D>::BYTES, 2 * D / kChainSplit)
+    LA_GBW_LAUNCH(grad_state_kernel<D>, units, GradASmem<D>::BYTES, kThreads)
+    LA_GBW_LAUNCH(grad_rest_kernel<D>, units, GradBSmem<D>::BYTES, kThreads)
 #undef LA_GBW_LAUNCH
     return cudaSuccess;
 }
@@ -937,11 +1115,13 @@ size_t carve(Params& p, uint8_t* base, int BH, int T, int D) {
         off += (bytes + 255) & ~static_cast<size_t>(255);
         return r;
     };
-    p.wb = reinterpret_cast<float*>(take(units * C * 4));
+    p.wb = reinterpret_cast<float*>(take(units * 2 * C * 4));
     p.wti = reinterpret_cast<float*>(take(units * C * C * 4));
     p.ww = reinterpret_cast<float*>(take(units * C * D * 4));
     p.wut = reinterpret_cast<float*>(take(units * C * D * 4));
-    p.wqh = reinterpret_cast<float*>(take(units * C * D * 4));
+    p.wqht = reinterpret_cast<float*>(take(units * C * D * 4));
+    p.wlkt = reinterpret_cast<float*>(take(units * C * D * 4));
+    p.wlwt = reinterpret_cast<float*>(take(units * C * D * 4));
     p.ws0 = reinterpret_cast<bf16*>(take(units * D * D * 2));
     p.wsc = reinterpret_cast<bf16*>(take(units * D * D * 2));
     p.wdu = reinterpret_cast<float*>(take(units * C * D * 4));
