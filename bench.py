@@ -564,7 +564,7 @@ def gpu_arm(args):
                       "gpu_launches": args.steps * br.launches_per_step})
         del br
         torch.cuda.empty_cache()
-        # the gated delta rule's backward on the headline's shapes (token-serial)
+        # the gated delta rule's backward on the headline's shapes (chunkwise)
         gs = max(3, args.steps // 4)
         gr = GatedBackwardRunner(GATED_BACKWARD, 0, torch, la)
         tot, per = time_steps(gr, gs, args.warmup, torch)
@@ -580,7 +580,8 @@ def gpu_arm(args):
                                    "traffic": traffic_from_profiles("backward/gdn"), "algorithmic_bytes": byts,
                                    "kernel_ms": round(kms, 4),
                                    "peak_source": pk["source"] + " (burst copy bandwidth)",
-                                   "note": "token-serial CUDA-core kernel (rows split over CTAs): latency-bound"},
+                                   "note": "chunkwise: per-chunk prep, both chunk chains in one launch, two "
+                                           "per-chunk gradient kernels; warp-level tf32 MMAs"},
                       "gpu_launches": gs * gr.launches_per_step})
         del gr
         torch.cuda.empty_cache()

@@ -322,15 +322,26 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
  * LA_FLAG_IDENTITY_PHI). LA_GLA and LA_NORM_DECAY take no beta: beta and
  * dbeta may be NULL and are ignored; LA_GLA's state_in, dstate_out and
  * dstate_in are [B,H,d_k*d_v] (S [d_k][d_v]).
- * Token-serial CUDA-core kernel: the state's value rows (LA_GLA: its key
- * channels) are split over CTAs of 16 rows, run forward with checkpoints
- * every 8 tokens, then walked back segment by segment; sums over rows are
- * accumulated in fp32 (the order of those additions varies from run to run,
- * so the last bits of dq, dk, dgate and dbeta, or of LA_GLA's dv, may too).
- * Its workspace (4 * B*H * (ceil(T/8) * d_v*d_k + 2*T*d_k) bytes; LA_GLA:
- * T*d_v in place of 2*T*d_k) is allocated by the handle on first use and
- * grown when a call needs more (la_destroy frees it). la_last_launches reports 2 (plus
- * memsets of the accumulated outputs, not counted).
+ * LA_GDN with bf16 io and d_k = d_v (64 or 128): the chunkwise form (chunks
+ * of 64 tokens), five launches: a per-chunk prep (the UT inverse of the
+ * chunk and its W, Ut and gam Q - P W), one launch walking both chunk chains
+ * (the state forward, its gradient backward, value rows split over CTAs),
+ * and two per-chunk gradient kernels; every product is a tf32 MMA with fp32
+ * accumulation. Its workspace is 4 * B*H * ceil(T/64) * (8*64*d + 64*64 +
+ * 4*64) + 2 * B*H * ceil(T/64) * 2*d*d bytes (d = d_k, each part rounded up
+ * to 256 bytes); la_last_launches reports 5. The gate gradient's per-chunk
+ * terms are added by several CTAs in fp32, so its last bits may vary from
+ * run to run.
+ * Every other case: a token-serial CUDA-core kernel: the state's value rows
+ * (LA_GLA: its key channels) are split over CTAs of 16 rows, run forward
+ * with checkpoints every 8 tokens, then walked back segment by segment; sums
+ * over rows are accumulated in fp32 (the order of those additions varies
+ * from run to run, so the last bits of dq, dk, dgate and dbeta, or of
+ * LA_GLA's dv, may too). Its workspace (4 * B*H * (ceil(T/8) * d_v*d_k +
+ * 2*T*d_k) bytes; LA_GLA: T*d_v in place of 2*T*d_k) and the chunkwise one
+ * are allocated by the handle on first use and grown when a call needs more
+ * (la_destroy frees it). la_last_launches reports 2 (plus memsets of the
+ * accumulated outputs, not counted).
  * Errors: LA_ERR_UNSUPPORTED for another variant or head size,
  * LA_ERR_INVALID_ARG (T < 1, a required pointer NULL), LA_ERR_MISALIGNED,
  * LA_ERR_CUDA.
@@ -347,7 +358,8 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
  * count (1: the recurrent kernel or a decode step; 1 or 2: the chunk kernel,
  * with segment summaries when B*H is small; 3: the three-phase parallel form;
  * LA_GDN, LA_KDA and LA_GLA: one per group of 32 sequence-heads; la_backward:
- * 5 per head group for the chunkwise form, 1 for the token-serial kernel). */
+ * 5 per head group for the chunkwise form, 1 for the token-serial kernel;
+ * la_backward_gated: 5 for the chunkwise form, 2 for the token-serial one). */
 int la_last_launches(const la_handle* h);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
