@@ -62,7 +62,9 @@ namespace la {
 namespace gbw {
 
 constexpr int C = 64;            // tokens per chunk
-constexpr int kThreads = 256;    // eight warps
+constexpr int kThreads = 256;    // eight warps (prep)
+constexpr int kGradThreads = 512;   // sixteen warps (gradient kernels), each a 16-row tile:
+constexpr int GMT = 1;              // m16 tiles per warp in the per-chunk products
 using bf16 = __nv_bfloat16;
 
 template <int D>
@@ -269,14 +271,13 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// rows x cols tile copy, global row stride gs, shared row stride ss (both in
+// rows x COLS tile copy, global row stride gs, shared row stride ss (both in
 // elements of T), rows >= valid filled with zeros; asynchronous 16-byte
 // pieces (the caller commits and waits).
-template <typename T>
-__device__ __forceinline__ void copy_tile_async(T* dst, int ss, const T* src, size_t gs, int rows, int cols,
-                                                int valid) {
+template <int COLS, typename T>
+__device__ __forceinline__ void copy_tile_async(T* dst, int ss, const T* src, size_t gs, int rows, int valid) {
     constexpr int E = 16 / sizeof(T);
-    const int per = cols / E;
+    constexpr int per = COLS / E;   // a power of two: the index split is shifts
     for (int x = threadIdx.x; x < rows * per; x += blockDim.x) {
         const int r = x / per, c = (x % per) * E;
         const bool in = r < valid;
@@ -346,9 +347,9 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Params p) {
     const int n = min(C, p.T - c * C);
     const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
 
-    copy_tile_async(sQ, HD, p.q + tok0 * D, D, C, D, n);
-    copy_tile_async(sK, HD, p.k + tok0 * D, D, C, D, n);
-    copy_tile_async(sV, HD, p.v + tok0 * D, D, C, D, n);
+    copy_tile_async<D>(sQ, HD, p.q + tok0 * D, D, C, n);
+    copy_tile_async<D>(sK, HD, p.k + tok0 * D, D, C, n);
+    copy_tile_async<D>(sV, HD, p.v + tok0 * D, D, C, n);
     cp_async_commit();
     gate_sums(p, tok0, n, vb, vbeta);
     for (int x = tid; x < C * FC; x += kThreads) sT[x] = 0.f;
@@ -528,15 +529,15 @@ __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, ui
         const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
         uint8_t* b = stage(buf);
         if (!rev) {
-            copy_tile_async(reinterpret_cast<float*>(b), FW, p.ww + ub * C * D, D, C, D, C);
-            copy_tile_async(reinterpret_cast<bf16*>(b + L::W_T), HD, p.q + tok0 * D, D, C, D, n);
-            copy_tile_async(reinterpret_cast<float*>(b + L::W_T + L::H_T), FT, p.wlkt + ub * C * D, C, D, C, D);
-            copy_tile_async(reinterpret_cast<float*>(b + L::FWD - C * 4), C, p.wb + ub * 2 * C + C, C, 1, C, 1);
+            copy_tile_async<D>(reinterpret_cast<float*>(b), FW, p.ww + ub * C * D, D, C, C);
+            copy_tile_async<D>(reinterpret_cast<bf16*>(b + L::W_T), HD, p.q + tok0 * D, D, C, n);
+            copy_tile_async<C>(reinterpret_cast<float*>(b + L::W_T + L::H_T), FT, p.wlkt + ub * C * D, C, D, D);
+            copy_tile_async<C>(reinterpret_cast<float*>(b + L::FWD - C * 4), C, p.wb + ub * 2 * C + C, C, 1, 1);
         } else {
-            copy_tile_async(reinterpret_cast<bf16*>(b), HD, p.k + tok0 * D, D, C, D, n);
-            copy_tile_async(reinterpret_cast<float*>(b + L::H_T), FT, p.wlwt + ub * C * D, C, D, C, D);
-            copy_tile_async(reinterpret_cast<float*>(b + L::H_T + L::T_T), FT, p.wqht + ub * C * D, C, D, C, D);
-            copy_tile_async(reinterpret_cast<float*>(b + L::REV - C * 4), C, p.wb + ub * 2 * C + C, C, 1, C, 1);
+            copy_tile_async<D>(reinterpret_cast<bf16*>(b), HD, p.k + tok0 * D, D, C, n);
+            copy_tile_async<C>(reinterpret_cast<float*>(b + L::H_T), FT, p.wlwt + ub * C * D, C, D, D);
+            copy_tile_async<C>(reinterpret_cast<float*>(b + L::H_T + L::T_T), FT, p.wqht + ub * C * D, C, D, D);
+            copy_tile_async<C>(reinterpret_cast<float*>(b + L::REV - C * 4), C, p.wb + ub * 2 * C + C, C, 1, 1);
         }
     };
     // the warp's slice of Ut (state chain) and of dO for chunk step j, in
@@ -735,7 +736,7 @@ struct GradASmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p) {
+__global__ void __launch_bounds__(kGradThreads, 1) grad_state_kernel(const Params p) {
     using Dm = Dims<D>;
     using L = GradASmem<D>;
     constexpr int FD = Dm::FD, HD = Dm::HD, FC = Dm::FC, NT = Dm::NT;
@@ -759,13 +760,13 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
     const size_t ub = static_cast<size_t>(unit);
 
-    copy_tile_async(sQ, HD, p.q + tok0 * D, D, C, D, n);
-    copy_tile_async(sK, HD, p.k + tok0 * D, D, C, D, n);
-    copy_tile_async(sO, HD, p.dout + tok0 * D, D, C, D, n);
-    copy_tile_async(sS0, HD, p.ws0 + ub * D * D, D, D, D, D);
-    copy_tile_async(sSC, HD, p.wsc + ub * D * D, D, D, D, D);
-    copy_tile_async(sW, FD, p.ww + ub * C * D, D, C, D, C);
-    copy_tile_async(sU, FD, p.wut + ub * C * D, D, C, D, C);
+    copy_tile_async<D>(sQ, HD, p.q + tok0 * D, D, C, n);
+    copy_tile_async<D>(sK, HD, p.k + tok0 * D, D, C, n);
+    copy_tile_async<D>(sO, HD, p.dout + tok0 * D, D, C, n);
+    copy_tile_async<D>(sS0, HD, p.ws0 + ub * D * D, D, D, D);
+    copy_tile_async<D>(sSC, HD, p.wsc + ub * D * D, D, D, D);
+    copy_tile_async<D>(sW, FD, p.ww + ub * C * D, D, C, C);
+    copy_tile_async<D>(sU, FD, p.wut + ub * C * D, D, C, C);
     cp_async_commit();
     if (tid < C) {
         vb[tid] = p.wb[ub * 2 * C + tid];
@@ -780,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     }
     __syncthreads();
     const float gC = expf(vb[C - 1]);
-    const int m0 = (warp >> 2) * 32, n0c = (warp & 3) * 16, n0d = (warp & 3) * (D / 4);
+    const int m0 = (warp >> 2) * 16 * GMT, n0c = (warp & 3) * 16, n0d = (warp & 3) * (D / 4);
     const auto fQ = [&](int m, int k) { return rowh(sQ + m * HD + k); };
     const auto fQc = [&](int k, int nn) { return colh(sQ + k * HD + nn, HD); };
     const auto fO = [&](int m, int k) { return rowh(sO + m * HD + k); };
@@ -794,29 +795,29 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
 
     // P = lower(E o Q K^T); U = Ut - W S_0^T (in place); dQ <- gam dO S_0
     {
-        float qk[2][2][4];
+        float qk[GMT][2][4];
         zero(qk);
-        warp_mma<2, 2, false, false>(qk, fQ, fKt, m0, n0c, 0, D);
+        warp_mma<GMT, 2, false, false>(qk, fQ, fKt, m0, n0c, 0, D);
         for_acc(qk, m0, n0c, [&](int r, int s, float& x, int rs, int cs) {
             sP[r * FC + s] = s <= r ? expf(vb[r] - vb[s]) * x : 0.f;
         });
-        float ws[2][NT][4];
+        float ws[GMT][NT][4];
         zero(ws);
-        warp_mma<2, NT, true, false>(ws, [&](int m, int k) { return rowf(sW + m * FD + k); }, fS0t, m0, n0d, 0, D);
+        warp_mma<GMT, NT, true, false>(ws, [&](int m, int k) { return rowf(sW + m * FD + k); }, fS0t, m0, n0d, 0, D);
         for_acc(ws, m0, n0d, [&](int r, int i, float& x, int rs, int cs) { sU[r * FD + i] -= x; });
     }
-    float dq[2][NT][4];
+    float dq[GMT][NT][4];
     zero(dq);
-    warp_mma<2, NT, false, false>(dq, fO, fS0, m0, n0d, 0, D);
+    warp_mma<GMT, NT, false, false>(dq, fO, fS0, m0, n0d, 0, D);
     for_acc(dq, m0, n0d, [&](int r, int k, float& x, int rs, int cs) { x *= vgam[r]; });
     __syncthreads();   // sP, sU complete; W no longer read
     // dU = P^T dO + diag(lam) K dS_C^T -> sW and the workspace
     {
-        float du[2][NT][4];
+        float du[GMT][NT][4];
         zero(du);
-        warp_mma<2, NT, true, false>(du, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fOc,
+        warp_mma<GMT, NT, true, false>(du, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fOc,
                         m0, n0d, m0, C);
-        warp_mma<2, NT, true, false>(du, [&](int m, int k) { return scale2(rowh(sK + m * HD + k), vlam[m]); }, fSCt, m0,
+        warp_mma<GMT, NT, true, false>(du, [&](int m, int k) { return scale2(rowh(sK + m * HD + k), vlam[m]); }, fSCt, m0,
                                      n0d, 0, D);
         float* g = p.wdu + ub * C * D;
         for_acc(du, m0, n0d, [&](int r, int i, float& x, int rs, int cs) {
@@ -827,15 +828,15 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     __syncthreads();
     // dW = -dU S_0 -> workspace; dP = lower(dO U^T) -> dP o E in place of P
     {
-        float dw[2][NT][4];
+        float dw[GMT][NT][4];
         zero(dw);
-        warp_mma<2, NT, true, false>(dw, [&](int m, int k) { return rowf(sW + m * FD + k); }, fS0, m0, n0d, 0, D);
+        warp_mma<GMT, NT, true, false>(dw, [&](int m, int k) { return rowf(sW + m * FD + k); }, fS0, m0, n0d, 0, D);
         float* g = p.wdw + ub * C * D;
         for_acc(dw, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) { g[r * D + kk] = -x; });
-        float dp[2][2][4];
+        float dp[GMT][2][4];
         zero(dp);
-        warp_mma<2, 2, false, true>(dp, fO, [&](int k, int nn) { return rowf(sU + nn * FD + k); }, m0, n0c, 0, D);
-        float hr[4] = {}, hc[4] = {};
+        warp_mma<GMT, 2, false, true>(dp, fO, [&](int k, int nn) { return rowf(sU + nn * FD + k); }, m0, n0c, 0, D);
+        float hr[2 * GMT] = {}, hc[4] = {};
         for_acc(dp, m0, n0c, [&](int r, int s, float& x, int rs, int cs) {
             float out = 0.f;
             if (s <= r) {
@@ -846,16 +847,16 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
             }
             sP[r * FC + s] = out;
         });
-        add_rows<2>(hr, m0, vdb);
+        add_rows<GMT>(hr, m0, vdb);
         add_cols<2>(hc, n0c, vdb);
     }
     __syncthreads();   // dP o E complete
     // dQ += (dP o E) K -> global
-    warp_mma<2, NT, true, false>(dq, [&](int m, int k) { return rowf(sP + m * FC + k); }, fK, m0, n0d, 0, m0 + 32);
+    warp_mma<GMT, NT, true, false>(dq, [&](int m, int k) { return rowf(sP + m * FC + k); }, fK, m0, n0d, 0, m0 + 16 * GMT);
     {
         bf16* g = p.dq + tok0 * D;
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < GMT; ++i)
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int lane = tid & 31, r = m0 + 16 * i + (lane >> 2), cc = n0d + 8 * j + 2 * (lane & 3);
@@ -868,29 +869,29 @@ __global__ void __launch_bounds__(kThreads, 1) grad_state_kernel(const Params p)
     }
     // state terms of dK: diag(lam) U dS_C (and c_s), then + (dP o E)^T Q
     {
-        float dk[2][NT][4];
+        float dk[GMT][NT][4];
         zero(dk);
-        warp_mma<2, NT, true, false>(dk, [&](int m, int k) { return scale2(rowf(sU + m * FD + k), vlam[m]); }, fSC, m0,
+        warp_mma<GMT, NT, true, false>(dk, [&](int m, int k) { return scale2(rowf(sU + m * FD + k), vlam[m]); }, fSC, m0,
                                      n0d, 0, D);
-        float h[4] = {};
+        float h[2 * GMT] = {};
         for_acc(dk, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) {
             h[rs] -= x * bf(sK, r * HD + kk);
         });
         float tot = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tot -= h[i];
-        add_rows<2>(h, m0, vdb);
+        for (int i = 0; i < 2 * GMT; ++i) tot -= h[i];
+        add_rows<GMT>(h, m0, vdb);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
         if ((tid & 31) == 0) atomicAdd(vdb + C - 1, tot);
-        warp_mma<2, NT, true, false>(dk, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fQc, m0, n0d, m0, C);
+        warp_mma<GMT, NT, true, false>(dk, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fQc, m0, n0d, m0, C);
         float* g = p.wdk + ub * C * D;
         for_acc(dk, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) { g[r * D + kk] = x; });
     }
     // gam_C <dS_C, S_0>
     {
         float s = 0.f;
-        for (int x = tid; x < D * D; x += kThreads) {
+        for (int x = tid; x < D * D; x += kGradThreads) {
             const int r = x / D, cc = x % D;
             s += bf(sSC, r * HD + cc) * bf(sS0, r * HD + cc);
         }
@@ -919,7 +920,7 @@ struct GradBSmem {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) {
+__global__ void __launch_bounds__(kGradThreads, 1) grad_rest_kernel(const Params p) {
     using Dm = Dims<D>;
     using L = GradBSmem<D>;
     constexpr int FD = Dm::FD, HD = Dm::HD, FC = Dm::FC, NT = Dm::NT;
@@ -943,13 +944,13 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
     const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
     const size_t ub = static_cast<size_t>(unit);
 
-    copy_tile_async(sT, FC, p.wti + ub * C * C, C, C, C, C);
-    copy_tile_async(sW, FD, p.ww + ub * C * D, D, C, D, C);
-    copy_tile_async(sUt, FD, p.wut + ub * C * D, D, C, D, C);
-    copy_tile_async(sdU, FD, p.wdu + ub * C * D, D, C, D, C);
-    copy_tile_async(sdW, FD, p.wdw + ub * C * D, D, C, D, C);
-    copy_tile_async(sK, HD, p.k + tok0 * D, D, C, D, n);
-    copy_tile_async(sV, HD, p.v + tok0 * D, D, C, D, n);
+    copy_tile_async<C>(sT, FC, p.wti + ub * C * C, C, C, C);
+    copy_tile_async<D>(sW, FD, p.ww + ub * C * D, D, C, C);
+    copy_tile_async<D>(sUt, FD, p.wut + ub * C * D, D, C, C);
+    copy_tile_async<D>(sdU, FD, p.wdu + ub * C * D, D, C, C);
+    copy_tile_async<D>(sdW, FD, p.wdw + ub * C * D, D, C, C);
+    copy_tile_async<D>(sK, HD, p.k + tok0 * D, D, C, n);
+    copy_tile_async<D>(sV, HD, p.v + tok0 * D, D, C, n);
     cp_async_commit();
     if (tid < C) {
         vb[tid] = p.wb[ub * 2 * C + tid];
@@ -961,26 +962,26 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
     __syncthreads();
     if (tid < C) vgam[tid] = expf(vb[tid]);
     __syncthreads();
-    const int m0 = (warp >> 2) * 32, n0c = (warp & 3) * 16, n0d = (warp & 3) * (D / 4);
+    const int m0 = (warp >> 2) * 16 * GMT, n0c = (warp & 3) * 16, n0d = (warp & 3) * (D / 4);
     const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
     // dRv = Ti^T dU, dRk = Ti^T dW (Ti^T upper: k >= m0); K K^T -> sA
-    float rv[2][NT][4], rk[2][NT][4];
+    float rv[GMT][NT][4], rk[GMT][NT][4];
     zero(rv);
     zero(rk);
     {
         const auto ftt = [&](int m, int k) { return colf(sT + k * FC + m, FC); };
-        warp_mma<2, NT>(rv, ftt, [&](int k, int nn) { return colf(sdU + k * FD + nn, FD); }, m0, n0d, m0, C);
-        warp_mma<2, NT>(rk, ftt, [&](int k, int nn) { return colf(sdW + k * FD + nn, FD); }, m0, n0d, m0, C);
-        float kk[2][2][4];
+        warp_mma<GMT, NT>(rv, ftt, [&](int k, int nn) { return colf(sdU + k * FD + nn, FD); }, m0, n0d, m0, C);
+        warp_mma<GMT, NT>(rk, ftt, [&](int k, int nn) { return colf(sdW + k * FD + nn, FD); }, m0, n0d, m0, C);
+        float kk[GMT][2][4];
         zero(kk);
-        warp_mma<2, 2, false, false>(kk, [&](int m, int k) { return rowh(sK + m * HD + k); },
+        warp_mma<GMT, 2, false, false>(kk, [&](int m, int k) { return rowh(sK + m * HD + k); },
                                      [&](int k, int nn) { return rowh(sK + nn * HD + k); }, m0, n0c, 0, D);
         for_acc(kk, m0, n0c, [&](int r, int s, float& x, int rs, int cs) { sA[r * FC + s] = x; });
         // dV = beta dRv; dbeta += dRv.v + gam dRk.k; db += beta gam dRk.k
         bf16* gv = p.dv + tok0 * D;
-        float hb[4] = {}, hg[4] = {};
+        float hb[2 * GMT] = {}, hg[2 * GMT] = {};
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < GMT; ++i)
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -995,8 +996,8 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
                     hb[2 * i + e2] += a0 * bf(sV, r * HD + cc) + a1 * bf(sV, r * HD + cc + 1) + vgam[r] * kr;
                     hg[2 * i + e2] += vbeta[r] * vgam[r] * kr;
                 }
-        add_rows<2>(hb, m0, vdbeta);
-        add_rows<2>(hg, m0, vdb);
+        add_rows<GMT>(hb, m0, vdbeta);
+        add_rows<GMT>(hg, m0, vdb);
     }
     __syncthreads();   // dU, dW no longer read
     for_acc(rv, m0, n0d, [&](int r, int i, float& x, int rs, int cs) { sdU[r * FD + i] = x; });
@@ -1004,13 +1005,13 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
     __syncthreads();
     // dA = -(dRv Ut^T + dRk W^T), strictly lower; F = beta dA o E in place of K K^T
     {
-        float da[2][2][4];
+        float da[GMT][2][4];
         zero(da);
-        warp_mma<2, 2>(da, [&](int m, int k) { return rowf(sdU + m * FD + k); },
+        warp_mma<GMT, 2>(da, [&](int m, int k) { return rowf(sdU + m * FD + k); },
                        [&](int k, int nn) { return rowf(sUt + nn * FD + k); }, m0, n0c, 0, D);
-        warp_mma<2, 2>(da, [&](int m, int k) { return rowf(sdW + m * FD + k); },
+        warp_mma<GMT, 2>(da, [&](int m, int k) { return rowf(sdW + m * FD + k); },
                        [&](int k, int nn) { return rowf(sW + nn * FD + k); }, m0, n0c, 0, D);
-        float hr[4] = {}, hc[4] = {}, hb[4] = {};
+        float hr[2 * GMT] = {}, hc[4] = {}, hb[2 * GMT] = {};
         for_acc(da, m0, n0c, [&](int r, int s, float& x, int rs, int cs) {
             float f = 0.f;
             if (s < r) {
@@ -1023,9 +1024,9 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
             }
             sA[r * FC + s] = f;
         });
-        add_rows<2>(hr, m0, vdb);
+        add_rows<GMT>(hr, m0, vdb);
         add_cols<2>(hc, n0c, vdb);
-        add_rows<2>(hb, m0, vdbeta);
+        add_rows<GMT>(hb, m0, vdbeta);
     }
     __syncthreads();   // F complete
     // dK = F K + F^T K + diag(beta gam) dRk + state terms
@@ -1033,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
         const float* g1 = p.wdk + ub * C * D;
         float2 pre[2][NT][2];   // state terms, loaded before the products
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < GMT; ++i)
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -1041,13 +1042,13 @@ __global__ void __launch_bounds__(kThreads, 1) grad_rest_kernel(const Params p) 
                     const int lane = tid & 31, r = m0 + 16 * i + (lane >> 2) + 8 * e2;
                     pre[i][j][e2] = *reinterpret_cast<const float2*>(g1 + r * D + n0d + 8 * j + 2 * (lane & 3));
                 }
-        float dk[2][NT][4];
+        float dk[GMT][NT][4];
         zero(dk);
-        warp_mma<2, NT, true, false>(dk, [&](int m, int k) { return rowf(sA + m * FC + k); }, fK, m0, n0d, 0, m0 + 32);
-        warp_mma<2, NT, true, false>(dk, [&](int m, int k) { return colf(sA + k * FC + m, FC); }, fK, m0, n0d, m0, C);
+        warp_mma<GMT, NT, true, false>(dk, [&](int m, int k) { return rowf(sA + m * FC + k); }, fK, m0, n0d, 0, m0 + 16 * GMT);
+        warp_mma<GMT, NT, true, false>(dk, [&](int m, int k) { return colf(sA + k * FC + m, FC); }, fK, m0, n0d, m0, C);
         bf16* gk = p.dk + tok0 * D;
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < GMT; ++i)
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -1100,8 +1101,8 @@ cudaError_t launch_all(const Params& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     LA_GBW_LAUNCH(prep_kernel<D>, units, PrepSmem<D>::BYTES, kThreads)
     LA_GBW_LAUNCH(chain_kernel<D>, 2 * p.BH * kChainSplit, ChainSmem<D>::BYTES, 2 * D / kChainSplit)
-    LA_GBW_LAUNCH(grad_state_kernel<D>, units, GradASmem<D>::BYTES, kThreads)
-    LA_GBW_LAUNCH(grad_rest_kernel<D>, units, GradBSmem<D>::BYTES, kThreads)
+    LA_GBW_LAUNCH(grad_state_kernel<D>, units, GradASmem<D>::BYTES, kGradThreads)
+    LA_GBW_LAUNCH(grad_rest_kernel<D>, units, GradBSmem<D>::BYTES, kGradThreads)
 #undef LA_GBW_LAUNCH
     return cudaSuccess;
 }
