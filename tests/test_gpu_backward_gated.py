@@ -117,3 +117,35 @@ def test_backward_gated_rejects_what_it_cannot_run():
         h.backward_gated(z, z, z, g, g, z)
     assert e.value.code == la.LA_ERR_UNSUPPORTED
     h.close()
+
+
+def test_backward_gdn_full_size_sampled_heads():
+    # The gated delta rule's gradients at the benchmark's full size (B2 H16
+    # T8192 d128, bf16: the chunkwise path, every sequence-head on the GPU),
+    # with a final-state cotangent; the first and the last sequence-head
+    # against the float64 token-by-token oracle (about 1 GB of states each).
+    import torch
+    from oracle import backward
+    w = W.GDN_B2H16_T8192_D128
+    inp = W.draw(w, 0)
+    q, k, v, g, b = oracle_inputs(inp)
+    rng = np.random.default_rng(1)
+    do_s = W.round_io(rng.standard_normal((w.B, w.H, w.T, w.dv)), w.io)
+    dso = (rng.standard_normal((w.B, w.H, w.dv * w.dk)) * 0.05).astype(np.float32)
+    h = la.Handle(w.B, w.H, w.dk, w.dv, io=w.io)
+    dev = h.device
+    got = h.backward_gated(to_torch(inp.q, dev), to_torch(inp.k, dev), to_torch(inp.v, dev), to_torch(inp.gate, dev),
+                           to_torch(inp.beta, dev), to_torch(do_s, dev), None, torch.from_numpy(dso).to(dev),
+                           variant="gdn")
+    torch.cuda.synchronize()
+    assert h.last_launches() == 5 and h.status() == la.LA_OK
+    h.close()
+    got = [x.float().cpu().numpy() for x in got]
+    do64 = W.as_f64(do_s)
+    for bi, hi in ((0, 0), (w.B - 1, w.H - 1)):
+        sl = lambda a: a[bi:bi + 1, hi:hi + 1]
+        ref = backward.delta_backward(sl(q), sl(k), sl(v), sl(g), sl(b), sl(do64), None, sl(dso))
+        for name, x, r in zip(NAMES, got, ref):
+            e = slice_rel_err(sl(x), r)
+            assert np.all(np.isfinite(sl(x))), name
+            assert e <= TOL["bf16"], (bi, hi, name, e)
