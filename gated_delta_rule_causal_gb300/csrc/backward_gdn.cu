@@ -494,30 +494,37 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Params p) {
 //    state chain:    Y = X W^T,  Z = Ut^T - Y,   X <- gam_C X + Z (lam K)
 //    gradient chain: Y = X K^T,  Z = -Y,         X <- gam_C X + Z (lam W) + dO^T Qh
 // The B operands come from double-buffered tiles (W, Q, K as stored; the
-// transposed lam K, lam W and Qh written by the prep), the Ut and dO slices
-// of the warp's rows from registers loaded a chunk ahead.
+// transposed lam K, lam W and Qh written by the prep), staged two chunks
+// ahead with the Ut and dO slices of the CTA's rows.
+
+constexpr int kChainSplit = 2;   // CTAs per (sequence-head, direction), D / kChainSplit rows each
 
 template <int D>
 struct ChainSmem {
+    static constexpr int RW = D / kChainSplit;   // the CTA's value rows
     static constexpr int FW = D + 8;    // fp32 [C][FW]: W (pairs along d)
     static constexpr int HD = D + 8;    // bf16 [C][HD]: Q, K (pairs along d)
     static constexpr int FT = C + 8;    // fp32 [D][FT]: (lam K)^T, (lam W)^T, Qh^T (pairs along tokens)
+    static constexpr int SU = RW + 4;   // fp32 [C][SU]: the CTA's columns of Ut
+    static constexpr int SO = RW + 8;   // bf16 [C][SO]: the CTA's columns of dO
     static constexpr size_t W_T = size_t(C) * FW * 4, H_T = size_t(C) * HD * 2, T_T = size_t(D) * FT * 4;
-    // state chain: W, Q, (lam K)^T, gam; gradient chain: K, (lam W)^T, Qh^T, gam
-    static constexpr size_t FWD = W_T + H_T + T_T + C * 4;
-    static constexpr size_t REV = H_T + 2 * T_T + C * 4;
+    static constexpr size_t U_T = size_t(C) * SU * 4, O_T = size_t(C) * SO * 2;
+    // state chain: W, Q, (lam K)^T, Ut slice, dO slice, gam;
+    // gradient chain: K, (lam W)^T, Qh^T, dO slice, gam
+    static constexpr size_t FWD = W_T + H_T + T_T + U_T + O_T + C * 4;
+    static constexpr size_t REV = H_T + 2 * T_T + O_T + C * 4;
     static constexpr size_t STAGE = ((FWD > REV ? FWD : REV) + 127) / 128 * 128;
     static constexpr size_t BYTES = 2 * STAGE;
+    static_assert(BYTES <= 232448, "two stages fit the opt-in shared memory");
 };
-
-constexpr int kChainSplit = 2;   // CTAs per (sequence-head, direction), D / kChainSplit rows each
 
 template <int D, bool rev>
 __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, uint8_t* smem) {
     using L = ChainSmem<D>;
     constexpr int FW = L::FW, HD = L::HD, FT = L::FT, NJ = D / 8;   // NJ column blocks of X
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int row0 = part * (D / kChainSplit) + 16 * warp;   // this warp's first row
+    constexpr int RW = L::RW, SU = L::SU, SO = L::SO;
+    const int rbase = part * RW, rl = 16 * warp, row0 = rbase + rl;   // the CTA's and this warp's first row
     const int NC = p.NC;
     const size_t ss = static_cast<size_t>(D) * D;
 
@@ -532,40 +539,20 @@ __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, ui
             copy_tile_async<D>(reinterpret_cast<float*>(b), FW, p.ww + ub * C * D, D, C, C);
             copy_tile_async<D>(reinterpret_cast<bf16*>(b + L::W_T), HD, p.q + tok0 * D, D, C, n);
             copy_tile_async<C>(reinterpret_cast<float*>(b + L::W_T + L::H_T), FT, p.wlkt + ub * C * D, C, D, D);
+            copy_tile_async<RW>(reinterpret_cast<float*>(b + L::W_T + L::H_T + L::T_T), SU,
+                                p.wut + ub * C * D + rbase, D, C, C);
+            copy_tile_async<RW>(reinterpret_cast<bf16*>(b + L::W_T + L::H_T + L::T_T + L::U_T), SO,
+                                p.dout + tok0 * D + rbase, D, C, n);
             copy_tile_async<C>(reinterpret_cast<float*>(b + L::FWD - C * 4), C, p.wb + ub * 2 * C + C, C, 1, 1);
         } else {
             copy_tile_async<D>(reinterpret_cast<bf16*>(b), HD, p.k + tok0 * D, D, C, n);
             copy_tile_async<C>(reinterpret_cast<float*>(b + L::H_T), FT, p.wlwt + ub * C * D, C, D, D);
             copy_tile_async<C>(reinterpret_cast<float*>(b + L::H_T + L::T_T), FT, p.wqht + ub * C * D, C, D, D);
+            copy_tile_async<RW>(reinterpret_cast<bf16*>(b + L::H_T + 2 * L::T_T), SO, p.dout + tok0 * D + rbase, D, C,
+                                n);
             copy_tile_async<C>(reinterpret_cast<float*>(b + L::REV - C * 4), C, p.wb + ub * 2 * C + C, C, 1, 1);
         }
     };
-    // the warp's slice of Ut (state chain) and of dO for chunk step j, in
-    // accumulator order: [block jb][row half h][pair e]; loaded once the
-    // previous step's are used, a little under a step ahead
-    float ut[8][2][2];
-    uint32_t dop[8][2];   // dO as bf16 pairs (tokens 8 jb + 2t, +1 at row g + 8h)
-    auto fetch = [&](int j, float (&u)[8][2][2], uint32_t (&o)[8][2]) {
-        const int c = rev ? NC - 1 - j : j;
-        const int n = min(C, p.T - c * C);
-        const size_t ub = static_cast<size_t>(bh) * NC + c;
-        const size_t tok0 = static_cast<size_t>(bh) * p.T + static_cast<size_t>(c) * C;
-        const uint16_t* dO = reinterpret_cast<const uint16_t*>(p.dout);
-#pragma unroll
-        for (int jb = 0; jb < 8; ++jb)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = row0 + g + 8 * h, tk = 8 * jb + 2 * t;
-                if (!rev) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) u[jb][h][e] = p.wut[(ub * C + tk + e) * D + row];
-                }
-                const uint32_t lo = tk < n ? dO[(tok0 + tk) * D + row] : 0u;
-                const uint32_t hi = tk + 1 < n ? dO[(tok0 + tk + 1) * D + row] : 0u;
-                o[jb][h] = lo | (hi << 16);
-            }
-    };
-
     float x[NJ][4];
     {
         const float* x0 = rev ? p.dstate_out : p.state_in;
@@ -581,7 +568,6 @@ __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, ui
     cp_async_commit();
     if (NC > 1) issue(1, 1);
     cp_async_commit();
-    fetch(0, ut, dop);
 
     bf16* gout = rev ? p.wsc : p.ws0;
     for (int j = 0; j < NC; ++j) {
@@ -589,6 +575,8 @@ __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, ui
         const int c = rev ? NC - 1 - j : j;
         const uint8_t* b = stage(buf);
         const float* tgam = reinterpret_cast<const float*>(b + (rev ? L::REV : L::FWD) - C * 4);
+        const float* tUs = reinterpret_cast<const float*>(b + L::W_T + L::H_T + L::T_T);
+        const bf16* tOs = reinterpret_cast<const bf16*>(b + (rev ? L::H_T + 2 * L::T_T : L::W_T + L::H_T + L::T_T + L::U_T));
         // the rows entering this chunk
         {
             bf16* o = gout + (static_cast<size_t>(bh) * NC + c) * ss;
@@ -635,13 +623,12 @@ __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, ui
             for (int jb = 0; jb < 8; ++jb)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const float d0 = __uint_as_float((dop[jb][0] >> (16 * e)) << 16);
-                    const float d1 = __uint_as_float((dop[jb][1] >> (16 * e)) << 16);
+                    const int tok = 8 * jb + 2 * t + e;
+                    const float d0 = bf(tOs, tok * SO + rl + g), d1 = bf(tOs, tok * SO + rl + g + 8);
                     part[jb][e] = y2[jb][e] * d0 + y2[jb][2 + e] * d1;
-                    y[jb][e] = ut[jb][0][e] - y[jb][e];
-                    y[jb][2 + e] = ut[jb][1][e] - y[jb][2 + e];
+                    y[jb][e] = tUs[tok * SU + rl + g] - y[jb][e];
+                    y[jb][2 + e] = tUs[tok * SU + rl + g + 8] - y[jb][2 + e];
                 }
-            if (j + 1 < NC) fetch(j + 1, ut, dop);
             float* gdb = p.wdb0 + (static_cast<size_t>(bh) * NC + c) * C;
 #pragma unroll
             for (int jb = 0; jb < 8; ++jb)
@@ -673,10 +660,12 @@ __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, ui
             const uint32_t a[4] = {to_tf32(y[kk][0]), to_tf32(y[kk][2]), to_tf32(y[kk][1]), to_tf32(y[kk][3])};
             uint32_t a2[4];
             if (rev) {   // dO^T: rows g, g + 8, tokens 8 kk + 2t, +1 (bf16: already tf32)
-                a2[0] = dop[kk][0] << 16;
-                a2[1] = dop[kk][1] << 16;
-                a2[2] = dop[kk][0] & 0xffff0000u;
-                a2[3] = dop[kk][1] & 0xffff0000u;
+                const float2 lo = colh(tOs + (8 * kk + 2 * t) * SO + rl + g, SO);
+                const float2 hi = colh(tOs + (8 * kk + 2 * t) * SO + rl + g + 8, SO);
+                a2[0] = __float_as_uint(lo.x);
+                a2[1] = __float_as_uint(hi.x);
+                a2[2] = __float_as_uint(lo.y);
+                a2[3] = __float_as_uint(hi.y);
             }
 #pragma unroll
             for (int jb = 0; jb < NJ; ++jb) {
@@ -693,7 +682,6 @@ __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, ui
                 }
             }
         }
-        if (rev && j + 1 < NC) fetch(j + 1, ut, dop);
         __syncthreads();   // every warp is done with this stage
         if (j + 2 < NC) issue(j + 2, buf);
         cp_async_commit();
