@@ -876,7 +876,7 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
     if (chunked) {
         const cudaError_t e = la::launch_gdn_chunk_backward(a, static_cast<cudaStream_t>(cuda_stream));
         if (e != cudaSuccess) return cuda_fail(h, e, "gated backward launch");
-        h->last_launches = 5;   // prep, the two chunk chains, the two gradient kernels
+        h->last_launches = 4;   // prep, both chunk chains in one launch, the two gradient kernels
         return LA_OK;
     }
     const cudaError_t e = la::launch_delta_backward(a, static_cast<cudaStream_t>(cuda_stream));

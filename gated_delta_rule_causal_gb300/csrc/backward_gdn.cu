@@ -32,21 +32,21 @@
 // Every value row of X follows that map on its own, so the two chains split
 // by rows.
 //
-// Five launches per call:
+// Four launches per call:
 //  1. prep, one CTA per (sequence-head, chunk): gate prefix sums, K K^T and
 //     Q K^T, Ti in fp32 (16x16 diagonal blocks by forward substitution, then
 //     two merge levels), W, Ut and Qh = gam Q - P W; fp32 into the workspace
 //     (W, lam W, lam K and Qh, only ever MMA operands, already rounded to tf32).
-//  2. the state chain, one CTA per (sequence-head, 32 value rows), walking the
-//     chunks with the rows in fp32 and storing every chunk's S_0 (bf16). It
-//     also forms the gate term gam_r dO_r.(S_0 q_r) from the fp32 rows (as
-//     two tf32 halves): that term cancels against the others of the gate
-//     gradient, and bf16 rows would cost it up to ~3% of the result.
-//  3. the gradient chain, the same from the last chunk, storing every chunk's
+//  2. both chains at once, CTAs of D/2 value rows: the state chain walks the
+//     chunks with the rows in fp32 and stores every chunk's S_0 (bf16); it
+//     also forms the gate term gam_r dO_r.(S_0 q_r) from the fp32 rows
+//     rounded once to tf32, since that term cancels against the others of
+//     the gate gradient and bf16 rows would cost it up to ~3% of the result.
+//     The gradient chain walks from the last chunk, storing every chunk's
 //     dS_C (bf16) and the gradient of the initial state (fp32).
-//  4. the state-dependent gradients per chunk: U, dU, dW, dQ (final), the
+//  3. the state-dependent gradients per chunk: U, dU, dW, dQ (final), the
 //     state terms of dK and of the gate gradient.
-//  5. the rest per chunk: dRv, dRk, dA, dV, dK, dbeta and the gate gradient.
+//  4. the rest per chunk: dRv, dRk, dA, dV, dK, dbeta and the gate gradient.
 // Every product is a warp-level tf32 MMA (m16n8k8, fp32 accumulation) on
 // shared-memory tiles; the chains prefetch the next chunk's tiles with
 // asynchronous copies while they compute the current one.

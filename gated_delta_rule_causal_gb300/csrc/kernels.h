@@ -113,7 +113,7 @@ size_t norm_rows_fwd_bytes(int BH, int T, int dv, int io);
 cudaError_t launch_delta_backward(const DeltaBwdArgs& a, cudaStream_t s);
 
 // Chunkwise gradients of the scalar-gate delta rule (see backward_gdn.cu):
-// bf16 io, dk_dim = dv_dim = 64 or 128, no per-channel decay. Five launches;
+// bf16 io, dk_dim = dv_dim = 64 or 128, no per-channel decay. Four launches;
 // the workspace holds gdn_chunk_backward_bytes(BH, T, d) bytes.
 size_t gdn_chunk_backward_bytes(int BH, int T, int d);
 cudaError_t launch_gdn_chunk_backward(const DeltaBwdArgs& a, cudaStream_t s);

@@ -323,13 +323,13 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
  * dbeta may be NULL and are ignored; LA_GLA's state_in, dstate_out and
  * dstate_in are [B,H,d_k*d_v] (S [d_k][d_v]).
  * LA_GDN with bf16 io and d_k = d_v (64 or 128): the chunkwise form (chunks
- * of 64 tokens), five launches: a per-chunk prep (the UT inverse of the
+ * of 64 tokens), four launches: a per-chunk prep (the UT inverse of the
  * chunk and its W, Ut and gam Q - P W), one launch walking both chunk chains
  * (the state forward, its gradient backward, value rows split over CTAs),
  * and two per-chunk gradient kernels; every product is a tf32 MMA with fp32
  * accumulation. Its workspace is 4 * B*H * ceil(T/64) * (8*64*d + 64*64 +
  * 4*64) + 2 * B*H * ceil(T/64) * 2*d*d bytes (d = d_k, each part rounded up
- * to 256 bytes); la_last_launches reports 5. The gate gradient's per-chunk
+ * to 256 bytes); la_last_launches reports 4. The gate gradient's per-chunk
  * terms are added by several CTAs in fp32, so its last bits may vary from
  * run to run.
  * Every other case: a token-serial CUDA-core kernel: the state's value rows
@@ -359,7 +359,7 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
  * with segment summaries when B*H is small; 3: the three-phase parallel form;
  * LA_GDN, LA_KDA and LA_GLA: one per group of 32 sequence-heads; la_backward:
  * 5 per head group for the chunkwise form, 1 for the token-serial kernel;
- * la_backward_gated: 5 for the chunkwise form, 2 for the token-serial one). */
+ * la_backward_gated: 4 for the chunkwise form, 2 for the token-serial one). */
 int la_last_launches(const la_handle* h);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
