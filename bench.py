@@ -603,6 +603,8 @@ def kernel_only(args):
          else W.BY_NAME[args.workload] if args.workload else HEADLINE)
     if args.gated_backward and args.workload:
         w = W.BY_NAME[args.workload]   # a smaller gated workload, for ncu captures
+    if args.seq_len:
+        w = w.with_(T=args.seq_len)    # a shorter sequence of the same shapes, for ncu captures
     props = torch.cuda.get_device_properties(0)
     if args.backward:
         r = BackwardRunner(w, 0, int(getattr(props, "L2_cache_size", 126 * 2 ** 20)), torch, la)
@@ -691,6 +693,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None, choices=sorted(W.BY_NAME))
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="with --only-kernel: the workload at this T (small ncu captures)")
     ap.add_argument("--no-suite", action="store_true")
     ap.add_argument("--only-kernel", action="store_true",
                     help="run warmup + steps of the workload's kernel and nothing else (for ncu)")
