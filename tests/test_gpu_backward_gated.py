@@ -149,3 +149,13 @@ def test_backward_gdn_full_size_sampled_heads():
             e = slice_rel_err(sl(x), r)
             assert np.all(np.isfinite(sl(x))), name
             assert e <= TOL["bf16"], (bi, hi, name, e)
+
+
+def test_backward_gdn_more_chain_ctas_than_sms():
+    # 80 sequence-heads: 2 directions x 80 x 2 = 320 chunk-chain CTAs, more than
+    # the GPU has SMs, so the chains run in several waves (no chain waits on
+    # another CTA), and 240 per-chunk CTAs of each per-chunk kernel.
+    got, ref = _case("gdn", 4, 20, 130, 64, "bf16", seed=41)
+    for name, x, r in zip(NAMES, got, ref):
+        assert np.all(np.isfinite(x)), name
+        assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
