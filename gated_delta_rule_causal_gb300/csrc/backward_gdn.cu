@@ -168,6 +168,56 @@ __device__ __forceinline__ void warp_mma(float (&acc)[MT][NT][4], const FA& fa, 
     }
 }
 
+// B operand from a row-major bf16 [k][n] tile (row stride ld elements, rows
+// 16-byte aligned): ldmatrix .trans of the 8 x 8 block at rows k..k+7,
+// columns n..n+7 gives lane (g, t) the pair (B[k + 2t][n + g], B[k + 2t + 1][n + g])
+// in one register, the lower k in the lower half: the k-pair order above.
+struct BT {
+    const bf16* p;
+    int ld;
+};
+
+template <int NT>
+__device__ __forceinline__ void ldsm_trans(uint32_t (&r)[NT], const bf16* row_addr) {
+    const uint32_t a = smem_u32(row_addr);
+    if constexpr (NT == 4)
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+    else if constexpr (NT == 2)
+        asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(a));
+    else
+        asm volatile("ldmatrix.sync.aligned.m8n8.x1.trans.shared.b16 {%0}, [%1];" : "=r"(r[0]) : "r"(a));
+}
+
+template <int MT, int NT, bool RA = true, class FA>
+__device__ __forceinline__ void warp_mma(float (&acc)[MT][NT][4], const FA& fa, const BT& bt, int m0, int n0, int k0,
+                                         int k1) {
+    static_assert(NT == 1 || NT == 2 || NT == 4, "one ldmatrix per k step");
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    // this lane's row address: block j = lane / 8 (of NT), row lane % 8
+    const bf16* rp = bt.p + (lane & 7) * bt.ld + n0 + 8 * ((lane >> 3) % NT);
+#pragma unroll 4
+    for (int k = k0; k < k1; k += 8) {
+        uint32_t a[MT][4], r[NT];
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const int m = m0 + 16 * i + g;
+            const float2 lo = fa(m, k + 2 * t), hi = fa(m + 8, k + 2 * t);
+            a[i][0] = tf32_of<RA>(lo.x);
+            a[i][1] = tf32_of<RA>(hi.x);
+            a[i][2] = tf32_of<RA>(lo.y);
+            a[i][3] = tf32_of<RA>(hi.y);
+        }
+        ldsm_trans<NT>(r, rp + k * bt.ld);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const uint32_t b[2] = {r[j] << 16, r[j] & 0xffff0000u};
+#pragma unroll
+            for (int i = 0; i < MT; ++i) mma_tf32_m16n8k8(acc[i][j], a[i], b);
+        }
+    }
+}
+
 // Two products sharing the A operand: acc1 += fa fb1, acc2 += fa fb2.
 template <int MT, int NT, bool RA, bool RB1, bool RB2, class FA, class FB1, class FB2>
 __device__ __forceinline__ void warp_mma2(float (&acc1)[MT][NT][4], float (&acc2)[MT][NT][4], const FA& fa,
@@ -426,10 +476,8 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Params p) {
         zero(u);
         const auto fw = [&](int m, int k) { return mul2(rowf(sT + m * FC + k), rowf(vbg + k)); };
         const auto fu = [&](int m, int k) { return mul2(rowf(sT + m * FC + k), rowf(vbeta + k)); };
-        const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
-        const auto fV = [&](int k, int nn) { return colh(sV + k * HD + nn, HD); };
-        warp_mma<2, NT, true, false>(w, fw, fK, m0, n0, 0, m0 + 32);
-        warp_mma<2, NT, true, false>(u, fu, fV, m0, n0, 0, m0 + 32);
+        warp_mma<2, NT>(w, fw, BT{sK, HD}, m0, n0, 0, m0 + 32);
+        warp_mma<2, NT>(u, fu, BT{sV, HD}, m0, n0, 0, m0 + 32);
         float* gw = p.ww + ub * C * D;
         float* gu = p.wut + ub * C * D;
         float* glw = p.wlwt + ub * C * D;
@@ -458,8 +506,7 @@ __global__ void __launch_bounds__(kThreads, 2) prep_kernel(const Params p) {
         float qh[2][NT][4];
         zero(qh);
         const auto fa = [&](int m, int k) { return mul2(rowf(sA + m * FC + k), rowf(vbg + k)); };
-        const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
-        warp_mma<2, NT, true, false>(qh, fa, fK, m0, n0, 0, m0 + 32);
+        warp_mma<2, NT>(qh, fa, BT{sK, HD}, m0, n0, 0, m0 + 32);
         float* gq = p.wqht + ub * C * D;
         for_acc(qh, m0, n0, [&](int r, int cc, float& x, int rs, int cs) {
             gq[cc * C + r] = tf32r(vgam[r] * bf(sQ, r * HD + cc) - x);
@@ -699,7 +746,7 @@ __device__ __forceinline__ void chain_body(const Params& p, int bh, int part, ui
 
 template <int D>
 __global__ void __launch_bounds__(2 * D / kChainSplit, 1) chain_kernel(const Params p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(16) uint8_t smem[];
     const int per_dir = p.BH * kChainSplit;
     const int i = blockIdx.x % per_dir;
     if (blockIdx.x < per_dir) chain_body<D, false>(p, i / kChainSplit, i % kChainSplit, smem);
@@ -771,15 +818,15 @@ __global__ void __launch_bounds__(kGradThreads, 1) grad_state_kernel(const Param
     const float gC = expf(vb[C - 1]);
     const int m0 = (warp >> 2) * 16 * GMT, n0c = (warp & 3) * 16, n0d = (warp & 3) * (D / 4);
     const auto fQ = [&](int m, int k) { return rowh(sQ + m * HD + k); };
-    const auto fQc = [&](int k, int nn) { return colh(sQ + k * HD + nn, HD); };
+    const BT fQc{sQ, HD};
     const auto fO = [&](int m, int k) { return rowh(sO + m * HD + k); };
-    const auto fOc = [&](int k, int nn) { return colh(sO + k * HD + nn, HD); };
+    const BT fOc{sO, HD};
     const auto fKt = [&](int k, int nn) { return rowh(sK + nn * HD + k); };
-    const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
-    const auto fS0 = [&](int k, int nn) { return colh(sS0 + k * HD + nn, HD); };
+    const BT fK{sK, HD};
+    const BT fS0{sS0, HD};
     const auto fS0t = [&](int k, int nn) { return rowh(sS0 + nn * HD + k); };
     const auto fSCt = [&](int k, int nn) { return rowh(sSC + nn * HD + k); };
-    const auto fSC = [&](int k, int nn) { return colh(sSC + k * HD + nn, HD); };
+    const BT fSC{sSC, HD};
 
     // P = lower(E o Q K^T); U = Ut - W S_0^T (in place); dQ <- gam dO S_0
     {
@@ -796,14 +843,14 @@ __global__ void __launch_bounds__(kGradThreads, 1) grad_state_kernel(const Param
     }
     float dq[GMT][NT][4];
     zero(dq);
-    warp_mma<GMT, NT, false, false>(dq, fO, fS0, m0, n0d, 0, D);
+    warp_mma<GMT, NT, false>(dq, fO, fS0, m0, n0d, 0, D);
     for_acc(dq, m0, n0d, [&](int r, int k, float& x, int rs, int cs) { x *= vgam[r]; });
     __syncthreads();   // sP, sU complete; W no longer read
     // dU = P^T dO + diag(lam) K dS_C^T -> sW and the workspace
     {
         float du[GMT][NT][4];
         zero(du);
-        warp_mma<GMT, NT, true, false>(du, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fOc,
+        warp_mma<GMT, NT>(du, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fOc,
                         m0, n0d, m0, C);
         warp_mma<GMT, NT, true, false>(du, [&](int m, int k) { return scale2(rowh(sK + m * HD + k), vlam[m]); }, fSCt, m0,
                                      n0d, 0, D);
@@ -818,7 +865,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) grad_state_kernel(const Param
     {
         float dw[GMT][NT][4];
         zero(dw);
-        warp_mma<GMT, NT, true, false>(dw, [&](int m, int k) { return rowf(sW + m * FD + k); }, fS0, m0, n0d, 0, D);
+        warp_mma<GMT, NT>(dw, [&](int m, int k) { return rowf(sW + m * FD + k); }, fS0, m0, n0d, 0, D);
         float* g = p.wdw + ub * C * D;
         for_acc(dw, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) { g[r * D + kk] = -x; });
         float dp[GMT][2][4];
@@ -840,7 +887,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) grad_state_kernel(const Param
     }
     __syncthreads();   // dP o E complete
     // dQ += (dP o E) K -> global
-    warp_mma<GMT, NT, true, false>(dq, [&](int m, int k) { return rowf(sP + m * FC + k); }, fK, m0, n0d, 0, m0 + 16 * GMT);
+    warp_mma<GMT, NT>(dq, [&](int m, int k) { return rowf(sP + m * FC + k); }, fK, m0, n0d, 0, m0 + 16 * GMT);
     {
         bf16* g = p.dq + tok0 * D;
 #pragma unroll
@@ -859,7 +906,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) grad_state_kernel(const Param
     {
         float dk[GMT][NT][4];
         zero(dk);
-        warp_mma<GMT, NT, true, false>(dk, [&](int m, int k) { return scale2(rowf(sU + m * FD + k), vlam[m]); }, fSC, m0,
+        warp_mma<GMT, NT>(dk, [&](int m, int k) { return scale2(rowf(sU + m * FD + k), vlam[m]); }, fSC, m0,
                                      n0d, 0, D);
         float h[2 * GMT] = {};
         for_acc(dk, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) {
@@ -872,7 +919,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) grad_state_kernel(const Param
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
         if ((tid & 31) == 0) atomicAdd(vdb + C - 1, tot);
-        warp_mma<GMT, NT, true, false>(dk, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fQc, m0, n0d, m0, C);
+        warp_mma<GMT, NT>(dk, [&](int m, int k) { return colf(sP + k * FC + m, FC); }, fQc, m0, n0d, m0, C);
         float* g = p.wdk + ub * C * D;
         for_acc(dk, m0, n0d, [&](int r, int kk, float& x, int rs, int cs) { g[r * D + kk] = x; });
     }
@@ -951,7 +998,7 @@ __global__ void __launch_bounds__(kGradThreads, 1) grad_rest_kernel(const Params
     if (tid < C) vgam[tid] = expf(vb[tid]);
     __syncthreads();
     const int m0 = (warp >> 2) * 16 * GMT, n0c = (warp & 3) * 16, n0d = (warp & 3) * (D / 4);
-    const auto fK = [&](int k, int nn) { return colh(sK + k * HD + nn, HD); };
+    const BT fK{sK, HD};
     // dRv = Ti^T dU, dRk = Ti^T dW (Ti^T upper: k >= m0); K K^T -> sA
     float rv[GMT][NT][4], rk[GMT][NT][4];
     zero(rv);
@@ -1032,8 +1079,8 @@ __global__ void __launch_bounds__(kGradThreads, 1) grad_rest_kernel(const Params
                 }
         float dk[GMT][NT][4];
         zero(dk);
-        warp_mma<GMT, NT, true, false>(dk, [&](int m, int k) { return rowf(sA + m * FC + k); }, fK, m0, n0d, 0, m0 + 16 * GMT);
-        warp_mma<GMT, NT, true, false>(dk, [&](int m, int k) { return colf(sA + k * FC + m, FC); }, fK, m0, n0d, m0, C);
+        warp_mma<GMT, NT>(dk, [&](int m, int k) { return rowf(sA + m * FC + k); }, fK, m0, n0d, 0, m0 + 16 * GMT);
+        warp_mma<GMT, NT>(dk, [&](int m, int k) { return colf(sA + k * FC + m, FC); }, fK, m0, n0d, m0, C);
         bf16* gk = p.dk + tok0 * D;
 #pragma unroll
         for (int i = 0; i < GMT; ++i)
