@@ -48,8 +48,8 @@
 //     state terms of dK and of the gate gradient.
 //  4. the rest per chunk: dRv, dRk, dA, dV, dK, dbeta and the gate gradient.
 // Every product is a warp-level tf32 MMA (m16n8k8, fp32 accumulation) on
-// shared-memory tiles; the chains prefetch the next chunk's tiles with
-// asynchronous copies while they compute the current one.
+// shared-memory tiles loaded by asynchronous copies; the chains keep their
+// rows in registers and stage each chunk's tiles two chunks ahead.
 //
 // Tail chunks: rows past T load as zeros, with g = 1 and beta = 0, so they
 // leave every real row's result unchanged; no row past T is written.
@@ -215,41 +215,6 @@ __device__ __forceinline__ void warp_mma(float (&acc)[MT][NT][4], const FA& fa, 
 #pragma unroll
             for (int i = 0; i < MT; ++i) mma_tf32_m16n8k8(acc[i][j], a[i], b);
         }
-    }
-}
-
-// Two products sharing the A operand: acc1 += fa fb1, acc2 += fa fb2.
-template <int MT, int NT, bool RA, bool RB1, bool RB2, class FA, class FB1, class FB2>
-__device__ __forceinline__ void warp_mma2(float (&acc1)[MT][NT][4], float (&acc2)[MT][NT][4], const FA& fa,
-                                          const FB1& fb1, const FB2& fb2, int m0, int n0, int k0, int k1) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll 4
-    for (int k = k0; k < k1; k += 8) {
-        uint32_t a[MT][4], b1[NT][2], b2[NT][2];
-#pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            const int m = m0 + 16 * i + g;
-            const float2 lo = fa(m, k + 2 * t), hi = fa(m + 8, k + 2 * t);
-            a[i][0] = tf32_of<RA>(lo.x);
-            a[i][1] = tf32_of<RA>(hi.x);
-            a[i][2] = tf32_of<RA>(lo.y);
-            a[i][3] = tf32_of<RA>(hi.y);
-        }
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const float2 v1 = fb1(k + 2 * t, n0 + 8 * j + g), v2 = fb2(k + 2 * t, n0 + 8 * j + g);
-            b1[j][0] = tf32_of<RB1>(v1.x);
-            b1[j][1] = tf32_of<RB1>(v1.y);
-            b2[j][0] = tf32_of<RB2>(v2.x);
-            b2[j][1] = tf32_of<RB2>(v2.y);
-        }
-#pragma unroll
-        for (int i = 0; i < MT; ++i)
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                mma_tf32_m16n8k8(acc1[i][j], a[i], b1[j]);
-                mma_tf32_m16n8k8(acc2[i][j], a[i], b2[j]);
-            }
     }
 }
 
