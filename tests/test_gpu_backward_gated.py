@@ -14,28 +14,29 @@ pytestmark = pytest.mark.gpu
 la = pytest.importorskip("gated_delta_rule_causal_gb300")
 
 
-def _workload(variant, B, H, T, d, io):
+def _workload(variant, B, H, T, d, io, dv=None):
     base = {"gdn": W.GDN_B2H16_T8192_D128, "gla": W.GLA_B4H16_T4096_D128,
             "norm_decay": W.NORM_DECAY_B4H8_T2048_D64,
             "kda": W.KDA_DECODE_N256H16_D128.with_(B=4, H=16, T=2048, decode_steps=0, state_std=0.0)}[variant]
-    return W.small(base, B=B, H=H, T=T, dk=d, dv=d).with_(io=io)
+    return W.small(base, B=B, H=H, T=T, dk=d, dv=dv or d).with_(io=io)
 
 
-def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True, flags=0):
+def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True, flags=0, dv=None):
     import torch
     from oracle import backward
-    w = _workload(variant, B, H, T, d, io)
+    dv = dv or d
+    w = _workload(variant, B, H, T, d, io, dv)
     inp = W.draw(w, seed)
     q, k, v, g, b = oracle_inputs(inp)
     rng = np.random.default_rng(seed + 1000)
-    ss = d * d + (d if variant == "norm_decay" else 0)
-    do_s = W.round_io(rng.standard_normal((B, H, T, d)), io)
+    ss = d * dv + (d if variant == "norm_decay" else 0)
+    do_s = W.round_io(rng.standard_normal((B, H, T, dv)), io)
     do64 = W.as_f64(do_s)
     sin = (rng.standard_normal((B, H, ss)) * 0.1).astype(np.float32) if with_state else None
     if sin is not None and variant == "norm_decay":   # a positive normalizer state
-        sin[..., d * d:] = np.abs(sin[..., d * d:]) * 50 + 1.0
+        sin[..., d * dv:] = np.abs(sin[..., d * dv:]) * 50 + 1.0
     dso = (rng.standard_normal((B, H, ss)) * 0.05).astype(np.float32) if with_dstate else None
-    h = la.Handle(B, H, d, d, io=io, flags=flags)
+    h = la.Handle(B, H, d, dv, io=io, flags=flags)
     dev = h.device
     t = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     got = h.backward_gated(to_torch(inp.q, dev), to_torch(inp.k, dev), to_torch(inp.v, dev),
@@ -45,9 +46,9 @@ def _case(variant, B, H, T, d, io, seed, with_state=True, with_dstate=True, flag
         assert got[4] is None
         got = got[:4] + got[5:]
     torch.cuda.synchronize()
-    # the scalar-gate rule in bf16: four chunkwise launches; otherwise the row
-    # kernel and its conversion (norm_decay: after the forward's)
-    if variant == "gdn" and io == "bf16":
+    # the scalar-gate rule in bf16 with square heads: four chunkwise launches;
+    # otherwise the row kernel and its conversion (norm_decay: after the forward's)
+    if variant == "gdn" and io == "bf16" and dv == d:
         assert h.last_launches() == 4
     elif variant == "norm_decay":
         assert h.last_launches() >= 3
@@ -186,4 +187,14 @@ def test_backward_gdn_strong_gates(gate_mu, beta_mu):
     ref = backward.delta_backward(q, k, v, g, b, W.as_f64(do_s), None, dso)
     for name, x, r in zip(NAMES, [x.float().cpu().numpy() for x in got], ref):
         assert np.all(np.isfinite(x)), name
+        assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
+
+
+@pytest.mark.parametrize("variant", ["gdn", "kda", "gla"])
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64)])
+def test_backward_gated_rectangular_heads(variant, dk, dv):
+    # d_k != d_v: the token-serial kernel (the chunkwise form takes square heads)
+    got, ref = _case(variant, 1, 2, 70, dk, "bf16", seed=61 + dk, dv=dv)
+    for name, x, r in zip(names(variant), got, ref):
+        assert x.shape == r.shape, name
         assert slice_rel_err(x, r) <= TOL["bf16"], (name, slice_rel_err(x, r))
