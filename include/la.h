@@ -341,7 +341,8 @@ int la_backward(la_handle* h, const void* q, const void* k, const void* v,
  * 2*T*d_k) bytes; LA_GLA: T*d_v in place of 2*T*d_k) and the chunkwise one
  * are allocated by the handle on first use and grown when a call needs more
  * (la_destroy frees it). la_last_launches reports 2 (plus memsets of the
- * accumulated outputs, not counted).
+ * accumulated outputs, not counted; LA_NORM_DECAY: the forward's launches
+ * plus 2).
  * Errors: LA_ERR_UNSUPPORTED for another variant or head size,
  * LA_ERR_INVALID_ARG (T < 1, a required pointer NULL), LA_ERR_MISALIGNED,
  * LA_ERR_CUDA.
@@ -359,7 +360,8 @@ int la_backward_gated(la_handle* h, const void* q, const void* k, const void* v,
  * with segment summaries when B*H is small; 3: the three-phase parallel form;
  * LA_GDN, LA_KDA and LA_GLA: one per group of 32 sequence-heads; la_backward:
  * 5 per head group for the chunkwise form, 1 for the token-serial kernel;
- * la_backward_gated: 4 for the chunkwise form, 2 for the token-serial one). */
+ * la_backward_gated: 4 for the chunkwise form, 2 for the token-serial one,
+ * the forward's + 2 for LA_NORM_DECAY). */
 int la_last_launches(const la_handle* h);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
